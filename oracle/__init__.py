@@ -1,0 +1,290 @@
+"""float64 CPU oracle for paged-KV attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never imports, links or
+calls it, and it shares no code with the CUDA library: the arithmetic lives in
+``pkv_oracle.c`` (plain C, float64), this module only marshals numpy arrays.
+
+Every function restates a definition from the SGLang attention-backend pages:
+
+* ``strided_page_table`` -- flashattention_backend.py, ``init_forward_metadata``
+  ("Convert the page table to a strided format").
+* ``swa_page_table`` -- flashattention_backend.py, ``_build_pa_page_table_kernel``.
+* ``topk_to_slots`` -- nsa_backend.py, ``TopkTransformMethod.PAGED``.
+* ``attention`` -- flashattention_backend.py ``forward_decode`` /
+  ``forward_extend`` (``flash_attn_with_kvcache``), absorbed MLA call,
+  nsa_backend.py ``forward_decode`` (top-k), bottom-right causal alignment
+  (nsa_backend.py ``seqlens_expanded``), empty-KV convention
+  (dual_chunk_flashattention_backend.py,
+  ``_dual_chunk_flash_attn_decoding_with_exp_sums``).
+* ``merge_state`` -- dual_chunk_flashattention_backend.py,
+  ``_merge_attn_outputs``; ``merge_state_v2`` call in flashattention_backend.py.
+* ``split_bounds`` / ``split_attention`` -- split-KV partials combined by the
+  state merge (flashattention_backend.py ``num_splits``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from ._build import build_oracle, oracle_lib_path
+
+__all__ = [
+    "strided_page_table",
+    "swa_page_table",
+    "topk_to_slots",
+    "attention",
+    "merge_state",
+    "split_bounds",
+    "split_attention",
+    "bf16_bits",
+]
+
+_LIB = None
+
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_f64p = ctypes.POINTER(ctypes.c_double)
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        path = oracle_lib_path()
+        if not os.path.exists(path) or os.path.getmtime(path) < _src_mtime():
+            build_oracle()
+        lib = ctypes.CDLL(path)
+        lib.orc_strided_page_table.argtypes = [
+            _i32p, _i64, _i64, _i64p, _int, _int, _int, _i32p, _i64]
+        lib.orc_swa_page_table.argtypes = [
+            _i32p, _i64, _i64, _i64p, _i32p, _i32p, _int, _int, _i32p, _i64,
+            _int, _i32p]
+        lib.orc_topk_to_slots.argtypes = [
+            _i32p, _i64, _int, _int, _i32p, _i32p, _i64, _int, _int, _i32p,
+            _i32p, _i64]
+        lib.orc_attention.argtypes = [
+            _u16p, _i64, _i64, _int, _int, _int,
+            _u16p, _i64, _i64, _i64,
+            _u16p, _i64, _i64, _i64, _int,
+            _int, _int, _i64,
+            _i32p, _i64, _int,
+            _i32p, _i32p, _int, ctypes.c_double, _int, _int,
+            _i32p, _i64, _int,
+            _i32p, _int, _f64p, _f64p, _int]
+        lib.orc_merge_state.argtypes = [
+            _f64p, _f64p, _f64p, _f64p, _i64, _int, _f64p, _f64p]
+        for fn in ("orc_strided_page_table", "orc_swa_page_table",
+                   "orc_topk_to_slots", "orc_attention", "orc_merge_state"):
+            getattr(lib, fn).restype = ctypes.c_int
+        _LIB = lib
+    return _LIB
+
+
+def _src_mtime() -> float:
+    here = os.path.dirname(os.path.abspath(__file__))
+    return max(os.path.getmtime(os.path.join(here, f))
+               for f in ("pkv_oracle.c", "pkv_oracle.h"))
+
+
+def _ptr(a: np.ndarray | None, ctype):
+    if a is None:
+        return ctypes.cast(None, ctypes.POINTER(ctype))
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def bf16_bits(t) -> np.ndarray:
+    """Raw bf16 bit patterns of a CPU torch bf16 tensor, as a uint16 array."""
+    import torch
+
+    assert t.dtype == torch.bfloat16
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _elem_strides(a: np.ndarray) -> tuple[int, ...]:
+    return tuple(s // a.itemsize for s in a.strides)
+
+
+def strided_page_table(req_to_token, req_pool_indices, page_size: int,
+                       n_cols: int) -> np.ndarray:
+    rtt = np.ascontiguousarray(req_to_token, dtype=np.int32)
+    rpi = np.ascontiguousarray(req_pool_indices, dtype=np.int64)
+    out = np.zeros((len(rpi), n_cols), dtype=np.int32)
+    rc = _lib().orc_strided_page_table(
+        _ptr(rtt, ctypes.c_int32), rtt.shape[1], rtt.shape[1],
+        _ptr(rpi, ctypes.c_int64), len(rpi), page_size, n_cols,
+        _ptr(out, ctypes.c_int32), n_cols)
+    if rc != 0:
+        raise ValueError(f"orc_strided_page_table rejected its arguments ({rc})")
+    return out
+
+
+def swa_page_table(req_to_token, req_pool_indices, seq_lens, prefill_lens,
+                   window: int, dst_cols: int, fill: int = 0):
+    """Returns (dst [B, dst_cols] int32, kv_lens [B] int32, n_rows_too_long).
+
+    Columns at or past kv_len keep ``fill``; a row whose kv_len exceeds
+    dst_cols is left as ``fill`` with kv_len -1 and counted."""
+    rtt = np.ascontiguousarray(req_to_token, dtype=np.int32)
+    rpi = np.ascontiguousarray(req_pool_indices, dtype=np.int64)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    pf = np.ascontiguousarray(prefill_lens, dtype=np.int32)
+    dst = np.full((len(rpi), dst_cols), fill, dtype=np.int32)
+    kv = np.zeros(len(rpi), dtype=np.int32)
+    rc = _lib().orc_swa_page_table(
+        _ptr(rtt, ctypes.c_int32), rtt.shape[1], rtt.shape[1],
+        _ptr(rpi, ctypes.c_int64), _ptr(sl, ctypes.c_int32),
+        _ptr(pf, ctypes.c_int32), len(rpi), window, _ptr(dst, ctypes.c_int32),
+        dst_cols, dst_cols, _ptr(kv, ctypes.c_int32))
+    if rc < 0:
+        raise ValueError(f"orc_swa_page_table rejected its arguments ({rc})")
+    return dst, kv, rc
+
+
+def topk_to_slots(topk, row_req, page_table, page_size: int,
+                  cache_seqlens=None):
+    """Returns (slots [rows, topk] int32, n_out_of_range)."""
+    tk = np.ascontiguousarray(topk, dtype=np.int32)
+    rr = np.ascontiguousarray(row_req, dtype=np.int32)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    cs = None if cache_seqlens is None else np.ascontiguousarray(
+        cache_seqlens, dtype=np.int32)
+    out = np.zeros_like(tk)
+    rc = _lib().orc_topk_to_slots(
+        _ptr(tk, ctypes.c_int32), tk.shape[1], tk.shape[0], tk.shape[1],
+        _ptr(rr, ctypes.c_int32), _ptr(pt, ctypes.c_int32), pt.shape[1],
+        pt.shape[1], page_size, _ptr(cs, ctypes.c_int32),
+        _ptr(out, ctypes.c_int32), tk.shape[1])
+    if rc < 0:
+        raise ValueError(f"orc_topk_to_slots rejected its arguments ({rc})")
+    return out, rc
+
+
+def attention(q_bits, k_bits, v_bits, page_table, cache_seqlens, cu_seqlens_q,
+              scale: float, causal: bool = False, window_left: int = -1,
+              topk=None, rows=None, d_v: int | None = None,
+              num_threads: int = 0):
+    """Paged attention in float64.
+
+    q_bits: uint16 [total_q, H_q, D_qk]; k_bits / v_bits: uint16
+    [num_pages, P, H_kv, D] views (any element strides; D contiguous).
+    ``d_v`` defaults to v_bits.shape[3] (pass 512 with v_bits = k_bits for
+    absorbed MLA).  ``rows``: optional int array [n, 2] of (token, head).
+    Returns (out [n, d_v] float64, lse [n] float64, n_skipped); without
+    ``rows`` out is [total_q, H_q, d_v] and lse [total_q, H_q].
+    """
+    q = np.asarray(q_bits)
+    k = np.asarray(k_bits)
+    v = np.asarray(v_bits)
+    assert q.dtype == np.uint16 and k.dtype == np.uint16 and v.dtype == np.uint16
+    assert q.strides[2] == 2 and k.strides[3] == 2 and v.strides[3] == 2
+    total_q, h_q, d_qk = q.shape
+    num_pages, page_size, h_kv, dk = k.shape
+    assert dk >= d_qk
+    if d_v is None:
+        d_v = v.shape[3]
+    qs = _elem_strides(q)
+    ks = _elem_strides(k)
+    vs = _elem_strides(v)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    cs = np.ascontiguousarray(cache_seqlens, dtype=np.int32)
+    cu = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
+    tk = None if topk is None else np.ascontiguousarray(topk, dtype=np.int32)
+    rw = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    n = total_q * h_q if rw is None else rw.shape[0]
+    out = np.zeros((n, d_v), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    rc = _lib().orc_attention(
+        _ptr(q, ctypes.c_uint16), qs[0], qs[1], total_q, h_q, d_qk,
+        _ptr(k, ctypes.c_uint16), ks[0], ks[1], ks[2],
+        _ptr(v, ctypes.c_uint16), vs[0], vs[1], vs[2], d_v,
+        h_kv, page_size, num_pages,
+        _ptr(pt, ctypes.c_int32), pt.shape[1] if pt.ndim == 2 else 0,
+        pt.shape[1] if pt.ndim == 2 else 0,
+        _ptr(cs, ctypes.c_int32), _ptr(cu, ctypes.c_int32), len(cs),
+        float(scale), int(bool(causal)), int(window_left),
+        _ptr(tk, ctypes.c_int32), 0 if tk is None else tk.shape[1],
+        0 if tk is None else tk.shape[1],
+        _ptr(rw, ctypes.c_int32), 0 if rw is None else rw.shape[0],
+        _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double),
+        int(num_threads))
+    if rc < 0:
+        raise ValueError(f"orc_attention rejected its arguments ({rc})")
+    if rw is None:
+        out = out.reshape(total_q, h_q, d_v)
+        lse = lse.reshape(total_q, h_q)
+    return out, lse, rc
+
+
+def merge_state(v_a, lse_a, v_b, lse_b):
+    """Two-state log-sum-exp merge in float64: v [..., D], lse [...]."""
+    va = np.ascontiguousarray(v_a, dtype=np.float64)
+    vb = np.ascontiguousarray(v_b, dtype=np.float64)
+    la = np.ascontiguousarray(lse_a, dtype=np.float64)
+    lb = np.ascontiguousarray(lse_b, dtype=np.float64)
+    assert va.shape == vb.shape and la.shape == lb.shape == va.shape[:-1]
+    d = va.shape[-1]
+    n = la.size
+    vo = np.zeros_like(va)
+    lo = np.zeros_like(la)
+    rc = _lib().orc_merge_state(
+        _ptr(va, ctypes.c_double), _ptr(la, ctypes.c_double),
+        _ptr(vb, ctypes.c_double), _ptr(lb, ctypes.c_double), n, d,
+        _ptr(vo, ctypes.c_double), _ptr(lo, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("orc_merge_state rejected its arguments")
+    return vo, lo
+
+
+def split_bounds(kv_len: int, num_splits: int, page_size: int):
+    """Split-KV chunk boundaries used by the oracle: contiguous, page-aligned,
+    near-equal chunks.  Chunk c covers [c*S, min((c+1)*S, kv_len)) with
+    S = ceil(ceil(kv_len / num_splits) / page_size) * page_size; trailing
+    chunks may be empty.  The pages leave the boundaries open; the merged
+    result does not depend on them."""
+    per = -(-kv_len // num_splits)
+    size = -(-per // page_size) * page_size
+    return [(min(c * size, kv_len), min((c + 1) * size, kv_len))
+            for c in range(num_splits)]
+
+
+def split_attention(q_bits, k_bits, v_bits, page_table, cache_seqlens,
+                    cu_seqlens_q, scale: float, num_splits: int,
+                    num_threads: int = 0):
+    """Decode attention computed as ``num_splits`` partial states over
+    disjoint key chunks, combined by repeated two-state merges (left to
+    right).  Decode only (one query token per request, every key visible).
+    Each chunk is an ordinary paged-attention call whose page table holds
+    the chunk's pages and whose key window selects the chunk."""
+    k = np.asarray(k_bits)
+    page_size = k.shape[1]
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    cs = np.ascontiguousarray(cache_seqlens, dtype=np.int32)
+    cu = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
+    assert np.all(np.diff(cu) == 1), "split_attention is decode-only"
+    b_count = len(cs)
+    acc_o = acc_l = None
+    for c in range(num_splits):
+        # Chunk c of request b: keys [lo_b, hi_b).  Present it as a request
+        # whose page table starts at page lo_b / P and whose length is
+        # hi_b - lo_b, so the chunk's keys are exactly its visible keys.
+        cols = pt.shape[1]
+        pt_c = np.zeros_like(pt)
+        len_c = np.zeros(b_count, dtype=np.int32)
+        for b in range(b_count):
+            lo, hi = split_bounds(int(cs[b]), num_splits, page_size)[c]
+            p0 = lo // page_size
+            n_pages = cols - p0
+            pt_c[b, :n_pages] = pt[b, p0:]
+            len_c[b] = hi - lo
+        o_c, l_c, _ = attention(q_bits, k_bits, v_bits, pt_c, len_c, cu, scale,
+                                num_threads=num_threads)
+        if acc_o is None:
+            acc_o, acc_l = o_c, l_c
+        else:
+            acc_o, acc_l = merge_state(acc_o, acc_l, o_c, l_c)
+    return acc_o, acc_l

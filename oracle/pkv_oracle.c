@@ -1,0 +1,259 @@
+/*
+ * pkv_oracle.c -- float64 CPU oracle for paged-KV attention.
+ *
+ * TEST INFRASTRUCTURE ONLY: loaded by the tests, the smoke check and the
+ * bench's CPU-baseline leg, never by the CUDA library.  Each function follows
+ * the definition stated in pkv_oracle.h step by step, with no blocking,
+ * fusion or reordering: one (token, head) row at a time, keys in order.
+ * OpenMP only distributes independent rows over host threads.
+ */
+#include "pkv_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Exact widening of a bf16 bit pattern: bf16 is the top half of a binary32. */
+static double bf16_bits_to_double(uint16_t bits) {
+  uint32_t w = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
+int orc_strided_page_table(const int32_t *req_to_token, int64_t rtt_stride,
+                           int64_t rtt_cols, const int64_t *req_pool_indices,
+                           int batch, int page_size, int n_cols, int32_t *out,
+                           int64_t out_stride) {
+  if (batch < 0 || page_size < 1 || n_cols < 0) return -1;
+  if ((int64_t)(n_cols - 1) * page_size >= rtt_cols && n_cols > 0) return -1;
+  for (int b = 0; b < batch; ++b) {
+    const int32_t *row = req_to_token + req_pool_indices[b] * rtt_stride;
+    for (int c = 0; c < n_cols; ++c) {
+      /* slots are non-negative, so C division equals the floor division
+         that the page applies (`// page_size`). */
+      out[(int64_t)b * out_stride + c] = row[(int64_t)c * page_size] / page_size;
+    }
+  }
+  return 0;
+}
+
+int orc_swa_page_table(const int32_t *req_to_token, int64_t rtt_stride,
+                       int64_t rtt_cols, const int64_t *req_pool_indices,
+                       const int32_t *seq_lens, const int32_t *prefill_lens,
+                       int batch, int window, int32_t *dst, int64_t dst_stride,
+                       int dst_cols, int32_t *kv_lens) {
+  if (batch < 0 || window < 0 || dst_cols < 0) return -1;
+  int too_long = 0;
+  for (int b = 0; b < batch; ++b) {
+    int64_t req = req_pool_indices[b];
+    int32_t sl = seq_lens[b];
+    int32_t pf = prefill_lens[req];
+    /* the whole prompt, then the last `window` tokens that follow it */
+    int32_t decode_start = pf > sl - window ? pf : sl - window;
+    int32_t gap = decode_start > pf ? decode_start - pf : 0;
+    int32_t kv_len = sl - gap;
+    /* last source column read: kv_len-1, shifted by the gap if past pf */
+    int64_t last_src = kv_len - 1 < pf ? kv_len - 1 : (int64_t)kv_len - 1 + gap;
+    if (kv_len > dst_cols || (kv_len > 0 && last_src >= rtt_cols)) {
+      kv_lens[b] = -1;
+      ++too_long;
+      continue;
+    }
+    kv_lens[b] = kv_len;
+    const int32_t *src = req_to_token + req * rtt_stride;
+    for (int32_t i = 0; i < kv_len; ++i) {
+      int32_t pos = i < pf ? i : i + gap;
+      dst[(int64_t)b * dst_stride + i] = src[pos];
+    }
+  }
+  return too_long;
+}
+
+int orc_topk_to_slots(const int32_t *topk, int64_t topk_stride, int n_rows,
+                      int topk_len, const int32_t *row_req,
+                      const int32_t *page_table, int64_t pt_stride,
+                      int pt_cols, int page_size,
+                      const int32_t *cache_seqlens, int32_t *out,
+                      int64_t out_stride) {
+  if (n_rows < 0 || topk_len < 0 || page_size < 1 || pt_cols < 0) return -1;
+  int bad = 0;
+  for (int r = 0; r < n_rows; ++r) {
+    int b = row_req[r];
+    int64_t limit = cache_seqlens ? (int64_t)cache_seqlens[b]
+                                  : (int64_t)pt_cols * page_size;
+    if (limit > (int64_t)pt_cols * page_size) limit = (int64_t)pt_cols * page_size;
+    for (int k = 0; k < topk_len; ++k) {
+      int32_t idx = topk[(int64_t)r * topk_stride + k];
+      int32_t slot;
+      if (idx == -1) {
+        slot = -1;
+      } else if (idx < -1 || idx >= limit) {
+        slot = -1;
+        ++bad;
+      } else {
+        slot = page_table[(int64_t)b * pt_stride + idx / page_size] * page_size +
+               idx % page_size;
+      }
+      out[(int64_t)r * out_stride + k] = slot;
+    }
+  }
+  return bad;
+}
+
+/* One (token, head) row of paged attention, straight from the definition. */
+static int attend_row(const uint16_t *q, int64_t q_st, int64_t q_sh, int d_qk,
+                      const uint16_t *k_cache, int64_t k_sp, int64_t k_spos,
+                      int64_t k_sh, const uint16_t *v_cache, int64_t v_sp,
+                      int64_t v_spos, int64_t v_sh, int d_v, int h_q, int h_kv,
+                      int page_size, int64_t num_pages,
+                      const int32_t *page_table, int64_t pt_stride, int pt_cols,
+                      const int32_t *cache_seqlens, const int32_t *cu_seqlens_q,
+                      int batch, double scale, int causal, int window_left,
+                      const int32_t *topk, int64_t topk_stride, int topk_len,
+                      int t, int h, double *o, double *lse_out, double *s_buf,
+                      int64_t *slot_buf) {
+  /* request of token t: cu[b] <= t < cu[b+1] */
+  int b = 0;
+  while (b < batch && !(cu_seqlens_q[b] <= t && t < cu_seqlens_q[b + 1])) ++b;
+  int skipped = 0;
+  for (int d = 0; d < d_v; ++d) o[d] = 0.0;
+  if (b == batch) { /* token not covered by any request: no keys */
+    if (lse_out) *lse_out = -INFINITY;
+    return 0;
+  }
+  int64_t kv_len = cache_seqlens[b];
+  int64_t q_len = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+  int64_t i = kv_len - q_len + (t - cu_seqlens_q[b]); /* bottom-right */
+  int kvh = h / (h_q / h_kv);
+
+  /* 1. the candidate logical key list */
+  int64_t n_cand = topk ? topk_len : kv_len;
+  int64_t n = 0;
+  for (int64_t c = 0; c < n_cand; ++c) {
+    int64_t j;
+    if (topk) {
+      j = topk[(int64_t)t * topk_stride + c];
+      if (j == -1) continue;
+      if (j < -1 || j >= kv_len) { ++skipped; continue; }
+    } else {
+      j = c;
+    }
+    if (causal && j > i) continue;
+    if (window_left >= 0 && (j > i || j < i - window_left)) continue;
+    /* 2. logical position -> physical slot through the page table */
+    if (j / page_size >= pt_cols) { ++skipped; continue; }
+    int64_t page = page_table[(int64_t)b * pt_stride + j / page_size];
+    if (page < 0 || page >= num_pages) { ++skipped; continue; }
+    slot_buf[n++] = page * page_size + j % page_size;
+  }
+
+  if (n == 0) {
+    if (lse_out) *lse_out = -INFINITY;
+    return skipped;
+  }
+
+  /* 3. scores s_j = scale * <q, K_j> in float64 */
+  const uint16_t *qrow = q + (int64_t)t * q_st + (int64_t)h * q_sh;
+  double m = -INFINITY;
+  for (int64_t c = 0; c < n; ++c) {
+    int64_t slot = slot_buf[c];
+    const uint16_t *krow = k_cache + (slot / page_size) * k_sp +
+                           (slot % page_size) * k_spos + (int64_t)kvh * k_sh;
+    double dot = 0.0;
+    for (int d = 0; d < d_qk; ++d)
+      dot += bf16_bits_to_double(qrow[d]) * bf16_bits_to_double(krow[d]);
+    s_buf[c] = scale * dot;
+    if (s_buf[c] > m) m = s_buf[c];
+  }
+
+  /* 4. lse = m + log sum exp(s - m);  o = sum exp(s - lse) V */
+  double sum = 0.0;
+  for (int64_t c = 0; c < n; ++c) sum += exp(s_buf[c] - m);
+  double lse = m + log(sum);
+  for (int64_t c = 0; c < n; ++c) {
+    int64_t slot = slot_buf[c];
+    const uint16_t *vrow = v_cache + (slot / page_size) * v_sp +
+                           (slot % page_size) * v_spos + (int64_t)kvh * v_sh;
+    double w = exp(s_buf[c] - lse);
+    for (int d = 0; d < d_v; ++d) o[d] += w * bf16_bits_to_double(vrow[d]);
+  }
+  if (lse_out) *lse_out = lse;
+  return skipped;
+}
+
+int orc_attention(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q,
+                  int h_q, int d_qk, const uint16_t *k_cache, int64_t k_sp,
+                  int64_t k_spos, int64_t k_sh, const uint16_t *v_cache,
+                  int64_t v_sp, int64_t v_spos, int64_t v_sh, int d_v,
+                  int h_kv, int page_size, int64_t num_pages,
+                  const int32_t *page_table, int64_t pt_stride, int pt_cols,
+                  const int32_t *cache_seqlens, const int32_t *cu_seqlens_q,
+                  int batch, double scale, int causal, int window_left,
+                  const int32_t *topk, int64_t topk_stride, int topk_len,
+                  const int32_t *rows, int n_rows, double *out, double *lse,
+                  int num_threads) {
+  if (total_q < 0 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0 || d_qk < 1 ||
+      d_v < 1 || page_size < 1 || batch < 0 || window_left < -1)
+    return -1;
+  int64_t n_work = rows ? (int64_t)n_rows : (int64_t)total_q * h_q;
+  /* longest candidate list any row can have */
+  int64_t max_keys = 0;
+  if (topk) {
+    max_keys = topk_len;
+  } else {
+    for (int b = 0; b < batch; ++b)
+      if (cache_seqlens[b] > max_keys) max_keys = cache_seqlens[b];
+  }
+  if (max_keys < 1) max_keys = 1;
+  int skipped_total = 0;
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#endif
+#pragma omp parallel reduction(+ : skipped_total)
+  {
+    double *s_buf = (double *)malloc(sizeof(double) * (size_t)max_keys);
+    int64_t *slot_buf = (int64_t *)malloc(sizeof(int64_t) * (size_t)max_keys);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t w = 0; w < n_work; ++w) {
+      int t = rows ? rows[2 * w] : (int)(w / h_q);
+      int h = rows ? rows[2 * w + 1] : (int)(w % h_q);
+      int sk = attend_row(q, q_st, q_sh, d_qk, k_cache, k_sp, k_spos, k_sh,
+                          v_cache, v_sp, v_spos, v_sh, d_v, h_q, h_kv,
+                          page_size, num_pages, page_table, pt_stride, pt_cols,
+                          cache_seqlens, cu_seqlens_q, batch, scale, causal,
+                          window_left, topk, topk_stride, topk_len, t, h,
+                          out + w * d_v, lse ? lse + w : NULL, s_buf, slot_buf);
+      /* a token's skipped entries are the same for every head: count them
+         on its head-0 row only */
+      if (h == 0) skipped_total += sk;
+    }
+    free(s_buf);
+    free(slot_buf);
+  }
+  return skipped_total;
+}
+
+int orc_merge_state(const double *v_a, const double *lse_a, const double *v_b,
+                    const double *lse_b, int64_t n, int d, double *v_out,
+                    double *lse_out) {
+  if (n < 0 || d < 1) return -1;
+  for (int64_t r = 0; r < n; ++r) {
+    double la = lse_a[r], lb = lse_b[r];
+    double m = la > lb ? la : lb;
+    if (m == -INFINITY) { /* both states empty */
+      for (int c = 0; c < d; ++c) v_out[r * d + c] = 0.0;
+      if (lse_out) lse_out[r] = -INFINITY;
+      continue;
+    }
+    double lse = m + log(exp(la - m) + exp(lb - m));
+    double wa = exp(la - lse), wb = exp(lb - lse);
+    for (int c = 0; c < d; ++c)
+      v_out[r * d + c] = wa * v_a[r * d + c] + wb * v_b[r * d + c];
+    if (lse_out) lse_out[r] = lse;
+  }
+  return 0;
+}

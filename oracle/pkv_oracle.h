@@ -1,0 +1,128 @@
+/*
+ * pkv_oracle.h -- float64 CPU oracle for paged-KV attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is the plain, slow, obviously-correct
+ * restatement of what the paged-KV attention path computes, used to check the
+ * CUDA library.  Only the test suite, the smoke check and the bench's
+ * CPU-baseline leg may load it.  It shares no code, header, table or helper
+ * with the CUDA library, and the CUDA library never calls it.
+ *
+ * Sources (SGLang attention-backend source pages):
+ *   - flashattention_backend.py, `init_forward_metadata` (strided page table,
+ *     decode/extend metadata), `_build_pa_page_table_kernel` (prefill-aware
+ *     sliding-window page table), `forward_extend` / `forward_decode`
+ *     (`flash_attn_with_kvcache` calls, window_size convention, absorbed MLA
+ *     call with q_rope/k_rope and q_nope/c_kv).
+ *   - dual_chunk_flashattention_backend.py, `_merge_attn_outputs` and the
+ *     three-way decode merge (log-sum-exp state merge), and
+ *     `_dual_chunk_flash_attn_decoding_with_exp_sums` (empty-KV convention:
+ *     out = 0, lse = -inf).
+ *   - nsa_backend.py, `TopkTransformMethod.PAGED`, `forward_decode`,
+ *     `_pad_topk_indices` (top-k logical index -> KV slot, -1 = skip),
+ *     `init_forward_metadata` (`seqlens_expanded`: bottom-right causal).
+ *
+ * Conventions.  All bf16 arrays are passed as their raw 16-bit patterns and
+ * widened exactly to double.  Every function returns 0 on success, a
+ * negative value on a malformed argument, or a positive count of skipped
+ * out-of-range entries where stated.
+ */
+#ifndef PKV_ORACLE_H
+#define PKV_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Strided page table (flashattention_backend.py, `init_forward_metadata`,
+ * "Convert the page table to a strided format"):
+ *   out[b][c] = req_to_token[req_pool_indices[b]][c * page_size] / page_size
+ * for c in [0, n_cols).  Returns 0, or -1 on bad arguments. */
+int orc_strided_page_table(const int32_t *req_to_token, int64_t rtt_stride,
+                           int64_t rtt_cols, const int64_t *req_pool_indices,
+                           int batch, int page_size, int n_cols,
+                           int32_t *out, int64_t out_stride);
+
+/* Prefill-aware sliding-window page table
+ * (flashattention_backend.py, `_build_pa_page_table_kernel`):
+ *   decode_start = max(pf, sl - window); gap = max(decode_start - pf, 0);
+ *   kv_len = sl - gap; dst[i] = req_to_token[req][i < pf ? i : i + gap]
+ * for i < kv_len.  Entries of dst at or past kv_len are left untouched.
+ * Returns 0, -1 on bad arguments, or the number of rows whose kv_len did not
+ * fit in dst_cols (those rows are left untouched and kv_lens gets -1). */
+int orc_swa_page_table(const int32_t *req_to_token, int64_t rtt_stride,
+                       int64_t rtt_cols, const int64_t *req_pool_indices,
+                       const int32_t *seq_lens, const int32_t *prefill_lens,
+                       int batch, int window, int32_t *dst, int64_t dst_stride,
+                       int dst_cols, int32_t *kv_lens);
+
+/* Top-k logical index -> physical KV slot (nsa_backend.py,
+ * `TopkTransformMethod.PAGED`):
+ *   slot = page_table[b][idx / page_size] * page_size + idx % page_size,
+ * -1 stays -1.  Row r of `topk` belongs to request row_req[r].  An index
+ * < -1 or >= limit[b] (limit = cache_seqlens when given, else
+ * pt_cols * page_size) is written as -1 and counted.
+ * Returns the number of such out-of-range entries, or -1 on bad arguments. */
+int orc_topk_to_slots(const int32_t *topk, int64_t topk_stride, int n_rows,
+                      int topk_len, const int32_t *row_req,
+                      const int32_t *page_table, int64_t pt_stride,
+                      int pt_cols, int page_size,
+                      const int32_t *cache_seqlens, int32_t *out,
+                      int64_t out_stride);
+
+/* Paged attention of new query tokens against a paged KV cache
+ * (flashattention_backend.py `forward_decode` / `forward_extend`,
+ * nsa_backend.py `forward_decode` for the top-k variant).
+ *
+ * q:        bf16 bits, element (t, h, d) at q[t*q_st + h*q_sh + d], d < d_qk.
+ * k_cache:  bf16 bits, element (page, pos, head, d) at
+ *           k[page*k_sp + pos*k_spos + head*k_sh + d], d < d_qk.
+ * v_cache:  same with v_* strides, d < d_v.  For absorbed MLA pass the
+ *           k buffer again: the value row is the first d_v entries of the
+ *           576-wide latent row.
+ * page_table: int32 [batch][pt_cols] page ids (row stride pt_stride).
+ * cache_seqlens: int32 [batch], total KV length including the new tokens.
+ * cu_seqlens_q:  int32 [batch+1], query token offsets.
+ * Query token t of request b at local index u = t - cu[b] sits at absolute
+ * position i = cache_seqlens[b] - (cu[b+1]-cu[b]) + u (bottom-right causal).
+ * Dense key set: j in [0, kv_len); causal => j <= i;
+ * window_left >= 0 => i - window_left <= j <= i (window (left, 0), both ends
+ * inclusive).  Top-k (topk != NULL): the keys are the entries of
+ * topk[t*topk_stride + 0 .. topk_len), -1 skipped, each occurrence counted,
+ * then the same masks; an index < -1 or >= kv_len is skipped and counted.
+ * q head h reads kv head h / (h_q / h_kv).
+ * s_j = scale * <q, K_j>;  lse = log sum_j exp(s_j);  o = sum_j exp(s_j-lse) V_j.
+ * Empty key set: o = 0, lse = -inf.
+ *
+ * rows: optional list of n_rows (token, head) pairs (int32 pairs) to compute;
+ *       NULL computes every (token, head), n_rows ignored.
+ * out:  double, [n][d_v] in row order (all rows: n = total_q*h_q, ordered
+ *       token-major then head).  lse: double [n] (may be NULL).
+ * Returns the number of skipped out-of-range top-k entries or page ids, or
+ * a negative value on bad arguments. */
+int orc_attention(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q,
+                  int h_q, int d_qk, const uint16_t *k_cache, int64_t k_sp,
+                  int64_t k_spos, int64_t k_sh, const uint16_t *v_cache,
+                  int64_t v_sp, int64_t v_spos, int64_t v_sh, int d_v,
+                  int h_kv, int page_size, int64_t num_pages,
+                  const int32_t *page_table, int64_t pt_stride, int pt_cols,
+                  const int32_t *cache_seqlens, const int32_t *cu_seqlens_q,
+                  int batch, double scale, int causal, int window_left,
+                  const int32_t *topk, int64_t topk_stride, int topk_len,
+                  const int32_t *rows, int n_rows, double *out, double *lse,
+                  int num_threads);
+
+/* Log-sum-exp state merge (dual_chunk_flashattention_backend.py,
+ * `_merge_attn_outputs`; merge_state_v2 in flashattention_backend.py):
+ *   m = max(lse_a, lse_b); lse = m + log(exp(lse_a-m) + exp(lse_b-m));
+ *   o = exp(lse_a-lse) o_a + exp(lse_b-lse) o_b.
+ * Both -inf gives (0, -inf).  Arrays are contiguous [n][d] / [n]. */
+int orc_merge_state(const double *v_a, const double *lse_a, const double *v_b,
+                    const double *lse_b, int64_t n, int d, double *v_out,
+                    double *lse_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,469 @@
+"""Pins for the float64 oracle: checks against facts that the pages and the
+mathematics fix, independent of the oracle's own code.
+
+Each test names what it pins.  A plausible slip anywhere in the oracle (a
+dropped term, a wrong sign or index, a transposed operand, an off-by-one mask
+or window, a wrong page/slot map, a wrong merge weight) fails at least one.
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from conftest import read_golden
+from paged_kv_cache_203_gb300 import workloads
+
+
+def bf16(a):
+    """float array -> (bf16 bit patterns, exact float64 values)."""
+    t = torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return oracle.bf16_bits(t), t.to(torch.float64).numpy()
+
+
+def paged_from_logical(rng, kv_logical, page_size, extra_pages=3):
+    """Scatter per-request logical rows [L_b, H_kv, D] into a shuffled page
+    pool.  Returns (cache [pages, P, H_kv, D] float, page_table int32)."""
+    h_kv, d = kv_logical[0].shape[1:]
+    n_pages_req = [max(1, -(-len(x) // page_size)) for x in kv_logical]
+    num_pages = sum(n_pages_req) + extra_pages
+    perm = rng.permutation(num_pages)
+    cache = rng.standard_normal((num_pages, page_size, h_kv, d))  # junk fill
+    pt = np.full((len(kv_logical), max(n_pages_req)), 0, dtype=np.int32)
+    off = 0
+    for b, x in enumerate(kv_logical):
+        for c in range(n_pages_req[b]):
+            page = perm[off]
+            off += 1
+            pt[b, c] = page
+            rows = x[c * page_size:(c + 1) * page_size]
+            cache[page, : len(rows)] = rows
+    return cache, pt
+
+
+def dense_reference_row(q, K, V, scale):
+    """Attention of one query over explicit key/value rows via scipy's
+    softmax / logsumexp (a library routine)."""
+    s = scale * (K @ q)
+    return scipy.special.softmax(s) @ V, scipy.special.logsumexp(s)
+
+
+# ----------------------------------------------------------------- page tables
+
+def test_strided_page_table_recovers_allocated_pages():
+    """a1 closed form: when request b owns pages pt[b, c] and req_to_token
+    holds slot pt[b, j//P]*P + j%P, the strided table is pt itself."""
+    for p in (1, 16, 64):
+        wl = workloads.make("varlen_extend", batch=5, new_lo=3, new_hi=70,
+                            prefix_hi=200, page_size=p, pool_pages=4096 // p + 64,
+                            h_q=2, h_kv=1, d=8)
+        n_cols = wl.page_table.shape[1]
+        got = oracle.strided_page_table(wl.req_to_token.numpy(),
+                                        wl.req_pool_indices.numpy(), p, n_cols)
+        assert np.array_equal(got, wl.page_table.numpy())
+
+
+def test_strided_page_table_hand_example():
+    """a1 on a hand-built row: slots 40..47 then 8..15 with P=8 are pages 5, 1;
+    floor division of the first slot of each page."""
+    rtt = np.array([[40, 41, 42, 43, 44, 45, 46, 47, 8, 9, 10, 11, 12, 13, 14, 15]],
+                   dtype=np.int32)
+    got = oracle.strided_page_table(rtt, np.array([0]), 8, 2)
+    assert got.tolist() == [[5, 1]]
+
+
+@pytest.mark.parametrize("row", read_golden("swa_rows.txt"))
+def test_swa_rows_hand_worked(row):
+    """a2: hand-worked rows of the prefill-aware SWA rule (golden fixture)."""
+    (pf, sl, w), (kv_len,), kept = row
+    rtt = (np.arange(64, dtype=np.int32) * 7 + 3)[None, :]  # distinct slots
+    dst, kv, bad = oracle.swa_page_table(rtt, np.array([0]), np.array([sl]),
+                                         np.array([pf]), w, 32, fill=-5)
+    assert bad == 0
+    assert kv.tolist() == [kv_len]
+    assert dst[0, :kv_len].tolist() == [int(rtt[0, i]) for i in kept]
+    assert np.all(dst[0, kv_len:] == -5)  # the tail is left untouched
+
+
+def test_swa_rows_match_set_membership():
+    """a2 against the set definition: position i of the sequence is kept iff
+    it is part of the prompt (i < pf) or among the last `window` tokens
+    (i >= sl - window); kept positions stay in order."""
+    rng = np.random.default_rng(7)
+    pool = 9
+    rtt = rng.permutation(pool * 300).astype(np.int32).reshape(pool, 300)
+    for _ in range(40):
+        b = 6
+        rpi = rng.permutation(pool)[:b]
+        pf_pool = rng.integers(0, 120, pool).astype(np.int32)
+        sl = rng.integers(1, 300, b).astype(np.int32)
+        w = int(rng.integers(0, 150))
+        dst, kv, bad = oracle.swa_page_table(rtt, rpi, sl, pf_pool, w, 300)
+        assert bad == 0
+        for r in range(b):
+            pf = pf_pool[rpi[r]]
+            kept = [i for i in range(sl[r]) if i < pf or i >= sl[r] - w]
+            assert kv[r] == len(kept)
+            assert dst[r, : kv[r]].tolist() == [int(rtt[rpi[r], i]) for i in kept]
+
+
+def test_swa_row_too_long_is_reported():
+    rtt = np.arange(40, dtype=np.int32)[None, :]
+    dst, kv, bad = oracle.swa_page_table(rtt, np.array([0]), np.array([30]),
+                                         np.array([10]), 8, 12)
+    assert bad == 1 and kv.tolist() == [-1]
+
+
+def test_topk_to_slots_matches_token_level_table():
+    """a3: the page-level map pt[b, idx//P]*P + idx%P equals the token-level
+    lookup req_to_token[req_b, idx] (the page_size-1 table of the NSA path),
+    -1 stays -1, out-of-range entries become -1 and are counted."""
+    for p in (1, 16, 64):
+        wl = workloads.make("varlen_extend", batch=4, new_lo=1, new_hi=40,
+                            prefix_hi=300, page_size=p,
+                            pool_pages=2048 // p + 40, h_q=1, h_kv=1, d=8)
+        rng = np.random.default_rng(p)
+        kv = wl.cache_seqlens.numpy()
+        rows, row_req = [], []
+        for b in range(4):
+            for _ in range(3):
+                idx = rng.integers(0, kv[b], 10)
+                idx[rng.random(10) < 0.2] = -1
+                rows.append(idx)
+                row_req.append(b)
+        topk = np.array(rows, dtype=np.int32)
+        topk[0, 0] = kv[0]          # one past the end -> counted, -1
+        topk[1, 1] = -7             # below -1 -> counted, -1
+        slots, bad = oracle.topk_to_slots(topk, row_req, wl.page_table.numpy(),
+                                          p, kv)
+        assert bad == 2
+        rtt = wl.req_to_token.numpy()
+        rpi = wl.req_pool_indices.numpy()
+        for r, b in enumerate(row_req):
+            for k, idx in enumerate(topk[r]):
+                want = -1 if (idx < 0 or idx >= kv[b]) else rtt[rpi[b], idx]
+                assert slots[r, k] == want
+
+
+# -------------------------------------------------------------------- attention
+
+def _tiny_case(rng, batch, q_lens, kv_lens, h_q, h_kv, d, page_size, d_v=None):
+    d_v = d if d_v is None else d_v
+    kl = [rng.standard_normal((n, h_kv, d)) for n in kv_lens]
+    vl = [rng.standard_normal((n, h_kv, d_v)) for n in kv_lens]
+    kc, pt = paged_from_logical(np.random.default_rng(11), kl, page_size)
+    vc, pt2 = paged_from_logical(np.random.default_rng(11), vl, page_size)
+    assert np.array_equal(pt, pt2)
+    total_q = sum(q_lens)
+    q = rng.standard_normal((total_q, h_q, d))
+    qb, qf = bf16(q)
+    kb, kf = bf16(kc)
+    vb, vf = bf16(vc)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    # exact (bf16-rounded) logical rows, for the reference computations
+    klog = [np.stack([kf[pt[b, j // page_size], j % page_size] for j in range(n)])
+            if n else np.zeros((0, h_kv, d)) for b, n in enumerate(kv_lens)]
+    vlog = [np.stack([vf[pt[b, j // page_size], j % page_size] for j in range(n)])
+            if n else np.zeros((0, h_kv, d_v)) for b, n in enumerate(kv_lens)]
+    return dict(qb=qb, qf=qf, kb=kb, vb=vb, pt=pt, cu=cu,
+                kv=np.array(kv_lens, dtype=np.int32), klog=klog, vlog=vlog)
+
+
+@pytest.mark.parametrize("page_size", [1, 3, 16])
+def test_attention_matches_scipy_softmax(page_size):
+    """Dense paged attention equals softmax(scale K q) V computed by scipy on
+    the logical (unpaged) rows, GQA head map h -> h // (H_q/H_kv), causal
+    bottom-right alignment and windows included."""
+    rng = np.random.default_rng(page_size)
+    h_q, h_kv, d = 6, 2, 16
+    q_lens, kv_lens = [1, 4, 3], [9, 13, 3]
+    c = _tiny_case(rng, 3, q_lens, kv_lens, h_q, h_kv, d, page_size)
+    scale = 0.37
+    for causal, wl in [(False, -1), (True, -1), (True, 2), (False, 5)]:
+        out, lse, sk = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"],
+                                        c["cu"], scale, causal, wl)
+        assert sk == 0
+        for b in range(3):
+            for u in range(q_lens[b]):
+                t = c["cu"][b] + u
+                i = kv_lens[b] - q_lens[b] + u
+                js = [j for j in range(kv_lens[b])
+                      if (not causal or j <= i) and (wl < 0 or i - wl <= j <= i)]
+                for h in range(h_q):
+                    kvh = h // (h_q // h_kv)
+                    K = c["klog"][b][js, kvh]
+                    V = c["vlog"][b][js, kvh]
+                    o_ref, l_ref = dense_reference_row(c["qf"][t, h], K, V, scale)
+                    np.testing.assert_allclose(out[t, h], o_ref, rtol=0, atol=1e-12)
+                    assert abs(lse[t, h] - l_ref) < 1e-12
+
+
+@pytest.mark.parametrize("row", read_golden("causal_counts.txt"))
+def test_visible_key_counts(row):
+    """Bottom-right causal alignment and the (W, 0) window (golden fixture):
+    with q = 0 every visible key gets weight 1/n, so with V = identity rows
+    the output is 1/n on exactly the visible keys and lse = log n."""
+    (kv_len, q_len, wl), counts = row
+    d = kv_len
+    kc = np.zeros((kv_len, 1, 1, d))
+    vc = np.eye(kv_len).reshape(kv_len, 1, 1, d)
+    qb, _ = bf16(np.zeros((q_len, 1, d)))
+    kb, _ = bf16(kc)
+    vb, _ = bf16(vc)
+    pt = np.arange(kv_len, dtype=np.int32)[None, :]
+    out, lse, _ = oracle.attention(qb, kb, vb, pt, [kv_len], [0, q_len], 1.0,
+                                   causal=True, window_left=wl)
+    for u in range(q_len):
+        n = counts[u]
+        i = kv_len - q_len + u
+        expect = np.zeros(kv_len)
+        expect[i - n + 1: i + 1] = 1.0 / n  # the n keys ending at position i
+        np.testing.assert_allclose(out[u, 0], expect, atol=1e-15)
+        assert abs(lse[u, 0] - math.log(n)) < 1e-14
+
+
+def test_single_key_returns_its_value_row():
+    """One visible key: weight 1, o = V_0 exactly, lse = s_0."""
+    rng = np.random.default_rng(3)
+    c = _tiny_case(rng, 1, [1], [1], 2, 1, 8, 4)
+    out, lse, _ = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"],
+                                   c["cu"], 0.5)
+    for h in range(2):
+        assert np.array_equal(out[0, h], c["vlog"][0][0, 0])
+        s0 = 0.5 * float(np.dot(c["qf"][0, h], c["klog"][0][0, 0]))
+        assert abs(lse[0, h] - s0) < 1e-13
+
+
+def test_constant_value_rows_return_the_constant():
+    """Softmax weights sum to 1: V_j = v for all j gives o = v."""
+    rng = np.random.default_rng(4)
+    c = _tiny_case(rng, 2, [1, 1], [37, 5], 4, 2, 8, 4)
+    vc = np.broadcast_to(np.array([1.5, -2.0, 0.25, 3.0, 0.0, 1.0, -0.5, 8.0]),
+                         (c["vb"].shape)).copy()
+    vb, _ = bf16(vc)
+    out, _, _ = oracle.attention(c["qb"], c["kb"], vb, c["pt"], c["kv"], c["cu"], 0.9)
+    np.testing.assert_allclose(out, np.broadcast_to(vc[0, 0, 0], out.shape),
+                               rtol=0, atol=1e-13)
+
+
+def test_two_keys_closed_form():
+    """Two keys: o = sigma(s0 - s1) V0 + sigma(s1 - s0) V1,
+    lse = s0 + log(1 + exp(s1 - s0))."""
+    kc = np.array([[[[1.0, 0.0]]], [[[0.0, 1.0]]]])  # keys e0, e1
+    vc = np.array([[[[2.0, -1.0]]], [[[0.5, 4.0]]]])
+    qb, _ = bf16(np.array([[[3.0, 1.0]]]))
+    kb, _ = bf16(kc)
+    vb, _ = bf16(vc)
+    out, lse, _ = oracle.attention(qb, kb, vb, np.array([[0, 1]]), [2], [0, 1], 0.5)
+    s0, s1 = 1.5, 0.5
+    w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    np.testing.assert_allclose(out[0, 0], w0 * vc[0, 0, 0] + (1 - w0) * vc[1, 0, 0],
+                               atol=1e-15)
+    assert abs(lse[0, 0] - (s0 + math.log1p(math.exp(s1 - s0)))) < 1e-15
+
+
+def test_large_scale_selects_argmax_row():
+    """scale -> infinity: softmax -> one-hot on the largest score."""
+    rng = np.random.default_rng(5)
+    c = _tiny_case(rng, 1, [1], [50], 1, 1, 16, 1)
+    out, _, _ = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"],
+                                 c["cu"], 1e4)
+    s = c["klog"][0][:, 0] @ c["qf"][0, 0]
+    np.testing.assert_allclose(out[0, 0], c["vlog"][0][int(np.argmax(s)), 0], atol=1e-9)
+
+
+def test_empty_kv_gives_zero_and_minus_inf():
+    """cache_seqlens == 0 -> out = 0, lse = -inf
+    (dual_chunk_flashattention_backend.py, exp-sums decode)."""
+    rng = np.random.default_rng(6)
+    c = _tiny_case(rng, 2, [1, 1], [0, 4], 2, 1, 8, 2)
+    out, lse, _ = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"],
+                                   c["cu"], 1.0)
+    assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
+    assert np.all(np.isfinite(lse[1]))
+
+
+def test_page_permutation_invariance():
+    """Relabelling physical pages (moving their contents and remapping the
+    table) leaves every output bit unchanged."""
+    rng = np.random.default_rng(8)
+    c = _tiny_case(rng, 3, [1, 2, 1], [30, 17, 45], 4, 2, 8, 4)
+    out0, lse0, _ = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"],
+                                     c["cu"], 0.4, causal=True)
+    perm = rng.permutation(c["kb"].shape[0])  # new page id of old page p
+    kb2 = np.empty_like(c["kb"])
+    vb2 = np.empty_like(c["vb"])
+    kb2[perm] = c["kb"]
+    vb2[perm] = c["vb"]
+    pt2 = perm[c["pt"]].astype(np.int32)
+    out1, lse1, _ = oracle.attention(c["qb"], kb2, vb2, pt2, c["kv"], c["cu"], 0.4,
+                                     causal=True)
+    assert np.array_equal(out0, out1) and np.array_equal(lse0, lse1)
+
+
+def test_page_size_does_not_change_result():
+    """The same logical KV laid out with P=1 and P=16 gives the same output."""
+    rng = np.random.default_rng(9)
+    kl = [rng.standard_normal((n, 1, 8)) for n in (21, 40)]
+    vl = [rng.standard_normal((n, 1, 8)) for n in (21, 40)]
+    qb, _ = bf16(rng.standard_normal((2, 2, 8)))
+    outs = []
+    for p in (1, 16):
+        kc, pt = paged_from_logical(np.random.default_rng(1), kl, p)
+        vc, _ = paged_from_logical(np.random.default_rng(1), vl, p)
+        kb, _ = bf16(kc)
+        vb, _ = bf16(vc)
+        outs.append(oracle.attention(qb, kb, vb, pt, [21, 40], [0, 1, 2], 0.3)[:2])
+    np.testing.assert_allclose(outs[0][0], outs[1][0], atol=1e-14)
+    np.testing.assert_allclose(outs[0][1], outs[1][1], atol=1e-14)
+
+
+def test_wide_window_equals_no_window_and_decode_equals_extend():
+    rng = np.random.default_rng(10)
+    c = _tiny_case(rng, 2, [1, 1], [25, 9], 2, 1, 8, 4)
+    a = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"], c["cu"], 0.3)
+    b = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"], c["cu"], 0.3,
+                         causal=True, window_left=25)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_mla_zero_rope_equals_mqa_over_latent():
+    """Absorbed MLA (q = q_nope || q_rope, K row = c_kv || k_rope, V = c_kv):
+    with k_rope = 0 the score is q_nope . c_kv, i.e. plain MQA over the latent
+    dims with the value rows equal to the key rows."""
+    rng = np.random.default_rng(12)
+    d_l, d_r = 16, 4
+    rows = rng.standard_normal((20, 1, 1, d_l + d_r))
+    rows[..., d_l:] = 0.0
+    kb, _ = bf16(rows)
+    qb, _ = bf16(rng.standard_normal((1, 3, d_l + d_r)))
+    pt = np.arange(20, dtype=np.int32)[None, :]
+    mla = oracle.attention(qb, kb, kb, pt, [20], [0, 1], 0.2, d_v=d_l)
+    lat = np.ascontiguousarray(kb[..., :d_l])
+    mqa = oracle.attention(np.ascontiguousarray(qb[..., :d_l]), lat, lat, pt, [20],
+                           [0, 1], 0.2)
+    np.testing.assert_allclose(mla[0], mqa[0], atol=1e-14)
+    np.testing.assert_allclose(mla[1], mqa[1], atol=1e-14)
+
+
+def test_topk_full_list_equals_dense_and_duplicates_count():
+    rng = np.random.default_rng(13)
+    c = _tiny_case(rng, 2, [1, 1], [19, 33], 2, 1, 8, 4)
+    dense = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"], c["cu"], 0.3)
+    topk = np.full((2, 40), -1, dtype=np.int32)
+    topk[0, :19] = rng.permutation(19)
+    topk[1, :33] = rng.permutation(33)
+    sparse = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"], c["cu"],
+                              0.3, topk=topk)
+    np.testing.assert_allclose(dense[0], sparse[0], atol=1e-14)
+    np.testing.assert_allclose(dense[1], sparse[1], atol=1e-14)
+    # an index listed twice counts twice: weight 2 e^{s_a} against e^{s_b}
+    two = np.array([[3, 3, 7, -1], [0, -1, -1, -1]], dtype=np.int32)
+    out, lse, _ = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"],
+                                   c["cu"], 0.3, topk=two)
+    s = 0.3 * (c["klog"][0][[3, 7], 0] @ c["qf"][0, 0])
+    wa = 2 * math.exp(s[0]) / (2 * math.exp(s[0]) + math.exp(s[1]))
+    want = wa * c["vlog"][0][3, 0] + (1 - wa) * c["vlog"][0][7, 0]
+    np.testing.assert_allclose(out[0, 0], want, atol=1e-13)
+    # all -1: empty
+    empty = np.full((2, 4), -1, dtype=np.int32)
+    out, lse, sk = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"],
+                                    c["cu"], 0.3, topk=empty)
+    assert sk == 0 and np.all(out == 0) and np.all(np.isneginf(lse))
+    # out of range entries are skipped and counted
+    bad = np.array([[3, 19, -3, -1], [0, 1, 2, 3]], dtype=np.int32)
+    _, _, sk = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"],
+                                c["cu"], 0.3, topk=bad)
+    assert sk == 2
+
+
+def test_row_subset_matches_full():
+    rng = np.random.default_rng(14)
+    c = _tiny_case(rng, 2, [3, 2], [10, 20], 4, 2, 8, 4)
+    full, lfull, _ = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"],
+                                      c["cu"], 0.3, causal=True)
+    rows = np.array([[0, 3], [4, 1], [2, 0]], dtype=np.int32)
+    sub, lsub, _ = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"],
+                                    c["cu"], 0.3, causal=True, rows=rows)
+    for n, (t, h) in enumerate(rows):
+        assert np.array_equal(sub[n], full[t, h]) and lsub[n] == lfull[t, h]
+
+
+# ------------------------------------------------------------------------ merge
+
+def test_merge_of_two_halves_equals_full_attention():
+    """Merging the states of any two disjoint key halves equals attention
+    over the whole key set (every split point, empty halves included)."""
+    rng = np.random.default_rng(15)
+    n = 23
+    c = _tiny_case(rng, 1, [1], [n], 2, 1, 8, 1)
+    full_o, full_l, _ = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"],
+                                         c["cu"], 0.6)
+    for cut in range(0, n + 1):
+        pa = c["pt"][:, :max(cut, 1)]
+        pb = np.ascontiguousarray(c["pt"][:, cut:]) if cut < n else c["pt"][:, :1]
+        oa, la, _ = oracle.attention(c["qb"], c["kb"], c["vb"], pa, [cut], c["cu"], 0.6)
+        ob, lb, _ = oracle.attention(c["qb"], c["kb"], c["vb"], pb, [n - cut], c["cu"], 0.6)
+        om, lm = oracle.merge_state(oa, la, ob, lb)
+        np.testing.assert_allclose(om, full_o, atol=1e-13)
+        np.testing.assert_allclose(lm, full_l, atol=1e-13)
+
+
+def test_merge_closed_forms_and_algebra():
+    rng = np.random.default_rng(16)
+    va, vb, vc = (rng.standard_normal((5, 3, 4)) for _ in range(3))
+    la, lb, lc = (rng.standard_normal((5, 3)) * 3 for _ in range(3))
+    # equal lse: plain average, lse + log 2
+    o, l = oracle.merge_state(va, la, vb, la)
+    np.testing.assert_allclose(o, (va + vb) / 2, atol=1e-15)
+    np.testing.assert_allclose(l, la + math.log(2), atol=1e-15)
+    # commutative and associative
+    o1, l1 = oracle.merge_state(va, la, vb, lb)
+    o2, l2 = oracle.merge_state(vb, lb, va, la)
+    np.testing.assert_allclose(o1, o2, atol=1e-15)
+    np.testing.assert_allclose(l1, l2, atol=1e-15)
+    x, lx = oracle.merge_state(*oracle.merge_state(va, la, vb, lb), vc, lc)
+    y, ly = oracle.merge_state(va, la, *oracle.merge_state(vb, lb, vc, lc))
+    np.testing.assert_allclose(x, y, atol=1e-14)
+    np.testing.assert_allclose(lx, ly, atol=1e-14)
+    # the n-way form on the pages (weights softmax(lse_i), merged lse of two
+    # states = max + log1p(exp(-|lse_0 - lse_1|)))
+    w = scipy.special.softmax(np.stack([la, lb, lc]), axis=0)
+    np.testing.assert_allclose(x, w[0][..., None] * va + w[1][..., None] * vb
+                               + w[2][..., None] * vc, atol=1e-14)
+    np.testing.assert_allclose(l1, np.maximum(la, lb) + np.log1p(np.exp(-np.abs(la - lb))),
+                               atol=1e-14)
+    # an empty state is the identity; two empty states give (0, -inf)
+    ninf = np.full_like(la, -np.inf)
+    o, l = oracle.merge_state(va, la, np.zeros_like(vb), ninf)
+    np.testing.assert_allclose(o, va, atol=0)
+    np.testing.assert_allclose(l, la, atol=0)
+    o, l = oracle.merge_state(va, ninf, vb, ninf)
+    assert np.all(o == 0) and np.all(np.isneginf(l))
+
+
+@pytest.mark.parametrize("num_splits", [1, 2, 4, 7])
+def test_split_attention_equals_full(num_splits):
+    """Split-KV partial states merged left to right equal single-pass
+    attention, whatever the chunk boundaries."""
+    wl = workloads.make("gqa_split_decode", batch=5, len_lo=1, len_hi=150,
+                        pool_pages=200, h_q=4, h_kv=2, d=16)
+    args = (oracle.bf16_bits(wl.q), oracle.bf16_bits(wl.k_cache),
+            oracle.bf16_bits(wl.v_cache), wl.page_table.numpy(),
+            wl.cache_seqlens.numpy(), wl.cu_seqlens_q.numpy(), wl.scale)
+    full_o, full_l, _ = oracle.attention(*args)
+    so, sl = oracle.split_attention(*args, num_splits=num_splits)
+    np.testing.assert_allclose(so, full_o, atol=1e-13)
+    np.testing.assert_allclose(sl, full_l, atol=1e-13)
+
+
+def test_split_bounds_are_page_aligned_and_cover():
+    for kv in (0, 1, 15, 16, 17, 1000, 8191):
+        for p in (1, 16, 64):
+            for s in (1, 2, 4, 5):
+                b = oracle.split_bounds(kv, s, p)
+                assert b[0][0] == 0 and b[-1][1] == kv
+                for (lo, hi), (lo2, _) in zip(b, b[1:]):
+                    assert hi == lo2 and (lo % p == 0 or lo == kv)
