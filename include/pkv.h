@@ -1,0 +1,239 @@
+/*
+ * pkv.h -- C ABI of libpkv, paged-KV attention for GB300 (sm_103a).
+ *
+ * The operations are those of the SGLang attention-backend pages
+ * (flashattention_backend.py, dual_chunk_flashattention_backend.py,
+ * nsa_backend.py): attention of new query tokens against a paged KV cache,
+ * the log-sum-exp state merge, and the integer page-table builders.
+ *
+ * General rules for every entry point
+ * -----------------------------------
+ * - Tensors are passed as `pkv_tensor` descriptors: a pointer, a dtype, a
+ *   rank and per-dimension sizes and strides counted in ELEMENTS.  All data
+ *   pointers are DEVICE pointers on the current CUDA device, owned by the
+ *   caller; the library never allocates, frees or retains them.  An optional
+ *   tensor is "absent" when its `data` is NULL.
+ * - Every call is asynchronous on `stream` (0 = the legacy default stream)
+ *   and returns an `int` status: PKV_OK (0) or a negative PKV_ERR_* code.  A
+ *   negative status means nothing was launched.  No C++ exception crosses
+ *   this boundary.
+ * - Data-dependent faults that can only be seen on the device (a page id
+ *   outside the KV pool, a top-k index outside [-1, kv_len), a page-table row
+ *   too short for its sequence) never trap: the offending entry is skipped
+ *   (treated as masked / written as -1) and a sticky bit is set in a device
+ *   error word, read with pkv_get_error_flags() after synchronising.
+ * - The library keeps no state between calls apart from that error word.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ types */
+
+enum pkv_dtype {
+  PKV_BF16 = 1, /* bfloat16 */
+  PKV_F32 = 2,  /* float32 */
+  PKV_I32 = 3,  /* int32 */
+  PKV_I64 = 4   /* int64 */
+};
+
+enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = -1, /* shape / dtype / stride / value mismatch */
+  PKV_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. head dim) */
+  PKV_ERR_CUDA = -3,        /* a CUDA runtime call failed */
+  PKV_ERR_WORKSPACE = -4    /* workspace missing or too small */
+};
+
+/* Bits of the device error word (sticky until pkv_clear_error_flags). */
+enum pkv_error_bits {
+  PKV_EFLAG_PAGE_OOB = 1,    /* page id outside [0, num_pages): key skipped */
+  PKV_EFLAG_TOPK_OOB = 2,    /* top-k index < -1 or >= kv_len: entry skipped */
+  PKV_EFLAG_ROW_TOO_SHORT = 4, /* page-table / dst row narrower than needed */
+  PKV_EFLAG_SRC_OOB = 8      /* req_to_token column or pool row out of range */
+};
+
+typedef struct pkv_tensor {
+  void *data;        /* device pointer; NULL = absent (optional tensors) */
+  int32_t dtype;     /* enum pkv_dtype */
+  int32_t ndim;      /* 1..4 */
+  int64_t shape[4];  /* sizes; unused trailing entries ignored */
+  int64_t stride[4]; /* strides in elements */
+} pkv_tensor;
+
+/* ------------------------------------------------------------- attention */
+
+/*
+ * pkv_attn_with_kvcache -- paged attention of new query tokens.
+ *
+ * Defined by the `flash_attn_with_kvcache` calls of
+ * flashattention_backend.py (`forward_decode`, `forward_extend`, the
+ * absorbed-MLA call that passes q_rope/k_rope plus q_nope/c_kv) and by the
+ * NSA sparse decode of nsa_backend.py (`forward_decode`: top-k lists mapped
+ * through the page table, `TopkTransformMethod.PAGED`).
+ *
+ * For request b (B = cache_seqlens.shape[0]) with q_len_b =
+ * cu_seqlens_q[b+1] - cu_seqlens_q[b] new tokens and kv_len_b =
+ * cache_seqlens[b] keys (the new tokens included), new token u sits at
+ * absolute position i = kv_len_b - q_len_b + u (bottom-right alignment,
+ * `seqlens_expanded` in nsa_backend.py).  Query head h reads KV head
+ * h / (H_q / H_kv).  Logical key j lives in slot
+ *   page_table[b][j / P] * P + j % P,   P = k_cache.shape[1].
+ * Visible keys: j < kv_len_b; j <= i if causal; i - window_left <= j <= i
+ * if window_left >= 0 (the (window_left, 0) window, both ends inclusive).
+ * With topk_indices the keys are instead the entries of that token's row
+ * (logical positions; -1 = skip; each occurrence counts), under the same
+ * masks.
+ *   s_j = scale * <q, K_j>,  lse = ln sum_j exp(s_j),
+ *   out = sum_j exp(s_j - lse) V_j;  no visible key: out = 0, lse = -inf.
+ *
+ * q            bf16 [total_q, H_q, Dq], last dim contiguous.
+ * k_cache      bf16 [num_pages, P, H_kv, Dq], last dim contiguous.
+ * v_cache      bf16 [num_pages, P, H_kv, Dv], last dim contiguous.  For
+ *              absorbed MLA (Dq = 576, Dv = 512, H_kv = 1) pass a view of
+ *              the k_cache rows (same pointer and strides, shape[3] = 512).
+ * page_table   int32 [B, max_pages] page ids.
+ * cache_seqlens int32 [B].
+ * cu_seqlens_q int32 [B + 1], non-decreasing, cu[B] <= total_q.
+ * max_seqlen_q host int, >= every q_len_b.
+ * topk_indices optional int32 [total_q, topk] logical key positions.
+ * num_splits   0 = chosen by the library, 1 = no split, k = at most k
+ *              contiguous key chunks per (request, KV head), combined by the
+ *              log-sum-exp state merge inside the library.
+ * out          bf16 [total_q, H_q, Dv] (written).
+ * lse          optional fp32 [total_q, H_q], natural log (written).
+ * workspace    device scratch of at least pkv_attn_workspace_size(...) bytes
+ *              for the same arguments (may be NULL when that size is 0).
+ *              Its contents need no initialisation and are clobbered.
+ *
+ * Supported: Dq = Dv in {64, 128} with H_q % H_kv == 0; and absorbed MLA
+ * Dq = 576, Dv = 512, H_kv = 1.  Other shapes return PKV_ERR_UNSUPPORTED.
+ * Concurrent calls that share one workspace race.
+ */
+int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
+                          pkv_tensor page_table, pkv_tensor cache_seqlens,
+                          pkv_tensor cu_seqlens_q, int max_seqlen_q,
+                          float scale, int causal, int window_left,
+                          pkv_tensor topk_indices, int num_splits,
+                          pkv_tensor out, pkv_tensor lse, void *workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of workspace pkv_attn_with_kvcache needs for these sizes (0 if
+ * none).  Arguments mirror the attention call's; returns 0 and sets
+ * *bytes, or a negative status. */
+int pkv_attn_workspace_size(pkv_tensor q, pkv_tensor k_cache,
+                            pkv_tensor v_cache, pkv_tensor page_table,
+                            pkv_tensor cache_seqlens, int max_seqlen_q,
+                            pkv_tensor topk_indices, int num_splits,
+                            size_t *bytes);
+
+/*
+ * pkv_merge_state -- log-sum-exp merge of two attention states.
+ *
+ * Defined by `_merge_attn_outputs` and the three-way decode merge of
+ * dual_chunk_flashattention_backend.py and by the merge_state_v2 call of
+ * flashattention_backend.py (cascade decode), per row (n, h):
+ *   m = max(lse_a, lse_b);  lse = m + ln(exp(lse_a - m) + exp(lse_b - m));
+ *   v = exp(lse_a - lse) v_a + exp(lse_b - lse) v_b;
+ * both lse = -inf gives v = 0, lse = -inf.
+ *
+ * v_a, v_b   bf16 or fp32 [N, H, D], last dim contiguous (same dtype).
+ * lse_a/b    fp32 [N, H] (natural log; the transposed FA layout).
+ * v_out      bf16 or fp32 [N, H, D].
+ * lse_out    optional fp32 [N, H].
+ * v_out may alias v_a or v_b (in-place merge); lse_out must not alias
+ * lse_a or lse_b (PKV_ERR_INVALID_ARG).  D must be a multiple of 8 with
+ * 16-byte aligned rows (PKV_ERR_UNSUPPORTED otherwise).
+ */
+int pkv_merge_state(pkv_tensor v_a, pkv_tensor lse_a, pkv_tensor v_b,
+                    pkv_tensor lse_b, pkv_tensor v_out, pkv_tensor lse_out,
+                    cudaStream_t stream);
+
+/* ---------------------------------------------------------- page tables */
+
+/*
+ * pkv_build_swa_page_table -- prefill-aware sliding-window page table.
+ *
+ * Defined by `_build_pa_page_table_kernel` / `_build_pa_page_table` in
+ * flashattention_backend.py.  For row b with req = req_pool_indices[b],
+ * sl = seq_lens[b], pf = prefill_lens[req]:
+ *   decode_start = max(pf, sl - window);  gap = max(decode_start - pf, 0);
+ *   kv_len = sl - gap;
+ *   dst_page_table[b][i] = req_to_token[req][i < pf ? i : i + gap], i < kv_len;
+ *   dst_kv_lens[b] = kv_len.
+ * Entries at or past kv_len are not written (in-place refill of caller
+ * buffers, as in CUDA-graph replay).
+ *
+ * req_to_token     int32 [pool_rows, max_ctx].
+ * req_pool_indices int32 or int64 [B].
+ * seq_lens         int32 [B].
+ * prefill_lens     int32 [pool_rows] (indexed through req_pool_indices).
+ * window           >= 0 (the model's sliding window, as passed by the page).
+ * dst_page_table   int32 [B, W]; a row whose kv_len exceeds W is not
+ *                  written, gets dst_kv_lens = -1 and sets
+ *                  PKV_EFLAG_ROW_TOO_SHORT.
+ * dst_kv_lens      int32 [B].
+ */
+int pkv_build_swa_page_table(pkv_tensor req_to_token,
+                             pkv_tensor req_pool_indices, pkv_tensor seq_lens,
+                             pkv_tensor prefill_lens, int window,
+                             pkv_tensor dst_page_table, pkv_tensor dst_kv_lens,
+                             cudaStream_t stream);
+
+/*
+ * pkv_strided_page_table -- token-level table to page-level table.
+ *
+ * Defined in flashattention_backend.py `init_forward_metadata` ("Convert
+ * the page table to a strided format"):
+ *   out[b][c] = req_to_token[req_pool_indices[b]][c * page_size] / page_size,
+ * for c < out.shape[1].  Columns whose source lies past req_to_token's width
+ * are written as -1 and set PKV_EFLAG_SRC_OOB.
+ *
+ * req_to_token int32 [pool_rows, max_ctx]; req_pool_indices int32|int64 [B];
+ * out int32 [B, n_cols].
+ */
+int pkv_strided_page_table(pkv_tensor req_to_token,
+                           pkv_tensor req_pool_indices, int page_size,
+                           pkv_tensor out, cudaStream_t stream);
+
+/*
+ * pkv_topk_to_slots -- top-k logical positions to physical KV slots.
+ *
+ * Defined by nsa_backend.py `TopkTransformMethod.PAGED` (the page-table
+ * transform of `forward_decode`):
+ *   out[t][k] = page_table[b][idx / P] * P + idx % P,  idx = topk[t][k],
+ * where b is the request of token t (cu_seqlens_q[b] <= t < cu[b+1]);
+ * idx = -1 stays -1; idx < -1 or idx >= cache_seqlens[b] is written as -1
+ * and sets PKV_EFLAG_TOPK_OOB.
+ *
+ * topk int32 [total_q, K]; cu_seqlens_q int32 [B+1]; page_table int32
+ * [B, max_pages]; cache_seqlens int32 [B]; out int32 [total_q, K].
+ */
+int pkv_topk_to_slots(pkv_tensor topk, pkv_tensor cu_seqlens_q,
+                      pkv_tensor page_table, pkv_tensor cache_seqlens,
+                      int page_size, pkv_tensor out, cudaStream_t stream);
+
+/* ------------------------------------------------------------ errors */
+
+/* Reads the current device's error word (synchronous copy; call after the
+ * work of interest has completed).  Returns PKV_OK and sets *flags. */
+int pkv_get_error_flags(uint32_t *flags);
+
+/* Clears the current device's error word (synchronous). */
+int pkv_clear_error_flags(void);
+
+/* Library version, for the bindings' sanity check. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

@@ -1,0 +1,244 @@
+"""paged_kv_cache_203_gb300 -- paged-KV attention on GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libpkv.so`` (declared in
+``include/pkv.h``).  The functions here only marshal torch tensors into
+``pkv_tensor`` descriptors, allocate outputs / workspace with torch and pass
+torch's current stream; every step of the computation runs in the library's
+CUDA kernels.  There is no CPU or eager fallback: if the library is missing
+the first call raises.
+
+Entry points (names as in the C ABI, without the ``pkv_`` prefix):
+
+* ``attn_with_kvcache`` -- paged attention of new query tokens
+  (flashattention_backend.py ``flash_attn_with_kvcache`` calls; nsa_backend.py
+  top-k sparse decode), with split-KV combined by the state merge.
+* ``merge_state`` -- log-sum-exp merge of two attention states
+  (``merge_state_v2`` / ``_merge_attn_outputs``).
+* ``build_swa_page_table`` -- prefill-aware sliding-window page table
+  (``_build_pa_page_table``).
+* ``strided_page_table`` -- token-level to page-level table.
+* ``topk_to_slots`` -- top-k logical positions to KV slots
+  (``TopkTransformMethod.PAGED``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import build_library, lib_path
+
+__all__ = [
+    "attn_with_kvcache",
+    "attn_workspace_size",
+    "merge_state",
+    "build_swa_page_table",
+    "strided_page_table",
+    "topk_to_slots",
+    "get_error_flags",
+    "clear_error_flags",
+    "load_library",
+    "build_library",
+    "PkvError",
+    "EXPORTED_SYMBOLS",
+    "EFLAG_PAGE_OOB",
+    "EFLAG_TOPK_OOB",
+    "EFLAG_ROW_TOO_SHORT",
+    "EFLAG_SRC_OOB",
+]
+
+# dtype codes and status codes of include/pkv.h
+_BF16, _F32, _I32, _I64 = 1, 2, 3, 4
+_STATUS = {0: "PKV_OK", -1: "PKV_ERR_INVALID_ARG", -2: "PKV_ERR_UNSUPPORTED",
+           -3: "PKV_ERR_CUDA", -4: "PKV_ERR_WORKSPACE"}
+EFLAG_PAGE_OOB, EFLAG_TOPK_OOB, EFLAG_ROW_TOO_SHORT, EFLAG_SRC_OOB = 1, 2, 4, 8
+
+EXPORTED_SYMBOLS = (
+    "pkv_attn_with_kvcache",
+    "pkv_attn_workspace_size",
+    "pkv_merge_state",
+    "pkv_build_swa_page_table",
+    "pkv_strided_page_table",
+    "pkv_topk_to_slots",
+    "pkv_get_error_flags",
+    "pkv_clear_error_flags",
+    "pkv_version",
+)
+
+_DTYPES = {torch.bfloat16: _BF16, torch.float32: _F32, torch.int32: _I32,
+           torch.int64: _I64}
+
+
+class PkvError(RuntimeError):
+    """A libpkv entry point returned a negative status."""
+
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {_STATUS.get(code, code)}")
+        self.code = code
+
+
+class _Tensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32),
+                ("ndim", ctypes.c_int32), ("shape", ctypes.c_int64 * 4),
+                ("stride", ctypes.c_int64 * 4)]
+
+
+_ABSENT = _Tensor()
+_LIB = None
+
+
+def load_library(path: str | None = None):
+    """Load libpkv.so (built by ``build_library()`` / ``__graft_entry__.build``).
+    Raises if it is missing: there is no fallback path."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = path or lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"libpkv.so not found at {path}; build it first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    T = _Tensor
+    c_int, c_float, c_void_p, c_size_t = (ctypes.c_int, ctypes.c_float,
+                                          ctypes.c_void_p, ctypes.c_size_t)
+    lib.pkv_attn_with_kvcache.argtypes = [T, T, T, T, T, T, c_int, c_float, c_int,
+                                          c_int, T, c_int, T, T, c_void_p, c_size_t,
+                                          c_void_p]
+    lib.pkv_attn_workspace_size.argtypes = [T, T, T, T, T, c_int, T, c_int,
+                                            ctypes.POINTER(c_size_t)]
+    lib.pkv_merge_state.argtypes = [T, T, T, T, T, T, c_void_p]
+    lib.pkv_build_swa_page_table.argtypes = [T, T, T, T, c_int, T, T, c_void_p]
+    lib.pkv_strided_page_table.argtypes = [T, T, c_int, T, c_void_p]
+    lib.pkv_topk_to_slots.argtypes = [T, T, T, T, c_int, T, c_void_p]
+    lib.pkv_get_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.pkv_clear_error_flags.argtypes = []
+    lib.pkv_version.argtypes = []
+    for name in EXPORTED_SYMBOLS:
+        getattr(lib, name).restype = ctypes.c_int
+    _LIB = lib
+    return lib
+
+
+def _desc(t: torch.Tensor | None) -> _Tensor:
+    if t is None:
+        return _ABSENT
+    if t.dim() > 4:
+        raise ValueError("pkv tensors have at most 4 dimensions")
+    d = _Tensor()
+    d.data = t.data_ptr() if t.numel() > 0 else (t.data_ptr() or 16)
+    d.dtype = _DTYPES.get(t.dtype, 0)
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise PkvError(fn, rc)
+
+
+def attn_workspace_size(q, k_cache, v_cache, page_table, cache_seqlens,
+                        max_seqlen_q: int, topk_indices=None,
+                        num_splits: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check("pkv_attn_workspace_size", load_library().pkv_attn_workspace_size(
+        _desc(q), _desc(k_cache), _desc(v_cache), _desc(page_table),
+        _desc(cache_seqlens), int(max_seqlen_q), _desc(topk_indices),
+        int(num_splits), ctypes.byref(n)))
+    return n.value
+
+
+def attn_with_kvcache(q, k_cache, v_cache, page_table, cache_seqlens,
+                      cu_seqlens_q, max_seqlen_q: int, softmax_scale: float,
+                      causal: bool = False, window_left: int = -1,
+                      topk_indices=None, num_splits: int = 0, out=None,
+                      lse=None, return_softmax_lse: bool = False,
+                      workspace=None):
+    """Paged attention (see include/pkv.h, pkv_attn_with_kvcache).
+
+    Returns ``out`` or ``(out, lse)`` when ``return_softmax_lse``; ``lse`` is
+    [total_q, H_q] fp32 (natural log)."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty(q.shape[0], q.shape[1], v_cache.shape[-1],
+                          dtype=torch.bfloat16, device=q.device)
+    if return_softmax_lse and lse is None:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32,
+                          device=q.device)
+    ws_bytes = attn_workspace_size(q, k_cache, v_cache, page_table,
+                                   cache_seqlens, max_seqlen_q, topk_indices,
+                                   num_splits)
+    if ws_bytes > 0 and (workspace is None or workspace.numel() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if ws_bytes > 0 else None
+    _check("pkv_attn_with_kvcache", lib.pkv_attn_with_kvcache(
+        _desc(q), _desc(k_cache), _desc(v_cache), _desc(page_table),
+        _desc(cache_seqlens), _desc(cu_seqlens_q), int(max_seqlen_q),
+        float(softmax_scale), int(bool(causal)), int(window_left),
+        _desc(topk_indices), int(num_splits), _desc(out), _desc(lse), ws_ptr,
+        ws_bytes, _stream(q)))
+    return (out, lse) if return_softmax_lse else out
+
+
+def merge_state(v_a, lse_a, v_b, lse_b, v_out=None, lse_out=None):
+    """Log-sum-exp merge of two states; returns (v_out, lse_out)."""
+    lib = load_library()
+    if v_out is None:
+        v_out = torch.empty_like(v_a)
+    if lse_out is None:
+        lse_out = torch.empty_like(lse_a)
+    _check("pkv_merge_state", lib.pkv_merge_state(
+        _desc(v_a), _desc(lse_a), _desc(v_b), _desc(lse_b), _desc(v_out),
+        _desc(lse_out), _stream(v_a)))
+    return v_out, lse_out
+
+
+def build_swa_page_table(req_to_token, req_pool_indices, seq_lens,
+                         prefill_lens, window: int, dst_page_table,
+                         dst_kv_lens):
+    """Prefill-aware SWA page table, written in place; returns the two
+    destination tensors."""
+    _check("pkv_build_swa_page_table", load_library().pkv_build_swa_page_table(
+        _desc(req_to_token), _desc(req_pool_indices), _desc(seq_lens),
+        _desc(prefill_lens), int(window), _desc(dst_page_table),
+        _desc(dst_kv_lens), _stream(req_to_token)))
+    return dst_page_table, dst_kv_lens
+
+
+def strided_page_table(req_to_token, req_pool_indices, page_size: int,
+                       n_cols: int, out=None):
+    if out is None:
+        out = torch.empty(req_pool_indices.shape[0], n_cols, dtype=torch.int32,
+                          device=req_to_token.device)
+    _check("pkv_strided_page_table", load_library().pkv_strided_page_table(
+        _desc(req_to_token), _desc(req_pool_indices), int(page_size),
+        _desc(out), _stream(req_to_token)))
+    return out
+
+
+def topk_to_slots(topk, cu_seqlens_q, page_table, cache_seqlens,
+                  page_size: int, out=None):
+    if out is None:
+        out = torch.empty_like(topk)
+    _check("pkv_topk_to_slots", load_library().pkv_topk_to_slots(
+        _desc(topk), _desc(cu_seqlens_q), _desc(page_table),
+        _desc(cache_seqlens), int(page_size), _desc(out), _stream(topk)))
+    return out
+
+
+def get_error_flags() -> int:
+    v = ctypes.c_uint32(0)
+    _check("pkv_get_error_flags", load_library().pkv_get_error_flags(ctypes.byref(v)))
+    return v.value
+
+
+def clear_error_flags() -> None:
+    _check("pkv_clear_error_flags", load_library().pkv_clear_error_flags())

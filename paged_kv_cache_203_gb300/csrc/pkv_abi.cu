@@ -1,0 +1,376 @@
+// pkv_abi.cu -- the C entry points of libpkv (include/pkv.h): argument
+// validation, split-KV planning, workspace carving and kernel dispatch.
+// Every step of the computation runs in this library's CUDA kernels.
+#include <math.h>
+
+#include <algorithm>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// Sticky device error word (one per device that loads the library).
+static __device__ uint32_t g_error_word;
+
+uint32_t *device_error_word() {
+  static uint32_t *cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  if (dev >= 64) return nullptr;
+  if (cache[dev] == nullptr) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<uint32_t *>(ptr);
+  }
+  return cache[dev];
+}
+
+namespace {
+
+bool present(const pkv_tensor &t) { return t.data != nullptr; }
+
+bool has(const pkv_tensor &t, int dtype, int ndim) {
+  return t.data != nullptr && t.dtype == dtype && t.ndim == ndim;
+}
+
+bool aligned16(const void *p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+// vector (16-byte) access along the last dimension of a bf16/fp32 tensor
+bool vec_ok(const pkv_tensor &t, int elem_bytes) {
+  if (!aligned16(t.data)) return false;
+  if (t.stride[t.ndim - 1] != 1) return false;
+  const int per16 = 16 / elem_bytes;
+  for (int i = 0; i < t.ndim - 1; ++i)
+    if (t.stride[i] % per16 != 0) return false;
+  return true;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct AttnPlan {
+  int kind;          // 0 = decode-gqa kernel
+  int num_splits;
+  int n_row_tiles;
+  size_t ws_o_bytes, ws_lse_bytes, ws_ctr_bytes;
+  size_t total() const {
+    return num_splits > 1 ? ws_o_bytes + ws_lse_bytes + ws_ctr_bytes : 0;
+  }
+};
+
+// Validates the attention arguments (everything but the outputs) and plans
+// the launch.  Returns a pkv_status.
+int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
+                   const pkv_tensor &v, const pkv_tensor &pt,
+                   const pkv_tensor &cs, int max_seqlen_q,
+                   const pkv_tensor &topk, int num_splits, AttnPlan *plan) {
+  if (!has(q, PKV_BF16, 3) || !has(k, PKV_BF16, 4) || !has(v, PKV_BF16, 4) ||
+      !has(pt, PKV_I32, 2) || !has(cs, PKV_I32, 1))
+    return PKV_ERR_INVALID_ARG;
+  const int64_t total_q = q.shape[0], h_q = q.shape[1], d = q.shape[2];
+  const int64_t num_pages = k.shape[0], page = k.shape[1], h_kv = k.shape[2];
+  const int64_t dv = v.shape[3];
+  const int64_t batch = cs.shape[0];
+  if (total_q < 0 || h_q < 1 || d < 1 || num_pages < 1 || page < 1 || h_kv < 1)
+    return PKV_ERR_INVALID_ARG;
+  if (k.shape[3] != d || v.shape[0] != num_pages || v.shape[1] != page ||
+      v.shape[2] != h_kv || h_q % h_kv != 0)
+    return PKV_ERR_INVALID_ARG;
+  if (pt.shape[0] != batch || pt.stride[1] != 1 || cs.stride[0] != 1)
+    return PKV_ERR_INVALID_ARG;
+  if (max_seqlen_q < 0 || num_splits < 0) return PKV_ERR_INVALID_ARG;
+  if (!vec_ok(q, 2) || !vec_ok(k, 2) || !vec_ok(v, 2)) return PKV_ERR_INVALID_ARG;
+  if (present(topk)) {
+    if (!has(topk, PKV_I32, 2) || topk.shape[0] != total_q || topk.stride[1] != 1)
+      return PKV_ERR_INVALID_ARG;
+  }
+  if (total_q > 0x7fffffffLL || batch > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+
+  const int group = static_cast<int>(h_q / h_kv);
+  if (!((d == 128 && dv == 128) || (d == 64 && dv == 64)))
+    return PKV_ERR_UNSUPPORTED;
+
+  plan->kind = 0;
+  if (present(topk)) {
+    plan->n_row_tiles = max_seqlen_q * ((group + kDecodeRowTile - 1) / kDecodeRowTile);
+  } else {
+    const int64_t rows = static_cast<int64_t>(max_seqlen_q) * group;
+    plan->n_row_tiles = static_cast<int>((rows + kDecodeRowTile - 1) / kDecodeRowTile);
+  }
+  int splits = num_splits;
+  if (splits == 0) {
+    // Enough CTAs for ~4 waves at two resident CTAs per SM, but never chunks
+    // shorter than 256 keys.
+    const int64_t base = std::max<int64_t>(1, batch * h_kv * plan->n_row_tiles);
+    const int64_t max_keys = present(topk) ? topk.shape[1] : pt.shape[1] * page;
+    const int64_t target = 4LL * kNumSMs * 2;
+    int64_t s = (target + base - 1) / base;
+    s = std::min<int64_t>(s, std::max<int64_t>(1, max_keys / 256));
+    splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s, 64)));
+  }
+  splits = std::min(splits, 1024);
+  plan->num_splits = splits;
+  const size_t rows_total = static_cast<size_t>(total_q) * h_q;
+  plan->ws_o_bytes = align256(static_cast<size_t>(splits) * rows_total * dv * 4);
+  plan->ws_lse_bytes = align256(static_cast<size_t>(splits) * rows_total * 4);
+  plan->ws_ctr_bytes =
+      align256(static_cast<size_t>(batch) * h_kv * plan->n_row_tiles * 4);
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int pkv_version(void) { return 1; }
+
+int pkv_get_error_flags(uint32_t *flags) {
+  if (flags == nullptr) return PKV_ERR_INVALID_ARG;
+  return cudaMemcpyFromSymbol(flags, g_error_word, sizeof(uint32_t)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+int pkv_clear_error_flags(void) {
+  const uint32_t zero = 0;
+  return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(uint32_t)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+int pkv_attn_workspace_size(pkv_tensor q, pkv_tensor k_cache,
+                            pkv_tensor v_cache, pkv_tensor page_table,
+                            pkv_tensor cache_seqlens, int max_seqlen_q,
+                            pkv_tensor topk_indices, int num_splits,
+                            size_t *bytes) {
+  if (bytes == nullptr) return PKV_ERR_INVALID_ARG;
+  AttnPlan plan;
+  const int rc = plan_attention(q, k_cache, v_cache, page_table, cache_seqlens,
+                                max_seqlen_q, topk_indices, num_splits, &plan);
+  if (rc != PKV_OK) return rc;
+  *bytes = plan.total();
+  return PKV_OK;
+}
+
+int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
+                          pkv_tensor page_table, pkv_tensor cache_seqlens,
+                          pkv_tensor cu_seqlens_q, int max_seqlen_q,
+                          float scale, int causal, int window_left,
+                          pkv_tensor topk_indices, int num_splits,
+                          pkv_tensor out, pkv_tensor lse, void *workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  AttnPlan plan;
+  int rc = plan_attention(q, k_cache, v_cache, page_table, cache_seqlens,
+                          max_seqlen_q, topk_indices, num_splits, &plan);
+  if (rc != PKV_OK) return rc;
+  const int64_t batch = cache_seqlens.shape[0];
+  if (!has(cu_seqlens_q, PKV_I32, 1) || cu_seqlens_q.shape[0] != batch + 1 ||
+      cu_seqlens_q.stride[0] != 1)
+    return PKV_ERR_INVALID_ARG;
+  if (!has(out, PKV_BF16, 3) || out.shape[0] != q.shape[0] ||
+      out.shape[1] != q.shape[1] || out.shape[2] != v_cache.shape[3] ||
+      !vec_ok(out, 2))
+    return PKV_ERR_INVALID_ARG;
+  if (present(lse) && (!has(lse, PKV_F32, 2) || lse.shape[0] != q.shape[0] ||
+                       lse.shape[1] != q.shape[1]))
+    return PKV_ERR_INVALID_ARG;
+  if (window_left < -1 || !isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (plan.total() > 0 && (workspace == nullptr || workspace_bytes < plan.total() ||
+                           (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return PKV_ERR_WORKSPACE;
+  uint32_t *err = device_error_word();
+  if (err == nullptr) return PKV_ERR_CUDA;
+
+  AttnParams p{};
+  p.q = static_cast<const bf16 *>(q.data);
+  p.q_st = q.stride[0];
+  p.q_sh = q.stride[1];
+  p.k = static_cast<const bf16 *>(k_cache.data);
+  p.k_sp = k_cache.stride[0];
+  p.k_spos = k_cache.stride[1];
+  p.k_sh = k_cache.stride[2];
+  p.v = static_cast<const bf16 *>(v_cache.data);
+  p.v_sp = v_cache.stride[0];
+  p.v_spos = v_cache.stride[1];
+  p.v_sh = v_cache.stride[2];
+  p.num_pages = k_cache.shape[0];
+  p.page_size = static_cast<int>(k_cache.shape[1]);
+  p.page_table = static_cast<const int32_t *>(page_table.data);
+  p.pt_stride = page_table.stride[0];
+  p.pt_cols = static_cast<int>(page_table.shape[1]);
+  p.cache_seqlens = static_cast<const int32_t *>(cache_seqlens.data);
+  p.cu_seqlens_q = static_cast<const int32_t *>(cu_seqlens_q.data);
+  p.batch = static_cast<int>(batch);
+  p.total_q = static_cast<int>(q.shape[0]);
+  p.h_q = static_cast<int>(q.shape[1]);
+  p.h_kv = static_cast<int>(k_cache.shape[2]);
+  p.group = p.h_q / p.h_kv;
+  p.d = static_cast<int>(q.shape[2]);
+  p.dv = static_cast<int>(v_cache.shape[3]);
+  p.max_seqlen_q = max_seqlen_q;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal ? 1 : 0;
+  p.window_left = window_left;
+  if (present(topk_indices)) {
+    p.topk = static_cast<const int32_t *>(topk_indices.data);
+    p.topk_stride = topk_indices.stride[0];
+    p.topk_len = static_cast<int>(topk_indices.shape[1]);
+  }
+  p.out = static_cast<bf16 *>(out.data);
+  p.o_st = out.stride[0];
+  p.o_sh = out.stride[1];
+  if (present(lse)) {
+    p.lse = static_cast<float *>(lse.data);
+    p.lse_st = lse.stride[0];
+    p.lse_sh = lse.stride[1];
+  }
+  p.num_splits = plan.num_splits;
+  p.n_row_tiles = plan.n_row_tiles;
+  p.err = err;
+  if (plan.num_splits > 1) {
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    p.ws_o = reinterpret_cast<float *>(ws);
+    p.ws_lse = reinterpret_cast<float *>(ws + plan.ws_o_bytes);
+    p.ws_counter = reinterpret_cast<int32_t *>(ws + plan.ws_o_bytes + plan.ws_lse_bytes);
+    if (cudaMemsetAsync(p.ws_counter, 0, plan.ws_ctr_bytes, stream) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
+  if (p.total_q == 0) return PKV_OK;
+  return launch_decode_gqa(p, stream);
+}
+
+int pkv_merge_state(pkv_tensor v_a, pkv_tensor lse_a, pkv_tensor v_b,
+                    pkv_tensor lse_b, pkv_tensor v_out, pkv_tensor lse_out,
+                    cudaStream_t stream) {
+  if (v_a.data == nullptr || v_b.data == nullptr || v_out.data == nullptr)
+    return PKV_ERR_INVALID_ARG;
+  if (v_a.ndim != 3 || v_b.ndim != 3 || v_out.ndim != 3) return PKV_ERR_INVALID_ARG;
+  if (v_a.dtype != v_b.dtype || (v_a.dtype != PKV_BF16 && v_a.dtype != PKV_F32) ||
+      (v_out.dtype != PKV_BF16 && v_out.dtype != PKV_F32))
+    return PKV_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; ++i)
+    if (v_b.shape[i] != v_a.shape[i] || v_out.shape[i] != v_a.shape[i])
+      return PKV_ERR_INVALID_ARG;
+  const int64_t n = v_a.shape[0], h = v_a.shape[1], d = v_a.shape[2];
+  if (!has(lse_a, PKV_F32, 2) || !has(lse_b, PKV_F32, 2) || lse_a.shape[0] != n ||
+      lse_a.shape[1] != h || lse_b.shape[0] != n || lse_b.shape[1] != h)
+    return PKV_ERR_INVALID_ARG;
+  if (present(lse_out) && (!has(lse_out, PKV_F32, 2) || lse_out.shape[0] != n ||
+                           lse_out.shape[1] != h))
+    return PKV_ERR_INVALID_ARG;
+  if (present(lse_out) && (lse_out.data == lse_a.data || lse_out.data == lse_b.data))
+    return PKV_ERR_INVALID_ARG;
+  const int eb_in = v_a.dtype == PKV_BF16 ? 2 : 4;
+  const int eb_out = v_out.dtype == PKV_BF16 ? 2 : 4;
+  if (d % 8 != 0 || !vec_ok(v_a, eb_in) || !vec_ok(v_b, eb_in) || !vec_ok(v_out, eb_out))
+    return PKV_ERR_UNSUPPORTED;
+  if (h > 0x7fffffffLL || d > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  return launch_merge_state(
+      v_a.data, v_b.data, v_out.data, v_a.dtype, v_out.dtype, n,
+      static_cast<int>(h), static_cast<int>(d), v_a.stride[0], v_a.stride[1],
+      v_b.stride[0], v_b.stride[1], v_out.stride[0], v_out.stride[1],
+      static_cast<const float *>(lse_a.data), lse_a.stride[0], lse_a.stride[1],
+      static_cast<const float *>(lse_b.data), lse_b.stride[0], lse_b.stride[1],
+      static_cast<float *>(lse_out.data), present(lse_out) ? lse_out.stride[0] : 0,
+      present(lse_out) ? lse_out.stride[1] : 0, stream);
+}
+
+int pkv_build_swa_page_table(pkv_tensor req_to_token,
+                             pkv_tensor req_pool_indices, pkv_tensor seq_lens,
+                             pkv_tensor prefill_lens, int window,
+                             pkv_tensor dst_page_table, pkv_tensor dst_kv_lens,
+                             cudaStream_t stream) {
+  if (!has(req_to_token, PKV_I32, 2) || req_to_token.stride[1] != 1)
+    return PKV_ERR_INVALID_ARG;
+  if (req_pool_indices.data == nullptr || req_pool_indices.ndim != 1 ||
+      (req_pool_indices.dtype != PKV_I32 && req_pool_indices.dtype != PKV_I64) ||
+      req_pool_indices.stride[0] != 1)
+    return PKV_ERR_INVALID_ARG;
+  const int64_t batch = req_pool_indices.shape[0];
+  if (!has(seq_lens, PKV_I32, 1) || seq_lens.shape[0] != batch || seq_lens.stride[0] != 1)
+    return PKV_ERR_INVALID_ARG;
+  if (!has(prefill_lens, PKV_I32, 1) || prefill_lens.shape[0] != req_to_token.shape[0] ||
+      prefill_lens.stride[0] != 1)
+    return PKV_ERR_INVALID_ARG;
+  if (!has(dst_page_table, PKV_I32, 2) || dst_page_table.shape[0] != batch ||
+      dst_page_table.stride[1] != 1)
+    return PKV_ERR_INVALID_ARG;
+  if (!has(dst_kv_lens, PKV_I32, 1) || dst_kv_lens.shape[0] != batch ||
+      dst_kv_lens.stride[0] != 1)
+    return PKV_ERR_INVALID_ARG;
+  if (window < 0) return PKV_ERR_INVALID_ARG;
+  if (batch > 0x7fffffffLL || dst_page_table.shape[1] > 0x7fffffffLL)
+    return PKV_ERR_UNSUPPORTED;
+  uint32_t *err = device_error_word();
+  if (err == nullptr) return PKV_ERR_CUDA;
+  return launch_swa_page_table(
+      static_cast<const int32_t *>(req_to_token.data), req_to_token.stride[0],
+      req_to_token.shape[0], req_to_token.shape[1], req_pool_indices.data,
+      req_pool_indices.dtype == PKV_I64, static_cast<const int32_t *>(seq_lens.data),
+      static_cast<const int32_t *>(prefill_lens.data), static_cast<int>(batch), window,
+      static_cast<int32_t *>(dst_page_table.data), dst_page_table.stride[0],
+      static_cast<int>(dst_page_table.shape[1]),
+      static_cast<int32_t *>(dst_kv_lens.data), err, stream);
+}
+
+int pkv_strided_page_table(pkv_tensor req_to_token,
+                           pkv_tensor req_pool_indices, int page_size,
+                           pkv_tensor out, cudaStream_t stream) {
+  if (!has(req_to_token, PKV_I32, 2) || req_to_token.stride[1] != 1)
+    return PKV_ERR_INVALID_ARG;
+  if (req_pool_indices.data == nullptr || req_pool_indices.ndim != 1 ||
+      (req_pool_indices.dtype != PKV_I32 && req_pool_indices.dtype != PKV_I64) ||
+      req_pool_indices.stride[0] != 1)
+    return PKV_ERR_INVALID_ARG;
+  const int64_t batch = req_pool_indices.shape[0];
+  if (!has(out, PKV_I32, 2) || out.shape[0] != batch || out.stride[1] != 1)
+    return PKV_ERR_INVALID_ARG;
+  if (page_size < 1) return PKV_ERR_INVALID_ARG;
+  if (batch > 65535 || out.shape[1] > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  uint32_t *err = device_error_word();
+  if (err == nullptr) return PKV_ERR_CUDA;
+  return launch_strided_page_table(
+      static_cast<const int32_t *>(req_to_token.data), req_to_token.stride[0],
+      req_to_token.shape[0], req_to_token.shape[1], req_pool_indices.data,
+      req_pool_indices.dtype == PKV_I64, static_cast<int>(batch), page_size,
+      static_cast<int32_t *>(out.data), out.stride[0],
+      static_cast<int>(out.shape[1]), err, stream);
+}
+
+int pkv_topk_to_slots(pkv_tensor topk, pkv_tensor cu_seqlens_q,
+                      pkv_tensor page_table, pkv_tensor cache_seqlens,
+                      int page_size, pkv_tensor out, cudaStream_t stream) {
+  if (!has(topk, PKV_I32, 2) || topk.stride[1] != 1) return PKV_ERR_INVALID_ARG;
+  if (!has(cache_seqlens, PKV_I32, 1) || cache_seqlens.stride[0] != 1)
+    return PKV_ERR_INVALID_ARG;
+  const int64_t batch = cache_seqlens.shape[0];
+  if (!has(cu_seqlens_q, PKV_I32, 1) || cu_seqlens_q.shape[0] != batch + 1 ||
+      cu_seqlens_q.stride[0] != 1)
+    return PKV_ERR_INVALID_ARG;
+  if (!has(page_table, PKV_I32, 2) || page_table.shape[0] != batch ||
+      page_table.stride[1] != 1)
+    return PKV_ERR_INVALID_ARG;
+  if (!has(out, PKV_I32, 2) || out.shape[0] != topk.shape[0] ||
+      out.shape[1] != topk.shape[1] || out.stride[1] != 1)
+    return PKV_ERR_INVALID_ARG;
+  if (page_size < 1) return PKV_ERR_INVALID_ARG;
+  if (topk.shape[0] > 0x7fffffffLL || topk.shape[1] > 0x7fffffffLL)
+    return PKV_ERR_UNSUPPORTED;
+  uint32_t *err = device_error_word();
+  if (err == nullptr) return PKV_ERR_CUDA;
+  return launch_topk_to_slots(
+      static_cast<const int32_t *>(topk.data), topk.stride[0],
+      static_cast<int>(topk.shape[0]), static_cast<int>(topk.shape[1]),
+      static_cast<const int32_t *>(cu_seqlens_q.data), static_cast<int>(batch),
+      static_cast<const int32_t *>(page_table.data), page_table.stride[0],
+      static_cast<int>(page_table.shape[1]),
+      static_cast<const int32_t *>(cache_seqlens.data), page_size,
+      static_cast<int32_t *>(out.data), out.stride[0], err, stream);
+}
+
+}  // extern "C"

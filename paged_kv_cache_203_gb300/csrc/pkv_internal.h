@@ -1,0 +1,93 @@
+// pkv_internal.h -- parameter blocks and launchers shared by libpkv's
+// translation units.  Nothing here is part of the public C ABI (include/pkv.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kNumSMs = 152;        // GB300: 2 dies x 76 SMs
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Everything a paged-attention kernel needs, with strides in elements.
+struct AttnParams {
+  const bf16 *q;
+  int64_t q_st, q_sh;                 // token, head strides
+  const bf16 *k;
+  int64_t k_sp, k_spos, k_sh;         // page, in-page position, head strides
+  const bf16 *v;
+  int64_t v_sp, v_spos, v_sh;
+  int64_t num_pages;
+  int page_size;
+  const int32_t *page_table;
+  int64_t pt_stride;
+  int pt_cols;
+  const int32_t *cache_seqlens;       // [batch]
+  const int32_t *cu_seqlens_q;        // [batch + 1]
+  int batch, total_q, h_q, h_kv, group, d, dv;
+  int max_seqlen_q;
+  float scale;                        // softmax scale
+  float scale_log2;                   // scale * log2(e)
+  int causal, window_left;
+  const int32_t *topk;                // optional [total_q, topk_len]
+  int64_t topk_stride;
+  int topk_len;
+  bf16 *out;
+  int64_t o_st, o_sh;
+  float *lse;                         // optional
+  int64_t lse_st, lse_sh;
+  // split-KV
+  int num_splits;
+  int n_row_tiles;                    // row tiles per (request, kv head)
+  float *ws_o;                        // [splits][total_q][h_q][dv] partial O
+  float *ws_lse;                      // [splits][total_q][h_q] partial lse
+  int32_t *ws_counter;                // [batch][h_kv][n_row_tiles]
+  uint32_t *err;                      // device error word
+};
+
+// Error word of the current device (static __device__ in pkv_abi.cu).
+uint32_t *device_error_word();
+
+// ---- launchers (return a pkv_status) ----
+// GQA decode / small-q paged attention on mma.sync tiles.
+int launch_decode_gqa(const AttnParams &p, cudaStream_t stream);
+// Rows per (request, kv head) tile used by the decode kernel.
+constexpr int kDecodeRowTile = 16;
+
+int launch_merge_state(const void *va, const void *vb, void *vo, int v_dtype,
+                       int o_dtype, int64_t n, int h, int d, int64_t va_sn,
+                       int64_t va_sh, int64_t vb_sn, int64_t vb_sh,
+                       int64_t vo_sn, int64_t vo_sh, const float *la,
+                       int64_t la_sn, int64_t la_sh, const float *lb,
+                       int64_t lb_sn, int64_t lb_sh, float *lo, int64_t lo_sn,
+                       int64_t lo_sh, cudaStream_t stream);
+
+int launch_swa_page_table(const int32_t *rtt, int64_t rtt_stride,
+                          int64_t rtt_rows, int64_t rtt_cols, const void *rpi,
+                          int rpi_is_64, const int32_t *seq_lens,
+                          const int32_t *prefill_lens, int batch, int window,
+                          int32_t *dst, int64_t dst_stride, int dst_cols,
+                          int32_t *kv_lens, uint32_t *err,
+                          cudaStream_t stream);
+
+int launch_strided_page_table(const int32_t *rtt, int64_t rtt_stride,
+                              int64_t rtt_rows, int64_t rtt_cols,
+                              const void *rpi, int rpi_is_64, int batch,
+                              int page_size, int32_t *out, int64_t out_stride,
+                              int n_cols, uint32_t *err, cudaStream_t stream);
+
+int launch_topk_to_slots(const int32_t *topk, int64_t topk_stride,
+                         int total_q, int topk_len, const int32_t *cu,
+                         int batch, const int32_t *pt, int64_t pt_stride,
+                         int pt_cols, const int32_t *cache_seqlens,
+                         int page_size, int32_t *out, int64_t out_stride,
+                         uint32_t *err, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,75 @@
+"""The C-ABI library builds, loads without a GPU and exports every entry point
+that include/pkv.h declares (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t)\s+(pkv_\w+)\s*\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import paged_kv_cache_203_gb300 as pkv
+    from paged_kv_cache_203_gb300 import _build
+
+    if _build.sources_newer_than_library():
+        _build.build_library()
+    return pkv.load_library()
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("pkv_attn_with_kvcache", "pkv_merge_state", "pkv_build_swa_page_table"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import paged_kv_cache_203_gb300 as pkv
+
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+    assert set(declared_symbols()) == set(pkv.EXPORTED_SYMBOLS)
+
+
+def test_version_without_gpu(lib):
+    assert lib.pkv_version() == 1
+
+
+def test_binding_rejects_bad_arguments_on_host(lib):
+    """Argument validation runs on the host: malformed descriptors are
+    refused with a status code before anything touches a device."""
+    import torch
+
+    import paged_kv_cache_203_gb300 as pkv
+
+    q = torch.zeros(2, 4, 128, dtype=torch.bfloat16)
+    k = torch.zeros(8, 16, 2, 128, dtype=torch.bfloat16)
+    pt = torch.zeros(2, 4, dtype=torch.int32)
+    cs = torch.zeros(2, dtype=torch.int32)
+    # H_q not a multiple of H_kv
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.attn_workspace_size(q[:, :3], k, k, pt, cs, 1)
+    assert e.value.code == -1
+    # unsupported head dim
+    q96 = torch.zeros(2, 4, 96, dtype=torch.bfloat16)
+    k96 = torch.zeros(8, 16, 2, 96, dtype=torch.bfloat16)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.attn_workspace_size(q96, k96, k96, pt, cs, 1)
+    assert e.value.code == -2
+    # wrong dtype of the page table
+    with pytest.raises(pkv.PkvError):
+        pkv.attn_workspace_size(q, k, k, pt.long(), cs, 1)
+    # workspace planning: no split -> no workspace; 4 splits -> partials
+    assert pkv.attn_workspace_size(q, k, k, pt, cs, 1, num_splits=1) == 0
+    ws = pkv.attn_workspace_size(q, k, k, pt, cs, 1, num_splits=4)
+    assert ws >= 4 * 2 * 4 * 128 * 4 + 4 * 2 * 4 * 4

@@ -1,0 +1,413 @@
+"""GPU-vs-oracle parity through the C ABI (libpkv) on seeded inputs.
+
+Bars: integer outputs (page tables, kv_lens, slots) bit-exact; bf16 attention
+outputs max |err| <= 2e-2 and mean |err| <= 2e-3 against the float64 oracle
+(fp32 accumulation on the GPU), lse within 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_203_gb300 as pkv
+from paged_kv_cache_203_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS, LSE_ABS = 2e-2, 2e-3, 1e-3
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _clean_flags():
+    pkv.clear_error_flags()
+    yield
+
+
+def check_close(out, lse, ref_o, ref_l, what=""):
+    o = out.float().cpu().numpy().reshape(ref_o.shape)
+    err = np.abs(o - ref_o)
+    assert np.isfinite(o).all(), what
+    assert err.max() <= MAX_ABS, f"{what}: max|err| {err.max():.3e}"
+    assert err.mean() <= MEAN_ABS, f"{what}: mean|err| {err.mean():.3e}"
+    if lse is not None:
+        l = lse.cpu().numpy().reshape(ref_l.shape)
+        fin = np.isfinite(ref_l)
+        assert np.array_equal(np.isfinite(l), fin), what
+        assert np.all(l[~fin] == ref_l[~fin]), what
+        if fin.any():
+            d = np.abs(l[fin] - ref_l[fin]).max()
+            assert d <= LSE_ABS, f"{what}: max|dlse| {d:.3e}"
+
+
+def oracle_attn(wl, **kw):
+    args = dict(causal=wl.causal, window_left=wl.window_left)
+    args.update(kw)
+    topk = args.pop("topk", wl.topk_indices)
+    pt = args.pop("page_table", wl.page_table)
+    cs = args.pop("cache_seqlens", wl.cache_seqlens)
+    d_v = wl.v_cache.shape[-1]
+    return oracle.attention(
+        oracle.bf16_bits(wl.q), oracle.bf16_bits(wl.k_cache),
+        oracle.bf16_bits(wl.v_cache), np.asarray(pt.cpu()), np.asarray(cs.cpu()),
+        wl.cu_seqlens_q.cpu().numpy(), wl.scale,
+        topk=None if topk is None else topk.cpu().numpy(), d_v=d_v, **args)
+
+
+def gpu_attn(g, **kw):
+    args = dict(causal=g.causal, window_left=g.window_left, num_splits=g.num_splits,
+                topk_indices=g.topk_indices)
+    args.update(kw)
+    pt = args.pop("page_table", g.page_table)
+    cs = args.pop("cache_seqlens", g.cache_seqlens)
+    out, lse = pkv.attn_with_kvcache(
+        g.q, g.k_cache, g.v_cache, pt, cs, g.cu_seqlens_q, g.max_seqlen_q,
+        g.scale, return_softmax_lse=True, **args)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+# ------------------------------------------------------------- page tables
+
+@pytest.mark.parametrize("page_size", [1, 16, 64])
+def test_strided_page_table_bit_exact(page_size):
+    wl = workloads.make("varlen_extend", page_size=page_size,
+                        pool_pages=(1 << 17) // page_size, h_q=1, h_kv=1, d=8)
+    n_cols = wl.page_table.shape[1]
+    ref = oracle.strided_page_table(wl.req_to_token.numpy(),
+                                    wl.req_pool_indices.numpy(), page_size, n_cols)
+    got = pkv.strided_page_table(wl.req_to_token.to(DEV), wl.req_pool_indices.to(DEV),
+                                 page_size, n_cols)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy(), ref)
+    assert np.array_equal(ref, wl.page_table.numpy())
+    assert pkv.get_error_flags() == 0
+
+
+def test_swa_page_table_full_workload_bit_exact():
+    """Sliding-window decode workload: batch 32, window 4096, prefill
+    U[256, 2048], seq U[pf+1, 32768] -- table and kv_lens bit-exact."""
+    wl = workloads.make("swa_decode", value_device="cpu", h_kv=1, d=8, h_q=1)
+    w = wl.window
+    pa_max = min(int(wl.prefill_lens.max()) + w, int(wl.seq_lens.max()))
+    ref, ref_kv, bad = oracle.swa_page_table(
+        wl.req_to_token.numpy(), wl.req_pool_indices.numpy(), wl.seq_lens.numpy(),
+        wl.prefill_lens.numpy(), w, pa_max, fill=-7)
+    assert bad == 0
+    for idx_dtype in (torch.int64, torch.int32):
+        dst = torch.full((len(wl.seq_lens), pa_max), -7, dtype=torch.int32, device=DEV)
+        kv = torch.zeros(len(wl.seq_lens), dtype=torch.int32, device=DEV)
+        pkv.build_swa_page_table(wl.req_to_token.to(DEV),
+                                 wl.req_pool_indices.to(idx_dtype).to(DEV),
+                                 wl.seq_lens.to(DEV), wl.prefill_lens.to(DEV), w, dst, kv)
+        torch.cuda.synchronize()
+        assert np.array_equal(kv.cpu().numpy(), ref_kv)
+        assert np.array_equal(dst.cpu().numpy(), ref)  # tail untouched too
+    assert pkv.get_error_flags() == 0
+
+
+def test_swa_page_table_edge_cases():
+    rng = np.random.default_rng(3)
+    pool, ctx = 7, 64
+    rtt = rng.permutation(pool * ctx).astype(np.int32).reshape(pool, ctx)
+    cases = [(3, 10, 4), (5, 7, 4), (0, 10, 4), (8, 9, 1), (10, 4, 3), (4, 20, 0),
+             (0, 0, 5), (6, 6, 6), (30, 64, 10)]
+    for pf, sl, w in cases:
+        pfl = np.zeros(pool, dtype=np.int32)
+        pfl[2] = pf
+        ref, ref_kv, _ = oracle.swa_page_table(rtt, [2], [sl], pfl, w, 48, fill=-3)
+        dst = torch.full((1, 48), -3, dtype=torch.int32, device=DEV)
+        kv = torch.zeros(1, dtype=torch.int32, device=DEV)
+        pkv.build_swa_page_table(torch.from_numpy(rtt).to(DEV),
+                                 torch.tensor([2], device=DEV),
+                                 torch.tensor([sl], dtype=torch.int32, device=DEV),
+                                 torch.from_numpy(pfl).to(DEV), w, dst, kv)
+        torch.cuda.synchronize()
+        assert kv.item() == ref_kv[0], (pf, sl, w)
+        assert np.array_equal(dst.cpu().numpy(), ref), (pf, sl, w)
+    # a row too long for dst: not written, kv_len -1, flag set, no trap
+    dst = torch.full((1, 8), -3, dtype=torch.int32, device=DEV)
+    kv = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pfl = np.zeros(pool, dtype=np.int32)
+    pkv.build_swa_page_table(torch.from_numpy(rtt).to(DEV), torch.tensor([0], device=DEV),
+                             torch.tensor([40], dtype=torch.int32, device=DEV),
+                             torch.from_numpy(pfl).to(DEV), 20, dst, kv)
+    torch.cuda.synchronize()
+    assert kv.item() == -1 and torch.all(dst == -3)
+    assert pkv.get_error_flags() & pkv.EFLAG_ROW_TOO_SHORT
+
+
+def test_topk_to_slots_bit_exact():
+    wl = workloads.make("mla_topk_decode", batch=16, d_qk=64, d_v=32, h_q=1,
+                        pool_pages=16 * 128 + 10)
+    topk = wl.topk_indices.clone()
+    topk[:, -5:] = -1
+    topk[3, 7] = 8192       # == kv_len: out of range
+    topk[5, 9] = -2         # below -1: out of range
+    row_req = np.arange(16)
+    ref, bad = oracle.topk_to_slots(topk.numpy(), row_req, wl.page_table.numpy(),
+                                    wl.page_size, wl.cache_seqlens.numpy())
+    assert bad == 2
+    got = pkv.topk_to_slots(topk.to(DEV), wl.cu_seqlens_q.to(DEV), wl.page_table.to(DEV),
+                            wl.cache_seqlens.to(DEV), wl.page_size)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy(), ref)
+    assert pkv.get_error_flags() & pkv.EFLAG_TOPK_OOB
+
+
+# ------------------------------------------------------------------ merge
+
+@pytest.mark.parametrize("in_dtype,out_dtype", [(torch.float32, torch.float32),
+                                                (torch.bfloat16, torch.bfloat16),
+                                                (torch.float32, torch.bfloat16)])
+def test_merge_state(in_dtype, out_dtype):
+    g = torch.Generator().manual_seed(5)
+    n, h, d = 257, 8, 128
+    va = torch.randn(n, h, d, generator=g).to(in_dtype)
+    vb = torch.randn(n, h, d, generator=g).to(in_dtype)
+    la = torch.randn(n, h, generator=g) * 4
+    lb = torch.randn(n, h, generator=g) * 4
+    la[0, :] = -float("inf")
+    la[1, :] = -float("inf")
+    lb[1, :] = -float("inf")
+    lb[2, :3] = la[2, :3]
+    ref_o, ref_l = oracle.merge_state(va.double().numpy(), la.double().numpy(),
+                                      vb.double().numpy(), lb.double().numpy())
+    vo = torch.empty(n, h, d, dtype=out_dtype, device=DEV)
+    o, l = pkv.merge_state(va.to(DEV), la.to(DEV), vb.to(DEV), lb.to(DEV), v_out=vo)
+    torch.cuda.synchronize()
+    tol = 1e-5 if out_dtype == torch.float32 else 2e-2
+    np.testing.assert_allclose(o.float().cpu().numpy(), ref_o, atol=tol, rtol=tol)
+    lg = l.cpu().numpy()
+    assert np.array_equal(np.isneginf(lg), np.isneginf(ref_l))
+    fin = np.isfinite(ref_l)
+    np.testing.assert_allclose(lg[fin], ref_l[fin], atol=1e-5)
+    # in place into v_a
+    va_d = va.to(DEV)
+    pkv.merge_state(va_d, la.to(DEV), vb.to(DEV), lb.to(DEV), v_out=va_d)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(va_d.float().cpu().numpy(), ref_o, atol=2e-2, rtol=2e-2)
+
+
+# -------------------------------------------------------------- attention
+
+@pytest.mark.parametrize("num_splits", [1, 2, 0])
+def test_tiny_decode_full_workload(num_splits):
+    """Tiny paged decode: batch 4, 8/2 heads, D 128, page 1, seqlens U[1,256]."""
+    wl = workloads.make("tiny_decode")
+    g = wl.to(DEV)
+    out, lse = gpu_attn(g, num_splits=num_splits)
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, f"splits={num_splits}")
+    assert pkv.get_error_flags() == 0
+
+
+@pytest.mark.parametrize("num_splits", [4, 1, 0, 7])
+def test_gqa_split_decode_reduced(num_splits):
+    """GQA split-KV decode recipe (32/8 heads, D 128, page 16) at a size the
+    oracle finishes quickly: 12 requests, lengths U[1, 3000]."""
+    wl = workloads.make("gqa_split_decode", batch=12, len_lo=1, len_hi=3000,
+                        pool_pages=4000)
+    g = wl.to(DEV)
+    out, lse = gpu_attn(g, num_splits=num_splits)
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, f"splits={num_splits}")
+
+
+def test_split_states_merged_by_merge_state_equal_single_call():
+    """Four explicit chunk calls (each chunk a request of its own page-table
+    slice) combined with pkv_merge_state equal one unsplit call and the
+    oracle: the split-KV route of the gqa split decode workload."""
+    wl = workloads.make("gqa_split_decode", batch=6, len_lo=100, len_hi=2000,
+                        pool_pages=2000)
+    g = wl.to(DEV)
+    P = wl.page_size
+    acc_o = acc_l = None
+    cs = wl.cache_seqlens.numpy()
+    for c in range(4):
+        pt_c = torch.zeros_like(wl.page_table)
+        len_c = torch.zeros_like(wl.cache_seqlens)
+        for b in range(len(cs)):
+            lo, hi = oracle.split_bounds(int(cs[b]), 4, P)
+            p0 = lo // P
+            pt_c[b, : pt_c.shape[1] - p0] = wl.page_table[b, p0:]
+            len_c[b] = hi - lo
+        o_c, l_c = gpu_attn(g, page_table=pt_c.to(DEV), cache_seqlens=len_c.to(DEV),
+                            num_splits=1)
+        if acc_o is None:
+            acc_o, acc_l = o_c.float(), l_c
+        else:
+            acc_o, acc_l = pkv.merge_state(acc_o, acc_l, o_c.float(), l_c)
+    torch.cuda.synchronize()
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(acc_o, acc_l, ref_o, ref_l, "chunked + merge_state")
+
+
+def test_swa_decode_reduced_prefill_aware():
+    """Sliding-window decode recipe (64/8 heads, page 1, window 4096) with the
+    table built on the GPU by the prefill-aware rule, then attended with no
+    window; compared with the oracle's table + attention."""
+    wl = workloads.make("swa_decode", batch=6, sl_hi=9000)
+    g = wl.to(DEV)
+    w = wl.window
+    pa_max = min(int(wl.prefill_lens.max()) + w, int(wl.seq_lens.max()))
+    dst = torch.zeros(6, pa_max, dtype=torch.int32, device=DEV)
+    kv = torch.zeros(6, dtype=torch.int32, device=DEV)
+    pkv.build_swa_page_table(g.req_to_token, g.req_pool_indices, g.seq_lens,
+                             g.prefill_lens, w, dst, kv)
+    ref_pt, ref_kv, _ = oracle.swa_page_table(
+        wl.req_to_token.numpy(), wl.req_pool_indices.numpy(), wl.seq_lens.numpy(),
+        wl.prefill_lens.numpy(), w, pa_max)
+    out, lse = gpu_attn(g, page_table=dst, cache_seqlens=kv, num_splits=0)
+    assert np.array_equal(kv.cpu().numpy(), ref_kv)
+    ref_o, ref_l, _ = oracle_attn(wl, page_table=torch.from_numpy(ref_pt),
+                                  cache_seqlens=torch.from_numpy(ref_kv))
+    check_close(out, lse, ref_o, ref_l, "pa-swa")
+
+
+def test_prefill_aware_with_no_prompt_equals_dense_window():
+    """With prefill_len 0 the prefill-aware table keeps the last `window`
+    tokens, i.e. dense attention with window_left = window - 1."""
+    wl = workloads.make("swa_decode", batch=4, sl_hi=6000, pf_lo=0, pf_hi=0,
+                        window=1000, h_q=16, h_kv=4)
+    g = wl.to(DEV)
+    dst = torch.zeros(4, 1000, dtype=torch.int32, device=DEV)
+    kv = torch.zeros(4, dtype=torch.int32, device=DEV)
+    pkv.build_swa_page_table(g.req_to_token, g.req_pool_indices, g.seq_lens,
+                             g.prefill_lens, 1000, dst, kv)
+    o1, l1 = gpu_attn(g, page_table=dst, cache_seqlens=kv)
+    pt = g.req_to_token[g.req_pool_indices.long()].contiguous()
+    o2, l2 = gpu_attn(g, page_table=pt, cache_seqlens=g.seq_lens, window_left=999)
+    assert torch.allclose(o1.float(), o2.float(), atol=1e-2)
+    assert torch.allclose(l1, l2, atol=1e-3)
+
+
+@pytest.mark.parametrize("d,page_size,h_q,h_kv,q_len,window,causal", [
+    (64, 16, 8, 8, 1, -1, False),      # MHA, D 64
+    (128, 3, 6, 2, 1, -1, False),      # page size not a power of two
+    (128, 64, 32, 2, 1, 100, False),   # group 16, window
+    (128, 16, 64, 2, 1, -1, False),    # group 32: two row tiles per token
+    (128, 16, 16, 4, 5, -1, True),     # short causal runs (MTP-style)
+    (128, 1, 8, 1, 3, 40, True),       # causal + window, group 8
+    (64, 8, 4, 2, 17, 7, True),        # rows across tiles, tiny window
+])
+def test_attention_variants(d, page_size, h_q, h_kv, q_len, window, causal):
+    wl = workloads.make("tiny_decode", d=d, page_size=page_size, h_q=h_q, h_kv=h_kv,
+                        q_len=q_len, window_left=window, causal=causal,
+                        len_lo=q_len, len_hi=700, pool_tokens=8 * 700 * 2 + 64,
+                        batch=5)
+    g = wl.to(DEV)
+    for splits in (1, 3):
+        out, lse = gpu_attn(g, num_splits=splits)
+        ref_o, ref_l, _ = oracle_attn(wl)
+        check_close(out, lse, ref_o, ref_l, f"splits={splits}")
+
+
+def test_gqa_topk_sparse_decode():
+    """Top-k lists (with -1 padding and duplicates) on a GQA cache."""
+    wl = workloads.make("tiny_decode", batch=6, h_q=16, h_kv=4, page_size=16,
+                        len_lo=300, len_hi=900, pool_tokens=6 * 912 + 64)
+    cs = wl.cache_seqlens.numpy()
+    g_ = torch.Generator().manual_seed(9)
+    topk = torch.full((6, 256), -1, dtype=torch.int32)
+    for b in range(6):
+        n = 200 + b * 8
+        topk[b, :n] = torch.randperm(int(cs[b]), generator=g_)[:n].to(torch.int32)
+    topk[0, 250] = topk[0, 3]  # a duplicate counts twice
+    wl.topk_indices = topk
+    g = wl.to(DEV)
+    for splits in (1, 2, 0):
+        out, lse = gpu_attn(g, num_splits=splits)
+        ref_o, ref_l, _ = oracle_attn(wl)
+        check_close(out, lse, ref_o, ref_l, f"topk splits={splits}")
+    assert pkv.get_error_flags() == 0
+
+
+def test_empty_rows_and_requests():
+    """kv_len 0 -> out 0, lse -inf; a request with no new tokens is skipped."""
+    wl = workloads.make("tiny_decode", batch=4, len_lo=5, len_hi=60)
+    wl.cache_seqlens[1] = 0
+    g = wl.to(DEV)
+    for splits in (1, 4):
+        out, lse = gpu_attn(g, num_splits=splits)
+        ref_o, ref_l, _ = oracle_attn(wl)
+        check_close(out, lse, ref_o, ref_l, f"empty splits={splits}")
+        assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+    # request 2 has no new token: cu = [0,1,2,2,3] over 3 tokens
+    wl3 = workloads.make("tiny_decode", batch=4, len_lo=5, len_hi=60)
+    wl3.cu_seqlens_q = torch.tensor([0, 1, 2, 2, 3], dtype=torch.int32)
+    wl3.q = wl3.q[:3].contiguous()
+    g3 = wl3.to(DEV)
+    out, lse = gpu_attn(g3, num_splits=2)
+    ref_o, ref_l, _ = oracle_attn(wl3)
+    check_close(out, lse, ref_o, ref_l, "zero-length request")
+
+
+def test_bad_page_ids_are_skipped_and_flagged():
+    """Out-of-pool page ids never trap: those keys are skipped (as the oracle
+    skips them) and PKV_EFLAG_PAGE_OOB is raised."""
+    wl = workloads.make("gqa_split_decode", batch=4, len_lo=100, len_hi=400,
+                        pool_pages=200, h_q=8, h_kv=2)
+    wl.page_table[1, 2] = 10_000_000
+    wl.page_table[2, 0] = -5
+    g = wl.to(DEV)
+    out, lse = gpu_attn(g, num_splits=2)
+    ref_o, ref_l, skipped = oracle_attn(wl)
+    assert skipped > 0
+    check_close(out, lse, ref_o, ref_l, "bad pages")
+    assert pkv.get_error_flags() & pkv.EFLAG_PAGE_OOB
+
+
+# ----------------------------------------------- full-size workloads, sampled
+
+def _sample_rows(total_q, h_q, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.integers(0, total_q, n), rng.integers(0, h_q, n)],
+                    axis=1).astype(np.int32)
+
+
+def test_gqa_split_decode_full_size_sampled():
+    """Full batched GQA split-KV decode workload (batch 64, 32/8 heads,
+    seqlens U[512, 8192], 40k-page pool) in the bench's launch configuration
+    (num_splits 4); 96 sampled (token, head) rows against the oracle."""
+    g = workloads.make("gqa_split_decode", value_device=DEV)
+    out, lse = gpu_attn(g, num_splits=4)
+    rows = _sample_rows(g.q.shape[0], g.q.shape[1], 96, 1)
+    ref_o, ref_l, _ = oracle.attention(
+        oracle.bf16_bits(g.q), oracle.bf16_bits(g.k_cache), oracle.bf16_bits(g.v_cache),
+        g.page_table.cpu().numpy(), g.cache_seqlens.cpu().numpy(),
+        g.cu_seqlens_q.cpu().numpy(), g.scale, rows=rows)
+    idx = torch.from_numpy(rows).long()
+    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
+                ref_o, ref_l, "full-size sampled")
+    assert pkv.get_error_flags() == 0
+
+
+def test_swa_decode_full_size_sampled():
+    """Full sliding-window decode workload (batch 32, 64/8 heads, window
+    4096, seq up to 32768) as the bench runs it: GPU-built table, then the
+    attention with the library's split choice; sampled rows."""
+    g = workloads.make("swa_decode", value_device=DEV)
+    w = g.window
+    pa_max = min(int(g.prefill_lens.max()) + w, int(g.seq_lens.max()))
+    dst = torch.zeros(32, pa_max, dtype=torch.int32, device=DEV)
+    kv = torch.zeros(32, dtype=torch.int32, device=DEV)
+    pkv.build_swa_page_table(g.req_to_token, g.req_pool_indices, g.seq_lens,
+                             g.prefill_lens, w, dst, kv)
+    out, lse = gpu_attn(g, page_table=dst, cache_seqlens=kv, num_splits=0)
+    rows = _sample_rows(32, 64, 64, 2)
+    ref_o, ref_l, _ = oracle.attention(
+        oracle.bf16_bits(g.q), oracle.bf16_bits(g.k_cache), oracle.bf16_bits(g.v_cache),
+        dst.cpu().numpy(), kv.cpu().numpy(), g.cu_seqlens_q.cpu().numpy(), g.scale,
+        rows=rows)
+    ref_pt, ref_kv, _ = oracle.swa_page_table(
+        g.req_to_token.cpu().numpy(), g.req_pool_indices.cpu().numpy(),
+        g.seq_lens.cpu().numpy(), g.prefill_lens.cpu().numpy(), w, pa_max)
+    assert np.array_equal(kv.cpu().numpy(), ref_kv)
+    kvn = ref_kv
+    d = dst.cpu().numpy()
+    for b in range(32):
+        assert np.array_equal(d[b, :kvn[b]], ref_pt[b, :kvn[b]])
+    idx = torch.from_numpy(rows).long()
+    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
+                ref_o, ref_l, "swa full-size sampled")
