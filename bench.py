@@ -1,0 +1,555 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV attention hot path on GB300.
+
+One *step* is one pass of the hot path over one batch of synthetic input held
+in HBM.  The headline workload is the batched GQA split-KV decode (batch 64,
+32 q heads / 8 KV heads, head_dim 128, page_size 16, cache_seqlens
+U[512, 8192], 40k-page pool): a step builds the page-level table from
+req_to_token (strided conversion), runs the split-KV paged attention with 4
+key chunks per (request, KV head), and combines the chunks with the
+log-sum-exp state merge (inside the attention launch).
+
+Metric: decode KV HBM GB/s = algorithmic K+V bytes of the step
+(sum_b kv_len_b * H_kv * (D + Dv) * 2 B) / step time.  ``--workload`` selects
+one of the other synthetic workloads (sliding-window decode with the
+prefill-aware table, varlen causal extend [TFLOP/s], MLA top-k sparse decode).
+
+Arms: ``--impl pkv`` (default) times libpkv; ``--impl reference`` times the
+float64 CPU oracle on the host cores on a bounded sample of the same workload
+(the pages publish no implementation or numbers to compare with).
+
+Under torchrun each rank runs its own replica of the workload (weak scaling,
+no collective on the data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import paged_kv_cache_203_gb300 as pkv  # noqa: E402
+from paged_kv_cache_203_gb300 import workloads  # noqa: E402
+
+HEADLINE = "gqa_split_decode"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# --------------------------------------------------------------------- peaks
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+            "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# -------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks / throttle reasons every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- workloads
+
+class Step:
+    """One pass of the hot path over a device-resident workload.
+
+    ``run()`` launches the step on the current stream; ``attn_events`` (when
+    given) brackets the dominant kernel (the attention launch) so its device
+    time can be accumulated.  ``algo`` holds the algorithmic bytes / flops of
+    one step."""
+
+    def __init__(self, name: str, device, overrides: dict):
+        self.name = name
+        self.dev = device
+        self.g = workloads.make(name, value_device=device, **overrides)
+        g = self.g
+        self.kernels_per_step = 0
+        self.ws = None
+        self.h2d_bytes = 0
+        self.d2h_bytes = 0
+        d, dv, h_kv = g.q.shape[-1], g.v_cache.shape[-1], g.k_cache.shape[2]
+        if g.topk_indices is None:
+            kv_tokens = int(g.cache_seqlens.sum())
+        else:
+            kv_tokens = int((g.topk_indices >= 0).sum())
+        self.out = torch.empty(g.q.shape[0], g.q.shape[1], dv, dtype=torch.bfloat16,
+                               device=device)
+        self.lse = torch.empty(g.q.shape[0], g.q.shape[1], dtype=torch.float32,
+                               device=device)
+        if (g.kind == "swa"):
+            self.pa_max = min(int(g.prefill_lens.max()) + g.window, int(g.seq_lens.max()))
+            self.pt = torch.zeros(g.seq_lens.shape[0], self.pa_max, dtype=torch.int32,
+                                  device=device)
+            self.kv = torch.zeros(g.seq_lens.shape[0], dtype=torch.int32, device=device)
+            # algorithmic KV rows: the prefill-aware lengths
+            pf = g.prefill_lens[g.req_pool_indices.long()].cpu()
+            sl = g.seq_lens.cpu()
+            kv_tokens = int(torch.minimum(sl, pf + g.window).sum())
+        else:
+            self.n_cols = g.page_table.shape[1]
+            self.pt = torch.zeros_like(g.page_table)
+        self.kv_bytes = kv_tokens * h_kv * (d + dv) * 2 if g.topk_indices is None else \
+            kv_tokens * d * 2  # absorbed MLA: one 576-wide row per gathered key
+        self.flops = self._flops()
+        self.workspace_bytes = pkv.attn_workspace_size(
+            g.q, g.k_cache, g.v_cache, self.pt if not (g.kind == "swa") else self.pt,
+            g.cache_seqlens if not (g.kind == "swa") else self.kv, g.max_seqlen_q,
+            g.topk_indices, g.num_splits)
+        if self.workspace_bytes:
+            self.ws = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=device)
+
+    def _flops(self):
+        g = self.g
+        d, dv, h_q = g.q.shape[-1], g.v_cache.shape[-1], g.q.shape[1]
+        cs = g.cache_seqlens.cpu().numpy().astype(np.int64)
+        cu = g.cu_seqlens_q.cpu().numpy().astype(np.int64)
+        if g.topk_indices is not None:
+            pairs = int((g.topk_indices >= 0).sum())
+        elif (g.kind == "swa"):
+            pf = g.prefill_lens[g.req_pool_indices.long()].cpu().numpy()
+            pairs = int(np.minimum(g.seq_lens.cpu().numpy(), pf + g.window).sum())
+        else:
+            pairs = 0
+            for b in range(len(cs)):
+                ql = cu[b + 1] - cu[b]
+                kv = cs[b]
+                if g.causal:
+                    pairs += ql * (kv - ql) + ql * (ql + 1) // 2
+                else:
+                    pairs += ql * kv
+        return 2 * pairs * h_q * (d + dv)
+
+    def per_request_work(self):
+        """Algorithmic work of each request (keys x rows), for sampling."""
+        g = self.g
+        if g.topk_indices is not None:
+            return (g.topk_indices.cpu() >= 0).sum(1).numpy().astype(np.float64)
+        cs = g.cache_seqlens.cpu().numpy().astype(np.float64)
+        if g.kind == "swa":
+            pf = g.prefill_lens[g.req_pool_indices.long()].cpu().numpy()
+            return np.minimum(g.seq_lens.cpu().numpy(), pf + g.window).astype(np.float64)
+        ql = np.diff(g.cu_seqlens_q.cpu().numpy()).astype(np.float64)
+        if g.causal:
+            return ql * (cs - ql) + ql * (ql + 1) / 2
+        return ql * cs
+
+    def run(self, ev=None):
+        g = self.g
+        if (g.kind == "swa"):
+            pkv.build_swa_page_table(g.req_to_token, g.req_pool_indices, g.seq_lens,
+                                     g.prefill_lens, g.window, self.pt, self.kv)
+            pt, cs = self.pt, self.kv
+        else:
+            pkv.strided_page_table(g.req_to_token, g.req_pool_indices, g.page_size,
+                                   self.n_cols, out=self.pt)
+            pt, cs = self.pt, g.cache_seqlens
+        if ev is not None:
+            ev[0].record()
+        pkv.attn_with_kvcache(g.q, g.k_cache, g.v_cache, pt, cs, g.cu_seqlens_q,
+                              g.max_seqlen_q, g.scale, causal=g.causal,
+                              window_left=g.window_left, topk_indices=g.topk_indices,
+                              num_splits=g.num_splits, out=self.out, lse=self.lse,
+                              workspace=self.ws)
+        if ev is not None:
+            ev[1].record()
+
+    KERNELS_PER_STEP = 2  # table builder + attention
+
+
+def parse_overrides(s: str | None) -> dict:
+    out = {}
+    if not s:
+        return out
+    for kv in s.split(","):
+        k, v = kv.split("=")
+        out[k] = int(v)
+    return out
+
+
+# ------------------------------------------------------------- end to end
+
+def run_e2e(step: Step, steps: int):
+    """Same metric through the public API with the step's inputs in pinned
+    host memory: per step, copy q / req_to_token / indices / lengths host ->
+    device, run the step, copy out and lse back.  The KV cache stays
+    resident in HBM (it is the cache)."""
+    g = step.g
+    names = ["q", "req_to_token", "req_pool_indices", "cache_seqlens", "cu_seqlens_q"]
+    if (g.kind == "swa"):
+        names += ["seq_lens", "prefill_lens"]
+    if g.topk_indices is not None:
+        names += ["topk_indices"]
+    host = {n: getattr(g, n).cpu().pin_memory() for n in names}
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    lse_h = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    dev_t = {n: getattr(g, n) for n in names}
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        for n in names:
+            dev_t[n].copy_(host[n], non_blocking=True)
+        step.run()
+        out_h.copy_(step.out, non_blocking=True)
+        lse_h.copy_(step.lse, non_blocking=True)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    return ms, h2d, d2h
+
+
+# ------------------------------------------------------------ cpu baseline
+
+class OracleSample:
+    """The oracle as it stands, on the host cores, over a bounded sample of
+    the same workload: its own strided / prefill-aware table, then attention
+    (and, for split workloads, chunk states combined by its merge) for the
+    first ``nreq`` requests.  ``frac`` is the share of the step's algorithmic
+    work the sample covers."""
+
+    def __init__(self, step: Step, pass_budget_s: float):
+        import oracle
+
+        self.oracle = oracle
+        g = step.g
+        self.step = step
+        self.q = oracle.bf16_bits(g.q)
+        self.k = oracle.bf16_bits(g.k_cache)
+        self.v = (self.k[..., : g.v_cache.shape[-1]] if g.topk_indices is not None
+                  else oracle.bf16_bits(g.v_cache))
+        self.rtt = g.req_to_token.cpu().numpy()
+        self.rpi = g.req_pool_indices.cpu().numpy()
+        self.cu = g.cu_seqlens_q.cpu().numpy()
+        self.cs = g.cache_seqlens.cpu().numpy()
+        self.topk = None if g.topk_indices is None else g.topk_indices.cpu().numpy()
+        self.threads = os.cpu_count() or 1
+        batch = len(self.cs)
+        t = time.perf_counter()
+        self.run(1)
+        per_req = max(time.perf_counter() - t, 1e-4)
+        self.nreq = batch if per_req * batch <= pass_budget_s else \
+            max(1, int(pass_budget_s / per_req))
+        work = step.per_request_work()
+        self.frac = float(work[: self.nreq].sum() / max(1e-30, work.sum()))
+        self.batch = batch
+
+    def run(self, nreq=None):
+        o, g, st = self.oracle, self.step.g, self.step
+        nreq = self.nreq if nreq is None else nreq
+        cu_s = self.cu[: nreq + 1]
+        q = self.q[: cu_s[-1]]
+        if g.kind == "swa":
+            pt, kv, _ = o.swa_page_table(self.rtt, self.rpi[:nreq],
+                                         g.seq_lens.cpu().numpy()[:nreq],
+                                         g.prefill_lens.cpu().numpy(), g.window, st.pa_max)
+            o.attention(q, self.k, self.v, pt, kv, cu_s, g.scale, num_threads=self.threads)
+            return
+        pt = o.strided_page_table(self.rtt, self.rpi[:nreq], g.page_size, st.n_cols)
+        if g.num_splits > 1:
+            o.split_attention(q, self.k, self.v, pt, self.cs[:nreq], cu_s, g.scale,
+                              g.num_splits, num_threads=self.threads)
+        else:
+            o.attention(q, self.k, self.v, pt, self.cs[:nreq], cu_s, g.scale,
+                        causal=g.causal, window_left=g.window_left,
+                        topk=None if self.topk is None else self.topk[: cu_s[-1]],
+                        d_v=g.v_cache.shape[-1], num_threads=self.threads)
+
+    def describe(self, passes):
+        if self.nreq == self.batch:
+            return f"{passes} pass(es) over the full step ({self.batch} requests)"
+        return (f"{passes} pass(es) over the first {self.nreq} of {self.batch} "
+                f"requests ({self.frac:.1%} of the step's work)")
+
+
+def oracle_step_time(step: Step, budget_s: float = 10.0):
+    """Seconds per full step for the oracle, from whole passes over a sample
+    repeated until ``budget_s`` has elapsed."""
+    smp = OracleSample(step, budget_s)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        smp.run()
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return el / done / smp.frac, smp.threads, smp.describe(done)
+
+
+# --------------------------------------------------------------------- main
+
+def metric_of(step: Step):
+    if step.name == "varlen_extend":
+        return "extend TFLOP/s", "TFLOP/s", step.flops / 1e12
+    return "decode KV HBM GB/s", "GB/s", step.kv_bytes / 1e9
+
+
+def run_reference(args, rank, world):
+    """The oracle on the host cores: W warm-up and K timed passes, each pass a
+    bounded sample of the workload sized so the whole run stays within about
+    two minutes."""
+    if rank != 0:
+        return
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    step = Step(args.workload, dev, parse_overrides(args.override))
+    metric, unit, per_step = metric_of(step)
+    pass_budget = min(args.ref_budget, 120.0 / (args.steps + args.warmup))
+    smp = OracleSample(step, pass_budget)
+    for _ in range(args.warmup):
+        smp.run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        smp.run()
+    s_per_pass = (time.perf_counter() - t0) / args.steps
+    val = per_step * smp.frac / s_per_pass
+    line = {
+        "impl": "reference", "metric": metric, "value": val, "unit": unit,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": s_per_pass * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, **parse_overrides(args.override)},
+        "cpu_baseline": {"value": val, "unit": unit, "cores": smp.threads,
+                         "kind": "oracle", "sample": smp.describe(args.steps)},
+        "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=list(workloads.CONFIGS))
+    ap.add_argument("--override", default=None,
+                    help="comma list key=int shrinking the workload (profiling)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the per-workload summary of the other workloads")
+    ap.add_argument("--ref-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "pkv" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkv.load_library()
+    peaks = measured_peaks()
+    step = Step(args.workload, dev, parse_overrides(args.override))
+    metric, unit, per_step = metric_of(step)
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    pkv.clear_error_flags()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(args.steps):
+        step.run(evs[i])
+    t1.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    attn_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    flags = pkv.get_error_flags()
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public API with host buffers
+    e2e_ms, h2d, d2h = run_e2e(step, max(3, args.steps // 4))
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    value = per_step * world / (ms / 1e3)
+    e2e_val = per_step * world / (e2e_ms / 1e3)
+    if unit == "GB/s":
+        achieved = step.kv_bytes / 1e9 / (attn_ms / 1e3)
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "kernel": "decode_gqa_kernel (attention launch)",
+                "peak_source": peaks["source"]}
+    else:
+        achieved = step.flops / 1e12 / (attn_ms / 1e3)
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": None, "kernel": "attention launch",
+                "peak_source": peaks["source"]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s_per_step, threads, sample = oracle_step_time(step, 10.0)
+        cpu = {"value": per_step / s_per_step, "unit": unit, "cores": threads,
+               "kind": "oracle", "sample": sample}
+
+    n_tokens = int(step.g.q.shape[0])
+    others = {}
+    if rank == 0 and not args.no_others and args.workload == HEADLINE and not args.override:
+        del step.g
+        torch.cuda.empty_cache()
+        for name in workloads.CONFIGS:
+            if name == HEADLINE:
+                continue
+            try:
+                s2 = Step(name, dev, {})
+                for _ in range(3):
+                    s2.run()
+                torch.cuda.synchronize()
+                e2 = [(torch.cuda.Event(enable_timing=True),
+                       torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record()
+                for i in range(20):
+                    s2.run(e2[i])
+                b.record()
+                torch.cuda.synchronize()
+                sms = a.elapsed_time(b) / 20
+                kms = sum(x.elapsed_time(y) for x, y in e2) / 20
+                others[name] = {
+                    "ms_per_step": sms, "attn_ms": kms,
+                    "kv_GBps": s2.kv_bytes / 1e9 / (kms / 1e3),
+                    "kv_frac_hbm": s2.kv_bytes / 1e9 / (kms / 1e3) / peaks["hbm_gbs"],
+                    "TFLOPs": s2.flops / 1e12 / (kms / 1e3),
+                    "tflop_frac_bf16": s2.flops / 1e12 / (kms / 1e3) / peaks["bf16_tflops"],
+                    "tokens_per_s": s2.g.q.shape[0] / (sms / 1e3)}
+                del s2
+                torch.cuda.empty_cache()
+            except pkv.PkvError as e:
+                others[name] = {"unavailable": str(e)}
+
+    if rank == 0:
+        g_cfg = {"workload": args.workload}
+        g_cfg.update(workloads.CONFIGS[args.workload])
+        g_cfg.pop("kind", None)
+        g_cfg.pop("seed", None)
+        g_cfg.update(parse_overrides(args.override))
+        g_cfg["algorithmic_kv_bytes_per_step"] = step.kv_bytes
+        g_cfg["l2"] = ("inputs larger than L2: %.2f GB of K/V per step vs 129 MB L2"
+                       % (step.kv_bytes / 1e9)) if step.kv_bytes > L2_BYTES else \
+            "inputs smaller than L2 (no flush)"
+        line = {
+            "metric": metric, "value": value, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": g_cfg,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": Step.KERNELS_PER_STEP * args.steps,
+            "clocks": clk,
+            "tokens_per_s": n_tokens * world / (ms / 1e3),
+            "error_flags": flags,
+        }
+        if others:
+            line["other_workloads"] = others
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -68,6 +68,7 @@ class PagedBatch:
     """One batch of paged-attention inputs (see module docstring)."""
 
     name: str
+    kind: str
     q: torch.Tensor
     k_cache: torch.Tensor
     v_cache: torch.Tensor
@@ -173,7 +174,7 @@ def make(name: str, value_device="cpu", seed: Optional[int] = None,
         vc = _normal_bf16((num_pages, p, cfg["h_kv"], cfg["d"]), value_device, seed + 2)
         q = _normal_bf16((b * q_len, cfg["h_q"], cfg["d"]), value_device, seed + 3)
         batch = PagedBatch(
-            name=name, q=q, k_cache=kc, v_cache=vc, req_to_token=rtt,
+            name=name, kind=kind, q=q, k_cache=kc, v_cache=vc, req_to_token=rtt,
             req_pool_indices=rpi, page_table=pt, cache_seqlens=kv.to(torch.int32),
             cu_seqlens_q=cu, max_seqlen_q=q_len, scale=1.0 / math.sqrt(cfg["d"]),
             causal=bool(cfg.get("causal", q_len > 1)),
@@ -192,7 +193,7 @@ def make(name: str, value_device="cpu", seed: Optional[int] = None,
         vc = _normal_bf16((num_slots, 1, cfg["h_kv"], cfg["d"]), value_device, seed + 2)
         q = _normal_bf16((b, cfg["h_q"], cfg["d"]), value_device, seed + 3)
         batch = PagedBatch(
-            name=name, q=q, k_cache=kc, v_cache=vc, req_to_token=rtt,
+            name=name, kind=kind, q=q, k_cache=kc, v_cache=vc, req_to_token=rtt,
             req_pool_indices=rpi, page_table=pt, cache_seqlens=sl.to(torch.int32),
             cu_seqlens_q=torch.arange(b + 1, dtype=torch.int32), max_seqlen_q=1,
             scale=1.0 / math.sqrt(cfg["d"]), causal=False, window_left=-1,
@@ -211,7 +212,7 @@ def make(name: str, value_device="cpu", seed: Optional[int] = None,
         vc = _normal_bf16((cfg["pool_pages"], p, cfg["h_kv"], cfg["d"]), value_device, seed + 2)
         q = _normal_bf16((int(new.sum()), cfg["h_q"], cfg["d"]), value_device, seed + 3)
         batch = PagedBatch(
-            name=name, q=q, k_cache=kc, v_cache=vc, req_to_token=rtt,
+            name=name, kind=kind, q=q, k_cache=kc, v_cache=vc, req_to_token=rtt,
             req_pool_indices=rpi, page_table=pt, cache_seqlens=kv.to(torch.int32),
             cu_seqlens_q=cu, max_seqlen_q=int(new.max()),
             scale=1.0 / math.sqrt(cfg["d"]), causal=True,
@@ -228,7 +229,7 @@ def make(name: str, value_device="cpu", seed: Optional[int] = None,
         kc = _normal_bf16((cfg["pool_pages"], p, 1, cfg["d_qk"]), value_device, seed + 1)
         q = _normal_bf16((b, cfg["h_q"], cfg["d_qk"]), value_device, seed + 3)
         batch = PagedBatch(
-            name=name, q=q, k_cache=kc, v_cache=kc[..., : cfg["d_v"]],
+            name=name, kind=kind, q=q, k_cache=kc, v_cache=kc[..., : cfg["d_v"]],
             req_to_token=rtt, req_pool_indices=rpi, page_table=pt,
             cache_seqlens=kv.to(torch.int32),
             cu_seqlens_q=torch.arange(b + 1, dtype=torch.int32), max_seqlen_q=1,

@@ -228,7 +228,7 @@ def test_split_states_merged_by_merge_state_equal_single_call():
         pt_c = torch.zeros_like(wl.page_table)
         len_c = torch.zeros_like(wl.cache_seqlens)
         for b in range(len(cs)):
-            lo, hi = oracle.split_bounds(int(cs[b]), 4, P)
+            lo, hi = oracle.split_bounds(int(cs[b]), 4, P)[c]
             p0 = lo // P
             pt_c[b, : pt_c.shape[1] - p0] = wl.page_table[b, p0:]
             len_c[b] = hi - lo
