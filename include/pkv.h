@@ -135,6 +135,47 @@ int pkv_attn_workspace_size(pkv_tensor q, pkv_tensor k_cache,
                             pkv_tensor topk_indices, int num_splits,
                             size_t *bytes);
 
+/* Size of the library-owned scratch array used by
+ * pkv_attn_with_kvcache_noalloc (32 MiB per device that loads the library,
+ * held until the process exits). */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * pkv_attn_with_kvcache_noalloc -- pkv_attn_with_kvcache without workspace.
+ *
+ * The source pages have no counterpart to this entry point; it exists for
+ * callers that cannot allocate device memory on this path.  Such callers
+ * are handed only their input and output buffers (a plugin interface with
+ * no workspace hook), or run under a memory plan that forbids allocating
+ * after start-up, or must not call cudaMalloc / cudaFree here because those
+ * calls can synchronise the device or fail while another allocator holds
+ * the memory.
+ *
+ * Same arguments, computation, outputs and status codes as
+ * pkv_attn_with_kvcache, minus the workspace.  The caller still passes all
+ * inputs and outputs.  The split-KV scratch is a fixed array inside the
+ * library (PKV_NOALLOC_SCRATCH_BYTES per device); this entry point never
+ * allocates or frees device memory.
+ * - If the call would need more scratch than PKV_NOALLOC_SCRATCH_BYTES
+ *   (pkv_attn_workspace_size for the same arguments), it returns
+ *   PKV_ERR_WORKSPACE and launches nothing; ask for fewer splits
+ *   (num_splits = 1 needs no scratch).
+ * - The first call on a device, with that device current, looks up the
+ *   array's device address (cudaGetSymbolAddress) and caches it; make that
+ *   first call before any stream capture.
+ * - All calls on a device share the array and it keeps the last call's
+ *   contents; what must start at zero is cleared by every call.  Calls whose
+ *   work overlaps on the GPU (e.g. on two unordered streams) race on it.
+ */
+int pkv_attn_with_kvcache_noalloc(pkv_tensor q, pkv_tensor k_cache,
+                                  pkv_tensor v_cache, pkv_tensor page_table,
+                                  pkv_tensor cache_seqlens,
+                                  pkv_tensor cu_seqlens_q, int max_seqlen_q,
+                                  float scale, int causal, int window_left,
+                                  pkv_tensor topk_indices, int num_splits,
+                                  pkv_tensor out, pkv_tensor lse,
+                                  cudaStream_t stream);
+
 /*
  * pkv_merge_state -- log-sum-exp merge of two attention states.
  *

@@ -32,6 +32,8 @@ from ._build import build_library, lib_path
 __all__ = [
     "attn_with_kvcache",
     "attn_workspace_size",
+    "attn_with_kvcache_noalloc",
+    "NOALLOC_SCRATCH_BYTES",
     "merge_state",
     "build_swa_page_table",
     "strided_page_table",
@@ -64,6 +66,7 @@ EXPORTED_SYMBOLS = (
     "pkv_get_error_flags",
     "pkv_clear_error_flags",
     "pkv_version",
+    "pkv_attn_with_kvcache_noalloc",
 )
 
 _DTYPES = {torch.bfloat16: _BF16, torch.float32: _F32, torch.int32: _I32,
@@ -108,6 +111,9 @@ def load_library(path: str | None = None):
                                           c_void_p]
     lib.pkv_attn_workspace_size.argtypes = [T, T, T, T, T, c_int, T, c_int,
                                             ctypes.POINTER(c_size_t)]
+    lib.pkv_attn_with_kvcache_noalloc.argtypes = [T, T, T, T, T, T, c_int, c_float,
+                                                  c_int, c_int, T, c_int, T, T,
+                                                  c_void_p]
     lib.pkv_merge_state.argtypes = [T, T, T, T, T, T, c_void_p]
     lib.pkv_build_swa_page_table.argtypes = [T, T, T, T, c_int, T, T, c_void_p]
     lib.pkv_strided_page_table.argtypes = [T, T, c_int, T, c_void_p]
@@ -186,6 +192,29 @@ def attn_with_kvcache(q, k_cache, v_cache, page_table, cache_seqlens,
         _desc(topk_indices), int(num_splits), _desc(out), _desc(lse), ws_ptr,
         ws_bytes, _stream(q)))
     return (out, lse) if return_softmax_lse else out
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # PKV_NOALLOC_SCRATCH_BYTES
+
+
+def attn_with_kvcache_noalloc(q, k_cache, v_cache, page_table, cache_seqlens,
+                              cu_seqlens_q, max_seqlen_q: int,
+                              softmax_scale: float, out, lse=None,
+                              causal: bool = False, window_left: int = -1,
+                              topk_indices=None, num_splits: int = 0):
+    """pkv_attn_with_kvcache_noalloc: the same attention for callers that
+    cannot allocate device memory.  The caller passes every buffer,
+    including ``out`` (and ``lse`` if wanted); the split scratch is the
+    library's own fixed per-device array, so this call allocates nothing.
+    Calls that would need more than NOALLOC_SCRATCH_BYTES of scratch raise
+    PkvError (PKV_ERR_WORKSPACE); calls that overlap on the GPU race on the
+    shared array."""
+    _check("pkv_attn_with_kvcache_noalloc", load_library().pkv_attn_with_kvcache_noalloc(
+        _desc(q), _desc(k_cache), _desc(v_cache), _desc(page_table),
+        _desc(cache_seqlens), _desc(cu_seqlens_q), int(max_seqlen_q),
+        float(softmax_scale), int(bool(causal)), int(window_left),
+        _desc(topk_indices), int(num_splits), _desc(out), _desc(lse), _stream(q)))
+    return out
 
 
 def merge_state(v_a, lse_a, v_b, lse_b, v_out=None, lse_out=None):

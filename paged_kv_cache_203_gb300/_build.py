@@ -20,6 +20,7 @@ SOURCES = [
     "pkv_pagetable.cu",
     "pkv_merge.cu",
     "pkv_decode.cu",
+    "pkv_noalloc.cu",
 ]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
