@@ -58,7 +58,8 @@ enum pkv_error_bits {
   PKV_EFLAG_PAGE_OOB = 1,    /* page id outside [0, num_pages): key skipped */
   PKV_EFLAG_TOPK_OOB = 2,    /* top-k index < -1 or >= kv_len: entry skipped */
   PKV_EFLAG_ROW_TOO_SHORT = 4, /* page-table / dst row narrower than needed */
-  PKV_EFLAG_SRC_OOB = 8      /* req_to_token column or pool row out of range */
+  PKV_EFLAG_SRC_OOB = 8,     /* req_to_token column or pool row out of range */
+  PKV_EFLAG_TIMEOUT = 16     /* a bounded in-kernel wait expired (work dropped) */
 };
 
 typedef struct pkv_tensor {

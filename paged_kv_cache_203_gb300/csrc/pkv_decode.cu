@@ -7,32 +7,83 @@
 // (dual_chunk_flashattention_backend.py, `_merge_attn_outputs`).
 //
 // Design (HBM-bound: every K/V byte is read once per KV head):
-//  * One CTA = 4 warps = one tile of 16 query rows.  The rows are the
-//    (new token, q head) pairs that share one KV head, so all GQA heads of a
-//    KV head are served by a single read of its K/V rows.
-//  * Keys stream through a NSTAGE-deep cp.async pipeline of 64-key stages.
-//    Each key row (D * 2 bytes, contiguous) is gathered through the page
-//    table with 16-byte cp.async into XOR-swizzled shared memory (16-byte
-//    chunk index ^= row & 7), so ldmatrix reads are bank-conflict free.
-//  * Warp w owns keys [16w, 16w + 16) of every stage: S = Q K^T and O += P V
-//    on bf16 mma.sync m16n8k16 tensor-core tiles with fp32 accumulation and a
-//    per-warp online softmax in the log2 domain.  The four warps' states are
-//    merged through shared memory at the end.
+//  * One CTA = 4 consumer warps + producer warp(s), one tile of 16 query rows.
+//    The rows are the (new token, q head) pairs that share one KV head, so all
+//    GQA heads of a KV head are served by a single read of its K/V rows.
+//  * Keys stream through an NSTAGE-deep shared-memory ring of 64-key stages,
+//    handed over with mbarriers (full: data landed, empty: consumers done).
+//    Two loaders fill the same layout:
+//      - TMA (page size a multiple of 8): one producer lane per page issues
+//        one 4-D tensor-map box per 64-column half of K and of V
+//        ([D, H_kv, P, pages] map, 128-byte swizzle), completion counted in
+//        bytes on the stage's full barrier;
+//      - cp.async (any page size, top-k lists): two producer warps gather
+//        16-byte chunks through the page table, each thread's completion
+//        tracked by the full barrier (cp.async.mbarrier.arrive).
+//    Layout of a [rows][D] bf16 tile: [D/64 halves][rows][128 B], 16-byte
+//    chunk c of row r at chunk (c ^ (r & 7)) -- the TMA 128-byte swizzle --
+//    so the ldmatrix reads of the consumers are bank-conflict free.
+//  * Consumer warp w owns keys [16w, 16w + 16) of every stage: S = Q K^T and
+//    O += P V on bf16 mma.sync m16n8k16 tiles with fp32 accumulation and an
+//    online softmax in the log2 domain; the four warps' states are merged in
+//    shared memory at the end.  Keys outside the chunk, masked by
+//    causality / window, or skipped (bad page id, -1 / out-of-range top-k
+//    entry) get -inf scores; the V rows of skipped keys are zeroed before use
+//    so that stale or garbage rows of a partially used page never reach the
+//    output.
 //  * Split-KV: the CTA for chunk s writes its normalised partial (O_s, lse_s)
 //    to the workspace; the last CTA of the (request, KV head, tile) to finish
 //    (atomic ticket, no waiting) merges all partials and writes the output.
+//  * Every mbarrier wait is bounded; on expiry the kernel sets
+//    PKV_EFLAG_TIMEOUT and leaves the loop instead of hanging.
+#include <cuda.h>
+#include <string.h>
+
 #include "pkv_internal.h"
 
 namespace pkv {
 namespace {
 
-constexpr int BK = 64;       // keys per pipeline stage
-constexpr int NWARP = 4;
-constexpr int NTHREAD = NWARP * 32;
+constexpr int BK = 64;          // keys per stage
+constexpr int NCW = 4;          // consumer warps
+constexpr int NCT = NCW * 32;   // consumer threads
 constexpr int ROWS = kDecodeRowTile;  // 16
+constexpr uint32_t kWaitLimit = 1u << 24;  // bounded mbarrier polls
+
+// ------------------------------------------------------------ PTX helpers
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity; false on expiry.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src,
@@ -41,12 +92,30 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src,
                "l"(src), "r"(src_bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
+// Makes the barrier count this thread's earlier cp.async as one arrival at
+// their completion (pending count raised first, so the thread still arrives
+// normally afterwards).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];\n" ::"r"(bar)
+               : "memory");
 }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map,
+                                            int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;\n" ::"n"(NCT) : "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0,
@@ -82,23 +151,24 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// byte offset of 16-byte chunk c of row r in a swizzled [rows][D] bf16 tile
-template <int D>
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-  return static_cast<uint32_t>((r * D + ((c ^ (r & 7)) << 3)) * 2);
+// Byte offset of 16-byte chunk c of row r in a [rows][D] tile stored as
+// [D/64 halves][rows][128 B] with the 128-byte swizzle.
+template <int NROWS>
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+  return static_cast<uint32_t>((c >> 3) * (NROWS * 128) + r * 128 +
+                               (((c & 7) ^ (r & 7)) << 4));
 }
 
 struct RowInfo {
-  int tok;    // query token index, -1 if the row is padding
-  int head;   // q head
-  int pos;    // absolute position i of the token
+  int tok;   // query token index, -1 if the row is padding
+  int head;  // q head
+  int pos;   // absolute position i of the token
 };
 
-// Row r (0..15) of tile `tile` of request b / KV head kvh.
-__device__ __forceinline__ RowInfo row_info(const AttnParams &p, int b,
-                                            int kvh, int tile, int r,
-                                            int q_len, int kv_len,
-                                            int q_begin) {
+// Row r (0..15) of tile `tile` of KV head kvh of the current request.
+__device__ __forceinline__ RowInfo row_info(const AttnParams &p, int kvh,
+                                            int tile, int r, int q_len,
+                                            int kv_len, int q_begin) {
   RowInfo ri{-1, 0, 0};
   int u, g;
   if (p.topk != nullptr) {
@@ -122,24 +192,52 @@ __device__ __forceinline__ RowInfo row_info(const AttnParams &p, int b,
   return ri;
 }
 
-template <int D, int NSTAGE>
-__global__ void __launch_bounds__(NTHREAD, 2)
-decode_gqa_kernel(const AttnParams p) {
-  constexpr int CPR = D / 8;             // 16-byte chunks per row
-  constexpr int RPP = NTHREAD / CPR;     // rows per producer pass
-  constexpr int PASSES = BK / RPP;
-  constexpr int KT = D / 16;             // k-steps of QK^T
-  constexpr int NT = D / 8;              // n-tiles of PV
-  constexpr uint32_t STAGE_BYTES = BK * D * 2;
+struct DecodeMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+};
 
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t *sQ = smem;                                   // [16][D] bf16
-  uint8_t *sK = sQ + ROWS * D * 2;                      // [NSTAGE][BK][D]
-  uint8_t *sV = sK + NSTAGE * STAGE_BYTES;              // [NSTAGE][BK][D]
-  int *sPos = reinterpret_cast<int *>(sV + NSTAGE * STAGE_BYTES);  // [NSTAGE][BK]
-  float *sM = reinterpret_cast<float *>(sPos + NSTAGE * BK);       // [NWARP][16]
-  float *sL = sM + NWARP * ROWS;                                   // [NWARP][16]
-  int *sFlag = reinterpret_cast<int *>(sL + NWARP * ROWS);
+// Shared-memory plan (offsets from a 1024-byte aligned base).
+template <int D, int NSTAGE>
+struct Smem {
+  static constexpr uint32_t kStage = BK * D * 2;            // one K (or V) stage
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kK + NSTAGE * kStage;
+  static constexpr uint32_t kQ = kV + NSTAGE * kStage;       // [16][D]
+  static constexpr uint32_t kPos = kQ + ROWS * D * 2;        // int [NSTAGE][BK]
+  static constexpr uint32_t kBar = kPos + NSTAGE * BK * 4;   // full, empty
+  static constexpr uint32_t kM = kBar + 2 * NSTAGE * 8;      // float [NCW][16]
+  static constexpr uint32_t kL = kM + NCW * ROWS * 4;
+  static constexpr uint32_t kFlag = kL + NCW * ROWS * 4;
+  static constexpr uint32_t kEnd = kFlag + 16;
+  static constexpr size_t kDynamic = kEnd + 1024;  // + alignment slack
+  static_assert(NCW * ROWS * (D + 4) * 4 <= 2 * NSTAGE * kStage,
+                "epilogue buffer must fit in the stage buffers");
+  static_assert(kBar % 8 == 0, "mbarriers need 8-byte alignment");
+};
+
+// ---------------------------------------------------------------- kernel
+
+template <int D, int NSTAGE, bool TMA>
+__global__ void __launch_bounds__(NCT + (TMA ? 32 : 64), 2)
+decode_gqa_kernel(const __grid_constant__ AttnParams p,
+                  const __grid_constant__ DecodeMaps maps) {
+  using S = Smem<D, NSTAGE>;
+  constexpr int CPR = D / 8;   // 16-byte chunks per row
+  constexpr int KT = D / 16;   // k-steps of QK^T
+  constexpr int NT = D / 8;    // n-tiles of PV
+  constexpr int NPROD = TMA ? 1 : 2;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  int *sPos = reinterpret_cast<int *>(smem + S::kPos);
+  float *sM = reinterpret_cast<float *>(smem + S::kM);
+  float *sL = reinterpret_cast<float *>(smem + S::kL);
+  int *sFlag = reinterpret_cast<int *>(smem + S::kFlag);
+  const uint32_t full0 = sbase + S::kBar;
+  const uint32_t empty0 = full0 + NSTAGE * 8;
 
   const int split = blockIdx.x;
   const int kvh = blockIdx.y / p.n_row_tiles;
@@ -154,29 +252,27 @@ decode_gqa_kernel(const AttnParams p) {
   const int kv_len = p.cache_seqlens[b];
 
   // ---- rows of this tile; CTAs past the request's rows have no work ----
-  int n_valid_rows = 0, u_min = 0x7fffffff, u_max = -1;
-  {
-    if (p.topk != nullptr) {
-      const int tpt = (p.group + ROWS - 1) / ROWS;
-      const int u = tile / tpt;
-      const int g0 = (tile % tpt) * ROWS;
-      if (u < q_len && g0 < p.group && q_begin + u >= 0 && q_begin + u < p.total_q) {
-        n_valid_rows = min(ROWS, p.group - g0);
-        u_min = u_max = u;
-      }
-    } else {
-      const int R0 = tile * ROWS;
-      const int R1 = min(R0 + ROWS, q_len * p.group);
-      if (R1 > R0) {
-        n_valid_rows = R1 - R0;
-        u_min = R0 / p.group;
-        u_max = (R1 - 1) / p.group;
-      }
+  int n_valid_rows = 0, u_min = 0, u_max = -1;
+  if (p.topk != nullptr) {
+    const int tpt = (p.group + ROWS - 1) / ROWS;
+    const int u = tile / tpt;
+    const int g0 = (tile % tpt) * ROWS;
+    if (u < q_len && g0 < p.group && q_begin + u >= 0 && q_begin + u < p.total_q) {
+      n_valid_rows = min(ROWS, p.group - g0);
+      u_min = u_max = u;
+    }
+  } else {
+    const int R0 = tile * ROWS;
+    const int R1 = min(R0 + ROWS, q_len * p.group);
+    if (R1 > R0) {
+      n_valid_rows = R1 - R0;
+      u_min = R0 / p.group;
+      u_max = (R1 - 1) / p.group;
     }
   }
   if (n_valid_rows == 0) return;  // uniform over the CTA
 
-  // ---- key range of this tile, then this split's chunk of it ----
+  // ---- key range [lo, hi) of the tile; this split's 64-key tiles ----
   int lo, hi;
   if (p.topk != nullptr) {
     lo = 0;
@@ -190,106 +286,164 @@ decode_gqa_kernel(const AttnParams p) {
     if (p.window_left >= 0) lo = max(0, i_min - p.window_left);
     hi = max(hi, lo);
   }
-  int k0, k1;
-  {
-    const int len = hi - lo;
-    int chunk = (len + p.num_splits - 1) / p.num_splits;
-    chunk = (chunk + BK - 1) / BK * BK;
-    k0 = min(hi, lo + split * chunk);
-    k1 = min(hi, k0 + chunk);
-  }
-  const int n_kt = (k1 - k0 + BK - 1) / BK;
+  const int t_lo = lo / BK;
+  const int t_hi = (hi + BK - 1) / BK;
+  const int per = (t_hi - t_lo + p.num_splits - 1) / p.num_splits;
+  const int t0 = min(t_hi, t_lo + split * per);
+  const int t1 = min(t_hi, t0 + per);
+  const int n_kt = t1 - t0;
 
-  // ---- stage Q rows into shared memory (zero rows for padding) ----
-  for (int e = tid; e < ROWS * CPR; e += NTHREAD) {
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(full0 + 8 * s, TMA ? 1 : NPROD * 32);
+      mbar_init(empty0 + 8 * s, NCW);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    fence_proxy_async();
+  }
+  __syncthreads();
+
+  if (warp >= NCW) {
+    // ================================ producer ================================
+    const int ptid = tid - NCT;
+    for (int kt = 0; kt < n_kt; ++kt) {
+      const int st = kt % NSTAGE;
+      const uint32_t full = full0 + 8 * st;
+      if (kt >= NSTAGE && !mbar_wait(empty0 + 8 * st, ((kt / NSTAGE) & 1) ^ 1)) {
+        if ((ptid & 31) == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+        break;
+      }
+      const int base = (t0 + kt) * BK;  // absolute key (or list) index of row 0
+      const uint32_t kdst = sbase + S::kK + st * S::kStage;
+      const uint32_t vdst = sbase + S::kV + st * S::kStage;
+      if constexpr (TMA) {
+        // page box: the page, or 64 rows of a longer page
+        const int pbox = p.page_size <= BK ? p.page_size : BK;
+        const int nbox = BK / pbox;
+        bool box_ok = false;
+        int page = 0, inpage = 0;
+        const int bpos0 = base + lane * pbox;
+        if (lane < nbox && bpos0 < hi && bpos0 + pbox > lo) {
+          const int pidx = bpos0 / p.page_size;
+          inpage = bpos0 - pidx * p.page_size;
+          if (pidx < p.pt_cols) {
+            const int64_t pg = p.page_table[static_cast<int64_t>(b) * p.pt_stride + pidx];
+            if (pg >= 0 && pg < p.num_pages) {
+              page = static_cast<int>(pg);
+              box_ok = true;
+            } else {
+              atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
+            }
+          } else {
+            atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
+          }
+        }
+        // positions of rows lane and lane + 32 (-1: skipped)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = lane + 32 * h;
+          const int ok = __shfl_sync(0xffffffffu, box_ok ? 1 : 0, r / pbox);
+          const int pos = base + r;
+          sPos[st * BK + r] = (ok && pos >= lo && pos < hi) ? pos : -1;
+        }
+        const uint32_t box_bytes = static_cast<uint32_t>(pbox) * 128u;
+        uint32_t bytes = box_ok ? box_bytes * (D / 64) * 2 : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(full, bytes);
+        __syncwarp();
+        if (box_ok) {
+          const uint32_t roff = static_cast<uint32_t>(lane * pbox) * 128u;
+#pragma unroll
+          for (int hf = 0; hf < D / 64; ++hf) {
+            const uint32_t hoff = hf * (BK * 128) + roff;
+            tma_load_4d(kdst + hoff, &maps.k, hf * 64, kvh, inpage, page, full);
+            tma_load_4d(vdst + hoff, &maps.v, hf * 64, kvh, inpage, page, full);
+          }
+        }
+      } else {
+        // cp.async gather: thread -> (chunk, row within a pass)
+        constexpr int RPP = NPROD * 32 / CPR;  // rows per pass
+        const int chunk = ptid % CPR;
+        const int prow = ptid / CPR;
+        const int topk_tok = q_begin + u_min;
+#pragma unroll 4
+        for (int r = prow; r < BK; r += RPP) {
+          const int j = base + r;
+          int pos = -1;
+          const bf16 *ksrc = p.k;
+          const bf16 *vsrc = p.v;
+          if (j >= lo && j < hi) {
+            pos = j;
+            bool ok = true;
+            if (p.topk != nullptr) {
+              pos = p.topk[static_cast<int64_t>(topk_tok) * p.topk_stride + j];
+              if (pos < 0 || pos >= kv_len) {
+                if (pos != -1 && chunk == 0) atomicOr(p.err, PKV_EFLAG_TOPK_OOB);
+                ok = false;
+              }
+            }
+            if (ok) {
+              const int pidx = pos / p.page_size;
+              if (pidx >= p.pt_cols) {
+                if (chunk == 0) atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
+                ok = false;
+              } else {
+                const int64_t pg = p.page_table[static_cast<int64_t>(b) * p.pt_stride + pidx];
+                if (pg < 0 || pg >= p.num_pages) {
+                  if (chunk == 0) atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
+                  ok = false;
+                } else {
+                  const int inpage = pos - pidx * p.page_size;
+                  ksrc = p.k + pg * p.k_sp + inpage * p.k_spos + kvh * p.k_sh + chunk * 8;
+                  vsrc = p.v + pg * p.v_sp + inpage * p.v_spos + kvh * p.v_sh + chunk * 8;
+                }
+              }
+            }
+            if (!ok) pos = -1;
+          }
+          const int nbytes = pos >= 0 ? 16 : 0;
+          cp_async16(kdst + tile_off<BK>(r, chunk), ksrc, nbytes);
+          cp_async16(vdst + tile_off<BK>(r, chunk), vsrc, nbytes);
+          if (chunk == 0) sPos[st * BK + r] = pos;
+        }
+        cp_async_arrive(full);
+        mbar_arrive(full);
+      }
+    }
+    return;
+  }
+
+  // ================================== consumers ==================================
+  // Q rows into shared memory (zero rows for padding)
+  for (int e = tid; e < ROWS * CPR; e += NCT) {
     const int r = e / CPR, c = e % CPR;
-    const RowInfo ri = row_info(p, b, kvh, tile, r, q_len, kv_len, q_begin);
+    const RowInfo ri = row_info(p, kvh, tile, r, q_len, kv_len, q_begin);
     uint4 val = make_uint4(0, 0, 0, 0);
     if (ri.tok >= 0)
-      val = *reinterpret_cast<const uint4 *>(
-          p.q + static_cast<int64_t>(ri.tok) * p.q_st +
-          static_cast<int64_t>(ri.head) * p.q_sh + c * 8);
-    *reinterpret_cast<uint4 *>(sQ + swz<D>(r, c)) = val;
+      val = *reinterpret_cast<const uint4 *>(p.q + static_cast<int64_t>(ri.tok) * p.q_st +
+                                             static_cast<int64_t>(ri.head) * p.q_sh + c * 8);
+    *reinterpret_cast<uint4 *>(smem + S::kQ + tile_off<ROWS>(r, c)) = val;
   }
+  consumer_sync();
 
-  // ---- producer: gather one 64-key stage of K and V rows ----
-  const int prow = tid / CPR;   // row within a pass
-  const int pchunk = tid % CPR;
-  const int topk_tok = q_begin + u_min;  // top-k mode: one token per tile
-  auto issue_stage = [&](int kt) {
-    const int st = kt % NSTAGE;
-    const int base = k0 + kt * BK;
-    const uint32_t kdst0 = smem_addr(sK + st * STAGE_BYTES);
-    const uint32_t vdst0 = smem_addr(sV + st * STAGE_BYTES);
-#pragma unroll
-    for (int ps = 0; ps < PASSES; ++ps) {
-      const int r = ps * RPP + prow;
-      const int j = base + r;
-      int pos = -1;
-      const bf16 *ksrc = p.k;
-      const bf16 *vsrc = p.v;
-      if (j < k1) {
-        pos = j;
-        bool ok = true;
-        if (p.topk != nullptr) {
-          pos = p.topk[static_cast<int64_t>(topk_tok) * p.topk_stride + j];
-          if (pos < 0 || pos >= kv_len) {
-            if (pos != -1 && pchunk == 0) atomicOr(p.err, PKV_EFLAG_TOPK_OOB);
-            ok = false;
-          }
-        }
-        if (ok) {
-          const int pidx = pos / p.page_size;
-          if (pidx >= p.pt_cols) {
-            if (pchunk == 0) atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
-            ok = false;
-          } else {
-            const int64_t page = p.page_table[static_cast<int64_t>(b) * p.pt_stride + pidx];
-            if (page < 0 || page >= p.num_pages) {
-              if (pchunk == 0) atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
-              ok = false;
-            } else {
-              const int inpage = pos - pidx * p.page_size;
-              ksrc = p.k + page * p.k_sp + inpage * p.k_spos + kvh * p.k_sh + pchunk * 8;
-              vsrc = p.v + page * p.v_sp + inpage * p.v_spos + kvh * p.v_sh + pchunk * 8;
-            }
-          }
-        }
-        if (!ok) pos = -1;
-      }
-      const int bytes = pos >= 0 ? 16 : 0;
-      cp_async16(kdst0 + swz<D>(r, pchunk), ksrc, bytes);
-      cp_async16(vdst0 + swz<D>(r, pchunk), vsrc, bytes);
-      if (pchunk == 0) sPos[st * BK + r] = pos;
-    }
-  };
-
-#pragma unroll
-  for (int s = 0; s < NSTAGE - 1; ++s) {
-    if (s < n_kt) issue_stage(s);
-    cp_async_commit();
-  }
-  __syncthreads();  // Q tile visible
-
-  // ---- Q fragments (A operand, 16 x D) ----
   uint32_t qf[KT][4];
   {
-    const uint32_t qbase = smem_addr(sQ);
     const int m = lane >> 3;
     const int r = (m & 1) * 8 + (lane & 7);
 #pragma unroll
     for (int kk = 0; kk < KT; ++kk)
-      ldsm_x4(qbase + swz<D>(r, 2 * kk + (m >> 1)), qf[kk][0], qf[kk][1],
+      ldsm_x4(sbase + S::kQ + tile_off<ROWS>(r, 2 * kk + (m >> 1)), qf[kk][0], qf[kk][1],
               qf[kk][2], qf[kk][3]);
   }
 
-  // positions of this thread's two rows (g and g + 8)
   const int g = lane >> 2;
   const int tq = lane & 3;
   int rpos[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h)
-    rpos[h] = row_info(p, b, kvh, tile, g + 8 * h, q_len, kv_len, q_begin).pos;
+    rpos[h] = row_info(p, kvh, tile, g + 8 * h, q_len, kv_len, q_begin).pos;
   const bool use_upper = p.causal || p.window_left >= 0;
 
   float o[NT][4];
@@ -297,18 +451,32 @@ decode_gqa_kernel(const AttnParams p) {
   for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY};
   float l_run[2] = {0.f, 0.f};
+  const int key0 = warp * 16;
 
-  // ---- main loop ----
   for (int kt = 0; kt < n_kt; ++kt) {
-    cp_async_wait<NSTAGE - 2>();
-    __syncthreads();
-    if (kt + NSTAGE - 1 < n_kt) issue_stage(kt + NSTAGE - 1);
-    cp_async_commit();
-
     const int st = kt % NSTAGE;
-    const uint32_t kbase = smem_addr(sK + st * STAGE_BYTES);
-    const uint32_t vbase = smem_addr(sV + st * STAGE_BYTES);
-    const int key0 = warp * 16;
+    if (!mbar_wait(full0 + 8 * st, (kt / NSTAGE) & 1)) {
+      if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+      break;
+    }
+    const uint32_t kbase = sbase + S::kK + st * S::kStage;
+    const uint32_t vbase = sbase + S::kV + st * S::kStage;
+    const int *pos_st = sPos + st * BK + key0;
+
+    // zero the V rows of skipped keys among this warp's 16 (a masked key must
+    // contribute exactly 0, whatever its row holds)
+    const bool any_skipped = __any_sync(0xffffffffu, pos_st[lane & 15] < 0);
+    if (any_skipped) {
+#pragma unroll
+      for (int i = 0; i < 16 * CPR / 32; ++i) {
+        const int idx = i * 32 + lane;
+        const int rr = idx / CPR, cc = idx % CPR;
+        if (pos_st[rr] < 0)
+          *reinterpret_cast<uint4 *>(smem + S::kV + st * S::kStage +
+                                     tile_off<BK>(key0 + rr, cc)) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
 
     // S = Q K^T for this warp's 16 keys
     float s[2][4];
@@ -320,18 +488,18 @@ decode_gqa_kernel(const AttnParams p) {
 #pragma unroll
       for (int kk = 0; kk < KT; ++kk) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + swz<D>(kr, 2 * kk + kc), b0, b1, b2, b3);
+        ldsm_x4(kbase + tile_off<BK>(kr, 2 * kk + kc), b0, b1, b2, b3);
         mma_bf16(s[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
         mma_bf16(s[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
       }
     }
 
-    // masks, scale to log2 domain
+    // masks; scale to the log2 domain
     int kpos[2][2];
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
-      kpos[n][0] = sPos[st * BK + key0 + n * 8 + 2 * tq];
-      kpos[n][1] = sPos[st * BK + key0 + n * 8 + 2 * tq + 1];
+      kpos[n][0] = pos_st[n * 8 + 2 * tq];
+      kpos[n][1] = pos_st[n * 8 + 2 * tq + 1];
     }
 #pragma unroll
     for (int n = 0; n < 2; ++n)
@@ -348,8 +516,7 @@ decode_gqa_kernel(const AttnParams p) {
     // online softmax per row
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      float mx = fmaxf(fmaxf(s[0][2 * h], s[0][2 * h + 1]),
-                       fmaxf(s[1][2 * h], s[1][2 * h + 1]));
+      float mx = fmaxf(fmaxf(s[0][2 * h], s[0][2 * h + 1]), fmaxf(s[1][2 * h], s[1][2 * h + 1]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float m_new = fmaxf(m_run[h], mx);
@@ -383,14 +550,18 @@ decode_gqa_kernel(const AttnParams p) {
 #pragma unroll
       for (int cc = 0; cc < NT / 2; ++cc) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vbase + swz<D>(vr, 2 * cc + vc), b0, b1, b2, b3);
+        ldsm_x4_t(vbase + tile_off<BK>(vr, 2 * cc + vc), b0, b1, b2, b3);
         mma_bf16(o[2 * cc], a0, a1, a2, a3, b0, b1);
         mma_bf16(o[2 * cc + 1], a0, a1, a2, a3, b2, b3);
       }
     }
+
+    // hand the stage back to the producer
+    if (TMA && any_skipped) fence_proxy_async();  // generic zeros before TMA rewrites
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
   }
-  cp_async_wait<0>();
-  __syncthreads();  // pipeline buffers free for the epilogue
+  consumer_sync();  // every consumer is done with the stage buffers
 
   // ---- merge the four warps' states ----
 #pragma unroll
@@ -404,15 +575,15 @@ decode_gqa_kernel(const AttnParams p) {
     sL[warp * ROWS + g] = l_run[0];
     sL[warp * ROWS + g + 8] = l_run[1];
   }
-  __syncthreads();
+  consumer_sync();
   constexpr int OSTRIDE = D + 4;  // padded fp32 row
-  float *sO = reinterpret_cast<float *>(sK);  // [NWARP][16][D + 4]
+  float *sO = reinterpret_cast<float *>(smem + S::kK);  // [NCW][16][D + 4]
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int r = g + 8 * h;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NWARP; ++w) M = fmaxf(M, sM[w * ROWS + r]);
+    for (int w = 0; w < NCW; ++w) M = fmaxf(M, sM[w * ROWS + r]);
     const float f = M == -INFINITY ? 0.f : exp2f(m_run[h] - M);
     float *dst = sO + (warp * ROWS + r) * OSTRIDE;
 #pragma unroll
@@ -420,26 +591,24 @@ decode_gqa_kernel(const AttnParams p) {
       *reinterpret_cast<float2 *>(dst + n * 8 + 2 * tq) =
           make_float2(o[n][2 * h] * f, o[n][2 * h + 1] * f);
   }
-  __syncthreads();
+  consumer_sync();
 
-  // each thread: one row, D/8 consecutive columns
-  constexpr int CPT = D / 8;  // columns per thread
+  // each consumer thread: one row, D/8 consecutive columns
+  constexpr int CPT = D / 8;
   const int fr = tid >> 3;
   const int fc = (tid & 7) * CPT;
   float M = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < NWARP; ++w) M = fmaxf(M, sM[w * ROWS + fr]);
+  for (int w = 0; w < NCW; ++w) M = fmaxf(M, sM[w * ROWS + fr]);
   float L = 0.f;
 #pragma unroll
-  for (int w = 0; w < NWARP; ++w) {
-    const float mw = sM[w * ROWS + fr];
-    L += (M == -INFINITY) ? 0.f : sL[w * ROWS + fr] * exp2f(mw - M);
-  }
+  for (int w = 0; w < NCW; ++w)
+    L += (M == -INFINITY) ? 0.f : sL[w * ROWS + fr] * exp2f(sM[w * ROWS + fr] - M);
   float acc[CPT];
 #pragma unroll
   for (int c = 0; c < CPT; ++c) acc[c] = 0.f;
 #pragma unroll
-  for (int w = 0; w < NWARP; ++w) {
+  for (int w = 0; w < NCW; ++w) {
     const float *src = sO + (w * ROWS + fr) * OSTRIDE + fc;
 #pragma unroll
     for (int c = 0; c < CPT; c += 4) {
@@ -449,7 +618,7 @@ decode_gqa_kernel(const AttnParams p) {
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const float lse_nat = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-  const RowInfo fri = row_info(p, b, kvh, tile, fr, q_len, kv_len, q_begin);
+  const RowInfo fri = row_info(p, kvh, tile, fr, q_len, kv_len, q_begin);
 
   if (p.num_splits == 1) {
     if (fri.tok >= 0) {
@@ -482,14 +651,13 @@ decode_gqa_kernel(const AttnParams p) {
     if ((tid & 7) == 0) __stcg(p.ws_lse + split * rows_total + row, lse_nat);
   }
   __threadfence();
-  __syncthreads();
+  consumer_sync();
   if (tid == 0) {
-    int32_t *ctr = p.ws_counter +
-                   (static_cast<int64_t>(b) * p.h_kv + kvh) * p.n_row_tiles + tile;
+    int32_t *ctr = p.ws_counter + (static_cast<int64_t>(b) * p.h_kv + kvh) * p.n_row_tiles + tile;
     const int ticket = atomicAdd(ctr, 1);
     *sFlag = (ticket == p.num_splits - 1);
   }
-  __syncthreads();
+  consumer_sync();
   if (!*sFlag) return;
   __threadfence();  // every other chunk's state is visible from here on
 
@@ -497,11 +665,10 @@ decode_gqa_kernel(const AttnParams p) {
   if (fri.tok < 0) return;
   const int64_t row = static_cast<int64_t>(fri.tok) * p.h_q + fri.head;
   float Ms = -INFINITY;
-  for (int sp = 0; sp < p.num_splits; ++sp)
-    Ms = fmaxf(Ms, __ldcg(p.ws_lse + sp * rows_total + row));
-  float out[CPT];
+  for (int sp = 0; sp < p.num_splits; ++sp) Ms = fmaxf(Ms, __ldcg(p.ws_lse + sp * rows_total + row));
+  float outv[CPT];
 #pragma unroll
-  for (int c = 0; c < CPT; ++c) out[c] = 0.f;
+  for (int c = 0; c < CPT; ++c) outv[c] = 0.f;
   float wsum = 0.f;
   if (Ms != -INFINITY) {
     for (int sp = 0; sp < p.num_splits; ++sp) {
@@ -512,8 +679,8 @@ decode_gqa_kernel(const AttnParams p) {
 #pragma unroll
       for (int c = 0; c < CPT; c += 4) {
         const float4 v4 = __ldcg(reinterpret_cast<const float4 *>(src + c));
-        out[c] += w * v4.x; out[c + 1] += w * v4.y;
-        out[c + 2] += w * v4.z; out[c + 3] += w * v4.w;
+        outv[c] += w * v4.x; outv[c + 1] += w * v4.y;
+        outv[c + 2] += w * v4.z; outv[c + 3] += w * v4.w;
       }
     }
   }
@@ -523,10 +690,10 @@ decode_gqa_kernel(const AttnParams p) {
 #pragma unroll
   for (int c = 0; c < CPT; c += 8) {
     uint4 u;
-    u.x = pack_bf16(out[c] * winv, out[c + 1] * winv);
-    u.y = pack_bf16(out[c + 2] * winv, out[c + 3] * winv);
-    u.z = pack_bf16(out[c + 4] * winv, out[c + 5] * winv);
-    u.w = pack_bf16(out[c + 6] * winv, out[c + 7] * winv);
+    u.x = pack_bf16(outv[c] * winv, outv[c + 1] * winv);
+    u.y = pack_bf16(outv[c + 2] * winv, outv[c + 3] * winv);
+    u.z = pack_bf16(outv[c + 4] * winv, outv[c + 5] * winv);
+    u.w = pack_bf16(outv[c + 6] * winv, outv[c + 7] * winv);
     *reinterpret_cast<uint4 *>(dst + c) = u;
   }
   if (p.lse != nullptr && (tid & 7) == 0)
@@ -534,29 +701,80 @@ decode_gqa_kernel(const AttnParams p) {
         wsum > 0.f ? Ms + logf(wsum) : -INFINITY;
 }
 
-template <int D, int NSTAGE>
-constexpr size_t decode_smem_bytes() {
-  return ROWS * D * 2 + 2 * NSTAGE * BK * D * 2 + NSTAGE * BK * 4 +
-         2 * NWARP * ROWS * 4 + 16;
+// ------------------------------------------------------------------- host
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
+                                   void *, const cuuint64_t *, const cuuint64_t *,
+                                   const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    tried = true;
+  }
+  return fn;
 }
 
-template <int D, int NSTAGE>
-int launch_typed(const AttnParams &p, cudaStream_t stream) {
-  constexpr size_t smem = decode_smem_bytes<D, NSTAGE>();
-  static_assert(NWARP * ROWS * (D + 4) * 4 <= 2 * NSTAGE * BK * D * 2,
-                "epilogue buffer must fit in the pipeline buffers");
+// 4-D map over a [pages][P][H_kv][D] cache (dims innermost first); one box =
+// one 64-column half of `pbox` rows of one page of one head.
+bool encode_kv_map(CUtensorMap *map, const bf16 *base, int d, int h_kv, int page,
+                   int64_t num_pages, int64_t s_head, int64_t s_pos, int64_t s_page,
+                   int pbox) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h_kv),
+                        static_cast<cuuint64_t>(page), static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s_head) * 2,
+                           static_cast<cuuint64_t>(s_pos) * 2,
+                           static_cast<cuuint64_t>(s_page) * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(pbox), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<bf16 *>(base), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The TMA loader covers dense attention with page boxes of 8 or more rows
+// (1024-byte aligned in shared memory) and strides that nest (head inside
+// position inside page).
+bool tma_eligible(const AttnParams &p) {
+  if (p.topk != nullptr) return false;
+  const int P = p.page_size;
+  if (P % 8 != 0) return false;
+  if (P <= BK ? (BK % P != 0) : (P % BK != 0)) return false;
+  if (p.num_pages > 0xffffffffLL) return false;
+  auto nests = [&](int64_t sh, int64_t spos, int64_t sp, int d) {
+    return sh >= d && spos >= sh * p.h_kv && sp >= spos * P;
+  };
+  return nests(p.k_sh, p.k_spos, p.k_sp, p.d) && nests(p.v_sh, p.v_spos, p.v_sp, p.dv);
+}
+
+template <int D, int NSTAGE, bool TMA>
+int launch_typed(const AttnParams &p, const DecodeMaps &maps, cudaStream_t stream) {
+  constexpr size_t smem = Smem<D, NSTAGE>::kDynamic;
+  constexpr int threads = NCT + (TMA ? 32 : 64);
   static bool configured[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (dev < 64 && !configured[dev]) {
-    if (cudaFuncSetAttribute(decode_gqa_kernel<D, NSTAGE>,
+    if (cudaFuncSetAttribute(decode_gqa_kernel<D, NSTAGE, TMA>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return PKV_ERR_CUDA;
     configured[dev] = true;
   }
   dim3 grid(p.num_splits, p.h_kv * p.n_row_tiles, p.batch);
-  decode_gqa_kernel<D, NSTAGE><<<grid, NTHREAD, smem, stream>>>(p);
+  decode_gqa_kernel<D, NSTAGE, TMA><<<grid, threads, smem, stream>>>(p, maps);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -566,9 +784,24 @@ int launch_decode_gqa(const AttnParams &p, cudaStream_t stream) {
   if (p.batch == 0 || p.n_row_tiles == 0) return PKV_OK;
   if (p.h_kv * p.n_row_tiles > 65535 || p.batch > 65535 || p.num_splits > 65535)
     return PKV_ERR_UNSUPPORTED;
-  if (p.d == 128 && p.dv == 128) return launch_typed<128, 3>(p, stream);
-  if (p.d == 64 && p.dv == 64) return launch_typed<64, 4>(p, stream);
-  return PKV_ERR_UNSUPPORTED;
+  if (!((p.d == 128 && p.dv == 128) || (p.d == 64 && p.dv == 64)))
+    return PKV_ERR_UNSUPPORTED;
+  DecodeMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  bool tma = tma_eligible(p);
+  if (tma) {
+    const int pbox = p.page_size <= BK ? p.page_size : BK;
+    tma = encode_kv_map(&maps.k, p.k, p.d, p.h_kv, p.page_size, p.num_pages, p.k_sh,
+                        p.k_spos, p.k_sp, pbox) &&
+          encode_kv_map(&maps.v, p.v, p.dv, p.h_kv, p.page_size, p.num_pages, p.v_sh,
+                        p.v_spos, p.v_sp, pbox);
+  }
+  if (p.d == 128) {
+    return tma ? launch_typed<128, 3, true>(p, maps, stream)
+               : launch_typed<128, 3, false>(p, maps, stream);
+  }
+  return tma ? launch_typed<64, 4, true>(p, maps, stream)
+             : launch_typed<64, 4, false>(p, maps, stream);
 }
 
 }  // namespace pkv

@@ -411,3 +411,63 @@ def test_swa_decode_full_size_sampled():
     idx = torch.from_numpy(rows).long()
     check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
                 ref_o, ref_l, "swa full-size sampled")
+
+
+# ------------------------------------------- loader coverage (TMA / cp.async)
+
+@pytest.mark.parametrize("page_size,q_len,window,causal", [
+    (8, 1, -1, False), (32, 1, 300, False), (64, 4, -1, True), (128, 1, -1, False),
+    (128, 3, 200, True), (16, 2, 0, True),
+])
+def test_page_box_sizes(page_size, q_len, window, causal):
+    """Page sizes served by whole-page tensor-map boxes (multiples of 8, and
+    pages longer than a 64-key stage), with windows and causal runs."""
+    wl = workloads.make("tiny_decode", d=128, page_size=page_size, h_q=16, h_kv=4,
+                        q_len=q_len, window_left=window, causal=causal,
+                        len_lo=q_len, len_hi=1500, batch=6,
+                        pool_tokens=6 * (1500 + page_size) * 2)
+    g = wl.to(DEV)
+    for splits in (1, 3):
+        out, lse = gpu_attn(g, num_splits=splits)
+        ref_o, ref_l, _ = oracle_attn(wl)
+        check_close(out, lse, ref_o, ref_l, f"P={page_size} splits={splits}")
+    assert pkv.get_error_flags() == 0
+
+
+@pytest.mark.parametrize("page_size", [16, 3, 64])
+def test_garbage_outside_valid_rows_never_leaks(page_size):
+    """Every cache row that is not one of a request's first kv_len keys is
+    NaN (e.g. the unused tail of the last page): outputs must equal the
+    oracle's, which reads only valid rows."""
+    wl = workloads.make("tiny_decode", page_size=page_size, h_q=8, h_kv=2, batch=5,
+                        len_lo=1, len_hi=900, pool_tokens=5 * (900 + 64) * 2)
+    valid = torch.zeros(wl.k_cache.shape[0] * page_size, dtype=torch.bool)
+    for b in range(5):
+        n = int(wl.cache_seqlens[b])
+        j = torch.arange(n)
+        slots = wl.page_table[b, j // page_size].long() * page_size + j % page_size
+        valid[slots] = True
+    valid = valid.view(-1, page_size)
+    wl.k_cache[~valid] = float("nan")
+    wl.v_cache[~valid] = float("nan")
+    g = wl.to(DEV)
+    for splits in (1, 4):
+        out, lse = gpu_attn(g, num_splits=splits)
+        ref_o, ref_l, _ = oracle_attn(wl)
+        check_close(out, lse, ref_o, ref_l, f"nan P={page_size} splits={splits}")
+
+
+def test_head_major_cache_layout():
+    """A cache laid out [pages, H_kv, P, D] (head outside position) is read
+    through its strides; results equal the oracle's."""
+    wl = workloads.make("tiny_decode", page_size=16, h_q=8, h_kv=2, batch=4,
+                        len_lo=10, len_hi=700, pool_tokens=4 * 720 * 2)
+    k_hm = wl.k_cache.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+    v_hm = wl.v_cache.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+    assert k_hm.stride(1) == 128 and k_hm.stride(2) == 16 * 128
+    g = wl.to(DEV)
+    g.k_cache = k_hm.to(DEV).permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+    g.v_cache = v_hm.to(DEV).permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+    out, lse = gpu_attn(g, num_splits=2)
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, "head-major")
