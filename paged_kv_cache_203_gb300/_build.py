@@ -20,6 +20,7 @@ SOURCES = [
     "pkv_pagetable.cu",
     "pkv_merge.cu",
     "pkv_decode.cu",
+    "pkv_extend.cu",
     "pkv_noalloc.cu",
 ]
 

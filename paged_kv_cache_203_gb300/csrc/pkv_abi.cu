@@ -50,7 +50,7 @@ bool vec_ok(const pkv_tensor &t, int elem_bytes) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct AttnPlan {
-  int kind;          // 0 = decode-gqa kernel
+  int kind;          // 0 = decode-gqa kernel, 1 = tcgen05 extend kernel
   int num_splits;
   int n_row_tiles;
   size_t ws_o_bytes, ws_lse_bytes, ws_ctr_bytes;
@@ -92,6 +92,24 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
     return PKV_ERR_UNSUPPORTED;
 
   plan->kind = 0;
+  if (!present(topk) && d == 128 && dv == 128 && max_seqlen_q >= kExtendMinSeqlenQ) {
+    AttnParams lp{};
+    lp.d = 128;
+    lp.dv = 128;
+    lp.h_q = static_cast<int>(h_q);
+    lp.h_kv = static_cast<int>(h_kv);
+    lp.page_size = static_cast<int>(page);
+    lp.num_pages = num_pages;
+    lp.q_st = q.stride[0];
+    lp.q_sh = q.stride[1];
+    lp.k_sp = k.stride[0];
+    lp.k_spos = k.stride[1];
+    lp.k_sh = k.stride[2];
+    lp.v_sp = v.stride[0];
+    lp.v_spos = v.stride[1];
+    lp.v_sh = v.stride[2];
+    if (extend_eligible(lp)) plan->kind = 1;  // tcgen05 extend, no workspace
+  }
   if (present(topk)) {
     plan->n_row_tiles = max_seqlen_q * ((group + kDecodeRowTile - 1) / kDecodeRowTile);
   } else {
@@ -110,6 +128,7 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
     splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s, 64)));
   }
   splits = std::min(splits, 1024);
+  if (plan->kind == 1) splits = 1;
   plan->num_splits = splits;
   const size_t rows_total = static_cast<size_t>(total_q) * h_q;
   plan->ws_o_bytes = align256(static_cast<size_t>(splits) * rows_total * dv * 4);
@@ -241,6 +260,11 @@ int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
       return PKV_ERR_CUDA;
   }
   if (p.total_q == 0) return PKV_OK;
+  if (plan.kind == 1) {
+    rc = launch_extend_tc(p, stream);
+    if (rc != PKV_ERR_UNSUPPORTED) return rc;
+    p.num_splits = 1;  // tensor maps not encodable: unsplit decode kernel
+  }
   return launch_decode_gqa(p, stream);
 }
 

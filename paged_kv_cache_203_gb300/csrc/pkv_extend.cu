@@ -1,0 +1,637 @@
+// pkv_extend.cu -- varlen causal extend (chunked prefill) against a paged KV
+// cache on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// Computes the same attention as the decode kernel (flashattention_backend.py
+// `forward_extend`: `flash_attn_with_kvcache` with cu_seqlens_q, causal, the
+// (W, 0) window, bottom-right alignment) for long runs of new tokens, where
+// it is a dense contraction.
+//
+// One CTA = one tile of 128 consecutive new tokens of one request for one q
+// head; its keys stream in 128-key tiles (whole page boxes).
+//   warp 4  producer: TMA loads of the Q tile once, then K and V tiles into
+//           two 2-stage rings (4-D tensor-map boxes per page and 64-column
+//           half, 128-byte swizzle), plus a per-tile key-validity bitmask;
+//   warp 5  MMA issuer (one thread): S_j = Q K_j^T into TMEM buffer j%2,
+//           then O += P_{j-1} V_{j-1} into the TMEM accumulator, each a chain
+//           of eight 128x128x16 bf16 MMAs with fp32 accumulation; completion
+//           signalled with tcgen05.commit on mbarriers (a K stage is released
+//           when its QK^T is done, a V stage when its PV is done);
+//   warps 0-3 softmax (thread = query row = TMEM lane): one 128-column TMEM
+//           load of S_j, online softmax in the log2 domain with a lazy
+//           reference max (O and l are rescaled in place only when the row
+//           max grows by more than 2^8), P_j (bf16) written to shared memory
+//           as the A operand of the PV MMA; V rows of keys past the sequence
+//           or in skipped pages are zeroed.
+// TMEM: S0 | S1 | O (128 columns each; 512 allocated, 1 CTA per SM).
+// Every mbarrier wait is bounded (PKV_EFLAG_TIMEOUT on expiry).
+#include <cuda.h>
+#include <limits.h>
+#include <string.h>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int BM = 128;           // query rows per CTA
+constexpr int BN = 128;           // keys per tile
+constexpr int D = 128;            // head dim (q/k and v)
+constexpr int NTHREADS = 192;     // 4 softmax warps, producer, MMA
+constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr uint32_t kTileBytes = BM * D * 2;  // 32 KB, any 128x128 bf16 tile
+
+struct Smem {
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK = kQ + kTileBytes;       // 2 stages
+  static constexpr uint32_t kV = kK + 2 * kTileBytes;   // 2 stages
+  static constexpr uint32_t kP = kV + 2 * kTileBytes;   // 2 buffers
+  static constexpr uint32_t kMask = kP + 2 * kTileBytes;  // uint32 [2][4]
+  static constexpr uint32_t kBar = kMask + 32;
+  // barriers: q_full, k_full[2], v_full[2], k_empty[2], v_empty[2],
+  //           s_full[2], s_free[2], p_full[2], o_done[2]
+  static constexpr int kNumBars = 17;
+  static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
+  static constexpr uint32_t kEnd = kTmemSlot + 16;
+  static constexpr size_t kDynamic = kEnd + 1024;
+};
+static_assert(Smem::kDynamic <= 232448, "shared memory plan exceeds 227 KB");
+
+enum BarId {
+  Q_FULL = 0, K_FULL = 1, V_FULL = 3, K_EMPTY = 5, V_EMPTY = 7, S_FULL = 9, S_FREE = 11,
+  P_FULL = 13, O_DONE = 15
+};
+
+// ------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0,
+                                            int c1, int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0,
+                                            int c1, int c2, int c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor, kind::f16: bf16 x bf16 -> f32, M = 128, N = 128.
+__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |
+         (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+      : "memory");
+}
+// 32 lanes x 32 consecutive fp32 columns -> 32 registers per thread
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Byte offset of 16-byte chunk c of row r of a 128-row tile stored as
+// [2 halves][128 rows][128 B] with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+  return static_cast<uint32_t>((c >> 3) * (BM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+struct ExtendMaps {
+  CUtensorMap q;
+  CUtensorMap k;
+  CUtensorMap v;
+};
+
+// 128 consecutive fp32 columns of this thread's TMEM lane (one load + wait
+// in a single statement, so no register is read before the data lands)
+#define PKV_O4(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3])
+#define PKV_O16(i) PKV_O4(i), PKV_O4(i + 4), PKV_O4(i + 8), PKV_O4(i + 12)
+#define PKV_O64(i) PKV_O16(i), PKV_O16(i + 16), PKV_O16(i + 32), PKV_O16(i + 48)
+#define PKV_I4(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3])
+#define PKV_I16(i) PKV_I4(i), PKV_I4(i + 4), PKV_I4(i + 8), PKV_I4(i + 12)
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : PKV_O64(0), PKV_O64(64)
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  uint32_t r[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+               PKV_I16(0), PKV_I16(16)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
+// ---------------------------------------------------------------- kernel
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ ExtendMaps maps) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  uint32_t *sMask = reinterpret_cast<uint32_t *>(smem + Smem::kMask);
+  uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + Smem::kTmemSlot);
+  auto bar = [&](int id) { return sbase + Smem::kBar + 8u * id; };
+
+  const int n_qt = gridDim.x;
+  const int qt = n_qt - 1 - blockIdx.x;  // longest tiles first
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  const int q_begin = p.cu_seqlens_q[b];
+  const int q_len = p.cu_seqlens_q[b + 1] - q_begin;
+  const int kv_len = p.cache_seqlens[b];
+  const int u0 = qt * BM;
+  if (u0 >= q_len || q_begin < 0 || q_begin + u0 >= p.total_q) return;  // uniform
+  const int n_rows = min(BM, min(q_len - u0, p.total_q - (q_begin + u0)));
+  const int kvh = h / p.group;
+
+  // key range of the tile and its 128-key tiles
+  const int i_min = kv_len - q_len + u0;
+  const int i_max = i_min + n_rows - 1;
+  int kv_end = kv_len;
+  if (p.causal || p.window_left >= 0) kv_end = min(kv_end, i_max + 1);
+  int kv_begin = 0;
+  if (p.window_left >= 0) kv_begin = max(0, i_min - p.window_left);
+  kv_end = max(kv_end, kv_begin);
+  const int jt0 = kv_begin / BN;
+  const int n_kv = (kv_end + BN - 1) / BN - jt0;
+
+  if (tid == 0) {
+    mbar_init(bar(Q_FULL), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(K_FULL + s), 1);
+      mbar_init(bar(V_FULL + s), 1);
+      mbar_init(bar(K_EMPTY + s), 1);
+      mbar_init(bar(V_EMPTY + s), 1);
+      mbar_init(bar(S_FULL + s), 1);
+      mbar_init(bar(S_FREE + s), 4);
+      mbar_init(bar(P_FULL + s), 4);
+      mbar_init(bar(O_DONE + s), 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    fence_proxy_async();
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(
+                     smem_addr(sTmem))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+  const uint32_t tS0 = tmem, tO = tmem + 256;
+
+  if (warp == 4) {
+    // ================================ producer ================================
+    const int P = p.page_size;
+    const int pbox = P <= BN ? P : BN;
+    const int nbox = BN / pbox;
+    if (lane == 0 && n_kv > 0) {  // (no keys: nothing may stay in flight)
+      mbar_arrive_expect_tx(bar(Q_FULL), kTileBytes);
+      tma_load_3d(sbase + Smem::kQ, &maps.q, 0, h, q_begin + u0, bar(Q_FULL));
+      tma_load_3d(sbase + Smem::kQ + BM * 128, &maps.q, 64, h, q_begin + u0, bar(Q_FULL));
+    }
+    for (int jj = 0; jj < n_kv; ++jj) {
+      const int s = jj & 1;
+      const uint32_t prev = ((jj >> 1) - 1) & 1;
+      // ---- K tile (stage freed when QK of tile jj-2 completed) ----
+      if (jj >= 2 && !mbar_wait(bar(K_EMPTY + s), prev)) {
+        if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+        break;
+      }
+      const int key0 = (jt0 + jj) * BN;
+      bool box_ok = false;
+      int page = 0, inpage = 0;
+      const int bpos0 = key0 + lane * pbox;
+      if (lane < nbox && bpos0 < kv_len) {
+        const int pidx = bpos0 / P;
+        inpage = bpos0 - pidx * P;
+        if (pidx < p.pt_cols) {
+          const int64_t pg = p.page_table[static_cast<int64_t>(b) * p.pt_stride + pidx];
+          if (pg >= 0 && pg < p.num_pages) {
+            page = static_cast<int>(pg);
+            box_ok = true;
+          } else {
+            atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
+          }
+        } else {
+          atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
+        }
+      }
+      uint32_t bytes = box_ok ? static_cast<uint32_t>(pbox) * 256u : 0u;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+      const uint32_t roff = static_cast<uint32_t>(lane * pbox) * 128u;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL + s), bytes);
+      __syncwarp();
+      if (box_ok) {
+        const uint32_t kdst = sbase + Smem::kK + s * kTileBytes + roff;
+        tma_load_4d(kdst, &maps.k, 0, kvh, inpage, page, bar(K_FULL + s));
+        tma_load_4d(kdst + BN * 128, &maps.k, 64, kvh, inpage, page, bar(K_FULL + s));
+      }
+      // ---- V tile + key-validity mask (stage freed when PV of tile jj-2
+      //      completed, i.e. after the softmax of tile jj-2 read its mask) ----
+      if (jj >= 2 && !mbar_wait(bar(V_EMPTY + s), prev)) {
+        if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+        break;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane + 32 * i;
+        const int okr = __shfl_sync(0xffffffffu, box_ok ? 1 : 0, r / pbox);
+        const uint32_t bits = __ballot_sync(0xffffffffu, okr && key0 + r < kv_len);
+        if (lane == 0) sMask[s * 4 + i] = bits;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(bar(V_FULL + s), bytes);
+      __syncwarp();
+      if (box_ok) {
+        const uint32_t vdst = sbase + Smem::kV + s * kTileBytes + roff;
+        tma_load_4d(vdst, &maps.v, 0, kvh, inpage, page, bar(V_FULL + s));
+        tma_load_4d(vdst + BN * 128, &maps.v, 64, kvh, inpage, page, bar(V_FULL + s));
+      }
+    }
+  } else if (warp == 5) {
+    // ================================== MMA ==================================
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16(false);
+      constexpr uint32_t kIdescPV = idesc_bf16(true);
+      bool ok = n_kv == 0 || mbar_wait(bar(Q_FULL), 0);
+      for (int j = 0; ok && j <= n_kv; ++j) {
+        if (j < n_kv) {  // S_j = Q K_j^T
+          const int s = j & 1;
+          ok = mbar_wait(bar(K_FULL + s), (j >> 1) & 1) &&
+               (j < 2 || mbar_wait(bar(S_FREE + s), ((j >> 1) - 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t qa = sbase + Smem::kQ;
+          const uint32_t kb = sbase + Smem::kK + s * kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t koff = (ks >> 2) * (BM * 128) + (ks & 3) * 32;
+            umma(tS0 + s * 128, smem_desc(qa + koff, 0, 1024), smem_desc(kb + koff, 0, 1024),
+                 kIdescQK, ks > 0);
+          }
+          umma_commit(bar(S_FULL + s));
+          umma_commit(bar(K_EMPTY + s));
+        }
+        if (j >= 1) {  // O += P_{j-1} V_{j-1}
+          const int jj = j - 1;
+          const int s = jj & 1;
+          ok = mbar_wait(bar(P_FULL + s), (jj >> 1) & 1) &&
+               mbar_wait(bar(V_FULL + s), (jj >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t pa = sbase + Smem::kP + s * kTileBytes;
+          const uint32_t vb = sbase + Smem::kV + s * kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks) {
+            const uint32_t aoff = (ks >> 2) * (BM * 128) + (ks & 3) * 32;
+            umma(tO, smem_desc(pa + aoff, 0, 1024), smem_desc(vb + ks * 2048, BN * 128, 1024),
+                 kIdescPV, (jj > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(bar(O_DONE + s));
+          umma_commit(bar(V_EMPTY + s));
+        }
+      }
+      if (!ok) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+    }
+  } else {
+    // ================================ softmax ================================
+    const int row = tid;  // TMEM lane
+    const int u = u0 + row;
+    const int i_r = kv_len - q_len + u;
+    const bool use_upper = p.causal || p.window_left >= 0;
+    const int lo_r = p.window_left >= 0 ? i_r - p.window_left : INT_MIN;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float c = p.scale_log2;
+    float m_ref = -INFINITY;  // reference max (log2 domain) of O and l
+    float l = 0.f;
+    bool ok = true;
+
+    for (int jj = 0; jj < n_kv; ++jj) {
+      const int s = jj & 1;
+      const uint32_t ph = (jj >> 1) & 1;
+      if (!(ok = mbar_wait(bar(S_FULL + s), ph))) break;
+      tc_fence_after();
+      float x[BN];
+      tmem_ld128(tS0 + s * 128 + lane_off, x);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(S_FREE + s));  // S_jj is in registers
+
+      if (!(ok = mbar_wait(bar(V_FULL + s), ph))) break;  // key mask, V rows
+      const int key0 = (jt0 + jj) * BN;
+      uint32_t mask[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mask[i] = sMask[s * 4 + i];
+      const bool all_valid = (mask[0] & mask[1] & mask[2] & mask[3]) == 0xffffffffu;
+      const bool edge = !all_valid || (use_upper && key0 + BN - 1 > i_min) ||
+                        (p.window_left >= 0 && key0 < i_max - p.window_left);
+      if (edge) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          const int key = key0 + i;
+          const bool mk = !((mask[i >> 5] >> (i & 31)) & 1u) || (use_upper && key > i_r) ||
+                          key < lo_r;
+          x[i] = mk ? -INFINITY : x[i] * c;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) x[i] *= c;
+      }
+      // row max, eight independent chains
+      float pm[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) pm[k] = x[k];
+#pragma unroll
+      for (int i = 8; i < BN; ++i) pm[i & 7] = fmaxf(pm[i & 7], x[i]);
+      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+
+      // lazy rescale: move the reference only when the max grew by > 2^8
+      bool need = false;
+      float factor = 1.f;
+      if (mx > m_ref + 8.f) {
+        need = m_ref != -INFINITY;  // O and l hold data only then
+        factor = need ? exp2f(m_ref - mx) : 1.f;
+        m_ref = mx;
+      }
+      if (__any_sync(0xffffffffu, need)) {
+        // O holds P V of tiles 0..jj-1: wait for the last of them, scale rows
+        const int t = jj - 1;
+        if (!(ok = mbar_wait(bar(O_DONE + (t & 1)), (t >> 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          float v[32];
+          tmem_ld32(tO + lane_off + ch * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= factor;
+          tmem_st32(tO + lane_off + ch * 32, v);
+        }
+        tmem_st_wait();
+      }
+      l *= factor;
+
+      // P = exp2(x - m_ref), eight partial sums
+      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < BN; ++i) {
+        x[i] = exp2f(x[i] - mu);
+        ps[i & 7] += x[i];
+      }
+      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+
+      // P buffer s was last read by the PV of tile jj-2
+      if (jj >= 2 && !(ok = mbar_wait(bar(O_DONE + s), ((jj - 2) >> 1) & 1))) break;
+      uint8_t *pbuf = smem + Smem::kP + s * kTileBytes;
+#pragma unroll
+      for (int cc = 0; cc < BN / 8; ++cc) {
+        uint4 w;
+        w.x = pack_bf16(x[8 * cc], x[8 * cc + 1]);
+        w.y = pack_bf16(x[8 * cc + 2], x[8 * cc + 3]);
+        w.z = pack_bf16(x[8 * cc + 4], x[8 * cc + 5]);
+        w.w = pack_bf16(x[8 * cc + 6], x[8 * cc + 7]);
+        *reinterpret_cast<uint4 *>(pbuf + tile_off(row, cc)) = w;
+      }
+      // V rows of keys outside the sequence or in skipped pages must be zero
+      // (P is 0 there, but 0 * NaN would still poison the product)
+      // (this thread's own key row: word `warp` of the mask, selected
+      // without a dynamically indexed array)
+      const uint32_t own = warp == 0 ? mask[0] : warp == 1 ? mask[1] : warp == 2 ? mask[2] : mask[3];
+      if (!all_valid && !((own >> lane) & 1u)) {
+        uint8_t *vt = smem + Smem::kV + s * kTileBytes;
+#pragma unroll
+        for (int cc = 0; cc < D / 8; ++cc)
+          *reinterpret_cast<uint4 *>(vt + tile_off(row, cc)) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async();  // P (and zeroed V rows) visible to the tensor core
+      tc_fence_before();    // (and the rescaled O rows)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(P_FULL + s));
+    }
+
+    // epilogue: wait for the last PV, normalise, write bf16 row and lse
+    float o[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) o[i] = 0.f;
+    if (ok && n_kv > 0) {
+      const int t = n_kv - 1;
+      ok = mbar_wait(bar(O_DONE + (t & 1)), (t >> 1) & 1);
+      if (ok) {
+        tc_fence_after();
+        tmem_ld128(tO + lane_off, o);
+      }
+    }
+    if (!ok && lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+    if (row < n_rows) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int tok = q_begin + u;
+      bf16 *dst = p.out + static_cast<int64_t>(tok) * p.o_st + static_cast<int64_t>(h) * p.o_sh;
+#pragma unroll
+      for (int cc = 0; cc < D; cc += 8) {
+        uint4 w;
+        w.x = pack_bf16(o[cc] * inv, o[cc + 1] * inv);
+        w.y = pack_bf16(o[cc + 2] * inv, o[cc + 3] * inv);
+        w.z = pack_bf16(o[cc + 4] * inv, o[cc + 5] * inv);
+        w.w = pack_bf16(o[cc + 6] * inv, o[cc + 7] * inv);
+        *reinterpret_cast<uint4 *>(dst + cc) = w;
+      }
+      if (p.lse != nullptr)
+        p.lse[static_cast<int64_t>(tok) * p.lse_st + static_cast<int64_t>(h) * p.lse_sh] =
+            l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------- host
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    tried = true;
+  }
+  return fn;
+}
+
+bool encode(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
+            const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims,
+            strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool extend_eligible(const AttnParams &p) {
+  if (p.topk != nullptr || p.d != D || p.dv != D) return false;
+  const int P = p.page_size;
+  if (P % 8 != 0) return false;
+  if (P <= BN ? (BN % P != 0) : (P % BN != 0)) return false;
+  if (p.num_pages > 0xffffffffLL) return false;
+  auto nests = [&](int64_t sh, int64_t spos, int64_t sp) {
+    return sh >= D && spos >= sh * p.h_kv && sp >= spos * P;
+  };
+  return nests(p.k_sh, p.k_spos, p.k_sp) && nests(p.v_sh, p.v_spos, p.v_sp) &&
+         p.q_sh >= D && p.q_st >= p.q_sh * p.h_q;
+}
+
+int launch_extend_tc(const AttnParams &p, cudaStream_t stream) {
+  if (p.batch == 0 || p.total_q == 0 || p.max_seqlen_q == 0) return PKV_OK;
+  if (!extend_eligible(p)) return PKV_ERR_UNSUPPORTED;
+  const int n_qt = (p.max_seqlen_q + BM - 1) / BM;
+  if (p.h_q > 65535 || p.batch > 65535) return PKV_ERR_UNSUPPORTED;
+  ExtendMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  const int pbox = p.page_size <= BN ? p.page_size : BN;
+  {
+    cuuint64_t dims[3] = {D, static_cast<cuuint64_t>(p.h_q), static_cast<cuuint64_t>(p.total_q)};
+    cuuint64_t str[2] = {static_cast<cuuint64_t>(p.q_sh) * 2, static_cast<cuuint64_t>(p.q_st) * 2};
+    cuuint32_t box[3] = {64, 1, BM};
+    if (!encode(&maps.q, p.q, 3, dims, str, box)) return PKV_ERR_UNSUPPORTED;
+  }
+  {
+    cuuint64_t dims[4] = {D, static_cast<cuuint64_t>(p.h_kv), static_cast<cuuint64_t>(p.page_size),
+                          static_cast<cuuint64_t>(p.num_pages)};
+    cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(pbox), 1};
+    cuuint64_t sk[3] = {static_cast<cuuint64_t>(p.k_sh) * 2, static_cast<cuuint64_t>(p.k_spos) * 2,
+                        static_cast<cuuint64_t>(p.k_sp) * 2};
+    cuuint64_t sv[3] = {static_cast<cuuint64_t>(p.v_sh) * 2, static_cast<cuuint64_t>(p.v_spos) * 2,
+                        static_cast<cuuint64_t>(p.v_sp) * 2};
+    if (!encode(&maps.k, p.k, 4, dims, sk, box) || !encode(&maps.v, p.v, 4, dims, sv, box))
+      return PKV_ERR_UNSUPPORTED;
+  }
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev < 64 && !configured[dev]) {
+    if (cudaFuncSetAttribute(extend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Smem::kDynamic)) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    configured[dev] = true;
+  }
+  dim3 grid(n_qt, p.h_q, p.batch);
+  extend_tc_kernel<<<grid, NTHREADS, Smem::kDynamic, stream>>>(p, maps);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace pkv

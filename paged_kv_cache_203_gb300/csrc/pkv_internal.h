@@ -60,6 +60,11 @@ uint32_t *device_error_word();
 int launch_decode_gqa(const AttnParams &p, cudaStream_t stream);
 // Rows per (request, kv head) tile used by the decode kernel.
 constexpr int kDecodeRowTile = 16;
+// tcgen05 varlen extend kernel (head dim 128, whole-page TMA boxes).
+bool extend_eligible(const AttnParams &p);
+int launch_extend_tc(const AttnParams &p, cudaStream_t stream);
+// Query-run length from which the extend kernel serves a call.
+constexpr int kExtendMinSeqlenQ = 64;
 
 int launch_merge_state(const void *va, const void *vb, void *vo, int v_dtype,
                        int o_dtype, int64_t n, int h, int d, int64_t va_sn,

@@ -471,3 +471,62 @@ def test_head_major_cache_layout():
     out, lse = gpu_attn(g, num_splits=2)
     ref_o, ref_l, _ = oracle_attn(wl)
     check_close(out, lse, ref_o, ref_l, "head-major")
+
+
+# ------------------------------------------------ varlen extend (tcgen05 path)
+
+@pytest.mark.parametrize("page_size,window,causal", [
+    (64, -1, True), (16, -1, True), (128, -1, True), (64, 300, True), (64, -1, False),
+])
+def test_varlen_extend_reduced(page_size, window, causal):
+    """Varlen causal extend recipe (32/8 heads, D 128) at oracle-friendly
+    size: 4 requests, new U[64, 700] on a prefix U[0, 900] (ragged q tiles,
+    prefix 0 allowed)."""
+    wl = workloads.make("varlen_extend", batch=4, new_lo=64, new_hi=700, prefix_lo=0,
+                        prefix_hi=900, page_size=page_size,
+                        pool_pages=4 * (1600 // page_size + 2) + 8, window_left=window)
+    wl.causal = causal
+    g = wl.to(DEV)
+    out, lse = gpu_attn(g)
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, f"extend P={page_size} w={window} c={causal}")
+    assert pkv.get_error_flags() == 0
+
+
+def test_varlen_extend_garbage_and_bad_pages():
+    """Extend with NaN everywhere outside the requests' valid rows, plus an
+    out-of-pool page id: the bad page's keys are skipped and flagged,
+    nothing else changes."""
+    P = 64
+    wl = workloads.make("varlen_extend", batch=3, new_lo=100, new_hi=400, prefix_lo=50,
+                        prefix_hi=600, page_size=P, pool_pages=3 * 17 + 10)
+    valid = torch.zeros(wl.k_cache.shape[0] * P, dtype=torch.bool)
+    for b in range(3):
+        j = torch.arange(int(wl.cache_seqlens[b]))
+        valid[wl.page_table[b, j // P].long() * P + j % P] = True
+    valid = valid.view(-1, P)
+    wl.k_cache[~valid] = float("nan")
+    wl.v_cache[~valid] = float("nan")
+    wl.page_table[1, 1] = 1 << 30
+    g = wl.to(DEV)
+    out, lse = gpu_attn(g)
+    ref_o, ref_l, skipped = oracle_attn(wl)
+    assert skipped > 0
+    check_close(out, lse, ref_o, ref_l, "extend garbage/bad page")
+    assert pkv.get_error_flags() & pkv.EFLAG_PAGE_OOB
+
+
+def test_varlen_extend_full_size_sampled():
+    """Full varlen extend workload (batch 8, new U[128, 2048], prefix
+    U[0, 4096], page 64) as the bench runs it; sampled rows."""
+    g = workloads.make("varlen_extend", value_device=DEV)
+    out, lse = gpu_attn(g)
+    rows = _sample_rows(g.q.shape[0], g.q.shape[1], 96, 3)
+    ref_o, ref_l, _ = oracle.attention(
+        oracle.bf16_bits(g.q), oracle.bf16_bits(g.k_cache), oracle.bf16_bits(g.v_cache),
+        g.page_table.cpu().numpy(), g.cache_seqlens.cpu().numpy(),
+        g.cu_seqlens_q.cpu().numpy(), g.scale, causal=True, rows=rows)
+    idx = torch.from_numpy(rows).long()
+    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
+                ref_o, ref_l, "extend full-size sampled")
+    assert pkv.get_error_flags() == 0
