@@ -59,7 +59,8 @@ enum pkv_error_bits {
   PKV_EFLAG_TOPK_OOB = 2,    /* top-k index < -1 or >= kv_len: entry skipped */
   PKV_EFLAG_ROW_TOO_SHORT = 4, /* page-table / dst row narrower than needed */
   PKV_EFLAG_SRC_OOB = 8,     /* req_to_token column or pool row out of range */
-  PKV_EFLAG_TIMEOUT = 16     /* a bounded in-kernel wait expired (work dropped) */
+  PKV_EFLAG_TIMEOUT = 16,    /* a bounded in-kernel wait expired (work dropped) */
+  PKV_EFLAG_LAYOUT = 32      /* shared memory not aligned as a kernel needs (work dropped) */
 };
 
 typedef struct pkv_tensor {

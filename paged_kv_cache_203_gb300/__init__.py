@@ -49,6 +49,7 @@ __all__ = [
     "EFLAG_ROW_TOO_SHORT",
     "EFLAG_SRC_OOB",
     "EFLAG_TIMEOUT",
+    "EFLAG_LAYOUT",
 ]
 
 # dtype codes and status codes of include/pkv.h
@@ -57,6 +58,7 @@ _STATUS = {0: "PKV_OK", -1: "PKV_ERR_INVALID_ARG", -2: "PKV_ERR_UNSUPPORTED",
            -3: "PKV_ERR_CUDA", -4: "PKV_ERR_WORKSPACE"}
 EFLAG_PAGE_OOB, EFLAG_TOPK_OOB, EFLAG_ROW_TOO_SHORT, EFLAG_SRC_OOB = 1, 2, 4, 8
 EFLAG_TIMEOUT = 16
+EFLAG_LAYOUT = 32
 
 EXPORTED_SYMBOLS = (
     "pkv_attn_with_kvcache",

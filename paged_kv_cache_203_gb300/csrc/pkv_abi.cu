@@ -261,9 +261,10 @@ int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
   }
   if (p.total_q == 0) return PKV_OK;
   if (plan.kind == 1) {
-    rc = launch_extend_tc(p, stream);
+    // the extend kernel takes row maxima of raw scores: positive scale only
+    rc = scale > 0.f ? launch_extend_tc(p, stream) : PKV_ERR_UNSUPPORTED;
     if (rc != PKV_ERR_UNSUPPORTED) return rc;
-    p.num_splits = 1;  // tensor maps not encodable: unsplit decode kernel
+    p.num_splits = 1;  // otherwise the unsplit decode kernel (no workspace)
   }
   return launch_decode_gqa(p, stream);
 }

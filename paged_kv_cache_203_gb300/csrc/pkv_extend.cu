@@ -8,20 +8,22 @@
 //
 // One CTA = one tile of 128 consecutive new tokens of one request for one q
 // head; its keys stream in 128-key tiles (whole page boxes).
-//   warp 4  producer: TMA loads of the Q tile once, then K and V tiles into
+//   warp 8  producer: TMA loads of the Q tile once, then K and V tiles into
 //           two 2-stage rings (4-D tensor-map boxes per page and 64-column
 //           half, 128-byte swizzle), plus a per-tile key-validity bitmask;
-//   warp 5  MMA issuer (one thread): S_j = Q K_j^T into TMEM buffer j%2,
+//   warp 9  MMA issuer (one thread): S_j = Q K_j^T into TMEM buffer j%2,
 //           then O += P_{j-1} V_{j-1} into the TMEM accumulator, each a chain
 //           of eight 128x128x16 bf16 MMAs with fp32 accumulation; completion
 //           signalled with tcgen05.commit on mbarriers (a K stage is released
 //           when its QK^T is done, a V stage when its PV is done);
-//   warps 0-3 softmax (thread = query row = TMEM lane): one 128-column TMEM
-//           load of S_j, online softmax in the log2 domain with a lazy
-//           reference max (O and l are rescaled in place only when the row
-//           max grows by more than 2^8), P_j (bf16) written to shared memory
-//           as the A operand of the PV MMA; V rows of keys past the sequence
-//           or in skipped pages are zeroed.
+//   warps 0-7 softmax: warps w and w+4 share TMEM lane quadrant w (query
+//           rows 32w..32w+31) and split each row's 128 key columns in two
+//           halves; partial row maxima are exchanged through shared memory.
+//           Online softmax in the log2 domain with a lazy reference max (O and
+//           l are rescaled in place only when the row max grows by more than
+//           2^8), P_j (bf16) written to shared memory as the A operand of the
+//           PV MMA; V rows of keys past the sequence or in skipped pages are
+//           zeroed.
 // TMEM: S0 | S1 | O (128 columns each; 512 allocated, 1 CTA per SM).
 // Every mbarrier wait is bounded (PKV_EFLAG_TIMEOUT on expiry).
 #include <cuda.h>
@@ -36,7 +38,11 @@ namespace {
 constexpr int BM = 128;           // query rows per CTA
 constexpr int BN = 128;           // keys per tile
 constexpr int D = 128;            // head dim (q/k and v)
-constexpr int NTHREADS = 192;     // 4 softmax warps, producer, MMA
+constexpr int NSM_WARPS = 8;      // softmax warps: 2 per TMEM lane quadrant
+constexpr int NTHREADS = NSM_WARPS * 32 + 64;  // + producer warp, MMA warp
+constexpr int kProducerWarp = NSM_WARPS;
+constexpr int kMmaWarp = NSM_WARPS + 1;
+constexpr int HALF = BN / 2;      // S / P / O columns per softmax thread
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr uint32_t kTileBytes = BM * D * 2;  // 32 KB, any 128x128 bf16 tile
 
@@ -46,19 +52,22 @@ struct Smem {
   static constexpr uint32_t kV = kK + 2 * kTileBytes;   // 2 stages
   static constexpr uint32_t kP = kV + 2 * kTileBytes;   // 2 buffers
   static constexpr uint32_t kMask = kP + 2 * kTileBytes;  // uint32 [2][4]
-  static constexpr uint32_t kBar = kMask + 32;
+  static constexpr uint32_t kXchg = kMask + 32;  // float [2 parities][2 halves][128 rows]
+  static constexpr uint32_t kBar = kXchg + 2 * 2 * BM * 4;
   // barriers: q_full, k_full[2], v_full[2], k_empty[2], v_empty[2],
-  //           s_full[2], s_free[2], p_full[2], o_done[2]
-  static constexpr int kNumBars = 17;
+  //           s_full[2], s_free[2], p_full[2], o_done[2], xchg[2]
+  static constexpr int kNumBars = 19;
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kEnd = kTmemSlot + 16;
-  static constexpr size_t kDynamic = kEnd + 1024;
+  // The dynamic shared memory base must be 1024-byte aligned (128-byte
+  // swizzle atoms); the kernel checks it and does no work otherwise.
+  static constexpr size_t kDynamic = kEnd;
 };
 static_assert(Smem::kDynamic <= 232448, "shared memory plan exceeds 227 KB");
 
 enum BarId {
   Q_FULL = 0, K_FULL = 1, V_FULL = 3, K_EMPTY = 5, V_EMPTY = 7, S_FULL = 9, S_FREE = 11,
-  P_FULL = 13, O_DONE = 15
+  P_FULL = 13, O_DONE = 15, XCHG = 17
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -194,6 +203,23 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
 #pragma unroll
   for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : PKV_O64(0)
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 2^x on the MUFU (PTX ex2.approx, flush-to-zero; 2^-inf = 0)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   uint32_t r[32];
 #pragma unroll
@@ -210,9 +236,8 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ ExtendMaps maps) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw;
   const uint32_t sbase = smem_addr(smem);
   uint32_t *sMask = reinterpret_cast<uint32_t *>(smem + Smem::kMask);
   uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + Smem::kTmemSlot);
@@ -231,6 +256,10 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
   const int kv_len = p.cache_seqlens[b];
   const int u0 = qt * BM;
   if (u0 >= q_len || q_begin < 0 || q_begin + u0 >= p.total_q) return;  // uniform
+  if ((sbase & 1023u) != 0) {  // layout assumption violated: refuse, flag
+    if (tid == 0) atomicOr(p.err, PKV_EFLAG_LAYOUT);
+    return;
+  }
   const int n_rows = min(BM, min(q_len - u0, p.total_q - (q_begin + u0)));
   const int kvh = h / p.group;
 
@@ -253,14 +282,15 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       mbar_init(bar(K_EMPTY + s), 1);
       mbar_init(bar(V_EMPTY + s), 1);
       mbar_init(bar(S_FULL + s), 1);
-      mbar_init(bar(S_FREE + s), 4);
-      mbar_init(bar(P_FULL + s), 4);
+      mbar_init(bar(S_FREE + s), NSM_WARPS);
+      mbar_init(bar(P_FULL + s), NSM_WARPS);
       mbar_init(bar(O_DONE + s), 1);
+      mbar_init(bar(XCHG + s), NSM_WARPS);
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     fence_proxy_async();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(
                      smem_addr(sTmem))
                  : "memory");
@@ -272,7 +302,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
   const uint32_t tmem = *sTmem;
   const uint32_t tS0 = tmem, tO = tmem + 256;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ================================ producer ================================
     const int P = p.page_size;
     const int pbox = P <= BN ? P : BN;
@@ -343,7 +373,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
         tma_load_4d(vdst + BN * 128, &maps.v, 64, kvh, inpage, page, bar(V_FULL + s));
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ================================== MMA ==================================
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16(false);
@@ -390,15 +420,19 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
     }
   } else {
     // ================================ softmax ================================
-    const int row = tid;  // TMEM lane
+    const int quad = warp & 3;               // TMEM lane quadrant
+    const int hf = warp >> 2;                // which 64 key columns
+    const int row = quad * 32 + lane;        // query row = TMEM lane
     const int u = u0 + row;
     const int i_r = kv_len - q_len + u;
     const bool use_upper = p.causal || p.window_left >= 0;
     const int lo_r = p.window_left >= 0 ? i_r - p.window_left : INT_MIN;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const float c = p.scale_log2;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t col0 = hf * HALF;
+    const float c = p.scale_log2;  // > 0 on this path
+    float *xchg = reinterpret_cast<float *>(smem + Smem::kXchg);  // [2][2][128]
     float m_ref = -INFINITY;  // reference max (log2 domain) of O and l
-    float l = 0.f;
+    float l = 0.f;            // this half's share of the row sum
     bool ok = true;
 
     for (int jj = 0; jj < n_kv; ++jj) {
@@ -406,72 +440,74 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       const uint32_t ph = (jj >> 1) & 1;
       if (!(ok = mbar_wait(bar(S_FULL + s), ph))) break;
       tc_fence_after();
-      float x[BN];
-      tmem_ld128(tS0 + s * 128 + lane_off, x);
+      float x[HALF];
+      tmem_ld64(tS0 + s * 128 + col0 + lane_off, x);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(S_FREE + s));  // S_jj is in registers
 
       if (!(ok = mbar_wait(bar(V_FULL + s), ph))) break;  // key mask, V rows
-      const int key0 = (jt0 + jj) * BN;
-      uint32_t mask[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) mask[i] = sMask[s * 4 + i];
-      const bool all_valid = (mask[0] & mask[1] & mask[2] & mask[3]) == 0xffffffffu;
-      const bool edge = !all_valid || (use_upper && key0 + BN - 1 > i_min) ||
-                        (p.window_left >= 0 && key0 < i_max - p.window_left);
+      const int key0 = (jt0 + jj) * BN + col0;  // key of this thread's column 0
+      const uint32_t mk0 = sMask[s * 4 + 2 * hf], mk1 = sMask[s * 4 + 2 * hf + 1];
+      const uint32_t m_all = sMask[s * 4] & sMask[s * 4 + 1] & sMask[s * 4 + 2] & sMask[s * 4 + 3];
+      const bool all_valid = m_all == 0xffffffffu;
+      const int tile_key0 = (jt0 + jj) * BN;
+      const bool edge = !all_valid || (use_upper && tile_key0 + BN - 1 > i_min) ||
+                        (p.window_left >= 0 && tile_key0 < i_max - p.window_left);
       if (edge) {
 #pragma unroll
-        for (int i = 0; i < BN; ++i) {
+        for (int i = 0; i < HALF; ++i) {
           const int key = key0 + i;
-          const bool mk = !((mask[i >> 5] >> (i & 31)) & 1u) || (use_upper && key > i_r) ||
-                          key < lo_r;
-          x[i] = mk ? -INFINITY : x[i] * c;
+          const uint32_t w = i < 32 ? mk0 : mk1;
+          const bool msk = !((w >> (i & 31)) & 1u) || (use_upper && key > i_r) || key < lo_r;
+          x[i] = msk ? -INFINITY : x[i];
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < BN; ++i) x[i] *= c;
       }
-      // row max, eight independent chains
+      // partial row max (raw scores), eight chains; exchange with the other half
       float pm[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) pm[k] = x[k];
 #pragma unroll
-      for (int i = 8; i < BN; ++i) pm[i & 7] = fmaxf(pm[i & 7], x[i]);
-      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      for (int i = 8; i < HALF; ++i) pm[i & 7] = fmaxf(pm[i & 7], x[i]);
+      float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      xchg[(s * 2 + hf) * BM + row] = mx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(XCHG + s));
+      if (!(ok = mbar_wait(bar(XCHG + s), ph))) break;
+      mx = fmaxf(mx, xchg[(s * 2 + (hf ^ 1)) * BM + row]) * c;
 
       // lazy rescale: move the reference only when the max grew by > 2^8
       bool need = false;
       float factor = 1.f;
       if (mx > m_ref + 8.f) {
         need = m_ref != -INFINITY;  // O and l hold data only then
-        factor = need ? exp2f(m_ref - mx) : 1.f;
+        factor = need ? fast_exp2(m_ref - mx) : 1.f;
         m_ref = mx;
       }
       if (__any_sync(0xffffffffu, need)) {
-        // O holds P V of tiles 0..jj-1: wait for the last of them, scale rows
+        // O holds P V of tiles 0..jj-1: wait for the last of them, scale
         const int t = jj - 1;
         if (!(ok = mbar_wait(bar(O_DONE + (t & 1)), (t >> 1) & 1))) break;
         tc_fence_after();
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
+        for (int ch = 0; ch < HALF / 32; ++ch) {
           float v[32];
-          tmem_ld32(tO + lane_off + ch * 32, v);
+          tmem_ld32(tO + lane_off + col0 + ch * 32, v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= factor;
-          tmem_st32(tO + lane_off + ch * 32, v);
+          tmem_st32(tO + lane_off + col0 + ch * 32, v);
         }
         tmem_st_wait();
       }
       l *= factor;
 
-      // P = exp2(x - m_ref), eight partial sums
+      // P = 2^(x c - m_ref): one FFMA + one MUFU per element, eight sums
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
       float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < BN; ++i) {
-        x[i] = exp2f(x[i] - mu);
+      for (int i = 0; i < HALF; ++i) {
+        x[i] = fast_exp2(fmaf(x[i], c, -mu));
         ps[i & 7] += x[i];
       }
       l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
@@ -480,50 +516,63 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       if (jj >= 2 && !(ok = mbar_wait(bar(O_DONE + s), ((jj - 2) >> 1) & 1))) break;
       uint8_t *pbuf = smem + Smem::kP + s * kTileBytes;
 #pragma unroll
-      for (int cc = 0; cc < BN / 8; ++cc) {
+      for (int cc = 0; cc < HALF / 8; ++cc) {
         uint4 w;
         w.x = pack_bf16(x[8 * cc], x[8 * cc + 1]);
         w.y = pack_bf16(x[8 * cc + 2], x[8 * cc + 3]);
         w.z = pack_bf16(x[8 * cc + 4], x[8 * cc + 5]);
         w.w = pack_bf16(x[8 * cc + 6], x[8 * cc + 7]);
-        *reinterpret_cast<uint4 *>(pbuf + tile_off(row, cc)) = w;
+        *reinterpret_cast<uint4 *>(pbuf + tile_off(row, hf * 8 + cc)) = w;
       }
       // V rows of keys outside the sequence or in skipped pages must be zero
-      // (P is 0 there, but 0 * NaN would still poison the product)
-      // (this thread's own key row: word `warp` of the mask, selected
-      // without a dynamically indexed array)
-      const uint32_t own = warp == 0 ? mask[0] : warp == 1 ? mask[1] : warp == 2 ? mask[2] : mask[3];
+      // (P is 0 there, but 0 * NaN would still poison the product); key row
+      // `row` of the tile, this thread's half of its columns
+      const uint32_t own = quad == 0 ? sMask[s * 4] : quad == 1 ? sMask[s * 4 + 1]
+                         : quad == 2 ? sMask[s * 4 + 2] : sMask[s * 4 + 3];
       if (!all_valid && !((own >> lane) & 1u)) {
         uint8_t *vt = smem + Smem::kV + s * kTileBytes;
 #pragma unroll
-        for (int cc = 0; cc < D / 8; ++cc)
-          *reinterpret_cast<uint4 *>(vt + tile_off(row, cc)) = make_uint4(0, 0, 0, 0);
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4 *>(vt + tile_off(row, hf * 8 + cc)) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async();  // P (and zeroed V rows) visible to the tensor core
-      tc_fence_before();    // (and the rescaled O rows)
+      tc_fence_before();    // (and the rescaled O columns)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(P_FULL + s));
     }
 
-    // epilogue: wait for the last PV, normalise, write bf16 row and lse
-    float o[D];
+    // epilogue: wait for the last PV, combine the two halves' sums,
+    // normalise this half of the row, write bf16 and lse
+    float o[HALF];
 #pragma unroll
-    for (int i = 0; i < D; ++i) o[i] = 0.f;
+    for (int i = 0; i < HALF; ++i) o[i] = 0.f;
     if (ok && n_kv > 0) {
       const int t = n_kv - 1;
       ok = mbar_wait(bar(O_DONE + (t & 1)), (t >> 1) & 1);
       if (ok) {
         tc_fence_after();
-        tmem_ld128(tO + lane_off, o);
+        tmem_ld64(tO + lane_off + col0, o);
       }
+    }
+    // the halves' sums meet in the exchange slots of parity n_kv & 1, whose
+    // previous contents (tile n_kv - 2) both halves have read by now
+    float l_tot = l;
+    if (ok) {
+      const int ps_ = n_kv & 1;
+      xchg[(ps_ * 2 + hf) * BM + row] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(XCHG + ps_));
+      ok = mbar_wait(bar(XCHG + ps_), (n_kv >> 1) & 1);
+      if (ok) l_tot += xchg[(ps_ * 2 + (hf ^ 1)) * BM + row];
     }
     if (!ok && lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
     if (row < n_rows) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
       const int tok = q_begin + u;
-      bf16 *dst = p.out + static_cast<int64_t>(tok) * p.o_st + static_cast<int64_t>(h) * p.o_sh;
+      bf16 *dst = p.out + static_cast<int64_t>(tok) * p.o_st + static_cast<int64_t>(h) * p.o_sh +
+                  col0;
 #pragma unroll
-      for (int cc = 0; cc < D; cc += 8) {
+      for (int cc = 0; cc < HALF; cc += 8) {
         uint4 w;
         w.x = pack_bf16(o[cc] * inv, o[cc + 1] * inv);
         w.y = pack_bf16(o[cc + 2] * inv, o[cc + 3] * inv);
@@ -531,15 +580,15 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
         w.w = pack_bf16(o[cc + 6] * inv, o[cc + 7] * inv);
         *reinterpret_cast<uint4 *>(dst + cc) = w;
       }
-      if (p.lse != nullptr)
+      if (p.lse != nullptr && hf == 0)
         p.lse[static_cast<int64_t>(tok) * p.lse_st + static_cast<int64_t>(h) * p.lse_sh] =
-            l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+            l_tot > 0.f ? (m_ref + log2f(l_tot)) * kLn2 : -INFINITY;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem)
                  : "memory");

@@ -530,3 +530,15 @@ def test_varlen_extend_full_size_sampled():
     check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
                 ref_o, ref_l, "extend full-size sampled")
     assert pkv.get_error_flags() == 0
+
+
+def test_extend_shapes_with_negative_scale_use_the_decode_path():
+    """A non-positive softmax scale is served (by the decode kernel) with the
+    same results as the oracle."""
+    wl = workloads.make("varlen_extend", batch=2, new_lo=64, new_hi=200, prefix_hi=300,
+                        pool_pages=40)
+    wl.scale = -0.05
+    g = wl.to(DEV)
+    out, lse = gpu_attn(g)
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, "negative scale")
