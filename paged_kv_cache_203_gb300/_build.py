@@ -21,6 +21,7 @@ SOURCES = [
     "pkv_merge.cu",
     "pkv_decode.cu",
     "pkv_extend.cu",
+    "pkv_mla.cu",
     "pkv_noalloc.cu",
 ]
 

@@ -5,9 +5,38 @@
 
 #include <algorithm>
 
+#include <cuda.h>
+
 #include "pkv_internal.h"
+#include "pkv_ptx.cuh"
 
 namespace pkv {
+
+bool encode_tensor_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
+                       const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+  using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                     const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                     const cuuint32_t *, CUtensorMapInterleave,
+                                     CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                     CUtensorMapFloatOOBfill);
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    tried = true;
+  }
+  if (fn == nullptr) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims,
+            strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
 
 // Sticky device error word (one per device that loads the library).
 static __device__ uint32_t g_error_word;
@@ -50,7 +79,7 @@ bool vec_ok(const pkv_tensor &t, int elem_bytes) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct AttnPlan {
-  int kind;          // 0 = decode-gqa kernel, 1 = tcgen05 extend kernel
+  int kind;          // 0 = decode-gqa, 1 = tcgen05 extend, 2 = tcgen05 MLA top-k
   int num_splits;
   int n_row_tiles;
   size_t ws_o_bytes, ws_lse_bytes, ws_ctr_bytes;
@@ -88,6 +117,29 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
   if (total_q > 0x7fffffffLL || batch > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
 
   const int group = static_cast<int>(h_q / h_kv);
+  const bool mla = d == 576 && dv == 512;
+  if (mla) {
+    // absorbed MLA over top-k lists: 128 heads, one latent head, V = the
+    // first 512 columns of the K rows (same buffer and row strides)
+    if (!present(topk) || h_q != 128 || h_kv != 1 || v.data != k.data ||
+        v.stride[0] != k.stride[0] || v.stride[1] != k.stride[1])
+      return PKV_ERR_UNSUPPORTED;
+    plan->kind = 2;
+    plan->n_row_tiles = 0;
+    int splits = num_splits;
+    if (splits == 0) {  // about three waves of one-CTA-per-SM work
+      const int64_t base = std::max<int64_t>(1, total_q * 2);
+      splits = static_cast<int>((3LL * kNumSMs + base - 1) / base);
+      splits = std::max(1, std::min<int>(splits, static_cast<int>(topk.shape[1] / 256)));
+    }
+    splits = std::min(splits, kMlaMaxSplits);
+    plan->num_splits = splits;
+    const size_t rows_total = static_cast<size_t>(total_q) * h_q;
+    plan->ws_o_bytes = align256(static_cast<size_t>(splits) * rows_total * dv * 4);
+    plan->ws_lse_bytes = align256(2 * static_cast<size_t>(splits) * rows_total * 4);
+    plan->ws_ctr_bytes = align256(static_cast<size_t>(total_q) * 2 * 4);
+    return PKV_OK;
+  }
   if (!((d == 128 && dv == 128) || (d == 64 && dv == 64)))
     return PKV_ERR_UNSUPPORTED;
 
@@ -260,6 +312,7 @@ int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
       return PKV_ERR_CUDA;
   }
   if (p.total_q == 0) return PKV_OK;
+  if (plan.kind == 2) return launch_mla_topk(p, stream);
   if (plan.kind == 1) {
     // the extend kernel takes row maxima of raw scores: positive scale only
     rc = scale > 0.f ? launch_extend_tc(p, stream) : PKV_ERR_UNSUPPORTED;

@@ -31,6 +31,7 @@
 #include <string.h>
 
 #include "pkv_internal.h"
+#include "pkv_ptx.cuh"
 
 namespace pkv {
 namespace {
@@ -597,38 +598,6 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
 
 // ------------------------------------------------------------------- host
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                   CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    tried = true;
-  }
-  return fn;
-}
-
-bool encode(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
-            const cuuint64_t *strides_bytes, const cuuint32_t *box) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims,
-            strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
-
 }  // namespace
 
 bool extend_eligible(const AttnParams &p) {
@@ -656,7 +625,7 @@ int launch_extend_tc(const AttnParams &p, cudaStream_t stream) {
     cuuint64_t dims[3] = {D, static_cast<cuuint64_t>(p.h_q), static_cast<cuuint64_t>(p.total_q)};
     cuuint64_t str[2] = {static_cast<cuuint64_t>(p.q_sh) * 2, static_cast<cuuint64_t>(p.q_st) * 2};
     cuuint32_t box[3] = {64, 1, BM};
-    if (!encode(&maps.q, p.q, 3, dims, str, box)) return PKV_ERR_UNSUPPORTED;
+    if (!encode_tensor_map(&maps.q, p.q, 3, dims, str, box)) return PKV_ERR_UNSUPPORTED;
   }
   {
     cuuint64_t dims[4] = {D, static_cast<cuuint64_t>(p.h_kv), static_cast<cuuint64_t>(p.page_size),
@@ -666,7 +635,8 @@ int launch_extend_tc(const AttnParams &p, cudaStream_t stream) {
                         static_cast<cuuint64_t>(p.k_sp) * 2};
     cuuint64_t sv[3] = {static_cast<cuuint64_t>(p.v_sh) * 2, static_cast<cuuint64_t>(p.v_spos) * 2,
                         static_cast<cuuint64_t>(p.v_sp) * 2};
-    if (!encode(&maps.k, p.k, 4, dims, sk, box) || !encode(&maps.v, p.v, 4, dims, sv, box))
+    if (!encode_tensor_map(&maps.k, p.k, 4, dims, sk, box) ||
+        !encode_tensor_map(&maps.v, p.v, 4, dims, sv, box))
       return PKV_ERR_UNSUPPORTED;
   }
   static bool configured[64] = {false};

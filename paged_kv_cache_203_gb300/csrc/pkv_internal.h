@@ -65,6 +65,10 @@ bool extend_eligible(const AttnParams &p);
 int launch_extend_tc(const AttnParams &p, cudaStream_t stream);
 // Query-run length from which the extend kernel serves a call.
 constexpr int kExtendMinSeqlenQ = 64;
+// tcgen05 absorbed-MLA top-k kernel (128 heads, 576 / 512 dims, one latent
+// head; grid = splits x 2 value halves x tokens).
+int launch_mla_topk(const AttnParams &p, cudaStream_t stream);
+constexpr int kMlaMaxSplits = 64;
 
 int launch_merge_state(const void *va, const void *vb, void *vo, int v_dtype,
                        int o_dtype, int64_t n, int h, int d, int64_t va_sn,

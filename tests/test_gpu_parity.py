@@ -542,3 +542,57 @@ def test_extend_shapes_with_negative_scale_use_the_decode_path():
     out, lse = gpu_attn(g)
     ref_o, ref_l, _ = oracle_attn(wl)
     check_close(out, lse, ref_o, ref_l, "negative scale")
+
+
+# --------------------------------------------- MLA top-k sparse decode (tcgen05)
+
+def _mla_reduced(batch=6, kv_len=1500, topk=600, seed=None):
+    return workloads.make("mla_topk_decode", batch=batch, kv_len=kv_len, topk=topk,
+                          pool_pages=batch * (kv_len // 64 + 1) + 4, seed=seed)
+
+
+@pytest.mark.parametrize("num_splits", [1, 2, 0, 5])
+def test_mla_topk_decode_reduced(num_splits):
+    """Absorbed MLA (128 heads, 576/512, one latent head, page 64) over
+    top-k lists with -1 padding and a duplicate, against the oracle."""
+    wl = _mla_reduced()
+    wl.topk_indices[:, -37:] = -1
+    wl.topk_indices[2, 5] = wl.topk_indices[2, 6]  # a duplicate counts twice
+    g = wl.to(DEV)
+    out, lse = gpu_attn(g, num_splits=num_splits)
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, f"mla splits={num_splits}")
+    assert pkv.get_error_flags() == 0
+
+
+def test_mla_topk_bad_indices_and_empty_rows():
+    """Out-of-range top-k entries are skipped and flagged; a row of only -1
+    gives out 0 / lse -inf."""
+    wl = _mla_reduced(batch=4, kv_len=700, topk=256)
+    wl.topk_indices[1, 3] = 700          # == kv_len
+    wl.topk_indices[1, 9] = -4           # below -1
+    wl.topk_indices[3, :] = -1           # nothing to attend
+    g = wl.to(DEV)
+    out, lse = gpu_attn(g, num_splits=2)
+    ref_o, ref_l, skipped = oracle_attn(wl)
+    assert skipped == 2
+    check_close(out, lse, ref_o, ref_l, "mla bad indices")
+    assert torch.all(out[3] == 0) and torch.all(torch.isneginf(lse[3]))
+    assert pkv.get_error_flags() & pkv.EFLAG_TOPK_OOB
+
+
+def test_mla_topk_full_size_sampled():
+    """Full MLA top-k workload (batch 128, kv_len 8192, top-k 2048) in the
+    bench's launch configuration; 96 sampled (token, head) rows."""
+    g = workloads.make("mla_topk_decode", value_device=DEV)
+    out, lse = gpu_attn(g)
+    rows = _sample_rows(g.q.shape[0], g.q.shape[1], 96, 4)
+    kb = oracle.bf16_bits(g.k_cache)
+    ref_o, ref_l, _ = oracle.attention(
+        oracle.bf16_bits(g.q), kb, kb, g.page_table.cpu().numpy(),
+        g.cache_seqlens.cpu().numpy(), g.cu_seqlens_q.cpu().numpy(), g.scale,
+        topk=g.topk_indices.cpu().numpy(), rows=rows, d_v=512)
+    idx = torch.from_numpy(rows).long()
+    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
+                ref_o, ref_l, "mla full-size sampled")
+    assert pkv.get_error_flags() == 0
