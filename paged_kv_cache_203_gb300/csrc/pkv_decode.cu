@@ -49,6 +49,7 @@ constexpr int NCW = 4;          // consumer warps
 constexpr int NCT = NCW * 32;   // consumer threads
 constexpr int ROWS = kDecodeRowTile;  // 16
 constexpr uint32_t kWaitLimit = 1u << 24;  // bounded mbarrier polls
+constexpr int kPrefetchStages = 3;         // cp.async loader: L2 prefetch distance
 
 // ------------------------------------------------------------ PTX helpers
 
@@ -111,6 +112,10 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// Warm L2 with a contiguous global range (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
@@ -209,7 +214,9 @@ struct Smem {
   static constexpr uint32_t kM = kBar + 2 * NSTAGE * 8;      // float [NCW][16]
   static constexpr uint32_t kL = kM + NCW * ROWS * 4;
   static constexpr uint32_t kFlag = kL + NCW * ROWS * 4;
-  static constexpr uint32_t kEnd = kFlag + 16;
+  static constexpr uint32_t kProdFlag = kFlag + 4;            // producers: stage free
+  static constexpr uint32_t kOff = kFlag + 16;                // int64 [NSTAGE][BK][2]
+  static constexpr uint32_t kEnd = kOff + NSTAGE * BK * 16;
   static constexpr size_t kDynamic = kEnd + 1024;  // + alignment slack
   static_assert(NCW * ROWS * (D + 4) * 4 <= 2 * NSTAGE * kStage,
                 "epilogue buffer must fit in the stage buffers");
@@ -306,12 +313,26 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
   if (warp >= NCW) {
     // ================================ producer ================================
     const int ptid = tid - NCT;
+    volatile int *sProdFlag = reinterpret_cast<volatile int *>(smem + S::kProdFlag);
     for (int kt = 0; kt < n_kt; ++kt) {
       const int st = kt % NSTAGE;
       const uint32_t full = full0 + 8 * st;
-      if (kt >= NSTAGE && !mbar_wait(empty0 + 8 * st, ((kt / NSTAGE) & 1) ^ 1)) {
-        if ((ptid & 31) == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
-        break;
+      if constexpr (TMA) {
+        if (kt >= NSTAGE && !mbar_wait(empty0 + 8 * st, ((kt / NSTAGE) & 1) ^ 1)) {
+          if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+          break;
+        }
+      } else {
+        // one thread waits for the stage; all producer threads meet at the
+        // barrier and leave together on a timeout (no one is left behind
+        // at a named barrier)
+        if (ptid == 0) {
+          const bool free_ok = kt < NSTAGE || mbar_wait(empty0 + 8 * st, ((kt / NSTAGE) & 1) ^ 1);
+          if (!free_ok) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+          *sProdFlag = free_ok ? 1 : 0;
+        }
+        asm volatile("bar.sync 2, %0;\n" ::"n"(NPROD * 32) : "memory");
+        if (*sProdFlag == 0) break;
       }
       const int base = (t0 + kt) * BK;  // absolute key (or list) index of row 0
       const uint32_t kdst = sbase + S::kK + st * S::kStage;
@@ -363,50 +384,64 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
           }
         }
       } else {
-        // cp.async gather: thread -> (chunk, row within a pass)
+        // cp.async gather.  (1) one thread per row maps the stage's 64 keys
+        // (and those kPrefetchStages stages ahead, warming L2); (2) all
+        // producer threads copy 16-byte chunks using the mapped offsets.
+        int64_t *sOff = reinterpret_cast<int64_t *>(smem + S::kOff);
+        const int topk_tok = q_begin + u_min;
+        auto map_row = [&](int j, bool flag, int &pos, int64_t &koff, int64_t &voff) {
+          pos = -1;
+          koff = voff = -1;
+          if (j < lo || j >= hi || j >= t1 * BK) return;
+          int q = j;
+          if (p.topk != nullptr) {
+            q = p.topk[static_cast<int64_t>(topk_tok) * p.topk_stride + j];
+            if (q < 0 || q >= kv_len) {
+              if (flag && q != -1) atomicOr(p.err, PKV_EFLAG_TOPK_OOB);
+              return;
+            }
+          }
+          const int pidx = q / p.page_size;
+          if (pidx >= p.pt_cols) {
+            if (flag) atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
+            return;
+          }
+          const int64_t pg = p.page_table[static_cast<int64_t>(b) * p.pt_stride + pidx];
+          if (pg < 0 || pg >= p.num_pages) {
+            if (flag) atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
+            return;
+          }
+          const int inpage = q - pidx * p.page_size;
+          pos = q;
+          koff = pg * p.k_sp + static_cast<int64_t>(inpage) * p.k_spos + kvh * p.k_sh;
+          voff = pg * p.v_sp + static_cast<int64_t>(inpage) * p.v_spos + kvh * p.v_sh;
+        };
+        int pos = -1;
+        int64_t koff = -1, voff = -1;
+        if (ptid < BK) {
+          int pa;
+          int64_t ka, va;
+          map_row((t0 + kt + kPrefetchStages) * BK + ptid, false, pa, ka, va);
+          if (ka >= 0) {
+            prefetch_l2(p.k + ka, D * 2);
+            prefetch_l2(p.v + va, D * 2);
+          }
+          map_row(base + ptid, true, pos, koff, voff);
+          sPos[st * BK + ptid] = pos;
+          sOff[(st * BK + ptid) * 2] = koff;
+          sOff[(st * BK + ptid) * 2 + 1] = voff;
+        }
+        asm volatile("bar.sync 2, %0;\n" ::"n"(NPROD * 32) : "memory");
         constexpr int RPP = NPROD * 32 / CPR;  // rows per pass
         const int chunk = ptid % CPR;
         const int prow = ptid / CPR;
-        const int topk_tok = q_begin + u_min;
 #pragma unroll 4
         for (int r = prow; r < BK; r += RPP) {
-          const int j = base + r;
-          int pos = -1;
-          const bf16 *ksrc = p.k;
-          const bf16 *vsrc = p.v;
-          if (j >= lo && j < hi) {
-            pos = j;
-            bool ok = true;
-            if (p.topk != nullptr) {
-              pos = p.topk[static_cast<int64_t>(topk_tok) * p.topk_stride + j];
-              if (pos < 0 || pos >= kv_len) {
-                if (pos != -1 && chunk == 0) atomicOr(p.err, PKV_EFLAG_TOPK_OOB);
-                ok = false;
-              }
-            }
-            if (ok) {
-              const int pidx = pos / p.page_size;
-              if (pidx >= p.pt_cols) {
-                if (chunk == 0) atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
-                ok = false;
-              } else {
-                const int64_t pg = p.page_table[static_cast<int64_t>(b) * p.pt_stride + pidx];
-                if (pg < 0 || pg >= p.num_pages) {
-                  if (chunk == 0) atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
-                  ok = false;
-                } else {
-                  const int inpage = pos - pidx * p.page_size;
-                  ksrc = p.k + pg * p.k_sp + inpage * p.k_spos + kvh * p.k_sh + chunk * 8;
-                  vsrc = p.v + pg * p.v_sp + inpage * p.v_spos + kvh * p.v_sh + chunk * 8;
-                }
-              }
-            }
-            if (!ok) pos = -1;
-          }
-          const int nbytes = pos >= 0 ? 16 : 0;
-          cp_async16(kdst + tile_off<BK>(r, chunk), ksrc, nbytes);
-          cp_async16(vdst + tile_off<BK>(r, chunk), vsrc, nbytes);
-          if (chunk == 0) sPos[st * BK + r] = pos;
+          const int64_t ko = sOff[(st * BK + r) * 2];
+          const int64_t vo = sOff[(st * BK + r) * 2 + 1];
+          const int nbytes = ko >= 0 ? 16 : 0;
+          cp_async16(kdst + tile_off<BK>(r, chunk), ko >= 0 ? p.k + ko + chunk * 8 : p.k, nbytes);
+          cp_async16(vdst + tile_off<BK>(r, chunk), ko >= 0 ? p.v + vo + chunk * 8 : p.v, nbytes);
         }
         cp_async_arrive(full);
         mbar_arrive(full);

@@ -49,6 +49,7 @@ constexpr int NTHREADS = (NSOFT + 1 + NPROD) * 32;
 constexpr uint32_t kQBytes = NCH * H * 128;         // 147456
 constexpr uint32_t kKTile = NCH * BKEYS * 128;      // 36864
 constexpr uint32_t kPTile = H * BKEYS * 2;          // 8192
+constexpr int kPrefetchTiles = 4;  // L2 prefetch distance (tiles)
 
 struct Smem {
   static constexpr uint32_t kQ = 0;
@@ -156,8 +157,52 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
         tma_load_3d(sbase + Smem::kQ + c * (H * 128), &maps.q, c * 64, 0, t, bar(Q_FULL));
     }
     const int32_t *list = p.topk + static_cast<int64_t>(t) * p.topk_stride;
+    // position j of the list -> (logical position or -1, element offset of
+    // its row or -1); `flag` raises the error bits (current tile only)
+    auto map_key = [&](int j, bool flag, int &pos, int64_t &off) {
+      pos = -1;
+      off = -1;
+      if (j >= (tile0 + n_kv) * BKEYS || j >= p.topk_len) return;
+      const int idx = list[j];
+      if (idx < 0 || idx >= kv_len) {
+        if (flag && idx != -1) atomicOr(p.err, PKV_EFLAG_TOPK_OOB);
+        return;
+      }
+      const int pidx = idx / p.page_size;
+      if (pidx >= p.pt_cols) {
+        if (flag) atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
+        return;
+      }
+      const int64_t pg = p.page_table[static_cast<int64_t>(b) * p.pt_stride + pidx];
+      if (pg < 0 || pg >= p.num_pages) {
+        if (flag) atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
+        return;
+      }
+      pos = idx;
+      off = pg * p.k_sp + static_cast<int64_t>(idx - pidx * p.page_size) * p.k_spos;
+    };
+    // warm L2 with the rows of the first tiles (HBM latency off the ring)
+    if (ptid < BKEYS) {
+      for (int a = 0; a < kPrefetchTiles && a < n_kv; ++a) {
+        int pos;
+        int64_t off;
+        map_key((tile0 + a) * BKEYS + ptid, false, pos, off);
+        if (off >= 0) prefetch_l2(p.k + off, DQK * 2);
+      }
+    }
     for (int jj = 0; jj < n_kv; ++jj) {
       const int s = jj & 1;
+      // rows kPrefetchTiles tiles ahead into L2, and this tile's mapping,
+      // both issued before waiting for the stage
+      int pos = -1;
+      int64_t off = -1;
+      if (ptid < BKEYS) {
+        int pos_a;
+        int64_t off_a;
+        map_key((tile0 + jj + kPrefetchTiles) * BKEYS + ptid, false, pos_a, off_a);
+        if (off_a >= 0) prefetch_l2(p.k + off_a, DQK * 2);
+        map_key((tile0 + jj) * BKEYS + ptid, true, pos, off);
+      }
       // one thread waits for the stage; every producer thread always meets
       // at the barrier and leaves the loop together on a timeout
       if (ptid == 0) {
@@ -167,32 +212,7 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
       }
       asm volatile("bar.sync 3, %0;\n" ::"n"(NPROD * 32) : "memory");
       if (*sProdFlag == 0) break;
-      // map the tile's listed positions to row offsets (one thread per key)
       if (ptid < BKEYS) {
-        const int j = (tile0 + jj) * BKEYS + ptid;
-        int pos = -1;
-        int64_t off = -1;
-        if (j < p.topk_len) {
-          pos = list[j];
-          if (pos < 0 || pos >= kv_len) {
-            if (pos != -1) atomicOr(p.err, PKV_EFLAG_TOPK_OOB);
-            pos = -1;
-          } else {
-            const int pidx = pos / p.page_size;
-            if (pidx >= p.pt_cols) {
-              atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
-              pos = -1;
-            } else {
-              const int64_t pg = p.page_table[static_cast<int64_t>(b) * p.pt_stride + pidx];
-              if (pg < 0 || pg >= p.num_pages) {
-                atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
-                pos = -1;
-              } else {
-                off = pg * p.k_sp + static_cast<int64_t>(pos - pidx * p.page_size) * p.k_spos;
-              }
-            }
-          }
-        }
         sPos[s * BKEYS + ptid] = pos;
         sRow[s * BKEYS + ptid] = off;
       }
