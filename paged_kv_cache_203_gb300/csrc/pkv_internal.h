@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/pkv.h"
+#include "pkv.h"  // include/ is on the include path
 
 namespace pkv {
 
