@@ -322,17 +322,6 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
           if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
           break;
         }
-      } else {
-        // one thread waits for the stage; all producer threads meet at the
-        // barrier and leave together on a timeout (no one is left behind
-        // at a named barrier)
-        if (ptid == 0) {
-          const bool free_ok = kt < NSTAGE || mbar_wait(empty0 + 8 * st, ((kt / NSTAGE) & 1) ^ 1);
-          if (!free_ok) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
-          *sProdFlag = free_ok ? 1 : 0;
-        }
-        asm volatile("bar.sync 2, %0;\n" ::"n"(NPROD * 32) : "memory");
-        if (*sProdFlag == 0) break;
       }
       const int base = (t0 + kt) * BK;  // absolute key (or list) index of row 0
       const uint32_t kdst = sbase + S::kK + st * S::kStage;
@@ -416,6 +405,8 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
           koff = pg * p.k_sp + static_cast<int64_t>(inpage) * p.k_spos + kvh * p.k_sh;
           voff = pg * p.v_sp + static_cast<int64_t>(inpage) * p.v_spos + kvh * p.v_sh;
         };
+        // mapping loads (this stage, and L2 warming ahead) go out before the
+        // wait for the stage, so their latency overlaps it
         int pos = -1;
         int64_t koff = -1, voff = -1;
         if (ptid < BK) {
@@ -427,6 +418,18 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
             prefetch_l2(p.v + va, D * 2);
           }
           map_row(base + ptid, true, pos, koff, voff);
+        }
+        // one thread waits for the stage; all producer threads meet at the
+        // barrier and leave together on a timeout (no one is left behind at
+        // a named barrier)
+        if (ptid == 0) {
+          const bool free_ok = kt < NSTAGE || mbar_wait(empty0 + 8 * st, ((kt / NSTAGE) & 1) ^ 1);
+          if (!free_ok) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+          *sProdFlag = free_ok ? 1 : 0;
+        }
+        asm volatile("bar.sync 2, %0;\n" ::"n"(NPROD * 32) : "memory");
+        if (*sProdFlag == 0) break;
+        if (ptid < BK) {
           sPos[st * BK + ptid] = pos;
           sOff[(st * BK + ptid) * 2] = koff;
           sOff[(st * BK + ptid) * 2 + 1] = voff;

@@ -17,14 +17,16 @@
 //           signalled with tcgen05.commit on mbarriers (a K stage is released
 //           when its QK^T is done, a V stage when its PV is done);
 //   warps 0-7 softmax: warps w and w+4 share TMEM lane quadrant w (query
-//           rows 32w..32w+31) and split each row's 128 key columns in two
-//           halves; partial row maxima are exchanged through shared memory.
-//           Online softmax in the log2 domain with a lazy reference max (O and
-//           l are rescaled in place only when the row max grows by more than
-//           2^8), P_j (bf16) written to shared memory as the A operand of the
-//           PV MMA; V rows of keys past the sequence or in skipped pages are
-//           zeroed.
-// TMEM: S0 | S1 | O (128 columns each; 512 allocated, 1 CTA per SM).
+//           rows 32w..32w+31) and split each key tile's 128 columns in two
+//           halves.  Each half is an independent online softmax with its own
+//           accumulator (keys 0-63 of every tile go to O_A, keys 64-127 to
+//           O_B), so the halves never synchronise inside the loop; their
+//           states are combined once in the epilogue (log-sum-exp merge).
+//           Log2 domain, lazy reference max (O_hf and l rescaled in place only
+//           when the max grows by more than 2^8), P_j (bf16) written to shared
+//           memory as the A operand of the PV MMA; V rows of keys past the
+//           sequence or in skipped pages are zeroed.
+// TMEM: S0 | S1 | O_A | O_B (128 columns each, 512 in all; 1 CTA per SM).
 // Every mbarrier wait is bounded (PKV_EFLAG_TIMEOUT on expiry).
 #include <cuda.h>
 #include <limits.h>
@@ -52,8 +54,8 @@ struct Smem {
   static constexpr uint32_t kK = kQ + kTileBytes;       // 2 stages
   static constexpr uint32_t kV = kK + 2 * kTileBytes;   // 2 stages
   static constexpr uint32_t kP = kV + 2 * kTileBytes;   // 2 buffers
-  static constexpr uint32_t kMask = kP + 2 * kTileBytes;  // uint32 [2][4]
-  static constexpr uint32_t kXchg = kMask + 32;  // float [2 parities][2 halves][128 rows]
+  static constexpr uint32_t kMask = kP + 2 * kTileBytes;  // uint32 [4 tiles][4 words]
+  static constexpr uint32_t kXchg = kMask + 64;  // float [m, l][2 halves][128 rows]
   static constexpr uint32_t kBar = kXchg + 2 * 2 * BM * 4;
   // barriers: q_full, k_full[2], v_full[2], k_empty[2], v_empty[2],
   //           s_full[2], s_free[2], p_full[2], o_done[2], xchg[2]
@@ -301,7 +303,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sTmem;
-  const uint32_t tS0 = tmem, tO = tmem + 256;
+  const uint32_t tS0 = tmem, tO = tmem + 256;  // O_A at tO, O_B at tO + 128
 
   if (warp == kProducerWarp) {
     // ================================ producer ================================
@@ -344,6 +346,17 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
       const uint32_t roff = static_cast<uint32_t>(lane * pbox) * 128u;
+      // key-validity mask of the tile (inside the sequence, page loaded),
+      // published with K: slot jj & 3 was last read by the softmax of tile
+      // jj - 4, which finished before the V stage this loop waited on below
+      // for tile jj - 1 was released
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane + 32 * i;
+        const int okr = __shfl_sync(0xffffffffu, box_ok ? 1 : 0, r / pbox);
+        const uint32_t bits = __ballot_sync(0xffffffffu, okr && key0 + r < kv_len);
+        if (lane == 0) sMask[(jj & 3) * 4 + i] = bits;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL + s), bytes);
       __syncwarp();
@@ -352,18 +365,10 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
         tma_load_4d(kdst, &maps.k, 0, kvh, inpage, page, bar(K_FULL + s));
         tma_load_4d(kdst + BN * 128, &maps.k, 64, kvh, inpage, page, bar(K_FULL + s));
       }
-      // ---- V tile + key-validity mask (stage freed when PV of tile jj-2
-      //      completed, i.e. after the softmax of tile jj-2 read its mask) ----
+      // ---- V tile (stage freed when the PV of tile jj-2 completed) ----
       if (jj >= 2 && !mbar_wait(bar(V_EMPTY + s), prev)) {
         if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
         break;
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = lane + 32 * i;
-        const int okr = __shfl_sync(0xffffffffu, box_ok ? 1 : 0, r / pbox);
-        const uint32_t bits = __ballot_sync(0xffffffffu, okr && key0 + r < kv_len);
-        if (lane == 0) sMask[s * 4 + i] = bits;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(bar(V_FULL + s), bytes);
@@ -407,11 +412,14 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
           tc_fence_after();
           const uint32_t pa = sbase + Smem::kP + s * kTileBytes;
           const uint32_t vb = sbase + Smem::kV + s * kTileBytes;
+          // keys 0-63 of the tile accumulate into O_A, keys 64-127 into O_B
+          // (each half of the softmax keeps its own reference max)
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks) {
             const uint32_t aoff = (ks >> 2) * (BM * 128) + (ks & 3) * 32;
-            umma(tO, smem_desc(pa + aoff, 0, 1024), smem_desc(vb + ks * 2048, BN * 128, 1024),
-                 kIdescPV, (jj > 0 || ks > 0) ? 1u : 0u);
+            umma(tO + (ks >> 2) * 128, smem_desc(pa + aoff, 0, 1024),
+                 smem_desc(vb + ks * 2048, BN * 128, 1024), kIdescPV,
+                 (jj > 0 || (ks & 3) > 0) ? 1u : 0u);
           }
           umma_commit(bar(O_DONE + s));
           umma_commit(bar(V_EMPTY + s));
@@ -431,7 +439,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t col0 = hf * HALF;
     const float c = p.scale_log2;  // > 0 on this path
-    float *xchg = reinterpret_cast<float *>(smem + Smem::kXchg);  // [2][2][128]
+    float *xchg = reinterpret_cast<float *>(smem + Smem::kXchg);  // [m, l][2 halves][128]
     float m_ref = -INFINITY;  // reference max (log2 domain) of O and l
     float l = 0.f;            // this half's share of the row sum
     bool ok = true;
@@ -447,10 +455,12 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(S_FREE + s));  // S_jj is in registers
 
-      if (!(ok = mbar_wait(bar(V_FULL + s), ph))) break;  // key mask, V rows
+      // the tile's key mask was published with K (its full barrier)
+      if (!(ok = mbar_wait(bar(K_FULL + s), ph))) break;
+      const int ms = (jj & 3) * 4;
       const int key0 = (jt0 + jj) * BN + col0;  // key of this thread's column 0
-      const uint32_t mk0 = sMask[s * 4 + 2 * hf], mk1 = sMask[s * 4 + 2 * hf + 1];
-      const uint32_t m_all = sMask[s * 4] & sMask[s * 4 + 1] & sMask[s * 4 + 2] & sMask[s * 4 + 3];
+      const uint32_t mk0 = sMask[ms + 2 * hf], mk1 = sMask[ms + 2 * hf + 1];
+      const uint32_t m_all = sMask[ms] & sMask[ms + 1] & sMask[ms + 2] & sMask[ms + 3];
       const bool all_valid = m_all == 0xffffffffu;
       const int tile_key0 = (jt0 + jj) * BN;
       const bool edge = !all_valid || (use_upper && tile_key0 + BN - 1 > i_min) ||
@@ -464,7 +474,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
           x[i] = msk ? -INFINITY : x[i];
         }
       }
-      // partial row max (raw scores), eight chains; exchange with the other half
+      // row max over this half's 64 keys (raw scores), eight chains
       float pm[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) pm[k] = x[k];
@@ -472,11 +482,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       for (int i = 8; i < HALF; ++i) pm[i & 7] = fmaxf(pm[i & 7], x[i]);
       float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                        fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-      xchg[(s * 2 + hf) * BM + row] = mx;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(XCHG + s));
-      if (!(ok = mbar_wait(bar(XCHG + s), ph))) break;
-      mx = fmaxf(mx, xchg[(s * 2 + (hf ^ 1)) * BM + row]) * c;
+      mx *= c;  // this half's max; it owns its own accumulator O_hf
 
       // lazy rescale: move the reference only when the max grew by > 2^8
       bool need = false;
@@ -491,13 +497,14 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
         const int t = jj - 1;
         if (!(ok = mbar_wait(bar(O_DONE + (t & 1)), (t >> 1) & 1))) break;
         tc_fence_after();
-#pragma unroll
-        for (int ch = 0; ch < HALF / 32; ++ch) {
+        const uint32_t tOh = tO + hf * 128 + lane_off;  // this half's O
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
           float v[32];
-          tmem_ld32(tO + lane_off + col0 + ch * 32, v);
+          tmem_ld32(tOh + ch * 32, v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= factor;
-          tmem_st32(tO + lane_off + col0 + ch * 32, v);
+          tmem_st32(tOh + ch * 32, v);
         }
         tmem_st_wait();
       }
@@ -528,8 +535,9 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       // V rows of keys outside the sequence or in skipped pages must be zero
       // (P is 0 there, but 0 * NaN would still poison the product); key row
       // `row` of the tile, this thread's half of its columns
-      const uint32_t own = quad == 0 ? sMask[s * 4] : quad == 1 ? sMask[s * 4 + 1]
-                         : quad == 2 ? sMask[s * 4 + 2] : sMask[s * 4 + 3];
+      const uint32_t own = quad == 0 ? sMask[ms] : quad == 1 ? sMask[ms + 1]
+                         : quad == 2 ? sMask[ms + 2] : sMask[ms + 3];
+      if (!all_valid && !(ok = mbar_wait(bar(V_FULL + s), ph))) break;  // rows to zero
       if (!all_valid && !((own >> lane) & 1u)) {
         uint8_t *vt = smem + Smem::kV + s * kTileBytes;
 #pragma unroll
@@ -542,31 +550,44 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       if (lane == 0) mbar_arrive(bar(P_FULL + s));
     }
 
-    // epilogue: wait for the last PV, combine the two halves' sums,
-    // normalise this half of the row, write bf16 and lse
-    float o[HALF];
+    // epilogue: the two halves' states (m, l, O_hf) meet once: this thread
+    // writes output columns col0..col0+63 from O_A and O_B
+    float oa[HALF], ob[HALF];
 #pragma unroll
-    for (int i = 0; i < HALF; ++i) o[i] = 0.f;
+    for (int i = 0; i < HALF; ++i) oa[i] = ob[i] = 0.f;
     if (ok && n_kv > 0) {
       const int t = n_kv - 1;
       ok = mbar_wait(bar(O_DONE + (t & 1)), (t >> 1) & 1);
       if (ok) {
         tc_fence_after();
-        tmem_ld64(tO + lane_off + col0, o);
+        tmem_ld64(tO + lane_off + col0, oa);
+        tmem_ld64(tO + 128 + lane_off + col0, ob);
       }
     }
-    // the halves' sums meet in the exchange slots of parity n_kv & 1, whose
-    // previous contents (tile n_kv - 2) both halves have read by now
-    float l_tot = l;
-    if (ok) {
-      const int ps_ = n_kv & 1;
-      xchg[(ps_ * 2 + hf) * BM + row] = l;
+    float m_oth = -INFINITY, l_oth = 0.f;
+    if (ok) {  // the only use of the exchange barrier: its first phase
+      xchg[hf * BM + row] = m_ref;
+      xchg[(2 + hf) * BM + row] = l;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(XCHG + ps_));
-      ok = mbar_wait(bar(XCHG + ps_), (n_kv >> 1) & 1);
-      if (ok) l_tot += xchg[(ps_ * 2 + (hf ^ 1)) * BM + row];
+      if (lane == 0) mbar_arrive(bar(XCHG));
+      ok = mbar_wait(bar(XCHG), 0);
+      if (ok) {
+        m_oth = xchg[(hf ^ 1) * BM + row];
+        l_oth = xchg[(2 + (hf ^ 1)) * BM + row];
+      }
     }
     if (!ok && lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+    // this thread's (m, l) belong to O_hf; the partner's to the other one
+    const float m_a = hf == 0 ? m_ref : m_oth, l_a = hf == 0 ? l : l_oth;
+    const float m_b = hf == 0 ? m_oth : m_ref, l_b = hf == 0 ? l_oth : l;
+    const float m_tot = fmaxf(m_a, m_b);
+    const float f_a = m_a == -INFINITY ? 0.f : fast_exp2(m_a - m_tot);
+    const float f_b = m_b == -INFINITY ? 0.f : fast_exp2(m_b - m_tot);
+    const float l_tot = l_a * f_a + l_b * f_b;
+    float o[HALF];
+#pragma unroll
+    for (int i = 0; i < HALF; ++i) o[i] = oa[i] * f_a + ob[i] * f_b;
+    m_ref = m_tot;
     if (row < n_rows) {
       const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
       const int tok = q_begin + u;
