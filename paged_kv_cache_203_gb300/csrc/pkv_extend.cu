@@ -474,14 +474,19 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
           x[i] = msk ? -INFINITY : x[i];
         }
       }
-      // row max over this half's 64 keys (raw scores), eight chains
+      // row max over this half's 64 keys (raw scores): eight chains of
+      // three-input maxima
       float pm[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) pm[k] = x[k];
+      for (int k = 0; k < 8; ++k) pm[k] = ptx::fmax3(x[k], x[k + 8], x[k + 16]);
 #pragma unroll
-      for (int i = 8; i < HALF; ++i) pm[i & 7] = fmaxf(pm[i & 7], x[i]);
-      float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      for (int k = 0; k < 8; ++k) pm[k] = ptx::fmax3(pm[k], x[k + 24], x[k + 32]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) pm[k] = ptx::fmax3(pm[k], x[k + 40], x[k + 48]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], x[k + 56]);
+      float mx = ptx::fmax3(ptx::fmax3(pm[0], pm[1], pm[2]), ptx::fmax3(pm[3], pm[4], pm[5]),
+                            fmaxf(pm[6], pm[7]));
       mx *= c;  // this half's max; it owns its own accumulator O_hf
 
       // lazy rescale: move the reference only when the max grew by > 2^8
@@ -510,13 +515,16 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       }
       l *= factor;
 
-      // P = 2^(x c - m_ref): one FFMA + one MUFU per element, eight sums
+      // P = 2^(x c - m_ref): packed-pair FFMA, one MUFU per element,
+      // packed-pair running sums (four pair accumulators)
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
       float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < HALF; ++i) {
-        x[i] = fast_exp2(fmaf(x[i], c, -mu));
-        ps[i & 7] += x[i];
+      for (int i = 0; i < HALF; i += 2) {
+        ptx::ffma2(x[i], x[i + 1], c, -mu);
+        x[i] = fast_exp2(x[i]);
+        x[i + 1] = fast_exp2(x[i + 1]);
+        ptx::fadd2(ps[(i >> 1) & 3], ps[4 + ((i >> 1) & 3)], x[i], x[i + 1]);
       }
       l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
 

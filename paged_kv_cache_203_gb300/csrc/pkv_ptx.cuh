@@ -173,6 +173,28 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
+// Packed fp32 pair arithmetic (sm_100+): (a0, a1) * c + b on both lanes.
+__device__ __forceinline__ void ffma2(float &a0, float &a1, float c, float b) {
+  asm("{\n .reg .b64 x, cc, bb, r;\n"
+      " mov.b64 x, {%0, %1};\n mov.b64 cc, {%2, %2};\n mov.b64 bb, {%3, %3};\n"
+      " fma.rn.f32x2 r, x, cc, bb;\n mov.b64 {%0, %1}, r;\n}\n"
+      : "+f"(a0), "+f"(a1)
+      : "f"(c), "f"(b));
+}
+// (s0, s1) += (a0, a1)
+__device__ __forceinline__ void fadd2(float &s0, float &s1, float a0, float a1) {
+  asm("{\n .reg .b64 s, a;\n"
+      " mov.b64 s, {%0, %1};\n mov.b64 a, {%2, %3};\n"
+      " add.rn.f32x2 s, s, a;\n mov.b64 {%0, %1}, s;\n}\n"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+// max of three (sm_100+ three-input form)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
