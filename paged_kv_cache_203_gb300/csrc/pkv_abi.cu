@@ -79,13 +79,13 @@ bool vec_ok(const pkv_tensor &t, int elem_bytes) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct AttnPlan {
-  int kind;          // 0 = decode-gqa, 1 = tcgen05 extend, 2 = tcgen05 MLA top-k
-  int num_splits;
+  int kind;          // 0 = decode-gqa, 1 = tcgen05 extend, 2 = tcgen05 MLA top-k,
+                     // 3 = all-heads small-page decode
+  int num_splits;    // 0 with kind 3: balanced persistent schedule
   int n_row_tiles;
   size_t ws_o_bytes, ws_lse_bytes, ws_ctr_bytes;
-  size_t total() const {
-    return num_splits > 1 ? ws_o_bytes + ws_lse_bytes + ws_ctr_bytes : 0;
-  }
+  bool split() const { return num_splits > 1 || (kind == 3 && num_splits == 0); }
+  size_t total() const { return split() ? ws_o_bytes + ws_lse_bytes + ws_ctr_bytes : 0; }
 };
 
 // Validates the attention arguments (everything but the outputs) and plans
@@ -144,12 +144,14 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
     return PKV_ERR_UNSUPPORTED;
 
   plan->kind = 0;
-  if (!present(topk) && d == 128 && dv == 128 && max_seqlen_q >= kExtendMinSeqlenQ) {
+  if (!present(topk) && d == 128 && dv == 128) {
     AttnParams lp{};
     lp.d = 128;
     lp.dv = 128;
     lp.h_q = static_cast<int>(h_q);
     lp.h_kv = static_cast<int>(h_kv);
+    lp.group = group;
+    lp.max_seqlen_q = max_seqlen_q;
     lp.page_size = static_cast<int>(page);
     lp.num_pages = num_pages;
     lp.q_st = q.stride[0];
@@ -160,7 +162,10 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
     lp.v_sp = v.stride[0];
     lp.v_spos = v.stride[1];
     lp.v_sh = v.stride[2];
-    if (extend_eligible(lp)) plan->kind = 1;  // tcgen05 extend, no workspace
+    if (max_seqlen_q >= kExtendMinSeqlenQ && extend_eligible(lp))
+      plan->kind = 1;  // tcgen05 extend, no workspace
+    else if (decode_allheads_eligible(lp))
+      plan->kind = 3;  // small pages: one CTA covers every KV head of a request
   }
   if (present(topk)) {
     plan->n_row_tiles = max_seqlen_q * ((group + kDecodeRowTile - 1) / kDecodeRowTile);
@@ -170,11 +175,12 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
   }
   int splits = num_splits;
   if (splits == 0) {
-    // Enough CTAs for ~4 waves at two resident CTAs per SM, but never chunks
-    // shorter than 256 keys.
-    const int64_t base = std::max<int64_t>(1, batch * h_kv * plan->n_row_tiles);
+    // Enough CTAs for ~4 waves at two resident CTAs per SM (three waves at one
+    // per SM for the all-heads kernel), but never chunks shorter than 256 keys.
+    const int64_t base = std::max<int64_t>(
+        1, plan->kind == 3 ? batch : batch * h_kv * plan->n_row_tiles);
     const int64_t max_keys = present(topk) ? topk.shape[1] : pt.shape[1] * page;
-    const int64_t target = 4LL * kNumSMs * 2;
+    const int64_t target = plan->kind == 3 ? 3LL * kNumSMs : 4LL * kNumSMs * 2;
     int64_t s = (target + base - 1) / base;
     s = std::min<int64_t>(s, std::max<int64_t>(1, max_keys / 256));
     splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s, 64)));
@@ -187,6 +193,14 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
   plan->ws_lse_bytes = align256(static_cast<size_t>(splits) * rows_total * 4);
   plan->ws_ctr_bytes =
       align256(static_cast<size_t>(batch) * h_kv * plan->n_row_tiles * 4);
+  if (plan->kind == 3 && num_splits == 0 && batch <= kDecodeBalancedMaxBatch) {
+    // balanced persistent schedule: per CTA two partial slots (its first and
+    // last request) of one request's rows
+    plan->num_splits = 0;
+    const size_t slots = 2ull * kDecodeBalancedCtas * max_seqlen_q * h_q;
+    plan->ws_o_bytes = align256(slots * dv * 4);
+    plan->ws_lse_bytes = align256(slots * 4);
+  }
   return PKV_OK;
 }
 
@@ -303,7 +317,7 @@ int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
   p.num_splits = plan.num_splits;
   p.n_row_tiles = plan.n_row_tiles;
   p.err = err;
-  if (plan.num_splits > 1) {
+  if (plan.split()) {
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.ws_o = reinterpret_cast<float *>(ws);
     p.ws_lse = reinterpret_cast<float *>(ws + plan.ws_o_bytes);
@@ -313,6 +327,7 @@ int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
   }
   if (p.total_q == 0) return PKV_OK;
   if (plan.kind == 2) return launch_mla_topk(p, stream);
+  if (plan.kind == 3) return launch_decode_allheads(p, stream);
   if (plan.kind == 1) {
     // the extend kernel takes row maxima of raw scores: positive scale only
     rc = scale > 0.f ? launch_extend_tc(p, stream) : PKV_ERR_UNSUPPORTED;

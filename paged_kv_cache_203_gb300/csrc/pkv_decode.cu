@@ -739,6 +739,538 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
         wsum > 0.f ? Ms + logf(wsum) : -INFINITY;
 }
 
+// ============================================================================
+// All-heads decode for small pages (page size < 8, one slot = one row of all
+// KV heads).  A CTA covers every KV head of a request: consumer warp h < H_kv
+// owns KV head h and its GQA query rows, and a producer warp copies, per key,
+// the contiguous H_kv x D row of K and of V with one bulk copy each (no
+// tensor map) into shared memory at a pitch of H_kv * 256 + 16 bytes; the
+// 16-byte skew keeps the consumers' ldmatrix reads conflict-free without a
+// swizzle.  Against one CTA per (request, KV head), every key is one
+// contiguous 2 KB read per tensor instead of H_kv scattered 256-byte reads.
+// The page ids of a tile are fetched AH_LOOKAHEAD tiles before its copies
+// (4-byte cp.async into a shared ring), so the page-table latency is off the
+// copy path: a producer that waited for each tile's ids would be held to one
+// tile per global-load round trip.
+//
+// Two schedules share the kernel:
+//  * fixed splits (num_splits >= 1): CTA (split, request) takes an equal
+//    share of the request's 16-key tiles; partials are merged by the last CTA
+//    of each (request, KV head);
+//  * balanced (num_splits == 0, persistent, one CTA per SM): the 16-key tiles
+//    of the whole batch are laid end to end and CTA c takes the c-th equal
+//    share, crossing request boundaries with the copy pipeline still full.  A
+//    request covered by one CTA is written directly; a split request leaves
+//    one partial per CTA (slot 0 when it is the CTA's first request, slot 1
+//    when its last) and the CTA that finishes last merges them.
+// ============================================================================
+
+constexpr int AH_BK = 16;        // keys per stage
+constexpr int AH_NSTAGE = 3;
+constexpr int AH_MAXH = 8;       // KV heads per CTA (one consumer warp each)
+constexpr int AH_MAXPITCH = AH_MAXH * 256 + 16;
+constexpr int AH_MAXB = kDecodeBalancedMaxBatch;  // requests a balanced launch schedules
+constexpr int AH_LOOKAHEAD = 4;  // tiles the page-id fetch runs ahead of the copies
+constexpr int AH_RING = AH_LOOKAHEAD + 1;
+constexpr int AH_THREADS = (AH_MAXH + 1) * 32;
+
+// stage flags published by the producer beside each tile's key positions
+constexpr int AH_SEG_START = 1;  // first tile this CTA takes of the request
+constexpr int AH_SEG_END = 2;    // last tile this CTA takes of the request
+constexpr int AH_REQ_START = 4;  // the request's first tile
+constexpr int AH_REQ_END = 8;    // the request's last tile
+
+struct AhSmem {
+  static constexpr uint32_t kStage = AH_BK * AH_MAXPITCH;  // one K (or V) stage
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kK + AH_NSTAGE * kStage;
+  static constexpr uint32_t kPos = kV + AH_NSTAGE * kStage;        // int [NSTAGE][BK]
+  static constexpr uint32_t kMeta = kPos + AH_NSTAGE * AH_BK * 4;  // int [NSTAGE][2]
+  static constexpr uint32_t kRingPg = kMeta + AH_NSTAGE * 8;         // int [RING][BK] page ids
+  static constexpr uint32_t kRingJ = kRingPg + AH_RING * AH_BK * 4;  // int [RING][BK] key or -1
+  static constexpr uint32_t kPre = (kRingJ + AH_RING * AH_BK * 4 + 7) & ~7u;  // int64 [MAXB + 1]
+  static constexpr uint32_t kScan = kPre + (AH_MAXB + 1) * 8;  // int64 [warps]
+  static constexpr uint32_t kBar = kScan + 16 * 8;
+  static constexpr uint32_t kEnd = kBar + 2 * AH_NSTAGE * 8;
+  static constexpr size_t kDynamic = kEnd;
+};
+static_assert(AhSmem::kDynamic <= 232448, "all-heads decode smem plan exceeds 227 KB");
+static_assert(AhSmem::kBar % 8 == 0 && AhSmem::kPre % 8 == 0, "8-byte alignment");
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// A request's query run and key range [lo, hi) in 16-key tiles.
+struct AhReq {
+  int q_begin, q_len, kv_len, lo, hi, t_lo, ntiles;  // ntiles 0: nothing to do
+};
+
+__device__ __forceinline__ AhReq ah_request(const AttnParams &p, int b) {
+  AhReq r;
+  r.q_begin = p.cu_seqlens_q[b];
+  r.q_len = p.cu_seqlens_q[b + 1] - r.q_begin;
+  r.kv_len = p.cache_seqlens[b];
+  r.hi = max(r.kv_len, 0);
+  r.lo = p.window_left >= 0 ? max(0, r.kv_len - r.q_len - p.window_left) : 0;
+  r.hi = max(r.hi, r.lo);
+  r.t_lo = r.lo / AH_BK;
+  const int t_hi = (r.hi + AH_BK - 1) / AH_BK;
+  // a request with no key still takes one (empty) tile: its rows get 0 / -inf
+  r.ntiles = max(1, t_hi - r.t_lo);
+  if (r.q_len <= 0 || r.q_begin < 0 || r.q_begin + r.q_len > p.total_q) r.ntiles = 0;
+  return r;
+}
+
+// CTA of a balanced launch (g CTAs over t tiles) whose share holds tile x.
+__device__ __forceinline__ int ah_cta_of(int64_t x, int64_t g, int64_t t) {
+  return static_cast<int>(((x + 1) * g - 1) / t);
+}
+
+__global__ void __launch_bounds__(AH_THREADS, 1)
+decode_allheads_kernel(const __grid_constant__ AttnParams p) {
+  using S = AhSmem;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t sbase = smem_addr(smem);
+  int *sPos = reinterpret_cast<int *>(smem + S::kPos);
+  int *sMeta = reinterpret_cast<int *>(smem + S::kMeta);
+  int64_t *sPre = reinterpret_cast<int64_t *>(smem + S::kPre);
+  int64_t *sScan = reinterpret_cast<int64_t *>(smem + S::kScan);
+  const uint32_t full0 = sbase + S::kBar;
+  const uint32_t empty0 = full0 + AH_NSTAGE * 8;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int hkv = p.h_kv;
+  const bool balanced = p.num_splits == 0;
+  const uint32_t blk = static_cast<uint32_t>(hkv) * 256u;  // one slot row
+  const uint32_t pitch = blk + 16u;
+
+  if (tid == 0) {
+    for (int s = 0; s < AH_NSTAGE; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, hkv);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    fence_proxy_async();
+  }
+
+  // ---- this CTA's run of tiles: n tiles from tile t_first of request b_first ----
+  int b_first = 0, t_first = 0, n = 0;
+  int64_t T = 0, G = 1;
+  if (balanced) {
+    // exclusive prefix of tiles over the batch (each thread a contiguous run)
+    const int per = (p.batch + AH_THREADS - 1) / AH_THREADS;
+    const int e0 = min(p.batch, tid * per), e1 = min(p.batch, e0 + per);
+    int64_t sum = 0;
+    for (int b = e0; b < e1; ++b) sum += ah_request(p, b).ntiles;
+    int64_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) sScan[warp] = incl;
+    __syncthreads();
+    int64_t run = incl - sum;
+    for (int w = 0; w < warp; ++w) run += sScan[w];
+    for (int b = e0; b < e1; ++b) {
+      sPre[b] = run;
+      run += ah_request(p, b).ntiles;
+    }
+    if (tid == AH_THREADS - 1) sPre[p.batch] = run;
+    __syncthreads();
+    T = sPre[p.batch];
+    G = min(static_cast<int64_t>(gridDim.x), T);
+    const int64_t c = blockIdx.x;
+    if (c >= G) return;  // uniform: no work (also T == 0)
+    const int64_t x0 = c * T / G, x1 = (c + 1) * T / G;
+    n = static_cast<int>(x1 - x0);
+    // request holding tile x0: the last b with sPre[b] <= x0
+    int lo_b = 0, hi_b = p.batch;  // sPre[lo_b] <= x0 < sPre[hi_b]
+    while (hi_b - lo_b > 1) {
+      const int mid = (lo_b + hi_b) >> 1;
+      if (sPre[mid] <= x0) lo_b = mid; else hi_b = mid;
+    }
+    b_first = lo_b;
+    t_first = static_cast<int>(x0 - sPre[lo_b]);
+  } else {
+    __syncthreads();
+    b_first = blockIdx.z;
+    const AhReq r = ah_request(p, b_first);
+    if (r.ntiles == 0) return;  // uniform
+    const int split = blockIdx.x;
+    const int per = (r.ntiles + p.num_splits - 1) / p.num_splits;
+    const int t0 = min(r.ntiles, split * per);
+    const int t1 = min(r.ntiles, t0 + per);
+    t_first = t0;
+    n = max(1, t1 - t0);  // an empty share still reports (as an empty tile)
+  }
+
+  if (warp == AH_MAXH) {
+    // ================================ producer ================================
+    // Lanes 0-15 handle one key of a tile each.  A fetch cursor runs
+    // AH_LOOKAHEAD tiles ahead of the copy cursor: per tile it puts each key's
+    // page id (or -1 for a key outside the range) in a shared ring slot with
+    // a 4-byte cp.async, one commit group per tile; the copy cursor waits for
+    // its tile's group and reads the ids back (each lane its own entries).
+    int *ring_pg = reinterpret_cast<int *>(smem + S::kRingPg);
+    int *ring_j = reinterpret_cast<int *>(smem + S::kRingJ);
+    int b = b_first, t = t_first;
+    AhReq r = ah_request(p, b);
+    int fb = b, ft = t;
+    AhReq fr = r;
+    auto advance = [&](int &bb, int &tt, AhReq &rr) {
+      if (++tt >= rr.ntiles && balanced && bb < p.batch - 1) {
+        do {
+          ++bb;
+        } while (bb < p.batch - 1 && sPre[bb + 1] == sPre[bb]);
+        tt = 0;
+        rr = ah_request(p, bb);
+      }
+    };
+    // fetch tile x (the fetch cursor's) into ring slot x % AH_RING
+    auto fetch = [&](int x) {
+      if (lane < AH_BK) {
+        const int slot = (x % AH_RING) * AH_BK + lane;
+        const int j = (fr.t_lo + ft) * AH_BK + lane;
+        int jj = -1;
+        if (j >= fr.lo && j < fr.hi) {
+          const int pidx = j / p.page_size;
+          if (pidx < p.pt_cols) {
+            cp_async4(sbase + S::kRingPg + slot * 4,
+                      p.page_table + static_cast<int64_t>(fb) * p.pt_stride + pidx);
+            jj = j;
+          } else {
+            atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
+          }
+        }
+        ring_j[slot] = jj;
+      }
+      cp_async_commit();
+    };
+    for (int x = 0; x < AH_LOOKAHEAD; ++x) {
+      if (x < n) fetch(x);
+      else cp_async_commit();
+      if (x + 1 < n) advance(fb, ft, fr);
+    }
+    for (int kt = 0; kt < n; ++kt) {
+      const int st = kt % AH_NSTAGE;
+      if (kt + AH_LOOKAHEAD < n) fetch(kt + AH_LOOKAHEAD);
+      else cp_async_commit();
+      if (kt + AH_LOOKAHEAD + 1 < n) advance(fb, ft, fr);
+      cp_async_wait_group<AH_LOOKAHEAD>();  // this tile's ids have landed
+      int pos = -1;
+      int64_t koff = 0, voff = 0;
+      if (lane < AH_BK) {
+        const int slot = (kt % AH_RING) * AH_BK + lane;
+        const int j = ring_j[slot];
+        if (j >= 0) {
+          const int64_t pg = ring_pg[slot];
+          if (pg < 0 || pg >= p.num_pages) {
+            atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
+          } else {
+            const int inpage = j - (j / p.page_size) * p.page_size;
+            koff = pg * p.k_sp + static_cast<int64_t>(inpage) * p.k_spos;
+            voff = pg * p.v_sp + static_cast<int64_t>(inpage) * p.v_spos;
+            pos = j;
+          }
+        }
+      }
+      int flags = 0;
+      if (kt == 0 || t == 0) flags |= AH_SEG_START;
+      if (kt == n - 1 || t == r.ntiles - 1) flags |= AH_SEG_END;
+      if (t == 0) flags |= AH_REQ_START;
+      if (t == r.ntiles - 1) flags |= AH_REQ_END;
+
+      int ok = 1;
+      if (lane == 0 && kt >= AH_NSTAGE)
+        ok = mbar_wait(empty0 + 8 * st, ((kt / AH_NSTAGE) & 1) ^ 1) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+        break;
+      }
+      const uint32_t full = full0 + 8 * st;
+      if (lane < AH_BK) sPos[st * AH_BK + lane] = pos;
+      if (lane == 0) {
+        sMeta[2 * st] = b;
+        sMeta[2 * st + 1] = flags;
+      }
+      uint32_t bytes = pos >= 0 ? 2u * blk : 0u;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(full, bytes);
+      __syncwarp();
+      if (pos >= 0) {
+        bulk_g2s(sbase + S::kK + st * S::kStage + lane * pitch, p.k + koff, blk, full);
+        bulk_g2s(sbase + S::kV + st * S::kStage + lane * pitch, p.v + voff, blk, full);
+      }
+      // next tile (a balanced run moves on to the next request with tiles;
+      // a fixed split never leaves its request)
+      if (kt + 1 < n) advance(b, t, r);
+    }
+    cp_async_wait_group<0>();
+    return;
+  }
+  if (warp >= hkv) return;  // no KV head for this warp (never waited on)
+
+  // ================================ consumers ================================
+  const int h = warp;  // KV head
+  const int g = lane >> 2, tq = lane & 3;
+  const uint32_t hoff = static_cast<uint32_t>(h) * 256u;
+  const int64_t rows_total = static_cast<int64_t>(p.total_q) * p.h_q;
+  const int64_t rows_req = static_cast<int64_t>(p.max_seqlen_q) * p.h_q;  // balanced slots
+  const bool use_upper = p.causal || p.window_left >= 0;
+
+  uint32_t qf[8][4];
+  float o[16][4];
+  float m_run[2], l_run[2];
+  int rpos[2];
+  AhReq r{};
+  int n_rows = 0;
+  bool seg_req_start = false, first_seg = true;
+
+  for (int kt = 0; kt < n; ++kt) {
+    const int st = kt % AH_NSTAGE;
+    if (!mbar_wait(full0 + 8 * st, (kt / AH_NSTAGE) & 1)) {
+      if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+      break;
+    }
+    const int b = sMeta[2 * st];
+    const int flags = sMeta[2 * st + 1];
+    if (flags & AH_SEG_START) {
+      // a new request: its rows for this head, Q fragments from global memory
+      r = ah_request(p, b);
+      n_rows = min(r.q_len, p.max_seqlen_q) * p.group;  // <= 16 on this path
+      seg_req_start = (flags & AH_REQ_START) != 0;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int rr = g + 8 * hh;
+        const bool rv = rr < n_rows;
+        const int u = rv ? rr / p.group : 0;
+        const int gg = rv ? rr % p.group : 0;
+        rpos[hh] = r.kv_len - r.q_len + u;
+        const bf16 *qrow = p.q + static_cast<int64_t>(r.q_begin + u) * p.q_st +
+                           static_cast<int64_t>(h * p.group + gg) * p.q_sh;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int c0 = kk * 16 + 2 * tq;
+          qf[kk][hh] = rv ? *reinterpret_cast<const uint32_t *>(qrow + c0) : 0u;
+          qf[kk][2 + hh] = rv ? *reinterpret_cast<const uint32_t *>(qrow + c0 + 8) : 0u;
+        }
+      }
+#pragma unroll
+      for (int nn = 0; nn < 16; ++nn) o[nn][0] = o[nn][1] = o[nn][2] = o[nn][3] = 0.f;
+      m_run[0] = m_run[1] = -INFINITY;
+      l_run[0] = l_run[1] = 0.f;
+    }
+    const uint32_t kb = sbase + S::kK + st * S::kStage + hoff;
+    const uint32_t vb = sbase + S::kV + st * S::kStage + hoff;
+    const int *pos_st = sPos + st * AH_BK;
+    // zero this head's V rows of skipped keys (a masked key must add exactly 0)
+    const bool any_skipped = __any_sync(0xffffffffu, pos_st[lane & 15] < 0);
+    if (any_skipped) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int idx = i * 32 + lane;
+        const int rr = idx >> 4, cc = idx & 15;
+        if (pos_st[rr] < 0)
+          *reinterpret_cast<uint4 *>(smem + S::kV + st * S::kStage + rr * pitch + hoff + cc * 16) =
+              make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+    // S = Q K^T for the stage's 16 keys
+    float sc[2][4];
+#pragma unroll
+    for (int nn = 0; nn < 2; ++nn) sc[nn][0] = sc[nn][1] = sc[nn][2] = sc[nn][3] = 0.f;
+    {
+      const int key = (lane >> 4) * 8 + (lane & 7);
+      const int kc = (lane >> 3) & 1;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + key * pitch + (2 * kk + kc) * 16, b0, b1, b2, b3);
+        mma_bf16(sc[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+        mma_bf16(sc[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+      }
+    }
+    int kpos[2][2];
+#pragma unroll
+    for (int nn = 0; nn < 2; ++nn) {
+      kpos[nn][0] = pos_st[nn * 8 + 2 * tq];
+      kpos[nn][1] = pos_st[nn * 8 + 2 * tq + 1];
+    }
+#pragma unroll
+    for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int hh = e >> 1;
+        const int kp = kpos[nn][e & 1];
+        bool masked = kp < 0;
+        if (use_upper && kp > rpos[hh]) masked = true;
+        if (p.window_left >= 0 && kp < rpos[hh] - p.window_left) masked = true;
+        sc[nn][e] = masked ? -INFINITY : sc[nn][e] * p.scale_log2;
+      }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float mx = fmaxf(fmaxf(sc[0][2 * hh], sc[0][2 * hh + 1]), fmaxf(sc[1][2 * hh], sc[1][2 * hh + 1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run[hh], mx);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = exp2f(m_run[hh] - m_use);
+      m_run[hh] = m_new;
+      float sum = 0.f;
+#pragma unroll
+      for (int nn = 0; nn < 2; ++nn) {
+        sc[nn][2 * hh] = exp2f(sc[nn][2 * hh] - m_use);
+        sc[nn][2 * hh + 1] = exp2f(sc[nn][2 * hh + 1] - m_use);
+        sum += sc[nn][2 * hh] + sc[nn][2 * hh + 1];
+      }
+      l_run[hh] = l_run[hh] * alpha + sum;
+#pragma unroll
+      for (int nn = 0; nn < 16; ++nn) {
+        o[nn][2 * hh] *= alpha;
+        o[nn][2 * hh + 1] *= alpha;
+      }
+    }
+    const uint32_t a0 = pack_bf16(sc[0][0], sc[0][1]);
+    const uint32_t a1 = pack_bf16(sc[0][2], sc[0][3]);
+    const uint32_t a2 = pack_bf16(sc[1][0], sc[1][1]);
+    const uint32_t a3 = pack_bf16(sc[1][2], sc[1][3]);
+    {
+      const int m = lane >> 3;
+      const int key = (m & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vb + key * pitch + (2 * cc + (m >> 1)) * 16, b0, b1, b2, b3);
+        mma_bf16(o[2 * cc], a0, a1, a2, a3, b0, b1);
+        mma_bf16(o[2 * cc + 1], a0, a1, a2, a3, b2, b3);
+      }
+    }
+    if (any_skipped) fence_proxy_async();  // generic zeros before bulk rewrites
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+
+    if (!(flags & AH_SEG_END)) continue;
+    // ------------------- end of this CTA's share of request b -------------------
+    const bool whole = balanced ? (seg_req_start && (flags & AH_REQ_END) != 0) : p.num_splits == 1;
+    const int slot = first_seg ? 0 : 1;
+    first_seg = false;
+    float L[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      L[hh] = l_run[hh];
+      L[hh] += __shfl_xor_sync(0xffffffffu, L[hh], 1);
+      L[hh] += __shfl_xor_sync(0xffffffffu, L[hh], 2);
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int rr = g + 8 * hh;
+      if (rr >= n_rows) continue;
+      const int u = rr / p.group;
+      const int tok = r.q_begin + u;
+      const int head = h * p.group + rr % p.group;
+      const float inv = L[hh] > 0.f ? 1.f / L[hh] : 0.f;
+      const float lse_nat = L[hh] > 0.f ? (m_run[hh] + log2f(L[hh])) * kLn2 : -INFINITY;
+      if (whole) {
+        bf16 *dst = p.out + static_cast<int64_t>(tok) * p.o_st + static_cast<int64_t>(head) * p.o_sh;
+#pragma unroll
+        for (int nn = 0; nn < 16; ++nn)
+          *reinterpret_cast<uint32_t *>(dst + nn * 8 + 2 * tq) =
+              pack_bf16(o[nn][2 * hh] * inv, o[nn][2 * hh + 1] * inv);
+        if (p.lse != nullptr && tq == 0)
+          p.lse[static_cast<int64_t>(tok) * p.lse_st + static_cast<int64_t>(head) * p.lse_sh] =
+              lse_nat;
+      } else {
+        const int64_t widx =
+            balanced ? (static_cast<int64_t>(blockIdx.x) * 2 + slot) * rows_req +
+                           static_cast<int64_t>(u) * p.h_q + head
+                     : static_cast<int64_t>(blockIdx.x) * rows_total +
+                           static_cast<int64_t>(tok) * p.h_q + head;
+        float *dst = p.ws_o + widx * p.dv;
+#pragma unroll
+        for (int nn = 0; nn < 16; ++nn)
+          __stcg(reinterpret_cast<float2 *>(dst + nn * 8 + 2 * tq),
+                 make_float2(o[nn][2 * hh] * inv, o[nn][2 * hh + 1] * inv));
+        if (tq == 0) __stcg(p.ws_lse + widx, lse_nat);
+      }
+    }
+    if (whole) continue;
+
+    // partial written: the last CTA to finish this (request, KV head) merges
+    int expected = p.num_splits, c0 = 0;
+    bool c0_second_slot = false;
+    if (balanced) {
+      c0 = ah_cta_of(sPre[b], G, T);
+      expected = ah_cta_of(sPre[b + 1] - 1, G, T) - c0 + 1;
+      c0_second_slot = static_cast<int64_t>(c0) * T / G < sPre[b];
+    }
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0)
+      last = atomicAdd(p.ws_counter + static_cast<int64_t>(b) * hkv + h, 1) == expected - 1;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) continue;
+    __threadfence();
+    for (int rr = 0; rr < n_rows; ++rr) {
+      const int u = rr / p.group;
+      const int tok = r.q_begin + u;
+      const int head = h * p.group + rr % p.group;
+      const int64_t rloc = balanced ? static_cast<int64_t>(u) * p.h_q + head
+                                    : static_cast<int64_t>(tok) * p.h_q + head;
+      auto src = [&](int sp) -> int64_t {
+        return balanced ? (static_cast<int64_t>(c0 + sp) * 2 + (sp == 0 && c0_second_slot ? 1 : 0)) *
+                                  rows_req + rloc
+                        : static_cast<int64_t>(sp) * rows_total + rloc;
+      };
+      float Ms = -INFINITY;
+      for (int sp = 0; sp < expected; ++sp) Ms = fmaxf(Ms, __ldcg(p.ws_lse + src(sp)));
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float wsum = 0.f;
+      if (Ms != -INFINITY) {
+        for (int sp = 0; sp < expected; ++sp) {
+          const int64_t sidx = src(sp);
+          const float w = exp2f((__ldcg(p.ws_lse + sidx) - Ms) * kLog2e);
+          wsum += w;
+          const float4 v4 = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + sidx * p.dv + lane * 4));
+          acc[0] += w * v4.x; acc[1] += w * v4.y; acc[2] += w * v4.z; acc[3] += w * v4.w;
+        }
+      }
+      const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
+      bf16 *dst = p.out + static_cast<int64_t>(tok) * p.o_st + static_cast<int64_t>(head) * p.o_sh +
+                  lane * 4;
+      uint2 w2;
+      w2.x = pack_bf16(acc[0] * winv, acc[1] * winv);
+      w2.y = pack_bf16(acc[2] * winv, acc[3] * winv);
+      *reinterpret_cast<uint2 *>(dst) = w2;
+      if (p.lse != nullptr && lane == 0)
+        p.lse[static_cast<int64_t>(tok) * p.lse_st + static_cast<int64_t>(head) * p.lse_sh] =
+            wsum > 0.f ? Ms + logf(wsum) : -INFINITY;
+    }
+  }
+}
+
 // ------------------------------------------------------------------- host
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
@@ -817,6 +1349,36 @@ int launch_typed(const AttnParams &p, const DecodeMaps &maps, cudaStream_t strea
 }
 
 }  // namespace
+
+bool decode_allheads_eligible(const AttnParams &p) {
+  if (p.topk != nullptr || p.d != 128 || p.dv != 128) return false;
+  if (p.page_size >= 8 || p.h_kv > AH_MAXH) return false;
+  if (p.max_seqlen_q < 1 || p.max_seqlen_q * p.group > 16) return false;
+  // every slot's heads form one contiguous H_kv x D row in K and in V
+  return p.k_sh == 128 && p.k_spos == static_cast<int64_t>(p.h_kv) * 128 && p.v_sh == 128 &&
+         p.v_spos == static_cast<int64_t>(p.h_kv) * 128;
+}
+
+int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
+  if (p.batch == 0) return PKV_OK;
+  if (!decode_allheads_eligible(p)) return PKV_ERR_UNSUPPORTED;
+  if (p.batch > 65535 || p.num_splits > 65535) return PKV_ERR_UNSUPPORTED;
+  if (p.num_splits == 0 && p.batch > AH_MAXB) return PKV_ERR_UNSUPPORTED;
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev >= 64 || !configured[dev]) {
+    if (cudaFuncSetAttribute(decode_allheads_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(AhSmem::kDynamic)) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    if (dev < 64) configured[dev] = true;
+  }
+  // balanced: one persistent CTA per SM; fixed splits: (split, request)
+  const dim3 grid = p.num_splits == 0 ? dim3(kDecodeBalancedCtas, 1, 1)
+                                      : dim3(p.num_splits, 1, p.batch);
+  decode_allheads_kernel<<<grid, AH_THREADS, AhSmem::kDynamic, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
 
 int launch_decode_gqa(const AttnParams &p, cudaStream_t stream) {
   if (p.batch == 0 || p.n_row_tiles == 0) return PKV_OK;

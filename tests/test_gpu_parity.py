@@ -457,6 +457,69 @@ def test_garbage_outside_valid_rows_never_leaks(page_size):
         check_close(out, lse, ref_o, ref_l, f"nan P={page_size} splits={splits}")
 
 
+@pytest.mark.parametrize("page_size,h_q,h_kv,q_len,window,causal", [
+    (1, 64, 8, 1, -1, False),     # sliding-window decode shape: 8 KV heads, group 8
+    (2, 16, 8, 2, -1, True),      # 16 rows per KV head: a causal pair of tokens
+    (5, 8, 4, 4, 30, True),       # window + causal, group 2
+    (7, 4, 1, 4, -1, True),       # one KV head, group 4
+    (3, 2, 2, 16, 50, True),      # group 1, 16 query tokens per request
+    (1, 6, 2, 1, 0, False),       # window 0: the diagonal key only
+])
+def test_small_page_all_heads_decode(page_size, h_q, h_kv, q_len, window, causal):
+    """Small pages (< 8 slots) with at most 16 query rows per KV head run the
+    kernel that covers every KV head of a request in one CTA; unused slots hold
+    NaN, one page id is out of the pool (that key is skipped and flagged)."""
+    wl = workloads.make("tiny_decode", d=128, page_size=page_size, h_q=h_q, h_kv=h_kv,
+                        q_len=q_len, window_left=window, causal=causal,
+                        len_lo=q_len, len_hi=1300, batch=6,
+                        pool_tokens=6 * (1300 + page_size) * 2)
+    valid = torch.zeros(wl.k_cache.shape[0] * page_size, dtype=torch.bool)
+    for b in range(6):
+        n = int(wl.cache_seqlens[b])
+        j = torch.arange(n)
+        slots = wl.page_table[b, j // page_size].long() * page_size + j % page_size
+        valid[slots] = True
+    valid = valid.view(-1, page_size)
+    wl.k_cache[~valid] = float("nan")
+    wl.v_cache[~valid] = float("nan")
+    wl.cache_seqlens[4] = 0
+    if int(wl.cache_seqlens[2]) > 2 * page_size:
+        wl.page_table[2, 1] = 50_000_000
+    g = wl.to(DEV)
+    for splits in (1, 3, 0):
+        out, lse = gpu_attn(g, num_splits=splits)
+        ref_o, ref_l, _ = oracle_attn(wl)
+        check_close(out, lse, ref_o, ref_l, f"P={page_size} splits={splits}")
+    assert (pkv.get_error_flags() & ~pkv.EFLAG_PAGE_OOB) == 0
+
+
+def test_small_page_balanced_schedule_mixed_batch():
+    """The balanced schedule (num_splits 0) lays the batch's 16-key tiles end
+    to end over one CTA per SM: requests of very different lengths, requests
+    with no cached key and requests with no new token all land where the
+    oracle puts them."""
+    batch = 60
+    wl = workloads.make("tiny_decode", d=128, page_size=1, h_q=16, h_kv=4, batch=batch,
+                        len_lo=1, len_hi=3000, pool_tokens=batch * 3000 + 64, seed=77)
+    cs = wl.cache_seqlens
+    cs[3] = 0
+    cs[17] = 0
+    cs[40] = wl.page_table.shape[1]  # the longest request the table holds
+    no_tok = {5, 6, 31, 59}
+    cu = [0]
+    for b in range(batch):
+        cu.append(cu[-1] + (0 if b in no_tok else 1))
+    keep = [b for b in range(batch) if b not in no_tok]
+    wl.cu_seqlens_q = torch.tensor(cu, dtype=torch.int32)
+    wl.q = wl.q[keep].contiguous()
+    g = wl.to(DEV)
+    for splits in (0, 1, 2):
+        out, lse = gpu_attn(g, num_splits=splits)
+        ref_o, ref_l, _ = oracle_attn(wl)
+        check_close(out, lse, ref_o, ref_l, f"mixed batch splits={splits}")
+    assert pkv.get_error_flags() == 0
+
+
 def test_head_major_cache_layout():
     """A cache laid out [pages, H_kv, P, D] (head outside position) is read
     through its strides; results equal the oracle's."""
