@@ -154,6 +154,8 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
     lp.max_seqlen_q = max_seqlen_q;
     lp.page_size = static_cast<int>(page);
     lp.num_pages = num_pages;
+    lp.k = static_cast<const bf16 *>(k.data);
+    lp.v = static_cast<const bf16 *>(v.data);
     lp.q_st = q.stride[0];
     lp.q_sh = q.stride[1];
     lp.k_sp = k.stride[0];
@@ -164,8 +166,9 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
     lp.v_sh = v.stride[2];
     if (max_seqlen_q >= kExtendMinSeqlenQ && extend_eligible(lp))
       plan->kind = 1;  // tcgen05 extend, no workspace
-    else if (decode_allheads_eligible(lp))
-      plan->kind = 3;  // small pages: one CTA covers every KV head of a request
+    else if (decode_allheads_eligible(lp) &&
+             (page < 8 || (num_splits == 0 && batch <= kDecodeBalancedMaxBatch)))
+      plan->kind = 3;  // one CTA covers every KV head of a request
   }
   if (present(topk)) {
     plan->n_row_tiles = max_seqlen_q * ((group + kDecodeRowTile - 1) / kDecodeRowTile);

@@ -740,39 +740,44 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
 }
 
 // ============================================================================
-// All-heads decode for small pages (page size < 8, one slot = one row of all
-// KV heads).  A CTA covers every KV head of a request: consumer warp h < H_kv
-// owns KV head h and its GQA query rows, and a producer warp copies, per key,
-// the contiguous H_kv x D row of K and of V with one bulk copy each (no
-// tensor map) into shared memory at a pitch of H_kv * 256 + 16 bytes; the
-// 16-byte skew keeps the consumers' ldmatrix reads conflict-free without a
-// swizzle.  Against one CTA per (request, KV head), every key is one
-// contiguous 2 KB read per tensor instead of H_kv scattered 256-byte reads.
-// The page ids of a tile are fetched AH_LOOKAHEAD tiles before its copies
-// (4-byte cp.async into a shared ring), so the page-table latency is off the
-// copy path: a producer that waited for each tile's ids would be held to one
-// tile per global-load round trip.
+// All-heads decode (head dim 128).  A CTA covers `hpc` KV heads of a request
+// (every head in the balanced schedule): consumer warp w owns KV head
+// head0 + w and its GQA query rows (at most 16), and one producer warp stages
+// 16-key tiles of K and V for all of the CTA's heads at once, so each copy is
+// large and the copy engine's per-copy cost stays small against its bytes.
 //
-// Two schedules share the kernel:
-//  * fixed splits (num_splits >= 1): CTA (split, request) takes an equal
-//    share of the request's 16-key tiles; partials are merged by the last CTA
-//    of each (request, KV head);
-//  * balanced (num_splits == 0, persistent, one CTA per SM): the 16-key tiles
-//    of the whole batch are laid end to end and CTA c takes the c-th equal
-//    share, crossing request boundaries with the copy pipeline still full.  A
-//    request covered by one CTA is written directly; a split request leaves
-//    one partial per CTA (slot 0 when it is the CTA's first request, slot 1
-//    when its last) and the CTA that finishes last merges them.
+// Two copy modes:
+//  * slot rows (page size < 8, each slot one contiguous H_kv x 128 row): per
+//    key one bulk copy of the row for K and one for V, into shared memory at
+//    a pitch of H_kv * 256 + 16 bytes (the skew keeps ldmatrix reads
+//    conflict-free without a swizzle);
+//  * page boxes (page size a multiple of 16): per tile one TMA box
+//    {64 columns, 16 positions, hpc heads} per 64-column half and tensor, from
+//    a tensor map that lists position before head, so the box lands as
+//    [head][position][128-byte row] with the 128-byte swizzle: a head's 16
+//    rows are consecutive and their ldmatrix reads conflict-free.
+// Page ids are fetched AH_LOOKAHEAD tiles ahead of the copies (4-byte cp.async
+// into a shared ring), which keeps the page-table latency off the copy path.
+//
+// Two schedules:
+//  * fixed splits (num_splits >= 1): CTA (split, head group, request) takes
+//    an equal share of the request's 16-key tiles; partials are merged by the
+//    last CTA of each (request, KV head);
+//  * balanced (num_splits == 0, persistent, one CTA per SM, all heads): the
+//    16-key tiles of the whole batch are laid end to end and CTA c takes the
+//    c-th equal share, crossing request boundaries with the copy pipeline
+//    still full.  A request covered by one CTA is written directly; a split
+//    request leaves one partial per CTA (slot 0 when it is the CTA's first
+//    request, slot 1 when its last) and the CTA that finishes last merges.
 // ============================================================================
 
-constexpr int AH_BK = 16;        // keys per stage
+constexpr int AH_BK = 16;        // keys per tile (= per stage)
 constexpr int AH_NSTAGE = 3;
-constexpr int AH_MAXH = 8;       // KV heads per CTA (one consumer warp each)
-constexpr int AH_MAXPITCH = AH_MAXH * 256 + 16;
-constexpr int AH_MAXB = kDecodeBalancedMaxBatch;  // requests a balanced launch schedules
 constexpr int AH_LOOKAHEAD = 4;  // tiles the page-id fetch runs ahead of the copies
 constexpr int AH_RING = AH_LOOKAHEAD + 1;
-constexpr int AH_THREADS = (AH_MAXH + 1) * 32;
+constexpr int AH_MAXH = 8;       // KV heads per CTA (one consumer warp each)
+constexpr int AH_MAXB = kDecodeBalancedMaxBatch;  // requests a balanced launch schedules
+constexpr int AH_SMEM_MAX = 232448;
 
 // stage flags published by the producer beside each tile's key positions
 constexpr int AH_SEG_START = 1;  // first tile this CTA takes of the request
@@ -780,22 +785,35 @@ constexpr int AH_SEG_END = 2;    // last tile this CTA takes of the request
 constexpr int AH_REQ_START = 4;  // the request's first tile
 constexpr int AH_REQ_END = 8;    // the request's last tile
 
-struct AhSmem {
-  static constexpr uint32_t kStage = AH_BK * AH_MAXPITCH;  // one K (or V) stage
-  static constexpr uint32_t kK = 0;
-  static constexpr uint32_t kV = kK + AH_NSTAGE * kStage;
-  static constexpr uint32_t kPos = kV + AH_NSTAGE * kStage;        // int [NSTAGE][BK]
-  static constexpr uint32_t kMeta = kPos + AH_NSTAGE * AH_BK * 4;  // int [NSTAGE][2]
-  static constexpr uint32_t kRingPg = kMeta + AH_NSTAGE * 8;         // int [RING][BK] page ids
-  static constexpr uint32_t kRingJ = kRingPg + AH_RING * AH_BK * 4;  // int [RING][BK] key or -1
-  static constexpr uint32_t kPre = (kRingJ + AH_RING * AH_BK * 4 + 7) & ~7u;  // int64 [MAXB + 1]
-  static constexpr uint32_t kScan = kPre + (AH_MAXB + 1) * 8;  // int64 [warps]
-  static constexpr uint32_t kBar = kScan + 16 * 8;
-  static constexpr uint32_t kEnd = kBar + 2 * AH_NSTAGE * 8;
-  static constexpr size_t kDynamic = kEnd;
+// Shared-memory plan from the heads per CTA and the copy mode (the same
+// function on host and device).
+struct AhLayout {
+  uint32_t stage;  // bytes of one K (or V) stage
+  uint32_t k, v, pos, meta, ring_pg, ring_j, pre, scan, bar, end;
 };
-static_assert(AhSmem::kDynamic <= 232448, "all-heads decode smem plan exceeds 227 KB");
-static_assert(AhSmem::kBar % 8 == 0 && AhSmem::kPre % 8 == 0, "8-byte alignment");
+__host__ __device__ inline AhLayout ah_layout(int hpc, bool boxes, bool balanced) {
+  AhLayout L;
+  L.stage = boxes ? static_cast<uint32_t>(hpc) * AH_BK * 256u
+                  : AH_BK * (static_cast<uint32_t>(hpc) * 256u + 16u);
+  L.k = 0;
+  L.v = L.k + AH_NSTAGE * L.stage;
+  L.pos = L.v + AH_NSTAGE * L.stage;  // int [NSTAGE][BK]
+  L.meta = L.pos + AH_NSTAGE * AH_BK * 4;  // int [NSTAGE][2]
+  L.ring_pg = L.meta + AH_NSTAGE * 8;  // int [RING][BK] page ids
+  L.ring_j = L.ring_pg + AH_RING * AH_BK * 4;  // int [RING][BK] key or -1
+  L.pre = (L.ring_j + AH_RING * AH_BK * 4 + 7) & ~7u;  // int64 [MAXB + 1]
+  L.scan = L.pre + (balanced ? (AH_MAXB + 1) * 8 : 0);  // int64 [16]
+  L.bar = L.scan + 16 * 8;
+  L.end = L.bar + 2 * AH_NSTAGE * 8;
+  return L;
+}
+static_assert(AH_NSTAGE * 2 * (AH_BK * (AH_MAXH * 256 + 16)) + 18 * 1024 <= AH_SMEM_MAX,
+              "all-heads decode smem plan exceeds 227 KB");
+
+struct AhMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+};
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
                                          uint32_t bar) {
@@ -813,6 +831,12 @@ __device__ __forceinline__ void cp_async_commit() {
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+// 2^x on the MUFU (PTX ex2.approx, flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ah_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // A request's query run and key range [lo, hi) in 16-key tiles.
@@ -841,30 +865,37 @@ __device__ __forceinline__ int ah_cta_of(int64_t x, int64_t g, int64_t t) {
   return static_cast<int>(((x + 1) * g - 1) / t);
 }
 
-__global__ void __launch_bounds__(AH_THREADS, 1)
-decode_allheads_kernel(const __grid_constant__ AttnParams p) {
-  using S = AhSmem;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t sbase = smem_addr(smem);
-  int *sPos = reinterpret_cast<int *>(smem + S::kPos);
-  int *sMeta = reinterpret_cast<int *>(smem + S::kMeta);
-  int64_t *sPre = reinterpret_cast<int64_t *>(smem + S::kPre);
-  int64_t *sScan = reinterpret_cast<int64_t *>(smem + S::kScan);
-  const uint32_t full0 = sbase + S::kBar;
-  const uint32_t empty0 = full0 + AH_NSTAGE * 8;
-
+template <bool BOXES>
+__global__ void __launch_bounds__((AH_MAXH + 1) * 32, 1)
+decode_allheads_kernel(const __grid_constant__ AttnParams p,
+                       const __grid_constant__ AhMaps maps) {
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int hkv = p.h_kv;
+  const int nthreads = blockDim.x;
+  const int hpc = nthreads / 32 - 1;  // KV heads of this CTA = consumer warps
+  const int head0 = blockIdx.y * hpc;  // its first KV head
   const bool balanced = p.num_splits == 0;
-  const uint32_t blk = static_cast<uint32_t>(hkv) * 256u;  // one slot row
-  const uint32_t pitch = blk + 16u;
+  const AhLayout L = ah_layout(hpc, BOXES, balanced);
+  const uint32_t sbase = smem_addr(smem);
+  if (BOXES && (sbase & 1023u) != 0) {  // swizzled boxes need a 1024-byte aligned base
+    if (tid == 0) atomicOr(p.err, PKV_EFLAG_LAYOUT);
+    return;  // uniform
+  }
+  int *sPos = reinterpret_cast<int *>(smem + L.pos);
+  int *sMeta = reinterpret_cast<int *>(smem + L.meta);
+  int64_t *sPre = reinterpret_cast<int64_t *>(smem + L.pre);
+  int64_t *sScan = reinterpret_cast<int64_t *>(smem + L.scan);
+  const uint32_t full0 = sbase + L.bar;
+  const uint32_t empty0 = full0 + AH_NSTAGE * 8;
+  const uint32_t row_bytes = static_cast<uint32_t>(hpc) * 256u;  // the CTA's heads of one key
+  const uint32_t pitch = row_bytes + 16u;                         // slot-row mode
 
   if (tid == 0) {
     for (int s = 0; s < AH_NSTAGE; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, hkv);
+      mbar_init(empty0 + 8 * s, hpc);
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     fence_proxy_async();
@@ -875,7 +906,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
   int64_t T = 0, G = 1;
   if (balanced) {
     // exclusive prefix of tiles over the batch (each thread a contiguous run)
-    const int per = (p.batch + AH_THREADS - 1) / AH_THREADS;
+    const int per = (p.batch + nthreads - 1) / nthreads;
     const int e0 = min(p.batch, tid * per), e1 = min(p.batch, e0 + per);
     int64_t sum = 0;
     for (int b = e0; b < e1; ++b) sum += ah_request(p, b).ntiles;
@@ -893,7 +924,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
       sPre[b] = run;
       run += ah_request(p, b).ntiles;
     }
-    if (tid == AH_THREADS - 1) sPre[p.batch] = run;
+    if (tid == nthreads - 1) sPre[p.batch] = run;
     __syncthreads();
     T = sPre[p.batch];
     G = min(static_cast<int64_t>(gridDim.x), T);
@@ -922,15 +953,15 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
     n = max(1, t1 - t0);  // an empty share still reports (as an empty tile)
   }
 
-  if (warp == AH_MAXH) {
+  if (warp == hpc) {
     // ================================ producer ================================
-    // Lanes 0-15 handle one key of a tile each.  A fetch cursor runs
-    // AH_LOOKAHEAD tiles ahead of the copy cursor: per tile it puts each key's
-    // page id (or -1 for a key outside the range) in a shared ring slot with
-    // a 4-byte cp.async, one commit group per tile; the copy cursor waits for
-    // its tile's group and reads the ids back (each lane its own entries).
-    int *ring_pg = reinterpret_cast<int *>(smem + S::kRingPg);
-    int *ring_j = reinterpret_cast<int *>(smem + S::kRingJ);
+    // A fetch cursor runs AH_LOOKAHEAD tiles ahead of the copy cursor: per
+    // tile it puts page ids (slot rows: one per key, lanes 0-15; page boxes:
+    // one per tile, lane 0) in a shared ring slot with 4-byte cp.async, one
+    // commit group per tile, and the key (or -1) beside each; the copy cursor
+    // waits for its tile's group and reads the ids back (each lane its own).
+    int *ring_pg = reinterpret_cast<int *>(smem + L.ring_pg);
+    int *ring_j = reinterpret_cast<int *>(smem + L.ring_j);
     int b = b_first, t = t_first;
     AhReq r = ah_request(p, b);
     int fb = b, ft = t;
@@ -944,16 +975,31 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
         rr = ah_request(p, bb);
       }
     };
-    // fetch tile x (the fetch cursor's) into ring slot x % AH_RING
     auto fetch = [&](int x) {
-      if (lane < AH_BK) {
-        const int slot = (x % AH_RING) * AH_BK + lane;
-        const int j = (fr.t_lo + ft) * AH_BK + lane;
+      const int slot = (x % AH_RING) * AH_BK + lane;
+      const int key0 = (fr.t_lo + ft) * AH_BK;
+      if (BOXES) {
+        if (lane == 0) {
+          int jj = -1;
+          if (max(key0, fr.lo) < min(key0 + AH_BK, fr.hi)) {  // a key of the tile is live
+            const int pidx = key0 / p.page_size;  // the whole tile lies in this page
+            if (pidx < p.pt_cols) {
+              cp_async4(sbase + L.ring_pg + slot * 4,
+                        p.page_table + static_cast<int64_t>(fb) * p.pt_stride + pidx);
+              jj = key0;
+            } else {
+              atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
+            }
+          }
+          ring_j[slot] = jj;
+        }
+      } else if (lane < AH_BK) {
+        const int j = key0 + lane;
         int jj = -1;
         if (j >= fr.lo && j < fr.hi) {
           const int pidx = j / p.page_size;
           if (pidx < p.pt_cols) {
-            cp_async4(sbase + S::kRingPg + slot * 4,
+            cp_async4(sbase + L.ring_pg + slot * 4,
                       p.page_table + static_cast<int64_t>(fb) * p.pt_stride + pidx);
             jj = j;
           } else {
@@ -975,10 +1021,22 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
       else cp_async_commit();
       if (kt + AH_LOOKAHEAD + 1 < n) advance(fb, ft, fr);
       cp_async_wait_group<AH_LOOKAHEAD>();  // this tile's ids have landed
+      const int slot = (kt % AH_RING) * AH_BK + lane;
+      const int key0 = (r.t_lo + t) * AH_BK;
       int pos = -1;
-      int64_t koff = 0, voff = 0;
-      if (lane < AH_BK) {
-        const int slot = (kt % AH_RING) * AH_BK + lane;
+      int64_t koff = 0, voff = 0;  // slot-row mode: element offsets of the key's rows
+      int page = -1, inpage0 = 0;  // page-box mode: the tile's page
+      if (BOXES) {
+        if (lane == 0 && ring_j[slot] >= 0) {
+          const int64_t pg = ring_pg[slot];
+          if (pg < 0 || pg >= p.num_pages) atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
+          else page = static_cast<int>(pg);
+        }
+        page = __shfl_sync(0xffffffffu, page, 0);
+        inpage0 = key0 - (key0 / p.page_size) * p.page_size;
+        const int j = key0 + lane;
+        if (lane < AH_BK && page >= 0 && j >= r.lo && j < r.hi) pos = j;
+      } else if (lane < AH_BK) {
         const int j = ring_j[slot];
         if (j >= 0) {
           const int64_t pg = ring_pg[slot];
@@ -1007,37 +1065,62 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
         break;
       }
       const uint32_t full = full0 + 8 * st;
+      const uint32_t kdst = sbase + L.k + st * L.stage;
+      const uint32_t vdst = sbase + L.v + st * L.stage;
       if (lane < AH_BK) sPos[st * AH_BK + lane] = pos;
       if (lane == 0) {
         sMeta[2 * st] = b;
         sMeta[2 * st + 1] = flags;
       }
-      uint32_t bytes = pos >= 0 ? 2u * blk : 0u;
+      if (BOXES) {
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, page >= 0 ? 2u * L.stage : 0u);
+          if (page >= 0) {
+            const uint32_t half = L.stage / 2;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(full, bytes);
-      __syncwarp();
-      if (pos >= 0) {
-        bulk_g2s(sbase + S::kK + st * S::kStage + lane * pitch, p.k + koff, blk, full);
-        bulk_g2s(sbase + S::kV + st * S::kStage + lane * pitch, p.v + voff, blk, full);
+            for (int hf = 0; hf < 2; ++hf) {
+              tma_load_4d(kdst + hf * half, &maps.k, hf * 64, inpage0, head0, page, full);
+              tma_load_4d(vdst + hf * half, &maps.v, hf * 64, inpage0, head0, page, full);
+            }
+          }
+        }
+      } else {
+        uint32_t bytes = pos >= 0 ? 2u * row_bytes : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(full, bytes);
+        __syncwarp();
+        if (pos >= 0) {
+          bulk_g2s(kdst + lane * pitch, p.k + koff, row_bytes, full);
+          bulk_g2s(vdst + lane * pitch, p.v + voff, row_bytes, full);
+        }
       }
       // next tile (a balanced run moves on to the next request with tiles;
       // a fixed split never leaves its request)
       if (kt + 1 < n) advance(b, t, r);
     }
-    cp_async_wait_group<0>();
+    cp_async_commit();
+    cp_async_wait_group<0>();  // no ring write outlives the CTA
     return;
   }
-  if (warp >= hkv) return;  // no KV head for this warp (never waited on)
+  if (warp > hpc || head0 + warp >= p.h_kv) return;  // no KV head for this warp
 
   // ================================ consumers ================================
-  const int h = warp;  // KV head
+  const int w = warp;          // head within the CTA
+  const int h = head0 + w;     // KV head
   const int g = lane >> 2, tq = lane & 3;
-  const uint32_t hoff = static_cast<uint32_t>(h) * 256u;
   const int64_t rows_total = static_cast<int64_t>(p.total_q) * p.h_q;
   const int64_t rows_req = static_cast<int64_t>(p.max_seqlen_q) * p.h_q;  // balanced slots
   const bool use_upper = p.causal || p.window_left >= 0;
+  // byte offset of 16-byte chunk c of key `key` of this head within a stage
+  auto soff = [&](int key, int c) -> uint32_t {
+    if (BOXES)
+      return static_cast<uint32_t>((c >> 3) * (hpc * 2048) + w * 2048 + key * 128 +
+                                   (((c & 7) ^ (key & 7)) << 4));
+    return static_cast<uint32_t>(key) * pitch + static_cast<uint32_t>(w * 256 + c * 16);
+  };
 
   uint32_t qf[8][4];
   float o[16][4];
@@ -1081,8 +1164,8 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
       m_run[0] = m_run[1] = -INFINITY;
       l_run[0] = l_run[1] = 0.f;
     }
-    const uint32_t kb = sbase + S::kK + st * S::kStage + hoff;
-    const uint32_t vb = sbase + S::kV + st * S::kStage + hoff;
+    const uint32_t kb = sbase + L.k + st * L.stage;
+    const uint32_t vb = sbase + L.v + st * L.stage;
     const int *pos_st = sPos + st * AH_BK;
     // zero this head's V rows of skipped keys (a masked key must add exactly 0)
     const bool any_skipped = __any_sync(0xffffffffu, pos_st[lane & 15] < 0);
@@ -1092,7 +1175,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
         const int idx = i * 32 + lane;
         const int rr = idx >> 4, cc = idx & 15;
         if (pos_st[rr] < 0)
-          *reinterpret_cast<uint4 *>(smem + S::kV + st * S::kStage + rr * pitch + hoff + cc * 16) =
+          *reinterpret_cast<uint4 *>(smem + L.v + st * L.stage + soff(rr, cc)) =
               make_uint4(0, 0, 0, 0);
       }
       __syncwarp();
@@ -1107,7 +1190,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb + key * pitch + (2 * kk + kc) * 16, b0, b1, b2, b3);
+        ldsm_x4(kb + soff(key, 2 * kk + kc), b0, b1, b2, b3);
         mma_bf16(sc[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
         mma_bf16(sc[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
       }
@@ -1129,6 +1212,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
         if (p.window_left >= 0 && kp < rpos[hh] - p.window_left) masked = true;
         sc[nn][e] = masked ? -INFINITY : sc[nn][e] * p.scale_log2;
       }
+    float alpha[2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       float mx = fmaxf(fmaxf(sc[0][2 * hh], sc[0][2 * hh + 1]), fmaxf(sc[1][2 * hh], sc[1][2 * hh + 1]));
@@ -1136,20 +1220,25 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float m_new = fmaxf(m_run[hh], mx);
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = exp2f(m_run[hh] - m_use);
+      alpha[hh] = ah_exp2(m_run[hh] - m_use);  // exactly 1 while the max holds
       m_run[hh] = m_new;
       float sum = 0.f;
 #pragma unroll
       for (int nn = 0; nn < 2; ++nn) {
-        sc[nn][2 * hh] = exp2f(sc[nn][2 * hh] - m_use);
-        sc[nn][2 * hh + 1] = exp2f(sc[nn][2 * hh + 1] - m_use);
+        sc[nn][2 * hh] = ah_exp2(sc[nn][2 * hh] - m_use);
+        sc[nn][2 * hh + 1] = ah_exp2(sc[nn][2 * hh + 1] - m_use);
         sum += sc[nn][2 * hh] + sc[nn][2 * hh + 1];
       }
-      l_run[hh] = l_run[hh] * alpha + sum;
+      l_run[hh] = l_run[hh] * alpha[hh] + sum;
+    }
+    // rescale O only when some row's max moved
+    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
       for (int nn = 0; nn < 16; ++nn) {
-        o[nn][2 * hh] *= alpha;
-        o[nn][2 * hh + 1] *= alpha;
+        o[nn][0] *= alpha[0];
+        o[nn][1] *= alpha[0];
+        o[nn][2] *= alpha[1];
+        o[nn][3] *= alpha[1];
       }
     }
     const uint32_t a0 = pack_bf16(sc[0][0], sc[0][1]);
@@ -1162,12 +1251,12 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb + key * pitch + (2 * cc + (m >> 1)) * 16, b0, b1, b2, b3);
+        ldsm_x4_t(vb + soff(key, 2 * cc + (m >> 1)), b0, b1, b2, b3);
         mma_bf16(o[2 * cc], a0, a1, a2, a3, b0, b1);
         mma_bf16(o[2 * cc + 1], a0, a1, a2, a3, b2, b3);
       }
     }
-    if (any_skipped) fence_proxy_async();  // generic zeros before bulk rewrites
+    if (any_skipped) fence_proxy_async();  // generic zeros before async rewrites
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * st);
 
@@ -1176,12 +1265,12 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
     const bool whole = balanced ? (seg_req_start && (flags & AH_REQ_END) != 0) : p.num_splits == 1;
     const int slot = first_seg ? 0 : 1;
     first_seg = false;
-    float L[2];
+    float Lsum[2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      L[hh] = l_run[hh];
-      L[hh] += __shfl_xor_sync(0xffffffffu, L[hh], 1);
-      L[hh] += __shfl_xor_sync(0xffffffffu, L[hh], 2);
+      Lsum[hh] = l_run[hh];
+      Lsum[hh] += __shfl_xor_sync(0xffffffffu, Lsum[hh], 1);
+      Lsum[hh] += __shfl_xor_sync(0xffffffffu, Lsum[hh], 2);
     }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -1190,8 +1279,8 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
       const int u = rr / p.group;
       const int tok = r.q_begin + u;
       const int head = h * p.group + rr % p.group;
-      const float inv = L[hh] > 0.f ? 1.f / L[hh] : 0.f;
-      const float lse_nat = L[hh] > 0.f ? (m_run[hh] + log2f(L[hh])) * kLn2 : -INFINITY;
+      const float inv = Lsum[hh] > 0.f ? 1.f / Lsum[hh] : 0.f;
+      const float lse_nat = Lsum[hh] > 0.f ? (m_run[hh] + log2f(Lsum[hh])) * kLn2 : -INFINITY;
       if (whole) {
         bf16 *dst = p.out + static_cast<int64_t>(tok) * p.o_st + static_cast<int64_t>(head) * p.o_sh;
 #pragma unroll
@@ -1229,7 +1318,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
     __syncwarp();
     int last = 0;
     if (lane == 0)
-      last = atomicAdd(p.ws_counter + static_cast<int64_t>(b) * hkv + h, 1) == expected - 1;
+      last = atomicAdd(p.ws_counter + static_cast<int64_t>(b) * p.h_kv + h, 1) == expected - 1;
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) continue;
     __threadfence();
@@ -1251,10 +1340,10 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p) {
       if (Ms != -INFINITY) {
         for (int sp = 0; sp < expected; ++sp) {
           const int64_t sidx = src(sp);
-          const float w = exp2f((__ldcg(p.ws_lse + sidx) - Ms) * kLog2e);
-          wsum += w;
+          const float wgt = exp2f((__ldcg(p.ws_lse + sidx) - Ms) * kLog2e);
+          wsum += wgt;
           const float4 v4 = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + sidx * p.dv + lane * 4));
-          acc[0] += w * v4.x; acc[1] += w * v4.y; acc[2] += w * v4.z; acc[3] += w * v4.w;
+          acc[0] += wgt * v4.x; acc[1] += wgt * v4.y; acc[2] += wgt * v4.z; acc[3] += wgt * v4.w;
         }
       }
       const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
@@ -1350,33 +1439,88 @@ int launch_typed(const AttnParams &p, const DecodeMaps &maps, cudaStream_t strea
 
 }  // namespace
 
+namespace {
+
+// 4-D map over a paged cache listing position before head (dims innermost
+// first: D, position, head, page), whatever the strides' order; one box =
+// one 64-column half of 16 positions of `hpc` heads of one page.
+bool encode_allheads_map(CUtensorMap *map, const bf16 *base, int h_kv, int page,
+                         int64_t num_pages, int64_t s_head, int64_t s_pos, int64_t s_page,
+                         int hpc) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(page), static_cast<cuuint64_t>(h_kv),
+                        static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s_pos) * 2,
+                           static_cast<cuuint64_t>(s_head) * 2,
+                           static_cast<cuuint64_t>(s_page) * 2};
+  cuuint32_t box[4] = {64, AH_BK, static_cast<cuuint32_t>(hpc), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<bf16 *>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_allheads_maps(AhMaps *m, const AttnParams &p, int hpc) {
+  return encode_allheads_map(&m->k, p.k, p.h_kv, p.page_size, p.num_pages, p.k_sh, p.k_spos,
+                             p.k_sp, hpc) &&
+         encode_allheads_map(&m->v, p.v, p.h_kv, p.page_size, p.num_pages, p.v_sh, p.v_spos,
+                             p.v_sp, hpc);
+}
+
+}  // namespace
+
 bool decode_allheads_eligible(const AttnParams &p) {
   if (p.topk != nullptr || p.d != 128 || p.dv != 128) return false;
-  if (p.page_size >= 8 || p.h_kv > AH_MAXH) return false;
-  if (p.max_seqlen_q < 1 || p.max_seqlen_q * p.group > 16) return false;
-  // every slot's heads form one contiguous H_kv x D row in K and in V
-  return p.k_sh == 128 && p.k_spos == static_cast<int64_t>(p.h_kv) * 128 && p.v_sh == 128 &&
-         p.v_spos == static_cast<int64_t>(p.h_kv) * 128;
+  if (p.h_kv > AH_MAXH || p.max_seqlen_q < 1 || p.max_seqlen_q * p.group > 16) return false;
+  if (p.page_size < 8) {
+    // slot rows: every slot's heads form one contiguous H_kv x 128 row
+    return p.k_sh == 128 && p.k_spos == static_cast<int64_t>(p.h_kv) * 128 &&
+           p.v_sh == 128 && p.v_spos == static_cast<int64_t>(p.h_kv) * 128;
+  }
+  if (p.page_size % AH_BK != 0 || p.num_pages > 0x7fffffffLL) return false;
+  // page boxes: the driver must accept the maps (strides, alignment)
+  AhMaps m;
+  return encode_allheads_maps(&m, p, p.h_kv);
 }
 
 int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
   if (p.batch == 0) return PKV_OK;
   if (!decode_allheads_eligible(p)) return PKV_ERR_UNSUPPORTED;
   if (p.batch > 65535 || p.num_splits > 65535) return PKV_ERR_UNSUPPORTED;
-  if (p.num_splits == 0 && p.batch > AH_MAXB) return PKV_ERR_UNSUPPORTED;
+  const bool balanced = p.num_splits == 0;
+  if (balanced && p.batch > AH_MAXB) return PKV_ERR_UNSUPPORTED;
+  const bool boxes = p.page_size >= 8;
+  // page boxes run the balanced schedule only: with fixed splits a CTA that
+  // covers every head turns a long request's chunk into one long work item
+  if (boxes && !balanced) return PKV_ERR_UNSUPPORTED;
+  const int hpc = p.h_kv;
+  const AhLayout L = ah_layout(hpc, boxes, balanced);
+  if (L.end > AH_SMEM_MAX) return PKV_ERR_UNSUPPORTED;
   static bool configured[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (dev >= 64 || !configured[dev]) {
-    if (cudaFuncSetAttribute(decode_allheads_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(AhSmem::kDynamic)) != cudaSuccess)
+    if (cudaFuncSetAttribute(decode_allheads_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, AH_SMEM_MAX) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(decode_allheads_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, AH_SMEM_MAX) !=
+            cudaSuccess)
       return PKV_ERR_CUDA;
     if (dev < 64) configured[dev] = true;
   }
-  // balanced: one persistent CTA per SM; fixed splits: (split, request)
-  const dim3 grid = p.num_splits == 0 ? dim3(kDecodeBalancedCtas, 1, 1)
-                                      : dim3(p.num_splits, 1, p.batch);
-  decode_allheads_kernel<<<grid, AH_THREADS, AhSmem::kDynamic, stream>>>(p);
+  AhMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  if (boxes && !encode_allheads_maps(&maps, p, hpc)) return PKV_ERR_UNSUPPORTED;
+  // balanced: one persistent CTA per SM; fixed splits: (split, 1, request)
+  const dim3 grid = balanced ? dim3(kDecodeBalancedCtas, 1, 1)
+                             : dim3(p.num_splits, 1, p.batch);
+  const dim3 block((hpc + 1) * 32);
+  if (boxes)
+    decode_allheads_kernel<true><<<grid, block, L.end, stream>>>(p, maps);
+  else
+    decode_allheads_kernel<false><<<grid, block, L.end, stream>>>(p, maps);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -60,11 +60,12 @@ uint32_t *device_error_word();
 int launch_decode_gqa(const AttnParams &p, cudaStream_t stream);
 // Rows per (request, kv head) tile used by the decode kernel.
 constexpr int kDecodeRowTile = 16;
-// Small-page decode (page size < 8, head dim 128, <= 8 KV heads, <= 16 query
-// rows per KV head, each slot one contiguous H_kv x 128 row in K and in V):
-// one CTA covers every KV head of a request.  num_splits == 0 selects its
-// balanced persistent schedule: kDecodeBalancedCtas CTAs share the batch's
-// 16-key tiles equally (batches up to kDecodeBalancedMaxBatch requests).
+// All-heads decode (head dim 128, <= 8 KV heads, <= 16 query rows per KV
+// head; page size < 8 with each slot one contiguous H_kv x 128 row in K and
+// in V, or page size a multiple of 16): one CTA covers every KV head of a
+// request.  num_splits == 0 selects its balanced persistent schedule:
+// kDecodeBalancedCtas CTAs share the batch's 16-key tiles equally (batches up
+// to kDecodeBalancedMaxBatch requests); fixed splits serve page sizes < 8.
 constexpr int kDecodeBalancedCtas = kNumSMs;
 constexpr int kDecodeBalancedMaxBatch = 2048;
 bool decode_allheads_eligible(const AttnParams &p);

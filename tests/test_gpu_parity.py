@@ -351,11 +351,13 @@ def test_bad_page_ids_are_skipped_and_flagged():
     wl.page_table[1, 2] = 10_000_000
     wl.page_table[2, 0] = -5
     g = wl.to(DEV)
-    out, lse = gpu_attn(g, num_splits=2)
-    ref_o, ref_l, skipped = oracle_attn(wl)
-    assert skipped > 0
-    check_close(out, lse, ref_o, ref_l, "bad pages")
-    assert pkv.get_error_flags() & pkv.EFLAG_PAGE_OOB
+    for splits in (2, 0):
+        pkv.clear_error_flags()
+        out, lse = gpu_attn(g, num_splits=splits)
+        ref_o, ref_l, skipped = oracle_attn(wl)
+        assert skipped > 0
+        check_close(out, lse, ref_o, ref_l, f"bad pages splits={splits}")
+        assert pkv.get_error_flags() & pkv.EFLAG_PAGE_OOB
 
 
 # ----------------------------------------------- full-size workloads, sampled
@@ -427,7 +429,7 @@ def test_page_box_sizes(page_size, q_len, window, causal):
                         len_lo=q_len, len_hi=1500, batch=6,
                         pool_tokens=6 * (1500 + page_size) * 2)
     g = wl.to(DEV)
-    for splits in (1, 3):
+    for splits in (1, 3, 0):  # 0: balanced all-heads schedule (page boxes when P % 16 == 0)
         out, lse = gpu_attn(g, num_splits=splits)
         ref_o, ref_l, _ = oracle_attn(wl)
         check_close(out, lse, ref_o, ref_l, f"P={page_size} splits={splits}")
@@ -451,7 +453,7 @@ def test_garbage_outside_valid_rows_never_leaks(page_size):
     wl.k_cache[~valid] = float("nan")
     wl.v_cache[~valid] = float("nan")
     g = wl.to(DEV)
-    for splits in (1, 4):
+    for splits in (1, 4, 0):
         out, lse = gpu_attn(g, num_splits=splits)
         ref_o, ref_l, _ = oracle_attn(wl)
         check_close(out, lse, ref_o, ref_l, f"nan P={page_size} splits={splits}")
@@ -531,9 +533,10 @@ def test_head_major_cache_layout():
     g = wl.to(DEV)
     g.k_cache = k_hm.to(DEV).permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
     g.v_cache = v_hm.to(DEV).permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
-    out, lse = gpu_attn(g, num_splits=2)
-    ref_o, ref_l, _ = oracle_attn(wl)
-    check_close(out, lse, ref_o, ref_l, "head-major")
+    for splits in (2, 0):
+        out, lse = gpu_attn(g, num_splits=splits)
+        ref_o, ref_l, _ = oracle_attn(wl)
+        check_close(out, lse, ref_o, ref_l, f"head-major splits={splits}")
 
 
 # ------------------------------------------------ varlen extend (tcgen05 path)
