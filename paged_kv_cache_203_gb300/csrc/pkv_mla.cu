@@ -13,13 +13,16 @@
 // list).  The output accumulator for 128 heads x 256 value dims fills half
 // of TMEM; both halves recompute the scores (the full 128 x 512 accumulator
 // would leave no TMEM columns for them).
-//   warps 5-8 producers: per 32-key tile, map the listed positions through
-//            the page table once, then gather the 576-wide rows with 16-byte
-//            cp.async into a [9 chunks][32 rows][128 B] 128-byte-swizzled
-//            tile (zero rows for skipped keys), completion on mbarriers;
-//   warp 4   MMA issuer: S = Q K^T (M 128 heads, N 32 keys, K 576: 36
+//   warps 5-12 producers: per 16-key tile, gather the 576-wide rows with
+//            16-byte cp.async into a [9 chunks][16 rows][128 B] 128-byte-
+//            swizzled tile (zero rows for skipped keys), two rows per warp,
+//            completion on mbarriers, four tiles in flight.  The list
+//            entries and page ids of a tile are loaded one and two tiles
+//            ahead, so the two dependent lookups stay off the copy path
+//            (with them on it, each tile waited two global round trips);
+//   warp 4   MMA issuer: S = Q K^T (M 128 heads, N 16 keys, K 576: 36
 //            MMAs, both operands K-major), then O += P V (M 128, N 256 value
-//            dims, K 32 keys: V is an MN-major view of the same key tile);
+//            dims, K 16 keys: V is an MN-major view of the same key tile);
 //   warps 0-3 softmax (thread = head = TMEM lane): scores from TMEM, masks,
 //            online softmax in the log2 domain with a lazy reference max
 //            (O rescaled in TMEM only when the row max grows by > 2^8), P
@@ -40,34 +43,41 @@ constexpr int H = 128;        // query heads (the M dimension)
 constexpr int DQK = 576;      // latent + rope
 constexpr int DV = 512;       // latent (value) dims
 constexpr int DVH = 256;      // value dims per CTA
-constexpr int BKEYS = 32;     // keys per tile
+constexpr int BKEYS = 16;     // keys per tile
+constexpr int NSTG = 4;       // key-tile stages
 constexpr int NCH = DQK / 64; // 64-column chunks of a row (9)
-constexpr int NSOFT = 4, NPROD = 4;
+constexpr int NSOFT = 4, NPROD = 8;
 constexpr int kMmaWarp = NSOFT;
 constexpr int kProdWarp0 = NSOFT + 1;
 constexpr int NTHREADS = (NSOFT + 1 + NPROD) * 32;
+constexpr int kRowsPerWarp = BKEYS / NPROD;         // 2
 constexpr uint32_t kQBytes = NCH * H * 128;         // 147456
-constexpr uint32_t kKTile = NCH * BKEYS * 128;      // 36864
-constexpr uint32_t kPTile = H * BKEYS * 2;          // 8192
-constexpr int kPrefetchTiles = 4;  // L2 prefetch distance (tiles)
+constexpr uint32_t kKTile = NCH * BKEYS * 128;      // 18432
+constexpr uint32_t kPTile = H * BKEYS * 2;          // 4096
 
 struct Smem {
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kQBytes;          // 2 stages
-  static constexpr uint32_t kP = kK + 2 * kKTile;
-  static constexpr uint32_t kPos = kP + kPTile;         // int [2][32]
-  static constexpr uint32_t kRow = kPos + 2 * BKEYS * 4;  // int64 [2][32]
-  static constexpr uint32_t kBar = kRow + 2 * BKEYS * 8;
-  // q_full, full[2], empty[2], s_full[2], s_free[2], p_full, o_done
-  static constexpr int kNumBars = 11;
+  static constexpr uint32_t kK = kQ + kQBytes;          // NSTG stages
+  static constexpr uint32_t kP = kK + NSTG * kKTile;
+  static constexpr uint32_t kPos = kP + kPTile;         // int [NSTG][BKEYS]
+  static constexpr uint32_t kBar = kPos + NSTG * BKEYS * 4;
+  // q_full, full[NSTG], empty[NSTG], s_full[2], s_free[2], p_full, o_done
+  static constexpr int kNumBars = 3 + 2 * NSTG + 4;
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kFlag = kTmemSlot + 16;     // softmax: split ticket
-  static constexpr uint32_t kProdFlag = kFlag + 16;    // producers: stage free
-  static constexpr uint32_t kEnd = kProdFlag + 16;
+  static constexpr uint32_t kEnd = kFlag + 16;
   static constexpr size_t kDynamic = kEnd;  // base must be 1024-aligned (checked)
 };
 static_assert(Smem::kDynamic <= 232448, "shared memory plan exceeds 227 KB");
-enum BarId { Q_FULL = 0, FULL = 1, EMPTY = 3, S_FULL = 5, S_FREE = 7, P_FULL = 9, O_DONE = 10 };
+enum BarId {
+  Q_FULL = 0,
+  FULL = 1,
+  EMPTY = FULL + NSTG,
+  S_FULL = EMPTY + NSTG,
+  S_FREE = S_FULL + 2,
+  P_FULL = S_FREE + 2,
+  O_DONE = P_FULL + 1
+};
 
 // byte offset of 16-byte chunk c (0..71) of row r in a 128-byte-swizzled
 // [9][nrows][128 B] tile
@@ -75,10 +85,10 @@ template <int NROWS>
 __device__ __forceinline__ uint32_t sw_off(int r, int c) {
   return static_cast<uint32_t>((c >> 3) * (NROWS * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
-// P [128 heads][32 keys] bf16, unswizzled core matrices: 8 rows x 16 B,
-// 128 B apart along the keys, 512 B apart along the heads
+// P [128 heads][16 keys] bf16, unswizzled core matrices: 8 rows x 16 B,
+// 128 B apart along the keys, 256 B apart along the heads
 __device__ __forceinline__ uint32_t p_off(int m, int c) {
-  return static_cast<uint32_t>((m >> 3) * 512 + c * 128 + (m & 7) * 16);
+  return static_cast<uint32_t>((m >> 3) * 256 + c * 128 + (m & 7) * 16);
 }
 
 struct MlaMaps {
@@ -90,10 +100,8 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_addr(smem);
   int *sPos = reinterpret_cast<int *>(smem + Smem::kPos);
-  int64_t *sRow = reinterpret_cast<int64_t *>(smem + Smem::kRow);
   uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + Smem::kTmemSlot);
   int *sFlag = reinterpret_cast<int *>(smem + Smem::kFlag);
-  volatile int *sProdFlag = reinterpret_cast<volatile int *>(smem + Smem::kProdFlag);
   auto bar = [&](int id) { return sbase + Smem::kBar + 8u * id; };
 
   const int split = blockIdx.x;
@@ -130,9 +138,11 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
 
   if (tid == 0) {
     mbar_init(bar(Q_FULL), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NSTG; ++s) {
       mbar_init(bar(FULL + s), NPROD * 32);
       mbar_init(bar(EMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar(S_FULL + s), 1);
       mbar_init(bar(S_FREE + s), NSOFT);
     }
@@ -157,79 +167,74 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
         tma_load_3d(sbase + Smem::kQ + c * (H * 128), &maps.q, c * 64, 0, t, bar(Q_FULL));
     }
     const int32_t *list = p.topk + static_cast<int64_t>(t) * p.topk_stride;
-    // position j of the list -> (logical position or -1, element offset of
-    // its row or -1); `flag` raises the error bits (current tile only)
-    auto map_key = [&](int j, bool flag, int &pos, int64_t &off) {
-      pos = -1;
-      off = -1;
-      if (j >= (tile0 + n_kv) * BKEYS || j >= p.topk_len) return;
-      const int idx = list[j];
-      if (idx < 0 || idx >= kv_len) {
-        if (flag && idx != -1) atomicOr(p.err, PKV_EFLAG_TOPK_OOB);
-        return;
-      }
-      const int pidx = idx / p.page_size;
-      if (pidx >= p.pt_cols) {
-        if (flag) atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
-        return;
-      }
-      const int64_t pg = p.page_table[static_cast<int64_t>(b) * p.pt_stride + pidx];
-      if (pg < 0 || pg >= p.num_pages) {
-        if (flag) atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
-        return;
-      }
-      pos = idx;
-      off = pg * p.k_sp + static_cast<int64_t>(idx - pidx * p.page_size) * p.k_spos;
+    const int pw = warp - kProdWarp0;  // producer warp: rows pw + 8 i of each tile
+    const int end_j = (tile0 + n_kv) * BKEYS;
+    // lanes 0-15 follow key lane of the tile two ahead (list entry), one
+    // ahead (page id) and current (row offset)
+    auto load_idx = [&](int tile) -> int {
+      const int j = (tile0 + tile) * BKEYS + lane;
+      return (lane < BKEYS && tile < n_kv && j < end_j && j < p.topk_len) ? list[j] : -1;
     };
-    // warm L2 with the rows of the first tiles (HBM latency off the ring)
-    if (ptid < BKEYS) {
-      for (int a = 0; a < kPrefetchTiles && a < n_kv; ++a) {
-        int pos;
-        int64_t off;
-        map_key((tile0 + a) * BKEYS + ptid, false, pos, off);
-        if (off >= 0) prefetch_l2(p.k + off, DQK * 2);
-      }
-    }
+    auto page_of = [&](int idx) -> int64_t {
+      if (idx < 0 || idx >= kv_len) return -1;
+      const int pidx = idx / p.page_size;
+      if (pidx >= p.pt_cols) return -2;
+      return p.page_table[static_cast<int64_t>(b) * p.pt_stride + pidx];
+    };
+    int idx_cur = load_idx(0);
+    int64_t pg_cur = page_of(idx_cur);
+    int idx_nxt = load_idx(1);
     for (int jj = 0; jj < n_kv; ++jj) {
-      const int s = jj & 1;
-      // rows kPrefetchTiles tiles ahead into L2, and this tile's mapping,
-      // both issued before waiting for the stage
+      const int s = jj % NSTG;
+      // lookups for the next tiles go out first; their latency overlaps this
+      // tile's wait and copies
+      const int64_t pg_nxt = page_of(idx_nxt);
+      const int idx_nn = load_idx(jj + 2);
+      // this tile's key lane: position (or -1) and row offset
       int pos = -1;
       int64_t off = -1;
-      if (ptid < BKEYS) {
-        int pos_a;
-        int64_t off_a;
-        map_key((tile0 + jj + kPrefetchTiles) * BKEYS + ptid, false, pos_a, off_a);
-        if (off_a >= 0) prefetch_l2(p.k + off_a, DQK * 2);
-        map_key((tile0 + jj) * BKEYS + ptid, true, pos, off);
+      if (lane < BKEYS) {
+        if (idx_cur < -1 || idx_cur >= kv_len) {
+          if (pw == 0 && idx_cur != -1 && (tile0 + jj) * BKEYS + lane < p.topk_len)
+            atomicOr(p.err, PKV_EFLAG_TOPK_OOB);
+        } else if (idx_cur >= 0) {
+          if (pg_cur == -2) {
+            if (pw == 0) atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
+          } else if (pg_cur < 0 || pg_cur >= p.num_pages) {
+            if (pw == 0) atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
+          } else {
+            pos = idx_cur;
+            off = pg_cur * p.k_sp +
+                  static_cast<int64_t>(idx_cur - (idx_cur / p.page_size) * p.page_size) * p.k_spos;
+          }
+        }
       }
-      // one thread waits for the stage; every producer thread always meets
-      // at the barrier and leaves the loop together on a timeout
-      if (ptid == 0) {
-        const bool free_ok = jj < 2 || mbar_wait(bar(EMPTY + s), ((jj >> 1) - 1) & 1);
-        if (!free_ok) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
-        *sProdFlag = free_ok ? 1 : 0;
+      int ok = 1;
+      if (lane == 0 && jj >= NSTG)
+        ok = mbar_wait(bar(EMPTY + s), ((jj / NSTG) & 1) ^ 1) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+        break;
       }
-      asm volatile("bar.sync 3, %0;\n" ::"n"(NPROD * 32) : "memory");
-      if (*sProdFlag == 0) break;
-      if (ptid < BKEYS) {
-        sPos[s * BKEYS + ptid] = pos;
-        sRow[s * BKEYS + ptid] = off;
-      }
-      // (the previous tile's readers of slot s passed this tile's first
-      // barrier, so no one still reads what is rewritten here)
-      asm volatile("bar.sync 3, %0;\n" ::"n"(NPROD * 32) : "memory");
-      // gather: 32 rows x 72 chunks of 16 B
+      if (pw == 0 && lane < BKEYS) sPos[s * BKEYS + lane] = pos;
+      // gather this warp's rows: 72 chunks of 16 B each, lanes along the row
       const uint32_t kdst = sbase + Smem::kK + s * kKTile;
-#pragma unroll 2
-      for (int e = ptid; e < BKEYS * (DQK / 8); e += NPROD * 32) {
-        const int r = e / (DQK / 8), c = e - r * (DQK / 8);
-        const int64_t off = sRow[s * BKEYS + r];
-        const bf16 *src = off >= 0 ? p.k + off + c * 8 : p.k;
-        cp_async16(kdst + sw_off<BKEYS>(r, c), src, off >= 0 ? 16 : 0);
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int r = pw + NPROD * i;
+        const int64_t ro = __shfl_sync(0xffffffffu, off, r);
+        const bf16 *src = ro >= 0 ? p.k + ro : p.k;
+        const int nbytes = ro >= 0 ? 16 : 0;
+#pragma unroll
+        for (int c = lane; c < DQK / 8; c += 32)
+          cp_async16(kdst + sw_off<BKEYS>(r, c), ro >= 0 ? src + c * 8 : src, nbytes);
       }
       cp_async_arrive(bar(FULL + s));
       mbar_arrive(bar(FULL + s));
+      idx_cur = idx_nxt;
+      pg_cur = pg_nxt;
+      idx_nxt = idx_nn;
     }
   } else if (warp == kMmaWarp) {
     // ================================== MMA ==================================
@@ -239,9 +244,9 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
       bool ok = n_kv == 0 || mbar_wait(bar(Q_FULL), 0);
       for (int j = 0; ok && j <= n_kv; ++j) {
         if (j < n_kv) {  // S_j = Q K_j^T
-          const int s = j & 1;
-          ok = mbar_wait(bar(FULL + s), (j >> 1) & 1) &&
-               (j < 2 || mbar_wait(bar(S_FREE + s), ((j >> 1) - 1) & 1));
+          const int s = j % NSTG, sb = j & 1;
+          ok = mbar_wait(bar(FULL + s), (j / NSTG) & 1) &&
+               (j < 2 || mbar_wait(bar(S_FREE + sb), ((j >> 1) - 1) & 1));
           if (!ok) break;
           tc_fence_after();
           const uint32_t kb = sbase + Smem::kK + s * kKTile;
@@ -249,23 +254,21 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
           for (int ks = 0; ks < DQK / 16; ++ks) {
             const uint32_t qoff = (ks >> 2) * (H * 128) + (ks & 3) * 32;
             const uint32_t koff = (ks >> 2) * (BKEYS * 128) + (ks & 3) * 32;
-            umma(tS0 + s * BKEYS, smem_desc(sbase + Smem::kQ + qoff, 0, 1024, 2),
+            umma(tS0 + sb * BKEYS, smem_desc(sbase + Smem::kQ + qoff, 0, 1024, 2),
                  smem_desc(kb + koff, 0, 1024, 2), kIdescQK, ks > 0);
           }
-          umma_commit(bar(S_FULL + s));
+          umma_commit(bar(S_FULL + sb));
         }
         if (j >= 1) {  // O += P_{j-1} V_{j-1}
           const int jj = j - 1;
-          const int s = jj & 1;
+          const int s = jj % NSTG;
           ok = mbar_wait(bar(P_FULL), jj & 1);
           if (!ok) break;
           tc_fence_after();
           const uint32_t vb = sbase + Smem::kK + s * kKTile + hv * 4 * (BKEYS * 128);
-#pragma unroll
-          for (int ks = 0; ks < BKEYS / 16; ++ks)
-            umma(tO, smem_desc(sbase + Smem::kP + ks * 256, 128, 512, 0),
-                 smem_desc(vb + ks * 2048, BKEYS * 128, 1024, 2), kIdescPV,
-                 (jj > 0 || ks > 0) ? 1u : 0u);
+          static_assert(BKEYS == 16, "one K=16 step of P V per tile");
+          umma(tO, smem_desc(sbase + Smem::kP, 128, 256, 0),
+               smem_desc(vb, BKEYS * 128, 1024, 2), kIdescPV, jj > 0 ? 1u : 0u);
           umma_commit(bar(O_DONE));
           umma_commit(bar(EMPTY + s));
         }
@@ -283,15 +286,16 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
     float l = 0.f;
     bool ok = true;
     for (int jj = 0; jj < n_kv; ++jj) {
-      const int s = jj & 1;
-      const uint32_t ph = (jj >> 1) & 1;
-      if (!(ok = mbar_wait(bar(S_FULL + s), ph) && mbar_wait(bar(FULL + s), ph))) break;
+      const int s = jj % NSTG, sb = jj & 1;
+      if (!(ok = mbar_wait(bar(S_FULL + sb), (jj >> 1) & 1) &&
+                 mbar_wait(bar(FULL + s), (jj / NSTG) & 1)))
+        break;
       tc_fence_after();
       float x[BKEYS];
-      tmem_ld32(tS0 + s * BKEYS + lane_off, x);
+      tmem_ld16(tS0 + sb * BKEYS + lane_off, x);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(S_FREE + s));
+      if (lane == 0) mbar_arrive(bar(S_FREE + sb));
       float mx = -INFINITY;
 #pragma unroll
       for (int i = 0; i < BKEYS; ++i) {
