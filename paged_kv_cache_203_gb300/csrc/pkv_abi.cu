@@ -127,9 +127,12 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
     plan->kind = 2;
     plan->n_row_tiles = 0;
     int splits = num_splits;
-    if (splits == 0) {  // about three waves of one-CTA-per-SM work
+    if (splits == 0) {
+      // Each CTA pays a fixed start (Q into TMEM and shared memory, the index
+      // look-ahead) and a split adds a merge, so lists are split only as far
+      // as needed to give every SM a CTA (one CTA per SM fits).
       const int64_t base = std::max<int64_t>(1, total_q * 2);
-      splits = static_cast<int>((3LL * kNumSMs + base - 1) / base);
+      splits = static_cast<int>((kNumSMs + base - 1) / base);
       splits = std::max(1, std::min<int>(splits, static_cast<int>(topk.shape[1] / 256)));
     }
     splits = std::min(splits, kMlaMaxSplits);

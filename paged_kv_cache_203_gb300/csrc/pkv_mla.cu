@@ -12,17 +12,23 @@
 // One CTA = (query token, 256-wide half of the value dims, chunk of its key
 // list).  The output accumulator for 128 heads x 256 value dims fills half
 // of TMEM; both halves recompute the scores (the full 128 x 512 accumulator
-// would leave no TMEM columns for them).
-//   warps 5-12 producers: per 16-key tile, gather the 576-wide rows with
-//            16-byte cp.async into a [9 chunks][16 rows][128 B] 128-byte-
-//            swizzled tile (zero rows for skipped keys), two rows per warp,
-//            completion on mbarriers, four tiles in flight.  The list
+// would leave no TMEM columns for them).  The first 384 columns of Q live in
+// TMEM as the A operand of Q K^T and the other 192 in shared memory, which
+// leaves shared memory for two 64-key tiles.
+//   warps 5-12 producers: per 64-key tile, gather the 576-wide rows with
+//            16-byte cp.async into a [9 chunks][64 rows][128 B] 128-byte-
+//            swizzled tile (zero rows for skipped keys), eight rows per warp,
+//            completion on mbarriers, two tiles in flight.  The list
 //            entries and page ids of a tile are loaded one and two tiles
 //            ahead, so the two dependent lookups stay off the copy path
 //            (with them on it, each tile waited two global round trips);
-//   warp 4   MMA issuer: S = Q K^T (M 128 heads, N 16 keys, K 576: 36
-//            MMAs, both operands K-major), then O += P V (M 128, N 256 value
-//            dims, K 16 keys: V is an MN-major view of the same key tile);
+//   warp 4   MMA issuer: S = Q K^T (M 128 heads, N 64 keys, K 576: 36
+//            MMAs, K-major), then O += P V (M 128, N 256 value dims, K 64
+//            keys: V is an MN-major view of the same key tile).  A tensor-
+//            core instruction costs about the same up to N 64, so the tile is
+//            as wide as shared memory allows; descriptors are formed once per
+//            tile and the K steps fully unrolled (a lone issuing thread that
+//            rebuilt them per step took longer than the MMAs);
 //   warps 0-3 softmax (thread = head = TMEM lane): scores from TMEM, masks,
 //            online softmax in the log2 domain with a lazy reference max
 //            (O rescaled in TMEM only when the row max grows by > 2^8), P
@@ -43,26 +49,34 @@ constexpr int H = 128;        // query heads (the M dimension)
 constexpr int DQK = 576;      // latent + rope
 constexpr int DV = 512;       // latent (value) dims
 constexpr int DVH = 256;      // value dims per CTA
-constexpr int BKEYS = 16;     // keys per tile
-constexpr int NSTG = 4;       // key-tile stages
+constexpr int BKEYS = 64;     // keys per tile
+constexpr int NSTG = 2;       // key-tile stages
+constexpr int NCH_TM = 6;     // 64-column Q chunks held in TMEM (A operand)
 constexpr int NCH = DQK / 64; // 64-column chunks of a row (9)
 constexpr int NSOFT = 4, NPROD = 8;
 constexpr int kMmaWarp = NSOFT;
 constexpr int kProdWarp0 = NSOFT + 1;
 constexpr int NTHREADS = (NSOFT + 1 + NPROD) * 32;
-constexpr int kRowsPerWarp = BKEYS / NPROD;         // 2
-constexpr uint32_t kQBytes = NCH * H * 128;         // 147456
-constexpr uint32_t kKTile = NCH * BKEYS * 128;      // 18432
-constexpr uint32_t kPTile = H * BKEYS * 2;          // 4096
+constexpr int kRowsPerWarp = BKEYS / NPROD;         // 8
+constexpr uint32_t kQBytes = (NCH - NCH_TM) * H * 128;  // the shared-memory part: 49152
+// TMEM columns: S (64) | Q chunks 0-5 (192) | O (256)
+constexpr uint32_t kTmS = 0, kTmQ = BKEYS, kTmO = 256;
+static_assert(kTmQ + NCH_TM * 32 <= kTmO, "TMEM plan overflows");
+constexpr uint32_t kKTile = NCH * BKEYS * 128;      // 73728
+constexpr int kLook = 2;                          // look-ahead of each lookup level (tiles)
+constexpr int kRingA = 2 * kLook + 1, kRingB = kLook + 1;
+constexpr uint32_t kPTile = H * BKEYS * 2;          // 16384
 
 struct Smem {
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kK = kQ + kQBytes;          // NSTG stages
   static constexpr uint32_t kP = kK + NSTG * kKTile;
   static constexpr uint32_t kPos = kP + kPTile;         // int [NSTG][BKEYS]
-  static constexpr uint32_t kBar = kPos + NSTG * BKEYS * 4;
-  // q_full, full[NSTG], empty[NSTG], s_full[2], s_free[2], p_full, o_done
-  static constexpr int kNumBars = 3 + 2 * NSTG + 4;
+  // producers' look-ahead rings, per warp: list entries [RA][8], page ids [RB][8]
+  static constexpr uint32_t kRing = kPos + NSTG * BKEYS * 4;
+  static constexpr uint32_t kBar = kRing + NPROD * (kRingA + kRingB) * kRowsPerWarp * 4;
+  // q_full, full[NSTG], empty[NSTG], s_full, s_free, p_full, o_done, q_tmem
+  static constexpr int kNumBars = 2 * NSTG + 6;
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kFlag = kTmemSlot + 16;     // softmax: split ticket
   static constexpr uint32_t kEnd = kFlag + 16;
@@ -74,9 +88,10 @@ enum BarId {
   FULL = 1,
   EMPTY = FULL + NSTG,
   S_FULL = EMPTY + NSTG,
-  S_FREE = S_FULL + 2,
-  P_FULL = S_FREE + 2,
-  O_DONE = P_FULL + 1
+  S_FREE = S_FULL + 1,
+  P_FULL = S_FREE + 1,
+  O_DONE = P_FULL + 1,
+  Q_TMEM = O_DONE + 1
 };
 
 // byte offset of 16-byte chunk c (0..71) of row r in a 128-byte-swizzled
@@ -85,10 +100,10 @@ template <int NROWS>
 __device__ __forceinline__ uint32_t sw_off(int r, int c) {
   return static_cast<uint32_t>((c >> 3) * (NROWS * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
-// P [128 heads][16 keys] bf16, unswizzled core matrices: 8 rows x 16 B,
-// 128 B apart along the keys, 256 B apart along the heads
+// P [128 heads][64 keys] bf16, unswizzled core matrices: 8 rows x 16 B,
+// 128 B apart along the keys, 1024 B apart along the heads
 __device__ __forceinline__ uint32_t p_off(int m, int c) {
-  return static_cast<uint32_t>((m >> 3) * 256 + c * 128 + (m & 7) * 16);
+  return static_cast<uint32_t>((m >> 3) * 1024 + c * 128 + (m & 7) * 16);
 }
 
 struct MlaMaps {
@@ -142,12 +157,11 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
       mbar_init(bar(FULL + s), NPROD * 32);
       mbar_init(bar(EMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(S_FULL + s), 1);
-      mbar_init(bar(S_FREE + s), NSOFT);
-    }
+    mbar_init(bar(S_FULL), 1);
+    mbar_init(bar(S_FREE), NSOFT);
     mbar_init(bar(P_FULL), NSOFT);
     mbar_init(bar(O_DONE), 1);
+    mbar_init(bar(Q_TMEM), NSOFT);
     mbar_init_fence();
   }
   if (warp == kMmaWarp) tmem_alloc(smem_addr(sTmem), 512);
@@ -155,7 +169,7 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sTmem;
-  const uint32_t tS0 = tmem, tO = tmem + 256;
+  const uint32_t tS0 = tmem + kTmS, tQ = tmem + kTmQ, tO = tmem + kTmO;
 
   if (warp >= kProdWarp0) {
     // ================================ producers ================================
@@ -163,49 +177,76 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
     if (ptid == 0 && n_kv > 0) {
       mbar_arrive_expect_tx(bar(Q_FULL), kQBytes);
 #pragma unroll 1
-      for (int c = 0; c < NCH; ++c)
-        tma_load_3d(sbase + Smem::kQ + c * (H * 128), &maps.q, c * 64, 0, t, bar(Q_FULL));
+      for (int c = NCH_TM; c < NCH; ++c)
+        tma_load_3d(sbase + Smem::kQ + (c - NCH_TM) * (H * 128), &maps.q, c * 64, 0, t,
+                    bar(Q_FULL));
     }
     const int32_t *list = p.topk + static_cast<int64_t>(t) * p.topk_stride;
     const int pw = warp - kProdWarp0;  // producer warp: rows pw + 8 i of each tile
     const int end_j = (tile0 + n_kv) * BKEYS;
-    // lanes 0-15 follow key lane of the tile two ahead (list entry), one
-    // ahead (page id) and current (row offset)
-    auto load_idx = [&](int tile) -> int {
-      const int j = (tile0 + tile) * BKEYS + lane;
-      return (lane < BKEYS && tile < n_kv && j < end_j && j < p.topk_len) ? list[j] : -1;
+    // Lane i < 8 of producer warp pw owns row pw + 8 i of every tile.  Its
+    // list entry is fetched 2 * kLook tiles ahead and its page id kLook tiles
+    // ahead, both with 4-byte cp.async into this warp's rings (one commit
+    // group per tile), so no global load is waited on in the copy loop.
+    const int myrow = pw + NPROD * lane;
+    const bool keyl = lane < kRowsPerWarp;
+    int *ringA = reinterpret_cast<int *>(smem + Smem::kRing) +
+                 pw * (kRingA + kRingB) * kRowsPerWarp;
+    int *ringB = ringA + kRingA * kRowsPerWarp;
+    const uint32_t ringA_s = sbase + Smem::kRing + pw * (kRingA + kRingB) * kRowsPerWarp * 4;
+    const uint32_t ringB_s = ringA_s + kRingA * kRowsPerWarp * 4;
+    auto fetchA = [&](int tile) {  // list entry of this lane's row (or -1)
+      if (!keyl) return;
+      const int slot = (tile % kRingA) * kRowsPerWarp + lane;
+      const int j = (tile0 + tile) * BKEYS + myrow;
+      if (tile < n_kv && j < end_j && j < p.topk_len) cp_async4(ringA_s + slot * 4, list + j);
+      else ringA[slot] = -1;
     };
-    auto page_of = [&](int idx) -> int64_t {
-      if (idx < 0 || idx >= kv_len) return -1;
-      const int pidx = idx / p.page_size;
-      if (pidx >= p.pt_cols) return -2;
-      return p.page_table[static_cast<int64_t>(b) * p.pt_stride + pidx];
+    auto fetchB = [&](int tile) {  // page id of that entry (-1: no key, -2: row too short)
+      if (!keyl) return;
+      const int idx = ringA[(tile % kRingA) * kRowsPerWarp + lane];
+      const int slot = (tile % kRingB) * kRowsPerWarp + lane;
+      if (idx >= 0 && idx < kv_len) {
+        const int pidx = idx / p.page_size;
+        if (pidx < p.pt_cols)
+          cp_async4(ringB_s + slot * 4,
+                    p.page_table + static_cast<int64_t>(b) * p.pt_stride + pidx);
+        else
+          ringB[slot] = -2;
+      } else {
+        ringB[slot] = -1;
+      }
     };
-    int idx_cur = load_idx(0);
-    int64_t pg_cur = page_of(idx_cur);
-    int idx_nxt = load_idx(1);
+    for (int x = 0; x < 2 * kLook; ++x) fetchA(x);
+    cp_async_commit();
+    cp_async_wait_all();
+    for (int x = 0; x < kLook; ++x) fetchB(x);
+    cp_async_commit();
+    cp_async_wait_all();
     for (int jj = 0; jj < n_kv; ++jj) {
       const int s = jj % NSTG;
-      // lookups for the next tiles go out first; their latency overlaps this
-      // tile's wait and copies
-      const int64_t pg_nxt = page_of(idx_nxt);
-      const int idx_nn = load_idx(jj + 2);
-      // this tile's key lane: position (or -1) and row offset
+      // entries of tile jj + kLook and page ids of tile jj have landed
+      cp_async_wait_group<kLook - 1>();
+      fetchB(jj + kLook);
+      fetchA(jj + 2 * kLook);
+      cp_async_commit();
+      // this lane's row of tile jj: position (or -1) and row offset
       int pos = -1;
       int64_t off = -1;
-      if (lane < BKEYS) {
-        if (idx_cur < -1 || idx_cur >= kv_len) {
-          if (pw == 0 && idx_cur != -1 && (tile0 + jj) * BKEYS + lane < p.topk_len)
-            atomicOr(p.err, PKV_EFLAG_TOPK_OOB);
-        } else if (idx_cur >= 0) {
-          if (pg_cur == -2) {
-            if (pw == 0) atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
-          } else if (pg_cur < 0 || pg_cur >= p.num_pages) {
-            if (pw == 0) atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
+      if (keyl) {
+        const int ic = ringA[(jj % kRingA) * kRowsPerWarp + lane];
+        const int64_t pc = ringB[(jj % kRingB) * kRowsPerWarp + lane];
+        if (ic < -1 || ic >= kv_len) {
+          if (ic != -1) atomicOr(p.err, PKV_EFLAG_TOPK_OOB);
+        } else if (ic >= 0) {
+          if (pc == -2) {
+            atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
+          } else if (pc < 0 || pc >= p.num_pages) {
+            atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
           } else {
-            pos = idx_cur;
-            off = pg_cur * p.k_sp +
-                  static_cast<int64_t>(idx_cur - (idx_cur / p.page_size) * p.page_size) * p.k_spos;
+            pos = ic;
+            off = pc * p.k_sp +
+                  static_cast<int64_t>(ic - (ic / p.page_size) * p.page_size) * p.k_spos;
           }
         }
       }
@@ -217,13 +258,13 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
         if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
         break;
       }
-      if (pw == 0 && lane < BKEYS) sPos[s * BKEYS + lane] = pos;
+      if (keyl) sPos[s * BKEYS + myrow] = pos;
       // gather this warp's rows: 72 chunks of 16 B each, lanes along the row
       const uint32_t kdst = sbase + Smem::kK + s * kKTile;
-#pragma unroll
+#pragma unroll 2
       for (int i = 0; i < kRowsPerWarp; ++i) {
         const int r = pw + NPROD * i;
-        const int64_t ro = __shfl_sync(0xffffffffu, off, r);
+        const int64_t ro = __shfl_sync(0xffffffffu, off, i);
         const bf16 *src = ro >= 0 ? p.k + ro : p.k;
         const int nbytes = ro >= 0 ? 16 : 0;
 #pragma unroll
@@ -232,32 +273,37 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
       }
       cp_async_arrive(bar(FULL + s));
       mbar_arrive(bar(FULL + s));
-      idx_cur = idx_nxt;
-      pg_cur = pg_nxt;
-      idx_nxt = idx_nn;
     }
   } else if (warp == kMmaWarp) {
     // ================================== MMA ==================================
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16(H, BKEYS, false);
       constexpr uint32_t kIdescPV = idesc_bf16(H, DVH, true);
-      bool ok = n_kv == 0 || mbar_wait(bar(Q_FULL), 0);
+      bool ok = n_kv == 0 || (mbar_wait(bar(Q_FULL), 0) && mbar_wait(bar(Q_TMEM), 0));
+      const uint64_t qd0 = smem_desc(sbase + Smem::kQ, 0, 1024, 2);
+      const uint64_t pd0 = smem_desc(sbase + Smem::kP, 128, 1024, 0);
       for (int j = 0; ok && j <= n_kv; ++j) {
-        if (j < n_kv) {  // S_j = Q K_j^T
-          const int s = j % NSTG, sb = j & 1;
+        if (j < n_kv) {  // S_j = Q K_j^T (S is free once the softmax loaded S_{j-1})
+          const int s = j % NSTG;
           ok = mbar_wait(bar(FULL + s), (j / NSTG) & 1) &&
-               (j < 2 || mbar_wait(bar(S_FREE + sb), ((j >> 1) - 1) & 1));
+               (j < 1 || mbar_wait(bar(S_FREE), (j - 1) & 1));
           if (!ok) break;
           tc_fence_after();
-          const uint32_t kb = sbase + Smem::kK + s * kKTile;
-#pragma unroll 4
-          for (int ks = 0; ks < DQK / 16; ++ks) {
-            const uint32_t qoff = (ks >> 2) * (H * 128) + (ks & 3) * 32;
-            const uint32_t koff = (ks >> 2) * (BKEYS * 128) + (ks & 3) * 32;
-            umma(tS0 + sb * BKEYS, smem_desc(sbase + Smem::kQ + qoff, 0, 1024, 2),
-                 smem_desc(kb + koff, 0, 1024, 2), kIdescQK, ks > 0);
-          }
-          umma_commit(bar(S_FULL + sb));
+          const uint64_t kd0 = smem_desc(sbase + Smem::kK + s * kKTile, 0, 1024, 2);
+          // K step ks: 16 columns = 32 bytes within chunk ks / 4 (descriptor
+          // addresses are in 16-byte units)
+#pragma unroll
+          for (int ks = 0; ks < NCH_TM * 4; ++ks)  // A = Q columns from TMEM
+            umma_ts(tS0, tQ + ks * 8,
+                    kd0 + static_cast<uint64_t>(((ks >> 2) * (BKEYS * 128) + (ks & 3) * 32) >> 4),
+                    kIdescQK, ks > 0 ? 1u : 0u);
+#pragma unroll
+          for (int ks = NCH_TM * 4; ks < DQK / 16; ++ks)  // A = Q columns from smem
+            umma(tS0,
+                 qd0 + static_cast<uint64_t>((((ks >> 2) - NCH_TM) * (H * 128) + (ks & 3) * 32) >> 4),
+                 kd0 + static_cast<uint64_t>(((ks >> 2) * (BKEYS * 128) + (ks & 3) * 32) >> 4),
+                 kIdescQK, 1u);
+          umma_commit(bar(S_FULL));
         }
         if (j >= 1) {  // O += P_{j-1} V_{j-1}
           const int jj = j - 1;
@@ -265,10 +311,13 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
           ok = mbar_wait(bar(P_FULL), jj & 1);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t vb = sbase + Smem::kK + s * kKTile + hv * 4 * (BKEYS * 128);
-          static_assert(BKEYS == 16, "one K=16 step of P V per tile");
-          umma(tO, smem_desc(sbase + Smem::kP, 128, 256, 0),
-               smem_desc(vb, BKEYS * 128, 1024, 2), kIdescPV, jj > 0 ? 1u : 0u);
+          const uint64_t vd0 =
+              smem_desc(sbase + Smem::kK + s * kKTile + hv * 4 * (BKEYS * 128), BKEYS * 128, 1024, 2);
+#pragma unroll
+          for (int ks = 0; ks < BKEYS / 16; ++ks)  // 16 keys = 2 P chunks = 2 V row groups
+            umma(tO, pd0 + static_cast<uint64_t>((ks * 256) >> 4),
+                 vd0 + static_cast<uint64_t>((ks * 2048) >> 4), kIdescPV,
+                 (jj > 0 || ks > 0) ? 1u : 0u);
           umma_commit(bar(O_DONE));
           umma_commit(bar(EMPTY + s));
         }
@@ -285,24 +334,58 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
     float m_ref = -INFINITY;
     float l = 0.f;
     bool ok = true;
+    if (n_kv > 0) {
+      // Q row `row`, columns 0..447, as packed bf16 pairs into TMEM columns
+      // tQ .. tQ + 223 of this thread's lane (the A operand of Q K^T)
+      const uint4 *qsrc = reinterpret_cast<const uint4 *>(
+          p.q + static_cast<int64_t>(t) * p.q_st + static_cast<int64_t>(row) * p.q_sh);
+#pragma unroll 1
+      for (int cb = 0; cb < NCH_TM; ++cb) {
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 w = qsrc[cb * 8 + i];
+          r[4 * i] = w.x;
+          r[4 * i + 1] = w.y;
+          r[4 * i + 2] = w.z;
+          r[4 * i + 3] = w.w;
+        }
+        tmem_st32u(tQ + lane_off + cb * 32, r);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Q_TMEM));
+    }
     for (int jj = 0; jj < n_kv; ++jj) {
-      const int s = jj % NSTG, sb = jj & 1;
-      if (!(ok = mbar_wait(bar(S_FULL + sb), (jj >> 1) & 1) &&
-                 mbar_wait(bar(FULL + s), (jj / NSTG) & 1)))
+      const int s = jj % NSTG;
+      if (!(ok = mbar_wait(bar(S_FULL), jj & 1) && mbar_wait(bar(FULL + s), (jj / NSTG) & 1)))
         break;
       tc_fence_after();
       float x[BKEYS];
-      tmem_ld16(tS0 + sb * BKEYS + lane_off, x);
+      {
+        float (&x0)[32] = *reinterpret_cast<float (*)[32]>(&x[0]);
+        float (&x1)[32] = *reinterpret_cast<float (*)[32]>(&x[32]);
+        tmem_ld32(tS0 + lane_off, x0);
+        tmem_ld32(tS0 + 32 + lane_off, x1);
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(S_FREE + sb));
+      if (lane == 0) mbar_arrive(bar(S_FREE));
       float mx = -INFINITY;
+      const int4 *pos4 = reinterpret_cast<const int4 *>(sPos + s * BKEYS);
 #pragma unroll
-      for (int i = 0; i < BKEYS; ++i) {
-        const int pos = sPos[s * BKEYS + i];
-        const bool msk = pos < 0 || (use_upper && pos > i_pos) || pos < lo_r;
-        x[i] = msk ? -INFINITY : x[i] * c;
-        mx = fmaxf(mx, x[i]);
+      for (int i4 = 0; i4 < BKEYS / 4; ++i4) {
+        const int4 pp = pos4[i4];
+        const int pv[4] = {pp.x, pp.y, pp.z, pp.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = 4 * i4 + u;
+          const int pos = pv[u];
+          const bool msk = pos < 0 || (use_upper && pos > i_pos) || pos < lo_r;
+          x[i] = msk ? -INFINITY : x[i] * c;
+          mx = fmaxf(mx, x[i]);
+        }
       }
       bool need = false;
       float factor = 1.f;
