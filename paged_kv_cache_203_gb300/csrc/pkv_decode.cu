@@ -748,9 +748,13 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
 //
 // Two copy modes:
 //  * slot rows (page size < 8, each slot one contiguous H_kv x 128 row): per
-//    key one bulk copy of the row for K and one for V, into shared memory at
-//    a pitch of H_kv * 256 + 16 bytes (the skew keeps ldmatrix reads
-//    conflict-free without a swizzle);
+//    key one bulk copy of the K row by the producer, and the V row copied by
+//    the consumer warps themselves, each its own head's 256-byte slice with
+//    16-byte cp.async two tiles ahead (skipped keys zero-filled), into
+//    shared memory at a pitch of H_kv * 256 + 16 bytes (the skew keeps
+//    ldmatrix reads conflict-free without a swizzle).  At 2 KB per copy the
+//    bulk-copy engine's per-copy cost limits it, so it takes half the rows;
+//    moving K to cp.async as well measured slower;
 //  * page boxes (page size a multiple of 16): per tile one TMA box
 //    {64 columns, 16 positions, hpc heads} per 64-column half and tensor, from
 //    a tensor map that lists position before head, so the box lands as
@@ -789,7 +793,7 @@ constexpr int AH_REQ_END = 8;    // the request's last tile
 // function on host and device).
 struct AhLayout {
   uint32_t stage;  // bytes of one K (or V) stage
-  uint32_t k, v, pos, meta, ring_pg, ring_j, pre, scan, bar, end;
+  uint32_t k, v, pos, meta, ring_pg, ring_j, voff, pre, scan, bar, end;
 };
 __host__ __device__ inline AhLayout ah_layout(int hpc, bool boxes, bool balanced) {
   AhLayout L;
@@ -801,10 +805,11 @@ __host__ __device__ inline AhLayout ah_layout(int hpc, bool boxes, bool balanced
   L.meta = L.pos + AH_NSTAGE * AH_BK * 4;  // int [NSTAGE][2]
   L.ring_pg = L.meta + AH_NSTAGE * 8;  // int [RING][BK] page ids
   L.ring_j = L.ring_pg + AH_RING * AH_BK * 4;  // int [RING][BK] key or -1
-  L.pre = (L.ring_j + AH_RING * AH_BK * 4 + 7) & ~7u;  // int64 [MAXB + 1]
+  L.voff = (L.ring_j + AH_RING * AH_BK * 4 + 7) & ~7u;  // int64 [NSTAGE][BK] (slot rows)
+  L.pre = L.voff + AH_NSTAGE * AH_BK * 8;  // int64 [MAXB + 1]
   L.scan = L.pre + (balanced ? (AH_MAXB + 1) * 8 : 0);  // int64 [16]
   L.bar = L.scan + 16 * 8;
-  L.end = L.bar + 2 * AH_NSTAGE * 8;
+  L.end = L.bar + 3 * AH_NSTAGE * 8;  // full, empty, V offsets published
   return L;
 }
 static_assert(AH_NSTAGE * 2 * (AH_BK * (AH_MAXH * 256 + 16)) + 18 * 1024 <= AH_SMEM_MAX,
@@ -889,6 +894,8 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   int64_t *sScan = reinterpret_cast<int64_t *>(smem + L.scan);
   const uint32_t full0 = sbase + L.bar;
   const uint32_t empty0 = full0 + AH_NSTAGE * 8;
+  const uint32_t vmeta0 = empty0 + AH_NSTAGE * 8;
+  int64_t *sVoff = reinterpret_cast<int64_t *>(smem + L.voff);
   const uint32_t row_bytes = static_cast<uint32_t>(hpc) * 256u;  // the CTA's heads of one key
   const uint32_t pitch = row_bytes + 16u;                         // slot-row mode
 
@@ -896,6 +903,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     for (int s = 0; s < AH_NSTAGE; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, hpc);
+      mbar_init(vmeta0 + 8 * s, 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     fence_proxy_async();
@@ -1086,16 +1094,19 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
           }
         }
       } else {
-        uint32_t bytes = pos >= 0 ? 2u * row_bytes : 0u;
+        // K rows by bulk copy; the V rows' offsets are published for the
+        // consumer warps, which copy their own head's slices with cp.async
+        if (lane < AH_BK) sVoff[st * AH_BK + lane] = pos >= 0 ? voff : -1;
+        uint32_t bytes = pos >= 0 ? row_bytes : 0u;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(full, bytes);
-        __syncwarp();
-        if (pos >= 0) {
-          bulk_g2s(kdst + lane * pitch, p.k + koff, row_bytes, full);
-          bulk_g2s(vdst + lane * pitch, p.v + voff, row_bytes, full);
+        if (lane == 0) {
+          mbar_arrive(vmeta0 + 8 * st);
+          mbar_arrive_expect_tx(full, bytes);
         }
+        __syncwarp();
+        if (pos >= 0) bulk_g2s(kdst + lane * pitch, p.k + koff, row_bytes, full);
       }
       // next tile (a balanced run moves on to the next request with tiles;
       // a fixed split never leaves its request)
@@ -1130,9 +1141,32 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   int n_rows = 0;
   bool seg_req_start = false, first_seg = true;
 
-  for (int kt = 0; kt < n; ++kt) {
+  // Slot rows: this warp copies its head's 256-byte V slice of every key of
+  // tile x (16 rows x 16 chunks, 8 per lane; skipped keys zero-filled), one
+  // cp.async group per tile.  The stage's region of this head was last read
+  // by this warp's own PV three tiles earlier.
+  auto issue_v = [&](int x) -> bool {
+    if (!BOXES && x < n) {
+      const int sx = x % AH_NSTAGE;
+      if (!mbar_wait(vmeta0 + 8 * sx, (x / AH_NSTAGE) & 1)) return false;
+      const int c = lane & 15;
+      const uint32_t vdst = sbase + L.v + sx * L.stage;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = (lane >> 4) + 2 * i;
+        const int64_t vo = sVoff[sx * AH_BK + rr];
+        cp_async16(vdst + soff(rr, c), vo >= 0 ? p.v + vo + h * 128 + c * 8 : p.v,
+                   vo >= 0 ? 16 : 0);
+      }
+    }
+    if (!BOXES) cp_async_commit();
+    return true;
+  };
+  bool v_ok = issue_v(0) && issue_v(1);
+
+  for (int kt = 0; v_ok && kt < n; ++kt) {
     const int st = kt % AH_NSTAGE;
-    if (!mbar_wait(full0 + 8 * st, (kt / AH_NSTAGE) & 1)) {
+    if (!mbar_wait(full0 + 8 * st, (kt / AH_NSTAGE) & 1) || !issue_v(kt + 2)) {
       if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
       break;
     }
@@ -1167,8 +1201,9 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     const uint32_t kb = sbase + L.k + st * L.stage;
     const uint32_t vb = sbase + L.v + st * L.stage;
     const int *pos_st = sPos + st * AH_BK;
-    // zero this head's V rows of skipped keys (a masked key must add exactly 0)
-    const bool any_skipped = __any_sync(0xffffffffu, pos_st[lane & 15] < 0);
+    // page boxes: zero this head's V rows of skipped keys (a masked key must
+    // add exactly 0); slot rows arrive zero-filled
+    const bool any_skipped = BOXES && __any_sync(0xffffffffu, pos_st[lane & 15] < 0);
     if (any_skipped) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -1245,6 +1280,10 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     const uint32_t a1 = pack_bf16(sc[0][2], sc[0][3]);
     const uint32_t a2 = pack_bf16(sc[1][0], sc[1][1]);
     const uint32_t a3 = pack_bf16(sc[1][2], sc[1][3]);
+    if (!BOXES) {  // this tile's V slices (two later tiles' groups may be pending)
+      cp_async_wait_group<2>();
+      __syncwarp();
+    }
     {
       const int m = lane >> 3;
       const int key = (m & 1) * 8 + (lane & 7);
@@ -1358,6 +1397,8 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
             wsum > 0.f ? Ms + logf(wsum) : -INFINITY;
     }
   }
+  if (!v_ok) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+  if (!BOXES) cp_async_wait_group<0>();  // none of this warp's copies outlives the CTA
 }
 
 // ------------------------------------------------------------------- host
