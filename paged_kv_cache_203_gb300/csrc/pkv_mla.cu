@@ -12,23 +12,24 @@
 // One CTA = (query token, 256-wide half of the value dims, chunk of its key
 // list).  The output accumulator for 128 heads x 256 value dims fills half
 // of TMEM; both halves recompute the scores (the full 128 x 512 accumulator
-// would leave no TMEM columns for them).  The first 384 columns of Q live in
-// TMEM as the A operand of Q K^T and the other 192 in shared memory, which
-// leaves shared memory for two 64-key tiles.
-//   warps 5-12 producers: per 64-key tile, gather the 576-wide rows with
-//            16-byte cp.async into a [9 chunks][64 rows][128 B] 128-byte-
-//            swizzled tile (zero rows for skipped keys), eight rows per warp,
-//            completion on mbarriers, two tiles in flight.  The list
+// would leave no TMEM columns for them).  The first 448 columns of Q live in
+// TMEM as the A operand of Q K^T and the other 128 in shared memory, which
+// leaves shared memory for five 32-key tiles: the gather is the limit, and
+// a deeper ring measured faster than wider tiles (2 x 64 keys: 866 GB/s,
+// 3 x 48: 1303, 5 x 32: 1357).
+//   warps 5-12 producers: per 32-key tile, gather the 576-wide rows with
+//            16-byte cp.async into a [9 chunks][32 rows][128 B] 128-byte-
+//            swizzled tile (zero rows for skipped keys), four rows per warp,
+//            completion on mbarriers, up to five tiles in flight.  The list
 //            entries and page ids of a tile are loaded one and two tiles
 //            ahead, so the two dependent lookups stay off the copy path
 //            (with them on it, each tile waited two global round trips);
-//   warp 4   MMA issuer: S = Q K^T (M 128 heads, N 64 keys, K 576: 36
-//            MMAs, K-major), then O += P V (M 128, N 256 value dims, K 64
-//            keys: V is an MN-major view of the same key tile).  A tensor-
-//            core instruction costs about the same up to N 64, so the tile is
-//            as wide as shared memory allows; descriptors are formed once per
-//            tile and the K steps fully unrolled (a lone issuing thread that
-//            rebuilt them per step took longer than the MMAs);
+//   warp 4   MMA issuer: S = Q K^T (M 128 heads, N 32 keys, K 576: 36
+//            MMAs, K-major), then O += P V (M 128, N 256 value dims, K 32
+//            keys: V is an MN-major view of the same key tile).  Descriptors
+//            are formed once per tile and the K steps fully unrolled (a lone
+//            issuing thread that rebuilt them per step took longer than the
+//            MMAs);
 //   warps 0-3 softmax (thread = head = TMEM lane): scores from TMEM, masks,
 //            online softmax in the log2 domain with a lazy reference max
 //            (O rescaled in TMEM only when the row max grows by > 2^8), P
@@ -49,23 +50,24 @@ constexpr int H = 128;        // query heads (the M dimension)
 constexpr int DQK = 576;      // latent + rope
 constexpr int DV = 512;       // latent (value) dims
 constexpr int DVH = 256;      // value dims per CTA
-constexpr int BKEYS = 64;     // keys per tile
-constexpr int NSTG = 2;       // key-tile stages
-constexpr int NCH_TM = 6;     // 64-column Q chunks held in TMEM (A operand)
+constexpr int BKEYS = 32;     // keys per tile
+constexpr int NSTG = 5;       // key-tile stages
+constexpr int NCH_TM = 7;     // 64-column Q chunks held in TMEM (A operand)
 constexpr int NCH = DQK / 64; // 64-column chunks of a row (9)
 constexpr int NSOFT = 4, NPROD = 8;
 constexpr int kMmaWarp = NSOFT;
 constexpr int kProdWarp0 = NSOFT + 1;
 constexpr int NTHREADS = (NSOFT + 1 + NPROD) * 32;
-constexpr int kRowsPerWarp = BKEYS / NPROD;         // 8
+constexpr int kRowsPerWarp = BKEYS / NPROD;         // 4
 constexpr uint32_t kQBytes = (NCH - NCH_TM) * H * 128;  // the shared-memory part: 49152
-// TMEM columns: S (64) | Q chunks 0-5 (192) | O (256)
-constexpr uint32_t kTmS = 0, kTmQ = BKEYS, kTmO = 256;
+// TMEM columns: S (32) | Q chunks 0-6 (224) | O (256)
+constexpr uint32_t kTmS = 0, kTmQ = 32, kTmO = 256;
+static_assert(BKEYS <= kTmQ, "S fits its TMEM columns");
 static_assert(kTmQ + NCH_TM * 32 <= kTmO, "TMEM plan overflows");
-constexpr uint32_t kKTile = NCH * BKEYS * 128;      // 73728
+constexpr uint32_t kKTile = NCH * BKEYS * 128;      // 36864
 constexpr int kLook = 2;                          // look-ahead of each lookup level (tiles)
 constexpr int kRingA = 2 * kLook + 1, kRingB = kLook + 1;
-constexpr uint32_t kPTile = H * BKEYS * 2;          // 16384
+constexpr uint32_t kPTile = H * BKEYS * 2;          // 8192
 
 struct Smem {
   static constexpr uint32_t kQ = 0;
@@ -100,10 +102,10 @@ template <int NROWS>
 __device__ __forceinline__ uint32_t sw_off(int r, int c) {
   return static_cast<uint32_t>((c >> 3) * (NROWS * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
-// P [128 heads][64 keys] bf16, unswizzled core matrices: 8 rows x 16 B,
-// 128 B apart along the keys, 1024 B apart along the heads
+// P [128 heads][BKEYS keys] bf16, unswizzled core matrices: 8 rows x 16 B,
+// 128 B apart along the keys, BKEYS * 16 B apart along the heads
 __device__ __forceinline__ uint32_t p_off(int m, int c) {
-  return static_cast<uint32_t>((m >> 3) * 1024 + c * 128 + (m & 7) * 16);
+  return static_cast<uint32_t>((m >> 3) * (BKEYS * 16) + c * 128 + (m & 7) * 16);
 }
 
 struct MlaMaps {
@@ -281,7 +283,7 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
       constexpr uint32_t kIdescPV = idesc_bf16(H, DVH, true);
       bool ok = n_kv == 0 || (mbar_wait(bar(Q_FULL), 0) && mbar_wait(bar(Q_TMEM), 0));
       const uint64_t qd0 = smem_desc(sbase + Smem::kQ, 0, 1024, 2);
-      const uint64_t pd0 = smem_desc(sbase + Smem::kP, 128, 1024, 0);
+      const uint64_t pd0 = smem_desc(sbase + Smem::kP, 128, BKEYS * 16, 0);
       for (int j = 0; ok && j <= n_kv; ++j) {
         if (j < n_kv) {  // S_j = Q K_j^T (S is free once the softmax loaded S_{j-1})
           const int s = j % NSTG;
@@ -364,10 +366,8 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
       tc_fence_after();
       float x[BKEYS];
       {
-        float (&x0)[32] = *reinterpret_cast<float (*)[32]>(&x[0]);
-        float (&x1)[32] = *reinterpret_cast<float (*)[32]>(&x[32]);
-        tmem_ld32(tS0 + lane_off, x0);
-        tmem_ld32(tS0 + 32 + lane_off, x1);
+        static_assert(BKEYS == 32, "S row load below is written for 32 keys");
+        tmem_ld32(tS0 + lane_off, x);
       }
       tc_fence_before();
       __syncwarp();
