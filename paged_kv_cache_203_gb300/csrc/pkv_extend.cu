@@ -385,6 +385,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       constexpr uint32_t kIdescQK = idesc_bf16(false);
       constexpr uint32_t kIdescPV = idesc_bf16(true);
       bool ok = n_kv == 0 || mbar_wait(bar(Q_FULL), 0);
+      const uint64_t qd0 = smem_desc(sbase + Smem::kQ, 0, 1024);
       for (int j = 0; ok && j <= n_kv; ++j) {
         if (j < n_kv) {  // S_j = Q K_j^T
           const int s = j & 1;
@@ -392,13 +393,14 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
                (j < 2 || mbar_wait(bar(S_FREE + s), ((j >> 1) - 1) & 1));
           if (!ok) break;
           tc_fence_after();
-          const uint32_t qa = sbase + Smem::kQ;
-          const uint32_t kb = sbase + Smem::kK + s * kTileBytes;
+          // descriptors formed once per tile; a K step adds a constant to the
+          // start-address field (16-byte units), so the single issuing
+          // thread does no 64-bit descriptor arithmetic per MMA
+          const uint64_t kd0 = smem_desc(sbase + Smem::kK + s * kTileBytes, 0, 1024);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t koff = (ks >> 2) * (BM * 128) + (ks & 3) * 32;
-            umma(tS0 + s * 128, smem_desc(qa + koff, 0, 1024), smem_desc(kb + koff, 0, 1024),
-                 kIdescQK, ks > 0);
+            const uint64_t koff = ((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4;
+            umma(tS0 + s * 128, qd0 + koff, kd0 + koff, kIdescQK, ks > 0);
           }
           umma_commit(bar(S_FULL + s));
           umma_commit(bar(K_EMPTY + s));
@@ -410,15 +412,14 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
                mbar_wait(bar(V_FULL + s), (jj >> 1) & 1);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t pa = sbase + Smem::kP + s * kTileBytes;
-          const uint32_t vb = sbase + Smem::kV + s * kTileBytes;
+          const uint64_t pd0 = smem_desc(sbase + Smem::kP + s * kTileBytes, 0, 1024);
+          const uint64_t vd0 = smem_desc(sbase + Smem::kV + s * kTileBytes, BN * 128, 1024);
           // keys 0-63 of the tile accumulate into O_A, keys 64-127 into O_B
           // (each half of the softmax keeps its own reference max)
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks) {
-            const uint32_t aoff = (ks >> 2) * (BM * 128) + (ks & 3) * 32;
-            umma(tO + (ks >> 2) * 128, smem_desc(pa + aoff, 0, 1024),
-                 smem_desc(vb + ks * 2048, BN * 128, 1024), kIdescPV,
+            const uint64_t aoff = ((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4;
+            umma(tO + (ks >> 2) * 128, pd0 + aoff, vd0 + ((ks * 2048) >> 4), kIdescPV,
                  (jj > 0 || (ks & 3) > 0) ? 1u : 0u);
           }
           umma_commit(bar(O_DONE + s));
