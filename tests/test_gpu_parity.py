@@ -522,6 +522,48 @@ def test_small_page_balanced_schedule_mixed_batch():
     assert pkv.get_error_flags() == 0
 
 
+def test_small_page_batch_beyond_the_balanced_limit():
+    """More requests than the balanced schedule handles (2048): the library's
+    split choice falls back to fixed splits of the all-heads kernel; sampled
+    rows against the oracle."""
+    batch = 2100
+    wl = workloads.make("tiny_decode", d=128, page_size=1, h_q=16, h_kv=8, batch=batch,
+                        len_lo=1, len_hi=80, pool_tokens=batch * 80 + 64, seed=91)
+    g = wl.to(DEV)
+    out, lse = gpu_attn(g, num_splits=0)
+    rows = _sample_rows(batch, 16, 128, 5)
+    ref_o, ref_l, _ = oracle_attn(wl, rows=rows)
+    idx = torch.from_numpy(rows).long()
+    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
+                ref_o, ref_l, "batch 2100")
+    assert pkv.get_error_flags() == 0
+
+
+@pytest.mark.parametrize("page_size,q_len,window", [(16, 8, 100), (32, 4, -1), (64, 2, 0)])
+def test_page_box_balanced_sixteen_rows_per_kv_head(page_size, q_len, window):
+    """Page boxes under the balanced schedule with up to 16 query rows per KV
+    head (causal runs of new tokens, windows), NaN in every unused slot."""
+    h_kv = 8
+    h_q = h_kv * (16 // q_len)  # q_len * group = 16 rows per KV head
+    wl = workloads.make("tiny_decode", d=128, page_size=page_size, h_q=h_q, h_kv=h_kv,
+                        q_len=q_len, window_left=window, causal=True, len_lo=q_len,
+                        len_hi=1500, batch=7, pool_tokens=7 * (1500 + page_size) * 2, seed=31)
+    valid = torch.zeros(wl.k_cache.shape[0] * page_size, dtype=torch.bool)
+    for b in range(7):
+        n = int(wl.cache_seqlens[b])
+        j = torch.arange(n)
+        slots = wl.page_table[b, j // page_size].long() * page_size + j % page_size
+        valid[slots] = True
+    valid = valid.view(-1, page_size)
+    wl.k_cache[~valid] = float("nan")
+    wl.v_cache[~valid] = float("nan")
+    g = wl.to(DEV)
+    out, lse = gpu_attn(g, num_splits=0)
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, f"P={page_size} q_len={q_len}")
+    assert pkv.get_error_flags() == 0
+
+
 def test_head_major_cache_layout():
     """A cache laid out [pages, H_kv, P, D] (head outside position) is read
     through its strides; results equal the oracle's."""
