@@ -15,7 +15,8 @@
 //           then O += P_{j-1} V_{j-1} into the TMEM accumulator, each a chain
 //           of eight 128x128x16 bf16 MMAs with fp32 accumulation; completion
 //           signalled with tcgen05.commit on mbarriers (a K stage is released
-//           when its QK^T is done, a V stage when its PV is done);
+//           when its QK^T is done, a V stage and the S/P buffer when its PV
+//           is done);
 //   warps 0-7 softmax: warps w and w+4 share TMEM lane quadrant w (query
 //           rows 32w..32w+31) and split each key tile's 128 columns in two
 //           halves.  Each half is an independent online softmax with its own
@@ -23,10 +24,13 @@
 //           O_B), so the halves never synchronise inside the loop; their
 //           states are combined once in the epilogue (log-sum-exp merge).
 //           Log2 domain, lazy reference max (O_hf and l rescaled in place only
-//           when the max grows by more than 2^8), P_j (bf16) written to shared
-//           memory as the A operand of the PV MMA; V rows of keys past the
-//           sequence or in skipped pages are zeroed.
-// TMEM: S0 | S1 | O_A | O_B (128 columns each, 512 in all; 1 CTA per SM).
+//           when the max grows by more than 2^8); P_j (bf16, two per 32-bit
+//           column) is stored back into TMEM over the half's own S_j columns
+//           and is the A operand of the PV MMA straight from TMEM, so no
+//           shared-memory store or proxy fence sits in the softmax loop; V
+//           rows of keys past the sequence or in skipped pages are zeroed.
+// TMEM: S0 | S1 | O_A | O_B (128 columns each, 512 in all; 1 CTA per SM);
+// P_j occupies columns 0-31 and 64-95 of S_j's buffer until its PV is done.
 // Every mbarrier wait is bounded (PKV_EFLAG_TIMEOUT on expiry).
 #include <cuda.h>
 #include <limits.h>
@@ -53,8 +57,7 @@ struct Smem {
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kK = kQ + kTileBytes;       // 2 stages
   static constexpr uint32_t kV = kK + 2 * kTileBytes;   // 2 stages
-  static constexpr uint32_t kP = kV + 2 * kTileBytes;   // 2 buffers
-  static constexpr uint32_t kMask = kP + 2 * kTileBytes;  // uint32 [4 tiles][4 words]
+  static constexpr uint32_t kMask = kV + 2 * kTileBytes;  // uint32 [4 tiles][4 words]
   static constexpr uint32_t kXchg = kMask + 64;  // float [m, l][2 halves][128 rows]
   static constexpr uint32_t kBar = kXchg + 2 * 2 * BM * 4;
   // barriers: q_full, k_full[2], v_full[2], k_empty[2], v_empty[2],
@@ -149,6 +152,16 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D (+)= A B with A [128 x 16] from TMEM (rows on lanes, two bf16 of
+// consecutive k per 32-bit column, 8 columns per K=16 step).
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
@@ -231,6 +244,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
                PKV_I16(0), PKV_I16(16)
                : "memory");
 }
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
@@ -285,7 +310,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       mbar_init(bar(K_EMPTY + s), 1);
       mbar_init(bar(V_EMPTY + s), 1);
       mbar_init(bar(S_FULL + s), 1);
-      mbar_init(bar(S_FREE + s), NSM_WARPS);
+      mbar_init(bar(S_FREE + s), 1);  // PV of the tile that used the buffer is done
       mbar_init(bar(P_FULL + s), NSM_WARPS);
       mbar_init(bar(O_DONE + s), 1);
       mbar_init(bar(XCHG + s), NSM_WARPS);
@@ -412,18 +437,17 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
                mbar_wait(bar(V_FULL + s), (jj >> 1) & 1);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t pd0 = smem_desc(sbase + Smem::kP + s * kTileBytes, 0, 1024);
           const uint64_t vd0 = smem_desc(sbase + Smem::kV + s * kTileBytes, BN * 128, 1024);
           // keys 0-63 of the tile accumulate into O_A, keys 64-127 into O_B
-          // (each half of the softmax keeps its own reference max)
+          // (each half of the softmax keeps its own reference max); P_j is
+          // read from TMEM: keys 64h + 16k.. at column 128 s + 64 h + 8 k
 #pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks) {
-            const uint64_t aoff = ((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4;
-            umma(tO + (ks >> 2) * 128, pd0 + aoff, vd0 + ((ks * 2048) >> 4), kIdescPV,
-                 (jj > 0 || (ks & 3) > 0) ? 1u : 0u);
-          }
+          for (int ks = 0; ks < BN / 16; ++ks)
+            umma_ts(tO + (ks >> 2) * 128, tS0 + s * 128 + (ks >> 2) * 64 + (ks & 3) * 8,
+                    vd0 + ((ks * 2048) >> 4), kIdescPV, (jj > 0 || (ks & 3) > 0) ? 1u : 0u);
           umma_commit(bar(O_DONE + s));
           umma_commit(bar(V_EMPTY + s));
+          umma_commit(bar(S_FREE + s));  // S/P buffer s may take S_{jj+2}
         }
       }
       if (!ok) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
@@ -452,9 +476,6 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       tc_fence_after();
       float x[HALF];
       tmem_ld64(tS0 + s * 128 + col0 + lane_off, x);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(S_FREE + s));  // S_jj is in registers
 
       // the tile's key mask was published with K (its full barrier)
       if (!(ok = mbar_wait(bar(K_FULL + s), ph))) break;
@@ -529,17 +550,13 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       }
       l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
 
-      // P buffer s was last read by the PV of tile jj-2
-      if (jj >= 2 && !(ok = mbar_wait(bar(O_DONE + s), ((jj - 2) >> 1) & 1))) break;
-      uint8_t *pbuf = smem + Smem::kP + s * kTileBytes;
+      // P (bf16 pairs) over this half's own first 32 S columns: the PV's A
+      // operand in TMEM (the buffer was free for S_jj, so for P_jj too)
+      {
+        uint32_t pw[32];
 #pragma unroll
-      for (int cc = 0; cc < HALF / 8; ++cc) {
-        uint4 w;
-        w.x = pack_bf16(x[8 * cc], x[8 * cc + 1]);
-        w.y = pack_bf16(x[8 * cc + 2], x[8 * cc + 3]);
-        w.z = pack_bf16(x[8 * cc + 4], x[8 * cc + 5]);
-        w.w = pack_bf16(x[8 * cc + 6], x[8 * cc + 7]);
-        *reinterpret_cast<uint4 *>(pbuf + tile_off(row, hf * 8 + cc)) = w;
+        for (int i = 0; i < 32; ++i) pw[i] = pack_bf16(x[2 * i], x[2 * i + 1]);
+        tmem_st32u(tS0 + s * 128 + col0 + lane_off, pw);
       }
       // V rows of keys outside the sequence or in skipped pages must be zero
       // (P is 0 there, but 0 * NaN would still poison the product); key row
@@ -553,8 +570,9 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
         for (int cc = 0; cc < 8; ++cc)
           *reinterpret_cast<uint4 *>(vt + tile_off(row, hf * 8 + cc)) = make_uint4(0, 0, 0, 0);
       }
-      fence_proxy_async();  // P (and zeroed V rows) visible to the tensor core
-      tc_fence_before();    // (and the rescaled O columns)
+      if (!all_valid) fence_proxy_async();  // zeroed V rows visible to the tensor core
+      tmem_st_wait();     // P in TMEM
+      tc_fence_before();  // (and the rescaled O columns)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(P_FULL + s));
     }
