@@ -9,7 +9,7 @@
 // One CTA = one tile of 128 consecutive new tokens of one request for one q
 // head; its keys stream in 128-key tiles (whole page boxes).
 //   warp 8  producer: TMA loads of the Q tile once, then K and V tiles into
-//           two 2-stage rings (4-D tensor-map boxes per page and 64-column
+//           two 3-stage rings (4-D tensor-map boxes per page and 64-column
 //           half, 128-byte swizzle), plus a per-tile key-validity bitmask;
 //   warp 9  MMA issuer (one thread): S_j = Q K_j^T into TMEM buffer j%2,
 //           then O += P_{j-1} V_{j-1} into the TMEM accumulator, each a chain
@@ -52,17 +52,18 @@ constexpr int kMmaWarp = NSM_WARPS + 1;
 constexpr int HALF = BN / 2;      // S / P / O columns per softmax thread
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr uint32_t kTileBytes = BM * D * 2;  // 32 KB, any 128x128 bf16 tile
+constexpr int NKV = 3;            // K and V ring stages
 
 struct Smem {
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kTileBytes;       // 2 stages
-  static constexpr uint32_t kV = kK + 2 * kTileBytes;   // 2 stages
-  static constexpr uint32_t kMask = kV + 2 * kTileBytes;  // uint32 [4 tiles][4 words]
+  static constexpr uint32_t kK = kQ + kTileBytes;       // NKV stages
+  static constexpr uint32_t kV = kK + NKV * kTileBytes;   // NKV stages
+  static constexpr uint32_t kMask = kV + NKV * kTileBytes;  // uint32 [4 tiles][4 words]
   static constexpr uint32_t kXchg = kMask + 64;  // float [m, l][2 halves][128 rows]
   static constexpr uint32_t kBar = kXchg + 2 * 2 * BM * 4;
-  // barriers: q_full, k_full[2], v_full[2], k_empty[2], v_empty[2],
-  //           s_full[2], s_free[2], p_full[2], o_done[2], xchg[2]
-  static constexpr int kNumBars = 19;
+  // barriers: q_full, k_full[NKV], v_full[NKV], k_empty[NKV], v_empty[NKV],
+  //           s_full[2], s_free[2], p_full[2], o_done[2], xchg[2], mask_full[4]
+  static constexpr int kNumBars = 1 + 4 * NKV + 10 + 4;
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kEnd = kTmemSlot + 16;
   // The dynamic shared memory base must be 1024-byte aligned (128-byte
@@ -72,9 +73,12 @@ struct Smem {
 static_assert(Smem::kDynamic <= 232448, "shared memory plan exceeds 227 KB");
 
 enum BarId {
-  Q_FULL = 0, K_FULL = 1, V_FULL = 3, K_EMPTY = 5, V_EMPTY = 7, S_FULL = 9, S_FREE = 11,
-  P_FULL = 13, O_DONE = 15, XCHG = 17
+  Q_FULL = 0, K_FULL = 1, V_FULL = K_FULL + NKV, K_EMPTY = V_FULL + NKV,
+  V_EMPTY = K_EMPTY + NKV, S_FULL = V_EMPTY + NKV, S_FREE = S_FULL + 2,
+  P_FULL = S_FREE + 2, O_DONE = P_FULL + 2, XCHG = O_DONE + 2,
+  MASK_FULL = XCHG + 2  // [4]: the key mask of tile j is in slot j & 3
 };
+static_assert(MASK_FULL + 4 == Smem::kNumBars, "barrier plan and count agree");
 
 // ------------------------------------------------------------ PTX helpers
 
@@ -304,17 +308,20 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
 
   if (tid == 0) {
     mbar_init(bar(Q_FULL), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NKV; ++s) {
       mbar_init(bar(K_FULL + s), 1);
       mbar_init(bar(V_FULL + s), 1);
       mbar_init(bar(K_EMPTY + s), 1);
       mbar_init(bar(V_EMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar(S_FULL + s), 1);
       mbar_init(bar(S_FREE + s), 1);  // PV of the tile that used the buffer is done
       mbar_init(bar(P_FULL + s), NSM_WARPS);
       mbar_init(bar(O_DONE + s), 1);
       mbar_init(bar(XCHG + s), NSM_WARPS);
     }
+    for (int s = 0; s < 4; ++s) mbar_init(bar(MASK_FULL + s), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     fence_proxy_async();
   }
@@ -341,10 +348,10 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       tma_load_3d(sbase + Smem::kQ + BM * 128, &maps.q, 64, h, q_begin + u0, bar(Q_FULL));
     }
     for (int jj = 0; jj < n_kv; ++jj) {
-      const int s = jj & 1;
-      const uint32_t prev = ((jj >> 1) - 1) & 1;
-      // ---- K tile (stage freed when QK of tile jj-2 completed) ----
-      if (jj >= 2 && !mbar_wait(bar(K_EMPTY + s), prev)) {
+      const int s = jj % NKV;
+      const uint32_t prev = ((jj / NKV) & 1) ^ 1;
+      // ---- K tile (stage freed when QK of tile jj-NKV completed) ----
+      if (jj >= NKV && !mbar_wait(bar(K_EMPTY + s), prev)) {
         if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
         break;
       }
@@ -374,7 +381,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       // key-validity mask of the tile (inside the sequence, page loaded),
       // published with K: slot jj & 3 was last read by the softmax of tile
       // jj - 4, which finished before the V stage this loop waited on below
-      // for tile jj - 1 was released
+      // for tile jj - 1 was released (the PV of tile jj - 1 - NKV >= jj - 4)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = lane + 32 * i;
@@ -382,6 +389,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
         const uint32_t bits = __ballot_sync(0xffffffffu, okr && key0 + r < kv_len);
         if (lane == 0) sMask[(jj & 3) * 4 + i] = bits;
       }
+      if (lane == 0) mbar_arrive(bar(MASK_FULL + (jj & 3)));
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL + s), bytes);
       __syncwarp();
@@ -390,8 +398,8 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
         tma_load_4d(kdst, &maps.k, 0, kvh, inpage, page, bar(K_FULL + s));
         tma_load_4d(kdst + BN * 128, &maps.k, 64, kvh, inpage, page, bar(K_FULL + s));
       }
-      // ---- V tile (stage freed when the PV of tile jj-2 completed) ----
-      if (jj >= 2 && !mbar_wait(bar(V_EMPTY + s), prev)) {
+      // ---- V tile (stage freed when the PV of tile jj-NKV completed) ----
+      if (jj >= NKV && !mbar_wait(bar(V_EMPTY + s), prev)) {
         if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
         break;
       }
@@ -413,31 +421,31 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       const uint64_t qd0 = smem_desc(sbase + Smem::kQ, 0, 1024);
       for (int j = 0; ok && j <= n_kv; ++j) {
         if (j < n_kv) {  // S_j = Q K_j^T
-          const int s = j & 1;
-          ok = mbar_wait(bar(K_FULL + s), (j >> 1) & 1) &&
+          const int s = j & 1, sk = j % NKV;
+          ok = mbar_wait(bar(K_FULL + sk), (j / NKV) & 1) &&
                (j < 2 || mbar_wait(bar(S_FREE + s), ((j >> 1) - 1) & 1));
           if (!ok) break;
           tc_fence_after();
           // descriptors formed once per tile; a K step adds a constant to the
           // start-address field (16-byte units), so the single issuing
           // thread does no 64-bit descriptor arithmetic per MMA
-          const uint64_t kd0 = smem_desc(sbase + Smem::kK + s * kTileBytes, 0, 1024);
+          const uint64_t kd0 = smem_desc(sbase + Smem::kK + sk * kTileBytes, 0, 1024);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint64_t koff = ((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4;
             umma(tS0 + s * 128, qd0 + koff, kd0 + koff, kIdescQK, ks > 0);
           }
           umma_commit(bar(S_FULL + s));
-          umma_commit(bar(K_EMPTY + s));
+          umma_commit(bar(K_EMPTY + sk));
         }
         if (j >= 1) {  // O += P_{j-1} V_{j-1}
           const int jj = j - 1;
-          const int s = jj & 1;
+          const int s = jj & 1, sv = jj % NKV;
           ok = mbar_wait(bar(P_FULL + s), (jj >> 1) & 1) &&
-               mbar_wait(bar(V_FULL + s), (jj >> 1) & 1);
+               mbar_wait(bar(V_FULL + sv), (jj / NKV) & 1);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t vd0 = smem_desc(sbase + Smem::kV + s * kTileBytes, BN * 128, 1024);
+          const uint64_t vd0 = smem_desc(sbase + Smem::kV + sv * kTileBytes, BN * 128, 1024);
           // keys 0-63 of the tile accumulate into O_A, keys 64-127 into O_B
           // (each half of the softmax keeps its own reference max); P_j is
           // read from TMEM: keys 64h + 16k.. at column 128 s + 64 h + 8 k
@@ -446,7 +454,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
             umma_ts(tO + (ks >> 2) * 128, tS0 + s * 128 + (ks >> 2) * 64 + (ks & 3) * 8,
                     vd0 + ((ks * 2048) >> 4), kIdescPV, (jj > 0 || (ks & 3) > 0) ? 1u : 0u);
           umma_commit(bar(O_DONE + s));
-          umma_commit(bar(V_EMPTY + s));
+          umma_commit(bar(V_EMPTY + sv));
           umma_commit(bar(S_FREE + s));  // S/P buffer s may take S_{jj+2}
         }
       }
@@ -477,8 +485,11 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       float x[HALF];
       tmem_ld64(tS0 + s * 128 + col0 + lane_off, x);
 
-      // the tile's key mask was published with K (its full barrier)
-      if (!(ok = mbar_wait(bar(K_FULL + s), ph))) break;
+      // the tile's key mask (its slot is rewritten only for tile jj + 4,
+      // after this softmax is done, so the phase cannot run ahead)
+      const int skv = jj % NKV;
+      const uint32_t pkv = (jj / NKV) & 1;
+      if (!(ok = mbar_wait(bar(MASK_FULL + (jj & 3)), (jj >> 2) & 1))) break;
       const int ms = (jj & 3) * 4;
       const int key0 = (jt0 + jj) * BN + col0;  // key of this thread's column 0
       const uint32_t mk0 = sMask[ms + 2 * hf], mk1 = sMask[ms + 2 * hf + 1];
@@ -563,9 +574,9 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       // `row` of the tile, this thread's half of its columns
       const uint32_t own = quad == 0 ? sMask[ms] : quad == 1 ? sMask[ms + 1]
                          : quad == 2 ? sMask[ms + 2] : sMask[ms + 3];
-      if (!all_valid && !(ok = mbar_wait(bar(V_FULL + s), ph))) break;  // rows to zero
+      if (!all_valid && !(ok = mbar_wait(bar(V_FULL + skv), pkv))) break;  // rows to zero
       if (!all_valid && !((own >> lane) & 1u)) {
-        uint8_t *vt = smem + Smem::kV + s * kTileBytes;
+        uint8_t *vt = smem + Smem::kV + skv * kTileBytes;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
           *reinterpret_cast<uint4 *>(vt + tile_off(row, hf * 8 + cc)) = make_uint4(0, 0, 0, 0);
