@@ -30,6 +30,7 @@ import torch
 from ._build import build_library, lib_path
 
 __all__ = [
+    "cascade_attn_with_kvcache",
     "attn_with_kvcache",
     "attn_workspace_size",
     "attn_with_kvcache_noalloc",
@@ -232,6 +233,33 @@ def merge_state(v_a, lse_a, v_b, lse_b, v_out=None, lse_out=None):
         _desc(v_a), _desc(lse_a), _desc(v_b), _desc(lse_b), _desc(v_out),
         _desc(lse_out), _stream(v_a)))
     return v_out, lse_out
+
+
+def cascade_attn_with_kvcache(q, k_cache, v_cache, prefix_page_table, prefix_seqlens,
+                              suffix_page_table, suffix_seqlens, cu_seqlens_q,
+                              max_seqlen_q: int, softmax_scale: float, causal: bool = False,
+                              num_splits: int = 0, out=None, lse=None,
+                              return_softmax_lse: bool = False):
+    """Cascade attention over a key range held in two parts, as the
+    FlashAttention backend runs it (flashattention_backend.py, `forward_decode`
+    with `use_cascade_attn`): attention over the committed prefix with no
+    causal mask, attention over the suffix with its own page table and
+    lengths (causal within it when asked), and the log-sum-exp merge of the
+    two states (`merge_state_v2`).  Every step is a call into libpkv; the
+    partial outputs are bf16, as on that path.
+
+    prefix_page_table / prefix_seqlens: the part every query sees in full
+    (keys [0, prefix_len) of each request); suffix_page_table /
+    suffix_seqlens: the remaining keys, positioned after the prefix (the
+    queries sit at the end of the suffix, bottom-right).  No window."""
+    o1, l1 = attn_with_kvcache(q, k_cache, v_cache, prefix_page_table, prefix_seqlens,
+                               cu_seqlens_q, max_seqlen_q, softmax_scale, causal=False,
+                               num_splits=num_splits, return_softmax_lse=True)
+    o2, l2 = attn_with_kvcache(q, k_cache, v_cache, suffix_page_table, suffix_seqlens,
+                               cu_seqlens_q, max_seqlen_q, softmax_scale, causal=causal,
+                               num_splits=num_splits, return_softmax_lse=True)
+    out, lse = merge_state(o1, l1, o2, l2, out, lse)
+    return (out, lse) if return_softmax_lse else out
 
 
 def build_swa_page_table(req_to_token, req_pool_indices, seq_lens,

@@ -564,6 +564,46 @@ def test_page_box_balanced_sixteen_rows_per_kv_head(page_size, q_len, window):
     assert pkv.get_error_flags() == 0
 
 
+def test_cascade_shared_prefix_attention():
+    """Cascade attention through the library: every request shares the same
+    prefix pages (a common system prompt) and owns its suffix pages; prefix
+    call + suffix call + state merge equals the oracle's single call over
+    the concatenated table (causal runs of new tokens at the suffix end)."""
+    P, batch, q_len = 16, 5, 3
+    pre_pages = 6
+    wl = workloads.make("tiny_decode", d=128, page_size=P, h_q=16, h_kv=4, q_len=q_len,
+                        causal=True, len_lo=q_len + 1, len_hi=500, batch=batch,
+                        pool_tokens=(batch * 520 + pre_pages * P) * 2, seed=55)
+    n_own = [-(-int(wl.cache_seqlens[b]) // P) for b in range(batch)]
+    used = set()
+    for b in range(batch):
+        used.update(wl.page_table[b, :n_own[b]].tolist())
+    free = [p for p in range(wl.k_cache.shape[0]) if p not in used]
+    shared = torch.tensor(free[1::2][:pre_pages], dtype=torch.int32)  # pool pages no request owns
+    assert shared.numel() == pre_pages
+    full_pt = torch.zeros(batch, pre_pages + wl.page_table.shape[1], dtype=torch.int32)
+    suf_pt = torch.zeros(batch, wl.page_table.shape[1], dtype=torch.int32)
+    for b in range(batch):
+        own = wl.page_table[b, :n_own[b]]
+        full_pt[b, :pre_pages] = shared
+        full_pt[b, pre_pages:pre_pages + n_own[b]] = own
+        suf_pt[b, :n_own[b]] = own
+    suf_len = wl.cache_seqlens.clone()
+    pre_len = torch.full((batch,), pre_pages * P, dtype=torch.int32)
+    full_len = pre_len + suf_len
+    wl.page_table, wl.cache_seqlens = full_pt, full_len
+    g = wl.to(DEV)
+    # the prefix call reads the shared pages (the first columns of the full
+    # table); the suffix call reads each request's own pages
+    out, lse = pkv.cascade_attn_with_kvcache(
+        g.q, g.k_cache, g.v_cache, full_pt.to(DEV), pre_len.to(DEV), suf_pt.to(DEV),
+        suf_len.to(DEV), g.cu_seqlens_q, q_len, g.scale, causal=True, return_softmax_lse=True)
+    torch.cuda.synchronize()
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, "cascade")
+    assert pkv.get_error_flags() == 0
+
+
 def test_head_major_cache_layout():
     """A cache laid out [pages, H_kv, P, D] (head outside position) is read
     through its strides; results equal the oracle's."""
