@@ -11,6 +11,10 @@ Every function restates a definition from the SGLang attention-backend pages:
   ("Convert the page table to a strided format").
 * ``swa_page_table`` -- flashattention_backend.py, ``_build_pa_page_table_kernel``.
 * ``topk_to_slots`` -- nsa_backend.py, ``TopkTransformMethod.PAGED``.
+* ``local_virtual_batches`` -- flashattention_backend.py,
+  ``make_local_attention_virtual_batches`` (local chunked attention as
+  virtual batches) and the mask drawn in its worked example
+  (``attention(..., attn_chunk=C)``).
 * ``attention`` -- flashattention_backend.py ``forward_decode`` /
   ``forward_extend`` (``flash_attn_with_kvcache``), absorbed MLA call,
   nsa_backend.py ``forward_decode`` (top-k), bottom-right causal alignment
@@ -35,6 +39,7 @@ __all__ = [
     "strided_page_table",
     "swa_page_table",
     "topk_to_slots",
+    "local_virtual_batches",
     "attention",
     "merge_state",
     "split_bounds",
@@ -73,13 +78,17 @@ def _lib():
             _u16p, _i64, _i64, _i64, _int,
             _int, _int, _i64,
             _i32p, _i64, _int,
-            _i32p, _i32p, _int, ctypes.c_double, _int, _int,
+            _i32p, _i32p, _int, ctypes.c_double, _int, _int, _int,
             _i32p, _i64, _int,
             _i32p, _int, _f64p, _f64p, _int]
+        lib.orc_local_virtual_batches.argtypes = [
+            _int, _int, _i32p, _i32p, _int, _i32p, _i64, _int, _int,
+            _i32p, _i32p, _i32p, _i32p, _i64, _int, _i32p]
         lib.orc_merge_state.argtypes = [
             _f64p, _f64p, _f64p, _f64p, _i64, _int, _f64p, _f64p]
         for fn in ("orc_strided_page_table", "orc_swa_page_table",
-                   "orc_topk_to_slots", "orc_attention", "orc_merge_state"):
+                   "orc_topk_to_slots", "orc_attention", "orc_merge_state",
+                   "orc_local_virtual_batches"):
             getattr(lib, fn).restype = ctypes.c_int
         _LIB = lib
     return _LIB
@@ -164,11 +173,59 @@ def topk_to_slots(topk, row_req, page_table, page_size: int,
     return out, rc
 
 
+def local_virtual_batches(attn_chunk_size: int, page_size: int, cu_seqlens_q,
+                          seq_lens, page_table, capacity: int | None = None,
+                          bt_cols: int | None = None):
+    """Local (chunked) attention split into virtual batches.
+
+    Returns a dict with ``seqlens_q_local`` [cap], ``cu_seqlens_q_local``
+    [cap + 1], ``seqlens_k_local`` [cap], ``block_table_local`` [cap,
+    bt_cols] (int32), ``num_virtual``, ``chunk`` (the effective chunk),
+    ``max_q_local``, ``max_k_local`` and ``bad`` (malformed requests).
+    ``capacity`` defaults to the exact number of virtual batches and
+    ``bt_cols`` to chunk / page_size."""
+    cu = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    assert pt.ndim == 2 and pt.shape[0] == len(sl) and len(cu) == len(sl) + 1
+
+    def run(cap, cols):
+        outs = (np.zeros(cap, np.int32), np.zeros(cap + 1, np.int32),
+                np.zeros(cap, np.int32), np.zeros((cap, cols), np.int32))
+        info = np.zeros(4, np.int32)
+        rc = _lib().orc_local_virtual_batches(
+            int(attn_chunk_size), int(page_size), _ptr(cu, ctypes.c_int32),
+            _ptr(sl, ctypes.c_int32), len(sl), _ptr(pt, ctypes.c_int32),
+            pt.shape[1], pt.shape[1], cap, _ptr(outs[0], ctypes.c_int32),
+            _ptr(outs[1], ctypes.c_int32), _ptr(outs[2], ctypes.c_int32),
+            _ptr(outs[3], ctypes.c_int32), cols, cols, _ptr(info, ctypes.c_int32))
+        if rc < 0:
+            raise ValueError(f"orc_local_virtual_batches rejected its arguments ({rc})")
+        return outs, info, rc
+
+    if capacity is None or bt_cols is None:
+        # a sizing pass: no rows, table width large enough for any chunk
+        _, info, _ = run(0, max(attn_chunk_size // page_size, 1))
+        if capacity is None:
+            capacity = int(info[0])
+        if bt_cols is None:
+            bt_cols = int(info[1]) // page_size
+    (sq, cuq, sk, bt), info, rc = run(int(capacity), int(bt_cols))
+    return {"seqlens_q_local": sq, "cu_seqlens_q_local": cuq,
+            "seqlens_k_local": sk, "block_table_local": bt,
+            "num_virtual": int(info[0]), "chunk": int(info[1]),
+            "max_q_local": int(info[2]), "max_k_local": int(info[3]),
+            "bad": rc}
+
+
 def attention(q_bits, k_bits, v_bits, page_table, cache_seqlens, cu_seqlens_q,
               scale: float, causal: bool = False, window_left: int = -1,
               topk=None, rows=None, d_v: int | None = None,
-              num_threads: int = 0):
+              num_threads: int = 0, attn_chunk: int = 0):
     """Paged attention in float64.
+
+    ``attn_chunk`` > 0 restricts each query to the keys of its own
+    attn_chunk-sized chunk (local chunked attention).
 
     q_bits: uint16 [total_q, H_q, D_qk]; k_bits / v_bits: uint16
     [num_pages, P, H_kv, D] views (any element strides; D contiguous).
@@ -206,7 +263,7 @@ def attention(q_bits, k_bits, v_bits, page_table, cache_seqlens, cu_seqlens_q,
         _ptr(pt, ctypes.c_int32), pt.shape[1] if pt.ndim == 2 else 0,
         pt.shape[1] if pt.ndim == 2 else 0,
         _ptr(cs, ctypes.c_int32), _ptr(cu, ctypes.c_int32), len(cs),
-        float(scale), int(bool(causal)), int(window_left),
+        float(scale), int(bool(causal)), int(window_left), int(attn_chunk),
         _ptr(tk, ctypes.c_int32), 0 if tk is None else tk.shape[1],
         0 if tk is None else tk.shape[1],
         _ptr(rw, ctypes.c_int32), 0 if rw is None else rw.shape[0],

@@ -104,6 +104,92 @@ int orc_topk_to_slots(const int32_t *topk, int64_t topk_stride, int n_rows,
   return bad;
 }
 
+int orc_local_virtual_batches(int attn_chunk_size, int page_size,
+                              const int32_t *cu_seqlens_q,
+                              const int32_t *seq_lens, int batch,
+                              const int32_t *page_table, int64_t pt_stride,
+                              int pt_cols, int capacity,
+                              int32_t *seqlens_q_local,
+                              int32_t *cu_seqlens_q_local,
+                              int32_t *seqlens_k_local,
+                              int32_t *block_table_local, int64_t bt_stride,
+                              int bt_cols, int32_t *info) {
+  if (attn_chunk_size < 1 || page_size < 1 || pt_cols < 1 || batch < 0 ||
+      capacity < 0)
+    return -1;
+  /* 1. the effective chunk: no longer than the longest sequence, a whole
+        number of pages, at least one page */
+  int32_t max_seq_len = 0;
+  for (int b = 0; b < batch; ++b)
+    if (seq_lens[b] > max_seq_len) max_seq_len = seq_lens[b];
+  int32_t C = attn_chunk_size < max_seq_len ? attn_chunk_size : max_seq_len;
+  C = (C / page_size) * page_size;
+  if (C < page_size) C = page_size;
+  const int pages_per_local_batch = C / page_size;
+  if (bt_cols < pages_per_local_batch) return -1;
+
+  int bad = 0;
+  int64_t v = 0;            /* virtual batches so far */
+  int32_t cu = batch > 0 ? cu_seqlens_q[0] : 0;
+  int32_t max_q_local = 0, max_k_local = 0;
+  cu_seqlens_q_local[0] = cu;
+  for (int b = 0; b < batch; ++b) {
+    int32_t q = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+    int32_t kv = seq_lens[b];
+    if (q == 0) continue;
+    if (q < 0 || kv < q) { ++bad; continue; }
+    /* 2. new tokens in the chunk of the first new token; keys in the chunk
+          of the last key; number of chunks the new tokens touch */
+    int32_t first = C - (kv - q) % C;
+    if (first > q) first = q;
+    int32_t last_k = kv - C * ((kv - 1) / C);
+    int32_t blocks = 1 + (q - first + C - 1) / C;
+    /* 3. one virtual batch per chunk */
+    for (int32_t a = 0; a < blocks; ++a, ++v) {
+      int32_t r = blocks - 1 - a;
+      int32_t q_local;
+      if (a == 0) {
+        q_local = first;
+      } else {
+        q_local = q - first - C * (a - 1);
+        if (q_local > C) q_local = C;
+      }
+      int32_t k_local = r == 0 ? last_k : C;
+      int64_t k_start = (int64_t)kv - last_k - (int64_t)r * C;
+      if (q_local > max_q_local) max_q_local = q_local;
+      if (k_local > max_k_local) max_k_local = k_local;
+      cu += q_local;
+      if (v >= capacity) continue;
+      seqlens_q_local[v] = q_local;
+      cu_seqlens_q_local[v + 1] = cu; /* 4. running sum */
+      seqlens_k_local[v] = k_local;
+      /* 5. the pages that hold the chunk's keys */
+      int32_t *row = block_table_local + v * bt_stride;
+      for (int j = 0; j < bt_cols; ++j) {
+        if (j < pages_per_local_batch) {
+          int64_t col = k_start / page_size + j;
+          if (col > pt_cols - 1) col = pt_cols - 1;
+          row[j] = page_table[(int64_t)b * pt_stride + col];
+        } else {
+          row[j] = 0;
+        }
+      }
+    }
+  }
+  int64_t n_virtual = v;
+  for (; v < capacity; ++v) { /* padding rows */
+    seqlens_q_local[v] = 0;
+    cu_seqlens_q_local[v + 1] = cu;
+    seqlens_k_local[v] = 0;
+    for (int j = 0; j < bt_cols; ++j) block_table_local[v * bt_stride + j] = 0;
+  }
+  info[0] = (int32_t)n_virtual;
+  info[1] = C;
+  info[2] = max_q_local;
+  info[3] = max_k_local;
+  return bad;
+}
+
 /* One (token, head) row of paged attention, straight from the definition. */
 static int attend_row(const uint16_t *q, int64_t q_st, int64_t q_sh, int d_qk,
                       const uint16_t *k_cache, int64_t k_sp, int64_t k_spos,
@@ -113,7 +199,8 @@ static int attend_row(const uint16_t *q, int64_t q_st, int64_t q_sh, int d_qk,
                       const int32_t *page_table, int64_t pt_stride, int pt_cols,
                       const int32_t *cache_seqlens, const int32_t *cu_seqlens_q,
                       int batch, double scale, int causal, int window_left,
-                      const int32_t *topk, int64_t topk_stride, int topk_len,
+                      int attn_chunk, const int32_t *topk,
+                      int64_t topk_stride, int topk_len,
                       int t, int h, double *o, double *lse_out, double *s_buf,
                       int64_t *slot_buf) {
   /* request of token t: cu[b] <= t < cu[b+1] */
@@ -144,6 +231,9 @@ static int attend_row(const uint16_t *q, int64_t q_st, int64_t q_sh, int d_qk,
     }
     if (causal && j > i) continue;
     if (window_left >= 0 && (j > i || j < i - window_left)) continue;
+    /* local chunked attention: keys of the query's own chunk only (j and i
+       are non-negative, so C division is floor division) */
+    if (attn_chunk > 0 && j / attn_chunk != i / attn_chunk) continue;
     /* 2. logical position -> physical slot through the page table */
     if (j / page_size >= pt_cols) { ++skipped; continue; }
     int64_t page = page_table[(int64_t)b * pt_stride + j / page_size];
@@ -193,11 +283,12 @@ int orc_attention(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q,
                   const int32_t *page_table, int64_t pt_stride, int pt_cols,
                   const int32_t *cache_seqlens, const int32_t *cu_seqlens_q,
                   int batch, double scale, int causal, int window_left,
-                  const int32_t *topk, int64_t topk_stride, int topk_len,
-                  const int32_t *rows, int n_rows, double *out, double *lse,
-                  int num_threads) {
+                  int attn_chunk, const int32_t *topk, int64_t topk_stride,
+                  int topk_len, const int32_t *rows, int n_rows, double *out,
+                  double *lse, int num_threads) {
   if (total_q < 0 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0 || d_qk < 1 ||
-      d_v < 1 || page_size < 1 || batch < 0 || window_left < -1)
+      d_v < 1 || page_size < 1 || batch < 0 || window_left < -1 ||
+      attn_chunk < 0)
     return -1;
   int64_t n_work = rows ? (int64_t)n_rows : (int64_t)total_q * h_q;
   /* longest candidate list any row can have */
@@ -225,7 +316,8 @@ int orc_attention(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q,
                           v_cache, v_sp, v_spos, v_sh, d_v, h_q, h_kv,
                           page_size, num_pages, page_table, pt_stride, pt_cols,
                           cache_seqlens, cu_seqlens_q, batch, scale, causal,
-                          window_left, topk, topk_stride, topk_len, t, h,
+                          window_left, attn_chunk, topk, topk_stride,
+                          topk_len, t, h,
                           out + w * d_v, lse ? lse + w : NULL, s_buf, slot_buf);
       /* a token's skipped entries are the same for every head: count them
          on its head-0 row only */

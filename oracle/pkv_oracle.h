@@ -71,6 +71,42 @@ int orc_topk_to_slots(const int32_t *topk, int64_t topk_stride, int n_rows,
                       const int32_t *cache_seqlens, int32_t *out,
                       int64_t out_stride);
 
+/* Local (chunked) attention as virtual batches (flashattention_backend.py,
+ * `make_local_attention_virtual_batches` and its worked example):
+ *   1. effective chunk C = min(attn_chunk_size, max_b seq_lens[b]), rounded
+ *      down to a multiple of page_size, and at least page_size;
+ *   2. per request b with q = cu[b+1] - cu[b] new tokens and kv = seq_lens[b]
+ *      keys: first = min(C - (kv - q) % C, q) new tokens fall in the chunk
+ *      that holds the first new token; the chunk holding the last key has
+ *      last_k = kv - C * ((kv - 1) / C) keys; blocks = 1 + ceil((q - first) / C);
+ *   3. virtual batch a of request b (a = 0 .. blocks-1, reverse index
+ *      r = blocks - 1 - a): q_local = first for a = 0, else
+ *      min(q - first - C * (a - 1), C); k_local = last_k for r = 0, else C;
+ *      its keys start at kv - last_k - r * C;
+ *   4. cu_seqlens_q_local = cu[0] followed by the running sum of q_local;
+ *   5. block_table_local row = the C / page_size page ids that cover the
+ *      virtual batch's keys, page_table[b][min(start / page_size + j,
+ *      pt_cols - 1)] (a column past the row repeats its last entry).
+ * Virtual batches are numbered request by request.  A request with q = 0
+ * makes none; one with q < 0 or kv < q makes none and is counted.  Rows at
+ * or past the count, up to `capacity`, are padding: q_local = k_local = 0,
+ * cu repeats the total, table row all 0; table columns at or past
+ * C / page_size are 0.  info = {virtual batches, C, max q_local,
+ * max k_local} (the count may exceed capacity: only capacity rows exist).
+ * Returns the number of requests counted as malformed, or -1 on bad
+ * arguments (attn_chunk_size < 1, page_size < 1, pt_cols < 1,
+ * bt_cols < C / page_size). */
+int orc_local_virtual_batches(int attn_chunk_size, int page_size,
+                              const int32_t *cu_seqlens_q,
+                              const int32_t *seq_lens, int batch,
+                              const int32_t *page_table, int64_t pt_stride,
+                              int pt_cols, int capacity,
+                              int32_t *seqlens_q_local,
+                              int32_t *cu_seqlens_q_local,
+                              int32_t *seqlens_k_local,
+                              int32_t *block_table_local, int64_t bt_stride,
+                              int bt_cols, int32_t *info);
+
 /* Paged attention of new query tokens against a paged KV cache
  * (flashattention_backend.py `forward_decode` / `forward_extend`,
  * nsa_backend.py `forward_decode` for the top-k variant).
@@ -88,7 +124,9 @@ int orc_topk_to_slots(const int32_t *topk, int64_t topk_stride, int n_rows,
  * position i = cache_seqlens[b] - (cu[b+1]-cu[b]) + u (bottom-right causal).
  * Dense key set: j in [0, kv_len); causal => j <= i;
  * window_left >= 0 => i - window_left <= j <= i (window (left, 0), both ends
- * inclusive).  Top-k (topk != NULL): the keys are the entries of
+ * inclusive); attn_chunk > 0 => j / attn_chunk == i / attn_chunk (local
+ * chunked attention: a query sees only keys of its own chunk, the mask that
+ * flashattention_backend.py draws for `make_local_attention_virtual_batches`).  Top-k (topk != NULL): the keys are the entries of
  * topk[t*topk_stride + 0 .. topk_len), -1 skipped, each occurrence counted,
  * then the same masks; an index < -1 or >= kv_len is skipped and counted.
  * q head h reads kv head h / (h_q / h_kv).
@@ -109,9 +147,9 @@ int orc_attention(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q,
                   const int32_t *page_table, int64_t pt_stride, int pt_cols,
                   const int32_t *cache_seqlens, const int32_t *cu_seqlens_q,
                   int batch, double scale, int causal, int window_left,
-                  const int32_t *topk, int64_t topk_stride, int topk_len,
-                  const int32_t *rows, int n_rows, double *out, double *lse,
-                  int num_threads);
+                  int attn_chunk, const int32_t *topk, int64_t topk_stride,
+                  int topk_len, const int32_t *rows, int n_rows, double *out,
+                  double *lse, int num_threads);
 
 /* Log-sum-exp state merge (dual_chunk_flashattention_backend.py,
  * `_merge_attn_outputs`; merge_state_v2 in flashattention_backend.py):

@@ -411,6 +411,35 @@ def test_merge_of_two_halves_equals_full_attention():
         np.testing.assert_allclose(lm, full_l, atol=1e-13)
 
 
+def test_cascade_prefix_and_suffix_merge_to_single_call():
+    """Cascade attention (flashattention_backend.py, `use_cascade_attn`): a
+    call over the prefix pages without causal mask, a call over the suffix
+    pages with the suffix's own lengths (causal, bottom-right), merged by
+    log-sum-exp, equals one causal call over the whole table; prefixes of
+    zero, one and several pages."""
+    rng = np.random.default_rng(41)
+    P = 4
+    q_lens, kv_lens = [1, 3, 2], [13, 22, 9]
+    c = _tiny_case(rng, 3, q_lens, kv_lens, 4, 2, 8, P)
+    full_o, full_l, _ = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"],
+                                         c["cu"], 0.4, causal=True)
+    for pre_pages in ([0, 0, 0], [1, 2, 1], [3, 4, 1]):
+        pre_len = np.array([n * P for n in pre_pages], dtype=np.int32)
+        suf_len = (c["kv"] - pre_len).astype(np.int32)
+        assert np.all(suf_len >= np.array(q_lens))  # queries sit in the suffix
+        width = c["pt"].shape[1]
+        suf_pt = np.zeros_like(c["pt"])
+        for b, n in enumerate(pre_pages):
+            suf_pt[b, :width - n] = c["pt"][b, n:]
+        oa, la, _ = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], pre_len, c["cu"], 0.4,
+                                     causal=False)
+        ob, lb, _ = oracle.attention(c["qb"], c["kb"], c["vb"], suf_pt, suf_len, c["cu"], 0.4,
+                                     causal=True)
+        om, lm = oracle.merge_state(oa, la, ob, lb)
+        np.testing.assert_allclose(om, full_o, atol=1e-13)
+        np.testing.assert_allclose(lm, full_l, atol=1e-13)
+
+
 def test_merge_closed_forms_and_algebra():
     rng = np.random.default_rng(16)
     va, vb, vc = (rng.standard_normal((5, 3, 4)) for _ in range(3))
@@ -467,3 +496,198 @@ def test_split_bounds_are_page_aligned_and_cover():
                 assert b[0][0] == 0 and b[-1][1] == kv
                 for (lo, hi), (lo2, _) in zip(b, b[1:]):
                     assert hi == lo2 and (lo % p == 0 or lo == kv)
+
+
+# ------------------------------------------- local (chunked) attention batches
+
+def _vb_requests(cu, kv, out):
+    """Request index of every virtual batch, from where its query tokens lie."""
+    cu = np.asarray(cu)
+    reqs = []
+    for v in range(out["num_virtual"]):
+        lo = out["cu_seqlens_q_local"][v]
+        b = int(np.searchsorted(cu, lo, side="right") - 1)
+        while cu[b + 1] - cu[b] == 0:  # requests with no new tokens own none
+            b += 1
+        reqs.append(b)
+    return reqs
+
+
+def _check_chunk_picture(cu, kv, pt, P, out):
+    """Every virtual batch is the part of one request's queries that falls in
+    one chunk: its queries are consecutive absolute positions of one chunk,
+    the last of them is the last key the batch holds (bottom-right), its
+    keys are the chunk's keys up to there, and its table row maps local key
+    l to the page of absolute key chunk_start + l."""
+    C = out["chunk"]
+    cu = np.asarray(cu)
+    reqs = _vb_requests(cu, kv, out)
+    covered = np.zeros(cu[-1], dtype=int)
+    for v, b in enumerate(reqs):
+        lo, hi = out["cu_seqlens_q_local"][v], out["cu_seqlens_q_local"][v + 1]
+        assert hi - lo == out["seqlens_q_local"][v] >= 1
+        covered[lo:hi] += 1
+        q_len = cu[b + 1] - cu[b]
+        pos = [kv[b] - q_len + (t - cu[b]) for t in range(lo, hi)]
+        assert len({p // C for p in pos}) == 1
+        start = (pos[0] // C) * C
+        k_local = out["seqlens_k_local"][v]
+        assert start + k_local - 1 == pos[-1]
+        assert k_local == min(C, kv[b] - start)
+        for l in range(k_local):
+            assert out["block_table_local"][v, l // P] == pt[b, (start + l) // P]
+    # every query token is in exactly one virtual batch
+    assert np.all(covered[cu[0]:] == 1)
+
+
+@pytest.mark.parametrize("row", read_golden("local_virtual_batches.txt"))
+def test_local_virtual_batches_printed_example(row):
+    """The worked example printed with `make_local_attention_virtual_batches`
+    (golden fixture): q_seqlens_local, seqlens_k_local, first-block tokens and
+    local_blocks as printed; cu_seqlens_q_local is the running sum of the
+    query lengths, and the printed cu line is the running sum of the key
+    lengths."""
+    (chunk, P), cu, kv, first, blocks, q_local, k_local, printed_cu = row
+    width = -(-max(kv) // P)
+    pt = np.array([[1000 * b + j for j in range(width)] for b in range(len(kv))])
+    out = oracle.local_virtual_batches(chunk, P, cu, kv, pt)
+    assert out["bad"] == 0 and out["chunk"] == chunk
+    assert out["num_virtual"] == sum(blocks) == len(q_local)
+    assert list(out["seqlens_q_local"]) == q_local
+    assert list(out["seqlens_k_local"]) == k_local
+    assert list(out["cu_seqlens_q_local"]) == [0] + list(np.cumsum(q_local))
+    assert printed_cu == [0] + list(np.cumsum(k_local))
+    starts = np.concatenate([[0], np.cumsum(blocks)[:-1]])
+    assert [q_local[s] for s in starts] == first
+    for b, (s, n) in enumerate(zip(starts, blocks)):
+        assert sum(q_local[s:s + n]) == cu[b + 1] - cu[b]
+    assert out["max_q_local"] == max(q_local) and out["max_k_local"] == max(k_local)
+    _check_chunk_picture(cu, kv, pt, P, out)
+
+
+def test_local_mask_printed_example():
+    """The regular and the local (chunk 4) masks printed for batch index 0 of
+    the example (q_seqlens 4, kv_seqlens 6), read off the oracle's attention:
+    with q = 0 every visible key gets the same weight and one-hot value rows
+    show which keys those are."""
+    rows = read_golden("local_mask.txt")
+    kv_len, q_len = 6, 4
+    qb = np.zeros((q_len, 1, kv_len), dtype=np.uint16)
+    eye = bf16(np.eye(kv_len)[:, None, :])[0]  # value row j = e_j
+    kb = eye[None]  # one page of 6 slots, 1 head, D = 6
+    vb = eye[None]
+    pt = np.array([[0]], dtype=np.int32)
+    for chunk in (0, 4):
+        out, _, _ = oracle.attention(qb, kb, vb, pt, [kv_len], [0, q_len], 1.0,
+                                     causal=True, attn_chunk=chunk)
+        for (c, t), vis in rows:
+            if c != chunk:
+                continue
+            got = (out[t, 0] > 0).astype(int)
+            assert list(got) == vis
+            np.testing.assert_allclose(out[t, 0][got == 1], 1.0 / sum(vis), atol=1e-15)
+
+
+def _local_case(rng, q_lens, kv_lens, P, h_q=4, h_kv=2, d=8):
+    c = _tiny_case(rng, len(q_lens), q_lens, kv_lens, h_q, h_kv, d, P)
+    return c
+
+
+@pytest.mark.parametrize("chunk,P,q_lens,kv_lens", [
+    (4, 1, [4, 10, 5], [6, 17, 9]),          # the printed example
+    (8, 4, [1, 1, 1, 1], [1, 8, 9, 30]),     # decode: one virtual batch each
+    (8, 4, [13, 3, 8, 1], [13, 20, 16, 40]),  # extend spanning chunks
+    (12, 4, [7, 20, 2], [30, 45, 2]),        # chunk of three pages
+    (32, 4, [5, 17], [9, 17]),               # chunk > longest: cut to 16
+    (6, 4, [9, 4], [25, 11]),                # chunk not a page multiple: 4
+    (3, 4, [2, 5], [7, 12]),                 # chunk below a page: one page
+])
+def test_local_virtual_batches_equal_local_mask_attention(chunk, P, q_lens, kv_lens):
+    """Brute force: causal attention over the virtual batches (their query
+    offsets, key lengths and local tables) equals causal attention with the
+    local chunk mask over the original table, element by element; and every
+    virtual batch matches the chunk picture."""
+    rng = np.random.default_rng(sum(kv_lens) + chunk)
+    c = _local_case(rng, q_lens, kv_lens, P)
+    out = oracle.local_virtual_batches(chunk, P, c["cu"], c["kv"], c["pt"])
+    assert out["bad"] == 0
+    _check_chunk_picture(c["cu"], c["kv"], c["pt"], P, out)
+    ref_o, ref_l, _ = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"], c["cu"],
+                                       0.35, causal=True, attn_chunk=out["chunk"])
+    got_o, got_l, _ = oracle.attention(c["qb"], c["kb"], c["vb"], out["block_table_local"],
+                                       out["seqlens_k_local"], out["cu_seqlens_q_local"],
+                                       0.35, causal=True)
+    np.testing.assert_allclose(got_o, ref_o, atol=1e-13)
+    np.testing.assert_allclose(got_l, ref_l, atol=1e-13)
+
+
+def test_local_chunk_mask_changes_the_result():
+    """The chunk mask is not a no-op: a query in the second chunk differs
+    from plain causal attention, one in the first chunk does not."""
+    rng = np.random.default_rng(3)
+    c = _local_case(rng, [6], [6], 1)
+    a, _, _ = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"], c["cu"], 0.5,
+                               causal=True, attn_chunk=4)
+    b, _, _ = oracle.attention(c["qb"], c["kb"], c["vb"], c["pt"], c["kv"], c["cu"], 0.5,
+                               causal=True)
+    np.testing.assert_allclose(a[:4], b[:4], atol=1e-15)
+    assert np.abs(a[4:] - b[4:]).max() > 1e-3
+    # the token at position 4 sees only itself: its output is its value row
+    np.testing.assert_allclose(a[4], c["vlog"][0][4][np.arange(4) // 2], atol=1e-15)
+
+
+def test_local_effective_chunk_rule():
+    """The chunk actually used: the given one, no longer than the longest
+    sequence, cut down to whole pages, and never below one page."""
+    def chunk_of(chunk, P, kv):
+        cu = np.arange(len(kv) + 1)
+        pt = np.zeros((len(kv), max(1, -(-max(kv) // P))), dtype=np.int32)
+        return oracle.local_virtual_batches(chunk, P, cu, kv, pt)["chunk"]
+    assert chunk_of(8192, 16, [100, 3000, 9000]) == 8192
+    assert chunk_of(8192, 16, [100, 3000]) == 2992      # longest, whole pages
+    assert chunk_of(32, 4, [17, 2]) == 16
+    assert chunk_of(6, 4, [40]) == 4                     # whole pages
+    assert chunk_of(3, 4, [40]) == 4                     # at least a page
+    assert chunk_of(8, 4, [2]) == 4
+
+
+def test_local_single_chunk_reproduces_the_input():
+    """When the chunk covers every sequence, each request is one virtual
+    batch with its own lengths and its own table row."""
+    q_lens, kv = [3, 1, 16], [5, 9, 16]
+    cu = np.concatenate([[0], np.cumsum(q_lens)])
+    pt = np.arange(3 * 4, dtype=np.int32).reshape(3, 4) + 50
+    out = oracle.local_virtual_batches(64, 4, cu, kv, pt)
+    assert out["chunk"] == 16 and out["num_virtual"] == 3
+    assert list(out["seqlens_q_local"]) == q_lens
+    assert list(out["seqlens_k_local"]) == kv
+    assert list(out["cu_seqlens_q_local"]) == list(cu)
+    assert np.array_equal(out["block_table_local"], pt)
+
+
+def test_local_padding_idle_and_malformed_requests():
+    """Rows past the count up to the capacity are padding (lengths 0, the
+    running sum repeated, table row 0); a request with no new tokens makes
+    no virtual batch; one with fewer keys than new tokens makes none and is
+    counted; a table narrower than needed is rejected."""
+    cu = np.array([0, 2, 2, 7, 9])        # request 1 idle
+    kv = np.array([5, 4, 12, 1])          # request 3 malformed (kv < q)
+    pt = np.arange(4 * 3, dtype=np.int32).reshape(4, 3) + 7
+    out = oracle.local_virtual_batches(4, 2, cu, kv, pt, capacity=8, bt_cols=3)
+    assert out["bad"] == 1 and out["chunk"] == 4
+    n = out["num_virtual"]
+    # request 0: positions 3, 4 (chunks 0, 1); request 2: positions 7..11
+    # (chunks 1, 2)
+    assert n == 2 + 2
+    assert list(out["seqlens_q_local"][:n]) == [1, 1, 1, 4]
+    assert list(out["seqlens_k_local"][:n]) == [4, 1, 4, 4]
+    assert np.all(out["seqlens_q_local"][n:] == 0) and np.all(out["seqlens_k_local"][n:] == 0)
+    assert np.all(out["cu_seqlens_q_local"][n:] == out["cu_seqlens_q_local"][n])
+    assert np.all(out["block_table_local"][n:] == 0)
+    assert np.all(out["block_table_local"][:n, 2] == 0)   # columns past C / P
+    assert list(out["block_table_local"][0, :2]) == [pt[0, 0], pt[0, 1]]
+    # request 0's second chunk is keys [4, 8): pages 2 and 3 of a 3-column
+    # row -> the column past the row repeats its last entry
+    assert list(out["block_table_local"][1, :2]) == [pt[0, 2], pt[0, 2]]
+    with pytest.raises(ValueError):
+        oracle.local_virtual_batches(8, 2, cu, kv, pt, capacity=8, bt_cols=3)
