@@ -60,7 +60,9 @@ enum pkv_error_bits {
   PKV_EFLAG_ROW_TOO_SHORT = 4, /* page-table / dst row narrower than needed */
   PKV_EFLAG_SRC_OOB = 8,     /* req_to_token column or pool row out of range */
   PKV_EFLAG_TIMEOUT = 16,    /* a bounded in-kernel wait expired (work dropped) */
-  PKV_EFLAG_LAYOUT = 32      /* shared memory not aligned as a kernel needs (work dropped) */
+  PKV_EFLAG_LAYOUT = 32,     /* shared memory not aligned as a kernel needs (work dropped) */
+  PKV_EFLAG_BAD_LENGTHS = 64, /* a request with q_len < 0 or kv_len < q_len */
+  PKV_EFLAG_CAPACITY = 128   /* an output with fewer rows than the result needs */
 };
 
 typedef struct pkv_tensor {
@@ -263,6 +265,62 @@ int pkv_strided_page_table(pkv_tensor req_to_token,
 int pkv_topk_to_slots(pkv_tensor topk, pkv_tensor cu_seqlens_q,
                       pkv_tensor page_table, pkv_tensor cache_seqlens,
                       int page_size, pkv_tensor out, cudaStream_t stream);
+
+/*
+ * pkv_make_local_attention_virtual_batches -- local (chunked) attention as
+ * virtual batches.
+ *
+ * Defined by `make_local_attention_virtual_batches` in
+ * flashattention_backend.py (its docstring, steps and worked example), where
+ * local attention lets a query token see only the keys of its own
+ * attn_chunk_size-long chunk, up to itself.  Each request's new tokens are
+ * cut at chunk boundaries; every piece becomes one "virtual" request whose
+ * keys are its chunk's keys up to its last token, so that a plain causal
+ * pkv_attn_with_kvcache call over the virtual requests computes local
+ * attention.  With B requests, q = cu_seqlens_q[b+1] - cu_seqlens_q[b] and
+ * kv = seq_lens[b]:
+ *   C      = min(attn_chunk_size, max_b kv) rounded down to a multiple of
+ *            page_size, and at least page_size (the effective chunk);
+ *   first  = min(C - (kv - q) % C, q) new tokens in the first chunk;
+ *   last_k = kv - C * ((kv - 1) / C) keys in the chunk of the last key;
+ *   blocks = 1 + ceil((q - first) / C) virtual requests, a = 0 .. blocks-1,
+ *            r = blocks - 1 - a:
+ *   seqlens_q_local = first (a = 0), else min(q - first - C (a - 1), C);
+ *   seqlens_k_local = last_k (r = 0), else C;
+ *   block_table_local row = page_table[b][min(s / page_size + j, W - 1)] for
+ *            j < C / page_size, s = kv - last_k - r C the chunk's first key
+ *            (W = page_table.shape[1]; columns past the row repeat its last
+ *            entry, they lie past the virtual request's keys);
+ *   cu_seqlens_q_local = cu_seqlens_q[0], then the running sum of
+ *            seqlens_q_local.
+ * Virtual requests are numbered request by request, so the query rows keep
+ * their order and the attention output needs no reordering.  A request with
+ * q = 0 makes none.  A request with q < 0 makes none; one with kv < q has its
+ * tokens cut from its first token into pieces of at most C with
+ * seqlens_k_local = 0 and table rows of 0 (attention gives them out = 0,
+ * lse = -inf); both set PKV_EFLAG_BAD_LENGTHS.
+ *
+ * cu_seqlens_q  int32 [B + 1].   seq_lens int32 [B] (B <= 16384).
+ * page_table    int32 [B, W], W >= 1, last dim contiguous.
+ * attn_chunk_size >= 1, page_size >= 1.
+ * Outputs, sized for a capacity V chosen by the caller (no more than
+ * min(total_q, B * (1 + ceil((max_q - 1) / page_size))) rows are needed):
+ * seqlens_q_local int32 [V]; cu_seqlens_q_local int32 [V + 1];
+ * seqlens_k_local int32 [V]; block_table_local int32 [V, Wl] with
+ * Wl >= max(attn_chunk_size / page_size, 1), last dim contiguous;
+ * info int32 [4] = {virtual requests, C, max seqlens_q_local,
+ * max seqlens_k_local}.
+ * Rows past the count are padding: lengths 0, cu repeats the total, table
+ * row 0; table columns at or past C / page_size are 0.  If the count
+ * exceeds V only V rows are written, info[0] still holds the count and
+ * PKV_EFLAG_CAPACITY is set.  Every output entry is written, on the device;
+ * the host reads nothing back.
+ */
+int pkv_make_local_attention_virtual_batches(
+    int attn_chunk_size, int page_size, pkv_tensor cu_seqlens_q,
+    pkv_tensor seq_lens, pkv_tensor page_table, pkv_tensor seqlens_q_local,
+    pkv_tensor cu_seqlens_q_local, pkv_tensor seqlens_k_local,
+    pkv_tensor block_table_local, pkv_tensor info, cudaStream_t stream);
 
 /* ------------------------------------------------------------ errors */
 

@@ -130,19 +130,23 @@ int orc_local_virtual_batches(int attn_chunk_size, int page_size,
 
   int bad = 0;
   int64_t v = 0;            /* virtual batches so far */
-  int32_t cu = batch > 0 ? cu_seqlens_q[0] : 0;
+  int32_t cu = cu_seqlens_q[0];
   int32_t max_q_local = 0, max_k_local = 0;
   cu_seqlens_q_local[0] = cu;
   for (int b = 0; b < batch; ++b) {
     int32_t q = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
     int32_t kv = seq_lens[b];
     if (q == 0) continue;
-    if (q < 0 || kv < q) { ++bad; continue; }
+    if (q < 0) { ++bad; continue; }
+    /* more new tokens than keys: counted; its tokens are cut into chunks
+       from the first one and given no keys */
+    const int malformed = kv < q;
+    if (malformed) ++bad;
     /* 2. new tokens in the chunk of the first new token; keys in the chunk
           of the last key; number of chunks the new tokens touch */
-    int32_t first = C - (kv - q) % C;
+    int32_t first = malformed ? C : C - (kv - q) % C;
     if (first > q) first = q;
-    int32_t last_k = kv - C * ((kv - 1) / C);
+    int32_t last_k = malformed ? 0 : kv - C * ((kv - 1) / C);
     int32_t blocks = 1 + (q - first + C - 1) / C;
     /* 3. one virtual batch per chunk */
     for (int32_t a = 0; a < blocks; ++a, ++v) {
@@ -154,7 +158,7 @@ int orc_local_virtual_batches(int attn_chunk_size, int page_size,
         q_local = q - first - C * (a - 1);
         if (q_local > C) q_local = C;
       }
-      int32_t k_local = r == 0 ? last_k : C;
+      int32_t k_local = malformed ? 0 : (r == 0 ? last_k : C);
       int64_t k_start = (int64_t)kv - last_k - (int64_t)r * C;
       if (q_local > max_q_local) max_q_local = q_local;
       if (k_local > max_k_local) max_k_local = k_local;
@@ -166,7 +170,7 @@ int orc_local_virtual_batches(int attn_chunk_size, int page_size,
       /* 5. the pages that hold the chunk's keys */
       int32_t *row = block_table_local + v * bt_stride;
       for (int j = 0; j < bt_cols; ++j) {
-        if (j < pages_per_local_batch) {
+        if (j < pages_per_local_batch && !malformed) {
           int64_t col = k_start / page_size + j;
           if (col > pt_cols - 1) col = pt_cols - 1;
           row[j] = page_table[(int64_t)b * pt_stride + col];

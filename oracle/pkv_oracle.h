@@ -88,7 +88,10 @@ int orc_topk_to_slots(const int32_t *topk, int64_t topk_stride, int n_rows,
  *      virtual batch's keys, page_table[b][min(start / page_size + j,
  *      pt_cols - 1)] (a column past the row repeats its last entry).
  * Virtual batches are numbered request by request.  A request with q = 0
- * makes none; one with q < 0 or kv < q makes none and is counted.  Rows at
+ * makes none; one with q < 0 makes none and is counted; one with kv < q is
+ * counted and its tokens are cut into chunks from the first one (first =
+ * min(C, q)) with k_local = 0 and a table row of 0 (attention then gives
+ * those tokens the empty-key result).  Rows at
  * or past the count, up to `capacity`, are padding: q_local = k_local = 0,
  * cu repeats the total, table row all 0; table columns at or past
  * C / page_size are 0.  info = {virtual batches, C, max q_local,

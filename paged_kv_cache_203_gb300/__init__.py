@@ -19,6 +19,11 @@ Entry points (names as in the C ABI, without the ``pkv_`` prefix):
 * ``strided_page_table`` -- token-level to page-level table.
 * ``topk_to_slots`` -- top-k logical positions to KV slots
   (``TopkTransformMethod.PAGED``).
+* ``make_local_attention_virtual_batches`` -- local (chunked) attention cut
+  into virtual requests (``make_local_attention_virtual_batches``), built on
+  the device; ``local_attn_with_kvcache`` runs it and the attention.
+* ``cascade_attn_with_kvcache`` -- shared-prefix attention as two calls and
+  a state merge (``use_cascade_attn``).
 """
 from __future__ import annotations
 
@@ -39,6 +44,9 @@ __all__ = [
     "build_swa_page_table",
     "strided_page_table",
     "topk_to_slots",
+    "make_local_attention_virtual_batches",
+    "local_virtual_batch_capacity",
+    "local_attn_with_kvcache",
     "get_error_flags",
     "clear_error_flags",
     "load_library",
@@ -51,6 +59,8 @@ __all__ = [
     "EFLAG_SRC_OOB",
     "EFLAG_TIMEOUT",
     "EFLAG_LAYOUT",
+    "EFLAG_BAD_LENGTHS",
+    "EFLAG_CAPACITY",
 ]
 
 # dtype codes and status codes of include/pkv.h
@@ -60,6 +70,8 @@ _STATUS = {0: "PKV_OK", -1: "PKV_ERR_INVALID_ARG", -2: "PKV_ERR_UNSUPPORTED",
 EFLAG_PAGE_OOB, EFLAG_TOPK_OOB, EFLAG_ROW_TOO_SHORT, EFLAG_SRC_OOB = 1, 2, 4, 8
 EFLAG_TIMEOUT = 16
 EFLAG_LAYOUT = 32
+EFLAG_BAD_LENGTHS = 64
+EFLAG_CAPACITY = 128
 
 EXPORTED_SYMBOLS = (
     "pkv_attn_with_kvcache",
@@ -72,6 +84,7 @@ EXPORTED_SYMBOLS = (
     "pkv_clear_error_flags",
     "pkv_version",
     "pkv_attn_with_kvcache_noalloc",
+    "pkv_make_local_attention_virtual_batches",
 )
 
 _DTYPES = {torch.bfloat16: _BF16, torch.float32: _F32, torch.int32: _I32,
@@ -123,6 +136,8 @@ def load_library(path: str | None = None):
     lib.pkv_build_swa_page_table.argtypes = [T, T, T, T, c_int, T, T, c_void_p]
     lib.pkv_strided_page_table.argtypes = [T, T, c_int, T, c_void_p]
     lib.pkv_topk_to_slots.argtypes = [T, T, T, T, c_int, T, c_void_p]
+    lib.pkv_make_local_attention_virtual_batches.argtypes = [
+        c_int, c_int, T, T, T, T, T, T, T, T, c_void_p]
     lib.pkv_get_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.pkv_clear_error_flags.argtypes = []
     lib.pkv_version.argtypes = []
@@ -293,6 +308,68 @@ def topk_to_slots(topk, cu_seqlens_q, page_table, cache_seqlens,
         _desc(topk), _desc(cu_seqlens_q), _desc(page_table),
         _desc(cache_seqlens), int(page_size), _desc(out), _stream(topk)))
     return out
+
+
+def local_virtual_batch_capacity(batch: int, total_q: int, max_seqlen_q: int,
+                                 page_size: int) -> int:
+    """Rows that always hold the virtual requests of a batch: each request
+    makes at most one per new token, and at most 1 + ceil((q - 1) / C) with
+    the effective chunk C >= page_size."""
+    per_request = 1 + max(0, -(-(int(max_seqlen_q) - 1) // int(page_size)))
+    return max(0, min(int(total_q), int(batch) * per_request))
+
+
+def make_local_attention_virtual_batches(attn_chunk_size: int, page_size: int,
+                                         cu_seqlens_q, seq_lens, page_table,
+                                         capacity: int, out=None):
+    """Local (chunked) attention as virtual requests, built on the device
+    (include/pkv.h, pkv_make_local_attention_virtual_batches).
+
+    Returns ``(seqlens_q_local [V], cu_seqlens_q_local [V + 1],
+    seqlens_k_local [V], block_table_local [V, Wl], info [4])`` int32 device
+    tensors, V = ``capacity``, Wl = max(attn_chunk_size // page_size, 1);
+    ``info`` = (virtual requests, effective chunk, max local q, max local k).
+    ``out`` may pass those five tensors to be written in place."""
+    dev = cu_seqlens_q.device
+    cap = int(capacity)
+    if out is None:
+        wl = max(int(attn_chunk_size) // int(page_size), 1)
+        out = (torch.empty(cap, dtype=torch.int32, device=dev),
+               torch.empty(cap + 1, dtype=torch.int32, device=dev),
+               torch.empty(cap, dtype=torch.int32, device=dev),
+               torch.empty(cap, wl, dtype=torch.int32, device=dev),
+               torch.empty(4, dtype=torch.int32, device=dev))
+    sq, cuq, sk, bt, info = out
+    _check("pkv_make_local_attention_virtual_batches",
+           load_library().pkv_make_local_attention_virtual_batches(
+               int(attn_chunk_size), int(page_size), _desc(cu_seqlens_q), _desc(seq_lens),
+               _desc(page_table), _desc(sq), _desc(cuq), _desc(sk), _desc(bt), _desc(info),
+               _stream(cu_seqlens_q)))
+    return out
+
+
+def local_attn_with_kvcache(q, k_cache, v_cache, page_table, cache_seqlens,
+                            cu_seqlens_q, max_seqlen_q: int, attn_chunk_size: int,
+                            softmax_scale: float, num_splits: int = 0, out=None,
+                            lse=None, return_softmax_lse: bool = False):
+    """Local (chunked) causal attention, as the FlashAttention backend runs
+    it (flashattention_backend.py, `use_local_attn`): the batch is cut into
+    virtual requests on the device, then one causal attention call runs over
+    them (their query offsets, key lengths and local page table).  The
+    virtual requests keep the query rows in order, so ``out`` / ``lse`` are
+    indexed like ``q``.  No host synchronisation."""
+    page_size = k_cache.shape[1]
+    cap = local_virtual_batch_capacity(cache_seqlens.shape[0], q.shape[0], max_seqlen_q,
+                                       page_size)
+    _, cu_local, k_local, bt_local, _ = make_local_attention_virtual_batches(
+        attn_chunk_size, page_size, cu_seqlens_q, cache_seqlens, page_table, cap)
+    # a virtual request holds at most one effective chunk of new tokens, and
+    # the effective chunk is at most max(whole pages of attn_chunk_size, 1 page)
+    chunk_bound = max((int(attn_chunk_size) // page_size) * page_size, page_size)
+    max_q_local = min(int(max_seqlen_q), chunk_bound)
+    return attn_with_kvcache(q, k_cache, v_cache, bt_local, k_local, cu_local, max_q_local,
+                             softmax_scale, causal=True, num_splits=num_splits, out=out,
+                             lse=lse, return_softmax_lse=return_softmax_lse)
 
 
 def get_error_flags() -> int:

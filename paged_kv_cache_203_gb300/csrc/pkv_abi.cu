@@ -62,6 +62,11 @@ bool has(const pkv_tensor &t, int dtype, int ndim) {
   return t.data != nullptr && t.dtype == dtype && t.ndim == ndim;
 }
 
+// dimension `dim` steps by one element (any stride when it has <= 1 entry)
+bool unit_stride(const pkv_tensor &t, int dim) {
+  return t.shape[dim] <= 1 || t.stride[dim] == 1;
+}
+
 bool aligned16(const void *p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
@@ -470,6 +475,53 @@ int pkv_topk_to_slots(pkv_tensor topk, pkv_tensor cu_seqlens_q,
       static_cast<int>(page_table.shape[1]),
       static_cast<const int32_t *>(cache_seqlens.data), page_size,
       static_cast<int32_t *>(out.data), out.stride[0], err, stream);
+}
+
+int pkv_make_local_attention_virtual_batches(
+    int attn_chunk_size, int page_size, pkv_tensor cu_seqlens_q,
+    pkv_tensor seq_lens, pkv_tensor page_table, pkv_tensor seqlens_q_local,
+    pkv_tensor cu_seqlens_q_local, pkv_tensor seqlens_k_local,
+    pkv_tensor block_table_local, pkv_tensor info, cudaStream_t stream) {
+  if (attn_chunk_size < 1 || page_size < 1) return PKV_ERR_INVALID_ARG;
+  if (!has(seq_lens, PKV_I32, 1) || !unit_stride(seq_lens, 0)) return PKV_ERR_INVALID_ARG;
+  const int64_t batch = seq_lens.shape[0];
+  if (!has(cu_seqlens_q, PKV_I32, 1) || cu_seqlens_q.shape[0] != batch + 1 ||
+      !unit_stride(cu_seqlens_q, 0))
+    return PKV_ERR_INVALID_ARG;
+  if (!has(page_table, PKV_I32, 2) || page_table.shape[0] != batch ||
+      page_table.shape[1] < 1 || !unit_stride(page_table, 1))
+    return PKV_ERR_INVALID_ARG;
+  if (!has(seqlens_q_local, PKV_I32, 1) || !unit_stride(seqlens_q_local, 0))
+    return PKV_ERR_INVALID_ARG;
+  const int64_t cap = seqlens_q_local.shape[0];
+  if (!has(cu_seqlens_q_local, PKV_I32, 1) || cu_seqlens_q_local.shape[0] != cap + 1 ||
+      !unit_stride(cu_seqlens_q_local, 0))
+    return PKV_ERR_INVALID_ARG;
+  if (!has(seqlens_k_local, PKV_I32, 1) || seqlens_k_local.shape[0] != cap ||
+      !unit_stride(seqlens_k_local, 0))
+    return PKV_ERR_INVALID_ARG;
+  const int64_t min_cols = attn_chunk_size / page_size > 1 ? attn_chunk_size / page_size : 1;
+  if (!has(block_table_local, PKV_I32, 2) || block_table_local.shape[0] != cap ||
+      block_table_local.shape[1] < min_cols || !unit_stride(block_table_local, 1))
+    return PKV_ERR_INVALID_ARG;
+  if (!has(info, PKV_I32, 1) || info.shape[0] < 4 || !unit_stride(info, 0))
+    return PKV_ERR_INVALID_ARG;
+  if (batch > kLocalBatchesMaxBatch || cap > 0x7fffffffLL ||
+      page_table.shape[1] > 0x7fffffffLL || block_table_local.shape[1] > 0x7fffffffLL)
+    return PKV_ERR_UNSUPPORTED;
+  uint32_t *err = device_error_word();
+  if (err == nullptr) return PKV_ERR_CUDA;
+  return launch_local_virtual_batches(
+      attn_chunk_size, page_size, static_cast<const int32_t *>(cu_seqlens_q.data),
+      static_cast<const int32_t *>(seq_lens.data), static_cast<int>(batch),
+      static_cast<const int32_t *>(page_table.data), page_table.stride[0],
+      static_cast<int>(page_table.shape[1]), static_cast<int>(cap),
+      static_cast<int32_t *>(seqlens_q_local.data),
+      static_cast<int32_t *>(cu_seqlens_q_local.data),
+      static_cast<int32_t *>(seqlens_k_local.data),
+      static_cast<int32_t *>(block_table_local.data), block_table_local.stride[0],
+      static_cast<int>(block_table_local.shape[1]), static_cast<int32_t *>(info.data), err,
+      stream);
 }
 
 }  // extern "C"

@@ -102,6 +102,19 @@ int launch_strided_page_table(const int32_t *rtt, int64_t rtt_stride,
                               int page_size, int32_t *out, int64_t out_stride,
                               int n_cols, uint32_t *err, cudaStream_t stream);
 
+// Largest batch the local-attention virtual batch builder takes (two
+// [batch + 1] int32 arrays in shared memory).
+constexpr int kLocalBatchesMaxBatch = 16384;
+
+int launch_local_virtual_batches(int attn_chunk_size, int page_size,
+                                 const int32_t *cu, const int32_t *seq_lens,
+                                 int batch, const int32_t *pt,
+                                 int64_t pt_stride, int pt_cols, int capacity,
+                                 int32_t *q_local, int32_t *cu_local,
+                                 int32_t *k_local, int32_t *bt,
+                                 int64_t bt_stride, int bt_cols, int32_t *info,
+                                 uint32_t *err, cudaStream_t stream);
+
 int launch_topk_to_slots(const int32_t *topk, int64_t topk_stride,
                          int total_q, int topk_len, const int32_t *cu,
                          int batch, const int32_t *pt, int64_t pt_stride,

@@ -1,6 +1,7 @@
 // pkv_pagetable.cu -- integer metadata kernels: the prefill-aware
-// sliding-window page table, the strided (page-level) table and the top-k
-// index -> KV slot transform.  All integer, bit-exact by construction.
+// sliding-window page table, the strided (page-level) table, the top-k
+// index -> KV slot transform and the local-attention virtual batches.  All
+// integer, bit-exact by construction.
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -121,6 +122,218 @@ topk_to_slots_kernel(const int32_t *__restrict__ topk, int64_t topk_stride,
   if (bad) atomicOr(err, PKV_EFLAG_TOPK_OOB);
 }
 
+
+// ---------------------------------------------------------------------------
+// Local (chunked) attention as virtual batches (flashattention_backend.py,
+// `make_local_attention_virtual_batches`).  The page builds these arrays on
+// the host with numpy; here one launch builds them on the device, so the
+// forward needs no device-to-host copy.  Every CTA scans the whole batch
+// into shared memory (per request: first virtual batch and first query
+// token of the local arrays), then each warp owns output rows: a binary
+// search finds the row's request, the lane-0 writes the three lengths and
+// the warp gathers the row's pages.  Batches are small (<= 16384 requests),
+// so the redundant scan costs less than a second launch would.
+
+constexpr int kLvbThreads = 512;
+constexpr int kLvbWarps = kLvbThreads / 32;
+
+// Per-request quantities of the routine, for effective chunk C.
+struct LvbRequest {
+  int32_t q;       // new tokens (0 when none or negative)
+  int32_t kv;      // keys
+  int32_t first;   // new tokens in the chunk of the first new token
+  int32_t last_k;  // keys in the chunk of the last key
+  int32_t blocks;  // virtual batches of this request
+  bool keyless;    // kv < q: tokens chunked from the first, no keys
+  bool bad;        // q < 0 or kv < q
+};
+
+__device__ __forceinline__ LvbRequest lvb_request(const int32_t *cu,
+                                                  const int32_t *seq_lens,
+                                                  int b, int32_t C) {
+  LvbRequest r;
+  r.q = cu[b + 1] - cu[b];
+  r.kv = seq_lens[b];
+  r.first = r.last_k = r.blocks = 0;
+  r.keyless = false;
+  r.bad = r.q < 0;
+  if (r.q <= 0) {
+    r.q = 0;
+    return r;
+  }
+  r.keyless = r.kv < r.q;
+  r.bad = r.keyless;
+  // kv - q >= 0 on the regular path, so % is the floor remainder
+  r.first = min(r.keyless ? C : C - (r.kv - r.q) % C, r.q);
+  r.last_k = r.keyless ? 0 : r.kv - C * ((r.kv - 1) / C);
+  r.blocks = 1 + (r.q - r.first + C - 1) / C;
+  return r;
+}
+
+// Exclusive scan of one int per thread over the CTA; *total gets the sum.
+__device__ __forceinline__ int32_t lvb_block_scan(int32_t x, int32_t *warp_tot,
+                                                  int32_t *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int32_t incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t t = lane < kLvbWarps ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < kLvbWarps) warp_tot[lane] = t;  // inclusive warp prefix
+  }
+  __syncthreads();
+  const int32_t before = warp > 0 ? warp_tot[warp - 1] : 0;
+  *total = warp_tot[kLvbWarps - 1];
+  __syncthreads();  // warp_tot is reused by the next scan
+  return before + incl - x;
+}
+
+__device__ __forceinline__ int32_t lvb_block_max(int32_t x, int32_t *warp_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  x = __reduce_max_sync(0xffffffffu, x);
+  if (lane == 0) warp_tot[warp] = x;
+  __syncthreads();
+  int32_t m = warp_tot[0];
+#pragma unroll
+  for (int w = 1; w < kLvbWarps; ++w) m = max(m, warp_tot[w]);
+  __syncthreads();
+  return m;
+}
+
+__global__ void __launch_bounds__(kLvbThreads)
+local_virtual_batches_kernel(int attn_chunk_size, int page_size,
+                             const int32_t *__restrict__ cu,
+                             const int32_t *__restrict__ seq_lens, int batch,
+                             const int32_t *__restrict__ pt, int64_t pt_stride,
+                             int pt_cols, int capacity,
+                             int32_t *__restrict__ q_local,
+                             int32_t *__restrict__ cu_local,
+                             int32_t *__restrict__ k_local,
+                             int32_t *__restrict__ bt, int64_t bt_stride,
+                             int bt_cols, int32_t *__restrict__ info,
+                             uint32_t *err) {
+  extern __shared__ int32_t lvb_smem[];
+  int32_t *vbase = lvb_smem;              // [batch + 1] first virtual batch
+  int32_t *qbase = lvb_smem + batch + 1;  // [batch + 1] first local token
+  __shared__ int32_t warp_tot[kLvbWarps];
+  const int tid = threadIdx.x;
+
+  // 1. effective chunk: min(chunk, longest sequence), whole pages, >= 1 page
+  int32_t longest = 0;
+  for (int b = tid; b < batch; b += kLvbThreads) longest = max(longest, seq_lens[b]);
+  longest = lvb_block_max(longest, warp_tot);
+  int32_t C = min(attn_chunk_size, longest);
+  C = (C / page_size) * page_size;
+  if (C < page_size) C = page_size;
+  const int pages_per_batch = C / page_size;
+
+  // 2. per-request virtual batch and local token offsets
+  int32_t carry_v = 0, carry_q = 0, max_q = 0, max_k = 0;
+  bool any_bad = false;
+  for (int base = 0; base < batch; base += kLvbThreads) {
+    const int b = base + tid;
+    int32_t nb = 0, nq = 0;
+    if (b < batch) {
+      const LvbRequest r = lvb_request(cu, seq_lens, b, C);
+      nb = r.blocks;
+      nq = r.q;
+      any_bad |= r.bad;
+      if (r.blocks > 0) {
+        // the largest local q is the first block or a full later one; the
+        // largest local k is a full chunk unless there is one block
+        max_q = max(max_q, r.first);
+        if (r.blocks > 1) max_q = max(max_q, min(C, r.q - r.first));
+        max_k = max(max_k, r.keyless ? 0 : (r.blocks > 1 ? C : r.last_k));
+      }
+    }
+    int32_t tot_v, tot_q;
+    const int32_t ev = lvb_block_scan(nb, warp_tot, &tot_v);
+    const int32_t eq = lvb_block_scan(nq, warp_tot, &tot_q);
+    if (b < batch) {
+      vbase[b] = carry_v + ev;
+      qbase[b] = carry_q + eq;
+    }
+    carry_v += tot_v;
+    carry_q += tot_q;
+  }
+  if (tid == 0) {
+    vbase[batch] = carry_v;
+    qbase[batch] = carry_q;
+  }
+  const int32_t n_virtual = carry_v;
+  const int32_t cu0 = cu[0];
+  if (blockIdx.x == 0) {
+    max_q = lvb_block_max(max_q, warp_tot);
+    max_k = lvb_block_max(max_k, warp_tot);
+    const int bad = __syncthreads_or(any_bad);
+    if (tid == 0) {
+      info[0] = n_virtual;
+      info[1] = C;
+      info[2] = max_q;
+      info[3] = max_k;
+      cu_local[0] = cu0;
+      if (bad) atomicOr(err, PKV_EFLAG_BAD_LENGTHS);
+      if (n_virtual > capacity) atomicOr(err, PKV_EFLAG_CAPACITY);
+    }
+  }
+  __syncthreads();
+
+  // 3. one warp per output row
+  const int lane = tid & 31;
+  for (int v = blockIdx.x * kLvbWarps + (tid >> 5); v < capacity;
+       v += gridDim.x * kLvbWarps) {
+    int32_t ql = 0, kl = 0, cul = cu0 + carry_q;
+    int b = 0;
+    int64_t first_page = 0;
+    bool gather = false;
+    if (v < n_virtual) {
+      int lo = 0, hi = batch;  // largest b with vbase[b] <= v
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (vbase[mid] <= v) lo = mid; else hi = mid;
+      }
+      b = lo;
+      const LvbRequest r = lvb_request(cu, seq_lens, b, C);
+      const int32_t a = v - vbase[b];
+      const int32_t rev = r.blocks - 1 - a;
+      ql = a == 0 ? r.first : min(r.q - r.first - C * (a - 1), C);
+      kl = r.keyless ? 0 : (rev == 0 ? r.last_k : C);
+      cul = cu0 + qbase[b] + (a == 0 ? 0 : r.first + C * (a - 1)) + ql;
+      gather = !r.keyless;
+      const int64_t k_start = static_cast<int64_t>(r.kv) - r.last_k -
+                              static_cast<int64_t>(rev) * C;
+      first_page = k_start / page_size;
+    }
+    if (lane == 0) {
+      q_local[v] = ql;
+      cu_local[v + 1] = cul;
+      k_local[v] = kl;
+    }
+    const int32_t *src = pt + static_cast<int64_t>(b) * pt_stride;
+    int32_t *row = bt + static_cast<int64_t>(v) * bt_stride;
+    for (int j = lane; j < bt_cols; j += 32) {
+      int32_t val = 0;
+      if (gather && j < pages_per_batch) {
+        // a column past the row repeats its last entry (never read: it lies
+        // past the batch's keys)
+        const int64_t col = min(first_page + j, static_cast<int64_t>(pt_cols - 1));
+        val = src[col];
+      }
+      row[j] = val;
+    }
+  }
+}
+
 }  // namespace
 
 int launch_swa_page_table(const int32_t *rtt, int64_t rtt_stride,
@@ -160,6 +373,35 @@ int launch_topk_to_slots(const int32_t *topk, int64_t topk_stride,
   topk_to_slots_kernel<<<total_q, 256, 0, stream>>>(
       topk, topk_stride, topk_len, cu, batch, pt, pt_stride, pt_cols,
       cache_seqlens, page_size, out, out_stride, err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int launch_local_virtual_batches(int attn_chunk_size, int page_size,
+                                 const int32_t *cu, const int32_t *seq_lens,
+                                 int batch, const int32_t *pt,
+                                 int64_t pt_stride, int pt_cols, int capacity,
+                                 int32_t *q_local, int32_t *cu_local,
+                                 int32_t *k_local, int32_t *bt,
+                                 int64_t bt_stride, int bt_cols, int32_t *info,
+                                 uint32_t *err, cudaStream_t stream) {
+  if (batch > kLocalBatchesMaxBatch) return PKV_ERR_UNSUPPORTED;
+  const size_t smem = 2 * static_cast<size_t>(batch + 1) * sizeof(int32_t);
+  static bool configured[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev >= 64 || !configured[dev]) {
+    if (cudaFuncSetAttribute(local_virtual_batches_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             2 * (kLocalBatchesMaxBatch + 1) * 4) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    if (dev < 64) configured[dev] = true;
+  }
+  // about one row per warp, at most one CTA per SM
+  int grid = (capacity + kLvbWarps - 1) / kLvbWarps;
+  grid = max(1, min(grid, kNumSMs));
+  local_virtual_batches_kernel<<<grid, kLvbThreads, smem, stream>>>(
+      attn_chunk_size, page_size, cu, seq_lens, batch, pt, pt_stride, pt_cols,
+      capacity, q_local, cu_local, k_local, bt, bt_stride, bt_cols, info, err);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

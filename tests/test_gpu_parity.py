@@ -744,3 +744,134 @@ def test_mla_topk_full_size_sampled():
     check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
                 ref_o, ref_l, "mla full-size sampled")
     assert pkv.get_error_flags() == 0
+
+
+# ------------------------------------------- local (chunked) attention batches
+
+def _lvb_run(chunk, P, cu, kv, pt, cap, bt_cols=None):
+    """GPU build and oracle build of the virtual requests; every output
+    array and the info words must agree bit for bit."""
+    cols = bt_cols if bt_cols is not None else max(chunk // P, 1)
+    cu_t = torch.as_tensor(np.asarray(cu), dtype=torch.int32).to(DEV)
+    kv_t = torch.as_tensor(np.asarray(kv), dtype=torch.int32).to(DEV)
+    pt_t = torch.as_tensor(np.asarray(pt), dtype=torch.int32).to(DEV)
+    # outputs pre-filled with garbage: every entry must be written
+    out = (torch.full((cap,), -7, dtype=torch.int32, device=DEV),
+           torch.full((cap + 1,), -7, dtype=torch.int32, device=DEV),
+           torch.full((cap,), -7, dtype=torch.int32, device=DEV),
+           torch.full((cap, cols), -7, dtype=torch.int32, device=DEV),
+           torch.full((4,), -7, dtype=torch.int32, device=DEV))
+    pkv.make_local_attention_virtual_batches(chunk, P, cu_t, kv_t, pt_t, cap, out=out)
+    torch.cuda.synchronize()
+    sq, cuq, sk, bt, info = (t.cpu().numpy() for t in out)
+    ref = oracle.local_virtual_batches(chunk, P, cu, kv, pt, capacity=cap, bt_cols=cols)
+    assert np.array_equal(sq, ref["seqlens_q_local"])
+    assert np.array_equal(cuq, ref["cu_seqlens_q_local"])
+    assert np.array_equal(sk, ref["seqlens_k_local"])
+    assert np.array_equal(bt, ref["block_table_local"])
+    assert list(info) == [ref["num_virtual"], ref["chunk"], ref["max_q_local"],
+                          ref["max_k_local"]]
+    return ref
+
+
+def _lvb_batch(rng, B, q_hi, kv_extra_hi, P, decode_share=0.0):
+    q = rng.integers(1, q_hi + 1, B)
+    q[rng.random(B) < decode_share] = 1
+    kv = q + rng.integers(0, kv_extra_hi + 1, B)
+    cu = np.concatenate([[0], np.cumsum(q)]).astype(np.int32)
+    width = int(-(-kv.max() // P))
+    pt = rng.integers(0, 1 << 20, (B, width)).astype(np.int32)
+    return cu, kv.astype(np.int32), pt
+
+
+@pytest.mark.parametrize("P", [1, 2, 4])
+def test_local_virtual_batches_printed_example_on_gpu(P):
+    """The printed example (chunk 4, q_seqlens [4, 10, 5], kv [6, 17, 9]) at
+    its exact row count and with padding rows."""
+    cu, kv = [0, 4, 14, 19], [6, 17, 9]
+    pt = np.arange(3 * 17, dtype=np.int32).reshape(3, 17)[:, :-(-17 // P)] * 3 + 1
+    for cap in (8, 13):
+        ref = _lvb_run(4, P, cu, kv, pt, cap)
+        assert list(ref["seqlens_q_local"][:8]) == [2, 2, 1, 4, 4, 1, 4, 1]
+        assert list(ref["seqlens_k_local"][:8]) == [4, 2, 4, 4, 4, 1, 4, 1]
+    assert pkv.get_error_flags() == 0
+
+
+@pytest.mark.parametrize("B,P,chunk,q_hi,kv_hi,decode_share", [
+    (1, 1, 4, 10, 30, 0.0),
+    (37, 16, 256, 700, 5000, 0.3),        # extend and decode mixed
+    (512, 64, 8192, 1, 100000, 1.0),      # decode, long contexts
+    (3000, 16, 1024, 40, 20000, 0.5),     # several scan tiles
+    (16384, 16, 2048, 1, 9000, 1.0),      # largest batch
+    (200, 16, 100, 300, 3000, 0.0),       # chunk not a page multiple -> 96
+    (50, 64, 8192, 100, 2000, 0.0),       # chunk beyond the longest sequence
+    (9, 4, 3, 30, 50, 0.0),               # chunk below a page -> one page
+])
+def test_local_virtual_batches_bit_exact(B, P, chunk, q_hi, kv_hi, decode_share):
+    rng = np.random.default_rng(B * 7 + P + chunk)
+    cu, kv, pt = _lvb_batch(rng, B, q_hi, kv_hi, P, decode_share)
+    cap = pkv.local_virtual_batch_capacity(B, int(cu[-1]), int(np.diff(cu).max()), P)
+    ref = _lvb_run(chunk, P, cu, kv, pt, cap)
+    assert ref["num_virtual"] <= cap
+    assert pkv.get_error_flags() == 0
+
+
+def test_local_virtual_batches_edge_cases():
+    """Empty batch; idle requests; a wider table than needed; a request
+    with more new tokens than keys (flagged, key-less rows); a capacity
+    below the count (flagged, rows up to the capacity)."""
+    pt1 = np.zeros((0, 1), dtype=np.int32)
+    _lvb_run(16, 4, [5], np.zeros(0, np.int32), pt1, 3)
+    assert pkv.get_error_flags() == 0
+    cu = np.array([0, 0, 9, 9, 20], dtype=np.int32)
+    kv = np.array([4, 40, 0, 11], dtype=np.int32)
+    pt = (np.arange(4 * 10, dtype=np.int32).reshape(4, 10) * 5) + 2
+    _lvb_run(8, 4, cu, kv, pt, 12, bt_cols=5)
+    assert pkv.get_error_flags() == 0
+    kv_bad = kv.copy()
+    kv_bad[3] = 6                                   # 11 new tokens, 6 keys
+    ref = _lvb_run(8, 4, cu, kv_bad, pt, 12)
+    assert ref["bad"] == 1
+    assert pkv.get_error_flags() == pkv.EFLAG_BAD_LENGTHS
+    pkv.clear_error_flags()
+    ref = _lvb_run(4, 4, cu, kv, pt, 3)
+    assert ref["num_virtual"] > 3
+    assert pkv.get_error_flags() == pkv.EFLAG_CAPACITY
+
+
+def _local_check(wl, chunk, num_splits=0):
+    g = wl.to(DEV)
+    out, lse = pkv.local_attn_with_kvcache(
+        g.q, g.k_cache, g.v_cache, g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+        g.max_seqlen_q, chunk, g.scale, num_splits=num_splits, return_softmax_lse=True)
+    torch.cuda.synchronize()
+    P = wl.k_cache.shape[1]
+    eff = oracle.local_virtual_batches(chunk, P, wl.cu_seqlens_q.numpy(),
+                                       wl.cache_seqlens.numpy(), wl.page_table.numpy())["chunk"]
+    ref_o, ref_l, _ = oracle_attn(wl, causal=True, window_left=-1, attn_chunk=eff)
+    check_close(out, lse, ref_o, ref_l, f"local chunk={chunk} (effective {eff})")
+    assert pkv.get_error_flags() == 0
+    return eff
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_local_attention_decode(num_splits):
+    """Local attention on a GQA decode batch (32/8 heads, D 128, P 16):
+    each token sees only its own 512-key chunk."""
+    wl = workloads.make("tiny_decode", d=128, page_size=16, h_q=32, h_kv=8, batch=48,
+                        len_lo=1, len_hi=3000, pool_tokens=48 * 3008 + 64, seed=61)
+    assert _local_check(wl, 512, num_splits) == 512
+
+
+@pytest.mark.parametrize("page_size,chunk", [(64, 256), (16, 192), (64, 8192)])
+def test_local_attention_extend(page_size, chunk):
+    """Local attention on the varlen extend recipe, reduced (4 requests, new
+    U[64, 700] on a prefix U[0, 900]): requests cut into several virtual
+    requests of up to one chunk; a chunk beyond the longest sequence takes
+    the longest sequence's whole pages."""
+    wl = workloads.make("varlen_extend", batch=4, new_lo=64, new_hi=700, prefix_lo=0,
+                        prefix_hi=900, page_size=page_size,
+                        pool_pages=4 * (1600 // page_size + 2) + 8, seed=62)
+    eff = _local_check(wl, chunk)
+    if chunk < 1000:
+        assert eff == chunk

@@ -668,19 +668,25 @@ def test_local_single_chunk_reproduces_the_input():
 def test_local_padding_idle_and_malformed_requests():
     """Rows past the count up to the capacity are padding (lengths 0, the
     running sum repeated, table row 0); a request with no new tokens makes
-    no virtual batch; one with fewer keys than new tokens makes none and is
-    counted; a table narrower than needed is rejected."""
-    cu = np.array([0, 2, 2, 7, 9])        # request 1 idle
-    kv = np.array([5, 4, 12, 1])          # request 3 malformed (kv < q)
-    pt = np.arange(4 * 3, dtype=np.int32).reshape(4, 3) + 7
-    out = oracle.local_virtual_batches(4, 2, cu, kv, pt, capacity=8, bt_cols=3)
+    no virtual batch; one with fewer keys than new tokens is counted and its
+    tokens get key-less virtual batches of at most a chunk each, so later
+    batches still address their own query rows; a table narrower than
+    needed is rejected."""
+    cu = np.array([0, 2, 2, 7, 13, 15])   # request 1 idle
+    kv = np.array([5, 4, 12, 1, 3])       # request 3 malformed (kv < q)
+    pt = np.arange(5 * 3, dtype=np.int32).reshape(5, 3) + 7
+    out = oracle.local_virtual_batches(4, 2, cu, kv, pt, capacity=10, bt_cols=3)
     assert out["bad"] == 1 and out["chunk"] == 4
     n = out["num_virtual"]
     # request 0: positions 3, 4 (chunks 0, 1); request 2: positions 7..11
-    # (chunks 1, 2)
-    assert n == 2 + 2
-    assert list(out["seqlens_q_local"][:n]) == [1, 1, 1, 4]
-    assert list(out["seqlens_k_local"][:n]) == [4, 1, 4, 4]
+    # (chunks 1, 2); request 3: 6 tokens, no keys, chunks of 4 and 2;
+    # request 4: positions 1, 2 (chunk 0)
+    assert n == 2 + 2 + 2 + 1
+    assert list(out["seqlens_q_local"][:n]) == [1, 1, 1, 4, 4, 2, 2]
+    assert list(out["seqlens_k_local"][:n]) == [4, 1, 4, 4, 0, 0, 3]
+    assert list(out["cu_seqlens_q_local"][:n + 1]) == [0, 1, 2, 3, 7, 11, 13, 15]
+    assert np.all(out["block_table_local"][4:6] == 0)
+    assert out["max_q_local"] == 4 and out["max_k_local"] == 4
     assert np.all(out["seqlens_q_local"][n:] == 0) and np.all(out["seqlens_k_local"][n:] == 0)
     assert np.all(out["cu_seqlens_q_local"][n:] == out["cu_seqlens_q_local"][n])
     assert np.all(out["block_table_local"][n:] == 0)
