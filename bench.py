@@ -249,6 +249,139 @@ class Step:
         return "decode_gqa_kernel"
 
 
+def _event_ms(fn, reps: int = 20) -> float:
+    """Mean device time of ``fn`` (launches on the current stream)."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def local_attention_line(dev, peaks, chunk: int = 2048):
+    """Local (chunked) attention on the headline decode batch: the device
+    builder of the virtual requests, then one causal call over them.  The
+    algorithmic K/V bytes are the keys each request's new tokens can see:
+    from the start of the first new token's chunk to the last key."""
+    g = workloads.make(HEADLINE, value_device=dev)
+    P = g.page_size
+    B = g.cache_seqlens.shape[0]
+    max_q = g.max_seqlen_q
+    cap = pkv.local_virtual_batch_capacity(B, g.q.shape[0], max_q, P)
+    bufs = pkv.make_local_attention_virtual_batches(chunk, P, g.cu_seqlens_q, g.cache_seqlens,
+                                                    g.page_table, cap)
+    max_q_local = min(max_q, max((chunk // P) * P, P))
+    out = torch.empty(g.q.shape[0], g.q.shape[1], g.v_cache.shape[-1], dtype=torch.bfloat16,
+                      device=dev)
+    lse = torch.empty(g.q.shape[0], g.q.shape[1], dtype=torch.float32, device=dev)
+    ws_n = pkv.attn_workspace_size(g.q, g.k_cache, g.v_cache, bufs[3], bufs[2], max_q_local)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=dev)
+
+    def build():
+        pkv.make_local_attention_virtual_batches(chunk, P, g.cu_seqlens_q, g.cache_seqlens,
+                                                 g.page_table, cap, out=bufs)
+
+    def attend():
+        pkv.attn_with_kvcache(g.q, g.k_cache, g.v_cache, bufs[3], bufs[2], bufs[1],
+                              max_q_local, g.scale, causal=True, out=out, lse=lse,
+                              workspace=ws)
+
+    def step():
+        build()
+        attend()
+
+    kv = g.cache_seqlens.cpu().numpy().astype(np.int64)
+    ql = np.diff(g.cu_seqlens_q.cpu().numpy()).astype(np.int64)
+    eff = min(chunk, int(kv.max())) // P * P
+    eff = max(eff, P)
+    keys = int((kv - eff * ((kv - ql) // eff)).sum())
+    h_kv, d, dv = g.k_cache.shape[2], g.q.shape[-1], g.v_cache.shape[-1]
+    kv_bytes = keys * h_kv * (d + dv) * 2
+    b_ms, a_ms, s_ms = _event_ms(build), _event_ms(attend), _event_ms(step)
+    return {"kernel": "local_virtual_batches_kernel + attention", "chunk": chunk,
+            "effective_chunk": eff, "virtual_requests_capacity": cap,
+            "builder_ms": b_ms, "attn_ms": a_ms, "ms_per_step": s_ms,
+            "kv_GBps": kv_bytes / 1e9 / (a_ms / 1e3),
+            "kv_frac_hbm": kv_bytes / 1e9 / (a_ms / 1e3) / peaks["hbm_gbs"],
+            "tokens_per_s": g.q.shape[0] / (s_ms / 1e3)}
+
+
+def cascade_line(dev, peaks, prefix_tokens: int = 4096):
+    """Cascade attention on the headline decode batch with a shared
+    prefix: every request also sees the same prefix_tokens keys (one set of
+    pages), then its own keys; prefix call + suffix call + state merge.
+    ``kv_GBps_logical`` counts the prefix once per request, ``kv_GBps_unique``
+    once per step (the rest is served by L2)."""
+    g = workloads.make(HEADLINE, value_device=dev)
+    P = g.page_size
+    B = g.cache_seqlens.shape[0]
+    n_pre = prefix_tokens // P
+    pre_pt = torch.arange(n_pre, dtype=torch.int32, device=dev).repeat(B, 1).contiguous()
+    pre_len = torch.full((B,), prefix_tokens, dtype=torch.int32, device=dev)
+    out = torch.empty(g.q.shape[0], g.q.shape[1], g.v_cache.shape[-1], dtype=torch.bfloat16,
+                      device=dev)
+    lse = torch.empty(g.q.shape[0], g.q.shape[1], dtype=torch.float32, device=dev)
+
+    def step():
+        pkv.cascade_attn_with_kvcache(g.q, g.k_cache, g.v_cache, pre_pt, pre_len,
+                                      g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+                                      g.max_seqlen_q, g.scale, causal=True, out=out, lse=lse)
+
+    s_ms = _event_ms(step)
+    h_kv, d, dv = g.k_cache.shape[2], g.q.shape[-1], g.v_cache.shape[-1]
+    row = h_kv * (d + dv) * 2
+    own = int(g.cache_seqlens.sum())
+    logical = (own + B * prefix_tokens) * row
+    unique = (own + prefix_tokens) * row
+    return {"kernel": "2 x attention + merge_state_kernel", "prefix_tokens": prefix_tokens,
+            "ms_per_step": s_ms,
+            "kv_GBps_logical": logical / 1e9 / (s_ms / 1e3),
+            "kv_GBps_unique": unique / 1e9 / (s_ms / 1e3),
+            "unique_frac_hbm": unique / 1e9 / (s_ms / 1e3) / peaks["hbm_gbs"],
+            "tokens_per_s": g.q.shape[0] / (s_ms / 1e3)}
+
+
+def append_line(dev, peaks):
+    """The KV write before attention on the varlen extend workload: every
+    new token's K/V rows (8 heads x 128 x 2) stored to its slot, then the
+    causal extend attention over the updated pool.  The write moves each new
+    row twice (read + write)."""
+    g = workloads.make("varlen_extend", value_device=dev)
+    P = g.page_size
+    cu = g.cu_seqlens_q.cpu().numpy()
+    kv = g.cache_seqlens.cpu().numpy()
+    pt = g.page_table.cpu().numpy()
+    loc = np.concatenate([pt[b, np.arange(kv[b] - (cu[b + 1] - cu[b]), kv[b]) // P] * P +
+                          np.arange(kv[b] - (cu[b + 1] - cu[b]), kv[b]) % P
+                          for b in range(len(kv))])
+    loc = torch.from_numpy(loc.astype(np.int64)).to(dev)
+    k_new = g.k_cache.view(-1, *g.k_cache.shape[2:])[loc].clone()
+    v_new = g.v_cache.view(-1, *g.v_cache.shape[2:])[loc].clone()
+    out = torch.empty(g.q.shape[0], g.q.shape[1], g.v_cache.shape[-1], dtype=torch.bfloat16,
+                      device=dev)
+
+    def write():
+        pkv.set_kv_buffer(g.k_cache, g.v_cache, loc, k_new, v_new)
+
+    def step():
+        pkv.append_attn_with_kvcache(g.q, k_new, v_new, loc, g.k_cache, g.v_cache,
+                                     g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+                                     g.max_seqlen_q, g.scale, causal=True, out=out)
+
+    w_ms, s_ms = _event_ms(write), _event_ms(step)
+    moved = 2 * (k_new.numel() + v_new.numel()) * 2
+    return {"kernel": "set_kv_buffer_kernel (+ extend_tc_kernel)", "new_tokens": int(loc.numel()),
+            "write_ms": w_ms, "write_GBps": moved / 1e9 / (w_ms / 1e3),
+            "write_frac_hbm": moved / 1e9 / (w_ms / 1e3) / peaks["hbm_gbs"],
+            "ms_per_step": s_ms, "tokens_per_s": g.q.shape[0] / (s_ms / 1e3)}
+
+
 def parse_overrides(s: str | None) -> dict:
     out = {}
     if not s:
@@ -551,6 +684,14 @@ def main():
                 torch.cuda.empty_cache()
             except pkv.PkvError as e:
                 others[label] = {"unavailable": str(e)}
+        for label, fn in ((HEADLINE + "@local_chunk_2048", local_attention_line),
+                          (HEADLINE + "@cascade_shared_prefix_4096", cascade_line),
+                          ("varlen_extend@append_then_attend", append_line)):
+            try:
+                others[label] = fn(dev, peaks)
+            except pkv.PkvError as e:
+                others[label] = {"unavailable": str(e)}
+            torch.cuda.empty_cache()
 
     if rank == 0:
         g_cfg = {"workload": args.workload}

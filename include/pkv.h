@@ -267,6 +267,36 @@ int pkv_topk_to_slots(pkv_tensor topk, pkv_tensor cu_seqlens_q,
                       int page_size, pkv_tensor out, cudaStream_t stream);
 
 /*
+ * pkv_set_kv_buffer -- store the new tokens' K/V rows into the paged pool.
+ *
+ * Defined by the KV write that precedes attention in
+ * flashattention_backend.py (`forward_extend` / `forward_decode`:
+ * `token_to_kv_pool.set_kv_buffer(layer, cache_loc, k, v, ...)` with
+ * `cache_loc = forward_batch.out_cache_loc`; for MLA
+ * `set_mla_kv_buffer(layer, cache_loc, k, k_rope)`).  For every new token t
+ * and head h, with slot s = loc[t] = page * P + position (P =
+ * k_cache.shape[1]):
+ *   k_cache[s / P][s % P][h][:] = k[t][h][:],
+ *   v_cache[s / P][s % P][h][:] = v[t][h][:]   (when v is given).
+ * For absorbed MLA pass k = the nope part [T, 1, 512], v = the rope part
+ * [T, 1, 64], k_cache = the first 512 columns of the 576-wide latent pool and
+ * v_cache = its last 64 columns (two views of one buffer).
+ *
+ * loc      int32 or int64 [T] slot ids, distinct (with a repeated slot the
+ *          stored row is one of the candidates, unspecified which).
+ * k        bf16 [T, H, dk];  v optional bf16 [T, H, dv] (absent: K only).
+ * k_cache  bf16 [num_pages, P, H, dk];  v_cache bf16 [num_pages, P, H, dv]
+ *          (same num_pages and P), present iff v is.
+ * Last dimensions contiguous, rows 16-byte aligned, dk and dv multiples of 8
+ * (PKV_ERR_UNSUPPORTED otherwise).  A slot outside [0, num_pages * P) is
+ * skipped and sets PKV_EFLAG_PAGE_OOB.  No value is converted: the rows are
+ * copied bit for bit.
+ */
+int pkv_set_kv_buffer(pkv_tensor loc, pkv_tensor k, pkv_tensor v,
+                      pkv_tensor k_cache, pkv_tensor v_cache,
+                      cudaStream_t stream);
+
+/*
  * pkv_make_local_attention_virtual_batches -- local (chunked) attention as
  * virtual batches.
  *

@@ -11,6 +11,9 @@ Every function restates a definition from the SGLang attention-backend pages:
   ("Convert the page table to a strided format").
 * ``swa_page_table`` -- flashattention_backend.py, ``_build_pa_page_table_kernel``.
 * ``topk_to_slots`` -- nsa_backend.py, ``TopkTransformMethod.PAGED``.
+* ``set_kv_buffer`` -- flashattention_backend.py ``forward_extend`` /
+  ``forward_decode``: the new tokens' K/V written to their slots
+  (``set_kv_buffer`` / ``set_mla_kv_buffer``) before attention.
 * ``local_virtual_batches`` -- flashattention_backend.py,
   ``make_local_attention_virtual_batches`` (local chunked attention as
   virtual batches) and the mask drawn in its worked example
@@ -40,6 +43,7 @@ __all__ = [
     "swa_page_table",
     "topk_to_slots",
     "local_virtual_batches",
+    "set_kv_buffer",
     "attention",
     "merge_state",
     "split_bounds",
@@ -81,6 +85,9 @@ def _lib():
             _i32p, _i32p, _int, ctypes.c_double, _int, _int, _int,
             _i32p, _i64, _int,
             _i32p, _int, _f64p, _f64p, _int]
+        lib.orc_set_kv_buffer.argtypes = [
+            _u16p, _i64, _i64, _int, _int, _int, _i64p, _u16p, _i64, _i64, _i64,
+            _i64, _int]
         lib.orc_local_virtual_batches.argtypes = [
             _int, _int, _i32p, _i32p, _int, _i32p, _i64, _int, _int,
             _i32p, _i32p, _i32p, _i32p, _i64, _int, _i32p]
@@ -88,7 +95,7 @@ def _lib():
             _f64p, _f64p, _f64p, _f64p, _i64, _int, _f64p, _f64p]
         for fn in ("orc_strided_page_table", "orc_swa_page_table",
                    "orc_topk_to_slots", "orc_attention", "orc_merge_state",
-                   "orc_local_virtual_batches"):
+                   "orc_local_virtual_batches", "orc_set_kv_buffer"):
             getattr(lib, fn).restype = ctypes.c_int
         _LIB = lib
     return _LIB
@@ -171,6 +178,27 @@ def topk_to_slots(topk, row_req, page_table, page_size: int,
     if rc < 0:
         raise ValueError(f"orc_topk_to_slots rejected its arguments ({rc})")
     return out, rc
+
+
+def set_kv_buffer(cache_bits, rows_bits, loc):
+    """Writes new rows into a paged pool in place and returns the number of
+    skipped (out-of-pool) slots.  cache_bits: uint16 [num_pages, P, H, D]
+    (any element strides, D contiguous, writable); rows_bits: uint16
+    [T, H, D] (D contiguous); loc: T slot ids."""
+    c = cache_bits
+    r = np.asarray(rows_bits)
+    assert c.dtype == np.uint16 and r.dtype == np.uint16
+    assert c.strides[3] == 2 and r.strides[2] == 2 and c.flags.writeable
+    lc = np.ascontiguousarray(loc, dtype=np.int64)
+    cs = _elem_strides(c)
+    rs = _elem_strides(r)
+    n = _lib().orc_set_kv_buffer(
+        _ptr(r, ctypes.c_uint16), rs[0], rs[1], r.shape[0], r.shape[1], r.shape[2],
+        _ptr(lc, ctypes.c_int64), c.ctypes.data_as(_u16p), cs[0], cs[1], cs[2],
+        c.shape[0], c.shape[1])
+    if n < 0:
+        raise ValueError(f"orc_set_kv_buffer rejected its arguments ({n})")
+    return n
 
 
 def local_virtual_batches(attn_chunk_size: int, page_size: int, cu_seqlens_q,

@@ -104,6 +104,24 @@ int orc_topk_to_slots(const int32_t *topk, int64_t topk_stride, int n_rows,
   return bad;
 }
 
+int orc_set_kv_buffer(const uint16_t *rows, int64_t r_st, int64_t r_sh, int n_tokens,
+                      int heads, int d, const int64_t *loc, uint16_t *cache,
+                      int64_t c_sp, int64_t c_spos, int64_t c_sh, int64_t num_pages,
+                      int page_size) {
+  if (n_tokens < 0 || heads < 1 || d < 1 || page_size < 1 || num_pages < 0) return -1;
+  int skipped = 0;
+  for (int t = 0; t < n_tokens; ++t) {
+    int64_t slot = loc[t];
+    if (slot < 0 || slot >= num_pages * page_size) { ++skipped; continue; }
+    int64_t page = slot / page_size, pos = slot % page_size;
+    for (int h = 0; h < heads; ++h)
+      for (int c = 0; c < d; ++c)
+        cache[page * c_sp + pos * c_spos + h * c_sh + c] =
+            rows[(int64_t)t * r_st + (int64_t)h * r_sh + c];
+  }
+  return skipped;
+}
+
 int orc_local_virtual_batches(int attn_chunk_size, int page_size,
                               const int32_t *cu_seqlens_q,
                               const int32_t *seq_lens, int batch,

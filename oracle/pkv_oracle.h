@@ -71,6 +71,22 @@ int orc_topk_to_slots(const int32_t *topk, int64_t topk_stride, int n_rows,
                       const int32_t *cache_seqlens, int32_t *out,
                       int64_t out_stride);
 
+/* KV write before attention (flashattention_backend.py `forward_extend` /
+ * `forward_decode`: `token_to_kv_pool.set_kv_buffer(layer, cache_loc, k, v)`
+ * and, for MLA, `set_mla_kv_buffer(layer, cache_loc, k, k_rope)`): new row t
+ * (all heads) goes to slot loc[t] of the pool, slot s = page * page_size +
+ * position, i.e. cache[s / page_size][s % page_size][h][d] = rows[t][h][d].
+ * Called once for K and once for V.  rows: bf16 bits, element (t, h, d) at
+ * rows[t*r_st + h*r_sh + d]; cache: bf16 bits, (page, pos, h, d) at
+ * cache[page*c_sp + pos*c_spos + h*c_sh + d].  Tokens are written in order
+ * (a repeated slot keeps the last row).  A slot outside
+ * [0, num_pages * page_size) is skipped and counted.  Returns that count, or
+ * -1 on bad arguments. */
+int orc_set_kv_buffer(const uint16_t *rows, int64_t r_st, int64_t r_sh, int n_tokens,
+                      int heads, int d, const int64_t *loc, uint16_t *cache,
+                      int64_t c_sp, int64_t c_spos, int64_t c_sh, int64_t num_pages,
+                      int page_size);
+
 /* Local (chunked) attention as virtual batches (flashattention_backend.py,
  * `make_local_attention_virtual_batches` and its worked example):
  *   1. effective chunk C = min(attn_chunk_size, max_b seq_lens[b]), rounded

@@ -24,6 +24,9 @@ Entry points (names as in the C ABI, without the ``pkv_`` prefix):
   the device; ``local_attn_with_kvcache`` runs it and the attention.
 * ``cascade_attn_with_kvcache`` -- shared-prefix attention as two calls and
   a state merge (``use_cascade_attn``).
+* ``set_kv_buffer`` / ``set_mla_kv_buffer`` -- the new tokens' K/V stored
+  into their pool slots (``set_kv_buffer`` / ``set_mla_kv_buffer`` before
+  attention); ``append_attn_with_kvcache`` stores them and attends.
 """
 from __future__ import annotations
 
@@ -46,6 +49,9 @@ __all__ = [
     "topk_to_slots",
     "make_local_attention_virtual_batches",
     "local_virtual_batch_capacity",
+    "set_kv_buffer",
+    "set_mla_kv_buffer",
+    "append_attn_with_kvcache",
     "local_attn_with_kvcache",
     "get_error_flags",
     "clear_error_flags",
@@ -85,6 +91,7 @@ EXPORTED_SYMBOLS = (
     "pkv_version",
     "pkv_attn_with_kvcache_noalloc",
     "pkv_make_local_attention_virtual_batches",
+    "pkv_set_kv_buffer",
 )
 
 _DTYPES = {torch.bfloat16: _BF16, torch.float32: _F32, torch.int32: _I32,
@@ -136,6 +143,7 @@ def load_library(path: str | None = None):
     lib.pkv_build_swa_page_table.argtypes = [T, T, T, T, c_int, T, T, c_void_p]
     lib.pkv_strided_page_table.argtypes = [T, T, c_int, T, c_void_p]
     lib.pkv_topk_to_slots.argtypes = [T, T, T, T, c_int, T, c_void_p]
+    lib.pkv_set_kv_buffer.argtypes = [T, T, T, T, T, c_void_p]
     lib.pkv_make_local_attention_virtual_batches.argtypes = [
         c_int, c_int, T, T, T, T, T, T, T, T, c_void_p]
     lib.pkv_get_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -308,6 +316,36 @@ def topk_to_slots(topk, cu_seqlens_q, page_table, cache_seqlens,
         _desc(topk), _desc(cu_seqlens_q), _desc(page_table),
         _desc(cache_seqlens), int(page_size), _desc(out), _stream(topk)))
     return out
+
+
+def set_kv_buffer(k_cache, v_cache, loc, k, v=None):
+    """Stores new K (and V) rows into their pool slots (include/pkv.h,
+    pkv_set_kv_buffer): k_cache[loc // P, loc % P] = k, same for v."""
+    _check("pkv_set_kv_buffer", load_library().pkv_set_kv_buffer(
+        _desc(loc), _desc(k), _desc(v), _desc(k_cache), _desc(None if v is None else v_cache),
+        _stream(k)))
+    return k_cache, v_cache
+
+
+def set_mla_kv_buffer(kv_cache, loc, k_nope, k_rope):
+    """MLA latent rows: columns [0, Dn) of the [pages, P, 1, Dn + Dr] pool get
+    k_nope [T, 1, Dn], columns [Dn, Dn + Dr) get k_rope [T, 1, Dr]."""
+    dn = k_nope.shape[-1]
+    set_kv_buffer(kv_cache[..., :dn], kv_cache[..., dn:], loc, k_nope, k_rope)
+    return kv_cache
+
+
+def append_attn_with_kvcache(q, k, v, cache_loc, k_cache, v_cache, page_table,
+                             cache_seqlens, cu_seqlens_q, max_seqlen_q: int,
+                             softmax_scale: float, **attn_kwargs):
+    """The backend's forward order (flashattention_backend.py
+    `forward_extend` / `forward_decode`): the new tokens' K/V go to their
+    slots ``cache_loc`` first, then paged attention reads the cache that now
+    holds them.  Both launches are on the current stream, so attention sees
+    the stored rows; ``attn_kwargs`` are those of ``attn_with_kvcache``."""
+    set_kv_buffer(k_cache, v_cache, cache_loc, k, v)
+    return attn_with_kvcache(q, k_cache, v_cache, page_table, cache_seqlens, cu_seqlens_q,
+                             max_seqlen_q, softmax_scale, **attn_kwargs)
 
 
 def local_virtual_batch_capacity(batch: int, total_q: int, max_seqlen_q: int,

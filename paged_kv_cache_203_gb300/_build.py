@@ -23,6 +23,7 @@ SOURCES = [
     "pkv_extend.cu",
     "pkv_mla.cu",
     "pkv_noalloc.cu",
+    "pkv_append.cu",
 ]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -102,6 +102,28 @@ int launch_strided_page_table(const int32_t *rtt, int64_t rtt_stride,
                               int page_size, int32_t *out, int64_t out_stride,
                               int n_cols, uint32_t *err, cudaStream_t stream);
 
+// The KV write before attention: rows of k [T, H, dk] / v [T, H, dv] go to
+// slot loc[t] = page * page_size + pos of k_cache / v_cache (element strides;
+// last dimension contiguous, 16-byte aligned rows, dk and dv multiples of 8).
+struct SetKvParams {
+  const void *loc;
+  int loc_is64;
+  int n_tokens, heads, dk, dv;
+  const bf16 *k;
+  int64_t k_st, k_sh;
+  const bf16 *v;
+  int64_t v_st, v_sh;
+  bf16 *k_cache;
+  int64_t kc_sp, kc_spos, kc_sh;
+  bf16 *v_cache;
+  int64_t vc_sp, vc_spos, vc_sh;
+  int64_t num_pages;
+  int page_size;
+  uint32_t *err;
+};
+
+int launch_set_kv_buffer(const SetKvParams &p, cudaStream_t stream);
+
 // Largest batch the local-attention virtual batch builder takes (two
 // [batch + 1] int32 arrays in shared memory).
 constexpr int kLocalBatchesMaxBatch = 16384;

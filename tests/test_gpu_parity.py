@@ -875,3 +875,121 @@ def test_local_attention_extend(page_size, chunk):
     eff = _local_check(wl, chunk)
     if chunk < 1000:
         assert eff == chunk
+
+
+# ------------------------------------------------------------ KV write (append)
+
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("P,H,D,T,loc64,head_major", [
+    (16, 8, 128, 37, False, False),
+    (1, 8, 128, 4096, True, False),
+    (64, 2, 64, 1, False, False),
+    (16, 4, 128, 3000, True, True),
+])
+def test_set_kv_buffer_bit_exact(P, H, D, T, loc64, head_major):
+    """New rows scattered to distinct random slots: both pools equal the
+    oracle's scatter bit for bit (every other slot untouched)."""
+    g = torch.Generator().manual_seed(P * 1000 + T)
+    pages = T // P + 40
+    shape = (pages, H, P, D) if head_major else (pages, P, H, D)
+    kc = torch.randn(shape, generator=g).to(torch.bfloat16)
+    vc = torch.randn(shape, generator=g).to(torch.bfloat16)
+    if head_major:
+        kc, vc = kc.permute(0, 2, 1, 3), vc.permute(0, 2, 1, 3)
+    k = torch.randn(T, H, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(T, H, D, generator=g).to(torch.bfloat16)
+    loc = torch.randperm(pages * P, generator=g)[:T].to(torch.int64 if loc64 else torch.int32)
+    ref_k = _bits(kc.permute(0, 2, 1, 3)).transpose(0, 2, 1, 3).copy() if head_major \
+        else _bits(kc).copy()
+    ref_v = _bits(vc.permute(0, 2, 1, 3)).transpose(0, 2, 1, 3).copy() if head_major \
+        else _bits(vc).copy()
+    assert oracle.set_kv_buffer(ref_k, _bits(k), loc.numpy()) == 0
+    assert oracle.set_kv_buffer(ref_v, _bits(v), loc.numpy()) == 0
+    if head_major:
+        kd = kc.permute(0, 2, 1, 3).contiguous().to(DEV).permute(0, 2, 1, 3)
+        vd = vc.permute(0, 2, 1, 3).contiguous().to(DEV).permute(0, 2, 1, 3)
+    else:
+        kd, vd = kc.to(DEV), vc.to(DEV)
+    pkv.set_kv_buffer(kd, vd, loc.to(DEV), k.to(DEV), v.to(DEV))
+    torch.cuda.synchronize()
+    got_k = _bits(kd.permute(0, 2, 1, 3)).transpose(0, 2, 1, 3) if head_major else _bits(kd)
+    got_v = _bits(vd.permute(0, 2, 1, 3)).transpose(0, 2, 1, 3) if head_major else _bits(vd)
+    assert np.array_equal(got_k, ref_k) and np.array_equal(got_v, ref_v)
+    assert pkv.get_error_flags() == 0
+
+
+def test_set_kv_buffer_out_of_pool_and_k_only():
+    """Slots outside the pool are skipped and flagged; a K-only write leaves
+    V alone."""
+    P, H, D, pages = 16, 2, 128, 6
+    kc = torch.zeros(pages, P, H, D, dtype=torch.bfloat16, device=DEV)
+    k = torch.ones(4, H, D, dtype=torch.bfloat16, device=DEV)
+    loc = torch.tensor([3, pages * P, -5, 95], dtype=torch.int32, device=DEV)
+    pkv.set_kv_buffer(kc, None, loc, k)
+    torch.cuda.synchronize()
+    assert pkv.get_error_flags() == pkv.EFLAG_PAGE_OOB
+    flat = kc.view(pages * P, H, D)
+    assert torch.all(flat[3] == 1) and torch.all(flat[95] == 1)
+    assert flat.abs().sum().item() == 2 * H * D
+
+
+def test_set_mla_kv_buffer_bit_exact():
+    """MLA latent rows: nope into columns 0..511, rope into 512..575 of the
+    576-wide pool."""
+    g = torch.Generator().manual_seed(81)
+    P, pages, T = 64, 40, 300
+    pool = torch.randn(pages, P, 1, 576, generator=g).to(torch.bfloat16)
+    nope = torch.randn(T, 1, 512, generator=g).to(torch.bfloat16)
+    rope = torch.randn(T, 1, 64, generator=g).to(torch.bfloat16)
+    loc = torch.randperm(pages * P, generator=g)[:T]
+    ref = _bits(pool).copy()
+    assert oracle.set_kv_buffer(ref[..., :512], _bits(nope), loc.numpy()) == 0
+    assert oracle.set_kv_buffer(ref[..., 512:], _bits(rope), loc.numpy()) == 0
+    pd = pool.to(DEV)
+    pkv.set_mla_kv_buffer(pd, loc.to(DEV), nope.to(DEV), rope.to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(pd), ref)
+    assert pkv.get_error_flags() == 0
+
+
+@pytest.mark.parametrize("kind", ["decode", "extend"])
+def test_append_then_attend(kind):
+    """The backend's order: the new tokens' rows are written to their slots
+    (given as out_cache_loc), then attention reads them.  The pool starts
+    with NaN in those slots; afterwards it equals the workload's pool bit for
+    bit and the output equals the oracle's."""
+    if kind == "decode":
+        wl = workloads.make("tiny_decode", d=128, page_size=16, h_q=32, h_kv=8, batch=24,
+                            len_lo=1, len_hi=2000, pool_tokens=24 * 2008 + 64, seed=83)
+    else:
+        wl = workloads.make("varlen_extend", batch=3, new_lo=64, new_hi=500, prefix_lo=0,
+                            prefix_hi=700, page_size=64, pool_pages=3 * 22 + 8, seed=84)
+    P = wl.k_cache.shape[1]
+    cu = wl.cu_seqlens_q.numpy()
+    kv = wl.cache_seqlens.numpy()
+    pt = wl.page_table.numpy()
+    loc = []
+    for b in range(len(kv)):
+        for j in range(kv[b] - (cu[b + 1] - cu[b]), kv[b]):
+            loc.append(int(pt[b, j // P]) * P + j % P)
+    loc = torch.tensor(loc, dtype=torch.int64)
+    kf = wl.k_cache.view(-1, *wl.k_cache.shape[2:])
+    vf = wl.v_cache.view(-1, *wl.v_cache.shape[2:])
+    k_new, v_new = kf[loc].clone(), vf[loc].clone()
+    g = wl.to(DEV)
+    kd, vd = g.k_cache.clone(), g.v_cache.clone()
+    kd.view(-1, *kd.shape[2:])[loc.to(DEV)] = float("nan")
+    vd.view(-1, *vd.shape[2:])[loc.to(DEV)] = float("nan")
+    out, lse = pkv.append_attn_with_kvcache(
+        g.q, k_new.to(DEV), v_new.to(DEV), loc.to(DEV), kd, vd, g.page_table,
+        g.cache_seqlens, g.cu_seqlens_q, g.max_seqlen_q, g.scale, causal=g.causal,
+        return_softmax_lse=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(kd), _bits(wl.k_cache))
+    assert np.array_equal(_bits(vd), _bits(wl.v_cache))
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, f"append+attend {kind}")
+    assert pkv.get_error_flags() == 0

@@ -697,3 +697,81 @@ def test_local_padding_idle_and_malformed_requests():
     assert list(out["block_table_local"][1, :2]) == [pt[0, 2], pt[0, 2]]
     with pytest.raises(ValueError):
         oracle.local_virtual_batches(8, 2, cu, kv, pt, capacity=8, bt_cols=3)
+
+
+# ------------------------------------------------------------ KV write (append)
+
+@pytest.mark.parametrize("page_size", [1, 4, 16])
+def test_set_kv_buffer_builds_the_paged_cache(page_size):
+    """Writing every logical row of every request to slot
+    page_table[b][j / P] * P + j % P reproduces the paged cache built
+    page by page (the layout attention reads); the junk in unused slots is
+    untouched."""
+    rng = np.random.default_rng(71 + page_size)
+    kv_lens = [5, 17, 1, 33]
+    logical = [rng.standard_normal((n, 2, 8)) for n in kv_lens]
+    want, pt = paged_from_logical(np.random.default_rng(9), logical, page_size)
+    want_b, _ = bf16(want)
+    # start from the same junk, with every slot some request owns cleared
+    got = want_b.copy()
+    for b, n in enumerate(kv_lens):
+        for j in range(n):
+            got[pt[b, j // page_size], j % page_size] = 0
+    rows = np.concatenate([bf16(x)[0] for x in logical])
+    loc = np.concatenate([[pt[b, j // page_size] * page_size + j % page_size
+                           for j in range(n)] for b, n in enumerate(kv_lens)])
+    assert oracle.set_kv_buffer(got, rows, loc) == 0
+    assert np.array_equal(got, want_b)
+
+
+def test_set_kv_buffer_then_attention_equals_dense_rows():
+    """Append then attend: a pool holding each request's old keys, the new
+    tokens' K/V written to their slots, then causal attention equals scipy
+    softmax over the request's full logical rows."""
+    rng = np.random.default_rng(72)
+    P, q_lens, kv_lens = 4, [1, 3, 6], [9, 14, 6]
+    c = _tiny_case(rng, 3, q_lens, kv_lens, 4, 2, 8, P)
+    kb = c["kb"].copy()
+    vb = c["vb"].copy()
+    new_k, new_v, loc = [], [], []
+    for b, (ql, n) in enumerate(zip(q_lens, kv_lens)):
+        for j in range(n - ql, n):
+            slot = c["pt"][b, j // P] * P + j % P
+            loc.append(slot)
+            new_k.append(kb[slot // P, slot % P].copy())
+            new_v.append(vb[slot // P, slot % P].copy())
+            kb[slot // P, slot % P] = 0x7fc0  # NaN until written
+            vb[slot // P, slot % P] = 0x7fc0
+    assert oracle.set_kv_buffer(kb, np.stack(new_k), loc) == 0
+    assert oracle.set_kv_buffer(vb, np.stack(new_v), loc) == 0
+    out, lse, _ = oracle.attention(c["qb"], kb, vb, c["pt"], c["kv"], c["cu"], 0.3,
+                                   causal=True)
+    for b, (ql, n) in enumerate(zip(q_lens, kv_lens)):
+        for u in range(ql):
+            t = c["cu"][b] + u
+            i = n - ql + u
+            for h in range(4):
+                o, l = dense_reference_row(c["qf"][t, h], c["klog"][b][:i + 1, h // 2],
+                                           c["vlog"][b][:i + 1, h // 2], 0.3)
+                np.testing.assert_allclose(out[t, h], o, atol=1e-12)
+                assert abs(lse[t, h] - l) < 1e-12
+
+
+def test_set_kv_buffer_strides_and_out_of_pool_slots():
+    """A head-major pool (strided view) is written through its strides; slots
+    outside the pool are skipped and counted, nothing else changes; a
+    repeated slot keeps the later row."""
+    rng = np.random.default_rng(73)
+    pool = bf16(rng.standard_normal((5, 2, 4, 8)))[0]      # [pages, H, P, D]
+    view = pool.transpose(0, 2, 1, 3)                       # [pages, P, H, D]
+    before = pool.copy()
+    rows = bf16(rng.standard_normal((4, 2, 8)))[0]
+    loc = [3, 19, -1, 20]                                   # 20 = 5 * 4 is past the pool
+    assert oracle.set_kv_buffer(view, rows, loc) == 2
+    assert np.array_equal(view[0, 3], rows[0]) and np.array_equal(view[4, 3], rows[1])
+    mask = np.ones(pool.shape, bool)
+    mask[0, :, 3] = False
+    mask[4, :, 3] = False
+    assert np.array_equal(pool[mask], before[mask])
+    assert oracle.set_kv_buffer(view, rows[:2], [7, 7]) == 0
+    assert np.array_equal(view[1, 3], rows[1])
