@@ -382,6 +382,9 @@ def append_line(dev, peaks):
             "ms_per_step": s_ms, "tokens_per_s": g.q.shape[0] / (s_ms / 1e3)}
 
 
+EXTRA_LINES = {"local": local_attention_line, "cascade": cascade_line, "append": append_line}
+
+
 def parse_overrides(s: str | None) -> dict:
     out = {}
     if not s:
@@ -557,8 +560,18 @@ def main():
     ap.add_argument("--no-others", action="store_true",
                     help="skip the per-workload summary of the other workloads")
     ap.add_argument("--ref-budget", type=float, default=10.0)
+    ap.add_argument("--line", default=None, choices=sorted(EXTRA_LINES),
+                    help="run one of the extra lines alone (local attention, cascade, "
+                         "KV write) and print its JSON; for profiling")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.line is not None:
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        pkv.load_library()
+        print(json.dumps({"line": args.line, **EXTRA_LINES[args.line](dev, measured_peaks())}),
+              flush=True)
+        return
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
