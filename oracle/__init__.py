@@ -14,6 +14,9 @@ Every function restates a definition from the SGLang attention-backend pages:
 * ``set_kv_buffer`` -- flashattention_backend.py ``forward_extend`` /
   ``forward_decode``: the new tokens' K/V written to their slots
   (``set_kv_buffer`` / ``set_mla_kv_buffer``) before attention.
+* ``e4m3_value`` / ``e4m3_round`` / ``attention_fp8`` -- flashattention_backend.py
+  fp8 KV cache: q cast to the cache dtype, ``k_descale`` / ``v_descale`` per
+  (request, KV head).
 * ``local_virtual_batches`` -- flashattention_backend.py,
   ``make_local_attention_virtual_batches`` (local chunked attention as
   virtual batches) and the mask drawn in its worked example
@@ -44,6 +47,9 @@ __all__ = [
     "topk_to_slots",
     "local_virtual_batches",
     "set_kv_buffer",
+    "e4m3_value",
+    "e4m3_round",
+    "attention_fp8",
     "attention",
     "merge_state",
     "split_bounds",
@@ -85,6 +91,21 @@ def _lib():
             _i32p, _i32p, _int, ctypes.c_double, _int, _int, _int,
             _i32p, _i64, _int,
             _i32p, _int, _f64p, _f64p, _int]
+        _u8p = ctypes.POINTER(ctypes.c_uint8)
+        _f32p = ctypes.POINTER(ctypes.c_float)
+        lib.orc_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3_value.restype = ctypes.c_double
+        lib.orc_e4m3_round.argtypes = [ctypes.c_double]
+        lib.orc_e4m3_round.restype = ctypes.c_uint8
+        lib.orc_attention_fp8.argtypes = [
+            _u16p, _i64, _i64, _int, _int, _int,
+            _u8p, _i64, _i64, _i64,
+            _u8p, _i64, _i64, _i64, _int,
+            _int, _int, _i64,
+            _i32p, _i64, _int,
+            _i32p, _i32p, _int, ctypes.c_double, _int, _int,
+            _f32p, _f32p, _f64p, _f64p, _int]
+        lib.orc_attention_fp8.restype = ctypes.c_int
         lib.orc_set_kv_buffer.argtypes = [
             _u16p, _i64, _i64, _int, _int, _int, _i64p, _u16p, _i64, _i64, _i64,
             _i64, _int]
@@ -178,6 +199,53 @@ def topk_to_slots(topk, row_req, page_table, page_size: int,
     if rc < 0:
         raise ValueError(f"orc_topk_to_slots rejected its arguments ({rc})")
     return out, rc
+
+
+def e4m3_value(code: int) -> float:
+    """Value of one e4m3 code (NaN for 0x7f / 0xff)."""
+    return _lib().orc_e4m3_value(int(code))
+
+
+def e4m3_round(x: float) -> int:
+    """Nearest e4m3 code to x (ties to the even code; NaN code past 464)."""
+    return int(_lib().orc_e4m3_round(float(x)))
+
+
+def attention_fp8(q_bits, k_codes, v_codes, page_table, cache_seqlens, cu_seqlens_q,
+                  scale: float, causal: bool = False, window_left: int = -1,
+                  k_descale=None, v_descale=None, num_threads: int = 0):
+    """Attention over an fp8 (e4m3) paged cache in float64: q rounded to
+    e4m3, K/V codes widened and multiplied by their (request, KV head)
+    descales.  q_bits: uint16 [total_q, H_q, D]; k_codes / v_codes: uint8
+    [num_pages, P, H_kv, D] (D contiguous); descales: float32 [B, H_kv] or
+    None.  Returns (out [total_q, H_q, Dv], lse [total_q, H_q], n_skipped)."""
+    q = np.asarray(q_bits)
+    k = np.asarray(k_codes)
+    v = np.asarray(v_codes)
+    assert q.dtype == np.uint16 and k.dtype == np.uint8 and v.dtype == np.uint8
+    assert q.strides[2] == 2 and k.strides[3] == 1 and v.strides[3] == 1
+    total_q, h_q, d = q.shape
+    num_pages, page_size, h_kv, _ = k.shape
+    d_v = v.shape[3]
+    qs, ks, vs = _elem_strides(q), _elem_strides(k), _elem_strides(v)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    cs = np.ascontiguousarray(cache_seqlens, dtype=np.int32)
+    cu = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
+    kd = None if k_descale is None else np.ascontiguousarray(k_descale, dtype=np.float32)
+    vd = None if v_descale is None else np.ascontiguousarray(v_descale, dtype=np.float32)
+    out = np.zeros((total_q * h_q, d_v), dtype=np.float64)
+    lse = np.zeros(total_q * h_q, dtype=np.float64)
+    rc = _lib().orc_attention_fp8(
+        _ptr(q, ctypes.c_uint16), qs[0], qs[1], total_q, h_q, d,
+        k.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), ks[0], ks[1], ks[2],
+        v.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), vs[0], vs[1], vs[2], d_v,
+        h_kv, page_size, num_pages, _ptr(pt, ctypes.c_int32), pt.shape[1], pt.shape[1],
+        _ptr(cs, ctypes.c_int32), _ptr(cu, ctypes.c_int32), len(cs), float(scale),
+        int(bool(causal)), int(window_left), _ptr(kd, ctypes.c_float), _ptr(vd, ctypes.c_float),
+        _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double), int(num_threads))
+    if rc < 0:
+        raise ValueError(f"orc_attention_fp8 rejected its arguments ({rc})")
+    return out.reshape(total_q, h_q, d_v), lse.reshape(total_q, h_q), rc
 
 
 def set_kv_buffer(cache_bits, rows_bits, loc):

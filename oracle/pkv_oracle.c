@@ -351,6 +351,119 @@ int orc_attention(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q,
   return skipped_total;
 }
 
+double orc_e4m3_value(uint8_t code) {
+  const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = e == 0 ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -mag : mag;
+}
+
+uint8_t orc_e4m3_round(double x) {
+  if (isnan(x)) return 0x7f;
+  const uint8_t sign = x < 0 ? 0x80 : 0x00;
+  const double a = fabs(x);
+  /* nearest of the non-negative codes 0..127, code 127 standing for the
+     value 480 the format does not have (choosing it means "NaN") */
+  int best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c < 128; ++c) {
+    const double v = c == 127 ? 480.0 : orc_e4m3_value((uint8_t)c);
+    const double dist = fabs(a - v);
+    if (dist < best_d || (dist == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = dist;
+    }
+  }
+  if (best == 127) return (uint8_t)(sign | 0x7f);
+  return (uint8_t)(sign | best);
+}
+
+int orc_attention_fp8(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q,
+                      int h_q, int d_qk, const uint8_t *k_cache, int64_t k_sp,
+                      int64_t k_spos, int64_t k_sh, const uint8_t *v_cache,
+                      int64_t v_sp, int64_t v_spos, int64_t v_sh, int d_v,
+                      int h_kv, int page_size, int64_t num_pages,
+                      const int32_t *page_table, int64_t pt_stride, int pt_cols,
+                      const int32_t *cache_seqlens, const int32_t *cu_seqlens_q,
+                      int batch, double scale, int causal, int window_left,
+                      const float *k_descale, const float *v_descale,
+                      double *out, double *lse, int num_threads) {
+  if (total_q < 0 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0 || d_qk < 1 ||
+      d_v < 1 || page_size < 1 || batch < 0 || window_left < -1)
+    return -1;
+  int64_t max_keys = 1;
+  for (int b = 0; b < batch; ++b)
+    if (cache_seqlens[b] > max_keys) max_keys = cache_seqlens[b];
+  int skipped_total = 0;
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#endif
+#pragma omp parallel reduction(+ : skipped_total)
+  {
+    double *s_buf = (double *)malloc(sizeof(double) * (size_t)max_keys);
+    int64_t *slot_buf = (int64_t *)malloc(sizeof(int64_t) * (size_t)max_keys);
+    double *qv = (double *)malloc(sizeof(double) * (size_t)d_qk);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t w = 0; w < (int64_t)total_q * h_q; ++w) {
+      const int t = (int)(w / h_q), h = (int)(w % h_q);
+      double *o = out + w * d_v;
+      for (int dd = 0; dd < d_v; ++dd) o[dd] = 0.0;
+      if (lse) lse[w] = -INFINITY;
+      int b = 0; /* request of token t */
+      while (b < batch && !(cu_seqlens_q[b] <= t && t < cu_seqlens_q[b + 1])) ++b;
+      if (b == batch) continue;
+      const int64_t kv_len = cache_seqlens[b];
+      const int64_t q_len = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+      const int64_t i = kv_len - q_len + (t - cu_seqlens_q[b]); /* bottom-right */
+      const int kvh = h / (h_q / h_kv);
+      const double kd = k_descale ? (double)k_descale[(int64_t)b * h_kv + kvh] : 1.0;
+      const double vd = v_descale ? (double)v_descale[(int64_t)b * h_kv + kvh] : 1.0;
+      /* 1. q cast to the cache's e4m3 */
+      const uint16_t *qrow = q + (int64_t)t * q_st + (int64_t)h * q_sh;
+      for (int dd = 0; dd < d_qk; ++dd)
+        qv[dd] = orc_e4m3_value(orc_e4m3_round(bf16_bits_to_double(qrow[dd])));
+      /* 2. the visible keys and their slots */
+      int64_t n = 0;
+      for (int64_t j = 0; j < kv_len; ++j) {
+        if (causal && j > i) continue;
+        if (window_left >= 0 && (j > i || j < i - window_left)) continue;
+        if (j / page_size >= pt_cols) { ++skipped_total; continue; }
+        const int64_t page = page_table[(int64_t)b * pt_stride + j / page_size];
+        if (page < 0 || page >= num_pages) { ++skipped_total; continue; }
+        slot_buf[n++] = page * page_size + j % page_size;
+      }
+      if (n == 0) continue;
+      /* 3. s_j = scale * <q', K'_j>, K'_j = value(code) * k_descale */
+      double m = -INFINITY;
+      for (int64_t c = 0; c < n; ++c) {
+        const int64_t slot = slot_buf[c];
+        const uint8_t *krow = k_cache + (slot / page_size) * k_sp +
+                              (slot % page_size) * k_spos + (int64_t)kvh * k_sh;
+        double dot = 0.0;
+        for (int dd = 0; dd < d_qk; ++dd) dot += qv[dd] * (orc_e4m3_value(krow[dd]) * kd);
+        s_buf[c] = scale * dot;
+        if (s_buf[c] > m) m = s_buf[c];
+      }
+      /* 4. lse and o = sum exp(s - lse) V'_j, V'_j = value(code) * v_descale */
+      double sum = 0.0;
+      for (int64_t c = 0; c < n; ++c) sum += exp(s_buf[c] - m);
+      const double l = m + log(sum);
+      for (int64_t c = 0; c < n; ++c) {
+        const int64_t slot = slot_buf[c];
+        const uint8_t *vrow = v_cache + (slot / page_size) * v_sp +
+                              (slot % page_size) * v_spos + (int64_t)kvh * v_sh;
+        const double wgt = exp(s_buf[c] - l);
+        for (int dd = 0; dd < d_v; ++dd) o[dd] += wgt * (orc_e4m3_value(vrow[dd]) * vd);
+      }
+      if (lse) lse[w] = l;
+    }
+    free(s_buf);
+    free(slot_buf);
+    free(qv);
+  }
+  return skipped_total;
+}
+
 int orc_merge_state(const double *v_a, const double *lse_a, const double *v_b,
                     const double *lse_b, int64_t n, int d, double *v_out,
                     double *lse_out) {

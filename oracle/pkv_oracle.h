@@ -170,6 +170,36 @@ int orc_attention(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q,
                   int topk_len, const int32_t *rows, int n_rows, double *out,
                   double *lse, int num_threads);
 
+/* FP8 KV cache (flashattention_backend.py `forward_extend` / `forward_decode`
+ * with an fp8 `kv_cache_dtype`: `k_descale` / `v_descale` = the layer's
+ * k_scale / v_scale expanded to (batch, KV heads), and q cast to the cache
+ * dtype).  Format e4m3 ("fn"): sign, 4 exponent bits (bias 7), 3 mantissa
+ * bits, exponent 0 subnormal, codes 0x7f / 0xff NaN, no infinities; largest
+ * finite 448. */
+
+/* Value of an e4m3 code (NaN for 0x7f / 0xff). */
+double orc_e4m3_value(uint8_t code);
+
+/* Nearest e4m3 code to x, ties to the even code; a magnitude that rounds
+ * past 448 (above 464) gives the NaN code, as does NaN. */
+uint8_t orc_e4m3_round(double x);
+
+/* Attention over an fp8 cache: q rounded to e4m3 (orc_e4m3_round) and widened;
+ * K_j = value(k code) * k_descale[b * n_kv_heads + kvh], V_j likewise with
+ * v_descale (NULL descales = 1); then the definition of orc_attention (same
+ * layouts, masks, bottom-right alignment and empty-key result, no top-k).
+ * k / v: uint8 codes, (page, pos, head, d) at page*sp + pos*spos + head*sh + d. */
+int orc_attention_fp8(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q,
+                      int h_q, int d_qk, const uint8_t *k_cache, int64_t k_sp,
+                      int64_t k_spos, int64_t k_sh, const uint8_t *v_cache,
+                      int64_t v_sp, int64_t v_spos, int64_t v_sh, int d_v,
+                      int h_kv, int page_size, int64_t num_pages,
+                      const int32_t *page_table, int64_t pt_stride, int pt_cols,
+                      const int32_t *cache_seqlens, const int32_t *cu_seqlens_q,
+                      int batch, double scale, int causal, int window_left,
+                      const float *k_descale, const float *v_descale,
+                      double *out, double *lse, int num_threads);
+
 /* Log-sum-exp state merge (dual_chunk_flashattention_backend.py,
  * `_merge_attn_outputs`; merge_state_v2 in flashattention_backend.py):
  *   m = max(lse_a, lse_b); lse = m + log(exp(lse_a-m) + exp(lse_b-m));

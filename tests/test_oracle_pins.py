@@ -775,3 +775,109 @@ def test_set_kv_buffer_strides_and_out_of_pool_slots():
     assert np.array_equal(pool[mask], before[mask])
     assert oracle.set_kv_buffer(view, rows[:2], [7, 7]) == 0
     assert np.array_equal(view[1, 3], rows[1])
+
+
+# ------------------------------------------------------------------ FP8 KV
+
+def test_e4m3_values_match_torch():
+    """All 256 e4m3 codes widen to torch's float8_e4m3fn values (a library
+    conversion), NaN codes included."""
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.e4m3_value(c) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)])
+    assert oracle.e4m3_value(0x7e) == 448.0 and oracle.e4m3_value(0x01) == 2.0 ** -9
+
+
+def test_e4m3_rounding_matches_torch():
+    """Round to nearest, ties to the even code, NaN past the largest value,
+    subnormals: the oracle's encoder gives torch's codes for random values
+    over the whole range, every tie point and the overflow edge."""
+    rng = np.random.default_rng(91)
+    vals = list(rng.standard_normal(2000) * np.exp2(rng.integers(-12, 9, 2000)))
+    codes = np.arange(127)
+    mags = np.array([oracle.e4m3_value(c) for c in codes])
+    vals += list((mags[:-1] + mags[1:]) / 2)          # every midpoint (ties)
+    vals += [448.0, 450.0, 463.9, 464.0, 464.1, 470.0, 479.0, 480.0, 1e4, 2.0 ** -10,
+             3 * 2.0 ** -11, 2.0 ** -11, 0.0]
+    vals += [-v for v in vals[:500]]
+    x = torch.tensor(vals, dtype=torch.float64)
+    ref = x.to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_round(v) for v in x.to(torch.float32).double().tolist()])
+    assert np.array_equal(got, ref)
+
+
+def _fp8_case(rng, q_lens, kv_lens, P, h_q=4, h_kv=2, d=16):
+    c = _tiny_case(rng, len(q_lens), q_lens, kv_lens, h_q, h_kv, d, P)
+    codes = rng.integers(0, 256, size=c["kb"].shape, dtype=np.uint8)
+    codes[(codes & 0x7f) == 0x7f] = 0x38           # no NaN codes in the cache
+    vcodes = rng.integers(0, 256, size=c["vb"].shape, dtype=np.uint8)
+    vcodes[(vcodes & 0x7f) == 0x7f] = 0x30
+    return c, codes, vcodes
+
+
+def _codes_to_bf16_bits(codes):
+    vals = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).float()
+    return oracle.bf16_bits(vals.to(torch.bfloat16))
+
+
+def test_fp8_attention_equals_bf16_attention_on_the_widened_values():
+    """With unit descales, fp8 attention equals the bf16-path attention over
+    caches holding the widened codes and q replaced by its e4m3 rounding
+    (all exactly representable in bf16)."""
+    rng = np.random.default_rng(92)
+    c, kc, vc = _fp8_case(rng, [1, 3, 2], [9, 20, 5], 4)
+    q32 = torch.from_numpy(c["qf"].astype(np.float32))
+    q8 = q32.to(torch.float8_e4m3fn).float().to(torch.bfloat16)
+    out, lse, _ = oracle.attention_fp8(c["qb"], kc, vc, c["pt"], c["kv"], c["cu"], 0.3,
+                                       causal=True)
+    ref_o, ref_l, _ = oracle.attention(oracle.bf16_bits(q8), _codes_to_bf16_bits(kc),
+                                       _codes_to_bf16_bits(vc), c["pt"], c["kv"], c["cu"], 0.3,
+                                       causal=True)
+    np.testing.assert_allclose(out, ref_o, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_l, atol=1e-12)
+
+
+def test_fp8_descale_closed_forms():
+    """k_descale multiplies every score (same as a larger softmax scale);
+    v_descale multiplies the output and leaves the lse alone."""
+    rng = np.random.default_rng(93)
+    c, kc, vc = _fp8_case(rng, [2, 1], [7, 12], 4)
+    ones = np.ones((2, 2), np.float32)
+    base_o, base_l, _ = oracle.attention_fp8(c["qb"], kc, vc, c["pt"], c["kv"], c["cu"], 0.6,
+                                             k_descale=ones, v_descale=ones)
+    o2, l2, _ = oracle.attention_fp8(c["qb"], kc, vc, c["pt"], c["kv"], c["cu"], 0.3,
+                                     k_descale=2 * ones, v_descale=ones)
+    np.testing.assert_allclose(o2, base_o, atol=1e-12)
+    np.testing.assert_allclose(l2, base_l, atol=1e-12)
+    o3, l3, _ = oracle.attention_fp8(c["qb"], kc, vc, c["pt"], c["kv"], c["cu"], 0.6,
+                                     k_descale=ones, v_descale=3 * ones)
+    np.testing.assert_allclose(o3, 3 * base_o, atol=1e-12)
+    np.testing.assert_allclose(l3, base_l, atol=1e-12)
+
+
+def test_fp8_per_request_descales_against_scipy():
+    """Descales differ per (request, KV head): each row equals scipy's
+    softmax over that request's rows dequantized with its own factors."""
+    rng = np.random.default_rng(94)
+    q_lens, kv_lens, P = [1, 2], [6, 11], 4
+    c, kc, vc = _fp8_case(rng, q_lens, kv_lens, P, h_q=4, h_kv=2, d=8)
+    kd = rng.uniform(0.5, 2.0, (2, 2)).astype(np.float32)
+    vd = rng.uniform(0.5, 2.0, (2, 2)).astype(np.float32)
+    out, lse, _ = oracle.attention_fp8(c["qb"], kc, vc, c["pt"], c["kv"], c["cu"], 0.45,
+                                       causal=True, k_descale=kd, v_descale=vd)
+    kval = torch.from_numpy(kc.copy()).view(torch.float8_e4m3fn).double().numpy()
+    vval = torch.from_numpy(vc.copy()).view(torch.float8_e4m3fn).double().numpy()
+    q8 = torch.from_numpy(c["qf"].astype(np.float32)).to(torch.float8_e4m3fn).double().numpy()
+    for b, (ql, n) in enumerate(zip(q_lens, kv_lens)):
+        rows = [c["pt"][b, j // P] * P + j % P for j in range(n)]
+        for u in range(ql):
+            t = c["cu"][b] + u
+            i = n - ql + u
+            for h in range(4):
+                kvh = h // 2
+                K = np.stack([kval[s // P, s % P, kvh] for s in rows[:i + 1]]) * kd[b, kvh]
+                V = np.stack([vval[s // P, s % P, kvh] for s in rows[:i + 1]]) * vd[b, kvh]
+                o, l = dense_reference_row(q8[t, h], K, V, 0.45)
+                np.testing.assert_allclose(out[t, h], o, atol=1e-12)
+                assert abs(lse[t, h] - l) < 1e-12
