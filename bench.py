@@ -382,7 +382,37 @@ def append_line(dev, peaks):
             "ms_per_step": s_ms, "tokens_per_s": g.q.shape[0] / (s_ms / 1e3)}
 
 
-EXTRA_LINES = {"local": local_attention_line, "cascade": cascade_line, "append": append_line}
+def fp8_line(dev, peaks):
+    """The headline decode batch over an fp8 (e4m3) cache: the same keys as
+    the bf16 cache cast to e4m3 codes, per-(request, KV head) descales, the
+    library's split choice.  Algorithmic bytes are the codes read: 1 byte per
+    element (2048 B per token at 8 KV heads, head dim 128)."""
+    g = workloads.make(HEADLINE, value_device=dev)
+    k8 = g.k_cache.to(torch.float8_e4m3fn)
+    v8 = g.v_cache.to(torch.float8_e4m3fn)
+    del g.k_cache, g.v_cache
+    B, h_kv = g.cache_seqlens.shape[0], k8.shape[2]
+    kd = torch.full((B, h_kv), 0.75, device=dev)
+    vd = torch.full((B, h_kv), 1.25, device=dev)
+    out = torch.empty(g.q.shape[0], g.q.shape[1], 128, dtype=torch.bfloat16, device=dev)
+    ws_n = pkv.attn_workspace_size(g.q, k8, v8, g.page_table, g.cache_seqlens, g.max_seqlen_q)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=dev)
+
+    def attend():
+        pkv.attn_with_kvcache_fp8(g.q, k8, v8, g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+                                  g.max_seqlen_q, g.scale, k_descale=kd, v_descale=vd,
+                                  out=out, workspace=ws)
+
+    a_ms = _event_ms(attend)
+    kv_bytes = int(g.cache_seqlens.sum()) * h_kv * 256
+    return {"kernel": "decode_allheads_kernel (page boxes, balanced, fp8)",
+            "attn_ms": a_ms, "kv_GBps": kv_bytes / 1e9 / (a_ms / 1e3),
+            "kv_frac_hbm": kv_bytes / 1e9 / (a_ms / 1e3) / peaks["hbm_gbs"],
+            "tokens_per_s": g.q.shape[0] / (a_ms / 1e3)}
+
+
+EXTRA_LINES = {"local": local_attention_line, "cascade": cascade_line, "append": append_line,
+               "fp8": fp8_line}
 
 
 def parse_overrides(s: str | None) -> dict:
@@ -699,7 +729,8 @@ def main():
                 others[label] = {"unavailable": str(e)}
         for label, fn in ((HEADLINE + "@local_chunk_2048", local_attention_line),
                           (HEADLINE + "@cascade_shared_prefix_4096", cascade_line),
-                          ("varlen_extend@append_then_attend", append_line)):
+                          ("varlen_extend@append_then_attend", append_line),
+                          (HEADLINE + "@fp8_kv", fp8_line)):
             try:
                 others[label] = fn(dev, peaks)
             except pkv.PkvError as e:

@@ -42,7 +42,8 @@ enum pkv_dtype {
   PKV_BF16 = 1, /* bfloat16 */
   PKV_F32 = 2,  /* float32 */
   PKV_I32 = 3,  /* int32 */
-  PKV_I64 = 4   /* int64 */
+  PKV_I64 = 4,  /* int64 */
+  PKV_FP8_E4M3 = 5 /* fp8 e4m3 ("fn": bias 7, no infinities, largest 448) codes */
 };
 
 enum pkv_status {
@@ -120,6 +121,8 @@ typedef struct pkv_tensor {
  *
  * Supported: Dq = Dv in {64, 128} with H_q % H_kv == 0; and absorbed MLA
  * Dq = 576, Dv = 512, H_kv = 1.  Other shapes return PKV_ERR_UNSUPPORTED.
+ * k_cache / v_cache may also be fp8 codes (PKV_FP8_E4M3, both): see
+ * pkv_attn_with_kvcache_fp8 (this entry point uses descales of 1).
  * Concurrent calls that share one workspace race.
  */
 int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
@@ -129,6 +132,36 @@ int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
                           pkv_tensor topk_indices, int num_splits,
                           pkv_tensor out, pkv_tensor lse, void *workspace,
                           size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * pkv_attn_with_kvcache_fp8 -- paged attention over an fp8 (e4m3) KV cache.
+ *
+ * Defined by flashattention_backend.py with an fp8 `kv_cache_dtype`
+ * (`forward_extend` / `forward_decode`): `k_descale` / `v_descale` are the
+ * layer's k_scale / v_scale expanded to (batch, KV heads), and q is cast to
+ * the cache dtype before the call.  With K'_j = code_j * k_descale[b][kvh],
+ * V'_j = code_j * v_descale[b][kvh] and q' = q rounded to e4m3 (nearest,
+ * ties to even): the attention of pkv_attn_with_kvcache over q', K', V'.
+ * q must lie within the e4m3 range (|q| <= 448; larger values saturate).
+ *
+ * k_cache / v_cache  PKV_FP8_E4M3 [num_pages, P, H_kv, 128] codes, last dim
+ *                    contiguous, 16-byte aligned rows.
+ * k_descale / v_descale device pointers to fp32 [B][H_kv] (row-major,
+ *                    contiguous), or NULL for 1.
+ * Other arguments, outputs and workspace as pkv_attn_with_kvcache
+ * (pkv_attn_workspace_size takes the fp8 tensors as they are).
+ * Supported: head dim 128, H_kv <= 8, at most 16 query rows per KV head
+ * (max_seqlen_q * H_q / H_kv), page size a multiple of 16, num_splits = 0,
+ * no top-k lists, B <= 2048; otherwise PKV_ERR_UNSUPPORTED.
+ */
+int pkv_attn_with_kvcache_fp8(pkv_tensor q, pkv_tensor k_cache,
+                              pkv_tensor v_cache, pkv_tensor page_table,
+                              pkv_tensor cache_seqlens, pkv_tensor cu_seqlens_q,
+                              int max_seqlen_q, float scale, int causal,
+                              int window_left, const float *k_descale,
+                              const float *v_descale, int num_splits,
+                              pkv_tensor out, pkv_tensor lse, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
 
 /* Bytes of workspace pkv_attn_with_kvcache needs for these sizes (0 if
  * none).  Arguments mirror the attention call's; returns 0 and sets

@@ -9,6 +9,8 @@ the first call raises.
 
 Entry points (names as in the C ABI, without the ``pkv_`` prefix):
 
+* ``attn_with_kvcache_fp8`` -- the same over an fp8 (e4m3) cache with
+  per-(request, KV head) descales (fp8 ``kv_cache_dtype``).
 * ``attn_with_kvcache`` -- paged attention of new query tokens
   (flashattention_backend.py ``flash_attn_with_kvcache`` calls; nsa_backend.py
   top-k sparse decode), with split-KV combined by the state merge.
@@ -42,6 +44,7 @@ __all__ = [
     "attn_with_kvcache",
     "attn_workspace_size",
     "attn_with_kvcache_noalloc",
+    "attn_with_kvcache_fp8",
     "NOALLOC_SCRATCH_BYTES",
     "merge_state",
     "build_swa_page_table",
@@ -92,10 +95,12 @@ EXPORTED_SYMBOLS = (
     "pkv_attn_with_kvcache_noalloc",
     "pkv_make_local_attention_virtual_batches",
     "pkv_set_kv_buffer",
+    "pkv_attn_with_kvcache_fp8",
 )
 
+_FP8 = 5
 _DTYPES = {torch.bfloat16: _BF16, torch.float32: _F32, torch.int32: _I32,
-           torch.int64: _I64}
+           torch.int64: _I64, torch.float8_e4m3fn: _FP8}
 
 
 class PkvError(RuntimeError):
@@ -144,6 +149,9 @@ def load_library(path: str | None = None):
     lib.pkv_strided_page_table.argtypes = [T, T, c_int, T, c_void_p]
     lib.pkv_topk_to_slots.argtypes = [T, T, T, T, c_int, T, c_void_p]
     lib.pkv_set_kv_buffer.argtypes = [T, T, T, T, T, c_void_p]
+    lib.pkv_attn_with_kvcache_fp8.argtypes = [T, T, T, T, T, T, c_int, c_float, c_int, c_int,
+                                              c_void_p, c_void_p, c_int, T, T, c_void_p,
+                                              c_size_t, c_void_p]
     lib.pkv_make_local_attention_virtual_batches.argtypes = [
         c_int, c_int, T, T, T, T, T, T, T, T, c_void_p]
     lib.pkv_get_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -219,6 +227,47 @@ def attn_with_kvcache(q, k_cache, v_cache, page_table, cache_seqlens,
         float(softmax_scale), int(bool(causal)), int(window_left),
         _desc(topk_indices), int(num_splits), _desc(out), _desc(lse), ws_ptr,
         ws_bytes, _stream(q)))
+    return (out, lse) if return_softmax_lse else out
+
+
+def _descale_ptr(t, cache_seqlens, k_cache):
+    """Device pointer of a [B, H_kv] fp32 descale tensor (None -> NULL)."""
+    if t is None:
+        return None
+    want = (cache_seqlens.shape[0], k_cache.shape[2])
+    if (t.dtype != torch.float32 or tuple(t.shape) != want or not t.is_contiguous()
+            or t.device != k_cache.device):
+        raise ValueError(f"descale must be a contiguous float32 tensor of shape {want} "
+                         "on the cache's device")
+    return t.data_ptr()
+
+
+def attn_with_kvcache_fp8(q, k_cache, v_cache, page_table, cache_seqlens, cu_seqlens_q,
+                          max_seqlen_q: int, softmax_scale: float, causal: bool = False,
+                          window_left: int = -1, k_descale=None, v_descale=None,
+                          out=None, lse=None, return_softmax_lse: bool = False,
+                          workspace=None):
+    """Paged attention over an fp8 (e4m3) cache (include/pkv.h,
+    pkv_attn_with_kvcache_fp8): ``k_cache`` / ``v_cache`` are
+    torch.float8_e4m3fn tensors, ``k_descale`` / ``v_descale`` optional fp32
+    [B, H_kv]; q (bf16) is rounded to e4m3 inside the kernel."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty(q.shape[0], q.shape[1], v_cache.shape[-1], dtype=torch.bfloat16,
+                          device=q.device)
+    if return_softmax_lse and lse is None:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    ws_bytes = attn_workspace_size(q, k_cache, v_cache, page_table, cache_seqlens,
+                                   max_seqlen_q)
+    if ws_bytes > 0 and (workspace is None or workspace.numel() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if ws_bytes > 0 else None
+    _check("pkv_attn_with_kvcache_fp8", lib.pkv_attn_with_kvcache_fp8(
+        _desc(q), _desc(k_cache), _desc(v_cache), _desc(page_table), _desc(cache_seqlens),
+        _desc(cu_seqlens_q), int(max_seqlen_q), float(softmax_scale), int(bool(causal)),
+        int(window_left), _descale_ptr(k_descale, cache_seqlens, k_cache),
+        _descale_ptr(v_descale, cache_seqlens, k_cache), 0, _desc(out), _desc(lse),
+        ws_ptr, ws_bytes, _stream(q)))
     return (out, lse) if return_softmax_lse else out
 
 

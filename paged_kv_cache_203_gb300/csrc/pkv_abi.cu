@@ -99,7 +99,10 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
                    const pkv_tensor &v, const pkv_tensor &pt,
                    const pkv_tensor &cs, int max_seqlen_q,
                    const pkv_tensor &topk, int num_splits, AttnPlan *plan) {
-  if (!has(q, PKV_BF16, 3) || !has(k, PKV_BF16, 4) || !has(v, PKV_BF16, 4) ||
+  // the cache is bf16, or fp8 e4m3 codes (both tensors the same)
+  const bool fp8 = k.data != nullptr && k.dtype == PKV_FP8_E4M3;
+  const int kv_dtype = fp8 ? PKV_FP8_E4M3 : PKV_BF16;
+  if (!has(q, PKV_BF16, 3) || !has(k, kv_dtype, 4) || !has(v, kv_dtype, 4) ||
       !has(pt, PKV_I32, 2) || !has(cs, PKV_I32, 1))
     return PKV_ERR_INVALID_ARG;
   const int64_t total_q = q.shape[0], h_q = q.shape[1], d = q.shape[2];
@@ -114,7 +117,8 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
   if (pt.shape[0] != batch || pt.stride[1] != 1 || cs.stride[0] != 1)
     return PKV_ERR_INVALID_ARG;
   if (max_seqlen_q < 0 || num_splits < 0) return PKV_ERR_INVALID_ARG;
-  if (!vec_ok(q, 2) || !vec_ok(k, 2) || !vec_ok(v, 2)) return PKV_ERR_INVALID_ARG;
+  if (!vec_ok(q, 2) || !vec_ok(k, fp8 ? 1 : 2) || !vec_ok(v, fp8 ? 1 : 2))
+    return PKV_ERR_INVALID_ARG;
   if (present(topk)) {
     if (!has(topk, PKV_I32, 2) || topk.shape[0] != total_q || topk.stride[1] != 1)
       return PKV_ERR_INVALID_ARG;
@@ -123,6 +127,40 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
 
   const int group = static_cast<int>(h_q / h_kv);
   const bool mla = d == 576 && dv == 512;
+  if (fp8) {
+    // fp8 caches: the all-heads decode kernel with page boxes and its
+    // balanced schedule (head dim 128, <= 8 KV heads, <= 16 query rows per KV
+    // head, page size a multiple of 16), the library's split choice
+    if (present(topk) || d != 128 || dv != 128 || num_splits != 0 || batch > kDecodeBalancedMaxBatch)
+      return PKV_ERR_UNSUPPORTED;
+    AttnParams lp{};
+    lp.d = 128;
+    lp.dv = 128;
+    lp.h_q = static_cast<int>(h_q);
+    lp.h_kv = static_cast<int>(h_kv);
+    lp.group = group;
+    lp.max_seqlen_q = max_seqlen_q;
+    lp.page_size = static_cast<int>(page);
+    lp.num_pages = num_pages;
+    lp.k = static_cast<const bf16 *>(k.data);
+    lp.v = static_cast<const bf16 *>(v.data);
+    lp.k_sp = k.stride[0];
+    lp.k_spos = k.stride[1];
+    lp.k_sh = k.stride[2];
+    lp.v_sp = v.stride[0];
+    lp.v_spos = v.stride[1];
+    lp.v_sh = v.stride[2];
+    lp.kv_fp8 = 1;
+    if (max_seqlen_q < 1 || !decode_allheads_eligible(lp)) return PKV_ERR_UNSUPPORTED;
+    plan->kind = 3;
+    plan->num_splits = 0;
+    plan->n_row_tiles = 1;
+    const size_t slots = 2ull * kDecodeBalancedCtas * max_seqlen_q * h_q;
+    plan->ws_o_bytes = align256(slots * dv * 4);
+    plan->ws_lse_bytes = align256(slots * 4);
+    plan->ws_ctr_bytes = align256(static_cast<size_t>(batch) * h_kv * 4);
+    return PKV_OK;
+  }
   if (mla) {
     // absorbed MLA over top-k lists: 128 heads, one latent head, V = the
     // first 512 columns of the K rows (same buffer and row strides)
@@ -252,13 +290,16 @@ int pkv_attn_workspace_size(pkv_tensor q, pkv_tensor k_cache,
   return PKV_OK;
 }
 
-int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
-                          pkv_tensor page_table, pkv_tensor cache_seqlens,
-                          pkv_tensor cu_seqlens_q, int max_seqlen_q,
-                          float scale, int causal, int window_left,
-                          pkv_tensor topk_indices, int num_splits,
-                          pkv_tensor out, pkv_tensor lse, void *workspace,
-                          size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+int attn_impl(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache, pkv_tensor page_table,
+              pkv_tensor cache_seqlens, pkv_tensor cu_seqlens_q, int max_seqlen_q,
+              float scale, int causal, int window_left, pkv_tensor topk_indices,
+              int num_splits, pkv_tensor k_descale, pkv_tensor v_descale, pkv_tensor out,
+              pkv_tensor lse, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
   AttnPlan plan;
   int rc = plan_attention(q, k_cache, v_cache, page_table, cache_seqlens,
                           max_seqlen_q, topk_indices, num_splits, &plan);
@@ -275,6 +316,14 @@ int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
                        lse.shape[1] != q.shape[1]))
     return PKV_ERR_INVALID_ARG;
   if (window_left < -1 || !isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  const bool fp8 = k_cache.dtype == PKV_FP8_E4M3;
+  for (const pkv_tensor *ds : {&k_descale, &v_descale}) {
+    if (!present(*ds)) continue;
+    if (!fp8 || !has(*ds, PKV_F32, 2) || ds->shape[0] != batch ||
+        ds->shape[1] != k_cache.shape[2] || ds->stride[1] != 1 ||
+        ds->stride[0] != k_cache.shape[2])
+      return PKV_ERR_INVALID_ARG;
+  }
   if (plan.total() > 0 && (workspace == nullptr || workspace_bytes < plan.total() ||
                            (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
     return PKV_ERR_WORKSPACE;
@@ -328,6 +377,9 @@ int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
   p.num_splits = plan.num_splits;
   p.n_row_tiles = plan.n_row_tiles;
   p.err = err;
+  p.kv_fp8 = fp8 ? 1 : 0;
+  p.k_descale = static_cast<const float *>(k_descale.data);
+  p.v_descale = static_cast<const float *>(v_descale.data);
   if (plan.split()) {
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.ws_o = reinterpret_cast<float *>(ws);
@@ -346,6 +398,52 @@ int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
     p.num_splits = 1;  // otherwise the unsplit decode kernel (no workspace)
   }
   return launch_decode_gqa(p, stream);
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
+                          pkv_tensor page_table, pkv_tensor cache_seqlens,
+                          pkv_tensor cu_seqlens_q, int max_seqlen_q,
+                          float scale, int causal, int window_left,
+                          pkv_tensor topk_indices, int num_splits,
+                          pkv_tensor out, pkv_tensor lse, void *workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  const pkv_tensor none{};
+  return pkv::attn_impl(q, k_cache, v_cache, page_table, cache_seqlens, cu_seqlens_q,
+                        max_seqlen_q, scale, causal, window_left, topk_indices, num_splits,
+                        none, none, out, lse, workspace, workspace_bytes, stream);
+}
+
+int pkv_attn_with_kvcache_fp8(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
+                              pkv_tensor page_table, pkv_tensor cache_seqlens,
+                              pkv_tensor cu_seqlens_q, int max_seqlen_q, float scale,
+                              int causal, int window_left, const float *k_descale,
+                              const float *v_descale, int num_splits, pkv_tensor out,
+                              pkv_tensor lse, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+  if (k_cache.data == nullptr || k_cache.dtype != PKV_FP8_E4M3 || k_cache.ndim != 4 ||
+      cache_seqlens.data == nullptr || cache_seqlens.ndim != 1)
+    return PKV_ERR_INVALID_ARG;
+  const pkv_tensor none{};
+  // the descales as [B][H_kv] fp32 descriptors (contiguous rows)
+  pkv_tensor kd{}, vd{};
+  for (int i = 0; i < 2; ++i) {
+    pkv_tensor &t = i == 0 ? kd : vd;
+    t.data = const_cast<float *>(i == 0 ? k_descale : v_descale);
+    t.dtype = PKV_F32;
+    t.ndim = 2;
+    t.shape[0] = cache_seqlens.shape[0];
+    t.shape[1] = k_cache.shape[2];
+    t.stride[0] = k_cache.shape[2];
+    t.stride[1] = 1;
+  }
+  return pkv::attn_impl(q, k_cache, v_cache, page_table, cache_seqlens, cu_seqlens_q,
+                        max_seqlen_q, scale, causal, window_left, none, num_splits, kd, vd,
+                        out, lse, workspace, workspace_bytes, stream);
 }
 
 int pkv_merge_state(pkv_tensor v_a, pkv_tensor lse_a, pkv_tensor v_b,

@@ -37,6 +37,7 @@
 //  * Every mbarrier wait is bounded; on expiry the kernel sets
 //    PKV_EFLAG_TIMEOUT and leaves the loop instead of hanging.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <string.h>
 
 #include "pkv_internal.h"
@@ -149,6 +150,39 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0,
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col)
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                        uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Two e4m3 codes (low byte first) to f16x2, exactly (e4m3 values are f16 values).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  const uint16_t v = static_cast<uint16_t>(two_codes & 0xffffu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(v));
+  return r;
+}
+// (lo, hi) rounded to e4m3 (nearest even, saturating), widened to f16x2.
+__device__ __forceinline__ uint32_t round_e4m3_f16x2(float lo, float hi) {
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(c) : "f"(hi), "f"(lo));
+  return e4m3x2_to_f16x2(c);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -795,9 +829,12 @@ struct AhLayout {
   uint32_t stage;  // bytes of one K (or V) stage
   uint32_t k, v, pos, meta, ring_pg, ring_j, voff, pre, scan, bar, end;
 };
-__host__ __device__ inline AhLayout ah_layout(int hpc, bool boxes, bool balanced) {
+__host__ __device__ inline AhLayout ah_layout(int hpc, bool boxes, bool balanced,
+                                              bool fp8 = false) {
   AhLayout L;
-  L.stage = boxes ? static_cast<uint32_t>(hpc) * AH_BK * 256u
+  // page boxes: [head][16 positions][128 B] per 64-column half (bf16) or for
+  // all 128 columns (fp8 codes)
+  L.stage = boxes ? static_cast<uint32_t>(hpc) * AH_BK * (fp8 ? 128u : 256u)
                   : AH_BK * (static_cast<uint32_t>(hpc) * 256u + 16u);
   L.k = 0;
   L.v = L.k + AH_NSTAGE * L.stage;
@@ -870,10 +907,11 @@ __device__ __forceinline__ int ah_cta_of(int64_t x, int64_t g, int64_t t) {
   return static_cast<int>(((x + 1) * g - 1) / t);
 }
 
-template <bool BOXES>
+template <bool BOXES, bool FP8>
 __global__ void __launch_bounds__((AH_MAXH + 1) * 32, 1)
 decode_allheads_kernel(const __grid_constant__ AttnParams p,
                        const __grid_constant__ AhMaps maps) {
+  static_assert(BOXES || !FP8, "fp8 caches use page boxes");
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -882,7 +920,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   const int hpc = nthreads / 32 - 1;  // KV heads of this CTA = consumer warps
   const int head0 = blockIdx.y * hpc;  // its first KV head
   const bool balanced = p.num_splits == 0;
-  const AhLayout L = ah_layout(hpc, BOXES, balanced);
+  const AhLayout L = ah_layout(hpc, BOXES, balanced, FP8);
   const uint32_t sbase = smem_addr(smem);
   if (BOXES && (sbase & 1023u) != 0) {  // swizzled boxes need a 1024-byte aligned base
     if (tid == 0) atomicOr(p.err, PKV_EFLAG_LAYOUT);
@@ -1085,11 +1123,16 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
         if (lane == 0) {
           mbar_arrive_expect_tx(full, page >= 0 ? 2u * L.stage : 0u);
           if (page >= 0) {
-            const uint32_t half = L.stage / 2;
+            if (FP8) {  // one box of all 128 columns (bytes) per tensor
+              tma_load_4d(kdst, &maps.k, 0, inpage0, head0, page, full);
+              tma_load_4d(vdst, &maps.v, 0, inpage0, head0, page, full);
+            } else {
+              const uint32_t half = L.stage / 2;
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              tma_load_4d(kdst + hf * half, &maps.k, hf * 64, inpage0, head0, page, full);
-              tma_load_4d(vdst + hf * half, &maps.v, hf * 64, inpage0, head0, page, full);
+              for (int hf = 0; hf < 2; ++hf) {
+                tma_load_4d(kdst + hf * half, &maps.k, hf * 64, inpage0, head0, page, full);
+                tma_load_4d(vdst + hf * half, &maps.v, hf * 64, inpage0, head0, page, full);
+              }
             }
           }
         }
@@ -1126,7 +1169,10 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   const int64_t rows_req = static_cast<int64_t>(p.max_seqlen_q) * p.h_q;  // balanced slots
   const bool use_upper = p.causal || p.window_left >= 0;
   // byte offset of 16-byte chunk c of key `key` of this head within a stage
+  // (fp8: chunk c holds the 16 codes of columns 16c..16c+15)
   auto soff = [&](int key, int c) -> uint32_t {
+    if (FP8)
+      return static_cast<uint32_t>(w * 2048 + key * 128 + (((c & 7) ^ (key & 7)) << 4));
     if (BOXES)
       return static_cast<uint32_t>((c >> 3) * (hpc * 2048) + w * 2048 + key * 128 +
                                    (((c & 7) ^ (key & 7)) << 4));
@@ -1139,6 +1185,8 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   int rpos[2];
   AhReq r{};
   int n_rows = 0;
+  float sl2 = p.scale_log2;  // softmax scale (log2 domain), times k_descale
+  float vdesc = 1.f;         // v_descale of the current request and head
   bool seg_req_start = false, first_seg = true;
 
   // Slot rows: this warp copies its head's 256-byte V slice of every key of
@@ -1188,10 +1236,33 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
                            static_cast<int64_t>(h * p.group + gg) * p.q_sh;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const int c0 = kk * 16 + 2 * tq;
-          qf[kk][hh] = rv ? *reinterpret_cast<const uint32_t *>(qrow + c0) : 0u;
-          qf[kk][2 + hh] = rv ? *reinterpret_cast<const uint32_t *>(qrow + c0 + 8) : 0u;
+          if (FP8) {
+            // q rounded to e4m3 (the cache's type), as f16; the four columns
+            // 16kk + 4tq .. +3 take the fragment's k slots 2tq, 2tq+1,
+            // 2tq+8, 2tq+9 (the K fragments use the same column order)
+            const int c0 = kk * 16 + 4 * tq;
+            uint32_t lo = 0u, hi = 0u;
+            if (rv) {
+              const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162 *>(qrow + c0);
+              const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162 *>(qrow + c0 + 2);
+              lo = round_e4m3_f16x2(__low2float(q01), __high2float(q01));
+              hi = round_e4m3_f16x2(__low2float(q23), __high2float(q23));
+            }
+            qf[kk][hh] = lo;
+            qf[kk][2 + hh] = hi;
+          } else {
+            const int c0 = kk * 16 + 2 * tq;
+            qf[kk][hh] = rv ? *reinterpret_cast<const uint32_t *>(qrow + c0) : 0u;
+            qf[kk][2 + hh] = rv ? *reinterpret_cast<const uint32_t *>(qrow + c0 + 8) : 0u;
+          }
         }
+      }
+      sl2 = p.scale_log2;
+      vdesc = 1.f;
+      if (FP8) {
+        const int64_t di = static_cast<int64_t>(b) * p.h_kv + h;
+        if (p.k_descale != nullptr) sl2 *= p.k_descale[di];
+        if (p.v_descale != nullptr) vdesc = p.v_descale[di];
       }
 #pragma unroll
       for (int nn = 0; nn < 16; ++nn) o[nn][0] = o[nn][1] = o[nn][2] = o[nn][3] = 0.f;
@@ -1205,10 +1276,11 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     // add exactly 0); slot rows arrive zero-filled
     const bool any_skipped = BOXES && __any_sync(0xffffffffu, pos_st[lane & 15] < 0);
     if (any_skipped) {
+      constexpr int kChunks = FP8 ? 8 : 16;  // 16-byte chunks per key row of the head
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < AH_BK * kChunks / 32; ++i) {
         const int idx = i * 32 + lane;
-        const int rr = idx >> 4, cc = idx & 15;
+        const int rr = idx / kChunks, cc = idx % kChunks;
         if (pos_st[rr] < 0)
           *reinterpret_cast<uint4 *>(smem + L.v + st * L.stage + soff(rr, cc)) =
               make_uint4(0, 0, 0, 0);
@@ -1219,7 +1291,18 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     float sc[2][4];
 #pragma unroll
     for (int nn = 0; nn < 2; ++nn) sc[nn][0] = sc[nn][1] = sc[nn][2] = sc[nn][3] = 0.f;
-    {
+    if (FP8) {
+      // keys g and g + 8: four codes (columns 16kk + 4tq ..) per 32-bit read
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t w0 = lds32(kb + soff(g, kk) + 4 * tq);
+        const uint32_t w1 = lds32(kb + soff(g + 8, kk) + 4 * tq);
+        mma_f16(sc[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], e4m3x2_to_f16x2(w0),
+                e4m3x2_to_f16x2(w0 >> 16));
+        mma_f16(sc[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], e4m3x2_to_f16x2(w1),
+                e4m3x2_to_f16x2(w1 >> 16));
+      }
+    } else {
       const int key = (lane >> 4) * 8 + (lane & 7);
       const int kc = (lane >> 3) & 1;
 #pragma unroll
@@ -1245,7 +1328,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
         bool masked = kp < 0;
         if (use_upper && kp > rpos[hh]) masked = true;
         if (p.window_left >= 0 && kp < rpos[hh] - p.window_left) masked = true;
-        sc[nn][e] = masked ? -INFINITY : sc[nn][e] * p.scale_log2;
+        sc[nn][e] = masked ? -INFINITY : sc[nn][e] * sl2;
       }
     float alpha[2];
 #pragma unroll
@@ -1276,15 +1359,36 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
         o[nn][3] *= alpha[1];
       }
     }
-    const uint32_t a0 = pack_bf16(sc[0][0], sc[0][1]);
-    const uint32_t a1 = pack_bf16(sc[0][2], sc[0][3]);
-    const uint32_t a2 = pack_bf16(sc[1][0], sc[1][1]);
-    const uint32_t a3 = pack_bf16(sc[1][2], sc[1][3]);
+    const uint32_t a0 = FP8 ? pack_f16(sc[0][0], sc[0][1]) : pack_bf16(sc[0][0], sc[0][1]);
+    const uint32_t a1 = FP8 ? pack_f16(sc[0][2], sc[0][3]) : pack_bf16(sc[0][2], sc[0][3]);
+    const uint32_t a2 = FP8 ? pack_f16(sc[1][0], sc[1][1]) : pack_bf16(sc[1][0], sc[1][1]);
+    const uint32_t a3 = FP8 ? pack_f16(sc[1][2], sc[1][3]) : pack_bf16(sc[1][2], sc[1][3]);
     if (!BOXES) {  // this tile's V slices (two later tiles' groups may be pending)
       cp_async_wait_group<2>();
       __syncwarp();
     }
-    {
+    if (FP8) {
+      // transposed 8x8 loads of code pairs: a register holds columns
+      // (2g, 2g+1) of keys (2tq, 2tq+1); its even and odd columns are the B
+      // operands of two n-blocks: block 2ch covers columns 16ch + 2n, block
+      // 2ch + 1 columns 16ch + 2n + 1
+      const int m = lane >> 3;
+      const int key = (m & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int cp = 0; cp < 4; ++cp) {
+        uint32_t r0, r1, r2, r3;  // keys 0-7 / 8-15 of chunks 2cp and 2cp + 1
+        ldsm_x4_t(vb + soff(key, 2 * cp + (m >> 1)), r0, r1, r2, r3);
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          const uint32_t lo = hc ? r2 : r0, hi = hc ? r3 : r1;
+          const int ch = 2 * cp + hc;
+          mma_f16(o[2 * ch], a0, a1, a2, a3, e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x4420)),
+                  e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x4420)));
+          mma_f16(o[2 * ch + 1], a0, a1, a2, a3, e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x4431)),
+                  e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x4431)));
+        }
+      }
+    } else {
       const int m = lane >> 3;
       const int key = (m & 1) * 8 + (lane & 7);
 #pragma unroll
@@ -1318,14 +1422,25 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
       const int u = rr / p.group;
       const int tok = r.q_begin + u;
       const int head = h * p.group + rr % p.group;
-      const float inv = Lsum[hh] > 0.f ? 1.f / Lsum[hh] : 0.f;
+      // (v_descale multiplies the output and every partial: merges are linear)
+      const float inv = Lsum[hh] > 0.f ? vdesc / Lsum[hh] : 0.f;
       const float lse_nat = Lsum[hh] > 0.f ? (m_run[hh] + log2f(Lsum[hh])) * kLn2 : -INFINITY;
       if (whole) {
         bf16 *dst = p.out + static_cast<int64_t>(tok) * p.o_st + static_cast<int64_t>(head) * p.o_sh;
+        if (FP8) {  // blocks 2ch / 2ch+1 hold the even / odd columns of 16ch..
 #pragma unroll
-        for (int nn = 0; nn < 16; ++nn)
-          *reinterpret_cast<uint32_t *>(dst + nn * 8 + 2 * tq) =
-              pack_bf16(o[nn][2 * hh] * inv, o[nn][2 * hh + 1] * inv);
+          for (int ch = 0; ch < 8; ++ch) {
+            uint2 w2;
+            w2.x = pack_bf16(o[2 * ch][2 * hh] * inv, o[2 * ch + 1][2 * hh] * inv);
+            w2.y = pack_bf16(o[2 * ch][2 * hh + 1] * inv, o[2 * ch + 1][2 * hh + 1] * inv);
+            *reinterpret_cast<uint2 *>(dst + ch * 16 + 4 * tq) = w2;
+          }
+        } else {
+#pragma unroll
+          for (int nn = 0; nn < 16; ++nn)
+            *reinterpret_cast<uint32_t *>(dst + nn * 8 + 2 * tq) =
+                pack_bf16(o[nn][2 * hh] * inv, o[nn][2 * hh + 1] * inv);
+        }
         if (p.lse != nullptr && tq == 0)
           p.lse[static_cast<int64_t>(tok) * p.lse_st + static_cast<int64_t>(head) * p.lse_sh] =
               lse_nat;
@@ -1336,10 +1451,18 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
                      : static_cast<int64_t>(blockIdx.x) * rows_total +
                            static_cast<int64_t>(tok) * p.h_q + head;
         float *dst = p.ws_o + widx * p.dv;
+        if (FP8) {
 #pragma unroll
-        for (int nn = 0; nn < 16; ++nn)
-          __stcg(reinterpret_cast<float2 *>(dst + nn * 8 + 2 * tq),
-                 make_float2(o[nn][2 * hh] * inv, o[nn][2 * hh + 1] * inv));
+          for (int ch = 0; ch < 8; ++ch)
+            __stcg(reinterpret_cast<float4 *>(dst + ch * 16 + 4 * tq),
+                   make_float4(o[2 * ch][2 * hh] * inv, o[2 * ch + 1][2 * hh] * inv,
+                               o[2 * ch][2 * hh + 1] * inv, o[2 * ch + 1][2 * hh + 1] * inv));
+        } else {
+#pragma unroll
+          for (int nn = 0; nn < 16; ++nn)
+            __stcg(reinterpret_cast<float2 *>(dst + nn * 8 + 2 * tq),
+                   make_float2(o[nn][2 * hh] * inv, o[nn][2 * hh + 1] * inv));
+        }
         if (tq == 0) __stcg(p.ws_lse + widx, lse_nat);
       }
     }
@@ -1484,29 +1607,33 @@ namespace {
 
 // 4-D map over a paged cache listing position before head (dims innermost
 // first: D, position, head, page), whatever the strides' order; one box =
-// one 64-column half of 16 positions of `hpc` heads of one page.
-bool encode_allheads_map(CUtensorMap *map, const bf16 *base, int h_kv, int page,
+// one 64-column half (bf16) or all 128 columns (fp8 codes, one byte each) of
+// 16 positions of `hpc` heads of one page: 128-byte rows either way.
+bool encode_allheads_map(CUtensorMap *map, const void *base, int h_kv, int page,
                          int64_t num_pages, int64_t s_head, int64_t s_pos, int64_t s_page,
-                         int hpc) {
+                         int hpc, bool fp8) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
+  const cuuint64_t eb = fp8 ? 1 : 2;
   cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(page), static_cast<cuuint64_t>(h_kv),
                         static_cast<cuuint64_t>(num_pages)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s_pos) * 2,
-                           static_cast<cuuint64_t>(s_head) * 2,
-                           static_cast<cuuint64_t>(s_page) * 2};
-  cuuint32_t box[4] = {64, AH_BK, static_cast<cuuint32_t>(hpc), 1};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s_pos) * eb,
+                           static_cast<cuuint64_t>(s_head) * eb,
+                           static_cast<cuuint64_t>(s_page) * eb};
+  cuuint32_t box[4] = {fp8 ? 128u : 64u, AH_BK, static_cast<cuuint32_t>(hpc), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<bf16 *>(base), dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+            const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool encode_allheads_maps(AhMaps *m, const AttnParams &p, int hpc) {
+  const bool fp8 = p.kv_fp8 != 0;
   return encode_allheads_map(&m->k, p.k, p.h_kv, p.page_size, p.num_pages, p.k_sh, p.k_spos,
-                             p.k_sp, hpc) &&
+                             p.k_sp, hpc, fp8) &&
          encode_allheads_map(&m->v, p.v, p.h_kv, p.page_size, p.num_pages, p.v_sh, p.v_spos,
-                             p.v_sp, hpc);
+                             p.v_sp, hpc, fp8);
 }
 
 }  // namespace
@@ -1514,6 +1641,7 @@ bool encode_allheads_maps(AhMaps *m, const AttnParams &p, int hpc) {
 bool decode_allheads_eligible(const AttnParams &p) {
   if (p.topk != nullptr || p.d != 128 || p.dv != 128) return false;
   if (p.h_kv > AH_MAXH || p.max_seqlen_q < 1 || p.max_seqlen_q * p.group > 16) return false;
+  if (p.kv_fp8 && p.page_size % AH_BK != 0) return false;  // fp8: page boxes only
   if (p.page_size < 8) {
     // slot rows: every slot's heads form one contiguous H_kv x 128 row
     return p.k_sh == 128 && p.k_spos == static_cast<int64_t>(p.h_kv) * 128 &&
@@ -1535,17 +1663,22 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
   // page boxes run the balanced schedule only: with fixed splits a CTA that
   // covers every head turns a long request's chunk into one long work item
   if (boxes && !balanced) return PKV_ERR_UNSUPPORTED;
+  const bool fp8 = p.kv_fp8 != 0;
+  if (fp8 && !boxes) return PKV_ERR_UNSUPPORTED;
   const int hpc = p.h_kv;
-  const AhLayout L = ah_layout(hpc, boxes, balanced);
+  const AhLayout L = ah_layout(hpc, boxes, balanced, fp8);
   if (L.end > AH_SMEM_MAX) return PKV_ERR_UNSUPPORTED;
   static bool configured[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (dev >= 64 || !configured[dev]) {
-    if (cudaFuncSetAttribute(decode_allheads_kernel<true>,
+    if (cudaFuncSetAttribute(decode_allheads_kernel<true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, AH_SMEM_MAX) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(decode_allheads_kernel<false>,
+        cudaFuncSetAttribute(decode_allheads_kernel<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, AH_SMEM_MAX) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(decode_allheads_kernel<true, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, AH_SMEM_MAX) !=
             cudaSuccess)
       return PKV_ERR_CUDA;
@@ -1558,10 +1691,12 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
   const dim3 grid = balanced ? dim3(kDecodeBalancedCtas, 1, 1)
                              : dim3(p.num_splits, 1, p.batch);
   const dim3 block((hpc + 1) * 32);
-  if (boxes)
-    decode_allheads_kernel<true><<<grid, block, L.end, stream>>>(p, maps);
+  if (fp8)
+    decode_allheads_kernel<true, true><<<grid, block, L.end, stream>>>(p, maps);
+  else if (boxes)
+    decode_allheads_kernel<true, false><<<grid, block, L.end, stream>>>(p, maps);
   else
-    decode_allheads_kernel<false><<<grid, block, L.end, stream>>>(p, maps);
+    decode_allheads_kernel<false, false><<<grid, block, L.end, stream>>>(p, maps);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

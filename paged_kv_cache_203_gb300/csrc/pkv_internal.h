@@ -50,6 +50,10 @@ struct AttnParams {
   float *ws_lse;                      // [splits][total_q][h_q] partial lse
   int32_t *ws_counter;                // [batch][h_kv][n_row_tiles]
   uint32_t *err;                      // device error word
+  // fp8 (e4m3) cache: k / v point at byte codes, strides still in elements
+  int kv_fp8;
+  const float *k_descale;             // optional [batch][h_kv]
+  const float *v_descale;             // optional [batch][h_kv]
 };
 
 // Error word of the current device (static __device__ in pkv_abi.cu).

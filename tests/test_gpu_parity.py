@@ -993,3 +993,90 @@ def test_append_then_attend(kind):
     ref_o, ref_l, _ = oracle_attn(wl)
     check_close(out, lse, ref_o, ref_l, f"append+attend {kind}")
     assert pkv.get_error_flags() == 0
+
+
+# ------------------------------------------------------------------ FP8 KV
+
+def _to_fp8(t):
+    return t.float().to(torch.float8_e4m3fn)
+
+
+def _fp8_run(wl, descale=True, seed=0, entry="fp8"):
+    """GPU fp8 attention and the oracle's, on the workload's cache cast to
+    e4m3 codes; per-(request, KV head) descales drawn in [0.5, 2)."""
+    B, h_kv = wl.cache_seqlens.shape[0], wl.k_cache.shape[2]
+    k8, v8 = _to_fp8(wl.k_cache), _to_fp8(wl.v_cache)
+    gen = torch.Generator().manual_seed(seed)
+    kd = (torch.rand(B, h_kv, generator=gen) * 1.5 + 0.5) if descale else None
+    vd = (torch.rand(B, h_kv, generator=gen) * 1.5 + 0.5) if descale else None
+    g = wl.to(DEV)
+    if entry == "fp8":
+        out, lse = pkv.attn_with_kvcache_fp8(
+            g.q, k8.to(DEV), v8.to(DEV), g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+            g.max_seqlen_q, g.scale, causal=g.causal,
+            k_descale=None if kd is None else kd.to(DEV),
+            v_descale=None if vd is None else vd.to(DEV), return_softmax_lse=True)
+    else:  # the bf16 entry point with an fp8 cache: descales of 1
+        out, lse = pkv.attn_with_kvcache(
+            g.q, k8.to(DEV), v8.to(DEV), g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+            g.max_seqlen_q, g.scale, causal=g.causal, return_softmax_lse=True)
+    torch.cuda.synchronize()
+    ref_o, ref_l, _ = oracle.attention_fp8(
+        oracle.bf16_bits(wl.q), k8.view(torch.uint8).numpy(), v8.view(torch.uint8).numpy(),
+        wl.page_table.numpy(), wl.cache_seqlens.numpy(), wl.cu_seqlens_q.numpy(), wl.scale,
+        causal=wl.causal, k_descale=None if kd is None else kd.numpy(),
+        v_descale=None if vd is None else vd.numpy())
+    return out, lse, ref_o, ref_l
+
+
+@pytest.mark.parametrize("page_size,h_q,q_len", [(16, 32, 1), (64, 32, 2), (16, 64, 2)])
+def test_fp8_decode(page_size, h_q, q_len):
+    """FP8 cache (e4m3 codes), per-(request, KV head) descales, q cast to
+    e4m3 in the kernel: GQA decode shapes, 8 KV heads, head dim 128, up to 16
+    query rows per KV head, ragged lengths (the balanced schedule splits the
+    long requests over CTAs)."""
+    wl = workloads.make("tiny_decode", d=128, page_size=page_size, h_q=h_q, h_kv=8,
+                        q_len=q_len, causal=q_len > 1, batch=24, len_lo=q_len,
+                        len_hi=3000, pool_tokens=24 * 3072 + 256, seed=101 + page_size)
+    out, lse, ref_o, ref_l = _fp8_run(wl, seed=page_size)
+    check_close(out, lse, ref_o, ref_l, f"fp8 P={page_size} h_q={h_q} q_len={q_len}")
+    assert pkv.get_error_flags() == 0
+
+
+def test_fp8_unit_descale_entry_and_edges():
+    """The bf16 entry point with an fp8 cache (descales of 1); a request with
+    no keys (0 / -inf); a page id outside the pool (its keys skipped, V rows
+    zeroed, the flag set)."""
+    wl = workloads.make("tiny_decode", d=128, page_size=16, h_q=16, h_kv=4, batch=12,
+                        len_lo=0, len_hi=900, pool_tokens=12 * 912 + 64, seed=111)
+    wl.cache_seqlens[3] = 0
+    out, lse, ref_o, ref_l = _fp8_run(wl, descale=False, entry="bf16")
+    check_close(out, lse, ref_o, ref_l, "fp8 unit descales")
+    assert pkv.get_error_flags() == 0
+    n_pages = wl.k_cache.shape[0]
+    wl.page_table[5, 1] = n_pages + 7  # the second page of request 5 is bad
+    wl.cache_seqlens[5] = max(int(wl.cache_seqlens[5]), 40)
+    out, lse, ref_o, ref_l = _fp8_run(wl, seed=3)
+    check_close(out, lse, ref_o, ref_l, "fp8 bad page")
+    assert pkv.get_error_flags() & pkv.EFLAG_PAGE_OOB
+
+
+def test_fp8_unsupported_shapes_are_refused():
+    """Shapes outside the fp8 path return PKV_ERR_UNSUPPORTED: page size 1,
+    fixed splits."""
+    wl = workloads.make("tiny_decode", d=128, page_size=1, h_q=8, h_kv=2, batch=2,
+                        len_lo=10, len_hi=50, pool_tokens=256, seed=112)
+    g = wl.to(DEV)
+    k8, v8 = _to_fp8(g.k_cache), _to_fp8(g.v_cache)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.attn_with_kvcache_fp8(g.q, k8, v8, g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+                                  g.max_seqlen_q, g.scale)
+    assert e.value.code == -2
+    wl = workloads.make("tiny_decode", d=128, page_size=16, h_q=8, h_kv=2, batch=2,
+                        len_lo=10, len_hi=50, pool_tokens=512, seed=113)
+    g = wl.to(DEV)
+    k8, v8 = _to_fp8(g.k_cache), _to_fp8(g.v_cache)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.attn_with_kvcache(g.q, k8, v8, g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+                              g.max_seqlen_q, g.scale, num_splits=2)
+    assert e.value.code == -2
