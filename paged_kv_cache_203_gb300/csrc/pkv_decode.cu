@@ -169,11 +169,22 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(v));
   return r;
 }
-// (lo, hi) rounded to e4m3 (nearest even, saturating), widened to f16x2.
-__device__ __forceinline__ uint32_t round_e4m3_f16x2(float lo, float hi) {
+// (lo, hi) rounded to e4m3 (nearest even, saturating): lo in the low byte.
+__device__ __forceinline__ uint32_t round_e4m3x2(float lo, float hi) {
   uint16_t c;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(c) : "f"(hi), "f"(lo));
-  return e4m3x2_to_f16x2(c);
+  return c;
+}
+// D(16x8, f32) += A(16x32, e4m3, row) * B(32x8, e4m3, col); four codes per
+// register, the lowest k in the lowest byte.
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1,
+                                         uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
@@ -1237,19 +1248,24 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           if (FP8) {
-            // q rounded to e4m3 (the cache's type), as f16; the four columns
-            // 16kk + 4tq .. +3 take the fragment's k slots 2tq, 2tq+1,
-            // 2tq+8, 2tq+9 (the K fragments use the same column order)
-            const int c0 = kk * 16 + 4 * tq;
-            uint32_t lo = 0u, hi = 0u;
-            if (rv) {
-              const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162 *>(qrow + c0);
-              const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162 *>(qrow + c0 + 2);
-              lo = round_e4m3_f16x2(__low2float(q01), __high2float(q01));
-              hi = round_e4m3_f16x2(__low2float(q23), __high2float(q23));
+            // q rounded to e4m3 (the cache's type): the m16n8k32 A fragment,
+            // columns 32kk + 4tq .. +3 and 32kk + 16 + 4tq .. +3 (kk < 4)
+            if (kk < 4) {
+              uint32_t pk[2] = {0u, 0u};
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const int c0 = kk * 32 + half * 16 + 4 * tq;
+                if (rv) {
+                  const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162 *>(qrow + c0);
+                  const __nv_bfloat162 q23 =
+                      *reinterpret_cast<const __nv_bfloat162 *>(qrow + c0 + 2);
+                  pk[half] = round_e4m3x2(__low2float(q01), __high2float(q01)) |
+                             (round_e4m3x2(__low2float(q23), __high2float(q23)) << 16);
+                }
+              }
+              qf[kk][hh] = pk[0];
+              qf[kk][2 + hh] = pk[1];
             }
-            qf[kk][hh] = lo;
-            qf[kk][2 + hh] = hi;
           } else {
             const int c0 = kk * 16 + 2 * tq;
             qf[kk][hh] = rv ? *reinterpret_cast<const uint32_t *>(qrow + c0) : 0u;
@@ -1292,15 +1308,15 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
 #pragma unroll
     for (int nn = 0; nn < 2; ++nn) sc[nn][0] = sc[nn][1] = sc[nn][2] = sc[nn][3] = 0.f;
     if (FP8) {
-      // keys g and g + 8: four codes (columns 16kk + 4tq ..) per 32-bit read
+      // e4m3 MMAs on the codes as they lie: for keys g and g + 8, four codes
+      // of columns 32kk + 4tq .. and 32kk + 16 + 4tq .. per 32-bit read
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t w0 = lds32(kb + soff(g, kk) + 4 * tq);
-        const uint32_t w1 = lds32(kb + soff(g + 8, kk) + 4 * tq);
-        mma_f16(sc[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], e4m3x2_to_f16x2(w0),
-                e4m3x2_to_f16x2(w0 >> 16));
-        mma_f16(sc[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], e4m3x2_to_f16x2(w1),
-                e4m3x2_to_f16x2(w1 >> 16));
+      for (int kk = 0; kk < 4; ++kk) {
+        mma_e4m3(sc[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3],
+                 lds32(kb + soff(g, 2 * kk) + 4 * tq), lds32(kb + soff(g, 2 * kk + 1) + 4 * tq));
+        mma_e4m3(sc[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3],
+                 lds32(kb + soff(g + 8, 2 * kk) + 4 * tq),
+                 lds32(kb + soff(g + 8, 2 * kk + 1) + 4 * tq));
       }
     } else {
       const int key = (lane >> 4) * 8 + (lane & 7);
