@@ -1080,3 +1080,66 @@ def test_fp8_unsupported_shapes_are_refused():
         pkv.attn_with_kvcache(g.q, k8, v8, g.page_table, g.cache_seqlens, g.cu_seqlens_q,
                               g.max_seqlen_q, g.scale, num_splits=2)
     assert e.value.code == -2
+
+
+# ------------------------------------------------------- CUDA graph capture
+
+def test_paths_replay_from_cuda_graphs_with_new_lengths():
+    """Decode and local attention (device-built virtual requests) need no
+    host work inside a call: both are captured once into a CUDA graph, the
+    request lengths are changed in place, and the replay's results equal the
+    oracle's for the new lengths."""
+    wl = workloads.make("tiny_decode", d=128, page_size=16, h_q=32, h_kv=8, batch=8,
+                        len_lo=64, len_hi=1500, pool_tokens=8 * 1536 + 64, seed=121)
+    g = wl.to(DEV)
+    P = 16
+    cap = pkv.local_virtual_batch_capacity(8, g.q.shape[0], 1, P)
+    out_d = torch.empty(g.q.shape[0], 32, 128, dtype=torch.bfloat16, device=DEV)
+    lse_d = torch.empty(g.q.shape[0], 32, dtype=torch.float32, device=DEV)
+    ws = torch.empty(max(1, pkv.attn_workspace_size(g.q, g.k_cache, g.v_cache, g.page_table,
+                                                    g.cache_seqlens, 1)),
+                     dtype=torch.uint8, device=DEV)
+    out_l = torch.empty_like(out_d)
+    lse_l = torch.empty_like(lse_d)
+    bufs = (torch.empty(cap, dtype=torch.int32, device=DEV),
+            torch.empty(cap + 1, dtype=torch.int32, device=DEV),
+            torch.empty(cap, dtype=torch.int32, device=DEV),
+            torch.empty(cap, 512 // P, dtype=torch.int32, device=DEV),
+            torch.empty(4, dtype=torch.int32, device=DEV))
+    ws_l = torch.empty(max(1, pkv.attn_workspace_size(g.q, g.k_cache, g.v_cache, bufs[3],
+                                                      bufs[2], 1)),
+                       dtype=torch.uint8, device=DEV)
+
+    def run():
+        pkv.attn_with_kvcache(g.q, g.k_cache, g.v_cache, g.page_table, g.cache_seqlens,
+                              g.cu_seqlens_q, 1, g.scale, out=out_d, lse=lse_d, workspace=ws)
+        pkv.make_local_attention_virtual_batches(512, P, g.cu_seqlens_q, g.cache_seqlens,
+                                                 g.page_table, cap, out=bufs)
+        pkv.attn_with_kvcache(g.q, g.k_cache, g.v_cache, bufs[3], bufs[2], bufs[1], 1, g.scale,
+                              causal=True, out=out_l, lse=lse_l, workspace=ws_l)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    own = wl.cache_seqlens.clone()  # lengths stay within each request's pages
+    for trial in range(2):
+        frac = torch.rand(8, generator=torch.Generator().manual_seed(trial))
+        new_len = (1 + (frac * own.float()).long()).clamp(max=own.long())
+        wl.cache_seqlens.copy_(new_len.to(torch.int32))
+        g.cache_seqlens.copy_(wl.cache_seqlens.to(DEV))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref_o, ref_l, _ = oracle_attn(wl, causal=False)
+        check_close(out_d, lse_d, ref_o, ref_l, f"graph decode {trial}")
+        eff = oracle.local_virtual_batches(512, P, wl.cu_seqlens_q.numpy(),
+                                           wl.cache_seqlens.numpy(),
+                                           wl.page_table.numpy())["chunk"]
+        ref_o, ref_l, _ = oracle_attn(wl, causal=True, attn_chunk=eff)
+        check_close(out_l, lse_l, ref_o, ref_l, f"graph local {trial}")
+    assert pkv.get_error_flags() == 0
