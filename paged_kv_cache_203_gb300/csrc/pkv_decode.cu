@@ -822,6 +822,8 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
 
 constexpr int AH_BK = 16;        // keys per tile (= per stage)
 constexpr int AH_NSTAGE = 3;
+// fp8 stages hold half the bytes; twice as many keep as many bytes in flight
+constexpr int AH_NSTAGE_FP8 = 6;
 constexpr int AH_LOOKAHEAD = 4;  // tiles the page-id fetch runs ahead of the copies
 constexpr int AH_RING = AH_LOOKAHEAD + 1;
 constexpr int AH_MAXH = 8;       // KV heads per CTA (one consumer warp each)
@@ -843,21 +845,22 @@ struct AhLayout {
 __host__ __device__ inline AhLayout ah_layout(int hpc, bool boxes, bool balanced,
                                               bool fp8 = false) {
   AhLayout L;
+  const int ns = fp8 ? AH_NSTAGE_FP8 : AH_NSTAGE;
   // page boxes: [head][16 positions][128 B] per 64-column half (bf16) or for
   // all 128 columns (fp8 codes)
   L.stage = boxes ? static_cast<uint32_t>(hpc) * AH_BK * (fp8 ? 128u : 256u)
                   : AH_BK * (static_cast<uint32_t>(hpc) * 256u + 16u);
   L.k = 0;
-  L.v = L.k + AH_NSTAGE * L.stage;
-  L.pos = L.v + AH_NSTAGE * L.stage;  // int [NSTAGE][BK]
-  L.meta = L.pos + AH_NSTAGE * AH_BK * 4;  // int [NSTAGE][2]
-  L.ring_pg = L.meta + AH_NSTAGE * 8;  // int [RING][BK] page ids
+  L.v = L.k + ns * L.stage;
+  L.pos = L.v + ns * L.stage;  // int [NSTAGE][BK]
+  L.meta = L.pos + ns * AH_BK * 4;  // int [NSTAGE][2]
+  L.ring_pg = L.meta + ns * 8;  // int [RING][BK] page ids
   L.ring_j = L.ring_pg + AH_RING * AH_BK * 4;  // int [RING][BK] key or -1
   L.voff = (L.ring_j + AH_RING * AH_BK * 4 + 7) & ~7u;  // int64 [NSTAGE][BK] (slot rows)
-  L.pre = L.voff + AH_NSTAGE * AH_BK * 8;  // int64 [MAXB + 1]
+  L.pre = L.voff + ns * AH_BK * 8;  // int64 [MAXB + 1]
   L.scan = L.pre + (balanced ? (AH_MAXB + 1) * 8 : 0);  // int64 [16]
   L.bar = L.scan + 16 * 8;
-  L.end = L.bar + 3 * AH_NSTAGE * 8;  // full, empty, V offsets published
+  L.end = L.bar + 3 * ns * 8;  // full, empty, V offsets published
   return L;
 }
 static_assert(AH_NSTAGE * 2 * (AH_BK * (AH_MAXH * 256 + 16)) + 18 * 1024 <= AH_SMEM_MAX,
@@ -923,6 +926,7 @@ __global__ void __launch_bounds__((AH_MAXH + 1) * 32, 1)
 decode_allheads_kernel(const __grid_constant__ AttnParams p,
                        const __grid_constant__ AhMaps maps) {
   static_assert(BOXES || !FP8, "fp8 caches use page boxes");
+  constexpr int NST = FP8 ? AH_NSTAGE_FP8 : AH_NSTAGE;  // ring stages
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -942,14 +946,14 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   int64_t *sPre = reinterpret_cast<int64_t *>(smem + L.pre);
   int64_t *sScan = reinterpret_cast<int64_t *>(smem + L.scan);
   const uint32_t full0 = sbase + L.bar;
-  const uint32_t empty0 = full0 + AH_NSTAGE * 8;
-  const uint32_t vmeta0 = empty0 + AH_NSTAGE * 8;
+  const uint32_t empty0 = full0 + NST * 8;
+  const uint32_t vmeta0 = empty0 + NST * 8;
   int64_t *sVoff = reinterpret_cast<int64_t *>(smem + L.voff);
   const uint32_t row_bytes = static_cast<uint32_t>(hpc) * 256u;  // the CTA's heads of one key
   const uint32_t pitch = row_bytes + 16u;                         // slot-row mode
 
   if (tid == 0) {
-    for (int s = 0; s < AH_NSTAGE; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, hpc);
       mbar_init(vmeta0 + 8 * s, 1);
@@ -1073,7 +1077,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
       if (x + 1 < n) advance(fb, ft, fr);
     }
     for (int kt = 0; kt < n; ++kt) {
-      const int st = kt % AH_NSTAGE;
+      const int st = kt % NST;
       if (kt + AH_LOOKAHEAD < n) fetch(kt + AH_LOOKAHEAD);
       else cp_async_commit();
       if (kt + AH_LOOKAHEAD + 1 < n) advance(fb, ft, fr);
@@ -1114,8 +1118,8 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
       if (t == r.ntiles - 1) flags |= AH_REQ_END;
 
       int ok = 1;
-      if (lane == 0 && kt >= AH_NSTAGE)
-        ok = mbar_wait(empty0 + 8 * st, ((kt / AH_NSTAGE) & 1) ^ 1) ? 1 : 0;
+      if (lane == 0 && kt >= NST)
+        ok = mbar_wait(empty0 + 8 * st, ((kt / NST) & 1) ^ 1) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
@@ -1206,8 +1210,8 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   // by this warp's own PV three tiles earlier.
   auto issue_v = [&](int x) -> bool {
     if (!BOXES && x < n) {
-      const int sx = x % AH_NSTAGE;
-      if (!mbar_wait(vmeta0 + 8 * sx, (x / AH_NSTAGE) & 1)) return false;
+      const int sx = x % NST;
+      if (!mbar_wait(vmeta0 + 8 * sx, (x / NST) & 1)) return false;
       const int c = lane & 15;
       const uint32_t vdst = sbase + L.v + sx * L.stage;
 #pragma unroll
@@ -1224,8 +1228,8 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   bool v_ok = issue_v(0) && issue_v(1);
 
   for (int kt = 0; v_ok && kt < n; ++kt) {
-    const int st = kt % AH_NSTAGE;
-    if (!mbar_wait(full0 + 8 * st, (kt / AH_NSTAGE) & 1) || !issue_v(kt + 2)) {
+    const int st = kt % NST;
+    if (!mbar_wait(full0 + 8 * st, (kt / NST) & 1) || !issue_v(kt + 2)) {
       if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
       break;
     }
