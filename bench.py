@@ -639,6 +639,7 @@ def main():
     # decode step); the attention kernel's own time comes from an eager loop
     # with events around it.
     graph = None
+    graph_note = "eager (--no-graph)"
     if not args.no_graph:
         try:
             side = torch.cuda.Stream(device=dev)
@@ -652,8 +653,10 @@ def main():
                 step.run()
             graph.replay()
             torch.cuda.synchronize()
-        except RuntimeError:
+        except RuntimeError as e:  # report why, time the step eagerly
             graph = None
+            graph_note = "eager (graph capture failed: %s)" % str(e).splitlines()[0][:200]
+            print(graph_note, file=sys.stderr, flush=True)
     pkv.clear_error_flags()
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -680,6 +683,8 @@ def main():
         step.run(evs[i])
     torch.cuda.synchronize()
     clk = clocks.stop()
+    step_launch = ("CUDA graph replay of the step (the library's calls captured once)"
+                   if graph is not None else graph_note)
     ms = t0.elapsed_time(t1) / args.steps
     attn_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
     flags = pkv.get_error_flags()
@@ -775,8 +780,7 @@ def main():
         g_cfg.pop("seed", None)
         g_cfg.update(parse_overrides(args.override))
         g_cfg["algorithmic_kv_bytes_per_step"] = step.kv_bytes
-        g_cfg["step_launch"] = ("CUDA graph replay of the step (the library's calls "
-                                "captured once)" if graph is not None else "eager")
+        g_cfg["step_launch"] = step_launch
         g_cfg["l2"] = ("inputs larger than L2: %.2f GB of K/V per step vs 129 MB L2"
                        % (step.kv_bytes / 1e9)) if step.kv_bytes > L2_BYTES else \
             "inputs smaller than L2 (no flush)"

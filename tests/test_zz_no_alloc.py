@@ -103,3 +103,26 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     assert e.value.code == -4
     torch.cuda.synchronize()
     assert torch.all(out == 7.0)
+
+
+def test_noalloc_serves_an_fp8_cache():
+    """The no-allocation entry point with an fp8 (e4m3) cache: descales of 1,
+    same answer as the regular entry point, nothing allocated."""
+    wl = workloads.make("tiny_decode", d=128, page_size=16, h_q=32, h_kv=8, batch=10,
+                        len_lo=1, len_hi=2000, pool_tokens=10 * 2016 + 64, seed=131)
+    g = wl.to(DEV)
+    k8 = g.k_cache.float().to(torch.float8_e4m3fn)
+    v8 = g.v_cache.float().to(torch.float8_e4m3fn)
+    out = torch.empty(g.q.shape[0], 32, 128, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(g.q.shape[0], 32, dtype=torch.float32, device=DEV)
+    torch.cuda.synchronize()
+    before = torch.cuda.memory_stats().get("allocation.all.allocated", 0)
+    pkv.attn_with_kvcache_noalloc(g.q, k8, v8, g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+                                  g.max_seqlen_q, g.scale, out, lse=lse)
+    after = torch.cuda.memory_stats().get("allocation.all.allocated", 0)
+    assert after == before
+    ref_o, ref_l = pkv.attn_with_kvcache_fp8(g.q, k8, v8, g.page_table, g.cache_seqlens,
+                                             g.cu_seqlens_q, g.max_seqlen_q, g.scale,
+                                             return_softmax_lse=True)
+    torch.cuda.synchronize()
+    _close(out, ref_o, lse, ref_l)
