@@ -1143,3 +1143,103 @@ def test_paths_replay_from_cuda_graphs_with_new_lengths():
         ref_o, ref_l, _ = oracle_attn(wl, causal=True, attn_chunk=eff)
         check_close(out_l, lse_l, ref_o, ref_l, f"graph local {trial}")
     assert pkv.get_error_flags() == 0
+
+
+# ------------------------------------ full-size checks of the composed rows
+
+def test_fp8_full_size_sampled_requests():
+    """The bench's fp8 line: the GQA decode batch (64 requests, 32/8 heads,
+    kv U[512, 8192]) with its cache cast to e4m3 and descales 0.75 / 1.25,
+    the library's split choice; eight whole requests (all their rows)
+    against the oracle."""
+    g = workloads.make("gqa_split_decode", value_device=DEV)
+    k8, v8 = g.k_cache.to(torch.float8_e4m3fn), g.v_cache.to(torch.float8_e4m3fn)
+    B, h_kv = g.cache_seqlens.shape[0], k8.shape[2]
+    kd = torch.full((B, h_kv), 0.75, device=DEV)
+    vd = torch.full((B, h_kv), 1.25, device=DEV)
+    out, lse = pkv.attn_with_kvcache_fp8(g.q, k8, v8, g.page_table, g.cache_seqlens,
+                                         g.cu_seqlens_q, g.max_seqlen_q, g.scale,
+                                         k_descale=kd, v_descale=vd, return_softmax_lse=True)
+    torch.cuda.synchronize()
+    pick = np.array([0, 7, 13, 22, 31, 40, 51, 63])      # decode: token b is request b
+    pt = g.page_table.cpu().numpy()[pick]
+    ks = g.cache_seqlens.cpu().numpy()[pick]
+    ref_o, ref_l, _ = oracle.attention_fp8(
+        oracle.bf16_bits(g.q[torch.from_numpy(pick).to(DEV)]), k8.view(torch.uint8).cpu().numpy(),
+        v8.view(torch.uint8).cpu().numpy(), pt, ks, np.arange(len(pick) + 1, dtype=np.int32),
+        g.scale, k_descale=kd.cpu().numpy()[pick], v_descale=vd.cpu().numpy()[pick])
+    idx = torch.from_numpy(pick).long()
+    check_close(out.cpu()[idx], lse.cpu()[idx], ref_o, ref_l, "fp8 full-size")
+    assert pkv.get_error_flags() == 0
+
+
+def test_local_attention_full_size_sampled():
+    """The bench's local-attention line: the GQA decode batch with 2048-key
+    chunks (device-built virtual requests, one attention call); sampled rows
+    against the oracle's chunk-masked attention."""
+    g = workloads.make("gqa_split_decode", value_device=DEV)
+    out, lse = pkv.local_attn_with_kvcache(g.q, g.k_cache, g.v_cache, g.page_table,
+                                           g.cache_seqlens, g.cu_seqlens_q, g.max_seqlen_q,
+                                           2048, g.scale, return_softmax_lse=True)
+    torch.cuda.synchronize()
+    rows = _sample_rows(g.q.shape[0], g.q.shape[1], 96, 7)
+    ref_o, ref_l, _ = oracle.attention(
+        oracle.bf16_bits(g.q), oracle.bf16_bits(g.k_cache), oracle.bf16_bits(g.v_cache),
+        g.page_table.cpu().numpy(), g.cache_seqlens.cpu().numpy(),
+        g.cu_seqlens_q.cpu().numpy(), g.scale, causal=True, attn_chunk=2048, rows=rows)
+    idx = torch.from_numpy(rows).long()
+    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
+                ref_o, ref_l, "local full-size sampled")
+    assert pkv.get_error_flags() == 0
+
+
+def test_cascade_full_size_sampled():
+    """The bench's cascade line: every request of the GQA decode batch also
+    sees a shared 4096-token prefix (pages 0-255 of the pool); sampled rows
+    against one oracle call over the prefix pages followed by the request's
+    own pages."""
+    g = workloads.make("gqa_split_decode", value_device=DEV)
+    B = g.cache_seqlens.shape[0]
+    pre_pt = torch.arange(256, dtype=torch.int32, device=DEV).repeat(B, 1).contiguous()
+    pre_len = torch.full((B,), 4096, dtype=torch.int32, device=DEV)
+    out, lse = pkv.cascade_attn_with_kvcache(g.q, g.k_cache, g.v_cache, pre_pt, pre_len,
+                                             g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+                                             g.max_seqlen_q, g.scale, causal=True,
+                                             return_softmax_lse=True)
+    torch.cuda.synchronize()
+    full_pt = torch.cat([pre_pt.cpu(), g.page_table.cpu()], dim=1).numpy()
+    full_len = (g.cache_seqlens.cpu() + 4096).numpy()
+    rows = _sample_rows(g.q.shape[0], g.q.shape[1], 96, 8)
+    ref_o, ref_l, _ = oracle.attention(
+        oracle.bf16_bits(g.q), oracle.bf16_bits(g.k_cache), oracle.bf16_bits(g.v_cache),
+        full_pt, full_len, g.cu_seqlens_q.cpu().numpy(), g.scale, causal=True, rows=rows)
+    idx = torch.from_numpy(rows).long()
+    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
+                ref_o, ref_l, "cascade full-size sampled")
+    assert pkv.get_error_flags() == 0
+
+
+def test_set_kv_buffer_full_size_bit_exact():
+    """The bench's KV-write line: the varlen extend workload's new rows
+    (10k tokens, 8 heads x 128) stored to their slots; both pools equal the
+    oracle's scatter bit for bit."""
+    g = workloads.make("varlen_extend", value_device=DEV)
+    P = g.page_size
+    cu = g.cu_seqlens_q.cpu().numpy()
+    kv = g.cache_seqlens.cpu().numpy()
+    pt = g.page_table.cpu().numpy()
+    loc = np.concatenate([pt[b, np.arange(kv[b] - (cu[b + 1] - cu[b]), kv[b]) // P] * P +
+                          np.arange(kv[b] - (cu[b + 1] - cu[b]), kv[b]) % P
+                          for b in range(len(kv))]).astype(np.int64)
+    gen = torch.Generator(device=DEV).manual_seed(5)
+    k_new = torch.randn(len(loc), 8, 128, device=DEV, generator=gen).to(torch.bfloat16)
+    v_new = torch.randn(len(loc), 8, 128, device=DEV, generator=gen).to(torch.bfloat16)
+    ref_k = _bits(g.k_cache).copy()
+    ref_v = _bits(g.v_cache).copy()
+    assert oracle.set_kv_buffer(ref_k, _bits(k_new), loc) == 0
+    assert oracle.set_kv_buffer(ref_v, _bits(v_new), loc) == 0
+    pkv.set_kv_buffer(g.k_cache, g.v_cache, torch.from_numpy(loc).to(DEV), k_new, v_new)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(g.k_cache), ref_k)
+    assert np.array_equal(_bits(g.v_cache), ref_v)
+    assert pkv.get_error_flags() == 0
