@@ -294,10 +294,43 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
   const int split = blockIdx.x;
   const int kvh = blockIdx.y / p.n_row_tiles;
   const int tile = blockIdx.y % p.n_row_tiles;
-  const int b = blockIdx.z;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+
+  // ---- longest requests first: blockIdx.z is a rank, not a request ----
+  // The grid's CTAs start in launch order and their key ranges differ by
+  // up to 16x, so request order leaves the longest chunks for the last wave.
+  // Every CTA ranks the requests by keys to read (descending, ties by index:
+  // a permutation) and serves the one whose rank is its blockIdx.z; the
+  // ranks live in the key-position ring, which the producer fills only after
+  // the barrier that follows the mbarrier setup.
+  int b = blockIdx.z;
+  if (p.batch > 1 && p.batch <= static_cast<int>(blockDim.x) && p.batch <= NSTAGE * BK) {
+    int *sWork = sPos;
+    int *sPick = reinterpret_cast<int *>(smem + S::kFlag + 8);
+    if (tid < p.batch) {
+      int w = 0;
+      if (p.topk == nullptr) {
+        w = p.cache_seqlens[tid];
+        if (p.window_left >= 0)
+          w = min(w, p.window_left + p.cu_seqlens_q[tid + 1] - p.cu_seqlens_q[tid]);
+      }
+      sWork[tid] = w;
+    }
+    __syncthreads();
+    if (tid < p.batch) {
+      const int w = sWork[tid];
+      int rank = 0;
+      for (int j = 0; j < p.batch; ++j) {
+        const int v = sWork[j];
+        rank += (v > w) || (v == w && j < tid);
+      }
+      if (rank == static_cast<int>(blockIdx.z)) *sPick = tid;
+    }
+    __syncthreads();
+    b = *sPick;
+  }
 
   const int q_begin = p.cu_seqlens_q[b];
   const int q_len = p.cu_seqlens_q[b + 1] - q_begin;

@@ -214,6 +214,24 @@ def test_gqa_split_decode_reduced(num_splits):
     check_close(out, lse, ref_o, ref_l, f"splits={num_splits}")
 
 
+@pytest.mark.parametrize("batch,len_lo,len_hi", [(40, 300, 300), (40, 0, 900), (200, 1, 400)])
+def test_split_decode_request_order(batch, len_lo, len_hi):
+    """The fixed-split kernel serves the longest requests first (each CTA
+    ranks the batch's key counts): equal lengths (ties by index), empty
+    requests among long ones, and a batch above the ranking's limit (launch
+    order kept) all match the oracle, and every request's in-kernel merge
+    fires once."""
+    wl = workloads.make("gqa_split_decode", batch=batch, len_lo=len_lo, len_hi=len_hi,
+                        pool_pages=batch * (len_hi // 16 + 2) + 64, h_q=8, h_kv=2)
+    if len_lo == 0:
+        wl.cache_seqlens[::7] = 0
+    g = wl.to(DEV)
+    out, lse = gpu_attn(g, num_splits=3)
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, f"batch={batch}")
+    assert pkv.get_error_flags() == 0
+
+
 def test_split_states_merged_by_merge_state_equal_single_call():
     """Four explicit chunk calls (each chunk a request of its own page-table
     slice) combined with pkv_merge_state equal one unsplit call and the
