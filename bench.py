@@ -264,6 +264,32 @@ def _event_ms(fn, reps: int = 20) -> float:
     return a.elapsed_time(b) / reps
 
 
+def _timed(fn, reps: int = 20) -> tuple[float, dict]:
+    """Device time of ``fn`` as a serving engine runs it: the calls captured
+    once into a CUDA graph and replayed (a short call timed eagerly measures
+    the host's launch cost, not the GPU); the eager time beside it.  Falls
+    back to the eager time, with the reason, if capture fails."""
+    eager = _event_ms(fn, reps)
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            fn()
+        torch.cuda.synchronize()
+    except RuntimeError as e:
+        torch.cuda.synchronize()
+        return eager, {"eager_ms": eager,
+                       "launch": "eager (capture failed: %s)" % str(e).splitlines()[0][:160]}
+    ms = _event_ms(gr.replay, reps)
+    del gr
+    return ms, {"eager_ms": eager, "launch": "CUDA graph replay"}
+
+
 def local_attention_line(dev, peaks, chunk: int = 2048):
     """Local (chunked) attention on the headline decode batch: the device
     builder of the virtual requests, then one causal call over them.  The
@@ -303,10 +329,11 @@ def local_attention_line(dev, peaks, chunk: int = 2048):
     keys = int((kv - eff * ((kv - ql) // eff)).sum())
     h_kv, d, dv = g.k_cache.shape[2], g.q.shape[-1], g.v_cache.shape[-1]
     kv_bytes = keys * h_kv * (d + dv) * 2
-    b_ms, a_ms, s_ms = _event_ms(build), _event_ms(attend), _event_ms(step)
+    (b_ms, b_how), (a_ms, a_how), (s_ms, s_how) = _timed(build), _timed(attend), _timed(step)
     return {"kernel": "local_virtual_batches_kernel + attention", "chunk": chunk,
             "effective_chunk": eff, "virtual_requests_capacity": cap,
             "builder_ms": b_ms, "attn_ms": a_ms, "ms_per_step": s_ms,
+            "timing": {"builder": b_how, "attention": a_how, "step": s_how},
             "kv_GBps": kv_bytes / 1e9 / (a_ms / 1e3),
             "kv_frac_hbm": kv_bytes / 1e9 / (a_ms / 1e3) / peaks["hbm_gbs"],
             "tokens_per_s": g.q.shape[0] / (s_ms / 1e3)}
@@ -333,14 +360,14 @@ def cascade_line(dev, peaks, prefix_tokens: int = 4096):
                                       g.page_table, g.cache_seqlens, g.cu_seqlens_q,
                                       g.max_seqlen_q, g.scale, causal=True, out=out, lse=lse)
 
-    s_ms = _event_ms(step)
+    s_ms, s_how = _timed(step)
     h_kv, d, dv = g.k_cache.shape[2], g.q.shape[-1], g.v_cache.shape[-1]
     row = h_kv * (d + dv) * 2
     own = int(g.cache_seqlens.sum())
     logical = (own + B * prefix_tokens) * row
     unique = (own + prefix_tokens) * row
     return {"kernel": "2 x attention + merge_state_kernel", "prefix_tokens": prefix_tokens,
-            "ms_per_step": s_ms,
+            "ms_per_step": s_ms, "timing": s_how,
             "kv_GBps_logical": logical / 1e9 / (s_ms / 1e3),
             "kv_GBps_unique": unique / 1e9 / (s_ms / 1e3),
             "unique_frac_hbm": unique / 1e9 / (s_ms / 1e3) / peaks["hbm_gbs"],
@@ -374,9 +401,10 @@ def append_line(dev, peaks):
                                      g.page_table, g.cache_seqlens, g.cu_seqlens_q,
                                      g.max_seqlen_q, g.scale, causal=True, out=out)
 
-    w_ms, s_ms = _event_ms(write), _event_ms(step)
+    (w_ms, w_how), (s_ms, s_how) = _timed(write), _timed(step)
     moved = 2 * (k_new.numel() + v_new.numel()) * 2
     return {"kernel": "set_kv_buffer_kernel (+ extend_tc_kernel)", "new_tokens": int(loc.numel()),
+            "timing": {"write": w_how, "step": s_how},
             "write_ms": w_ms, "write_GBps": moved / 1e9 / (w_ms / 1e3),
             "write_frac_hbm": moved / 1e9 / (w_ms / 1e3) / peaks["hbm_gbs"],
             "ms_per_step": s_ms, "tokens_per_s": g.q.shape[0] / (s_ms / 1e3)}
@@ -403,10 +431,10 @@ def fp8_line(dev, peaks):
                                   g.max_seqlen_q, g.scale, k_descale=kd, v_descale=vd,
                                   out=out, workspace=ws)
 
-    a_ms = _event_ms(attend)
+    a_ms, a_how = _timed(attend)
     kv_bytes = int(g.cache_seqlens.sum()) * h_kv * 256
     return {"kernel": "decode_allheads_kernel (page boxes, balanced, fp8)",
-            "attn_ms": a_ms, "kv_GBps": kv_bytes / 1e9 / (a_ms / 1e3),
+            "attn_ms": a_ms, "timing": a_how, "kv_GBps": kv_bytes / 1e9 / (a_ms / 1e3),
             "kv_frac_hbm": kv_bytes / 1e9 / (a_ms / 1e3) / peaks["hbm_gbs"],
             "tokens_per_s": g.q.shape[0] / (a_ms / 1e3)}
 
@@ -742,18 +770,14 @@ def main():
                 torch.cuda.synchronize()
                 e2 = [(torch.cuda.Event(enable_timing=True),
                        torch.cuda.Event(enable_timing=True)) for _ in range(20)]
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record()
                 for i in range(20):
                     s2.run(e2[i])
-                b.record()
                 torch.cuda.synchronize()
-                sms = a.elapsed_time(b) / 20
                 kms = sum(x.elapsed_time(y) for x, y in e2) / 20
+                sms, how = _timed(s2.run)
                 others[label] = {
                     "kernel": s2.attention_kernel(),
-                    "ms_per_step": sms, "attn_ms": kms,
+                    "ms_per_step": sms, "step_timing": how, "attn_ms": kms,
                     "kv_GBps": s2.kv_bytes / 1e9 / (kms / 1e3),
                     "kv_frac_hbm": s2.kv_bytes / 1e9 / (kms / 1e3) / peaks["hbm_gbs"],
                     "TFLOPs": s2.flops / 1e12 / (kms / 1e3),
