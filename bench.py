@@ -401,10 +401,22 @@ def append_line(dev, peaks):
                                      g.page_table, g.cache_seqlens, g.cu_seqlens_q,
                                      g.max_seqlen_q, g.scale, causal=True, out=out)
 
+    # the same rows stored into pools of fp8 codes (value / 0.05)
+    k8 = torch.zeros(g.k_cache.shape, dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
+    v8 = torch.zeros(g.v_cache.shape, dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
+    scale = torch.tensor([0.05], dtype=torch.float32, device=dev)
+
+    def write_fp8():
+        pkv.set_kv_buffer(k8, v8, loc, k_new, v_new, k_scale=scale, v_scale=scale)
+
     (w_ms, w_how), (s_ms, s_how) = _timed(write), _timed(step)
+    w8_ms, w8_how = _timed(write_fp8)
     moved = 2 * (k_new.numel() + v_new.numel()) * 2
+    moved8 = (k_new.numel() + v_new.numel()) * 3  # 2 B read + 1 B code written
     return {"kernel": "set_kv_buffer_kernel (+ extend_tc_kernel)", "new_tokens": int(loc.numel()),
-            "timing": {"write": w_how, "step": s_how},
+            "timing": {"write": w_how, "step": s_how, "write_fp8": w8_how},
+            "write_fp8_ms": w8_ms, "write_fp8_GBps": moved8 / 1e9 / (w8_ms / 1e3),
+            "write_fp8_frac_hbm": moved8 / 1e9 / (w8_ms / 1e3) / peaks["hbm_gbs"],
             "write_ms": w_ms, "write_GBps": moved / 1e9 / (w_ms / 1e3),
             "write_frac_hbm": moved / 1e9 / (w_ms / 1e3) / peaks["hbm_gbs"],
             "ms_per_step": s_ms, "tokens_per_s": g.q.shape[0] / (s_ms / 1e3)}

@@ -323,11 +323,39 @@ int pkv_topk_to_slots(pkv_tensor topk, pkv_tensor cu_seqlens_q,
  * Last dimensions contiguous, rows 16-byte aligned, dk and dv multiples of 8
  * (PKV_ERR_UNSUPPORTED otherwise).  A slot outside [0, num_pages * P) is
  * skipped and sets PKV_EFLAG_PAGE_OOB.  No value is converted: the rows are
- * copied bit for bit.
+ * copied bit for bit.  Pools of fp8 codes (both PKV_FP8_E4M3) are stored as
+ * by pkv_set_kv_buffer_fp8 with scales of 1.
  */
 int pkv_set_kv_buffer(pkv_tensor loc, pkv_tensor k, pkv_tensor v,
                       pkv_tensor k_cache, pkv_tensor v_cache,
                       cudaStream_t stream);
+
+/*
+ * pkv_set_kv_buffer_fp8 -- store the new tokens' rows into a pool of fp8
+ * (e4m3) codes.
+ *
+ * The same write for a pool whose `kv_cache_dtype` is fp8, where the
+ * backend passes the layer's `k_scale` / `v_scale` to `set_kv_buffer`
+ * (flashattention_backend.py `forward_extend` / `forward_decode`).  Every
+ * element is divided by its tensor's scale in fp32 (IEEE division) and
+ * rounded to the nearest e4m3 code, ties to even:
+ *   k_cache[s / P][s % P][h][c] = e4m3(float(k[t][h][c]) / k_scale),
+ * v likewise with v_scale, so that pkv_attn_with_kvcache_fp8 with
+ * k_descale = k_scale (and v_descale = v_scale) reads back code * scale.
+ * A quotient whose magnitude is 464 or more, which the format cannot hold
+ * (torch's conversion gives NaN there), is stored as +-448: such inputs are
+ * outside the contract.
+ *
+ * k_cache / v_cache  PKV_FP8_E4M3 [num_pages, P, H, dk] / [.., dv], else as
+ *          pkv_set_kv_buffer (PKV_ERR_INVALID_ARG for any other dtype);
+ *          dk and dv multiples of 16.
+ * k_scale, v_scale  DEVICE pointers to one fp32 each (finite, > 0), read by
+ *          the kernel; NULL means 1.
+ */
+int pkv_set_kv_buffer_fp8(pkv_tensor loc, pkv_tensor k, pkv_tensor v,
+                          pkv_tensor k_cache, pkv_tensor v_cache,
+                          const float *k_scale, const float *v_scale,
+                          cudaStream_t stream);
 
 /*
  * pkv_make_local_attention_virtual_batches -- local (chunked) attention as

@@ -109,6 +109,10 @@ def _lib():
         lib.orc_set_kv_buffer.argtypes = [
             _u16p, _i64, _i64, _int, _int, _int, _i64p, _u16p, _i64, _i64, _i64,
             _i64, _int]
+        lib.orc_set_kv_buffer_fp8.argtypes = [
+            _u16p, _i64, _i64, _int, _int, _int, _i64p, ctypes.c_float, _u8p, _i64, _i64,
+            _i64, _i64, _int]
+        lib.orc_set_kv_buffer_fp8.restype = ctypes.c_int
         lib.orc_local_virtual_batches.argtypes = [
             _int, _int, _i32p, _i32p, _int, _i32p, _i64, _int, _int,
             _i32p, _i32p, _i32p, _i32p, _i64, _int, _i32p]
@@ -266,6 +270,29 @@ def set_kv_buffer(cache_bits, rows_bits, loc):
         c.shape[0], c.shape[1])
     if n < 0:
         raise ValueError(f"orc_set_kv_buffer rejected its arguments ({n})")
+    return n
+
+
+def set_kv_buffer_fp8(cache_codes, rows_bits, loc, scale: float):
+    """The KV write into a pool of e4m3 codes, in place: code of value /
+    scale (binary32 quotient, nearest code, ties to even; see
+    orc_set_kv_buffer_fp8).  cache_codes: uint8 [num_pages, P, H, D] (D
+    contiguous, writable); rows_bits: uint16 bf16 bits [T, H, D]; loc: T slot
+    ids.  Returns the number of skipped (out-of-pool) slots."""
+    c = cache_codes
+    r = np.asarray(rows_bits)
+    assert c.dtype == np.uint8 and r.dtype == np.uint16
+    assert c.strides[3] == 1 and r.strides[2] == 2 and c.flags.writeable
+    lc = np.ascontiguousarray(loc, dtype=np.int64)
+    cs = _elem_strides(c)
+    rs = _elem_strides(r)
+    n = _lib().orc_set_kv_buffer_fp8(
+        _ptr(r, ctypes.c_uint16), rs[0], rs[1], r.shape[0], r.shape[1], r.shape[2],
+        _ptr(lc, ctypes.c_int64), float(scale),
+        c.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), cs[0], cs[1], cs[2],
+        c.shape[0], c.shape[1])
+    if n < 0:
+        raise ValueError(f"orc_set_kv_buffer_fp8 rejected its arguments ({n})")
     return n
 
 

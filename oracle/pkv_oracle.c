@@ -378,6 +378,28 @@ uint8_t orc_e4m3_round(double x) {
   return (uint8_t)(sign | best);
 }
 
+int orc_set_kv_buffer_fp8(const uint16_t *rows, int64_t r_st, int64_t r_sh, int n_tokens,
+                          int heads, int d, const int64_t *loc, float scale, uint8_t *cache,
+                          int64_t c_sp, int64_t c_spos, int64_t c_sh, int64_t num_pages,
+                          int page_size) {
+  if (n_tokens < 0 || heads < 1 || d < 1 || page_size < 1 || num_pages < 0) return -1;
+  if (!(scale > 0.0f) || isinf(scale)) return -1;
+  int skipped = 0;
+  for (int t = 0; t < n_tokens; ++t) {
+    int64_t slot = loc[t];
+    if (slot < 0 || slot >= num_pages * page_size) { ++skipped; continue; }
+    int64_t page = slot / page_size, pos = slot % page_size;
+    for (int h = 0; h < heads; ++h)
+      for (int c = 0; c < d; ++c) {
+        /* the bf16 value is exact in binary32; one binary32 division */
+        const float x = (float)bf16_bits_to_double(rows[(int64_t)t * r_st + (int64_t)h * r_sh + c]);
+        const float quotient = x / scale;
+        cache[page * c_sp + pos * c_spos + h * c_sh + c] = orc_e4m3_round((double)quotient);
+      }
+  }
+  return skipped;
+}
+
 int orc_attention_fp8(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q,
                       int h_q, int d_qk, const uint8_t *k_cache, int64_t k_sp,
                       int64_t k_spos, int64_t k_sh, const uint8_t *v_cache,

@@ -184,6 +184,19 @@ double orc_e4m3_value(uint8_t code);
  * past 448 (above 464) gives the NaN code, as does NaN. */
 uint8_t orc_e4m3_round(double x);
 
+/* The KV write into a pool of fp8 codes (flashattention_backend.py: the
+ * layer's k_scale / v_scale passed to set_kv_buffer when kv_cache_dtype is
+ * fp8): as orc_set_kv_buffer, except that element (t, h, d) is stored as
+ * orc_e4m3_round(x / scale), where x is the bf16 value and the quotient is
+ * taken in binary32 (the precision the pool's writer divides in), so that
+ * reading the code back as value(code) * scale recovers x to e4m3 precision.
+ * cache: uint8 codes at cache[page*c_sp + pos*c_spos + h*c_sh + d].  Returns
+ * the skipped-slot count, or -1 on bad arguments (scale not finite and > 0). */
+int orc_set_kv_buffer_fp8(const uint16_t *rows, int64_t r_st, int64_t r_sh, int n_tokens,
+                          int heads, int d, const int64_t *loc, float scale, uint8_t *cache,
+                          int64_t c_sp, int64_t c_spos, int64_t c_sh, int64_t num_pages,
+                          int page_size);
+
 /* Attention over an fp8 cache: q rounded to e4m3 (orc_e4m3_round) and widened;
  * K_j = value(k code) * k_descale[b * n_kv_heads + kvh], V_j likewise with
  * v_descale (NULL descales = 1); then the definition of orc_attention (same

@@ -96,6 +96,7 @@ EXPORTED_SYMBOLS = (
     "pkv_make_local_attention_virtual_batches",
     "pkv_set_kv_buffer",
     "pkv_attn_with_kvcache_fp8",
+    "pkv_set_kv_buffer_fp8",
 )
 
 _FP8 = 5
@@ -149,6 +150,7 @@ def load_library(path: str | None = None):
     lib.pkv_strided_page_table.argtypes = [T, T, c_int, T, c_void_p]
     lib.pkv_topk_to_slots.argtypes = [T, T, T, T, c_int, T, c_void_p]
     lib.pkv_set_kv_buffer.argtypes = [T, T, T, T, T, c_void_p]
+    lib.pkv_set_kv_buffer_fp8.argtypes = [T, T, T, T, T, c_void_p, c_void_p, c_void_p]
     lib.pkv_attn_with_kvcache_fp8.argtypes = [T, T, T, T, T, T, c_int, c_float, c_int, c_int,
                                               c_void_p, c_void_p, c_int, T, T, c_void_p,
                                               c_size_t, c_void_p]
@@ -367,12 +369,32 @@ def topk_to_slots(topk, cu_seqlens_q, page_table, cache_seqlens,
     return out
 
 
-def set_kv_buffer(k_cache, v_cache, loc, k, v=None):
+def _scale_ptr(t, k_cache):
+    """Device pointer of a one-element fp32 scale tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if t.dtype != torch.float32 or t.numel() != 1 or t.device != k_cache.device:
+        raise ValueError("a scale must be a one-element float32 tensor on the cache's device")
+    return t.data_ptr()
+
+
+def set_kv_buffer(k_cache, v_cache, loc, k, v=None, k_scale=None, v_scale=None):
     """Stores new K (and V) rows into their pool slots (include/pkv.h,
-    pkv_set_kv_buffer): k_cache[loc // P, loc % P] = k, same for v."""
-    _check("pkv_set_kv_buffer", load_library().pkv_set_kv_buffer(
-        _desc(loc), _desc(k), _desc(v), _desc(k_cache), _desc(None if v is None else v_cache),
-        _stream(k)))
+    pkv_set_kv_buffer): k_cache[loc // P, loc % P] = k, same for v.  For
+    pools of fp8 codes (torch.float8_e4m3fn) each value is stored as the
+    e4m3 code of value / scale (pkv_set_kv_buffer_fp8); ``k_scale`` /
+    ``v_scale`` are one-element float32 device tensors (None: 1)."""
+    lib = load_library()
+    vc = None if v is None else v_cache
+    if k_cache.dtype == torch.float8_e4m3fn:
+        _check("pkv_set_kv_buffer_fp8", lib.pkv_set_kv_buffer_fp8(
+            _desc(loc), _desc(k), _desc(v), _desc(k_cache), _desc(vc),
+            _scale_ptr(k_scale, k_cache), _scale_ptr(v_scale, k_cache), _stream(k)))
+    else:
+        if k_scale is not None or v_scale is not None:
+            raise ValueError("scales apply to pools of fp8 codes only")
+        _check("pkv_set_kv_buffer", lib.pkv_set_kv_buffer(
+            _desc(loc), _desc(k), _desc(v), _desc(k_cache), _desc(vc), _stream(k)))
     return k_cache, v_cache
 
 
@@ -386,15 +408,26 @@ def set_mla_kv_buffer(kv_cache, loc, k_nope, k_rope):
 
 def append_attn_with_kvcache(q, k, v, cache_loc, k_cache, v_cache, page_table,
                              cache_seqlens, cu_seqlens_q, max_seqlen_q: int,
-                             softmax_scale: float, **attn_kwargs):
+                             softmax_scale: float, k_scale=None, v_scale=None,
+                             **attn_kwargs):
     """The backend's forward order (flashattention_backend.py
     `forward_extend` / `forward_decode`): the new tokens' K/V go to their
     slots ``cache_loc`` first, then paged attention reads the cache that now
     holds them.  Both launches are on the current stream, so attention sees
-    the stored rows; ``attn_kwargs`` are those of ``attn_with_kvcache``."""
-    set_kv_buffer(k_cache, v_cache, cache_loc, k, v)
-    return attn_with_kvcache(q, k_cache, v_cache, page_table, cache_seqlens, cu_seqlens_q,
-                             max_seqlen_q, softmax_scale, **attn_kwargs)
+    the stored rows; ``attn_kwargs`` are those of ``attn_with_kvcache``.
+    With pools of fp8 codes the rows are stored as codes of value / scale and
+    the attention reads them back with the scales as per-(request, KV head)
+    descales (the backend's ``k_scale.expand(batch, num_kv_heads)``)."""
+    set_kv_buffer(k_cache, v_cache, cache_loc, k, v, k_scale=k_scale, v_scale=v_scale)
+    if k_cache.dtype != torch.float8_e4m3fn:
+        return attn_with_kvcache(q, k_cache, v_cache, page_table, cache_seqlens,
+                                 cu_seqlens_q, max_seqlen_q, softmax_scale, **attn_kwargs)
+    shape = (cache_seqlens.shape[0], k_cache.shape[2])
+    kd = None if k_scale is None else k_scale.reshape(1, 1).expand(shape).contiguous()
+    vd = None if v_scale is None else v_scale.reshape(1, 1).expand(shape).contiguous()
+    return attn_with_kvcache_fp8(q, k_cache, v_cache, page_table, cache_seqlens, cu_seqlens_q,
+                                 max_seqlen_q, softmax_scale, k_descale=kd, v_descale=vd,
+                                 **attn_kwargs)
 
 
 def local_virtual_batch_capacity(batch: int, total_q: int, max_seqlen_q: int,

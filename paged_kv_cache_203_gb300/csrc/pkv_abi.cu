@@ -575,29 +575,38 @@ int pkv_topk_to_slots(pkv_tensor topk, pkv_tensor cu_seqlens_q,
       static_cast<int32_t *>(out.data), out.stride[0], err, stream);
 }
 
-int pkv_set_kv_buffer(pkv_tensor loc, pkv_tensor k, pkv_tensor v,
-                      pkv_tensor k_cache, pkv_tensor v_cache,
-                      cudaStream_t stream) {
+namespace pkv {
+namespace {
+
+int set_kv_impl(pkv_tensor loc, pkv_tensor k, pkv_tensor v, pkv_tensor k_cache,
+                pkv_tensor v_cache, const float *k_scale, const float *v_scale,
+                bool want_fp8, cudaStream_t stream) {
   if (loc.data == nullptr || loc.ndim != 1 || (loc.dtype != PKV_I32 && loc.dtype != PKV_I64) ||
       !unit_stride(loc, 0))
     return PKV_ERR_INVALID_ARG;
   const int64_t T = loc.shape[0];
-  if (!has(k, PKV_BF16, 3) || !has(k_cache, PKV_BF16, 4)) return PKV_ERR_INVALID_ARG;
+  // the pool's type: bf16 rows, or e4m3 codes (both pools alike)
+  const bool fp8 = k_cache.data != nullptr && k_cache.dtype == PKV_FP8_E4M3;
+  if (want_fp8 && !fp8) return PKV_ERR_INVALID_ARG;
+  const int cdt = fp8 ? PKV_FP8_E4M3 : PKV_BF16;
+  const int ces = fp8 ? 1 : 2;  // cache bytes per element
+  if (!has(k, PKV_BF16, 3) || !has(k_cache, cdt, 4)) return PKV_ERR_INVALID_ARG;
   if (present(v) != present(v_cache)) return PKV_ERR_INVALID_ARG;
   const int64_t H = k.shape[1], dk = k.shape[2];
   if (k.shape[0] != T || k_cache.shape[2] != H || k_cache.shape[3] != dk)
     return PKV_ERR_INVALID_ARG;
   int64_t dv = 0;
   if (present(v)) {
-    if (!has(v, PKV_BF16, 3) || !has(v_cache, PKV_BF16, 4)) return PKV_ERR_INVALID_ARG;
+    if (!has(v, PKV_BF16, 3) || !has(v_cache, cdt, 4)) return PKV_ERR_INVALID_ARG;
     dv = v.shape[2];
     if (v.shape[0] != T || v.shape[1] != H || v_cache.shape[0] != k_cache.shape[0] ||
         v_cache.shape[1] != k_cache.shape[1] || v_cache.shape[2] != H ||
         v_cache.shape[3] != dv)
       return PKV_ERR_INVALID_ARG;
   }
-  if (dk % 8 != 0 || dv % 8 != 0 || !vec_ok(k, 2) || !vec_ok(k_cache, 2) ||
-      (present(v) && (!vec_ok(v, 2) || !vec_ok(v_cache, 2))))
+  const int64_t epp = fp8 ? 16 : 8;  // elements per 16-byte piece of the pool
+  if (dk % epp != 0 || dv % epp != 0 || !vec_ok(k, 2) || !vec_ok(k_cache, ces) ||
+      (present(v) && (!vec_ok(v, 2) || !vec_ok(v_cache, ces))))
     return PKV_ERR_UNSUPPORTED;
   if (T > 0x7fffffffLL || H > 0x7fffffffLL || dk > 0x7fffffffLL || dv > 0x7fffffffLL ||
       k_cache.shape[1] > 0x7fffffffLL)
@@ -614,7 +623,7 @@ int pkv_set_kv_buffer(pkv_tensor loc, pkv_tensor k, pkv_tensor v,
   p.k = static_cast<const bf16 *>(k.data);
   p.k_st = k.stride[0];
   p.k_sh = k.stride[1];
-  p.k_cache = static_cast<bf16 *>(k_cache.data);
+  p.k_cache = k_cache.data;
   p.kc_sp = k_cache.stride[0];
   p.kc_spos = k_cache.stride[1];
   p.kc_sh = k_cache.stride[2];
@@ -622,15 +631,34 @@ int pkv_set_kv_buffer(pkv_tensor loc, pkv_tensor k, pkv_tensor v,
     p.v = static_cast<const bf16 *>(v.data);
     p.v_st = v.stride[0];
     p.v_sh = v.stride[1];
-    p.v_cache = static_cast<bf16 *>(v_cache.data);
+    p.v_cache = v_cache.data;
     p.vc_sp = v_cache.stride[0];
     p.vc_spos = v_cache.stride[1];
     p.vc_sh = v_cache.stride[2];
   }
   p.num_pages = k_cache.shape[0];
   p.page_size = static_cast<int>(k_cache.shape[1]);
+  p.fp8 = fp8 ? 1 : 0;
+  p.k_scale = fp8 ? k_scale : nullptr;
+  p.v_scale = fp8 ? v_scale : nullptr;
   p.err = err;
   return launch_set_kv_buffer(p, stream);
+}
+
+}  // namespace
+}  // namespace pkv
+
+int pkv_set_kv_buffer(pkv_tensor loc, pkv_tensor k, pkv_tensor v,
+                      pkv_tensor k_cache, pkv_tensor v_cache,
+                      cudaStream_t stream) {
+  return set_kv_impl(loc, k, v, k_cache, v_cache, nullptr, nullptr, false, stream);
+}
+
+int pkv_set_kv_buffer_fp8(pkv_tensor loc, pkv_tensor k, pkv_tensor v,
+                          pkv_tensor k_cache, pkv_tensor v_cache,
+                          const float *k_scale, const float *v_scale,
+                          cudaStream_t stream) {
+  return set_kv_impl(loc, k, v, k_cache, v_cache, k_scale, v_scale, true, stream);
 }
 
 int pkv_make_local_attention_virtual_batches(

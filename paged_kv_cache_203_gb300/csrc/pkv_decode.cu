@@ -169,12 +169,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(v));
   return r;
 }
-// (lo, hi) rounded to e4m3 (nearest even, saturating): lo in the low byte.
-__device__ __forceinline__ uint32_t round_e4m3x2(float lo, float hi) {
-  uint16_t c;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(c) : "f"(hi), "f"(lo));
-  return c;
-}
 // D(16x8, f32) += A(16x32, e4m3, row) * B(32x8, e4m3, col); four codes per
 // register, the lowest k in the lowest byte.
 __device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1,

@@ -16,6 +16,16 @@ constexpr int kNumSMs = 152;        // GB300: 2 dies x 76 SMs
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+#ifdef __CUDACC__
+// (lo, hi) rounded to e4m3 (nearest, ties to even; magnitudes past 448
+// saturate to 448): lo in the low byte of the result.
+__device__ __forceinline__ uint32_t round_e4m3x2(float lo, float hi) {
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(c) : "f"(hi), "f"(lo));
+  return c;
+}
+#endif
+
 // Everything a paged-attention kernel needs, with strides in elements.
 struct AttnParams {
   const bf16 *q;
@@ -117,12 +127,14 @@ struct SetKvParams {
   int64_t k_st, k_sh;
   const bf16 *v;
   int64_t v_st, v_sh;
-  bf16 *k_cache;
+  void *k_cache;  // bf16, or e4m3 codes when fp8
   int64_t kc_sp, kc_spos, kc_sh;
-  bf16 *v_cache;
+  void *v_cache;
   int64_t vc_sp, vc_spos, vc_sh;
   int64_t num_pages;
   int page_size;
+  int fp8;                             // caches hold e4m3 codes
+  const float *k_scale, *v_scale;      // fp8: one device float each, or null (1)
   uint32_t *err;
 };
 

@@ -69,6 +69,18 @@ def test_binding_rejects_bad_arguments_on_host(lib):
     # wrong dtype of the page table
     with pytest.raises(pkv.PkvError):
         pkv.attn_workspace_size(q, k, k, pt.long(), cs, 1)
+    # the fp8 KV write wants pools of e4m3 codes; a bf16 pool is refused
+    # (and a bf16 write refuses scales) before any device work
+    loc = torch.zeros(2, dtype=torch.int32)
+    rows = torch.zeros(2, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.load_library().pkv_set_kv_buffer_fp8  # exported
+        pkv._check("pkv_set_kv_buffer_fp8", pkv.load_library().pkv_set_kv_buffer_fp8(
+            pkv._desc(loc), pkv._desc(rows), pkv._desc(None), pkv._desc(k), pkv._desc(None),
+            None, None, None))
+    assert e.value.code == -1
+    with pytest.raises(ValueError):
+        pkv.set_kv_buffer(k, None, loc, rows, k_scale=torch.ones(1))
     # workspace planning: no split -> no workspace; 4 splits -> partials
     assert pkv.attn_workspace_size(q, k, k, pt, cs, 1, num_splits=1) == 0
     ws = pkv.attn_workspace_size(q, k, k, pt, cs, 1, num_splits=4)

@@ -1261,3 +1261,82 @@ def test_set_kv_buffer_full_size_bit_exact():
     assert np.array_equal(_bits(g.k_cache), ref_k)
     assert np.array_equal(_bits(g.v_cache), ref_v)
     assert pkv.get_error_flags() == 0
+
+
+# ----------------------------------------------- KV write into an fp8 pool
+
+def _scale_t(s):
+    return None if s is None else torch.tensor([s], dtype=torch.float32, device=DEV)
+
+
+@pytest.mark.parametrize("P,H,D,T,scales", [
+    (16, 8, 128, 300, (0.02, 0.7)),
+    (64, 2, 64, 37, (None, 0.05)),
+    (1, 8, 128, 2000, (0.3, None)),
+])
+def test_set_kv_buffer_fp8_bit_exact(P, H, D, T, scales):
+    """Quantising write into pools of e4m3 codes: every stored code equals
+    the oracle's (binary32 quotient value / scale, nearest code, ties to
+    even) and every other byte keeps its prior contents; an out-of-pool slot
+    is skipped and flagged.  Quotients stay inside the format's range."""
+    g = torch.Generator().manual_seed(P * 7 + T)
+    pages = T // P + 40
+    prior_k = torch.randint(0, 0x7e, (pages, P, H, D), generator=g, dtype=torch.uint8)
+    prior_v = torch.randint(0, 0x7e, (pages, P, H, D), generator=g, dtype=torch.uint8)
+    k = torch.randn(T, H, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(T, H, D, generator=g).to(torch.bfloat16)
+    loc = torch.randperm(pages * P, generator=g)[:T].to(torch.int64)
+    loc[T // 2] = pages * P                          # outside the pool
+    ks, vs = scales
+    ref_k, ref_v = prior_k.numpy().copy(), prior_v.numpy().copy()
+    assert oracle.set_kv_buffer_fp8(ref_k, _bits(k), loc.numpy(), 1.0 if ks is None else ks) == 1
+    assert oracle.set_kv_buffer_fp8(ref_v, _bits(v), loc.numpy(), 1.0 if vs is None else vs) == 1
+    k8 = prior_k.to(DEV).view(torch.float8_e4m3fn)
+    v8 = prior_v.to(DEV).view(torch.float8_e4m3fn)
+    pkv.set_kv_buffer(k8, v8, loc.to(DEV), k.to(DEV), v.to(DEV),
+                      k_scale=_scale_t(ks), v_scale=_scale_t(vs))
+    torch.cuda.synchronize()
+    assert np.array_equal(k8.view(torch.uint8).cpu().numpy(), ref_k)
+    assert np.array_equal(v8.view(torch.uint8).cpu().numpy(), ref_v)
+    assert pkv.get_error_flags() == pkv.EFLAG_PAGE_OOB
+
+
+def test_fp8_write_then_attend():
+    """A decode step over an fp8 pool as the backend runs it: the new
+    token's K/V stored as codes of value / scale, then attention with the
+    scales as per-(request, KV head) descales; against the oracle's write
+    followed by the oracle's fp8 attention."""
+    wl = workloads.make("tiny_decode", d=128, page_size=16, h_q=32, h_kv=8, batch=12,
+                        len_lo=20, len_hi=900, pool_tokens=12 * 928 * 2, seed=78)
+    ks, vs = 0.03, 0.05
+    k_scale, v_scale = _scale_t(ks), _scale_t(vs)
+    # the cached keys as codes, then each request's newest token rewritten
+    k_codes = (wl.k_cache.float() / ks).to(torch.float8_e4m3fn).view(torch.uint8)
+    v_codes = (wl.v_cache.float() / vs).to(torch.float8_e4m3fn).view(torch.uint8)
+    P = wl.page_size
+    kv = wl.cache_seqlens.numpy()
+    loc = np.array([wl.page_table[b, (kv[b] - 1) // P].item() * P + (kv[b] - 1) % P
+                    for b in range(len(kv))], dtype=np.int64)
+    gen = torch.Generator().manual_seed(5)
+    k_new = torch.randn(len(kv), 8, 128, generator=gen).to(torch.bfloat16)
+    v_new = torch.randn(len(kv), 8, 128, generator=gen).to(torch.bfloat16)
+    ref_k, ref_v = k_codes.numpy().copy(), v_codes.numpy().copy()
+    assert oracle.set_kv_buffer_fp8(ref_k, _bits(k_new), loc, ks) == 0
+    assert oracle.set_kv_buffer_fp8(ref_v, _bits(v_new), loc, vs) == 0
+    g = wl.to(DEV)
+    k8 = k_codes.to(DEV).view(torch.float8_e4m3fn)
+    v8 = v_codes.to(DEV).view(torch.float8_e4m3fn)
+    out, lse = pkv.append_attn_with_kvcache(
+        g.q, k_new.to(DEV), v_new.to(DEV), torch.from_numpy(loc).to(DEV), k8, v8,
+        g.page_table, g.cache_seqlens, g.cu_seqlens_q, g.max_seqlen_q, g.scale,
+        k_scale=k_scale, v_scale=v_scale, return_softmax_lse=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(k8.view(torch.uint8).cpu().numpy(), ref_k)
+    assert np.array_equal(v8.view(torch.uint8).cpu().numpy(), ref_v)
+    B, h_kv = len(kv), 8
+    ref_o, ref_l, _ = oracle.attention_fp8(
+        oracle.bf16_bits(wl.q), ref_k, ref_v, wl.page_table.numpy(), kv,
+        wl.cu_seqlens_q.numpy(), wl.scale,
+        k_descale=np.full((B, h_kv), ks, np.float32), v_descale=np.full((B, h_kv), vs, np.float32))
+    check_close(out, lse, ref_o, ref_l, "fp8 write then attend")
+    assert pkv.get_error_flags() == 0

@@ -881,3 +881,60 @@ def test_fp8_per_request_descales_against_scipy():
                 o, l = dense_reference_row(q8[t, h], K, V, 0.45)
                 np.testing.assert_allclose(out[t, h], o, atol=1e-12)
                 assert abs(lse[t, h] - l) < 1e-12
+
+
+# ------------------------------------------------- KV write into an fp8 pool
+
+@pytest.mark.parametrize("scale", [1.0, 0.05, 0.3, 7.0])
+def test_fp8_kv_write_equals_torch_division_and_cast(scale):
+    """The quantising write stores, at each slot, torch's e4m3 cast of the
+    binary32 quotient row / scale (a library routine the oracle does not
+    call): random rows over a wide range, rows whose quotients fall exactly
+    on midpoints between codes (ties), quotients past the format's range,
+    a strided pool and out-of-pool slots (skipped, counted, pool untouched)."""
+    rng = np.random.default_rng(95)
+    T, H, D, P, NP = 9, 2, 32, 4, 8
+    vals = rng.standard_normal((T, H, D)) * np.exp2(rng.integers(-6, 5, (T, H, D)))
+    mags = np.array([oracle.e4m3_value(c) for c in range(127)])
+    mids = (mags[:-1] + mags[1:]) / 2
+    vals[0, 0, :] = mids[rng.integers(40, 120, D)] * scale     # ties after division
+    vals[1, 1, :4] = [460.0 * scale, 470.0 * scale, -500.0 * scale, 448.0 * scale]
+    rows = torch.from_numpy(vals).to(torch.bfloat16)
+    bits = oracle.bf16_bits(rows)
+    big = np.zeros((NP, P, H + 1, D + 16), np.uint8)            # strided view
+    pool = big[:, :, 1:, 8:8 + D]
+    loc = np.array([5, 0, 31, -1, 17, 32, 2, 9, 30])
+    n = oracle.set_kv_buffer_fp8(pool, bits, loc, scale)
+    assert n == 2
+    ref = (rows.float() / torch.tensor(scale, dtype=torch.float32)).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+    want = np.zeros_like(pool)
+    for t, s in enumerate(loc):
+        if 0 <= s < NP * P:
+            want[s // P, s % P] = ref[t]
+    assert np.array_equal(pool, want)
+    assert not big[:, :, 0].any() and not big[:, :, :, :8].any() and not big[:, :, :, 8 + D:].any()
+
+
+def test_fp8_kv_write_reads_back_within_e4m3_precision():
+    """Reading a stored code back as value(code) * scale recovers the row
+    to e4m3 precision: relative error at most 2^-4 for normal codes, at most
+    half the subnormal step times the scale below them."""
+    rng = np.random.default_rng(96)
+    rows = torch.from_numpy(rng.standard_normal((16, 2, 64))).to(torch.bfloat16)
+    scale = 0.02
+    pool = np.zeros((4, 4, 2, 64), np.uint8)
+    assert oracle.set_kv_buffer_fp8(pool, oracle.bf16_bits(rows), np.arange(16), scale) == 0
+    back = np.vectorize(oracle.e4m3_value)(pool.reshape(16, 2, 64)) * scale
+    x = rows.double().numpy()
+    normal = np.abs(x) / scale >= 2.0 ** -6
+    assert np.all(np.abs(back - x)[normal] <= np.abs(x)[normal] * 2.0 ** -4 + 1e-12)
+    assert np.all(np.abs(back - x)[~normal] <= 2.0 ** -10 * scale + 1e-12)
+
+
+def test_fp8_kv_write_rejects_bad_scales():
+    pool = np.zeros((1, 1, 1, 16), np.uint8)
+    rows = np.zeros((1, 1, 16), np.uint16)
+    for s in (0.0, -1.0, float("inf"), float("nan")):
+        with pytest.raises(ValueError):
+            oracle.set_kv_buffer_fp8(pool, rows, np.zeros(1), s)
