@@ -259,6 +259,9 @@ int pkv_merge_state(pkv_tensor v_a, pkv_tensor lse_a, pkv_tensor v_b,
  *                  written, gets dst_kv_lens = -1 and sets
  *                  PKV_EFLAG_ROW_TOO_SHORT.
  * dst_kv_lens      int32 [B].
+ * A row whose pool index lies outside [0, pool_rows), or which would read a
+ * req_to_token column at or past max_ctx, is likewise not written at all:
+ * dst_kv_lens = -1 and PKV_EFLAG_SRC_OOB.
  */
 int pkv_build_swa_page_table(pkv_tensor req_to_token,
                              pkv_tensor req_pool_indices, pkv_tensor seq_lens,

@@ -77,7 +77,7 @@ def _lib():
         lib.orc_strided_page_table.argtypes = [
             _i32p, _i64, _i64, _i64p, _int, _int, _int, _i32p, _i64]
         lib.orc_swa_page_table.argtypes = [
-            _i32p, _i64, _i64, _i64p, _i32p, _i32p, _int, _int, _i32p, _i64,
+            _i32p, _i64, _i64, _i64, _i64p, _i32p, _i32p, _int, _int, _i32p, _i64,
             _int, _i32p]
         lib.orc_topk_to_slots.argtypes = [
             _i32p, _i64, _int, _int, _i32p, _i32p, _i64, _int, _int, _i32p,
@@ -166,10 +166,11 @@ def strided_page_table(req_to_token, req_pool_indices, page_size: int,
 
 def swa_page_table(req_to_token, req_pool_indices, seq_lens, prefill_lens,
                    window: int, dst_cols: int, fill: int = 0):
-    """Returns (dst [B, dst_cols] int32, kv_lens [B] int32, n_rows_too_long).
+    """Returns (dst [B, dst_cols] int32, kv_lens [B] int32, n_rows_skipped).
 
-    Columns at or past kv_len keep ``fill``; a row whose kv_len exceeds
-    dst_cols is left as ``fill`` with kv_len -1 and counted."""
+    Columns at or past kv_len keep ``fill``; a malformed row (pool index out
+    of range, kv_len past dst_cols, a source column past the table's width)
+    is left as ``fill`` with kv_len -1 and counted."""
     rtt = np.ascontiguousarray(req_to_token, dtype=np.int32)
     rpi = np.ascontiguousarray(req_pool_indices, dtype=np.int64)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
@@ -177,7 +178,7 @@ def swa_page_table(req_to_token, req_pool_indices, seq_lens, prefill_lens,
     dst = np.full((len(rpi), dst_cols), fill, dtype=np.int32)
     kv = np.zeros(len(rpi), dtype=np.int32)
     rc = _lib().orc_swa_page_table(
-        _ptr(rtt, ctypes.c_int32), rtt.shape[1], rtt.shape[1],
+        _ptr(rtt, ctypes.c_int32), rtt.shape[1], rtt.shape[1], rtt.shape[0],
         _ptr(rpi, ctypes.c_int64), _ptr(sl, ctypes.c_int32),
         _ptr(pf, ctypes.c_int32), len(rpi), window, _ptr(dst, ctypes.c_int32),
         dst_cols, dst_cols, _ptr(kv, ctypes.c_int32))

@@ -42,7 +42,8 @@ int orc_strided_page_table(const int32_t *req_to_token, int64_t rtt_stride,
 }
 
 int orc_swa_page_table(const int32_t *req_to_token, int64_t rtt_stride,
-                       int64_t rtt_cols, const int64_t *req_pool_indices,
+                       int64_t rtt_cols, int64_t rtt_rows,
+                       const int64_t *req_pool_indices,
                        const int32_t *seq_lens, const int32_t *prefill_lens,
                        int batch, int window, int32_t *dst, int64_t dst_stride,
                        int dst_cols, int32_t *kv_lens) {
@@ -50,6 +51,11 @@ int orc_swa_page_table(const int32_t *req_to_token, int64_t rtt_stride,
   int too_long = 0;
   for (int b = 0; b < batch; ++b) {
     int64_t req = req_pool_indices[b];
+    if (req < 0 || req >= rtt_rows) {
+      kv_lens[b] = -1;
+      ++too_long;
+      continue;
+    }
     int32_t sl = seq_lens[b];
     int32_t pf = prefill_lens[req];
     /* the whole prompt, then the last `window` tokens that follow it */

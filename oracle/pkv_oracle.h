@@ -49,10 +49,14 @@ int orc_strided_page_table(const int32_t *req_to_token, int64_t rtt_stride,
  *   decode_start = max(pf, sl - window); gap = max(decode_start - pf, 0);
  *   kv_len = sl - gap; dst[i] = req_to_token[req][i < pf ? i : i + gap]
  * for i < kv_len.  Entries of dst at or past kv_len are left untouched.
- * Returns 0, -1 on bad arguments, or the number of rows whose kv_len did not
- * fit in dst_cols (those rows are left untouched and kv_lens gets -1). */
+ * A malformed row -- req outside [0, rtt_rows), a kv_len that does not fit
+ * in dst_cols, or a source column past rtt_cols -- is skipped as a whole:
+ * left untouched, with kv_lens -1 (the data-dependent faults of the ABI are
+ * skipped and flagged, never partly applied).  Returns -1 on bad arguments,
+ * else the number of skipped rows. */
 int orc_swa_page_table(const int32_t *req_to_token, int64_t rtt_stride,
-                       int64_t rtt_cols, const int64_t *req_pool_indices,
+                       int64_t rtt_cols, int64_t rtt_rows,
+                       const int64_t *req_pool_indices,
                        const int32_t *seq_lens, const int32_t *prefill_lens,
                        int batch, int window, int32_t *dst, int64_t dst_stride,
                        int dst_cols, int32_t *kv_lens);

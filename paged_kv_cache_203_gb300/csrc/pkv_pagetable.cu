@@ -13,11 +13,20 @@ __device__ __forceinline__ int64_t load_index(const void *p, int is64, int i) {
 }
 
 // Prefill-aware SWA row build (flashattention_backend.py,
-// `_build_pa_page_table_kernel`).  One CTA per request row.  The kept source
-// positions form two contiguous runs, [0, pf) and [decode_start, sl), so the
-// row is two coalesced copies: dst[i] = src[i] for i < pf, and
-// dst[i] = src[i + gap] for pf <= i < kv_len.
-__global__ void __launch_bounds__(256)
+// `_build_pa_page_table_kernel`).  The kept source positions form two
+// contiguous runs, [0, pf) and [decode_start, sl), so the row is two
+// coalesced copies: dst[i] = src[i] for i < pf, and dst[i] = src[i + gap] for
+// pf <= i < kv_len.  One CTA per (row, 1024-entry chunk of it): each thread
+// issues its four loads before any store, so a chunk costs one memory round
+// trip after the two dependent index loads.  Every CTA of a row judges the
+// row the same way; a malformed row (pool index out of range, kv_len past
+// dst's width, a source column past req_to_token's width) is written by none
+// of them and gets kv_len -1 from chunk 0, which also sets the flag.
+constexpr int kSwaThreads = 256;
+constexpr int kSwaPerThread = 4;
+constexpr int kSwaChunk = kSwaThreads * kSwaPerThread;
+
+__global__ void __launch_bounds__(kSwaThreads)
 swa_page_table_kernel(const int32_t *__restrict__ rtt, int64_t rtt_stride,
                       int64_t rtt_rows, int64_t rtt_cols, const void *rpi,
                       int rpi_is_64, const int32_t *__restrict__ seq_lens,
@@ -26,9 +35,10 @@ swa_page_table_kernel(const int32_t *__restrict__ rtt, int64_t rtt_stride,
                       int dst_cols, int32_t *__restrict__ kv_lens,
                       uint32_t *err) {
   const int b = blockIdx.x;
+  const bool lead = blockIdx.y == 0 && threadIdx.x == 0;
   const int64_t req = load_index(rpi, rpi_is_64, b);
   if (req < 0 || req >= rtt_rows) {
-    if (threadIdx.x == 0) {
+    if (lead) {
       kv_lens[b] = -1;
       atomicOr(err, PKV_EFLAG_SRC_OOB);
     }
@@ -40,27 +50,37 @@ swa_page_table_kernel(const int32_t *__restrict__ rtt, int64_t rtt_stride,
   const int gap = max(decode_start - pf, 0);
   const int kv_len = sl - gap;
   if (kv_len > dst_cols) {
-    if (threadIdx.x == 0) {
+    if (lead) {
       kv_lens[b] = -1;
       atomicOr(err, PKV_EFLAG_ROW_TOO_SHORT);
     }
     return;
   }
-  if (threadIdx.x == 0) kv_lens[b] = kv_len;
+  // positions grow with i, so the last entry reads the largest column
+  const int64_t last_src =
+      kv_len - 1 < pf ? static_cast<int64_t>(kv_len) - 1 : static_cast<int64_t>(kv_len) - 1 + gap;
+  if (kv_len > 0 && last_src >= rtt_cols) {
+    if (lead) {
+      kv_lens[b] = -1;
+      atomicOr(err, PKV_EFLAG_SRC_OOB);
+    }
+    return;
+  }
+  if (lead) kv_lens[b] = kv_len;
   const int32_t *src = rtt + req * rtt_stride;
   int32_t *out = dst + static_cast<int64_t>(b) * dst_stride;
-  bool oob = false;
-  for (int i = threadIdx.x; i < kv_len; i += blockDim.x) {
-    const int64_t pos = i < pf ? i : static_cast<int64_t>(i) + gap;
-    int32_t v = -1;
-    if (pos < rtt_cols) {
-      v = src[pos];
-    } else {
-      oob = true;
-    }
-    out[i] = v;
+  const int i0 = blockIdx.y * kSwaChunk + threadIdx.x;
+  int32_t v[kSwaPerThread];
+#pragma unroll
+  for (int e = 0; e < kSwaPerThread; ++e) {
+    const int i = i0 + e * kSwaThreads;
+    v[e] = i < kv_len ? src[i < pf ? i : static_cast<int64_t>(i) + gap] : 0;
   }
-  if (oob) atomicOr(err, PKV_EFLAG_SRC_OOB);
+#pragma unroll
+  for (int e = 0; e < kSwaPerThread; ++e) {
+    const int i = i0 + e * kSwaThreads;
+    if (i < kv_len) out[i] = v[e];
+  }
 }
 
 // Strided table: out[b][c] = req_to_token[req_b][c * P] / P
@@ -344,7 +364,11 @@ int launch_swa_page_table(const int32_t *rtt, int64_t rtt_stride,
                           int32_t *kv_lens, uint32_t *err,
                           cudaStream_t stream) {
   if (batch == 0) return PKV_OK;
-  swa_page_table_kernel<<<batch, 256, 0, stream>>>(
+  // chunks of each row along y (at least one: chunk 0 writes kv_len)
+  const int64_t chunks = (static_cast<int64_t>(dst_cols) + kSwaChunk - 1) / kSwaChunk;
+  if (chunks > 65535) return PKV_ERR_UNSUPPORTED;
+  const dim3 grid(batch, static_cast<unsigned>(chunks > 0 ? chunks : 1));
+  swa_page_table_kernel<<<grid, kSwaThreads, 0, stream>>>(
       rtt, rtt_stride, rtt_rows, rtt_cols, rpi, rpi_is_64, seq_lens,
       prefill_lens, window, dst, dst_stride, dst_cols, kv_lens, err);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;

@@ -137,6 +137,33 @@ def test_swa_page_table_edge_cases():
     assert pkv.get_error_flags() & pkv.EFLAG_ROW_TOO_SHORT
 
 
+def test_swa_page_table_malformed_rows_and_chunks():
+    """Rows the builder must skip whole -- pool index out of range (rows 1,
+    4), a source column past req_to_token's width (row 3), kv_len past dst's
+    width (row 8) -- next to valid rows spanning up to four 1024-entry chunks,
+    one ending exactly on a chunk boundary (row 2): table, kv_lens and flags
+    equal the oracle's."""
+    rng = np.random.default_rng(98)
+    pool, ctx = 6, 5000
+    rtt = rng.permutation(pool * ctx).astype(np.int32).reshape(pool, ctx)
+    pfl = np.array([3, 0, 1500, 2500, 900, 1024], dtype=np.int32)
+    rpi = np.array([0, 9, 1, 2, -1, 3, 4, 5, 3], dtype=np.int64)
+    sl = np.array([1027, 5, 2048, 5001, 5, 3000, 4999, 4072, 5600], dtype=np.int32)
+    window, W = 3000, 5000
+    ref, ref_kv, n = oracle.swa_page_table(rtt, rpi, sl, pfl, window, W, fill=-5)
+    assert n == 4 and list(ref_kv[[1, 3, 4, 8]]) == [-1] * 4
+    assert list(ref_kv[[0, 2, 5, 6, 7]]) == [1027, 2048, 3000, 3900, 4024]
+    dst = torch.full((len(rpi), W), -5, dtype=torch.int32, device=DEV)
+    kv = torch.zeros(len(rpi), dtype=torch.int32, device=DEV)
+    pkv.build_swa_page_table(torch.from_numpy(rtt).to(DEV), torch.from_numpy(rpi).to(DEV),
+                             torch.from_numpy(sl).to(DEV), torch.from_numpy(pfl).to(DEV),
+                             window, dst, kv)
+    torch.cuda.synchronize()
+    assert np.array_equal(kv.cpu().numpy(), ref_kv)
+    assert np.array_equal(dst.cpu().numpy(), ref)
+    assert pkv.get_error_flags() == pkv.EFLAG_SRC_OOB | pkv.EFLAG_ROW_TOO_SHORT
+
+
 def test_topk_to_slots_bit_exact():
     wl = workloads.make("mla_topk_decode", batch=16, d_qk=64, d_v=32, h_q=1,
                         pool_pages=16 * 128 + 10)

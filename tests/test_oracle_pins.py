@@ -938,3 +938,27 @@ def test_fp8_kv_write_rejects_bad_scales():
     for s in (0.0, -1.0, float("inf"), float("nan")):
         with pytest.raises(ValueError):
             oracle.set_kv_buffer_fp8(pool, rows, np.zeros(1), s)
+
+
+def test_swa_page_table_skips_malformed_rows_whole():
+    """A row with a pool index out of range, a kv_len past dst's width or a
+    source column past req_to_token's width is not written at all and gets
+    kv_len -1; the valid rows of the same batch follow the rule (brute-force
+    membership: position p kept iff p < pf or p >= sl - window)."""
+    rng = np.random.default_rng(97)
+    pool, ctx = 5, 40
+    rtt = rng.permutation(pool * ctx).astype(np.int32).reshape(pool, ctx)
+    pfl = np.array([3, 0, 6, 2, 9], dtype=np.int32)
+    rpi = [0, 7, 1, 2, -1, 3, 4]
+    sl = [12, 5, 30, 41, 5, 20, 35]        # row 3 needs column 40 of a 40-wide row
+    window, W = 8, 16                       # row 6: kv_len 17 > 16
+    dst, kv, n = oracle.swa_page_table(rtt, rpi, sl, pfl, window, W, fill=-9)
+    assert n == 4
+    for b, (r, s) in enumerate(zip(rpi, sl)):
+        if b in (1, 3, 4, 6):
+            assert kv[b] == -1 and np.all(dst[b] == -9), b
+            continue
+        keep = [p for p in range(s) if p < pfl[r] or p >= s - window]
+        assert kv[b] == len(keep)
+        assert list(dst[b, :len(keep)]) == [rtt[r, p] for p in keep]
+        assert np.all(dst[b, len(keep):] == -9)
