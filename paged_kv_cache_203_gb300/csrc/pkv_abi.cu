@@ -7,6 +7,8 @@
 
 #include <cuda.h>
 
+#include <atomic>
+
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
 
@@ -19,17 +21,16 @@ bool encode_tensor_map(CUtensorMap *map, const void *base, int rank, const cuuin
                                      const cuuint32_t *, CUtensorMapInterleave,
                                      CUtensorMapSwizzle, CUtensorMapL2promotion,
                                      CUtensorMapFloatOOBfill);
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
+  // looked up once; a function-local static is initialised thread-safely
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void *ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
                                          cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    tried = true;
-  }
+      return reinterpret_cast<EncodeTiledFn>(ptr);
+    return nullptr;
+  }();
   if (fn == nullptr) return false;
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims,
@@ -42,16 +43,18 @@ bool encode_tensor_map(CUtensorMap *map, const void *base, int rank, const cuuin
 static __device__ uint32_t g_error_word;
 
 uint32_t *device_error_word() {
-  static uint32_t *cache[64] = {nullptr};
+  static std::atomic<uint32_t *> cache[64] = {};  // per device; calls may race
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
   if (dev >= 64) return nullptr;
-  if (cache[dev] == nullptr) {
+  uint32_t *word = cache[dev].load(std::memory_order_acquire);
+  if (word == nullptr) {
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<uint32_t *>(ptr);
+    word = static_cast<uint32_t *>(ptr);
+    cache[dev].store(word, std::memory_order_release);
   }
-  return cache[dev];
+  return word;
 }
 
 namespace {

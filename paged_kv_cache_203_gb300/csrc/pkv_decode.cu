@@ -40,6 +40,8 @@
 #include <cuda_fp16.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -1580,17 +1582,16 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
+  // looked up once; a function-local static is initialised thread-safely
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void *ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
                                          cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    tried = true;
-  }
+      return reinterpret_cast<EncodeTiledFn>(ptr);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -1633,15 +1634,15 @@ template <int D, int NSTAGE, bool TMA>
 int launch_typed(const AttnParams &p, const DecodeMaps &maps, cudaStream_t stream) {
   constexpr size_t smem = Smem<D, NSTAGE>::kDynamic;
   constexpr int threads = NCT + (TMA ? 32 : 64);
-  static bool configured[64] = {false};
+  static std::atomic<bool> configured[64] = {};  // per device; calls may race
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev < 64 && !configured[dev]) {
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(decode_gqa_kernel<D, NSTAGE, TMA>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return PKV_ERR_CUDA;
-    configured[dev] = true;
+    if (dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   dim3 grid(p.num_splits, p.h_kv * p.n_row_tiles, p.batch);
   decode_gqa_kernel<D, NSTAGE, TMA><<<grid, threads, smem, stream>>>(p, maps);
@@ -1715,10 +1716,10 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
   const int hpc = p.h_kv;
   const AhLayout L = ah_layout(hpc, boxes, balanced, fp8);
   if (L.end > AH_SMEM_MAX) return PKV_ERR_UNSUPPORTED;
-  static bool configured[64] = {false};
+  static std::atomic<bool> configured[64] = {};  // per device; calls may race
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev >= 64 || !configured[dev]) {
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(decode_allheads_kernel<true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, AH_SMEM_MAX) !=
             cudaSuccess ||
@@ -1729,7 +1730,7 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize, AH_SMEM_MAX) !=
             cudaSuccess)
       return PKV_ERR_CUDA;
-    if (dev < 64) configured[dev] = true;
+    if (dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   AhMaps maps;
   memset(&maps, 0, sizeof(maps));

@@ -36,6 +36,8 @@
 #include <limits.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
 
@@ -698,14 +700,14 @@ int launch_extend_tc(const AttnParams &p, cudaStream_t stream) {
         !encode_tensor_map(&maps.v, p.v, 4, dims, sv, box))
       return PKV_ERR_UNSUPPORTED;
   }
-  static bool configured[64] = {false};
+  static std::atomic<bool> configured[64] = {};  // per device; calls may race
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev < 64 && !configured[dev]) {
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(extend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Smem::kDynamic)) != cudaSuccess)
       return PKV_ERR_CUDA;
-    configured[dev] = true;
+    if (dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   dim3 grid(n_qt, p.h_q, p.batch);
   extend_tc_kernel<<<grid, NTHREADS, Smem::kDynamic, stream>>>(p, maps);

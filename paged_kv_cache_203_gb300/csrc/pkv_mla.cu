@@ -39,6 +39,8 @@
 #include <limits.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "pkv_ptx.cuh"
 
 namespace pkv {
@@ -553,14 +555,14 @@ int launch_mla_topk(const AttnParams &p, cudaStream_t stream) {
   cuuint64_t str[2] = {static_cast<cuuint64_t>(p.q_sh) * 2, static_cast<cuuint64_t>(p.q_st) * 2};
   cuuint32_t box[3] = {64, H, 1};
   if (!encode_tensor_map(&maps.q, p.q, 3, dims, str, box)) return PKV_ERR_UNSUPPORTED;
-  static bool configured[64] = {false};
+  static std::atomic<bool> configured[64] = {};  // per device; calls may race
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev < 64 && !configured[dev]) {
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(mla_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Smem::kDynamic)) != cudaSuccess)
       return PKV_ERR_CUDA;
-    configured[dev] = true;
+    if (dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   dim3 grid(p.num_splits, 2, p.total_q);
   mla_topk_kernel<<<grid, NTHREADS, Smem::kDynamic, stream>>>(p, maps);

@@ -2,6 +2,8 @@
 // sliding-window page table, the strided (page-level) table, the top-k
 // index -> KV slot transform and the local-attention virtual batches.  All
 // integer, bit-exact by construction.
+#include <atomic>
+
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -410,15 +412,15 @@ int launch_local_virtual_batches(int attn_chunk_size, int page_size,
                                  uint32_t *err, cudaStream_t stream) {
   if (batch > kLocalBatchesMaxBatch) return PKV_ERR_UNSUPPORTED;
   const size_t smem = 2 * static_cast<size_t>(batch + 1) * sizeof(int32_t);
-  static bool configured[64] = {};
+  static std::atomic<bool> configured[64] = {};  // per device; calls may race
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev >= 64 || !configured[dev]) {
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(local_virtual_batches_kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              2 * (kLocalBatchesMaxBatch + 1) * 4) != cudaSuccess)
       return PKV_ERR_CUDA;
-    if (dev < 64) configured[dev] = true;
+    if (dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   // about one row per warp, at most one CTA per SM
   int grid = (capacity + kLvbWarps - 1) / kLvbWarps;
