@@ -22,7 +22,10 @@
  *   too short for its sequence) never trap: the offending entry is skipped
  *   (treated as masked / written as -1) and a sticky bit is set in a device
  *   error word, read with pkv_get_error_flags() after synchronising.
- * - The library keeps no state between calls apart from that error word.
+ * - The library keeps no state between calls apart from that error word
+ *   (and per-device lookups made once).  Entry points may be called from
+ *   several host threads at once; each call must own its workspace and
+ *   outputs, and the error word is shared by all calls on a device.
  */
 #ifndef PKV_H
 #define PKV_H
