@@ -366,7 +366,7 @@ double orc_e4m3_value(uint8_t code) {
 
 uint8_t orc_e4m3_round(double x) {
   if (isnan(x)) return 0x7f;
-  const uint8_t sign = x < 0 ? 0x80 : 0x00;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;  /* -0.0 keeps its sign */
   const double a = fabs(x);
   /* nearest of the non-negative codes 0..127, code 127 standing for the
      value 480 the format does not have (choosing it means "NaN") */
