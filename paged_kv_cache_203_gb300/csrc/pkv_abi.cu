@@ -174,19 +174,20 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
     plan->n_row_tiles = 0;
     int splits = num_splits;
     if (splits == 0) {
-      // Each CTA pays a fixed start (Q into TMEM and shared memory, the index
-      // look-ahead) and a split adds a merge, so lists are split only as far
-      // as needed to give every SM a CTA (one CTA per SM fits).
-      const int64_t base = std::max<int64_t>(1, total_q * 2);
-      splits = static_cast<int>((kNumSMs + base - 1) / base);
-      splits = std::max(1, std::min<int>(splits, static_cast<int>(topk.shape[1] / 256)));
+      // One 2-CTA cluster per (token, split).  Each cluster pays a fixed
+      // start (Q into TMEM, the pipeline fill) and a split adds a 256 KB
+      // partial and a merge, so lists are split only as far as needed to
+      // give every SM pair a cluster, and never below 512 keys a split.
+      const int64_t base = std::max<int64_t>(1, total_q);
+      splits = static_cast<int>((kNumSMs / 2 + base - 1) / base);
+      splits = std::max(1, std::min<int>(splits, static_cast<int>(topk.shape[1] / 512)));
     }
     splits = std::min(splits, kMlaMaxSplits);
     plan->num_splits = splits;
     const size_t rows_total = static_cast<size_t>(total_q) * h_q;
     plan->ws_o_bytes = align256(static_cast<size_t>(splits) * rows_total * dv * 4);
-    plan->ws_lse_bytes = align256(2 * static_cast<size_t>(splits) * rows_total * 4);
-    plan->ws_ctr_bytes = align256(static_cast<size_t>(total_q) * 2 * 4);
+    plan->ws_lse_bytes = align256(static_cast<size_t>(splits) * rows_total * 4);
+    plan->ws_ctr_bytes = align256(static_cast<size_t>(total_q) * 4);
     return PKV_OK;
   }
   if (!((d == 128 && dv == 128) || (d == 64 && dv == 64)))

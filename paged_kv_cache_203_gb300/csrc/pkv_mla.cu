@@ -1,5 +1,6 @@
 // pkv_mla.cu -- absorbed-MLA paged attention over top-k sparse key lists on
-// the 5th-generation tensor cores (tcgen05 + TMEM).
+// the 5th-generation tensor cores (tcgen05 + TMEM), one 2-CTA cluster per
+// (query token, chunk of its key list).
 //
 // Computes the absorbed multi-latent attention of flashattention_backend.py
 // (`flash_attn_with_kvcache(q=q_rope, k_cache=k_rope, v_cache=c_kv,
@@ -7,35 +8,38 @@
 // the keys listed in each query's top-k row (nsa_backend.py `forward_decode`,
 // `TopkTransformMethod.PAGED`: logical position -> page-table slot; -1 =
 // skip).  Each key is one 576-wide latent row (512 c_kv + 64 k_rope); its
-// first 512 entries are the value row, so every gathered row is read once.
+// first 512 entries are the value row.
 //
-// One CTA = (query token, 256-wide half of the value dims, chunk of its key
-// list).  The output accumulator for 128 heads x 256 value dims fills half
-// of TMEM; both halves recompute the scores (the full 128 x 512 accumulator
-// would leave no TMEM columns for them).  The first 448 columns of Q live in
-// TMEM as the A operand of Q K^T and the other 128 in shared memory, which
-// leaves shared memory for five 32-key tiles: the gather is the limit, and
-// a deeper ring measured faster than wider tiles (2 x 64 keys: 866 GB/s,
-// 3 x 48: 1303, 5 x 32: 1357).
-//   warps 5-12 producers: per 32-key tile, gather the 576-wide rows with
-//            16-byte cp.async into a [9 chunks][32 rows][128 B] 128-byte-
-//            swizzled tile (zero rows for skipped keys), four rows per warp,
-//            completion on mbarriers, up to five tiles in flight.  The list
-//            entries and page ids of a tile are loaded one and two tiles
-//            ahead, so the two dependent lookups stay off the copy path
-//            (with them on it, each tile waited two global round trips);
-//   warp 4   MMA issuer: S = Q K^T (M 128 heads, N 32 keys, K 576: 36
-//            MMAs, K-major), then O += P V (M 128, N 256 value dims, K 32
-//            keys: V is an MN-major view of the same key tile).  Descriptors
-//            are formed once per tile and the K steps fully unrolled (a lone
-//            issuing thread that rebuilt them per step took longer than the
-//            MMAs);
-//   warps 0-3 softmax (thread = head = TMEM lane): scores from TMEM, masks,
-//            online softmax in the log2 domain with a lazy reference max
-//            (O rescaled in TMEM only when the row max grows by > 2^8), P
-//            (bf16) to shared memory in the unswizzled core-matrix layout.
-// Split lists are merged by the last CTA of each (token, half).  Every wait
-// is bounded (PKV_EFLAG_TIMEOUT on expiry).
+// TMEM holds 512 fp32 columns per SM: the 128 x 512 output accumulator fills
+// all of it, leaving nothing for the scores.  So the work of one (token,
+// chunk) is split by kind, not by value columns, over the two CTAs of a
+// cluster, and every score is computed once:
+//   rank 0 ("score CTA"): Q (all 576 columns, bf16) in TMEM as the A operand;
+//     per 64-key tile S = Q K^T (M 128 heads, N 64 keys, K 576: 36 MMAs) into
+//     one of two TMEM score buffers; four softmax warps (thread = head) add
+//     the key mask, run the online softmax in the log2 domain with a lazy
+//     reference max, and store P (bf16) and the per-head rescale factors
+//     straight into the value CTA's shared memory (distributed shared-memory
+//     stores, an async-proxy fence, a remote barrier arrive).  At the end it
+//     sends 1/l and the lse of each head.
+//   rank 1 ("value CTA"): O (128 x 512 fp32) in all of TMEM; per tile
+//     O += P V (M 128, N 2 x 256 value columns, K 64 keys: 8 MMAs); when the
+//     score CTA raised a head's reference max, its four epilogue warps
+//     rescale those O rows in TMEM first.  Epilogue: O * (1/l) -> bf16 output
+//     (or a split partial, merged by the last CTA of the token).
+// Each CTA gathers the columns it needs of every listed row (score CTA: 576,
+// value CTA: the first 512) with 16-byte cp.async into 128-byte-swizzled
+// [chunks][64 keys][128 B] tiles, three stages each, so neither pipeline
+// waits on the other's stage recycling; the second read of a row is an L2
+// hit.  (Gathering each row once and exchanging halves between the CTAs was
+// measured slower: the exchange ties the score CTA's stages to the value
+// CTA's, which are freed only after the softmax and PV.)  The gather loop is
+// bound by its issue rate through the shared-memory/MIO pipe, which it shares
+// with shuffles and barrier polls, so row offsets are broadcast once per tile
+// and every wait sleeps in hardware between polls.
+// Warps: 0-3 softmax (score) / epilogue + rescale (value); 4 MMA issuer;
+// 5 forwarder of "P consumed" to the score CTA (value CTA; idle in the score
+// CTA); 6-13 producers.  Every wait is bounded (PKV_EFLAG_TIMEOUT on expiry).
 #include <limits.h>
 #include <string.h>
 
@@ -51,85 +55,128 @@ using namespace ptx;
 constexpr int H = 128;        // query heads (the M dimension)
 constexpr int DQK = 576;      // latent + rope
 constexpr int DV = 512;       // latent (value) dims
-constexpr int DVH = 256;      // value dims per CTA
-constexpr int BKEYS = 32;     // keys per tile
-constexpr int NSTG = 5;       // key-tile stages
-constexpr int NCH_TM = 7;     // 64-column Q chunks held in TMEM (A operand)
-constexpr int NCH = DQK / 64; // 64-column chunks of a row (9)
+constexpr int BK = 64;        // keys per tile
+constexpr int NCH = DQK / 64; // 64-column (128-byte) chunks of a key row (9)
+constexpr int NSTG = 3;       // stages on each side
 constexpr int NSOFT = 4, NPROD = 8;
 constexpr int kMmaWarp = NSOFT;
-constexpr int kProdWarp0 = NSOFT + 1;
-constexpr int NTHREADS = (NSOFT + 1 + NPROD) * 32;
-constexpr int kRowsPerWarp = BKEYS / NPROD;         // 4
-constexpr uint32_t kQBytes = (NCH - NCH_TM) * H * 128;  // the shared-memory part: 49152
-// TMEM columns: S (32) | Q chunks 0-6 (224) | O (256)
-constexpr uint32_t kTmS = 0, kTmQ = 32, kTmO = 256;
-static_assert(BKEYS <= kTmQ, "S fits its TMEM columns");
-static_assert(kTmQ + NCH_TM * 32 <= kTmO, "TMEM plan overflows");
-constexpr uint32_t kKTile = NCH * BKEYS * 128;      // 36864
-constexpr int kLook = 2;                          // look-ahead of each lookup level (tiles)
-constexpr int kRingA = 2 * kLook + 1, kRingB = kLook + 1;
-constexpr uint32_t kPTile = H * BKEYS * 2;          // 8192
+constexpr int kFwdWarp = NSOFT + 1;
+constexpr int kProdWarp0 = NSOFT + 2;
+constexpr int NTHREADS = (NSOFT + 2 + NPROD) * 32;  // 448
+constexpr int kRowsPerWarp = BK / NPROD;            // 8
+constexpr uint32_t kChunk = BK * 128;               // 8192: one chunk of a tile
+constexpr uint32_t kKTile = NCH * kChunk;           // 73728 (score CTA: all 9 chunks)
+constexpr uint32_t kVTile = 8 * kChunk;             // 65536 (value CTA: chunks 0-7)
+constexpr uint32_t kPTile = H * BK * 2;             // 16384: P [128 heads][64 keys] bf16
+constexpr uint32_t kFacWarp = 144;                  // 32 factors, a flag word, padding
+constexpr uint32_t kPXfer = kPTile + NSOFT * kFacWarp;  // 16960 bytes per P buffer
+constexpr uint32_t kFinBytes = H * 8;               // (1/l, lse) per head
+// TMEM columns.  Score CTA: Q [0, 288) as packed bf16 pairs, S0 at 384, S1 at
+// 448.  Value CTA: O [0, 512).
+constexpr uint32_t kTmQ = 0, kTmS = 384;
+static_assert(kTmQ + DQK / 2 <= kTmS && kTmS + 2 * BK <= 512, "TMEM plan");
 
 struct Smem {
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kQBytes;          // NSTG stages
-  static constexpr uint32_t kP = kK + NSTG * kKTile;
-  static constexpr uint32_t kPos = kP + kPTile;         // int [NSTG][BKEYS]
-  // producers' look-ahead rings, per warp: list entries [RA][8], page ids [RB][8]
-  static constexpr uint32_t kRing = kPos + NSTG * BKEYS * 4;
-  static constexpr uint32_t kBar = kRing + NPROD * (kRingA + kRingB) * kRowsPerWarp * 4;
-  // q_full, full[NSTG], empty[NSTG], s_full, s_free, p_full, o_done, q_tmem
-  static constexpr int kNumBars = 2 * NSTG + 6;
-  static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
-  static constexpr uint32_t kFlag = kTmemSlot + 16;     // softmax: split ticket
-  static constexpr uint32_t kEnd = kFlag + 16;
+  // score CTA
+  static constexpr uint32_t kK = 0;                          // NSTG key tiles
+  static constexpr uint32_t kBias = kK + NSTG * kKTile;      // float [NSTG][BK]: 0 or -inf
+  // value CTA
+  static constexpr uint32_t kV = 0;                          // NSTG value tiles
+  static constexpr uint32_t kP = kV + NSTG * kVTile;         // P as received [2][kPXfer]
+  static constexpr uint32_t kFin = kP + 2 * kPXfer;          // float2 [H]
+  // both (same offsets in both CTAs: each CTA addresses the peer's barriers
+  // by their local offsets)
+  static constexpr uint32_t kCtl = kFin + kFinBytes;
+  static constexpr int kNumBars = 16;
+  static constexpr uint32_t kTmemSlot = kCtl + kNumBars * 8;
+  static constexpr uint32_t kWord = kTmemSlot + 16;          // int[4]: ticket, rescale tile
+  static constexpr uint32_t kEnd = kWord + 16;
   static constexpr size_t kDynamic = kEnd;  // base must be 1024-aligned (checked)
 };
+static_assert(Smem::kBias + NSTG * BK * 4 <= Smem::kCtl, "score-CTA plan overlaps the control block");
 static_assert(Smem::kDynamic <= 232448, "shared memory plan exceeds 227 KB");
+static_assert(kPXfer % 16 == 0 && kFacWarp % 16 == 0, "16-byte aligned P buffers");
+
 enum BarId {
-  Q_FULL = 0,
-  FULL = 1,
-  EMPTY = FULL + NSTG,
-  S_FULL = EMPTY + NSTG,
-  S_FREE = S_FULL + 1,
-  P_FULL = S_FREE + 1,
-  O_DONE = P_FULL + 1,
-  Q_TMEM = O_DONE + 1
+  FULL = 0,          // [3] the stage's rows landed (producers' cp.async)
+  EMPTY = 3,         // [3] the stage was consumed
+  P_FREE = 6,        // [2] score CTA: the value CTA finished the PV of P buffer b (remote)
+  S_FULL = 8,        // [2] score CTA: QK^T done      | value CTA: P_FULL (4 remote arrivals)
+  P_FULL = 8,
+  S_FREE = 10,       // [2] score CTA: S read         | value CTA: PV_DONE
+  PV_DONE = 10,
+  Q_TMEM = 12,       //     score CTA: Q is in TMEM   | value CTA: O_DONE (each PV done)
+  O_DONE = 12,
+  CORR_REQ = 13,     // value CTA: rescale request (or stop) to the epilogue warps
+  CORR_DONE = 14,    // value CTA: rescale done
+  FIN = 15           // value CTA: (1/l, lse) landed (4 remote arrivals)
 };
 
-// byte offset of 16-byte chunk c (0..71) of row r in a 128-byte-swizzled
-// [9][nrows][128 B] tile
-template <int NROWS>
+// byte offset of 16-byte unit c (0..71) of row r in a 128-byte-swizzled
+// [chunks][BK rows][128 B] tile
 __device__ __forceinline__ uint32_t sw_off(int r, int c) {
-  return static_cast<uint32_t>((c >> 3) * (NROWS * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+  return static_cast<uint32_t>((c >> 3) * kChunk + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
-// P [128 heads][BKEYS keys] bf16, unswizzled core matrices: 8 rows x 16 B,
-// 128 B apart along the keys, BKEYS * 16 B apart along the heads
+// P [128 heads][64 keys] bf16 in unswizzled core matrices (8 heads x 16 B):
+// 128 B apart along the keys, 1024 B apart along the heads.
 __device__ __forceinline__ uint32_t p_off(int m, int c) {
-  return static_cast<uint32_t>((m >> 3) * (BKEYS * 16) + c * 128 + (m & 7) * 16);
+  return static_cast<uint32_t>((m >> 3) * (BK * 16) + c * 128 + (m & 7) * 16);
 }
 
-struct MlaMaps {
-  CUtensorMap q;
+// One producer lane's view of a key: list position -> slot row offset.
+struct RowRef {
+  int pos;      // logical key position, or -1 (no key)
+  int64_t off;  // element offset of its row in the cache, or -1
 };
 
-__global__ void __launch_bounds__(NTHREADS, 1)
-mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ MlaMaps maps) {
+__device__ __forceinline__ int list_entry(const AttnParams &p, const int32_t *list, int j,
+                                          int end_j) {
+  return (j < end_j && j < p.topk_len) ? __ldg(list + j) : -1;
+}
+// Page id of a list entry: the page-table load (or -1: no key / bad entry,
+// -2: the row is too short).
+__device__ __forceinline__ int page_of(const AttnParams &p, int b, int e, int kv_len) {
+  if (e < 0 || e >= kv_len) return -1;
+  const int pidx = e / p.page_size;
+  if (pidx >= p.pt_cols) return -2;
+  return __ldg(p.page_table + static_cast<int64_t>(b) * p.pt_stride + pidx);
+}
+__device__ __forceinline__ RowRef resolve(const AttnParams &p, int e, int pc, int kv_len,
+                                          bool report) {
+  RowRef r{-1, -1};
+  if (e < -1 || e >= kv_len) {
+    if (report && e != -1) atomicOr(p.err, PKV_EFLAG_TOPK_OOB);
+  } else if (e >= 0) {
+    if (pc == -2) {
+      if (report) atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
+    } else if (pc < 0 || pc >= p.num_pages) {
+      if (report) atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
+    } else {
+      r.pos = e;
+      r.off = static_cast<int64_t>(pc) * p.k_sp +
+              static_cast<int64_t>(e - (e / p.page_size) * p.page_size) * p.k_spos;
+    }
+  }
+  return r;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+mla_topk_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_addr(smem);
-  int *sPos = reinterpret_cast<int *>(smem + Smem::kPos);
   uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + Smem::kTmemSlot);
-  int *sFlag = reinterpret_cast<int *>(smem + Smem::kFlag);
-  auto bar = [&](int id) { return sbase + Smem::kBar + 8u * id; };
+  volatile int *sWord = reinterpret_cast<volatile int *>(smem + Smem::kWord);
+  auto bar = [&](int id) { return sbase + Smem::kCtl + 8u * id; };
 
-  const int split = blockIdx.x;
-  const int hv = blockIdx.y;        // value half
-  const int t = blockIdx.z;         // query token
+  const uint32_t rank = cluster_ctarank();  // 0: scores + softmax, 1: values
+  const uint32_t peer = rank ^ 1u;
+  const bool score = rank == 0;
+  const int split = blockIdx.x >> 1;
+  const int t = blockIdx.z;                 // query token
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  if ((sbase & 1023u) != 0) {
+  if ((sbase & 1023u) != 0) {  // the same in both CTAs of a launch
     if (tid == 0) atomicOr(p.err, PKV_EFLAG_LAYOUT);
     return;
   }
@@ -149,246 +196,294 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
   const int kv_len = covered ? p.cache_seqlens[b] : 0;
   const int i_pos = kv_len - q_len + (t - q_begin);  // absolute position of the token
 
-  // this split's 32-key tiles of the token's list
-  const int n_tiles_all = covered ? (p.topk_len + BKEYS - 1) / BKEYS : 0;
+  // this split's 64-key tiles of the token's list
+  const int n_tiles_all = covered ? (p.topk_len + BK - 1) / BK : 0;
   const int per = (n_tiles_all + p.num_splits - 1) / p.num_splits;
   const int tile0 = min(n_tiles_all, split * per);
   const int n_kv = min(n_tiles_all, tile0 + per) - tile0;
 
+  if (score && warp < NSOFT && covered) {  // warm L2 with this head's Q row
+    const bf16 *qrow = p.q + static_cast<int64_t>(t) * p.q_st + static_cast<int64_t>(tid) * p.q_sh;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) prefetch_line_l2(qrow + i * 64);
+  }
   if (tid == 0) {
-    mbar_init(bar(Q_FULL), 1);
     for (int s = 0; s < NSTG; ++s) {
       mbar_init(bar(FULL + s), NPROD * 32);
-      mbar_init(bar(EMPTY + s), 1);
+      mbar_init(bar(EMPTY + s), score ? 1 + NSOFT : 1);
     }
-    mbar_init(bar(S_FULL), 1);
-    mbar_init(bar(S_FREE), NSOFT);
-    mbar_init(bar(P_FULL), NSOFT);
-    mbar_init(bar(O_DONE), 1);
-    mbar_init(bar(Q_TMEM), NSOFT);
+    if (score) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(bar(S_FULL + i), 1);
+        mbar_init(bar(S_FREE + i), NSOFT);
+        mbar_init(bar(P_FREE + i), 1);
+      }
+      mbar_init(bar(Q_TMEM), NSOFT);
+    } else {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(bar(P_FULL + i), NSOFT);
+        mbar_init(bar(PV_DONE + i), 1);
+      }
+      mbar_init(bar(O_DONE), 1);
+      mbar_init(bar(CORR_REQ), 1);
+      mbar_init(bar(CORR_DONE), NSOFT);
+      mbar_init(bar(FIN), NSOFT);
+    }
     mbar_init_fence();
   }
   if (warp == kMmaWarp) tmem_alloc(smem_addr(sTmem), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_sync();  // both CTAs' barriers are initialised before any remote use
   const uint32_t tmem = *sTmem;
-  const uint32_t tS0 = tmem + kTmS, tQ = tmem + kTmQ, tO = tmem + kTmO;
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const int end_j = (tile0 + n_kv) * BK;
+  const int32_t *list = p.topk + static_cast<int64_t>(t) * p.topk_stride;
+  const uint32_t ring = sbase + (score ? Smem::kK : Smem::kV);
+  const uint32_t tile_bytes = score ? kKTile : kVTile;
 
   if (warp >= kProdWarp0) {
     // ================================ producers ================================
-    const int ptid = tid - kProdWarp0 * 32;  // 0..127
-    if (ptid == 0 && n_kv > 0) {
-      mbar_arrive_expect_tx(bar(Q_FULL), kQBytes);
-#pragma unroll 1
-      for (int c = NCH_TM; c < NCH; ++c)
-        tma_load_3d(sbase + Smem::kQ + (c - NCH_TM) * (H * 128), &maps.q, c * 64, 0, t,
-                    bar(Q_FULL));
+    // Lane l < 8 of producer warp pw owns row pw * 8 + l of every tile.  Its
+    // list entry is loaded kAhead + kLagP + kLagE tiles ahead, its page id
+    // kAhead + kLagP tiles ahead and the row resolved kAhead tiles ahead, all
+    // in registers: each load has kLagE (kLagP) iterations to land before its
+    // value is used, since loads issued behind the SM's in-flight gathers
+    // take as long as the gathers.  Per tile: wait for the stage, gather this
+    // CTA's columns of the 64 rows (zeros for skipped keys), and (score CTA)
+    // publish each key's additive mask: 0, or -inf for no key / outside the
+    // causal or window bound.
+    constexpr int kAhead = 2, kLagP = 3, kLagE = 3;
+    const int pw = warp - kProdWarp0;
+    const bool own = lane < kRowsPerWarp;
+    const int myrow = pw * kRowsPerWarp + lane;
+    const bool use_upper = p.causal || p.window_left >= 0;
+    const int lo_r = p.window_left >= 0 ? i_pos - p.window_left : INT_MIN;
+    auto entry = [&](int tile) {
+      return (own && tile < n_kv) ? list_entry(p, list, (tile0 + tile) * BK + myrow, end_j) : -1;
+    };
+    auto page = [&](int e) { return own ? page_of(p, b, e, kv_len) : -1; };
+    auto res = [&](int e, int pg) {
+      return own ? resolve(p, e, pg, kv_len, score) : RowRef{-1, -1};
+    };
+    RowRef rr[kAhead + 1];        // rows of tiles jj .. jj + kAhead
+    int E[kLagP + kLagE + 1];     // entries of tiles jj + kAhead .. + kLagP + kLagE
+    int G[kLagP + 1];             // page ids of tiles jj + kAhead .. + kLagP
+#pragma unroll
+    for (int k = 0; k < kAhead; ++k) {
+      const int e = entry(k);
+      rr[k] = res(e, page(e));
     }
-    const int32_t *list = p.topk + static_cast<int64_t>(t) * p.topk_stride;
-    const int pw = warp - kProdWarp0;  // producer warp: rows pw + 8 i of each tile
-    const int end_j = (tile0 + n_kv) * BKEYS;
-    // Lane i < 8 of producer warp pw owns row pw + 8 i of every tile.  Its
-    // list entry is fetched 2 * kLook tiles ahead and its page id kLook tiles
-    // ahead, both with 4-byte cp.async into this warp's rings (one commit
-    // group per tile), so no global load is waited on in the copy loop.
-    const int myrow = pw + NPROD * lane;
-    const bool keyl = lane < kRowsPerWarp;
-    int *ringA = reinterpret_cast<int *>(smem + Smem::kRing) +
-                 pw * (kRingA + kRingB) * kRowsPerWarp;
-    int *ringB = ringA + kRingA * kRowsPerWarp;
-    const uint32_t ringA_s = sbase + Smem::kRing + pw * (kRingA + kRingB) * kRowsPerWarp * 4;
-    const uint32_t ringB_s = ringA_s + kRingA * kRowsPerWarp * 4;
-    auto fetchA = [&](int tile) {  // list entry of this lane's row (or -1)
-      if (!keyl) return;
-      const int slot = (tile % kRingA) * kRowsPerWarp + lane;
-      const int j = (tile0 + tile) * BKEYS + myrow;
-      if (tile < n_kv && j < end_j && j < p.topk_len) cp_async4(ringA_s + slot * 4, list + j);
-      else ringA[slot] = -1;
-    };
-    auto fetchB = [&](int tile) {  // page id of that entry (-1: no key, -2: row too short)
-      if (!keyl) return;
-      const int idx = ringA[(tile % kRingA) * kRowsPerWarp + lane];
-      const int slot = (tile % kRingB) * kRowsPerWarp + lane;
-      if (idx >= 0 && idx < kv_len) {
-        const int pidx = idx / p.page_size;
-        if (pidx < p.pt_cols)
-          cp_async4(ringB_s + slot * 4,
-                    p.page_table + static_cast<int64_t>(b) * p.pt_stride + pidx);
-        else
-          ringB[slot] = -2;
-      } else {
-        ringB[slot] = -1;
-      }
-    };
-    for (int x = 0; x < 2 * kLook; ++x) fetchA(x);
-    cp_async_commit();
-    cp_async_wait_all();
-    for (int x = 0; x < kLook; ++x) fetchB(x);
-    cp_async_commit();
-    cp_async_wait_all();
+#pragma unroll
+    for (int k = 0; k < kLagP + kLagE; ++k) E[k] = entry(kAhead + k);
+#pragma unroll
+    for (int k = 0; k < kLagP; ++k) G[k] = page(E[k]);
+    float *sBias = reinterpret_cast<float *>(smem + Smem::kBias);
     for (int jj = 0; jj < n_kv; ++jj) {
       const int s = jj % NSTG;
-      // entries of tile jj + kLook and page ids of tile jj have landed
-      cp_async_wait_group<kLook - 1>();
-      fetchB(jj + kLook);
-      fetchA(jj + 2 * kLook);
-      cp_async_commit();
-      // this lane's row of tile jj: position (or -1) and row offset
-      int pos = -1;
-      int64_t off = -1;
-      if (keyl) {
-        const int ic = ringA[(jj % kRingA) * kRowsPerWarp + lane];
-        const int64_t pc = ringB[(jj % kRingB) * kRowsPerWarp + lane];
-        if (ic < -1 || ic >= kv_len) {
-          if (ic != -1) atomicOr(p.err, PKV_EFLAG_TOPK_OOB);
-        } else if (ic >= 0) {
-          if (pc == -2) {
-            atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
-          } else if (pc < 0 || pc >= p.num_pages) {
-            atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
-          } else {
-            pos = ic;
-            off = pc * p.k_sp +
-                  static_cast<int64_t>(ic - (ic / p.page_size) * p.page_size) * p.k_spos;
-          }
-        }
-      }
+      E[kLagP + kLagE] = entry(jj + kAhead + kLagP + kLagE);
+      G[kLagP] = page(E[kLagP]);
+      rr[kAhead] = res(E[0], G[0]);
       int ok = 1;
       if (lane == 0 && jj >= NSTG)
-        ok = mbar_wait(bar(EMPTY + s), ((jj / NSTG) & 1) ^ 1) ? 1 : 0;
+        ok = mbar_wait_sleep(bar(EMPTY + s), ((jj / NSTG) & 1) ^ 1) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
         break;
       }
-      if (keyl) sPos[s * BKEYS + myrow] = pos;
-      // gather this warp's rows: 72 chunks of 16 B each, lanes along the row
-      const uint32_t kdst = sbase + Smem::kK + s * kKTile;
-#pragma unroll 2
-      for (int i = 0; i < kRowsPerWarp; ++i) {
-        const int r = pw + NPROD * i;
-        const int64_t ro = __shfl_sync(0xffffffffu, off, i);
-        const bf16 *src = ro >= 0 ? p.k + ro : p.k;
-        const int nbytes = ro >= 0 ? 16 : 0;
+      const uint32_t dst0 = ring + s * tile_bytes;
+      if (score && own) {
+        const int pos = rr[0].pos;
+        const bool vis = pos >= 0 && !(use_upper && pos > i_pos) && pos >= lo_r;
+        sBias[s * BK + myrow] = vis ? 0.f : -INFINITY;
+      }
+      // the warp's 8 row offsets, broadcast once (shuffles share the pipe
+      // with the copies and barrier polls); skipped keys read zeros
+      int64_t ro[kRowsPerWarp];
 #pragma unroll
-        for (int c = lane; c < DQK / 8; c += 32)
-          cp_async16(kdst + sw_off<BKEYS>(r, c), ro >= 0 ? src + c * 8 : src, nbytes);
+      for (int r = 0; r < kRowsPerWarp; ++r) ro[r] = __shfl_sync(0xffffffffu, rr[0].off, r);
+      // value chunks 0-7: half a row (512 B) per instruction, row known at
+      // compile time
+#pragma unroll
+      for (int i = 0; i < 2 * kRowsPerWarp; ++i) {
+        const int rl = i >> 1;
+        const int c = lane + 32 * (i & 1);
+        const bf16 *src = ro[rl] >= 0 ? p.k + ro[rl] + c * 8 : p.k;
+        cp_async16(dst0 + sw_off(pw * kRowsPerWarp + rl, c), src, ro[rl] >= 0 ? 16 : 0);
+      }
+      if (score) {
+        // the rope chunk (8): 4 rows per instruction
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int rl = (lane >> 3) + 4 * i;
+          const int c = (NCH - 1) * 8 + (lane & 7);
+          const int64_t r8 = __shfl_sync(0xffffffffu, rr[0].off, rl);
+          const bf16 *src = r8 >= 0 ? p.k + r8 + c * 8 : p.k;
+          cp_async16(dst0 + sw_off(pw * kRowsPerWarp + rl, c), src, r8 >= 0 ? 16 : 0);
+        }
       }
       cp_async_arrive(bar(FULL + s));
       mbar_arrive(bar(FULL + s));
+#pragma unroll
+      for (int k = 0; k < kAhead; ++k) rr[k] = rr[k + 1];
+#pragma unroll
+      for (int k = 0; k < kLagP + kLagE; ++k) E[k] = E[k + 1];
+#pragma unroll
+      for (int k = 0; k < kLagP; ++k) G[k] = G[k + 1];
     }
+    cp_async_wait_all();
   } else if (warp == kMmaWarp) {
     // ================================== MMA ==================================
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16(H, BKEYS, false);
-      constexpr uint32_t kIdescPV = idesc_bf16(H, DVH, true);
-      bool ok = n_kv == 0 || (mbar_wait(bar(Q_FULL), 0) && mbar_wait(bar(Q_TMEM), 0));
-      const uint64_t qd0 = smem_desc(sbase + Smem::kQ, 0, 1024, 2);
-      const uint64_t pd0 = smem_desc(sbase + Smem::kP, 128, BKEYS * 16, 0);
-      for (int j = 0; ok && j <= n_kv; ++j) {
-        if (j < n_kv) {  // S_j = Q K_j^T (S is free once the softmax loaded S_{j-1})
-          const int s = j % NSTG;
-          ok = mbar_wait(bar(FULL + s), (j / NSTG) & 1) &&
-               (j < 1 || mbar_wait(bar(S_FREE), (j - 1) & 1));
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t kd0 = smem_desc(sbase + Smem::kK + s * kKTile, 0, 1024, 2);
-          // K step ks: 16 columns = 32 bytes within chunk ks / 4 (descriptor
-          // addresses are in 16-byte units)
+    if (lane == 0 && score) {
+      constexpr uint32_t kIdescQK = idesc_bf16(H, BK, false);
+      bool ok = n_kv == 0 || mbar_wait_sleep(bar(Q_TMEM), 0);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j % NSTG, bb = j & 1;
+        ok = mbar_wait_sleep(bar(FULL + s), (j / NSTG) & 1) &&
+             (j < 2 || mbar_wait_sleep(bar(S_FREE + bb), ((j >> 1) - 1) & 1));
+        if (!ok) break;
+        fence_proxy_async();
+        tc_fence_after();
+        const uint64_t kd0 = smem_desc(ring + s * kKTile, 0, 1024, 2);
+        const uint32_t dS = tmem + kTmS + bb * BK;
+        // K step ks: 16 columns = 32 bytes within chunk ks / 4 (descriptor
+        // addresses are in 16-byte units); A = Q columns from TMEM
 #pragma unroll
-          for (int ks = 0; ks < NCH_TM * 4; ++ks)  // A = Q columns from TMEM
-            umma_ts(tS0, tQ + ks * 8,
-                    kd0 + static_cast<uint64_t>(((ks >> 2) * (BKEYS * 128) + (ks & 3) * 32) >> 4),
-                    kIdescQK, ks > 0 ? 1u : 0u);
-#pragma unroll
-          for (int ks = NCH_TM * 4; ks < DQK / 16; ++ks)  // A = Q columns from smem
-            umma(tS0,
-                 qd0 + static_cast<uint64_t>((((ks >> 2) - NCH_TM) * (H * 128) + (ks & 3) * 32) >> 4),
-                 kd0 + static_cast<uint64_t>(((ks >> 2) * (BKEYS * 128) + (ks & 3) * 32) >> 4),
-                 kIdescQK, 1u);
-          umma_commit(bar(S_FULL));
-        }
-        if (j >= 1) {  // O += P_{j-1} V_{j-1}
-          const int jj = j - 1;
-          const int s = jj % NSTG;
-          ok = mbar_wait(bar(P_FULL), jj & 1);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t vd0 =
-              smem_desc(sbase + Smem::kK + s * kKTile + hv * 4 * (BKEYS * 128), BKEYS * 128, 1024, 2);
-#pragma unroll
-          for (int ks = 0; ks < BKEYS / 16; ++ks)  // 16 keys = 2 P chunks = 2 V row groups
-            umma(tO, pd0 + static_cast<uint64_t>((ks * 256) >> 4),
-                 vd0 + static_cast<uint64_t>((ks * 2048) >> 4), kIdescPV,
-                 (jj > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(bar(O_DONE));
-          umma_commit(bar(EMPTY + s));
-        }
+        for (int ks = 0; ks < DQK / 16; ++ks)
+          umma_ts(dS, tmem + kTmQ + ks * 8,
+                  kd0 + static_cast<uint64_t>(((ks >> 2) * kChunk + (ks & 3) * 32) >> 4),
+                  kIdescQK, ks > 0 ? 1u : 0u);
+        umma_commit(bar(S_FULL + bb));
+        umma_commit(bar(EMPTY + s));
       }
       if (!ok) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+    } else if (lane == 0) {
+      constexpr uint32_t kIdescPV = idesc_bf16(H, 256, true);
+      bool ok = true;
+      int n_corr = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % NSTG, bb = j & 1;
+        ok = mbar_wait_sleep(bar(FULL + s), (j / NSTG) & 1) &&
+             mbar_wait_cluster_sleep(bar(P_FULL + bb), (j >> 1) & 1);
+        if (!ok) break;
+        // did the score CTA raise any head's reference max for this tile?
+        const uint8_t *fac = smem + Smem::kP + bb * kPXfer + kPTile;
+        int any = 0;
+#pragma unroll
+        for (int w = 0; w < NSOFT; ++w)
+          any |= *reinterpret_cast<const volatile int *>(fac + w * kFacWarp + 128);
+        if (any) {
+          sWord[1] = j;
+          mbar_arrive(bar(CORR_REQ));
+          ok = mbar_wait_sleep(bar(CORR_DONE), n_corr & 1);
+          ++n_corr;
+          if (!ok) break;
+        }
+        fence_proxy_async();
+        tc_fence_after();
+        const uint64_t pd0 = smem_desc(sbase + Smem::kP + bb * kPXfer, 128, BK * 16, 0);
+#pragma unroll
+        for (int ks = 0; ks < BK / 16; ++ks) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint64_t vd = smem_desc(ring + s * kVTile + h * 4 * kChunk, kChunk, 1024, 2);
+            umma(tmem + h * 256, pd0 + static_cast<uint64_t>((ks * 256) >> 4),
+                 vd + static_cast<uint64_t>((ks * 2048) >> 4), kIdescPV,
+                 (j > 0 || ks > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(bar(EMPTY + s));
+        umma_commit(bar(PV_DONE + bb));
+        umma_commit(bar(O_DONE));
+      }
+      if (!ok) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+      sWord[1] = -1;  // stop the epilogue warps' rescale loop
+      mbar_arrive(bar(CORR_REQ));
     }
-  } else {
-    // ================================ softmax ================================
+  } else if (warp == kFwdWarp) {
+    // ======================= forwarder (value CTA only) =======================
+    // The PV of P buffer b is done: tell the score CTA it may refill it.
+    if (!score && lane == 0) {
+      const uint32_t remote0 = map_to_cta(bar(P_FREE), peer);
+      for (int j = 0; j < n_kv; ++j) {
+        const int bb = j & 1;
+        if (!mbar_wait_sleep(bar(PV_DONE + bb), (j >> 1) & 1)) {
+          atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+          break;
+        }
+        mbar_arrive_remote(remote0 + 8u * bb);
+      }
+    }
+  } else if (score) {
+    // ============================ softmax (score CTA) ============================
     const int row = tid;  // head = TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const float c = p.scale_log2;
-    const bool use_upper = p.causal || p.window_left >= 0;
-    const int lo_r = p.window_left >= 0 ? i_pos - p.window_left : INT_MIN;
     float m_ref = -INFINITY;
     float l = 0.f;
     bool ok = true;
+    const uint32_t peer_P = map_to_cta(sbase + Smem::kP, peer);
+    const uint32_t peer_pfull = map_to_cta(bar(P_FULL), peer);
     if (n_kv > 0) {
-      // Q row `row`, columns 0..447, as packed bf16 pairs into TMEM columns
-      // tQ .. tQ + 223 of this thread's lane (the A operand of Q K^T)
+      // Q row `row` (576 bf16) as packed pairs into TMEM columns 0..287 of
+      // this thread's lane: the A operand of Q K^T (three 192-column loads
+      // in flight at a time; the row's lines were warmed at kernel start)
       const uint4 *qsrc = reinterpret_cast<const uint4 *>(
           p.q + static_cast<int64_t>(t) * p.q_st + static_cast<int64_t>(row) * p.q_sh);
 #pragma unroll 1
-      for (int cb = 0; cb < NCH_TM; ++cb) {
-        uint32_t r[32];
+      for (int cb0 = 0; cb0 < NCH; cb0 += 3) {
+        uint4 w[24];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 w = qsrc[cb * 8 + i];
-          r[4 * i] = w.x;
-          r[4 * i + 1] = w.y;
-          r[4 * i + 2] = w.z;
-          r[4 * i + 3] = w.w;
+        for (int i = 0; i < 24; ++i) w[i] = qsrc[cb0 * 8 + i];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          uint32_t r[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            r[4 * i] = w[8 * k + i].x;
+            r[4 * i + 1] = w[8 * k + i].y;
+            r[4 * i + 2] = w[8 * k + i].z;
+            r[4 * i + 3] = w[8 * k + i].w;
+          }
+          tmem_st32u(tmem + kTmQ + lane_off + (cb0 + k) * 32, r);
         }
-        tmem_st32u(tQ + lane_off + cb * 32, r);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(Q_TMEM));
     }
+    const float *sBias = reinterpret_cast<const float *>(smem + Smem::kBias);
     for (int jj = 0; jj < n_kv; ++jj) {
-      const int s = jj % NSTG;
-      if (!(ok = mbar_wait(bar(S_FULL), jj & 1) && mbar_wait(bar(FULL + s), (jj / NSTG) & 1)))
+      const int s = jj % NSTG, bb = jj & 1;
+      if (!(ok = mbar_wait_sleep(bar(S_FULL + bb), (jj >> 1) & 1) &&
+                 mbar_wait_sleep(bar(FULL + s), (jj / NSTG) & 1)))
         break;
       tc_fence_after();
-      float x[BKEYS];
+      float x[BK];
       {
-        static_assert(BKEYS == 32, "S row load below is written for 32 keys");
-        tmem_ld32(tS0 + lane_off, x);
+        float (&x0)[32] = *reinterpret_cast<float (*)[32]>(&x[0]);
+        float (&x1)[32] = *reinterpret_cast<float (*)[32]>(&x[32]);
+        tmem_ld32(tmem + kTmS + bb * BK + lane_off, x0);
+        tmem_ld32(tmem + kTmS + bb * BK + 32 + lane_off, x1);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(S_FREE));
-      float mx = -INFINITY;
-      const int4 *pos4 = reinterpret_cast<const int4 *>(sPos + s * BKEYS);
+      if (lane == 0) mbar_arrive(bar(S_FREE + bb));
+      // scale to the log2 domain and add the key mask (0 / -inf)
+      const float4 *b4 = reinterpret_cast<const float4 *>(sBias + s * BK);
 #pragma unroll
-      for (int i4 = 0; i4 < BKEYS / 4; ++i4) {
-        const int4 pp = pos4[i4];
-        const int pv[4] = {pp.x, pp.y, pp.z, pp.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = 4 * i4 + u;
-          const int pos = pv[u];
-          const bool msk = pos < 0 || (use_upper && pos > i_pos) || pos < lo_r;
-          x[i] = msk ? -INFINITY : x[i] * c;
-          mx = fmaxf(mx, x[i]);
-        }
+      for (int i4 = 0; i4 < BK / 4; ++i4) {
+        const float4 bq = b4[i4];
+        ffma2v(x[4 * i4], x[4 * i4 + 1], c, bq.x, bq.y);
+        ffma2v(x[4 * i4 + 2], x[4 * i4 + 3], c, bq.z, bq.w);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(EMPTY + s));  // mask read: the stage may refill
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < BK; i += 2) mx = fmax3(mx, x[i], x[i + 1]);
       bool need = false;
       float factor = 1.f;
       if (mx > m_ref + 8.f) {
@@ -396,70 +491,115 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
         factor = need ? fast_exp2(m_ref - mx) : 1.f;
         m_ref = mx;
       }
-      // P buffer (and O) are free once the PV of tile jj-1 completed
-      if (jj >= 1 && !(ok = mbar_wait(bar(O_DONE), (jj - 1) & 1))) break;
-      if (__any_sync(0xffffffffu, need)) {
-        tc_fence_after();
-#pragma unroll 1
-        for (int ch = 0; ch < DVH / 32; ++ch) {
-          float v[32];
-          tmem_ld32(tO + lane_off + ch * 32, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= factor;
-          tmem_st32(tO + lane_off + ch * 32, v);
-        }
-        tmem_st_wait();
-      }
       l *= factor;
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      float sum = 0.f;
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-      for (int i = 0; i < BKEYS; ++i) {
-        x[i] = fast_exp2(x[i] - mu);
-        sum += x[i];
+      for (int i = 0; i < BK; i += 2) {
+        fadd2(x[i], x[i + 1], -mu, -mu);
+        x[i] = fast_exp2(x[i]);
+        x[i + 1] = fast_exp2(x[i + 1]);
+        fadd2(s0, s1, x[i], x[i + 1]);
       }
-      l += sum;
+      l += s0 + s1;
+      // the value CTA's P buffer bb is free once its PV of tile jj-2 is done
+      int okw = 1;
+      if (lane == 0 && jj >= 2) okw = mbar_wait_cluster_sleep(bar(P_FREE + bb), ((jj >> 1) - 1) & 1);
+      if (!(ok = __shfl_sync(0xffffffffu, okw, 0) != 0)) break;
+      const uint32_t dst = peer_P + bb * kPXfer;
 #pragma unroll
-      for (int cc = 0; cc < BKEYS / 8; ++cc) {
+      for (int cc = 0; cc < BK / 8; ++cc) {
         uint4 w;
         w.x = pack_bf16(x[8 * cc], x[8 * cc + 1]);
         w.y = pack_bf16(x[8 * cc + 2], x[8 * cc + 3]);
         w.z = pack_bf16(x[8 * cc + 4], x[8 * cc + 5]);
         w.w = pack_bf16(x[8 * cc + 6], x[8 * cc + 7]);
-        *reinterpret_cast<uint4 *>(smem + Smem::kP + p_off(row, cc)) = w;
+        st_cluster_v4(dst + p_off(row, cc), w);
       }
-      fence_proxy_async();
+      const uint32_t fac = dst + kPTile + warp * kFacWarp;
+      st_cluster_b32(fac + lane * 4, __float_as_uint(factor));
+      const int any = __any_sync(0xffffffffu, need) ? 1 : 0;
+      if (lane == 0) st_cluster_b32(fac + 128, static_cast<uint32_t>(any));
+      fence_proxy_async_cluster();  // P is read by the value CTA's MMAs
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(peer_pfull + 8u * bb);
+    }
+    if (!ok && lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+    // final (1/l, lse) of each head to the value CTA
+    st_cluster_v2f(map_to_cta(sbase + Smem::kFin, peer) + row * 8, l > 0.f ? 1.f / l : 0.f,
+                   l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY);
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive_remote(map_to_cta(bar(FIN), peer));
+      // every arrival the value CTA sends here has landed before this CTA ends
+      if (warp == 0 && ok) {
+        for (int bb = 0; bb < 2; ++bb) {
+          const int uses = (n_kv - bb + 1) / 2;  // tiles jj < n_kv with jj & 1 == bb
+          if (uses > 0 && !mbar_wait_cluster_sleep(bar(P_FREE + bb), (uses - 1) & 1))
+            atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+        }
+      }
+    }
+  } else {
+    // ==================== epilogue + rescale (value CTA) ====================
+    const int row = tid;  // head = TMEM lane
+    bool ok = true;
+    for (int ev = 0;; ++ev) {
+      if (!mbar_wait_sleep(bar(CORR_REQ), ev & 1)) {
+        ok = false;
+        break;
+      }
+      const int j = sWord[1];
+      if (j < 0) break;
+      const float f =
+          reinterpret_cast<const float *>(smem + Smem::kP + (j & 1) * kPXfer + kPTile +
+                                          warp * kFacWarp)[lane];
+      if (__any_sync(0xffffffffu, f != 1.f)) {
+        // O holds tiles 0..j-1: wait for the last of them, then scale rows
+        if (j >= 1 && !(ok = mbar_wait_sleep(bar(O_DONE), (j - 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < DV / 32; ++ch) {
+          float v[32];
+          tmem_ld32(tmem + lane_off + ch * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= f;
+          tmem_st32(tmem + lane_off + ch * 32, v);
+        }
+        tmem_st_wait();
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(P_FULL));
+      if (lane == 0) mbar_arrive(bar(CORR_DONE));
     }
-
-    // ---- epilogue: this CTA's normalised state for its 256 value dims ----
+    if (ok) ok = mbar_wait_cluster_sleep(bar(FIN), 0);
     bool have_o = false;
     if (ok && n_kv > 0) {
-      ok = mbar_wait(bar(O_DONE), (n_kv - 1) & 1);
+      ok = mbar_wait_sleep(bar(O_DONE), (n_kv - 1) & 1);
       have_o = ok;
       if (ok) tc_fence_after();
     }
     if (!ok && lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    const float lse_nat = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+    const float2 fl = ok ? reinterpret_cast<const float2 *>(smem + Smem::kFin)[row]
+                         : make_float2(0.f, -INFINITY);
+    const float inv = fl.x, lse_nat = fl.y;
     const int64_t rows_total = static_cast<int64_t>(p.total_q) * p.h_q;
     const int64_t grow = static_cast<int64_t>(t) * p.h_q + row;
     const bool split_mode = p.num_splits > 1;
 #pragma unroll 1
-    for (int ch = 0; ch < DVH / 32; ++ch) {
+    for (int ch = 0; ch < DV / 32; ++ch) {
       float v[32];
       if (have_o) {
-        tmem_ld32(tO + lane_off + ch * 32, v);
+        tmem_ld32(tmem + lane_off + ch * 32, v);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.f;
       }
-      const int col = hv * DVH + ch * 32;
+      const int col = ch * 32;
       if (!split_mode) {
         if (covered) {
-          bf16 *dst = p.out + static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(row) * p.o_sh + col;
+          bf16 *dst = p.out + static_cast<int64_t>(t) * p.o_st +
+                      static_cast<int64_t>(row) * p.o_sh + col;
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 w;
@@ -471,7 +611,7 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
           }
         }
       } else {
-        float *dst = p.ws_o + (static_cast<int64_t>(split) * rows_total + grow) * p.dv + col;
+        float *dst = p.ws_o + (static_cast<int64_t>(split) * rows_total + grow) * DV + col;
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
           __stcg(reinterpret_cast<float4 *>(dst + i),
@@ -479,40 +619,33 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
       }
     }
     if (!split_mode) {
-      if (covered && hv == 0 && p.lse != nullptr)
+      if (covered && p.lse != nullptr)
         p.lse[static_cast<int64_t>(t) * p.lse_st + static_cast<int64_t>(row) * p.lse_sh] = lse_nat;
     } else {
-      // both value halves see the same scores, so each keeps its own copy of
-      // every split's lse ([half][split][token][head]) and merges from it
       const int ns = p.num_splits;
-      float *lse_half = p.ws_lse + static_cast<int64_t>(hv) * ns * rows_total;
-      __stcg(lse_half + split * rows_total + grow, lse_nat);
+      __stcg(p.ws_lse + split * rows_total + grow, lse_nat);
       __threadfence();
       asm volatile("bar.sync 1, %0;\n" ::"n"(NSOFT * 32) : "memory");
-      if (tid == 0) {
-        int32_t *ctr = p.ws_counter + static_cast<int64_t>(t) * 2 + hv;
-        *sFlag = (atomicAdd(ctr, 1) == ns - 1);
-      }
+      if (tid == 0) sWord[0] = (atomicAdd(p.ws_counter + t, 1) == ns - 1);
       asm volatile("bar.sync 1, %0;\n" ::"n"(NSOFT * 32) : "memory");
-      if (*sFlag && covered) {
+      if (sWord[0] && covered) {
         __threadfence();  // every split's state is visible from here on
         float Ms = -INFINITY;
-        for (int sp = 0; sp < ns; ++sp) Ms = fmaxf(Ms, __ldcg(lse_half + sp * rows_total + grow));
+        for (int sp = 0; sp < ns; ++sp) Ms = fmaxf(Ms, __ldcg(p.ws_lse + sp * rows_total + grow));
         float wsum = 0.f;
         for (int sp = 0; sp < ns; ++sp)
-          wsum += Ms == -INFINITY ? 0.f
-                                  : exp2f((__ldcg(lse_half + sp * rows_total + grow) - Ms) * kLog2e);
+          wsum += Ms == -INFINITY
+                      ? 0.f
+                      : exp2f((__ldcg(p.ws_lse + sp * rows_total + grow) - Ms) * kLog2e);
         const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
-        bf16 *dst = p.out + static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(row) * p.o_sh +
-                    hv * DVH;
+        bf16 *dst = p.out + static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(row) * p.o_sh;
 #pragma unroll 1
-        for (int cc = 0; cc < DVH; cc += 8) {
+        for (int cc = 0; cc < DV; cc += 8) {
           float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
           for (int sp = 0; sp < ns; ++sp) {
-            const float ls = __ldcg(lse_half + sp * rows_total + grow);
+            const float ls = __ldcg(p.ws_lse + sp * rows_total + grow);
             const float w = Ms == -INFINITY ? 0.f : exp2f((ls - Ms) * kLog2e);
-            const float *src = p.ws_o + (static_cast<int64_t>(sp) * rows_total + grow) * p.dv +
-                               hv * DVH + cc;
+            const float *src = p.ws_o + (static_cast<int64_t>(sp) * rows_total + grow) * DV + cc;
             const float4 a = __ldcg(reinterpret_cast<const float4 *>(src));
             const float4 bq = __ldcg(reinterpret_cast<const float4 *>(src + 4));
             acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
@@ -525,7 +658,7 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
           wv.w = pack_bf16(acc[6] * winv, acc[7] * winv);
           *reinterpret_cast<uint4 *>(dst + cc) = wv;
         }
-        if (hv == 0 && p.lse != nullptr)
+        if (p.lse != nullptr)
           p.lse[static_cast<int64_t>(t) * p.lse_st + static_cast<int64_t>(row) * p.lse_sh] =
               wsum > 0.f ? Ms + logf(wsum) : -INFINITY;
       }
@@ -538,6 +671,7 @@ mla_topk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ml
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  cluster_sync();  // no CTA leaves while the other may still address it
 }
 
 }  // namespace
@@ -547,14 +681,9 @@ int launch_mla_topk(const AttnParams &p, cudaStream_t stream) {
   if (p.topk == nullptr || p.h_q != H || p.h_kv != 1 || p.d != DQK || p.dv != DV)
     return PKV_ERR_UNSUPPORTED;
   if (p.v != p.k || p.v_sp != p.k_sp || p.v_spos != p.k_spos) return PKV_ERR_UNSUPPORTED;
-  if (p.q_sh < DQK || p.q_st < p.q_sh * H || p.num_splits > 64) return PKV_ERR_UNSUPPORTED;
+  if (p.q_sh < DQK || p.q_st < p.q_sh * H || p.num_splits > kMlaMaxSplits)
+    return PKV_ERR_UNSUPPORTED;
   if (p.total_q > 65535) return PKV_ERR_UNSUPPORTED;
-  MlaMaps maps;
-  memset(&maps, 0, sizeof(maps));
-  cuuint64_t dims[3] = {DQK, H, static_cast<cuuint64_t>(p.total_q)};
-  cuuint64_t str[2] = {static_cast<cuuint64_t>(p.q_sh) * 2, static_cast<cuuint64_t>(p.q_st) * 2};
-  cuuint32_t box[3] = {64, H, 1};
-  if (!encode_tensor_map(&maps.q, p.q, 3, dims, str, box)) return PKV_ERR_UNSUPPORTED;
   static std::atomic<bool> configured[64] = {};  // per device; calls may race
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -564,8 +693,8 @@ int launch_mla_topk(const AttnParams &p, cudaStream_t stream) {
       return PKV_ERR_CUDA;
     if (dev < 64) configured[dev].store(true, std::memory_order_release);
   }
-  dim3 grid(p.num_splits, 2, p.total_q);
-  mla_topk_kernel<<<grid, NTHREADS, Smem::kDynamic, stream>>>(p, maps);
+  dim3 grid(2 * p.num_splits, 1, p.total_q);
+  mla_topk_kernel<<<grid, NTHREADS, Smem::kDynamic, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

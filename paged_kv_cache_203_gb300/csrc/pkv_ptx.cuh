@@ -49,6 +49,132 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
+// try_wait with a suspend-time hint: the warp sleeps in hardware until the
+// phase completes (or the hint runs out) instead of re-issuing the poll.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait that sleeps between polls; gives up after ~2^31 SM cycles
+// (about a second), however long each sleep lasted.
+constexpr long long kSleepWaitCycles = 1ll << 31;
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (clock64() - t0 > kSleepWaitCycles) return false;
+  }
+}
+// Bounded wait by lane 0 of the calling warp, result broadcast to the warp:
+// the other lanes do not poll the barrier (polling threads compete with the
+// warp's loads for the shared-memory pipe).  Memory seen by lane 0 is visible
+// to the warp after the __syncwarp.  sleep_ns > 0 adds a back-off between
+// polls, for waits that are long by design.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               uint32_t sleep_ns = 0) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    ok = 0;
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+      if (mbar_try_wait(bar, parity)) {
+        ok = 1;
+        break;
+      }
+      if (sleep_ns) __nanosleep(sleep_ns);
+    }
+  }
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+// The same with acquire at cluster scope: for phases completed by another
+// CTA of the cluster (remote bulk copies, remote MMA-completion arrivals).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster_sleep(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(1000000u)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > kSleepWaitCycles) return false;
+  }
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint32_t bar, uint32_t parity) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_cluster(bar, parity) ? 1 : 0;
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// -------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+// Whole-cluster barrier (every thread of every CTA of the cluster).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// Shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(d) : "r"(saddr), "r"(rank));
+  return d;
+}
+// Bulk copy of `bytes` (multiple of 16, both ends 16-byte aligned) from this
+// CTA's shared memory into another CTA's; completes `bytes` of transaction
+// count on `remote_bar` (an mbarrier in the destination CTA).
+__device__ __forceinline__ void bulk_s2s(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,
+                                         uint32_t remote_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
+      " [%0], [%1], %2, [%3];\n" ::"r"(remote_dst),
+      "r"(local_src), "r"(bytes), "r"(remote_bar)
+      : "memory");
+}
+// Arrive (release, cluster scope) on an mbarrier of another CTA of the
+// cluster, given its shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(remote_bar)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+// Wait until at most N of this thread's bulk groups still read their source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;\n" ::"n"(N) : "memory");
+}
 
 // ----------------------------------------------------------- async copies
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
@@ -93,6 +219,29 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
 // Warm L2 with a contiguous global range (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
+// Warm L2 with the 128-byte line holding `p` (a plain load-path prefetch:
+// no copy-engine work).
+__device__ __forceinline__ void prefetch_line_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+// Orders this thread's generic-proxy writes to shared::cluster memory (its
+// own CTA's or a peer's) before later async-proxy reads of it.
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;\n" ::: "memory");
+}
+// 16-byte store into the shared memory of a CTA of the cluster.
+__device__ __forceinline__ void st_cluster_v4(uint32_t remote, uint4 v) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(remote), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_b32(uint32_t remote, uint32_t v) {
+  asm volatile("st.shared::cluster.b32 [%0], %1;\n" ::"r"(remote), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v2f(uint32_t remote, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(remote), "f"(a), "f"(b)
+               : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -224,6 +373,14 @@ __device__ __forceinline__ void ffma2(float &a0, float &a1, float c, float b) {
       " fma.rn.f32x2 r, x, cc, bb;\n mov.b64 {%0, %1}, r;\n}\n"
       : "+f"(a0), "+f"(a1)
       : "f"(c), "f"(b));
+}
+// (a0, a1) = (a0, a1) * c + (b0, b1)
+__device__ __forceinline__ void ffma2v(float &a0, float &a1, float c, float b0, float b1) {
+  asm("{\n .reg .b64 x, cc, bb, r;\n"
+      " mov.b64 x, {%0, %1};\n mov.b64 cc, {%2, %2};\n mov.b64 bb, {%3, %4};\n"
+      " fma.rn.f32x2 r, x, cc, bb;\n mov.b64 {%0, %1}, r;\n}\n"
+      : "+f"(a0), "+f"(a1)
+      : "f"(c), "f"(b0), "f"(b1));
 }
 // (s0, s1) += (a0, a1)
 __device__ __forceinline__ void fadd2(float &s0, float &s1, float a0, float a1) {

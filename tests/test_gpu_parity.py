@@ -758,6 +758,29 @@ def test_mla_topk_decode_reduced(num_splits):
     assert pkv.get_error_flags() == 0
 
 
+@pytest.mark.parametrize("num_splits", [1, 3])
+def test_mla_topk_reference_max_rises(num_splits):
+    """Scores that grow along the list (rope parts of later tiles' keys scaled up) make
+    the softmax raise its reference max mid-list, so the accumulated output
+    rows are rescaled before the next product; against the oracle."""
+    wl = _mla_reduced(batch=3, kv_len=1200, topk=640, seed=77)
+    P = wl.page_size
+    k = wl.k_cache.view(-1, wl.k_cache.shape[-1])
+    for t in range(wl.q.shape[0]):
+        lst = wl.topk_indices[t]
+        for j, idx in enumerate(lst.tolist()):
+            if idx < 0:
+                continue
+            slot = int(wl.page_table[t, idx // P]) * P + idx % P
+            # the rope columns only: the value row (the first 512) is unchanged
+            k[slot, 512:] = (k[slot, 512:].float() * (1.0 + 3.0 * (j // 64))).to(torch.bfloat16)
+    g = wl.to(DEV)
+    out, lse = gpu_attn(g, num_splits=num_splits)
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, f"mla rising scores splits={num_splits}")
+    assert pkv.get_error_flags() == 0
+
+
 def test_mla_topk_bad_indices_and_empty_rows():
     """Out-of-range top-k entries are skipped and flagged; a row of only -1
     gives out 0 / lse -inf."""
