@@ -43,85 +43,22 @@
 #include <atomic>
 
 #include "pkv_internal.h"
+#include "pkv_ptx.cuh"
 
 namespace pkv {
 namespace {
+
+using namespace ptx;
 
 constexpr int BK = 64;          // keys per stage
 constexpr int NCW = 4;          // consumer warps
 constexpr int NCT = NCW * 32;   // consumer threads
 constexpr int ROWS = kDecodeRowTile;  // 16
-constexpr uint32_t kWaitLimit = 1u << 24;  // bounded mbarrier polls
 constexpr int kPrefetchStages = 3;         // cp.async loader: L2 prefetch distance
 
 // ------------------------------------------------------------ PTX helpers
+// (mbarriers, cp.async, TMA and L2 prefetch come from pkv_ptx.cuh)
 
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase with the given parity; false on expiry.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src,
-                                           int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
-               "l"(src), "r"(src_bytes)
-               : "memory");
-}
-// Makes the barrier count this thread's earlier cp.async as one arrival at
-// their completion (pending count raised first, so the thread still arrives
-// normally afterwards).
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];\n" ::"r"(bar)
-               : "memory");
-}
-
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map,
-                                            int c0, int c1, int c2, int c3,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-      "r"(bar)
-      : "memory");
-}
-
-// Warm L2 with a contiguous global range (16-byte aligned, size % 16 == 0).
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;\n" ::"n"(NCT) : "memory");
 }
@@ -190,11 +127,6 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
   return v;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&h);
 }
 
 // Byte offset of 16-byte chunk c of row r in a [rows][D] tile stored as
@@ -392,7 +324,7 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
       const int st = kt % NSTAGE;
       const uint32_t full = full0 + 8 * st;
       if constexpr (TMA) {
-        if (kt >= NSTAGE && !mbar_wait(empty0 + 8 * st, ((kt / NSTAGE) & 1) ^ 1)) {
+        if (kt >= NSTAGE && !mbar_wait_sleep(empty0 + 8 * st, ((kt / NSTAGE) & 1) ^ 1)) {
           if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
           break;
         }
@@ -497,7 +429,7 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
         // barrier and leave together on a timeout (no one is left behind at
         // a named barrier)
         if (ptid == 0) {
-          const bool free_ok = kt < NSTAGE || mbar_wait(empty0 + 8 * st, ((kt / NSTAGE) & 1) ^ 1);
+          const bool free_ok = kt < NSTAGE || mbar_wait_sleep(empty0 + 8 * st, ((kt / NSTAGE) & 1) ^ 1);
           if (!free_ok) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
           *sProdFlag = free_ok ? 1 : 0;
         }
@@ -567,7 +499,7 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
 
   for (int kt = 0; kt < n_kt; ++kt) {
     const int st = kt % NSTAGE;
-    if (!mbar_wait(full0 + 8 * st, (kt / NSTAGE) & 1)) {
+    if (!mbar_wait_sleep(full0 + 8 * st, (kt / NSTAGE) & 1)) {
       if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
       break;
     }
@@ -1148,7 +1080,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
 
       int ok = 1;
       if (lane == 0 && kt >= NST)
-        ok = mbar_wait(empty0 + 8 * st, ((kt / NST) & 1) ^ 1) ? 1 : 0;
+        ok = mbar_wait_sleep(empty0 + 8 * st, ((kt / NST) & 1) ^ 1) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
@@ -1240,7 +1172,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   auto issue_v = [&](int x) -> bool {
     if (!BOXES && x < n) {
       const int sx = x % NST;
-      if (!mbar_wait(vmeta0 + 8 * sx, (x / NST) & 1)) return false;
+      if (!mbar_wait_sleep(vmeta0 + 8 * sx, (x / NST) & 1)) return false;
       const int c = lane & 15;
       const uint32_t vdst = sbase + L.v + sx * L.stage;
 #pragma unroll
@@ -1258,7 +1190,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
 
   for (int kt = 0; v_ok && kt < n; ++kt) {
     const int st = kt % NST;
-    if (!mbar_wait(full0 + 8 * st, (kt / NST) & 1) || !issue_v(kt + 2)) {
+    if (!mbar_wait_sleep(full0 + 8 * st, (kt / NST) & 1) || !issue_v(kt + 2)) {
       if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
       break;
     }

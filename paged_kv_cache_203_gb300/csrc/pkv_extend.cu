@@ -44,6 +44,8 @@
 namespace pkv {
 namespace {
 
+using namespace ptx;
+
 constexpr int BM = 128;           // query rows per CTA
 constexpr int BN = 128;           // keys per tile
 constexpr int D = 128;            // head dim (q/k and v)
@@ -52,7 +54,6 @@ constexpr int NTHREADS = NSM_WARPS * 32 + 64;  // + producer warp, MMA warp
 constexpr int kProducerWarp = NSM_WARPS;
 constexpr int kMmaWarp = NSM_WARPS + 1;
 constexpr int HALF = BN / 2;      // S / P / O columns per softmax thread
-constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr uint32_t kTileBytes = BM * D * 2;  // 32 KB, any 128x128 bf16 tile
 constexpr int NKV = 3;            // K and V ring stages
 
@@ -82,119 +83,6 @@ enum BarId {
 };
 static_assert(MASK_FULL + 4 == Smem::kNumBars, "barrier plan and count agree");
 
-// ------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0,
-                                            int c1, int c2, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0,
-                                            int c1, int c2, int c3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: 128-byte swizzle, version 1.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) |
-         (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
-}
-// Instruction descriptor, kind::f16: bf16 x bf16 -> f32, M = 128, N = 128.
-__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |
-         (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
-}
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                     uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// D (+)= A B with A [128 x 16] from TMEM (rows on lanes, two bf16 of
-// consecutive k per 32-bit column, 8 columns per K=16 step).
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
-      : "memory");
-}
-// 32 lanes x 32 consecutive fp32 columns -> 32 registers per thread
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&h);
-}
-
 // Byte offset of 16-byte chunk c of row r of a 128-row tile stored as
 // [2 halves][128 rows][128 B] with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t tile_off(int r, int c) {
@@ -206,65 +94,6 @@ struct ExtendMaps {
   CUtensorMap k;
   CUtensorMap v;
 };
-
-// 128 consecutive fp32 columns of this thread's TMEM lane (one load + wait
-// in a single statement, so no register is read before the data lands)
-#define PKV_O4(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3])
-#define PKV_O16(i) PKV_O4(i), PKV_O4(i + 4), PKV_O4(i + 8), PKV_O4(i + 12)
-#define PKV_O64(i) PKV_O16(i), PKV_O16(i + 16), PKV_O16(i + 32), PKV_O16(i + 48)
-#define PKV_I4(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3])
-#define PKV_I16(i) PKV_I4(i), PKV_I4(i + 4), PKV_I4(i + 8), PKV_I4(i + 12)
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
-  uint32_t r[128];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : PKV_O64(0), PKV_O64(64)
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-  uint32_t r[64];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : PKV_O64(0)
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
-}
-// 2^x on the MUFU (PTX ex2.approx, flush-to-zero; 2^-inf = 0)
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-  uint32_t r[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
-               PKV_I16(0), PKV_I16(16)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() {
-  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-}
 
 // ---------------------------------------------------------------- kernel
 
@@ -353,7 +182,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       const int s = jj % NKV;
       const uint32_t prev = ((jj / NKV) & 1) ^ 1;
       // ---- K tile (stage freed when QK of tile jj-NKV completed) ----
-      if (jj >= NKV && !mbar_wait(bar(K_EMPTY + s), prev)) {
+      if (jj >= NKV && !mbar_wait_sleep(bar(K_EMPTY + s), prev)) {
         if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
         break;
       }
@@ -401,7 +230,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
         tma_load_4d(kdst + BN * 128, &maps.k, 64, kvh, inpage, page, bar(K_FULL + s));
       }
       // ---- V tile (stage freed when the PV of tile jj-NKV completed) ----
-      if (jj >= NKV && !mbar_wait(bar(V_EMPTY + s), prev)) {
+      if (jj >= NKV && !mbar_wait_sleep(bar(V_EMPTY + s), prev)) {
         if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
         break;
       }
@@ -417,21 +246,21 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
   } else if (warp == kMmaWarp) {
     // ================================== MMA ==================================
     if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16(false);
-      constexpr uint32_t kIdescPV = idesc_bf16(true);
-      bool ok = n_kv == 0 || mbar_wait(bar(Q_FULL), 0);
-      const uint64_t qd0 = smem_desc(sbase + Smem::kQ, 0, 1024);
+      constexpr uint32_t kIdescQK = idesc_bf16(BM, BN, false);
+      constexpr uint32_t kIdescPV = idesc_bf16(BM, BN, true);
+      bool ok = n_kv == 0 || mbar_wait_sleep(bar(Q_FULL), 0);
+      const uint64_t qd0 = smem_desc(sbase + Smem::kQ, 0, 1024, 2);
       for (int j = 0; ok && j <= n_kv; ++j) {
         if (j < n_kv) {  // S_j = Q K_j^T
           const int s = j & 1, sk = j % NKV;
-          ok = mbar_wait(bar(K_FULL + sk), (j / NKV) & 1) &&
-               (j < 2 || mbar_wait(bar(S_FREE + s), ((j >> 1) - 1) & 1));
+          ok = mbar_wait_sleep(bar(K_FULL + sk), (j / NKV) & 1) &&
+               (j < 2 || mbar_wait_sleep(bar(S_FREE + s), ((j >> 1) - 1) & 1));
           if (!ok) break;
           tc_fence_after();
           // descriptors formed once per tile; a K step adds a constant to the
           // start-address field (16-byte units), so the single issuing
           // thread does no 64-bit descriptor arithmetic per MMA
-          const uint64_t kd0 = smem_desc(sbase + Smem::kK + sk * kTileBytes, 0, 1024);
+          const uint64_t kd0 = smem_desc(sbase + Smem::kK + sk * kTileBytes, 0, 1024, 2);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint64_t koff = ((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4;
@@ -443,11 +272,11 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
         if (j >= 1) {  // O += P_{j-1} V_{j-1}
           const int jj = j - 1;
           const int s = jj & 1, sv = jj % NKV;
-          ok = mbar_wait(bar(P_FULL + s), (jj >> 1) & 1) &&
-               mbar_wait(bar(V_FULL + sv), (jj / NKV) & 1);
+          ok = mbar_wait_sleep(bar(P_FULL + s), (jj >> 1) & 1) &&
+               mbar_wait_sleep(bar(V_FULL + sv), (jj / NKV) & 1);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t vd0 = smem_desc(sbase + Smem::kV + sv * kTileBytes, BN * 128, 1024);
+          const uint64_t vd0 = smem_desc(sbase + Smem::kV + sv * kTileBytes, BN * 128, 1024, 2);
           // keys 0-63 of the tile accumulate into O_A, keys 64-127 into O_B
           // (each half of the softmax keeps its own reference max); P_j is
           // read from TMEM: keys 64h + 16k.. at column 128 s + 64 h + 8 k
@@ -482,7 +311,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
     for (int jj = 0; jj < n_kv; ++jj) {
       const int s = jj & 1;
       const uint32_t ph = (jj >> 1) & 1;
-      if (!(ok = mbar_wait(bar(S_FULL + s), ph))) break;
+      if (!(ok = mbar_wait_sleep(bar(S_FULL + s), ph))) break;
       tc_fence_after();
       float x[HALF];
       tmem_ld64(tS0 + s * 128 + col0 + lane_off, x);
@@ -491,7 +320,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       // after this softmax is done, so the phase cannot run ahead)
       const int skv = jj % NKV;
       const uint32_t pkv = (jj / NKV) & 1;
-      if (!(ok = mbar_wait(bar(MASK_FULL + (jj & 3)), (jj >> 2) & 1))) break;
+      if (!(ok = mbar_wait_sleep(bar(MASK_FULL + (jj & 3)), (jj >> 2) & 1))) break;
       const int ms = (jj & 3) * 4;
       const int key0 = (jt0 + jj) * BN + col0;  // key of this thread's column 0
       const uint32_t mk0 = sMask[ms + 2 * hf], mk1 = sMask[ms + 2 * hf + 1];
@@ -535,7 +364,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       if (__any_sync(0xffffffffu, need)) {
         // O holds P V of tiles 0..jj-1: wait for the last of them, scale
         const int t = jj - 1;
-        if (!(ok = mbar_wait(bar(O_DONE + (t & 1)), (t >> 1) & 1))) break;
+        if (!(ok = mbar_wait_sleep(bar(O_DONE + (t & 1)), (t >> 1) & 1))) break;
         tc_fence_after();
         const uint32_t tOh = tO + hf * 128 + lane_off;  // this half's O
 #pragma unroll 1
@@ -576,7 +405,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       // `row` of the tile, this thread's half of its columns
       const uint32_t own = quad == 0 ? sMask[ms] : quad == 1 ? sMask[ms + 1]
                          : quad == 2 ? sMask[ms + 2] : sMask[ms + 3];
-      if (!all_valid && !(ok = mbar_wait(bar(V_FULL + skv), pkv))) break;  // rows to zero
+      if (!all_valid && !(ok = mbar_wait_sleep(bar(V_FULL + skv), pkv))) break;  // rows to zero
       if (!all_valid && !((own >> lane) & 1u)) {
         uint8_t *vt = smem + Smem::kV + skv * kTileBytes;
 #pragma unroll
@@ -597,7 +426,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
     for (int i = 0; i < HALF; ++i) oa[i] = ob[i] = 0.f;
     if (ok && n_kv > 0) {
       const int t = n_kv - 1;
-      ok = mbar_wait(bar(O_DONE + (t & 1)), (t >> 1) & 1);
+      ok = mbar_wait_sleep(bar(O_DONE + (t & 1)), (t >> 1) & 1);
       if (ok) {
         tc_fence_after();
         tmem_ld64(tO + lane_off + col0, oa);
@@ -610,7 +439,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       xchg[(2 + hf) * BM + row] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(XCHG));
-      ok = mbar_wait(bar(XCHG), 0);
+      ok = mbar_wait_sleep(bar(XCHG), 0);
       if (ok) {
         m_oth = xchg[(hf ^ 1) * BM + row];
         l_oth = xchg[(2 + (hf ^ 1)) * BM + row];
