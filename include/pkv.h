@@ -22,10 +22,14 @@
  *   too short for its sequence) never trap: the offending entry is skipped
  *   (treated as masked / written as -1) and a sticky bit is set in a device
  *   error word, read with pkv_get_error_flags() after synchronising.
- * - The library keeps no state between calls apart from that error word
- *   (and per-device lookups made once).  Entry points may be called from
- *   several host threads at once; each call must own its workspace and
- *   outputs, and the error word is shared by all calls on a device.
+ * - The library keeps no state between calls apart from that error word,
+ *   per-device lookups made once, and the fixed scratch array of
+ *   pkv_attn_with_kvcache_noalloc (PKV_NOALLOC_SCRATCH_BYTES per device that
+ *   loads the library; it keeps the last call's contents and calls of that
+ *   entry point that overlap on the GPU race on it: see its comment).  Entry
+ *   points may be called from several host threads at once; each call must
+ *   own its workspace and outputs, and the error word is shared by all calls
+ *   on a device.
  */
 #ifndef PKV_H
 #define PKV_H

@@ -368,6 +368,10 @@ uint8_t orc_e4m3_round(double x) {
   if (isnan(x)) return 0x7f;
   const uint8_t sign = signbit(x) ? 0x80 : 0x00;  /* -0.0 keeps its sign */
   const double a = fabs(x);
+  /* past the midpoint between the largest value (448) and the next step
+     the format would have (480) there is no code but NaN; this also covers
+     +-inf and magnitudes so large that both distances below round alike */
+  if (a > 464.0) return (uint8_t)(sign | 0x7f);
   /* nearest of the non-negative codes 0..127, code 127 standing for the
      value 480 the format does not have (choosing it means "NaN") */
   int best = 0;

@@ -17,6 +17,8 @@
 // cleared by every call with an asynchronous memset, and the partial states
 // are always written before they are read.  Two calls whose work overlaps on
 // the GPU (different streams, no ordering between them) race on the array.
+#include <atomic>
+
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -27,19 +29,21 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[PKV_NOALLOC_SCRATCH_B
 // Device address of g_noalloc_scratch for each device, filled on the first
 // call made with that device current.  In host code the array's name is only
 // a host-side stand-in, so the address must come from cudaGetSymbolAddress.
-void *g_scratch_addr[64] = {nullptr};
+// Calls may come from several host threads at once: two first calls on a
+// device may both look the address up and store the same value.
+std::atomic<void *> g_scratch_addr[64] = {};
 
 int scratch_for_current_device(void **ptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (dev < 0 || dev >= 64) return PKV_ERR_UNSUPPORTED;
-  if (g_scratch_addr[dev] == nullptr) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+  void *addr = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (addr == nullptr) {
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
       return PKV_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    g_scratch_addr[dev].store(addr, std::memory_order_release);
   }
-  *ptr = g_scratch_addr[dev];
+  *ptr = addr;
   return PKV_OK;
 }
 

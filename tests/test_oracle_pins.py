@@ -802,6 +802,7 @@ def test_e4m3_rounding_matches_torch():
              3 * 2.0 ** -11, 2.0 ** -11, 0.0]
     vals += [-v for v in vals[:500]]
     vals += [-0.0, -1e-30, -(2.0 ** -11), -(3 * 2.0 ** -11)]   # zero keeps its sign
+    vals += [float("inf"), float("-inf"), -464.0, -464.1, 1e30, -1e30]  # past the range
     x = torch.tensor(vals, dtype=torch.float64)
     ref = x.to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     got = np.array([oracle.e4m3_round(v) for v in x.to(torch.float32).double().tolist()])
