@@ -47,13 +47,9 @@ L2_BYTES = 129 * 1024 * 1024
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
 # attention kernel on the full-size workload, from one ncu capture of the
-# kernel as it is now; a kernel changed since its capture has no entry.
+# kernel as it is now; a kernel changed since its capture has no entry (its
+# traffic is reported as null).
 MEASURED_TRAFFIC = {
-    ("gqa_split_decode", "decode_gqa_kernel"): 1.1259e9,
-    ("gqa_split_decode", "decode_allheads_kernel (page boxes, balanced)"): 1.1171e9,
-    ("swa_decode", "decode_allheads_kernel (slot rows)"): 0.6487e9,
-    ("mla_topk_decode", "mla_topk_kernel"): 0.3356e9,
-    ("varlen_extend", "extend_tc_kernel"): 0.2653e9,
 }
 
 
@@ -168,12 +164,18 @@ class Step:
         self.kv_bytes = kv_tokens * h_kv * (d + dv) * 2 if g.topk_indices is None else \
             kv_tokens * d * 2  # absorbed MLA: one 576-wide row per gathered key
         self.flops = self._flops()
+
+    def prepare(self):
+        """Allocate the library's workspace (library arm only: the reference
+        arm never loads the CUDA library)."""
+        g = self.g
         self.workspace_bytes = pkv.attn_workspace_size(
-            g.q, g.k_cache, g.v_cache, self.pt if not (g.kind == "swa") else self.pt,
+            g.q, g.k_cache, g.v_cache, self.pt,
             g.cache_seqlens if not (g.kind == "swa") else self.kv, g.max_seqlen_q,
             g.topk_indices, g.num_splits)
         if self.workspace_bytes:
-            self.ws = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=device)
+            self.ws = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=self.dev)
+        return self
 
     def _flops(self):
         g = self.g
@@ -579,6 +581,40 @@ def oracle_step_time(step: Step, budget_s: float = 10.0):
 
 # --------------------------------------------------------------------- main
 
+def roofline_of(step: Step, attn_ms: float, peaks: dict, sized: bool = False) -> dict:
+    """Roofline object of a step's attention kernel: algorithmic bytes (decode)
+    or flops (extend) per launch over the launch's CUDA-event time, against
+    the measured peak; traffic from the ncu table (full-size workloads of
+    kernels unchanged since their capture), else null."""
+    traffic = None if sized else MEASURED_TRAFFIC.get((step.name, step.attention_kernel()))
+    if step.name == "varlen_extend":
+        achieved = step.flops / 1e12 / (attn_ms / 1e3)
+        return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": traffic, "kernel": step.attention_kernel(),
+                "peak_source": peaks["source"]}
+    achieved = step.kv_bytes / 1e9 / (attn_ms / 1e3)
+    return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+            "kernel": step.attention_kernel(), "peak_source": peaks["source"]}
+
+
+def config_summary(step: Step, attn_ms: float, step_ms: float, peaks: dict) -> dict:
+    """Compact per-workload record: the metric, the step time, the attention
+    kernel's roofline (and, for the MLA decode, whose bytes and flops meet
+    near the ridge, the tensor fraction beside it)."""
+    metric, unit, per_step = metric_of(step)
+    out = {"metric": metric, "value": per_step / (step_ms / 1e3), "unit": unit,
+           "ms_per_step": step_ms, "attn_ms": attn_ms,
+           "roofline": roofline_of(step, attn_ms, peaks),
+           "tokens_per_s": step.g.q.shape[0] / (step_ms / 1e3)}
+    if step.g.kind == "mla":
+        tf = step.flops / 1e12 / (attn_ms / 1e3)
+        out["tensor"] = {"achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"]}
+    return out
+
+
 def metric_of(step: Step):
     if step.name == "varlen_extend":
         return "extend TFLOP/s", "TFLOP/s", step.flops / 1e12
@@ -666,7 +702,7 @@ def main():
     torch.cuda.set_device(dev)
     pkv.load_library()
     peaks = measured_peaks()
-    step = Step(args.workload, dev, parse_overrides(args.override))
+    step = Step(args.workload, dev, parse_overrides(args.override)).prepare()
     metric, unit, per_step = metric_of(step)
 
     for _ in range(args.warmup):
@@ -743,20 +779,8 @@ def main():
     value = per_step * world / (ms / 1e3)
     e2e_val = per_step * world / (e2e_ms / 1e3)
     # full-size workloads only (a split-count override keeps the sizes)
-    sized = set(parse_overrides(args.override)) - {"num_splits"}
-    traffic = None if sized else MEASURED_TRAFFIC.get((args.workload, step.attention_kernel()))
-    if unit == "GB/s":
-        achieved = step.kv_bytes / 1e9 / (attn_ms / 1e3)
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                "kernel": step.attention_kernel(),
-                "peak_source": peaks["source"]}
-    else:
-        achieved = step.flops / 1e12 / (attn_ms / 1e3)
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                "traffic": traffic, "kernel": step.attention_kernel(),
-                "peak_source": peaks["source"]}
+    sized = bool(set(parse_overrides(args.override)) - {"num_splits"})
+    roof = roofline_of(step, attn_ms, peaks, sized)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -766,7 +790,9 @@ def main():
 
     n_tokens = int(step.g.q.shape[0])
     others = {}
+    configs = {}
     if rank == 0 and not args.no_others and args.workload == HEADLINE and not args.override:
+        configs[HEADLINE] = config_summary(step, attn_ms, ms, peaks)
         graph = None  # its captured buffers go with the workload
         del step.g
         torch.cuda.empty_cache()
@@ -776,7 +802,7 @@ def main():
         runs.append((HEADLINE + "@auto_split", HEADLINE, {"num_splits": 0}))
         for label, name, ov in runs:
             try:
-                s2 = Step(name, dev, ov)
+                s2 = Step(name, dev, ov).prepare()
                 for _ in range(3):
                     s2.run()
                 torch.cuda.synchronize()
@@ -787,6 +813,8 @@ def main():
                 torch.cuda.synchronize()
                 kms = sum(x.elapsed_time(y) for x, y in e2) / 20
                 sms, how = _timed(s2.run)
+                if not ov:
+                    configs[label] = config_summary(s2, kms, sms, peaks)
                 others[label] = {
                     "kernel": s2.attention_kernel(),
                     "ms_per_step": sms, "step_timing": how, "attn_ms": kms,
@@ -799,6 +827,8 @@ def main():
                 torch.cuda.empty_cache()
             except pkv.PkvError as e:
                 others[label] = {"unavailable": str(e)}
+                if not ov:
+                    configs[label] = {"unavailable": str(e)}
         for label, fn in ((HEADLINE + "@local_chunk_2048", local_attention_line),
                           (HEADLINE + "@cascade_shared_prefix_4096", cascade_line),
                           ("varlen_extend@append_then_attend", append_line),
@@ -835,6 +865,8 @@ def main():
             "tokens_per_s": n_tokens * world / (ms / 1e3),
             "error_flags": flags,
         }
+        if configs:  # the five workloads, compact, ahead of the long details
+            line["configs"] = configs
         if others:
             line["other_workloads"] = others
         print(json.dumps(line), flush=True)

@@ -40,3 +40,19 @@ def test_reference_arm_two_gloo_ranks():
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
     assert lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
+
+
+def test_reference_arm_does_not_load_the_cuda_library():
+    """The reference arm runs the oracle only: after it ran in this process,
+    the package's CUDA library has not been loaded."""
+    code = (
+        "import sys, runpy; sys.argv = ['bench.py', '--impl', 'reference', '--override', "
+        f"'{TINY}', '--steps', '1', '--warmup', '1']; "
+        "runpy.run_path('bench.py', run_name='__main__'); "
+        "import paged_kv_cache_203_gb300 as pkv; "
+        "maps = open('/proc/self/maps').read(); "
+        "assert pkv._LIB is None and 'libpkv.so' not in maps, 'libpkv loaded'; print('CLEAN')")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "CLEAN" in r.stdout

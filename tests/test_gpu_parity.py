@@ -405,35 +405,29 @@ def test_bad_page_ids_are_skipped_and_flagged():
         assert pkv.get_error_flags() & pkv.EFLAG_PAGE_OOB
 
 
-# ----------------------------------------------- full-size workloads, sampled
+# ------------------------------------- full-size workloads, every output row
 
-def _sample_rows(total_q, h_q, n, seed):
-    rng = np.random.default_rng(seed)
-    return np.stack([rng.integers(0, total_q, n), rng.integers(0, h_q, n)],
-                    axis=1).astype(np.int32)
-
-
-def test_gqa_split_decode_full_size_sampled():
+@pytest.mark.parametrize("num_splits", [4, 0])
+def test_gqa_split_decode_full_size(num_splits):
     """Full batched GQA split-KV decode workload (batch 64, 32/8 heads,
     seqlens U[512, 8192], 40k-page pool) in the bench's launch configuration
-    (num_splits 4); 96 sampled (token, head) rows against the oracle."""
+    (4 key chunks) and with the library's balanced schedule (requests cut at
+    CTA boundaries, partial last tiles): every (token, head) row of out and
+    lse against the oracle."""
     g = workloads.make("gqa_split_decode", value_device=DEV)
-    out, lse = gpu_attn(g, num_splits=4)
-    rows = _sample_rows(g.q.shape[0], g.q.shape[1], 96, 1)
+    out, lse = gpu_attn(g, num_splits=num_splits)
     ref_o, ref_l, _ = oracle.attention(
         oracle.bf16_bits(g.q), oracle.bf16_bits(g.k_cache), oracle.bf16_bits(g.v_cache),
         g.page_table.cpu().numpy(), g.cache_seqlens.cpu().numpy(),
-        g.cu_seqlens_q.cpu().numpy(), g.scale, rows=rows)
-    idx = torch.from_numpy(rows).long()
-    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
-                ref_o, ref_l, "full-size sampled")
+        g.cu_seqlens_q.cpu().numpy(), g.scale)
+    check_close(out, lse, ref_o, ref_l, f"full size, splits {num_splits}")
     assert pkv.get_error_flags() == 0
 
 
-def test_swa_decode_full_size_sampled():
+def test_swa_decode_full_size():
     """Full sliding-window decode workload (batch 32, 64/8 heads, window
     4096, seq up to 32768) as the bench runs it: GPU-built table, then the
-    attention with the library's split choice; sampled rows."""
+    attention with the library's split choice; every row."""
     g = workloads.make("swa_decode", value_device=DEV)
     w = g.window
     pa_max = min(int(g.prefill_lens.max()) + w, int(g.seq_lens.max()))
@@ -442,11 +436,9 @@ def test_swa_decode_full_size_sampled():
     pkv.build_swa_page_table(g.req_to_token, g.req_pool_indices, g.seq_lens,
                              g.prefill_lens, w, dst, kv)
     out, lse = gpu_attn(g, page_table=dst, cache_seqlens=kv, num_splits=0)
-    rows = _sample_rows(32, 64, 64, 2)
     ref_o, ref_l, _ = oracle.attention(
         oracle.bf16_bits(g.q), oracle.bf16_bits(g.k_cache), oracle.bf16_bits(g.v_cache),
-        dst.cpu().numpy(), kv.cpu().numpy(), g.cu_seqlens_q.cpu().numpy(), g.scale,
-        rows=rows)
+        dst.cpu().numpy(), kv.cpu().numpy(), g.cu_seqlens_q.cpu().numpy(), g.scale)
     ref_pt, ref_kv, _ = oracle.swa_page_table(
         g.req_to_token.cpu().numpy(), g.req_pool_indices.cpu().numpy(),
         g.seq_lens.cpu().numpy(), g.prefill_lens.cpu().numpy(), w, pa_max)
@@ -455,9 +447,7 @@ def test_swa_decode_full_size_sampled():
     d = dst.cpu().numpy()
     for b in range(32):
         assert np.array_equal(d[b, :kvn[b]], ref_pt[b, :kvn[b]])
-    idx = torch.from_numpy(rows).long()
-    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
-                ref_o, ref_l, "swa full-size sampled")
+    check_close(out, lse, ref_o, ref_l, "swa full size")
 
 
 # ------------------------------------------- loader coverage (TMA / cp.async)
@@ -569,18 +559,15 @@ def test_small_page_balanced_schedule_mixed_batch():
 
 def test_small_page_batch_beyond_the_balanced_limit():
     """More requests than the balanced schedule handles (2048): the library's
-    split choice falls back to fixed splits of the all-heads kernel; sampled
-    rows against the oracle."""
+    split choice falls back to fixed splits of the all-heads kernel; every
+    row against the oracle."""
     batch = 2100
     wl = workloads.make("tiny_decode", d=128, page_size=1, h_q=16, h_kv=8, batch=batch,
                         len_lo=1, len_hi=80, pool_tokens=batch * 80 + 64, seed=91)
     g = wl.to(DEV)
     out, lse = gpu_attn(g, num_splits=0)
-    rows = _sample_rows(batch, 16, 128, 5)
-    ref_o, ref_l, _ = oracle_attn(wl, rows=rows)
-    idx = torch.from_numpy(rows).long()
-    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
-                ref_o, ref_l, "batch 2100")
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, "batch 2100")
     assert pkv.get_error_flags() == 0
 
 
@@ -709,19 +696,16 @@ def test_varlen_extend_garbage_and_bad_pages():
     assert pkv.get_error_flags() & pkv.EFLAG_PAGE_OOB
 
 
-def test_varlen_extend_full_size_sampled():
+def test_varlen_extend_full_size():
     """Full varlen extend workload (batch 8, new U[128, 2048], prefix
-    U[0, 4096], page 64) as the bench runs it; sampled rows."""
+    U[0, 4096], page 64) as the bench runs it; every row."""
     g = workloads.make("varlen_extend", value_device=DEV)
     out, lse = gpu_attn(g)
-    rows = _sample_rows(g.q.shape[0], g.q.shape[1], 96, 3)
     ref_o, ref_l, _ = oracle.attention(
         oracle.bf16_bits(g.q), oracle.bf16_bits(g.k_cache), oracle.bf16_bits(g.v_cache),
         g.page_table.cpu().numpy(), g.cache_seqlens.cpu().numpy(),
-        g.cu_seqlens_q.cpu().numpy(), g.scale, causal=True, rows=rows)
-    idx = torch.from_numpy(rows).long()
-    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
-                ref_o, ref_l, "extend full-size sampled")
+        g.cu_seqlens_q.cpu().numpy(), g.scale, causal=True)
+    check_close(out, lse, ref_o, ref_l, "extend full size")
     assert pkv.get_error_flags() == 0
 
 
@@ -797,20 +781,17 @@ def test_mla_topk_bad_indices_and_empty_rows():
     assert pkv.get_error_flags() & pkv.EFLAG_TOPK_OOB
 
 
-def test_mla_topk_full_size_sampled():
+def test_mla_topk_full_size():
     """Full MLA top-k workload (batch 128, kv_len 8192, top-k 2048) in the
-    bench's launch configuration; 96 sampled (token, head) rows."""
+    bench's launch configuration; every (token, head) row."""
     g = workloads.make("mla_topk_decode", value_device=DEV)
     out, lse = gpu_attn(g)
-    rows = _sample_rows(g.q.shape[0], g.q.shape[1], 96, 4)
     kb = oracle.bf16_bits(g.k_cache)
     ref_o, ref_l, _ = oracle.attention(
         oracle.bf16_bits(g.q), kb, kb, g.page_table.cpu().numpy(),
         g.cache_seqlens.cpu().numpy(), g.cu_seqlens_q.cpu().numpy(), g.scale,
-        topk=g.topk_indices.cpu().numpy(), rows=rows, d_v=512)
-    idx = torch.from_numpy(rows).long()
-    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
-                ref_o, ref_l, "mla full-size sampled")
+        topk=g.topk_indices.cpu().numpy(), d_v=512)
+    check_close(out, lse, ref_o, ref_l, "mla full size")
     assert pkv.get_error_flags() == 0
 
 
@@ -1215,11 +1196,11 @@ def test_paths_replay_from_cuda_graphs_with_new_lengths():
 
 # ------------------------------------ full-size checks of the composed rows
 
-def test_fp8_full_size_sampled_requests():
+def test_fp8_full_size():
     """The bench's fp8 line: the GQA decode batch (64 requests, 32/8 heads,
     kv U[512, 8192]) with its cache cast to e4m3 and descales 0.75 / 1.25,
-    the library's split choice; eight whole requests (all their rows)
-    against the oracle."""
+    the library's split choice; every request (all rows) against the
+    oracle."""
     g = workloads.make("gqa_split_decode", value_device=DEV)
     k8, v8 = g.k_cache.to(torch.float8_e4m3fn), g.v_cache.to(torch.float8_e4m3fn)
     B, h_kv = g.cache_seqlens.shape[0], k8.shape[2]
@@ -1229,7 +1210,7 @@ def test_fp8_full_size_sampled_requests():
                                          g.cu_seqlens_q, g.max_seqlen_q, g.scale,
                                          k_descale=kd, v_descale=vd, return_softmax_lse=True)
     torch.cuda.synchronize()
-    pick = np.array([0, 7, 13, 22, 31, 40, 51, 63])      # decode: token b is request b
+    pick = np.arange(B)                                  # decode: token b is request b
     pt = g.page_table.cpu().numpy()[pick]
     ks = g.cache_seqlens.cpu().numpy()[pick]
     ref_o, ref_l, _ = oracle.attention_fp8(
@@ -1241,29 +1222,26 @@ def test_fp8_full_size_sampled_requests():
     assert pkv.get_error_flags() == 0
 
 
-def test_local_attention_full_size_sampled():
+def test_local_attention_full_size():
     """The bench's local-attention line: the GQA decode batch with 2048-key
-    chunks (device-built virtual requests, one attention call); sampled rows
+    chunks (device-built virtual requests, one attention call); every row
     against the oracle's chunk-masked attention."""
     g = workloads.make("gqa_split_decode", value_device=DEV)
     out, lse = pkv.local_attn_with_kvcache(g.q, g.k_cache, g.v_cache, g.page_table,
                                            g.cache_seqlens, g.cu_seqlens_q, g.max_seqlen_q,
                                            2048, g.scale, return_softmax_lse=True)
     torch.cuda.synchronize()
-    rows = _sample_rows(g.q.shape[0], g.q.shape[1], 96, 7)
     ref_o, ref_l, _ = oracle.attention(
         oracle.bf16_bits(g.q), oracle.bf16_bits(g.k_cache), oracle.bf16_bits(g.v_cache),
         g.page_table.cpu().numpy(), g.cache_seqlens.cpu().numpy(),
-        g.cu_seqlens_q.cpu().numpy(), g.scale, causal=True, attn_chunk=2048, rows=rows)
-    idx = torch.from_numpy(rows).long()
-    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
-                ref_o, ref_l, "local full-size sampled")
+        g.cu_seqlens_q.cpu().numpy(), g.scale, causal=True, attn_chunk=2048)
+    check_close(out, lse, ref_o, ref_l, "local full size")
     assert pkv.get_error_flags() == 0
 
 
-def test_cascade_full_size_sampled():
+def test_cascade_full_size():
     """The bench's cascade line: every request of the GQA decode batch also
-    sees a shared 4096-token prefix (pages 0-255 of the pool); sampled rows
+    sees a shared 4096-token prefix (pages 0-255 of the pool); every row
     against one oracle call over the prefix pages followed by the request's
     own pages."""
     g = workloads.make("gqa_split_decode", value_device=DEV)
@@ -1277,13 +1255,10 @@ def test_cascade_full_size_sampled():
     torch.cuda.synchronize()
     full_pt = torch.cat([pre_pt.cpu(), g.page_table.cpu()], dim=1).numpy()
     full_len = (g.cache_seqlens.cpu() + 4096).numpy()
-    rows = _sample_rows(g.q.shape[0], g.q.shape[1], 96, 8)
     ref_o, ref_l, _ = oracle.attention(
         oracle.bf16_bits(g.q), oracle.bf16_bits(g.k_cache), oracle.bf16_bits(g.v_cache),
-        full_pt, full_len, g.cu_seqlens_q.cpu().numpy(), g.scale, causal=True, rows=rows)
-    idx = torch.from_numpy(rows).long()
-    check_close(out.cpu()[idx[:, 0], idx[:, 1]], lse.cpu()[idx[:, 0], idx[:, 1]],
-                ref_o, ref_l, "cascade full-size sampled")
+        full_pt, full_len, g.cu_seqlens_q.cpu().numpy(), g.scale, causal=True)
+    check_close(out, lse, ref_o, ref_l, "cascade full size")
     assert pkv.get_error_flags() == 0
 
 
