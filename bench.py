@@ -248,6 +248,8 @@ class Step:
                 return "decode_allheads_kernel (slot rows)"
             if p % 16 == 0 and g.num_splits == 0:
                 return "decode_allheads_kernel (page boxes, balanced)"
+            if p % 16 == 0:
+                return "decode_allheads_kernel (page boxes, fixed splits)"
         return "decode_gqa_kernel"
 
 

@@ -217,8 +217,9 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
     if (max_seqlen_q >= kExtendMinSeqlenQ && extend_eligible(lp))
       plan->kind = 1;  // tcgen05 extend, no workspace
     else if (decode_allheads_eligible(lp) &&
-             (page < 8 || (num_splits == 0 && batch <= kDecodeBalancedMaxBatch)))
-      plan->kind = 3;  // one CTA covers every KV head of a request
+             (page < 8 || (num_splits == 0 && batch <= kDecodeBalancedMaxBatch) ||
+              (num_splits > 0 && kDecodeFixedSplitHeads > 0 && page % 16 == 0)))
+      plan->kind = 3;  // one CTA covers several (or every) KV heads of a request
   }
   if (present(topk)) {
     plan->n_row_tiles = max_seqlen_q * ((group + kDecodeRowTile - 1) / kDecodeRowTile);

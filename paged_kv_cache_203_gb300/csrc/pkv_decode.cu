@@ -770,8 +770,11 @@ decode_gqa_kernel(const __grid_constant__ AttnParams p,
 // into a shared ring), which keeps the page-table latency off the copy path.
 //
 // Two schedules:
-//  * fixed splits (num_splits >= 1): CTA (split, head group, request) takes
-//    an equal share of the request's 16-key tiles; partials are merged by the
+//  * fixed splits (num_splits >= 1): CTA (split, head group, request rank)
+//    takes an equal share of the request's 16-key tiles; the requests are
+//    ranked by length in the kernel so the longest chunks start first; page
+//    boxes use kDecodeFixedSplitHeads heads per CTA (smaller work items that
+//    balance over the grid, boxes still 8 KB); partials are merged by the
 //    last CTA of each (request, KV head);
 //  * balanced (num_splits == 0, persistent, one CTA per SM, all heads): the
 //    16-key tiles of the whole batch are laid end to end and CTA c takes the
@@ -790,6 +793,8 @@ constexpr int AH_RING = AH_LOOKAHEAD + 1;
 constexpr int AH_MAXH = 8;       // KV heads per CTA (one consumer warp each)
 constexpr int AH_MAXB = kDecodeBalancedMaxBatch;  // requests a balanced launch schedules
 constexpr int AH_SMEM_MAX = 232448;
+// KV heads per CTA for page boxes with fixed splits (see the launcher)
+constexpr int kAhFixedHeads = kDecodeFixedSplitHeads;
 
 // stage flags published by the producer beside each tile's key positions
 constexpr int AH_SEG_START = 1;  // first tile this CTA takes of the request
@@ -964,7 +969,30 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     t_first = static_cast<int>(x0 - sPre[lo_b]);
   } else {
     __syncthreads();
+    // longest requests first: blockIdx.z is a rank, not a request.  The
+    // chunks of a request are its tiles / num_splits, so request order would
+    // leave the longest chunks for the last wave; every CTA ranks the
+    // requests by tiles (descending, ties by index: a permutation) in the
+    // K ring, which the producer fills only after the barrier below.
     b_first = blockIdx.z;
+    if (p.batch > 1 && p.batch <= nthreads && p.batch * 4 <= static_cast<int>(L.stage)) {
+      int *sWork = reinterpret_cast<int *>(smem + L.k);
+      int *sPick = reinterpret_cast<int *>(smem + L.scan);
+      if (tid < p.batch) sWork[tid] = ah_request(p, tid).ntiles;
+      __syncthreads();
+      if (tid < p.batch) {
+        const int wv = sWork[tid];
+        int rank = 0;
+        for (int j = 0; j < p.batch; ++j) {
+          const int v = sWork[j];
+          rank += (v > wv) || (v == wv && j < tid);
+        }
+        if (rank == static_cast<int>(blockIdx.z)) *sPick = tid;
+      }
+      __syncthreads();
+      b_first = *sPick;
+      __syncthreads();  // the ranks are read before the ring is reused
+    }
     const AhReq r = ah_request(p, b_first);
     if (r.ntiles == 0) return;  // uniform
     const int split = blockIdx.x;
@@ -1116,9 +1144,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
         // K rows by bulk copy; the V rows' offsets are published for the
         // consumer warps, which copy their own head's slices with cp.async
         if (lane < AH_BK) sVoff[st * AH_BK + lane] = pos >= 0 ? voff : -1;
-        uint32_t bytes = pos >= 0 ? row_bytes : 0u;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, pos >= 0)) * row_bytes;
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(vmeta0 + 8 * st);
@@ -1640,12 +1666,13 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
   const bool balanced = p.num_splits == 0;
   if (balanced && p.batch > AH_MAXB) return PKV_ERR_UNSUPPORTED;
   const bool boxes = p.page_size >= 8;
-  // page boxes run the balanced schedule only: with fixed splits a CTA that
-  // covers every head turns a long request's chunk into one long work item
-  if (boxes && !balanced) return PKV_ERR_UNSUPPORTED;
   const bool fp8 = p.kv_fp8 != 0;
-  if (fp8 && !boxes) return PKV_ERR_UNSUPPORTED;
-  const int hpc = p.h_kv;
+  if (fp8 && (!boxes || !balanced)) return PKV_ERR_UNSUPPORTED;
+  // Page boxes with fixed splits: kAhFixedHeads KV heads per CTA, so a
+  // request's chunk is kAhFixedHeads / h_kv of a work item that covers every
+  // head, and the items balance over the grid (longest requests first).
+  int hpc = p.h_kv;
+  if (boxes && !balanced && p.h_kv % kAhFixedHeads == 0) hpc = kAhFixedHeads;
   const AhLayout L = ah_layout(hpc, boxes, balanced, fp8);
   if (L.end > AH_SMEM_MAX) return PKV_ERR_UNSUPPORTED;
   static std::atomic<bool> configured[64] = {};  // per device; calls may race
@@ -1667,9 +1694,10 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
   AhMaps maps;
   memset(&maps, 0, sizeof(maps));
   if (boxes && !encode_allheads_maps(&maps, p, hpc)) return PKV_ERR_UNSUPPORTED;
-  // balanced: one persistent CTA per SM; fixed splits: (split, 1, request)
+  // balanced: one persistent CTA per SM; fixed splits: (split, head group,
+  // request rank)
   const dim3 grid = balanced ? dim3(kDecodeBalancedCtas, 1, 1)
-                             : dim3(p.num_splits, 1, p.batch);
+                             : dim3(p.num_splits, p.h_kv / hpc, p.batch);
   const dim3 block((hpc + 1) * 32);
   if (fp8)
     decode_allheads_kernel<true, true><<<grid, block, L.end, stream>>>(p, maps);

@@ -79,8 +79,15 @@ constexpr int kDecodeRowTile = 16;
 // in V, or page size a multiple of 16): one CTA covers every KV head of a
 // request.  num_splits == 0 selects its balanced persistent schedule:
 // kDecodeBalancedCtas CTAs share the batch's 16-key tiles equally (batches up
-// to kDecodeBalancedMaxBatch requests); fixed splits serve page sizes < 8.
+// to kDecodeBalancedMaxBatch requests); fixed splits serve slot rows (all
+// heads per CTA) and page boxes (kDecodeFixedSplitHeads heads per CTA).
 constexpr int kDecodeBalancedCtas = kNumSMs;
+// Page boxes (page size a multiple of 16) with a fixed split count also run on
+// the all-heads kernel, kDecodeFixedSplitHeads KV heads per CTA (0: they stay
+// on the per-KV-head kernel).  Measured on the GQA decode batch with 4 key
+// chunks (64 requests, 8 KV heads): 2 heads 0.849, 4 heads 0.890, 8 heads
+// 0.875 of HBM, against 0.782 on the per-KV-head kernel.
+constexpr int kDecodeFixedSplitHeads = 4;
 constexpr int kDecodeBalancedMaxBatch = 2048;
 bool decode_allheads_eligible(const AttnParams &p);
 int launch_decode_allheads(const AttnParams &p, cudaStream_t stream);
