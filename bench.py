@@ -455,8 +455,91 @@ def fp8_line(dev, peaks):
             "tokens_per_s": g.q.shape[0] / (a_ms / 1e3)}
 
 
+def append_decode_line(dev, peaks):
+    """The KV write before decode attention on the GQA decode batch (each
+    request's last key is its new token), with the bench's 4 key chunks:
+    the unfused pair (set_kv_buffer, then attention) against the fused launch
+    (pkv_append_attn_with_kvcache).  Algorithmic bytes: the K/V read plus the
+    new rows read and written."""
+    g = workloads.make(HEADLINE, value_device=dev)
+    P = g.page_size
+    kv = g.cache_seqlens.cpu().numpy()
+    pt = g.page_table.cpu().numpy()
+    loc = torch.tensor([int(pt[b, (kv[b] - 1) // P]) * P + (kv[b] - 1) % P
+                        for b in range(len(kv))], dtype=torch.int64, device=dev)
+    k_new = g.k_cache.view(-1, *g.k_cache.shape[2:])[loc].clone()
+    v_new = g.v_cache.view(-1, *g.v_cache.shape[2:])[loc].clone()
+    out = torch.empty(g.q.shape[0], g.q.shape[1], g.v_cache.shape[-1], dtype=torch.bfloat16,
+                      device=dev)
+    ws_n = pkv.attn_workspace_size(g.q, g.k_cache, g.v_cache, g.page_table, g.cache_seqlens,
+                                   g.max_seqlen_q, None, g.num_splits)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=dev)
+
+    def unfused():
+        pkv.append_attn_with_kvcache(g.q, k_new, v_new, loc, g.k_cache, g.v_cache,
+                                     g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+                                     g.max_seqlen_q, g.scale, num_splits=g.num_splits,
+                                     out=out, workspace=ws)
+
+    def fused():
+        pkv.fused_append_attn_with_kvcache(g.q, k_new, v_new, loc, g.k_cache, g.v_cache,
+                                           g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+                                           g.max_seqlen_q, g.scale, num_splits=g.num_splits,
+                                           out=out, workspace=ws)
+
+    (u_ms, u_how), (f_ms, f_how) = _timed(unfused), _timed(fused)
+    h_kv, d = g.k_cache.shape[2], g.q.shape[-1]
+    bytes_ = int(g.cache_seqlens.sum()) * h_kv * 2 * d * 2 + 2 * loc.numel() * h_kv * 2 * d * 2
+    return {"kernel": "decode_allheads_kernel (fused append) vs set_kv_buffer_kernel + attention",
+            "new_tokens": int(loc.numel()), "unfused_ms": u_ms, "fused_ms": f_ms,
+            "timing": {"unfused": u_how, "fused": f_how},
+            "fused_GBps": bytes_ / 1e9 / (f_ms / 1e3),
+            "fused_frac_hbm": bytes_ / 1e9 / (f_ms / 1e3) / peaks["hbm_gbs"],
+            "unfused_GBps": bytes_ / 1e9 / (u_ms / 1e3)}
+
+
+def topk_line(dev, peaks):
+    """The top-k index -> slot transform on its own (the MLA decode batch's
+    lists: 128 tokens x 2048 entries, page size 64): reads each entry and its
+    page id, writes the slot; 12 B per entry (entry, page id, slot)."""
+    g = workloads.make("mla_topk_decode", value_device=dev)
+    out = torch.empty_like(g.topk_indices)
+
+    def step():
+        pkv.topk_to_slots(g.topk_indices, g.cu_seqlens_q, g.page_table, g.cache_seqlens,
+                          g.page_size, out=out)
+
+    s_ms, s_how = _timed(step)
+    moved = g.topk_indices.numel() * 12
+    return {"kernel": "topk_to_slots_kernel", "entries": int(g.topk_indices.numel()),
+            "ms_per_step": s_ms, "timing": s_how, "GBps": moved / 1e9 / (s_ms / 1e3),
+            "frac_hbm": moved / 1e9 / (s_ms / 1e3) / peaks["hbm_gbs"]}
+
+
+def merge_line(dev, peaks):
+    """The state merge on its own: two bf16 partial states of the GQA decode
+    batch's shape (64 tokens x 32 heads x 128, fp32 lse) merged into one;
+    reads 2 x (v + lse), writes v + lse."""
+    n, h, d = 64, 32, 128
+    gen = torch.Generator(device=dev).manual_seed(1005)
+    va = torch.randn(n, h, d, device=dev, generator=gen).to(torch.bfloat16)
+    vb = torch.randn(n, h, d, device=dev, generator=gen).to(torch.bfloat16)
+    la = torch.randn(n, h, device=dev, generator=gen)
+    lb = torch.randn(n, h, device=dev, generator=gen)
+    vo, lo = torch.empty_like(va), torch.empty_like(la)
+
+    def step():
+        pkv.merge_state(va, la, vb, lb, vo, lo)
+
+    s_ms, s_how = _timed(step)
+    moved = 3 * va.numel() * 2 + 3 * la.numel() * 4
+    return {"kernel": "merge_state_kernel", "rows": n * h, "ms_per_step": s_ms,
+            "timing": s_how, "GBps": moved / 1e9 / (s_ms / 1e3)}
+
+
 EXTRA_LINES = {"local": local_attention_line, "cascade": cascade_line, "append": append_line,
-               "fp8": fp8_line}
+               "fp8": fp8_line, "topk": topk_line, "merge": merge_line,
+               "append_decode": append_decode_line}
 
 
 def parse_overrides(s: str | None) -> dict:
@@ -834,6 +917,7 @@ def main():
         for label, fn in ((HEADLINE + "@local_chunk_2048", local_attention_line),
                           (HEADLINE + "@cascade_shared_prefix_4096", cascade_line),
                           ("varlen_extend@append_then_attend", append_line),
+                          (HEADLINE + "@fused_append", append_decode_line),
                           (HEADLINE + "@fp8_kv", fp8_line)):
             try:
                 others[label] = fn(dev, peaks)

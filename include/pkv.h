@@ -368,6 +368,48 @@ int pkv_set_kv_buffer_fp8(pkv_tensor loc, pkv_tensor k, pkv_tensor v,
                           cudaStream_t stream);
 
 /*
+ * pkv_append_attn_with_kvcache -- the KV write and the attention in one launch.
+ *
+ * flashattention_backend.py `forward_decode` (and `forward_extend`) stores the
+ * new tokens' K/V with `set_kv_buffer(layer, cache_loc, k, v)` and then runs
+ * `flash_attn_with_kvcache` over the cache that holds them.  This call has
+ * the same result as pkv_set_kv_buffer(cache_loc, k_new, v_new, k_cache,
+ * v_cache) followed by pkv_attn_with_kvcache(... num_splits ...) on one
+ * stream, in one kernel: the attention takes the rows of the request's new
+ * positions (the last q_len_b of its cache_seqlens[b] keys) from k_new /
+ * v_new, and the CTA that covers the request's last key tile stores them
+ * into the cache, so that no part of the launch reads a slot while it is
+ * being written.
+ *
+ * k_new, v_new  (descriptors passed by host pointer, read during the call)
+ *          bf16 [total_q, H_kv, D] / [total_q, H_kv, Dv]: the rows of
+ *          query token t (row t) for the key position
+ *          cache_seqlens[b] - q_len_b + (t - cu_seqlens_q[b]); last dimension
+ *          contiguous, a token's heads adjacent (stride D / Dv), rows
+ *          16-byte aligned.
+ * cache_loc (descriptor by host pointer) int32 or int64 [total_q] slots
+ *          (page * P + position) of those
+ *          positions: they must be the slots the page table maps the
+ *          positions to (the kernel reads the new rows' values from k_new /
+ *          v_new, not from the slots).  A slot outside [0, num_pages * P) is
+ *          skipped and sets PKV_EFLAG_PAGE_OOB.
+ * All other arguments as pkv_attn_with_kvcache (the workspace size is
+ * pkv_attn_workspace_size of the same call), with bf16 caches only.
+ * Served by the all-heads decode kernel (head dim 128, at most 8 KV heads,
+ * at most 16 query rows per KV head; page size below 8 with each slot one
+ * contiguous H_kv x 128 row, or page size a multiple of 16); other shapes
+ * and fp8 caches return PKV_ERR_UNSUPPORTED (use pkv_set_kv_buffer then
+ * pkv_attn_with_kvcache).
+ */
+int pkv_append_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
+                                 pkv_tensor page_table, pkv_tensor cache_seqlens,
+                                 pkv_tensor cu_seqlens_q, int max_seqlen_q, float scale,
+                                 int causal, int window_left, const pkv_tensor *k_new,
+                                 const pkv_tensor *v_new, const pkv_tensor *cache_loc,
+                                 int num_splits, pkv_tensor out, pkv_tensor lse,
+                                 void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * pkv_make_local_attention_virtual_batches -- local (chunked) attention as
  * virtual batches.
  *

@@ -55,6 +55,7 @@ __all__ = [
     "set_kv_buffer",
     "set_mla_kv_buffer",
     "append_attn_with_kvcache",
+    "fused_append_attn_with_kvcache",
     "local_attn_with_kvcache",
     "get_error_flags",
     "clear_error_flags",
@@ -97,6 +98,7 @@ EXPORTED_SYMBOLS = (
     "pkv_set_kv_buffer",
     "pkv_attn_with_kvcache_fp8",
     "pkv_set_kv_buffer_fp8",
+    "pkv_append_attn_with_kvcache",
 )
 
 _FP8 = 5
@@ -154,6 +156,10 @@ def load_library(path: str | None = None):
     lib.pkv_attn_with_kvcache_fp8.argtypes = [T, T, T, T, T, T, c_int, c_float, c_int, c_int,
                                               c_void_p, c_void_p, c_int, T, T, c_void_p,
                                               c_size_t, c_void_p]
+    TP = ctypes.POINTER(T)
+    lib.pkv_append_attn_with_kvcache.argtypes = [T, T, T, T, T, T, c_int, c_float, c_int,
+                                                 c_int, TP, TP, TP, c_int, T, T, c_void_p,
+                                                 c_size_t, c_void_p]
     lib.pkv_make_local_attention_virtual_batches.argtypes = [
         c_int, c_int, T, T, T, T, T, T, T, T, c_void_p]
     lib.pkv_get_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -428,6 +434,37 @@ def append_attn_with_kvcache(q, k, v, cache_loc, k_cache, v_cache, page_table,
     return attn_with_kvcache_fp8(q, k_cache, v_cache, page_table, cache_seqlens, cu_seqlens_q,
                                  max_seqlen_q, softmax_scale, k_descale=kd, v_descale=vd,
                                  **attn_kwargs)
+
+
+def fused_append_attn_with_kvcache(q, k, v, cache_loc, k_cache, v_cache, page_table,
+                                   cache_seqlens, cu_seqlens_q, max_seqlen_q: int,
+                                   softmax_scale: float, causal: bool = False,
+                                   window_left: int = -1, num_splits: int = 0, out=None,
+                                   lse=None, return_softmax_lse: bool = False,
+                                   workspace=None):
+    """The KV write and the attention in one launch (include/pkv.h,
+    pkv_append_attn_with_kvcache): the same result as
+    ``append_attn_with_kvcache`` (bf16 caches, the all-heads decode shapes);
+    ``k`` / ``v`` [total_q, H_kv, D] are the new tokens' rows and
+    ``cache_loc`` their slots."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty(q.shape[0], q.shape[1], v_cache.shape[-1], dtype=torch.bfloat16,
+                          device=q.device)
+    if return_softmax_lse and lse is None:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    ws_bytes = attn_workspace_size(q, k_cache, v_cache, page_table, cache_seqlens,
+                                   max_seqlen_q, None, num_splits)
+    if ws_bytes > 0 and (workspace is None or workspace.numel() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if ws_bytes > 0 else None
+    _check("pkv_append_attn_with_kvcache", lib.pkv_append_attn_with_kvcache(
+        _desc(q), _desc(k_cache), _desc(v_cache), _desc(page_table), _desc(cache_seqlens),
+        _desc(cu_seqlens_q), int(max_seqlen_q), float(softmax_scale), int(bool(causal)),
+        int(window_left), ctypes.byref(_desc(k)), ctypes.byref(_desc(v)),
+        ctypes.byref(_desc(cache_loc)), int(num_splits),
+        _desc(out), _desc(lse), ws_ptr, ws_bytes, _stream(q)))
+    return (out, lse) if return_softmax_lse else out
 
 
 def local_virtual_batch_capacity(batch: int, total_q: int, max_seqlen_q: int,

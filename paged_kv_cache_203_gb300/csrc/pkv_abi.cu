@@ -300,11 +300,16 @@ int pkv_attn_workspace_size(pkv_tensor q, pkv_tensor k_cache,
 namespace pkv {
 namespace {
 
+// The new tokens' rows for the fused KV append (pkv_append_attn_with_kvcache).
+struct AppendArgs {
+  pkv_tensor k_new, v_new, loc;
+};
+
 int attn_impl(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache, pkv_tensor page_table,
               pkv_tensor cache_seqlens, pkv_tensor cu_seqlens_q, int max_seqlen_q,
               float scale, int causal, int window_left, pkv_tensor topk_indices,
               int num_splits, pkv_tensor k_descale, pkv_tensor v_descale, pkv_tensor out,
-              pkv_tensor lse, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+              pkv_tensor lse, void *workspace, size_t workspace_bytes, cudaStream_t stream, const AppendArgs *app = nullptr) {
   AttnPlan plan;
   int rc = plan_attention(q, k_cache, v_cache, page_table, cache_seqlens,
                           max_seqlen_q, topk_indices, num_splits, &plan);
@@ -385,6 +390,31 @@ int attn_impl(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache, pkv_tensor p
   p.kv_fp8 = fp8 ? 1 : 0;
   p.k_descale = static_cast<const float *>(k_descale.data);
   p.v_descale = static_cast<const float *>(v_descale.data);
+  if (app != nullptr) {
+    // fused KV append: bf16 caches on the all-heads decode kernel
+    const int64_t T = q.shape[0], hkv = k_cache.shape[2];
+    const int64_t dk = k_cache.shape[3], dvv = v_cache.shape[3];
+    if (fp8 || plan.kind != 3) return PKV_ERR_UNSUPPORTED;
+    if (!has(app->k_new, PKV_BF16, 3) || !has(app->v_new, PKV_BF16, 3) ||
+        app->k_new.shape[0] != T || app->k_new.shape[1] != hkv || app->k_new.shape[2] != dk ||
+        app->v_new.shape[0] != T || app->v_new.shape[1] != hkv || app->v_new.shape[2] != dvv ||
+        !vec_ok(app->k_new, 2) || !vec_ok(app->v_new, 2))
+      return PKV_ERR_INVALID_ARG;
+    if (app->loc.data == nullptr || app->loc.ndim != 1 || app->loc.shape[0] != T ||
+        (app->loc.dtype != PKV_I32 && app->loc.dtype != PKV_I64) || !unit_stride(app->loc, 0))
+      return PKV_ERR_INVALID_ARG;
+    // a token's heads contiguous (slot rows copy a new row with one bulk copy)
+    if (app->k_new.stride[1] != dk || app->v_new.stride[1] != dvv) return PKV_ERR_UNSUPPORTED;
+    p.append = 1;
+    p.k_new = static_cast<const bf16 *>(app->k_new.data);
+    p.kn_st = app->k_new.stride[0];
+    p.kn_sh = app->k_new.stride[1];
+    p.v_new = static_cast<const bf16 *>(app->v_new.data);
+    p.vn_st = app->v_new.stride[0];
+    p.vn_sh = app->v_new.stride[1];
+    p.new_loc = app->loc.data;
+    p.new_loc_is64 = app->loc.dtype == PKV_I64 ? 1 : 0;
+  }
   if (plan.split()) {
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.ws_o = reinterpret_cast<float *>(ws);
@@ -421,6 +451,21 @@ int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
   return pkv::attn_impl(q, k_cache, v_cache, page_table, cache_seqlens, cu_seqlens_q,
                         max_seqlen_q, scale, causal, window_left, topk_indices, num_splits,
                         none, none, out, lse, workspace, workspace_bytes, stream);
+}
+
+int pkv_append_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
+                                 pkv_tensor page_table, pkv_tensor cache_seqlens,
+                                 pkv_tensor cu_seqlens_q, int max_seqlen_q, float scale,
+                                 int causal, int window_left, const pkv_tensor *k_new,
+                                 const pkv_tensor *v_new, const pkv_tensor *cache_loc,
+                                 int num_splits, pkv_tensor out, pkv_tensor lse,
+                                 void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (k_new == nullptr || v_new == nullptr || cache_loc == nullptr) return PKV_ERR_INVALID_ARG;
+  const pkv_tensor none{};
+  const pkv::AppendArgs app{*k_new, *v_new, *cache_loc};
+  return pkv::attn_impl(q, k_cache, v_cache, page_table, cache_seqlens, cu_seqlens_q,
+                        max_seqlen_q, scale, causal, window_left, none, num_splits, none, none,
+                        out, lse, workspace, workspace_bytes, stream, &app);
 }
 
 int pkv_attn_with_kvcache_fp8(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,

@@ -806,7 +806,7 @@ constexpr int AH_REQ_END = 8;    // the request's last tile
 // function on host and device).
 struct AhLayout {
   uint32_t stage;  // bytes of one K (or V) stage
-  uint32_t k, v, pos, meta, ring_pg, ring_j, voff, pre, scan, bar, end;
+  uint32_t k, v, pos, newt, meta, ring_pg, ring_j, voff, pre, scan, bar, end;
 };
 __host__ __device__ inline AhLayout ah_layout(int hpc, bool boxes, bool balanced,
                                               bool fp8 = false) {
@@ -819,7 +819,8 @@ __host__ __device__ inline AhLayout ah_layout(int hpc, bool boxes, bool balanced
   L.k = 0;
   L.v = L.k + ns * L.stage;
   L.pos = L.v + ns * L.stage;  // int [NSTAGE][BK]
-  L.meta = L.pos + ns * AH_BK * 4;  // int [NSTAGE][2]
+  L.newt = L.pos + ns * AH_BK * 4;  // int [NSTAGE][BK]: new token of the key, or -1
+  L.meta = L.newt + ns * AH_BK * 4;  // int [NSTAGE][2]
   L.ring_pg = L.meta + ns * 8;  // int [RING][BK] page ids
   L.ring_j = L.ring_pg + AH_RING * AH_BK * 4;  // int [RING][BK] key or -1
   L.voff = (L.ring_j + AH_RING * AH_BK * 4 + 7) & ~7u;  // int64 [NSTAGE][BK] (slot rows)
@@ -882,16 +883,40 @@ __device__ __forceinline__ AhReq ah_request(const AttnParams &p, int b) {
   return r;
 }
 
+// The request of rank blockIdx.z when the batch is ordered by tiles to read
+// (descending, ties by index: a permutation); every thread of the CTA calls
+// it (block barriers inside).  work: an int scratch of batch entries; pick:
+// one int.
+__device__ __forceinline__ int ah_rank_to_request(const AttnParams &p, int *work, int *pick) {
+  const int tid = threadIdx.x;
+  if (tid < p.batch) work[tid] = ah_request(p, tid).ntiles;
+  __syncthreads();
+  if (tid < p.batch) {
+    const int wv = work[tid];
+    int rank = 0;
+    for (int j = 0; j < p.batch; ++j) {
+      const int v = work[j];
+      rank += (v > wv) || (v == wv && j < tid);
+    }
+    if (rank == static_cast<int>(blockIdx.z)) *pick = tid;
+  }
+  __syncthreads();
+  const int b = *pick;
+  __syncthreads();  // the ranks are read before the scratch is reused
+  return b;
+}
+
 // CTA of a balanced launch (g CTAs over t tiles) whose share holds tile x.
 __device__ __forceinline__ int ah_cta_of(int64_t x, int64_t g, int64_t t) {
   return static_cast<int>(((x + 1) * g - 1) / t);
 }
 
-template <bool BOXES, bool FP8>
+template <bool BOXES, bool FP8, bool APPEND>
 __global__ void __launch_bounds__((AH_MAXH + 1) * 32, 1)
 decode_allheads_kernel(const __grid_constant__ AttnParams p,
                        const __grid_constant__ AhMaps maps) {
   static_assert(BOXES || !FP8, "fp8 caches use page boxes");
+  static_assert(!(FP8 && APPEND), "the fused append serves bf16 caches");
   constexpr int NST = FP8 ? AH_NSTAGE_FP8 : AH_NSTAGE;  // ring stages
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -908,6 +933,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     return;  // uniform
   }
   int *sPos = reinterpret_cast<int *>(smem + L.pos);
+  int *sNew = reinterpret_cast<int *>(smem + L.newt);
   int *sMeta = reinterpret_cast<int *>(smem + L.meta);
   int64_t *sPre = reinterpret_cast<int64_t *>(smem + L.pre);
   int64_t *sScan = reinterpret_cast<int64_t *>(smem + L.scan);
@@ -975,24 +1001,9 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     // requests by tiles (descending, ties by index: a permutation) in the
     // K ring, which the producer fills only after the barrier below.
     b_first = blockIdx.z;
-    if (p.batch > 1 && p.batch <= nthreads && p.batch * 4 <= static_cast<int>(L.stage)) {
-      int *sWork = reinterpret_cast<int *>(smem + L.k);
-      int *sPick = reinterpret_cast<int *>(smem + L.scan);
-      if (tid < p.batch) sWork[tid] = ah_request(p, tid).ntiles;
-      __syncthreads();
-      if (tid < p.batch) {
-        const int wv = sWork[tid];
-        int rank = 0;
-        for (int j = 0; j < p.batch; ++j) {
-          const int v = sWork[j];
-          rank += (v > wv) || (v == wv && j < tid);
-        }
-        if (rank == static_cast<int>(blockIdx.z)) *sPick = tid;
-      }
-      __syncthreads();
-      b_first = *sPick;
-      __syncthreads();  // the ranks are read before the ring is reused
-    }
+    if (p.batch > 1 && p.batch <= nthreads && p.batch * 4 <= static_cast<int>(L.stage))
+      b_first = ah_rank_to_request(p, reinterpret_cast<int *>(smem + L.k),
+                                   reinterpret_cast<int *>(smem + L.scan));
     const AhReq r = ah_request(p, b_first);
     if (r.ntiles == 0) return;  // uniform
     const int split = blockIdx.x;
@@ -1118,6 +1129,12 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
       const uint32_t kdst = sbase + L.k + st * L.stage;
       const uint32_t vdst = sbase + L.v + st * L.stage;
       if (lane < AH_BK) sPos[st * AH_BK + lane] = pos;
+      if (APPEND && lane < AH_BK) {
+        // fused append: a key at one of the request's new positions is read
+        // from the new rows, not from the cache slot the kernel is filling
+        const int first_new = r.kv_len - r.q_len;
+        sNew[st * AH_BK + lane] = (pos >= 0 && pos >= first_new) ? r.q_begin + (pos - first_new) : -1;
+      }
       if (lane == 0) {
         sMeta[2 * st] = b;
         sMeta[2 * st + 1] = flags;
@@ -1141,9 +1158,11 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
           }
         }
       } else {
-        // K rows by bulk copy; the V rows' offsets are published for the
+        // K rows by bulk copy (a new key's from the new rows: the kernel is
+        // filling its slot); the V rows' offsets are published for the
         // consumer warps, which copy their own head's slices with cp.async
         if (lane < AH_BK) sVoff[st * AH_BK + lane] = pos >= 0 ? voff : -1;
+        const int tk_new = (APPEND && lane < AH_BK) ? sNew[st * AH_BK + lane] : -1;
         const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, pos >= 0)) * row_bytes;
         __syncwarp();
         if (lane == 0) {
@@ -1151,7 +1170,37 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
           mbar_arrive_expect_tx(full, bytes);
         }
         __syncwarp();
-        if (pos >= 0) bulk_g2s(kdst + lane * pitch, p.k + koff, row_bytes, full);
+        if (pos >= 0)
+          bulk_g2s(kdst + lane * pitch,
+                   tk_new >= 0 ? p.k_new + tk_new * p.kn_st + head0 * p.kn_sh : p.k + koff,
+                   row_bytes, full);
+      }
+      // fused append: the CTA that takes the request's last tile stores the
+      // new rows of its heads into their slots (one writer per (request, KV
+      // head group); no CTA reads the new slots of the cache for attention)
+      if (APPEND && (flags & AH_REQ_END)) {
+        const int64_t slots = p.num_pages * p.page_size;
+        const int per_row = hpc * 16;  // 16-byte pieces of one tensor's row
+        for (int u = 0; u < r.q_len; ++u) {
+          const int tk = r.q_begin + u;
+          const int64_t slot = p.new_loc_is64 ? static_cast<const int64_t *>(p.new_loc)[tk]
+                                              : static_cast<const int32_t *>(p.new_loc)[tk];
+          if (slot < 0 || slot >= slots) {
+            if (lane == 0) atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
+            continue;
+          }
+          const int64_t pg = slot / p.page_size, ps = slot - pg * p.page_size;
+          for (int i = lane; i < 2 * per_row; i += 32) {
+            const bool is_v = i >= per_row;
+            const int piece = is_v ? i - per_row : i;
+            const int hh = head0 + piece / 16, c = piece % 16;
+            const bf16 *src = is_v ? p.v_new + tk * p.vn_st + hh * p.vn_sh + c * 8
+                                   : p.k_new + tk * p.kn_st + hh * p.kn_sh + c * 8;
+            bf16 *dst = is_v ? const_cast<bf16 *>(p.v) + pg * p.v_sp + ps * p.v_spos + hh * p.v_sh
+                             : const_cast<bf16 *>(p.k) + pg * p.k_sp + ps * p.k_spos + hh * p.k_sh;
+            *reinterpret_cast<uint4 *>(dst + c * 8) = *reinterpret_cast<const uint4 *>(src);
+          }
+        }
       }
       // next tile (a balanced run moves on to the next request with tiles;
       // a fixed split never leaves its request)
@@ -1205,8 +1254,11 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
       for (int i = 0; i < 8; ++i) {
         const int rr = (lane >> 4) + 2 * i;
         const int64_t vo = sVoff[sx * AH_BK + rr];
-        cp_async16(vdst + soff(rr, c), vo >= 0 ? p.v + vo + h * 128 + c * 8 : p.v,
-                   vo >= 0 ? 16 : 0);
+        const int tk = APPEND ? sNew[sx * AH_BK + rr] : -1;  // fused append: the new row
+        const bf16 *src = tk >= 0   ? p.v_new + tk * p.vn_st + h * p.vn_sh + c * 8
+                          : vo >= 0 ? p.v + vo + h * 128 + c * 8
+                                    : p.v;
+        cp_async16(vdst + soff(rr, c), src, (tk >= 0 || vo >= 0) ? 16 : 0);
       }
     }
     if (!BOXES) cp_async_commit();
@@ -1291,6 +1343,30 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
         if (pos_st[rr] < 0)
           *reinterpret_cast<uint4 *>(smem + L.v + st * L.stage + soff(rr, cc)) =
               make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+    // fused append, page boxes: the boxes hold the cache rows of the
+    // request's new positions as they were before this call (the slots are
+    // being filled by this launch); this head's K and V slices of those keys
+    // are replaced by the new rows (slot rows get them from the copies)
+    bool patched = false;
+    if (BOXES && APPEND) {
+      const int *new_st = sNew + st * AH_BK;
+      uint32_t nm = __ballot_sync(0xffffffffu, lane < AH_BK && new_st[lane & 15] >= 0);
+      patched = nm != 0;
+      while (nm) {
+        const int rr = __ffs(nm) - 1;
+        nm &= nm - 1;
+        const int tk = new_st[rr];
+        if (lane < 16) {
+          const uint4 kv = *reinterpret_cast<const uint4 *>(p.k_new + tk * p.kn_st + h * p.kn_sh +
+                                                            lane * 8);
+          const uint4 vv = *reinterpret_cast<const uint4 *>(p.v_new + tk * p.vn_st + h * p.vn_sh +
+                                                            lane * 8);
+          *reinterpret_cast<uint4 *>(smem + L.k + st * L.stage + soff(rr, lane)) = kv;
+          *reinterpret_cast<uint4 *>(smem + L.v + st * L.stage + soff(rr, lane)) = vv;
+        }
       }
       __syncwarp();
     }
@@ -1406,7 +1482,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
         mma_bf16(o[2 * cc + 1], a0, a1, a2, a3, b2, b3);
       }
     }
-    if (any_skipped) fence_proxy_async();  // generic zeros before async rewrites
+    if (any_skipped || patched) fence_proxy_async();  // generic writes before async rewrites
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * st);
 
@@ -1675,20 +1751,20 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
   if (boxes && !balanced && p.h_kv % kAhFixedHeads == 0) hpc = kAhFixedHeads;
   const AhLayout L = ah_layout(hpc, boxes, balanced, fp8);
   if (L.end > AH_SMEM_MAX) return PKV_ERR_UNSUPPORTED;
+  if (p.append && fp8) return PKV_ERR_UNSUPPORTED;
   static std::atomic<bool> configured[64] = {};  // per device; calls may race
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(decode_allheads_kernel<true, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, AH_SMEM_MAX) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(decode_allheads_kernel<false, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, AH_SMEM_MAX) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(decode_allheads_kernel<true, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, AH_SMEM_MAX) !=
-            cudaSuccess)
-      return PKV_ERR_CUDA;
+    const void *fns[] = {reinterpret_cast<const void *>(decode_allheads_kernel<true, false, false>),
+                         reinterpret_cast<const void *>(decode_allheads_kernel<false, false, false>),
+                         reinterpret_cast<const void *>(decode_allheads_kernel<true, true, false>),
+                         reinterpret_cast<const void *>(decode_allheads_kernel<true, false, true>),
+                         reinterpret_cast<const void *>(decode_allheads_kernel<false, false, true>)};
+    for (const void *fn : fns)
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, AH_SMEM_MAX) !=
+          cudaSuccess)
+        return PKV_ERR_CUDA;
     if (dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   AhMaps maps;
@@ -1700,11 +1776,15 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
                              : dim3(p.num_splits, p.h_kv / hpc, p.batch);
   const dim3 block((hpc + 1) * 32);
   if (fp8)
-    decode_allheads_kernel<true, true><<<grid, block, L.end, stream>>>(p, maps);
+    decode_allheads_kernel<true, true, false><<<grid, block, L.end, stream>>>(p, maps);
+  else if (boxes && p.append)
+    decode_allheads_kernel<true, false, true><<<grid, block, L.end, stream>>>(p, maps);
   else if (boxes)
-    decode_allheads_kernel<true, false><<<grid, block, L.end, stream>>>(p, maps);
+    decode_allheads_kernel<true, false, false><<<grid, block, L.end, stream>>>(p, maps);
+  else if (p.append)
+    decode_allheads_kernel<false, false, true><<<grid, block, L.end, stream>>>(p, maps);
   else
-    decode_allheads_kernel<false, false><<<grid, block, L.end, stream>>>(p, maps);
+    decode_allheads_kernel<false, false, false><<<grid, block, L.end, stream>>>(p, maps);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -64,6 +64,16 @@ struct AttnParams {
   int kv_fp8;
   const float *k_descale;             // optional [batch][h_kv]
   const float *v_descale;             // optional [batch][h_kv]
+  // fused KV append (all-heads decode kernel): the new tokens' rows k_new /
+  // v_new [total_q][h_kv][d] stand in for the cache rows of their positions
+  // and are stored into their slots new_loc[t] by the kernel
+  int append;
+  const bf16 *k_new;
+  int64_t kn_st, kn_sh;
+  const bf16 *v_new;
+  int64_t vn_st, vn_sh;
+  const void *new_loc;
+  int new_loc_is64;
 };
 
 // Error word of the current device (static __device__ in pkv_abi.cu).

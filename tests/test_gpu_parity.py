@@ -1044,6 +1044,126 @@ def test_append_then_attend(kind):
     assert pkv.get_error_flags() == 0
 
 
+def _new_rows(wl):
+    """Slots of every request's new positions (the last q_len of its keys)
+    and those rows' K / V, taken from the workload's pool."""
+    P = wl.k_cache.shape[1]
+    cu, kv, pt = wl.cu_seqlens_q.numpy(), wl.cache_seqlens.numpy(), wl.page_table.numpy()
+    loc = [int(pt[b, j // P]) * P + j % P
+           for b in range(len(kv)) for j in range(kv[b] - (cu[b + 1] - cu[b]), kv[b])]
+    loc = torch.tensor(loc, dtype=torch.int64)
+    kf = wl.k_cache.view(-1, *wl.k_cache.shape[2:])
+    vf = wl.v_cache.view(-1, *wl.v_cache.shape[2:])
+    return loc, kf[loc].clone(), vf[loc].clone()
+
+
+@pytest.mark.parametrize("page_size,q_len,num_splits,window",
+                         [(16, 1, 0, -1), (16, 1, 4, -1), (16, 4, 0, -1), (16, 3, 2, 300),
+                          (1, 1, 0, -1), (1, 1, 3, -1), (1, 4, 0, 200), (64, 2, 5, -1)])
+def test_fused_append_attend(page_size, q_len, num_splits, window):
+    """The KV write and the attention in one launch (slot rows and page
+    boxes, the balanced schedule and fixed splits, runs of new tokens that
+    straddle key tiles, windows): the pool starts with NaN in the new slots;
+    afterwards it equals the workload's pool bit for bit, the output equals
+    the oracle's, and it is bit-identical to the unfused write-then-attend
+    pair in the same launch configuration."""
+    h_q, h_kv = 8 * (4 // q_len if q_len <= 4 else 1), 8
+    wl = workloads.make("tiny_decode", d=128, page_size=page_size, h_q=h_q, h_kv=h_kv, batch=19,
+                        q_len=q_len, causal=True, window_left=window, len_lo=q_len,
+                        len_hi=1500, pool_tokens=19 * (1500 + page_size) + 64,
+                        seed=90 + page_size + q_len)
+    loc, k_new, v_new = _new_rows(wl)
+    g = wl.to(DEV)
+    outs = []
+    for fused in (True, False):
+        kd, vd = g.k_cache.clone(), g.v_cache.clone()
+        kd.view(-1, *kd.shape[2:])[loc.to(DEV)] = float("nan")
+        vd.view(-1, *vd.shape[2:])[loc.to(DEV)] = float("nan")
+        fn = pkv.fused_append_attn_with_kvcache if fused else pkv.append_attn_with_kvcache
+        out, lse = fn(g.q, k_new.to(DEV), v_new.to(DEV), loc.to(DEV), kd, vd, g.page_table,
+                      g.cache_seqlens, g.cu_seqlens_q, g.max_seqlen_q, g.scale, causal=True,
+                      window_left=window, num_splits=num_splits, return_softmax_lse=True)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(kd), _bits(wl.k_cache))
+        assert np.array_equal(_bits(vd), _bits(wl.v_cache))
+        outs.append((out, lse))
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(outs[0][0], outs[0][1], ref_o, ref_l, "fused append+attend")
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
+    assert pkv.get_error_flags() == 0
+
+
+def test_fused_append_attend_bad_slot_and_unsupported():
+    """A slot outside the pool is skipped and flagged (the attention still
+    uses the new row); fp8 caches and shapes off the all-heads kernel are
+    refused without a launch."""
+    wl = workloads.make("tiny_decode", d=128, page_size=16, h_q=32, h_kv=8, batch=5,
+                        len_lo=20, len_hi=300, pool_tokens=5 * 320 + 64, seed=97)
+    loc, k_new, v_new = _new_rows(wl)
+    bad = loc.clone()
+    bad[2] = wl.k_cache.shape[0] * 16 + 5
+    g = wl.to(DEV)
+    kd, vd = g.k_cache.clone(), g.v_cache.clone()
+    out, lse = pkv.fused_append_attn_with_kvcache(
+        g.q, k_new.to(DEV), v_new.to(DEV), bad.to(DEV), kd, vd, g.page_table, g.cache_seqlens,
+        g.cu_seqlens_q, g.max_seqlen_q, g.scale, return_softmax_lse=True)
+    torch.cuda.synchronize()
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, "fused append, bad slot")
+    assert pkv.get_error_flags() & pkv.EFLAG_PAGE_OOB
+    pkv.clear_error_flags()
+    k8, v8 = g.k_cache.to(torch.float8_e4m3fn), g.v_cache.to(torch.float8_e4m3fn)
+    with pytest.raises(pkv.PkvError, match="UNSUPPORTED"):
+        pkv.fused_append_attn_with_kvcache(
+            g.q, k_new.to(DEV), v_new.to(DEV), loc.to(DEV), k8, v8, g.page_table,
+            g.cache_seqlens, g.cu_seqlens_q, g.max_seqlen_q, g.scale)
+    wl64 = workloads.make("tiny_decode", d=64, page_size=16, h_q=8, h_kv=2, batch=3,
+                          len_lo=20, len_hi=100, pool_tokens=3 * 120 + 64, seed=98)
+    loc64, kn64, vn64 = _new_rows(wl64)
+    g64 = wl64.to(DEV)
+    with pytest.raises(pkv.PkvError, match="UNSUPPORTED"):
+        pkv.fused_append_attn_with_kvcache(
+            g64.q, kn64.to(DEV), vn64.to(DEV), loc64.to(DEV), g64.k_cache, g64.v_cache,
+            g64.page_table, g64.cache_seqlens, g64.cu_seqlens_q, g64.max_seqlen_q, g64.scale)
+
+
+def test_fused_append_attend_full_size():
+    """The GQA decode batch (64 requests, 32/8 heads, kv U[512, 8192], page
+    16) with each request's last key as its new token, in the bench's launch
+    configuration (4 key chunks): pool bit for bit, every output row against
+    the oracle."""
+    wl = workloads.make("gqa_split_decode", value_device=DEV)
+    loc, k_new, v_new = _new_rows_device(wl)
+    kd, vd = wl.k_cache.clone(), wl.v_cache.clone()
+    kd.view(-1, *kd.shape[2:])[loc] = float("nan")
+    vd.view(-1, *vd.shape[2:])[loc] = float("nan")
+    out, lse = pkv.fused_append_attn_with_kvcache(
+        wl.q, k_new, v_new, loc, kd, vd, wl.page_table, wl.cache_seqlens, wl.cu_seqlens_q,
+        wl.max_seqlen_q, wl.scale, num_splits=4, return_softmax_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(kd.view(torch.int16), wl.k_cache.view(torch.int16))
+    assert torch.equal(vd.view(torch.int16), wl.v_cache.view(torch.int16))
+    ref_o, ref_l, _ = oracle.attention(
+        oracle.bf16_bits(wl.q), oracle.bf16_bits(wl.k_cache), oracle.bf16_bits(wl.v_cache),
+        wl.page_table.cpu().numpy(), wl.cache_seqlens.cpu().numpy(),
+        wl.cu_seqlens_q.cpu().numpy(), wl.scale)
+    check_close(out, lse, ref_o, ref_l, "fused append full size")
+    assert pkv.get_error_flags() == 0
+
+
+def _new_rows_device(wl):
+    P = wl.k_cache.shape[1]
+    cu, kv = wl.cu_seqlens_q.cpu().numpy(), wl.cache_seqlens.cpu().numpy()
+    pt = wl.page_table.cpu().numpy()
+    loc = [int(pt[b, j // P]) * P + j % P
+           for b in range(len(kv)) for j in range(kv[b] - (cu[b + 1] - cu[b]), kv[b])]
+    loc = torch.tensor(loc, dtype=torch.int64, device=wl.k_cache.device)
+    kf = wl.k_cache.view(-1, *wl.k_cache.shape[2:])
+    vf = wl.v_cache.view(-1, *wl.v_cache.shape[2:])
+    return loc, kf[loc].clone(), vf[loc].clone()
+
+
 # ------------------------------------------------------------------ FP8 KV
 
 def _to_fp8(t):
