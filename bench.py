@@ -516,29 +516,36 @@ def topk_line(dev, peaks):
             "frac_hbm": moved / 1e9 / (s_ms / 1e3) / peaks["hbm_gbs"]}
 
 
-def merge_line(dev, peaks):
-    """The state merge on its own: two bf16 partial states of the GQA decode
-    batch's shape (64 tokens x 32 heads x 128, fp32 lse) merged into one;
-    reads 2 x (v + lse), writes v + lse."""
-    n, h, d = 64, 32, 128
-    gen = torch.Generator(device=dev).manual_seed(1005)
-    va = torch.randn(n, h, d, device=dev, generator=gen).to(torch.bfloat16)
-    vb = torch.randn(n, h, d, device=dev, generator=gen).to(torch.bfloat16)
-    la = torch.randn(n, h, device=dev, generator=gen)
-    lb = torch.randn(n, h, device=dev, generator=gen)
-    vo, lo = torch.empty_like(va), torch.empty_like(la)
+def merge_line(dev, peaks, sizes=(("decode_batch", 64), ("prefill", 32768))):
+    """The state merge on its own: two bf16 partial states (v [n, 32 heads,
+    128], fp32 lse) merged into one; reads 2 x (v + lse), writes v + lse.
+    Two sizes: the GQA decode batch's shape (64 tokens, launch-bound) and a
+    prefill-sized one (32768 tokens, 805 MB moved, larger than L2)."""
+    h, d = 32, 128
+    out = {"kernel": "merge_state_kernel"}
+    for label, n in sizes:
+        gen = torch.Generator(device=dev).manual_seed(1005)
+        va = torch.randn(n, h, d, device=dev, generator=gen).to(torch.bfloat16)
+        vb = torch.randn(n, h, d, device=dev, generator=gen).to(torch.bfloat16)
+        la = torch.randn(n, h, device=dev, generator=gen)
+        lb = torch.randn(n, h, device=dev, generator=gen)
+        vo, lo = torch.empty_like(va), torch.empty_like(la)
 
-    def step():
-        pkv.merge_state(va, la, vb, lb, vo, lo)
+        def step():
+            pkv.merge_state(va, la, vb, lb, vo, lo)
 
-    s_ms, s_how = _timed(step)
-    moved = 3 * va.numel() * 2 + 3 * la.numel() * 4
-    return {"kernel": "merge_state_kernel", "rows": n * h, "ms_per_step": s_ms,
-            "timing": s_how, "GBps": moved / 1e9 / (s_ms / 1e3)}
+        s_ms, s_how = _timed(step)
+        moved = 3 * va.numel() * 2 + 3 * la.numel() * 4
+        out[label] = {"rows": n * h, "ms_per_step": s_ms, "timing": s_how,
+                      "GBps": moved / 1e9 / (s_ms / 1e3),
+                      "frac_hbm": moved / 1e9 / (s_ms / 1e3) / peaks["hbm_gbs"]}
+        del va, vb, la, lb, vo, lo
+    return out
 
 
 EXTRA_LINES = {"local": local_attention_line, "cascade": cascade_line, "append": append_line,
                "fp8": fp8_line, "topk": topk_line, "merge": merge_line,
+               "merge_prefill": lambda dev, peaks: merge_line(dev, peaks, (("prefill", 32768),)),
                "append_decode": append_decode_line}
 
 

@@ -158,10 +158,11 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
     plan->kind = 3;
     plan->num_splits = 0;
     plan->n_row_tiles = 1;
-    const size_t slots = 2ull * kDecodeBalancedCtas * max_seqlen_q * h_q;
+    const size_t slots = 2ull * kDecodeBalancedShares * max_seqlen_q * h_q;
     plan->ws_o_bytes = align256(slots * dv * 4);
     plan->ws_lse_bytes = align256(slots * 4);
-    plan->ws_ctr_bytes = align256(static_cast<size_t>(batch) * h_kv * 4);
+    // merge tickets [batch][h_kv], then the share counter
+    plan->ws_ctr_bytes = align256((static_cast<size_t>(batch) * h_kv + 1) * 4);
     return PKV_OK;
   }
   if (mla) {
@@ -248,12 +249,14 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
   plan->ws_ctr_bytes =
       align256(static_cast<size_t>(batch) * h_kv * plan->n_row_tiles * 4);
   if (plan->kind == 3 && num_splits == 0 && batch <= kDecodeBalancedMaxBatch) {
-    // balanced persistent schedule: per CTA two partial slots (its first and
-    // last request) of one request's rows
+    // balanced persistent schedule: per share two partial slots (its first
+    // and last request) of one request's rows; the share counter follows the
+    // merge tickets
     plan->num_splits = 0;
-    const size_t slots = 2ull * kDecodeBalancedCtas * max_seqlen_q * h_q;
+    const size_t slots = 2ull * kDecodeBalancedShares * max_seqlen_q * h_q;
     plan->ws_o_bytes = align256(slots * dv * 4);
     plan->ws_lse_bytes = align256(slots * 4);
+    plan->ws_ctr_bytes = align256((static_cast<size_t>(batch) * h_kv + 1) * 4);
   }
   return PKV_OK;
 }

@@ -797,16 +797,20 @@ constexpr int AH_SMEM_MAX = 232448;
 constexpr int kAhFixedHeads = kDecodeFixedSplitHeads;
 
 // stage flags published by the producer beside each tile's key positions
-constexpr int AH_SEG_START = 1;  // first tile this CTA takes of the request
-constexpr int AH_SEG_END = 2;    // last tile this CTA takes of the request
-constexpr int AH_REQ_START = 4;  // the request's first tile
-constexpr int AH_REQ_END = 8;    // the request's last tile
+constexpr int AH_SEG_START = 1;    // first tile of a segment (a share's run of one request)
+constexpr int AH_SEG_END = 2;      // last tile of a segment
+constexpr int AH_REQ_START = 4;    // the request's first tile
+constexpr int AH_REQ_END = 8;      // the request's last tile
+constexpr int AH_SHARE_FIRST = 16; // the share's first tile
+constexpr int AH_CTA_LAST = 32;    // the CTA's last tile
+constexpr int AH_MQ = 64;          // merge-queue slots of a CTA (a ring)
+constexpr int AH_CLAIM_RING = 8;   // shares claimed ahead of the copy cursor
 
 // Shared-memory plan from the heads per CTA and the copy mode (the same
 // function on host and device).
 struct AhLayout {
   uint32_t stage;  // bytes of one K (or V) stage
-  uint32_t k, v, pos, newt, meta, ring_pg, ring_j, voff, pre, scan, bar, end;
+  uint32_t k, v, pos, newt, meta, ring_pg, ring_j, voff, pre, scan, mq, bar, end;
 };
 __host__ __device__ inline AhLayout ah_layout(int hpc, bool boxes, bool balanced,
                                               bool fp8 = false) {
@@ -820,18 +824,22 @@ __host__ __device__ inline AhLayout ah_layout(int hpc, bool boxes, bool balanced
   L.v = L.k + ns * L.stage;
   L.pos = L.v + ns * L.stage;  // int [NSTAGE][BK]
   L.newt = L.pos + ns * AH_BK * 4;  // int [NSTAGE][BK]: new token of the key, or -1
-  L.meta = L.newt + ns * AH_BK * 4;  // int [NSTAGE][2]
-  L.ring_pg = L.meta + ns * 8;  // int [RING][BK] page ids
+  L.meta = L.newt + ns * AH_BK * 4;  // int [NSTAGE][4]: request, flags, share
+  L.ring_pg = L.meta + ns * 16;  // int [RING][BK] page ids
   L.ring_j = L.ring_pg + AH_RING * AH_BK * 4;  // int [RING][BK] key or -1
   L.voff = (L.ring_j + AH_RING * AH_BK * 4 + 7) & ~7u;  // int64 [NSTAGE][BK] (slot rows)
   L.pre = L.voff + ns * AH_BK * 8;  // int64 [MAXB + 1]
   L.scan = L.pre + (balanced ? (AH_MAXB + 1) * 8 : 0);  // int64 [16]
-  L.bar = L.scan + 16 * 8;
+  // merge queue: int jobs [AH_MQ], int sequence numbers [AH_MQ], then head,
+  // tail, consumers done, first share, and the claimed shares [AH_CLAIM_RING]
+  L.mq = L.scan + 16 * 8;
+  L.bar = L.mq + (2 * AH_MQ + 4 + AH_CLAIM_RING) * 4;
   L.end = L.bar + 3 * ns * 8;  // full, empty, V offsets published
   return L;
 }
-static_assert(AH_NSTAGE * 2 * (AH_BK * (AH_MAXH * 256 + 16)) + 18 * 1024 <= AH_SMEM_MAX,
+static_assert(AH_NSTAGE * 2 * (AH_BK * (AH_MAXH * 256 + 16)) + 19 * 1024 <= AH_SMEM_MAX,
               "all-heads decode smem plan exceeds 227 KB");
+static_assert((2 * AH_MQ + 4 + AH_CLAIM_RING) % 2 == 0, "8-byte aligned barriers");
 
 struct AhMaps {
   CUtensorMap k;
@@ -911,8 +919,101 @@ __device__ __forceinline__ int ah_cta_of(int64_t x, int64_t g, int64_t t) {
   return static_cast<int>(((x + 1) * g - 1) / t);
 }
 
+__device__ __forceinline__ float ah_warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float ah_warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Log-sum-exp merge of the np partial states of rows [0, n_rows) of request
+// r, KV head h, into the output (one warp; Dv = 128, each lane 4 columns).
+// pidx(sp, rloc) is the workspace index of partial sp of the row whose
+// offset in the request's rows is rloc = u * h_q + head.  Four rows at a
+// time; partials in passes of 32 (lane = partial for the lse; the running
+// sums are rescaled between passes) with the value loads of a pass unrolled
+// so that 16 of them are in flight.
+template <class PIdx>
+__device__ void ah_merge_rows(const AttnParams &p, const AhReq &r, int h, int n_rows, int np,
+                              PIdx pidx) {
+  constexpr int R = 4;
+  const int lane = threadIdx.x & 31;
+  for (int rr0 = 0; rr0 < n_rows; rr0 += R) {
+    const int nr = min(R, n_rows - rr0);
+    int64_t rl[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int rr = rr0 + min(i, nr - 1);
+      rl[i] = static_cast<int64_t>(rr / p.group) * p.h_q + h * p.group + rr % p.group;
+    }
+    float Ms[R], ws[R], acc[R][4];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      Ms[i] = -INFINITY;
+      ws[i] = 0.f;
+      acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    }
+    for (int s0 = 0; s0 < np; s0 += 32) {
+      const int sp = s0 + lane;
+      float l[R], w[R];
+#pragma unroll
+      for (int i = 0; i < R; ++i)
+        l[i] = (sp < np && i < nr) ? __ldcg(p.ws_lse + pidx(sp, rl[i])) : -INFINITY;
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        const float mx = fmaxf(Ms[i], ah_warp_max(l[i]));
+        // rescale what earlier passes added (exactly 1 when the max holds)
+        const float sc = mx == -INFINITY ? 1.f : exp2f((Ms[i] - mx) * kLog2e);
+        ws[i] *= sc;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[i][e] *= sc;
+        Ms[i] = mx;
+        w[i] = l[i] == -INFINITY ? 0.f : exp2f((l[i] - mx) * kLog2e);
+        ws[i] += ah_warp_sum(w[i]);
+      }
+      const int cnt = min(32, np - s0);
+#pragma unroll 4
+      for (int j = 0; j < cnt; ++j) {
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          const float wj = __shfl_sync(0xffffffffu, w[i], j);
+          if (i < nr) {
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+                                        p.ws_o + pidx(s0 + j, rl[i]) * p.dv) + lane);
+            acc[i][0] += wj * v.x;
+            acc[i][1] += wj * v.y;
+            acc[i][2] += wj * v.z;
+            acc[i][3] += wj * v.w;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      if (i >= nr) break;
+      const int rr = rr0 + i;
+      const int tok = r.q_begin + rr / p.group;
+      const int head = h * p.group + rr % p.group;
+      const float winv = ws[i] > 0.f ? 1.f / ws[i] : 0.f;
+      bf16 *dst = p.out + static_cast<int64_t>(tok) * p.o_st + static_cast<int64_t>(head) * p.o_sh +
+                  lane * 4;
+      uint2 w2;
+      w2.x = pack_bf16(acc[i][0] * winv, acc[i][1] * winv);
+      w2.y = pack_bf16(acc[i][2] * winv, acc[i][3] * winv);
+      *reinterpret_cast<uint2 *>(dst) = w2;
+      if (p.lse != nullptr && lane == 0)
+        p.lse[static_cast<int64_t>(tok) * p.lse_st + static_cast<int64_t>(head) * p.lse_sh] =
+            ws[i] > 0.f ? Ms[i] + logf(ws[i]) : -INFINITY;
+    }
+  }
+}
+
 template <bool BOXES, bool FP8, bool APPEND>
-__global__ void __launch_bounds__((AH_MAXH + 1) * 32, 1)
+__global__ void __launch_bounds__((AH_MAXH + 2) * 32, 1)
 decode_allheads_kernel(const __grid_constant__ AttnParams p,
                        const __grid_constant__ AhMaps maps) {
   static_assert(BOXES || !FP8, "fp8 caches use page boxes");
@@ -923,9 +1024,11 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int nthreads = blockDim.x;
-  const int hpc = nthreads / 32 - 1;  // KV heads of this CTA = consumer warps
-  const int head0 = blockIdx.y * hpc;  // its first KV head
   const bool balanced = p.num_splits == 0;
+  // KV heads of this CTA = consumer warps; then the producer warp and (the
+  // balanced schedule) the merge warp
+  const int hpc = nthreads / 32 - (balanced ? 2 : 1);
+  const int head0 = blockIdx.y * hpc;  // its first KV head
   const AhLayout L = ah_layout(hpc, BOXES, balanced, FP8);
   const uint32_t sbase = smem_addr(smem);
   if (BOXES && (sbase & 1023u) != 0) {  // swizzled boxes need a 1024-byte aligned base
@@ -941,6 +1044,14 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   const uint32_t empty0 = full0 + NST * 8;
   const uint32_t vmeta0 = empty0 + NST * 8;
   int64_t *sVoff = reinterpret_cast<int64_t *>(smem + L.voff);
+  // merge queue: jobs, then head / tail / consumer warps done / the first
+  // share (balanced), then the ring of claimed shares
+  int *sQ = reinterpret_cast<int *>(smem + L.mq);
+  int *sQSeq = sQ + AH_MQ;
+  int *sQHead = sQ + 2 * AH_MQ, *sQTail = sQHead + 1, *sQDone = sQHead + 2;
+  int *sFirstShare = sQHead + 3;
+  int *sClaim = sQHead + 4;
+  int *share_ctr = p.ws_counter + static_cast<int64_t>(p.batch) * p.h_kv;  // balanced
   const uint32_t row_bytes = static_cast<uint32_t>(hpc) * 256u;  // the CTA's heads of one key
   const uint32_t pitch = row_bytes + 16u;                         // slot-row mode
 
@@ -952,9 +1063,16 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     fence_proxy_async();
+    // the CTA's first share (balanced); its latency overlaps the scan below
+    if (balanced) *sFirstShare = atomicAdd(share_ctr, 1);
+    *sQHead = 0;
+    *sQTail = 0;
+    *sQDone = 0;
   }
+  for (int i = tid; i < AH_MQ; i += nthreads) sQSeq[i] = i;  // slot i free for job i
 
-  // ---- this CTA's run of tiles: n tiles from tile t_first of request b_first ----
+  // ---- this CTA's tiles: balanced, the shares it claims (the first one
+  // above); fixed splits, n tiles from tile t_first of request b_first ----
   int b_first = 0, t_first = 0, n = 0;
   int64_t T = 0, G = 1;
   if (balanced) {
@@ -980,19 +1098,8 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     if (tid == nthreads - 1) sPre[p.batch] = run;
     __syncthreads();
     T = sPre[p.batch];
-    G = min(static_cast<int64_t>(gridDim.x), T);
-    const int64_t c = blockIdx.x;
-    if (c >= G) return;  // uniform: no work (also T == 0)
-    const int64_t x0 = c * T / G, x1 = (c + 1) * T / G;
-    n = static_cast<int>(x1 - x0);
-    // request holding tile x0: the last b with sPre[b] <= x0
-    int lo_b = 0, hi_b = p.batch;  // sPre[lo_b] <= x0 < sPre[hi_b]
-    while (hi_b - lo_b > 1) {
-      const int mid = (lo_b + hi_b) >> 1;
-      if (sPre[mid] <= x0) lo_b = mid; else hi_b = mid;
-    }
-    b_first = lo_b;
-    t_first = static_cast<int>(x0 - sPre[lo_b]);
+    G = min(static_cast<int64_t>(kDecodeBalancedShares), T);  // shares
+    if (*sFirstShare >= G) return;  // uniform: no share left (also T == 0)
   } else {
     __syncthreads();
     // longest requests first: blockIdx.z is a rank, not a request.  The
@@ -1023,30 +1130,88 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     // waits for its tile's group and reads the ids back (each lane its own).
     int *ring_pg = reinterpret_cast<int *>(smem + L.ring_pg);
     int *ring_j = reinterpret_cast<int *>(smem + L.ring_j);
-    int b = b_first, t = t_first;
-    AhReq r = ah_request(p, b);
-    int fb = b, ft = t;
-    AhReq fr = r;
-    auto advance = [&](int &bb, int &tt, AhReq &rr) {
-      if (++tt >= rr.ntiles && balanced && bb < p.batch - 1) {
+    // A cursor walks the CTA's tiles: share k of the CTA (share id c), tile i
+    // of the share's len, request b and its tile t.  A fixed split is one
+    // share of one request.  Balanced: the shares come from the counter; the
+    // fetch cursor claims them (one claim in flight ahead of it) and records
+    // them in a ring that the copy cursor reads.
+    struct Cur {
+      int k, c, i, len, b, t;
+      AhReq r;
+    };
+    auto enter = [&](Cur &u, int k, int c) {
+      u.k = k;
+      u.c = c;
+      u.i = 0;
+      if (balanced) {
+        const int64_t x0 = c * T / G, x1 = (c + 1) * T / G;
+        u.len = static_cast<int>(x1 - x0);
+        // request holding tile x0: the last b with sPre[b] <= x0
+        int lo_b = 0, hi_b = p.batch;  // sPre[lo_b] <= x0 < sPre[hi_b]
+        while (hi_b - lo_b > 1) {
+          const int mid = (lo_b + hi_b) >> 1;
+          if (sPre[mid] <= x0) lo_b = mid; else hi_b = mid;
+        }
+        u.b = lo_b;
+        u.t = static_cast<int>(x0 - sPre[lo_b]);
+      } else {
+        u.len = n;
+        u.b = b_first;
+        u.t = t_first;
+      }
+      u.r = ah_request(p, u.b);
+    };
+    // to the next tile of the share (a balanced share moves on to the next
+    // request with tiles; a fixed split never leaves its request)
+    auto step_in_share = [&](Cur &u) {
+      ++u.i;
+      if (++u.t >= u.r.ntiles && balanced && u.b < p.batch - 1) {
         do {
-          ++bb;
-        } while (bb < p.batch - 1 && sPre[bb + 1] == sPre[bb]);
-        tt = 0;
-        rr = ah_request(p, bb);
+          ++u.b;
+        } while (u.b < p.batch - 1 && sPre[u.b + 1] == sPre[u.b]);
+        u.t = 0;
+        u.r = ah_request(p, u.b);
       }
     };
+    int pend = 0;  // lane 0: the claim for the share after the fetch cursor's
+    if (balanced && lane == 0) pend = atomicAdd(share_ctr, 1);
+    // fetch cursor: to the next tile; false at the end of the CTA's tiles
+    auto fetch_step = [&](Cur &u) -> bool {
+      if (u.i + 1 < u.len) {
+        step_in_share(u);
+        return true;
+      }
+      if (!balanced) return false;
+      int c = __shfl_sync(0xffffffffu, pend, 0);
+      if (c >= G) c = -1;
+      if (lane == 0) {
+        sClaim[(u.k + 1) % AH_CLAIM_RING] = c;
+        if (c >= 0) pend = atomicAdd(share_ctr, 1);
+      }
+      __syncwarp();
+      if (c < 0) return false;
+      enter(u, u.k + 1, c);
+      return true;
+    };
+    // copy cursor: the share after share k (or -1), as the fetch cursor
+    // claimed it (the fetch cursor passed the end of share k first)
+    auto next_share = [&](const Cur &u) -> int {
+      return balanced ? sClaim[(u.k + 1) % AH_CLAIM_RING] : -1;
+    };
+    Cur f, cc;
+    enter(f, 0, balanced ? *sFirstShare : 0);
+    cc = f;
     auto fetch = [&](int x) {
       const int slot = (x % AH_RING) * AH_BK + lane;
-      const int key0 = (fr.t_lo + ft) * AH_BK;
+      const int key0 = (f.r.t_lo + f.t) * AH_BK;
       if (BOXES) {
         if (lane == 0) {
           int jj = -1;
-          if (max(key0, fr.lo) < min(key0 + AH_BK, fr.hi)) {  // a key of the tile is live
+          if (max(key0, f.r.lo) < min(key0 + AH_BK, f.r.hi)) {  // a key of the tile is live
             const int pidx = key0 / p.page_size;  // the whole tile lies in this page
             if (pidx < p.pt_cols) {
               cp_async4(sbase + L.ring_pg + slot * 4,
-                        p.page_table + static_cast<int64_t>(fb) * p.pt_stride + pidx);
+                        p.page_table + static_cast<int64_t>(f.b) * p.pt_stride + pidx);
               jj = key0;
             } else {
               atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
@@ -1057,11 +1222,11 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
       } else if (lane < AH_BK) {
         const int j = key0 + lane;
         int jj = -1;
-        if (j >= fr.lo && j < fr.hi) {
+        if (j >= f.r.lo && j < f.r.hi) {
           const int pidx = j / p.page_size;
           if (pidx < p.pt_cols) {
             cp_async4(sbase + L.ring_pg + slot * 4,
-                      p.page_table + static_cast<int64_t>(fb) * p.pt_stride + pidx);
+                      p.page_table + static_cast<int64_t>(f.b) * p.pt_stride + pidx);
             jj = j;
           } else {
             atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
@@ -1071,17 +1236,28 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
       }
       cp_async_commit();
     };
+    bool f_live = true;  // the fetch cursor points at a tile
     for (int x = 0; x < AH_LOOKAHEAD; ++x) {
-      if (x < n) fetch(x);
-      else cp_async_commit();
-      if (x + 1 < n) advance(fb, ft, fr);
+      if (f_live) {
+        fetch(x);
+        f_live = fetch_step(f);
+      } else {
+        cp_async_commit();
+      }
     }
-    for (int kt = 0; kt < n; ++kt) {
+    int kt = 0;
+    for (;; ++kt) {
       const int st = kt % NST;
-      if (kt + AH_LOOKAHEAD < n) fetch(kt + AH_LOOKAHEAD);
-      else cp_async_commit();
-      if (kt + AH_LOOKAHEAD + 1 < n) advance(fb, ft, fr);
+      if (f_live) {
+        fetch(kt + AH_LOOKAHEAD);
+        f_live = fetch_step(f);
+      } else {
+        cp_async_commit();
+      }
       cp_async_wait_group<AH_LOOKAHEAD>();  // this tile's ids have landed
+      const AhReq &r = cc.r;
+      const int b = cc.b, t = cc.t;
+      const bool cta_last = cc.i + 1 >= cc.len && next_share(cc) < 0;
       const int slot = (kt % AH_RING) * AH_BK + lane;
       const int key0 = (r.t_lo + t) * AH_BK;
       int pos = -1;
@@ -1112,10 +1288,12 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
         }
       }
       int flags = 0;
-      if (kt == 0 || t == 0) flags |= AH_SEG_START;
-      if (kt == n - 1 || t == r.ntiles - 1) flags |= AH_SEG_END;
+      if (cc.i == 0 || t == 0) flags |= AH_SEG_START;
+      if (cc.i == cc.len - 1 || t == r.ntiles - 1) flags |= AH_SEG_END;
       if (t == 0) flags |= AH_REQ_START;
       if (t == r.ntiles - 1) flags |= AH_REQ_END;
+      if (cc.i == 0) flags |= AH_SHARE_FIRST;
+      if (cta_last) flags |= AH_CTA_LAST;
 
       int ok = 1;
       if (lane == 0 && kt >= NST)
@@ -1136,8 +1314,9 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
         sNew[st * AH_BK + lane] = (pos >= 0 && pos >= first_new) ? r.q_begin + (pos - first_new) : -1;
       }
       if (lane == 0) {
-        sMeta[2 * st] = b;
-        sMeta[2 * st + 1] = flags;
+        sMeta[4 * st] = b;
+        sMeta[4 * st + 1] = flags;
+        sMeta[4 * st + 2] = cc.c;
       }
       if (BOXES) {
         __syncwarp();
@@ -1202,12 +1381,131 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
           }
         }
       }
-      // next tile (a balanced run moves on to the next request with tiles;
-      // a fixed split never leaves its request)
-      if (kt + 1 < n) advance(b, t, r);
+      if (cta_last) break;
+      if (cc.i + 1 < cc.len) step_in_share(cc);
+      else enter(cc, cc.k + 1, next_share(cc));
+    }
+    // Slot rows: the consumer warps copy V two tiles ahead, so the two
+    // stages after the CTA's last tile get V offsets too (none: zero fills),
+    // published once their previous tiles are released.
+    if (!BOXES) {
+      for (int x = kt + 1; x <= kt + 2; ++x) {
+        const int st = x % NST;
+        int ok = 1;
+        if (lane == 0 && x >= NST)
+          ok = mbar_wait_sleep(empty0 + 8 * st, ((x / NST) & 1) ^ 1) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+          break;
+        }
+        if (lane < AH_BK) {
+          sVoff[st * AH_BK + lane] = -1;
+          if (APPEND) sNew[st * AH_BK + lane] = -1;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(vmeta0 + 8 * st);
+      }
     }
     cp_async_commit();
     cp_async_wait_group<0>();  // no ring write outlives the CTA
+    return;
+  }
+  const int64_t rows_total = static_cast<int64_t>(p.total_q) * p.h_q;
+  const int64_t rows_req = static_cast<int64_t>(p.max_seqlen_q) * p.h_q;  // balanced slots
+  // Merge of the partial states of request b, KV head hk, by one warp:
+  // balanced, one partial per share that holds a tile of the request (the
+  // first share's second slot when the request starts inside it); fixed
+  // splits, one per split.
+  auto merge_job = [&](int b, int hk) {
+    const AhReq r = ah_request(p, b);
+    const int n_rows = min(r.q_len, p.max_seqlen_q) * p.group;
+    if (balanced) {
+      const int c0 = ah_cta_of(sPre[b], G, T);
+      const int np = ah_cta_of(sPre[b + 1] - 1, G, T) - c0 + 1;
+      const bool c0_second = static_cast<int64_t>(c0) * T / G < sPre[b];
+      ah_merge_rows(p, r, hk, n_rows, np, [&](int sp, int64_t rl) -> int64_t {
+        return (static_cast<int64_t>(c0 + sp) * 2 + (sp == 0 && c0_second ? 1 : 0)) * rows_req + rl;
+      });
+    } else {
+      const int64_t base = static_cast<int64_t>(r.q_begin) * p.h_q;
+      ah_merge_rows(p, r, hk, n_rows, p.num_splits, [&](int sp, int64_t rl) -> int64_t {
+        return static_cast<int64_t>(sp) * rows_total + base + rl;
+      });
+    }
+  };
+  volatile int *vQ = sQ;
+  const int n_cons = min(hpc, p.h_kv - head0);  // consumer warps with a KV head
+  // Merge queue of the CTA: a ring of AH_MQ jobs (request << 4 | KV head)
+  // with a sequence number per slot (job n goes to slot n % AH_MQ; the slot
+  // holds n when free for it and n + 1 once it holds it).  Consumer warps
+  // append (waiting for a free slot, which the merge warp always makes);
+  // the merge warp takes jobs while the consumers stream, and every warp
+  // once the consumers' tiles are done.  pop_job returns a job, or -1 when
+  // none is queued; lane 0 decides, the warp gets the result.
+  volatile int *vSeq = sQSeq;
+  auto pop_job = [&]() -> int {
+    int job = -1;
+    if (lane == 0) {
+      volatile int *vh = sQHead, *vt = sQTail;
+      int hd = *vh;
+      while (hd < *vt) {
+        const int got = atomicCAS(sQHead, hd, hd + 1);
+        if (got == hd) {
+          // job hd is written right after its ticket was taken (or once its
+          // slot was freed)
+          const int sl = hd % AH_MQ;
+          const long long t0 = clock64();
+          while (vSeq[sl] != hd + 1 && clock64() - t0 < kSleepWaitCycles) __nanosleep(32);
+          if (vSeq[sl] == hd + 1) {
+            __threadfence_block();
+            job = vQ[sl];
+            __threadfence_block();
+            vSeq[sl] = hd + AH_MQ;  // free for job hd + AH_MQ
+          } else {
+            atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+          }
+          break;
+        }
+        hd = got;
+      }
+    }
+    return __shfl_sync(0xffffffffu, job, 0);
+  };
+  // Takes jobs until every consumer warp is done and the queue is empty.
+  auto drain_jobs = [&](int sleep_ns) {
+    long long idle0 = clock64();
+    while (true) {
+      int job = pop_job();
+      if (job >= 0) {
+        __threadfence();  // the other CTAs' partials (their tickets came first)
+        merge_job(job >> 4, job & 15);
+        idle0 = clock64();
+        continue;
+      }
+      int done = lane == 0 ? *reinterpret_cast<volatile int *>(sQDone) : 0;
+      done = __shfl_sync(0xffffffffu, done, 0);
+      if (done >= n_cons) {
+        __threadfence_block();  // jobs queued before the last count are seen
+        job = pop_job();
+        if (job < 0) break;
+        __threadfence();
+        merge_job(job >> 4, job & 15);
+        continue;
+      }
+      if (clock64() - idle0 > kSleepWaitCycles) {
+        if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+        break;
+      }
+      __nanosleep(sleep_ns);
+    }
+  };
+
+  if (balanced && warp == hpc + 1) {
+    // =============================== merge warp ===============================
+    // Merges split requests from the queue while the consumer warps stream,
+    // so that neither they nor the CTA's ring wait on a merge.
+    drain_jobs(256);
     return;
   }
   if (warp > hpc || head0 + warp >= p.h_kv) return;  // no KV head for this warp
@@ -1216,8 +1514,6 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   const int w = warp;          // head within the CTA
   const int h = head0 + w;     // KV head
   const int g = lane >> 2, tq = lane & 3;
-  const int64_t rows_total = static_cast<int64_t>(p.total_q) * p.h_q;
-  const int64_t rows_req = static_cast<int64_t>(p.max_seqlen_q) * p.h_q;  // balanced slots
   const bool use_upper = p.causal || p.window_left >= 0;
   // byte offset of 16-byte chunk c of key `key` of this head within a stage
   // (fp8: chunk c holds the 16 codes of columns 16c..16c+15)
@@ -1238,14 +1534,14 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   int n_rows = 0;
   float sl2 = p.scale_log2;  // softmax scale (log2 domain), times k_descale
   float vdesc = 1.f;         // v_descale of the current request and head
-  bool seg_req_start = false, first_seg = true;
+  bool seg_req_start = false, seg_share_first = false;
 
   // Slot rows: this warp copies its head's 256-byte V slice of every key of
   // tile x (16 rows x 16 chunks, 8 per lane; skipped keys zero-filled), one
   // cp.async group per tile.  The stage's region of this head was last read
   // by this warp's own PV three tiles earlier.
   auto issue_v = [&](int x) -> bool {
-    if (!BOXES && x < n) {
+    if (!BOXES) {  // the producer publishes V offsets up to two tiles past the CTA's last
       const int sx = x % NST;
       if (!mbar_wait_sleep(vmeta0 + 8 * sx, (x / NST) & 1)) return false;
       const int c = lane & 15;
@@ -1266,19 +1562,23 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   };
   bool v_ok = issue_v(0) && issue_v(1);
 
-  for (int kt = 0; v_ok && kt < n; ++kt) {
+  bool stop = false;
+  for (int kt = 0; v_ok && !stop; ++kt) {
     const int st = kt % NST;
     if (!mbar_wait_sleep(full0 + 8 * st, (kt / NST) & 1) || !issue_v(kt + 2)) {
       if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
       break;
     }
-    const int b = sMeta[2 * st];
-    const int flags = sMeta[2 * st + 1];
+    const int b = sMeta[4 * st];
+    const int flags = sMeta[4 * st + 1];
+    const int share = sMeta[4 * st + 2];
+    stop = (flags & AH_CTA_LAST) != 0;
     if (flags & AH_SEG_START) {
       // a new request: its rows for this head, Q fragments from global memory
       r = ah_request(p, b);
       n_rows = min(r.q_len, p.max_seqlen_q) * p.group;  // <= 16 on this path
       seg_req_start = (flags & AH_REQ_START) != 0;
+      seg_share_first = (flags & AH_SHARE_FIRST) != 0;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int rr = g + 8 * hh;
@@ -1489,8 +1789,9 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     if (!(flags & AH_SEG_END)) continue;
     // ------------------- end of this CTA's share of request b -------------------
     const bool whole = balanced ? (seg_req_start && (flags & AH_REQ_END) != 0) : p.num_splits == 1;
-    const int slot = first_seg ? 0 : 1;
-    first_seg = false;
+    // a share's first segment takes its slot 0, its last one slot 1 (every
+    // other segment of the share is a whole request)
+    const int slot = seg_share_first ? 0 : 1;
     float Lsum[2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -1529,7 +1830,7 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
               lse_nat;
       } else {
         const int64_t widx =
-            balanced ? (static_cast<int64_t>(blockIdx.x) * 2 + slot) * rows_req +
+            balanced ? (static_cast<int64_t>(share) * 2 + slot) * rows_req +
                            static_cast<int64_t>(u) * p.h_q + head
                      : static_cast<int64_t>(blockIdx.x) * rows_total +
                            static_cast<int64_t>(tok) * p.h_q + head;
@@ -1551,14 +1852,11 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     }
     if (whole) continue;
 
-    // partial written: the last CTA to finish this (request, KV head) merges
-    int expected = p.num_splits, c0 = 0;
-    bool c0_second_slot = false;
-    if (balanced) {
-      c0 = ah_cta_of(sPre[b], G, T);
-      expected = ah_cta_of(sPre[b + 1] - 1, G, T) - c0 + 1;
-      c0_second_slot = static_cast<int64_t>(c0) * T / G < sPre[b];
-    }
+    // partial written: the last warp to finish this (request, KV head) hands
+    // the merge to its CTA's merge warp
+    int expected = p.num_splits;
+    if (balanced)
+      expected = ah_cta_of(sPre[b + 1] - 1, G, T) - ah_cta_of(sPre[b], G, T) + 1;
     __threadfence();
     __syncwarp();
     int last = 0;
@@ -1566,45 +1864,27 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
       last = atomicAdd(p.ws_counter + static_cast<int64_t>(b) * p.h_kv + h, 1) == expected - 1;
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) continue;
-    __threadfence();
-    for (int rr = 0; rr < n_rows; ++rr) {
-      const int u = rr / p.group;
-      const int tok = r.q_begin + u;
-      const int head = h * p.group + rr % p.group;
-      const int64_t rloc = balanced ? static_cast<int64_t>(u) * p.h_q + head
-                                    : static_cast<int64_t>(tok) * p.h_q + head;
-      auto src = [&](int sp) -> int64_t {
-        return balanced ? (static_cast<int64_t>(c0 + sp) * 2 + (sp == 0 && c0_second_slot ? 1 : 0)) *
-                                  rows_req + rloc
-                        : static_cast<int64_t>(sp) * rows_total + rloc;
-      };
-      float Ms = -INFINITY;
-      for (int sp = 0; sp < expected; ++sp) Ms = fmaxf(Ms, __ldcg(p.ws_lse + src(sp)));
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      float wsum = 0.f;
-      if (Ms != -INFINITY) {
-        for (int sp = 0; sp < expected; ++sp) {
-          const int64_t sidx = src(sp);
-          const float wgt = exp2f((__ldcg(p.ws_lse + sidx) - Ms) * kLog2e);
-          wsum += wgt;
-          const float4 v4 = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + sidx * p.dv + lane * 4));
-          acc[0] += wgt * v4.x; acc[1] += wgt * v4.y; acc[2] += wgt * v4.z; acc[3] += wgt * v4.w;
-        }
+    if (lane == 0) {
+      const int q = atomicAdd(sQTail, 1);
+      const int sl = q % AH_MQ;
+      const long long t0 = clock64();
+      while (vSeq[sl] != q && clock64() - t0 < kSleepWaitCycles) __nanosleep(64);
+      if (vSeq[sl] == q) {
+        vQ[sl] = (b << 4) | h;
+        __threadfence_block();
+        vSeq[sl] = q + 1;
+      } else {
+        atomicOr(p.err, PKV_EFLAG_TIMEOUT);
       }
-      const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
-      bf16 *dst = p.out + static_cast<int64_t>(tok) * p.o_st + static_cast<int64_t>(head) * p.o_sh +
-                  lane * 4;
-      uint2 w2;
-      w2.x = pack_bf16(acc[0] * winv, acc[1] * winv);
-      w2.y = pack_bf16(acc[2] * winv, acc[3] * winv);
-      *reinterpret_cast<uint2 *>(dst) = w2;
-      if (p.lse != nullptr && lane == 0)
-        p.lse[static_cast<int64_t>(tok) * p.lse_st + static_cast<int64_t>(head) * p.lse_sh] =
-            wsum > 0.f ? Ms + logf(wsum) : -INFINITY;
     }
   }
   if (!v_ok) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
   if (!BOXES) cp_async_wait_group<0>();  // none of this warp's copies outlives the CTA
+  if (lane == 0) {
+    __threadfence_block();  // the jobs this warp queued before the count
+    atomicAdd(sQDone, 1);
+  }
+  drain_jobs(64);  // the CTA's remaining merges, shared by all its warps
 }
 
 // ------------------------------------------------------------------- host
@@ -1770,11 +2050,11 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
   AhMaps maps;
   memset(&maps, 0, sizeof(maps));
   if (boxes && !encode_allheads_maps(&maps, p, hpc)) return PKV_ERR_UNSUPPORTED;
-  // balanced: one persistent CTA per SM; fixed splits: (split, head group,
-  // request rank)
+  // balanced: one persistent CTA per SM, claiming shares; fixed splits:
+  // (split, head group, request rank)
   const dim3 grid = balanced ? dim3(kDecodeBalancedCtas, 1, 1)
                              : dim3(p.num_splits, p.h_kv / hpc, p.batch);
-  const dim3 block((hpc + 1) * 32);
+  const dim3 block((hpc + (balanced ? 2 : 1)) * 32);  // + producer (+ merge warp)
   if (fp8)
     decode_allheads_kernel<true, true, false><<<grid, block, L.end, stream>>>(p, maps);
   else if (boxes && p.append)

@@ -88,10 +88,20 @@ constexpr int kDecodeRowTile = 16;
 // head; page size < 8 with each slot one contiguous H_kv x 128 row in K and
 // in V, or page size a multiple of 16): one CTA covers every KV head of a
 // request.  num_splits == 0 selects its balanced persistent schedule:
-// kDecodeBalancedCtas CTAs share the batch's 16-key tiles equally (batches up
-// to kDecodeBalancedMaxBatch requests); fixed splits serve slot rows (all
-// heads per CTA) and page boxes (kDecodeFixedSplitHeads heads per CTA).
+// the batch's 16-key tiles, laid end to end, are cut into
+// kDecodeBalancedShares equal shares, which kDecodeBalancedCtas persistent
+// CTAs claim from a counter (batches up to kDecodeBalancedMaxBatch
+// requests); fixed splits serve slot rows (all heads per CTA) and page boxes
+// (kDecodeFixedSplitHeads heads per CTA).
 constexpr int kDecodeBalancedCtas = kNumSMs;
+// Shares per CTA of the balanced schedule: finer shares would absorb the
+// SMs' different memory service rates, but each split adds a partial state
+// and a merge.  Measured with the merges in a background warp: 1 share per
+// CTA 0.718 / 0.891 of HBM (sliding-window / GQA decode batches), 2 shares
+// 0.600 / 0.843, 4 shares 0.448 / 0.762: the merges cost more than the
+// finer balance recovers.
+constexpr int kDecodeSharesPerCta = 1;
+constexpr int kDecodeBalancedShares = kDecodeBalancedCtas * kDecodeSharesPerCta;
 // Page boxes (page size a multiple of 16) with a fixed split count also run on
 // the all-heads kernel, kDecodeFixedSplitHeads KV heads per CTA (0: they stay
 // on the per-KV-head kernel).  Measured on the GQA decode batch with 4 key
