@@ -88,7 +88,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct AttnPlan {
   int kind;          // 0 = decode-gqa, 1 = tcgen05 extend, 2 = tcgen05 MLA top-k,
-                     // 3 = all-heads small-page decode
+                     // 3 = all-heads small-page decode, 4 = short decode
   int num_splits;    // 0 with kind 3: balanced persistent schedule
   int n_row_tiles;
   size_t ws_o_bytes, ws_lse_bytes, ws_ctr_bytes;
@@ -215,8 +215,11 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
     lp.v_sp = v.stride[0];
     lp.v_spos = v.stride[1];
     lp.v_sh = v.stride[2];
+    lp.pt_cols = static_cast<int>(std::min<int64_t>(pt.shape[1], 0x7fffffff));
     if (max_seqlen_q >= kExtendMinSeqlenQ && extend_eligible(lp))
       plan->kind = 1;  // tcgen05 extend, no workspace
+    else if (num_splits <= 1 && decode_short_eligible(lp))
+      plan->kind = 4;  // short requests: one CTA per (request, KV head), no workspace
     else if (decode_allheads_eligible(lp) &&
              (page < 8 || (num_splits == 0 && batch <= kDecodeBalancedMaxBatch) ||
               (num_splits > 0 && kDecodeFixedSplitHeads > 0 && page % 16 == 0)))
@@ -241,7 +244,7 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
     splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s, 64)));
   }
   splits = std::min(splits, 1024);
-  if (plan->kind == 1) splits = 1;
+  if (plan->kind == 1 || plan->kind == 4) splits = 1;
   plan->num_splits = splits;
   const size_t rows_total = static_cast<size_t>(total_q) * h_q;
   plan->ws_o_bytes = align256(static_cast<size_t>(splits) * rows_total * dv * 4);
@@ -394,9 +397,15 @@ int attn_impl(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache, pkv_tensor p
   p.k_descale = static_cast<const float *>(k_descale.data);
   p.v_descale = static_cast<const float *>(v_descale.data);
   if (app != nullptr) {
-    // fused KV append: bf16 caches on the all-heads decode kernel
+    // fused KV append: bf16 caches on the all-heads decode kernel (short
+    // batches too, unsplit: no workspace, as planned)
     const int64_t T = q.shape[0], hkv = k_cache.shape[2];
     const int64_t dk = k_cache.shape[3], dvv = v_cache.shape[3];
+    if (plan.kind == 4 && decode_allheads_eligible(p)) {
+      plan.kind = 3;
+      plan.num_splits = 1;
+      p.num_splits = 1;
+    }
     if (fp8 || plan.kind != 3) return PKV_ERR_UNSUPPORTED;
     if (!has(app->k_new, PKV_BF16, 3) || !has(app->v_new, PKV_BF16, 3) ||
         app->k_new.shape[0] != T || app->k_new.shape[1] != hkv || app->k_new.shape[2] != dk ||
@@ -429,6 +438,7 @@ int attn_impl(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache, pkv_tensor p
   if (p.total_q == 0) return PKV_OK;
   if (plan.kind == 2) return launch_mla_topk(p, stream);
   if (plan.kind == 3) return launch_decode_allheads(p, stream);
+  if (plan.kind == 4) return launch_decode_short(p, stream);
   if (plan.kind == 1) {
     // the extend kernel takes row maxima of raw scores: positive scale only
     rc = scale > 0.f ? launch_extend_tc(p, stream) : PKV_ERR_UNSUPPORTED;

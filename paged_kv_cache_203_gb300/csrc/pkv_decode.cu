@@ -846,30 +846,6 @@ struct AhMaps {
   CUtensorMap v;
 };
 
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
-      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
-// 2^x on the MUFU (PTX ex2.approx, flush-to-zero; 2^-inf = 0).
-__device__ __forceinline__ float ah_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // A request's query run and key range [lo, hi) in 16-key tiles.
 struct AhReq {
   int q_begin, q_len, kv_len, lo, hi, t_lo, ntiles;  // ntiles 0: nothing to do
@@ -1721,13 +1697,13 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float m_new = fmaxf(m_run[hh], mx);
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      alpha[hh] = ah_exp2(m_run[hh] - m_use);  // exactly 1 while the max holds
+      alpha[hh] = fast_exp2(m_run[hh] - m_use);  // exactly 1 while the max holds
       m_run[hh] = m_new;
       float sum = 0.f;
 #pragma unroll
       for (int nn = 0; nn < 2; ++nn) {
-        sc[nn][2 * hh] = ah_exp2(sc[nn][2 * hh] - m_use);
-        sc[nn][2 * hh + 1] = ah_exp2(sc[nn][2 * hh + 1] - m_use);
+        sc[nn][2 * hh] = fast_exp2(sc[nn][2 * hh] - m_use);
+        sc[nn][2 * hh + 1] = fast_exp2(sc[nn][2 * hh + 1] - m_use);
         sum += sc[nn][2 * hh] + sc[nn][2 * hh + 1];
       }
       l_run[hh] = l_run[hh] * alpha[hh] + sum;
@@ -1885,6 +1861,249 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     atomicAdd(sQDone, 1);
   }
   drain_jobs(64);  // the CTA's remaining merges, shared by all its warps
+}
+
+// ============================================================================
+// Short decode (head dim 128, <= 16 query rows per KV head, bf16 cache, a
+// page table that covers at most kDecodeShortMaxKeys keys): one CTA per
+// (request, KV head), SD_WARPS warps of SD_KEYS keys each.  Everything is
+// loaded up front: the request's lengths and each lane's page id in one
+// step (the ids of the whole table row are read, so they need not wait for
+// the lengths), then every K and V row of the warp's keys and the Q
+// fragments.  Each warp computes the softmax state of its keys (mma.sync,
+// log2 domain) and the CTA merges the warps' states in shared memory: no
+// split partials, tickets or second pass, for batches whose whole attention
+// is a few microseconds of latency.
+// ============================================================================
+
+constexpr int SD_WARPS = 8;
+constexpr int SD_KEYS = 32;                  // keys per warp
+constexpr int SD_PITCH = 128 * 2 + 16;       // bytes per K / V row (skewed: conflict-free ldmatrix)
+constexpr int SD_OPITCH = 128 + 4;           // floats per row of a warp's merged O
+static_assert(SD_WARPS * SD_KEYS == kDecodeShortMaxKeys, "short decode key budget");
+constexpr uint32_t SD_ROWS = 2u * SD_WARPS * SD_KEYS * SD_PITCH;  // K and V rows
+// then each key's (K, V) element offsets: int64 [WARPS][KEYS][2]
+constexpr uint32_t SD_SMEM = SD_ROWS + SD_WARPS * SD_KEYS * 16;
+static_assert(SD_WARPS * (2 * 16 + 16 * SD_OPITCH) * 4 <= SD_ROWS, "merge area fits the rows");
+
+__global__ void __launch_bounds__(SD_WARPS * 32, 1)
+decode_short_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x;  // KV head
+  const int b = blockIdx.y;  // request
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t kw = sbase + static_cast<uint32_t>(warp * SD_KEYS * SD_PITCH);
+  const uint32_t vw = kw + static_cast<uint32_t>(SD_WARPS * SD_KEYS * SD_PITCH);
+  const int g = lane >> 2, tq = lane & 3;
+
+  // ---- lengths and this lane's page id, loaded together ----
+  const int j = warp * SD_KEYS + lane;  // this lane's key
+  const int pidx = j / p.page_size;
+  const int pg_raw = pidx < p.pt_cols ? p.page_table[static_cast<int64_t>(b) * p.pt_stride + pidx] : -1;
+  const int q_begin = p.cu_seqlens_q[b];
+  const int q_len = p.cu_seqlens_q[b + 1] - q_begin;
+  const int kv_len = p.cache_seqlens[b];
+  if (q_len <= 0 || q_begin < 0 || q_begin + q_len > p.total_q) return;  // uniform
+  const int n_rows = min(q_len, p.max_seqlen_q) * p.group;  // <= 16
+  const int hi = max(kv_len, 0);
+  const int lo = p.window_left >= 0 ? max(0, kv_len - q_len - p.window_left) : 0;
+  bool live = j >= lo && j < hi;
+  if (live && pidx >= p.pt_cols) {
+    atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
+    live = false;
+  }
+  if (live && (pg_raw < 0 || pg_raw >= p.num_pages)) {
+    atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
+    live = false;
+  }
+  const int inpage = j - pidx * p.page_size;
+  const int64_t koff = live ? pg_raw * p.k_sp + static_cast<int64_t>(inpage) * p.k_spos + h * p.k_sh : -1;
+  const int64_t voff = live ? pg_raw * p.v_sp + static_cast<int64_t>(inpage) * p.v_spos + h * p.v_sh : -1;
+  const uint32_t live_mask = __ballot_sync(0xffffffffu, live);
+
+  // ---- the warp's K and V rows (dead keys zero-filled), then Q ----
+  // Offsets go through shared memory (one broadcast load per key instead of
+  // shuffles); a half of 16 keys with no live key is neither copied nor
+  // computed (its scores are masked, so its terms are exactly 0).
+  const bool half_live[2] = {(live_mask & 0xffffu) != 0u, (live_mask >> 16) != 0u};
+  {
+    int64_t *sOff = reinterpret_cast<int64_t *>(smem + SD_ROWS) + warp * SD_KEYS * 2;
+    sOff[2 * lane] = koff;
+    sOff[2 * lane + 1] = voff;
+    __syncwarp();
+    const int c = lane & 15;
+    const bool is_v = lane >= 16;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      if (!half_live[hf]) continue;
+#pragma unroll 8
+      for (int i = 16 * hf; i < 16 * hf + 16; ++i) {
+        const longlong2 kv = *reinterpret_cast<const longlong2 *>(sOff + 2 * i);
+        const int64_t off = is_v ? kv.y : kv.x;
+        const bf16 *base = is_v ? p.v : p.k;
+        cp_async16((is_v ? vw : kw) + static_cast<uint32_t>(i * SD_PITCH + c * 16),
+                   off >= 0 ? base + off + c * 8 : base, off >= 0 ? 16 : 0);
+      }
+    }
+    cp_async_commit();
+  }
+  uint32_t qf[8][4];
+  int rpos[2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int rr = g + 8 * hh;
+    const bool rv = rr < n_rows;
+    const int u = rv ? rr / p.group : 0;
+    const int gg = rv ? rr % p.group : 0;
+    rpos[hh] = kv_len - q_len + u;
+    const bf16 *qrow = p.q + static_cast<int64_t>(q_begin + u) * p.q_st +
+                       static_cast<int64_t>(h * p.group + gg) * p.q_sh;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int c0 = kk * 16 + 2 * tq;
+      qf[kk][hh] = rv ? *reinterpret_cast<const uint32_t *>(qrow + c0) : 0u;
+      qf[kk][2 + hh] = rv ? *reinterpret_cast<const uint32_t *>(qrow + c0 + 8) : 0u;
+    }
+  }
+  cp_async_wait_group<0>();
+  __syncwarp();
+
+  // ---- S = Q K^T over the warp's 32 keys (4 blocks of 8), masked ----
+  float sc[4][4];
+#pragma unroll
+  for (int nb = 0; nb < 4; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+  {
+    const int key = (lane >> 4) * 8 + (lane & 7);
+    const int kc = (lane >> 3) & 1;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      if (!half_live[hf]) continue;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kw + static_cast<uint32_t>((16 * hf + key) * SD_PITCH + (2 * kk + kc) * 16), b0,
+                b1, b2, b3);
+        mma_bf16(sc[2 * hf], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+        mma_bf16(sc[2 * hf + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+      }
+    }
+  }
+  const bool use_upper = p.causal || p.window_left >= 0;
+  float m_row[2], l_row[2];
+#pragma unroll
+  for (int nb = 0; nb < 4; ++nb)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int kl = nb * 8 + 2 * tq + (e & 1);  // key within the warp
+      const int kp = warp * SD_KEYS + kl;
+      const int hh = e >> 1;
+      bool masked = ((live_mask >> kl) & 1u) == 0u;
+      if (use_upper && kp > rpos[hh]) masked = true;
+      if (p.window_left >= 0 && kp < rpos[hh] - p.window_left) masked = true;
+      sc[nb][e] = masked ? -INFINITY : sc[nb][e] * p.scale_log2;
+    }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) mx = fmaxf(mx, fmaxf(sc[nb][2 * hh], sc[nb][2 * hh + 1]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mu = mx == -INFINITY ? 0.f : mx;
+    float sum = 0.f;
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) {
+      sc[nb][2 * hh] = fast_exp2(sc[nb][2 * hh] - mu);
+      sc[nb][2 * hh + 1] = fast_exp2(sc[nb][2 * hh + 1] - mu);
+      sum += sc[nb][2 * hh] + sc[nb][2 * hh + 1];
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    m_row[hh] = mx;
+    l_row[hh] = sum;
+  }
+
+  // ---- O = P V (two 16-key steps) ----
+  float o[16][4];
+#pragma unroll
+  for (int nn = 0; nn < 16; ++nn) o[nn][0] = o[nn][1] = o[nn][2] = o[nn][3] = 0.f;
+  {
+    const int m = lane >> 3;
+    const int key = (m & 1) * 8 + (lane & 7);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      if (!half_live[hf]) continue;
+      const uint32_t a0 = pack_bf16(sc[2 * hf][0], sc[2 * hf][1]);
+      const uint32_t a1 = pack_bf16(sc[2 * hf][2], sc[2 * hf][3]);
+      const uint32_t a2 = pack_bf16(sc[2 * hf + 1][0], sc[2 * hf + 1][1]);
+      const uint32_t a3 = pack_bf16(sc[2 * hf + 1][2], sc[2 * hf + 1][3]);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vw + static_cast<uint32_t>((16 * hf + key) * SD_PITCH + (2 * cc + (m >> 1)) * 16),
+                  b0, b1, b2, b3);
+        mma_bf16(o[2 * cc], a0, a1, a2, a3, b0, b1);
+        mma_bf16(o[2 * cc + 1], a0, a1, a2, a3, b2, b3);
+      }
+    }
+  }
+
+  // ---- the warps' states merged in shared memory (the rows' area reused) ----
+  __syncthreads();  // every warp is done with the K / V rows
+  float *sM = reinterpret_cast<float *>(smem);               // [WARPS][16]
+  float *sL = sM + SD_WARPS * 16;                            // [WARPS][16]
+  float *sO = sL + SD_WARPS * 16;                            // [WARPS][16][OPITCH]
+  if (tq == 0) {
+    sM[warp * 16 + g] = m_row[0];
+    sM[warp * 16 + g + 8] = m_row[1];
+    sL[warp * 16 + g] = l_row[0];
+    sL[warp * 16 + g + 8] = l_row[1];
+  }
+  float *ow = sO + warp * 16 * SD_OPITCH;
+#pragma unroll
+  for (int nn = 0; nn < 16; ++nn) {
+    if (live_mask == 0u) break;  // no key: m = -inf, the merge skips this warp
+    *reinterpret_cast<float2 *>(ow + g * SD_OPITCH + nn * 8 + 2 * tq) = make_float2(o[nn][0], o[nn][1]);
+    *reinterpret_cast<float2 *>(ow + (g + 8) * SD_OPITCH + nn * 8 + 2 * tq) =
+        make_float2(o[nn][2], o[nn][3]);
+  }
+  __syncthreads();
+  // thread -> (row, 8 columns)
+  const int r = tid >> 4, c8 = (tid & 15) * 8;
+  if (r < n_rows) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < SD_WARPS; ++w) M = fmaxf(M, sM[w * 16 + r]);
+    float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < SD_WARPS; ++w) {
+        const float mw = sM[w * 16 + r];
+        if (mw == -INFINITY) continue;
+        const float f = fast_exp2(mw - M);
+        L += f * sL[w * 16 + r];
+        const float *src = sO + (w * 16 + r) * SD_OPITCH + c8;
+        const float4 x0 = *reinterpret_cast<const float4 *>(src);
+        const float4 x1 = *reinterpret_cast<const float4 *>(src + 4);
+        acc[0] += f * x0.x; acc[1] += f * x0.y; acc[2] += f * x0.z; acc[3] += f * x0.w;
+        acc[4] += f * x1.x; acc[5] += f * x1.y; acc[6] += f * x1.z; acc[7] += f * x1.w;
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int tok = q_begin + r / p.group;
+    const int head = h * p.group + r % p.group;
+    uint4 w4;
+    w4.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    w4.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    w4.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+    w4.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(tok) * p.o_st +
+                               static_cast<int64_t>(head) * p.o_sh + c8) = w4;
+    if (p.lse != nullptr && (tid & 15) == 0)
+      p.lse[static_cast<int64_t>(tok) * p.lse_st + static_cast<int64_t>(head) * p.lse_sh] =
+          L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+  }
 }
 
 // ------------------------------------------------------------------- host
@@ -2065,6 +2284,29 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
     decode_allheads_kernel<false, false, true><<<grid, block, L.end, stream>>>(p, maps);
   else
     decode_allheads_kernel<false, false, false><<<grid, block, L.end, stream>>>(p, maps);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+bool decode_short_eligible(const AttnParams &p) {
+  return p.topk == nullptr && !p.kv_fp8 && p.d == 128 && p.dv == 128 && p.max_seqlen_q >= 1 &&
+         p.max_seqlen_q * p.group <= 16 && p.page_size >= 1 &&
+         static_cast<int64_t>(p.pt_cols) * p.page_size <= kDecodeShortMaxKeys;
+}
+
+int launch_decode_short(const AttnParams &p, cudaStream_t stream) {
+  if (p.batch == 0) return PKV_OK;
+  if (!decode_short_eligible(p)) return PKV_ERR_UNSUPPORTED;
+  if (p.batch > 65535 || p.h_kv > 65535) return PKV_ERR_UNSUPPORTED;
+  static std::atomic<bool> configured[64] = {};  // per device; calls may race
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(decode_short_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SD_SMEM)) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    if (dev < 64) configured[dev].store(true, std::memory_order_release);
+  }
+  decode_short_kernel<<<dim3(p.h_kv, p.batch), SD_WARPS * 32, SD_SMEM, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

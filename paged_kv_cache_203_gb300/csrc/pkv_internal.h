@@ -111,6 +111,13 @@ constexpr int kDecodeFixedSplitHeads = 4;
 constexpr int kDecodeBalancedMaxBatch = 2048;
 bool decode_allheads_eligible(const AttnParams &p);
 int launch_decode_allheads(const AttnParams &p, cudaStream_t stream);
+// Short decode (head dim 128, <= 16 query rows per KV head, bf16 cache, a
+// page table of at most kDecodeShortMaxKeys keys, no split): one CTA per
+// (request, KV head) with every row loaded up front and the warps' states
+// merged in shared memory; no workspace.
+constexpr int kDecodeShortMaxKeys = 256;
+bool decode_short_eligible(const AttnParams &p);
+int launch_decode_short(const AttnParams &p, cudaStream_t stream);
 // tcgen05 varlen extend kernel (head dim 128, whole-page TMA boxes).
 bool extend_eligible(const AttnParams &p);
 int launch_extend_tc(const AttnParams &p, cudaStream_t stream);

@@ -177,6 +177,15 @@ __device__ __forceinline__ void bulk_wait_read() {
 }
 
 // ----------------------------------------------------------- async copies
+// One contiguous global -> shared copy on the bulk-copy engine, completion
+// counted in bytes on the barrier (16-byte aligned addresses and size).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                "r"(src_bytes)

@@ -405,6 +405,57 @@ def test_bad_page_ids_are_skipped_and_flagged():
         assert pkv.get_error_flags() & pkv.EFLAG_PAGE_OOB
 
 
+@pytest.mark.parametrize("page_size,h_q,h_kv,q_len,window", [
+    (1, 8, 2, 1, -1),    # the tiny decode shape
+    (3, 16, 4, 1, 50),   # odd page size, window
+    (16, 32, 8, 2, -1),  # two new tokens per request (causal)
+    (1, 64, 8, 1, -1),   # 8 rows per KV head
+    (8, 16, 1, 1, 100),  # one KV head, 16 rows
+    (2, 32, 8, 4, 7)])   # 4 new tokens x group 4 = 16 rows, window
+def test_short_decode(page_size, h_q, h_kv, q_len, window):
+    """Page tables of at most 256 keys, no split: the short-decode kernel (one
+    CTA per request and KV head, all rows loaded up front, the warps' states
+    merged in shared memory).  NaN in every slot outside the valid rows, an
+    empty request, an out-of-pool page id (skipped and flagged, as the oracle
+    skips it), lengths up to the table's last key; no workspace; against the
+    oracle and against the all-heads kernel with two splits."""
+    batch = 9
+    len_hi = 256 - 256 % page_size
+    wl = workloads.make("tiny_decode", d=128, page_size=page_size, h_q=h_q, h_kv=h_kv,
+                        q_len=q_len, causal=q_len > 1, window_left=window, len_lo=q_len,
+                        len_hi=len_hi, batch=batch,
+                        pool_tokens=batch * (len_hi + page_size) + 64, seed=17 + page_size)
+    assert wl.page_table.shape[1] * page_size <= 256
+    wl.cache_seqlens[2] = 0
+    wl.cache_seqlens[5] = wl.page_table.shape[1] * page_size  # the table's last key
+    wl.cache_seqlens[5] = max(int(wl.cache_seqlens[5]), q_len)
+    valid = torch.zeros(wl.k_cache.shape[0] * page_size, dtype=torch.bool)
+    for b in range(batch):
+        n = int(wl.cache_seqlens[b])
+        j = torch.arange(n)
+        slots = wl.page_table[b, j // page_size].long() * page_size + j % page_size
+        valid[slots] = True
+    valid = valid.view(-1, page_size)
+    wl.k_cache[~valid] = float("nan")
+    wl.v_cache[~valid] = float("nan")
+    # out of the pool: the page of request 7's last key (inside any window)
+    wl.page_table[7, (int(wl.cache_seqlens[7]) - 1) // page_size] = 10_000_000
+    g = wl.to(DEV)
+    assert pkv.attn_workspace_size(g.q, g.k_cache, g.v_cache, g.page_table, g.cache_seqlens,
+                                   g.max_seqlen_q, num_splits=1) == 0
+    ref_o, ref_l, skipped = oracle_attn(wl)
+    assert skipped > 0
+    for splits in (1, 0):
+        pkv.clear_error_flags()
+        out, lse = gpu_attn(g, num_splits=splits)
+        check_close(out, lse, ref_o, ref_l, f"short decode splits={splits}")
+        assert pkv.get_error_flags() == pkv.EFLAG_PAGE_OOB
+        assert torch.all(out[2 * q_len:3 * q_len] == 0)
+        assert torch.all(torch.isneginf(lse[2 * q_len:3 * q_len]))
+    out2, lse2 = gpu_attn(g, num_splits=2)  # the all-heads kernel
+    assert (out.float() - out2.float()).abs().max().item() <= MAX_ABS
+
+
 # ------------------------------------- full-size workloads, every output row
 
 @pytest.mark.parametrize("num_splits", [4, 0])
@@ -561,9 +612,9 @@ def test_small_page_batch_beyond_the_balanced_limit():
     """More requests than the balanced schedule handles (2048): the library's
     split choice falls back to fixed splits of the all-heads kernel; every
     row against the oracle."""
-    batch = 2100
+    batch = 2100  # tables of 300 keys: wider than the short-decode kernel serves
     wl = workloads.make("tiny_decode", d=128, page_size=1, h_q=16, h_kv=8, batch=batch,
-                        len_lo=1, len_hi=80, pool_tokens=batch * 80 + 64, seed=91)
+                        len_lo=1, len_hi=300, pool_tokens=batch * 300 + 64, seed=91)
     g = wl.to(DEV)
     out, lse = gpu_attn(g, num_splits=0)
     ref_o, ref_l, _ = oracle_attn(wl)
