@@ -491,6 +491,33 @@ def fp8_line(dev, peaks):
             "tokens_per_s": g.q.shape[0] / (a_ms / 1e3)}
 
 
+def fp8_extend_line(dev, peaks):
+    """The varlen extend workload over an fp8 cache (the bf16 cache cast to
+    e4m3 codes, descales 0.75 / 1.25): e4m3 QK^T and f16 PV on the tensor
+    cores, flops over the visible (q, k) pairs as for the bf16 cache."""
+    g = workloads.make("varlen_extend", value_device=dev)
+    st = Step.__new__(Step)
+    st.g = g
+    flops = Step._flops(st)
+    k8 = g.k_cache.to(torch.float8_e4m3fn)
+    v8 = g.v_cache.to(torch.float8_e4m3fn)
+    del g.k_cache, g.v_cache
+    B, h_kv = g.cache_seqlens.shape[0], k8.shape[2]
+    kd = torch.full((B, h_kv), 0.75, device=dev)
+    vd = torch.full((B, h_kv), 1.25, device=dev)
+    out = torch.empty(g.q.shape[0], g.q.shape[1], 128, dtype=torch.bfloat16, device=dev)
+
+    def attend():
+        pkv.attn_with_kvcache_fp8(g.q, k8, v8, g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+                                  g.max_seqlen_q, g.scale, causal=True, k_descale=kd,
+                                  v_descale=vd, out=out)
+
+    a_ms, a_how = _timed(attend)
+    tf = flops / 1e12 / (a_ms / 1e3)
+    return {"kernel": "extend_tc_kernel (fp8 cache)", "attn_ms": a_ms, "timing": a_how,
+            "TFLOPs": tf, "tflop_frac_bf16": tf / peaks["bf16_tflops"]}
+
+
 def append_decode_line(dev, peaks):
     """The KV write before decode attention on the GQA decode batch (each
     request's last key is its new token), with the bench's 4 key chunks:
@@ -582,6 +609,7 @@ def merge_line(dev, peaks, sizes=(("decode_batch", 64), ("prefill", 32768))):
 EXTRA_LINES = {"local": local_attention_line, "cascade": cascade_line, "append": append_line,
                "fp8": fp8_line, "topk": topk_line, "merge": merge_line,
                "merge_prefill": lambda dev, peaks: merge_line(dev, peaks, (("prefill", 32768),)),
+               "fp8_extend": fp8_extend_line,
                "append_decode": append_decode_line}
 
 
@@ -973,7 +1001,8 @@ def main():
                           (HEADLINE + "@cascade_shared_prefix_4096", cascade_line),
                           ("varlen_extend@append_then_attend", append_line),
                           (HEADLINE + "@fused_append", append_decode_line),
-                          (HEADLINE + "@fp8_kv", fp8_line)):
+                          (HEADLINE + "@fp8_kv", fp8_line),
+                          ("varlen_extend@fp8_kv", fp8_extend_line)):
             try:
                 others[label] = fn(dev, peaks)
             except pkv.PkvError as e:

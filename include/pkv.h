@@ -157,9 +157,15 @@ int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
  *                    contiguous), or NULL for 1.
  * Other arguments, outputs and workspace as pkv_attn_with_kvcache
  * (pkv_attn_workspace_size takes the fp8 tensors as they are).
- * Supported: head dim 128, H_kv <= 8, at most 16 query rows per KV head
- * (max_seqlen_q * H_q / H_kv), page size a multiple of 16, num_splits = 0,
- * no top-k lists, B <= 2048; otherwise PKV_ERR_UNSUPPORTED.
+ * Supported, head dim 128 and no top-k lists in both cases:
+ *  - extend (max_seqlen_q >= 64): page size a multiple of 8 that divides 128
+ *    or is a multiple of 128, strides that nest (head inside position inside
+ *    page), any num_splits (no split is made, no workspace), any sign of
+ *    scale * k_descale;
+ *  - decode: H_kv <= 8, at most 16 query rows per KV head
+ *    (max_seqlen_q * H_q / H_kv), page size a multiple of 16, num_splits = 0,
+ *    B <= 2048;
+ * otherwise PKV_ERR_UNSUPPORTED.
  */
 int pkv_attn_with_kvcache_fp8(pkv_tensor q, pkv_tensor k_cache,
                               pkv_tensor v_cache, pkv_tensor page_table,

@@ -15,7 +15,7 @@
 namespace pkv {
 
 bool encode_tensor_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
-                       const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+                       const cuuint64_t *strides_bytes, const cuuint32_t *box, bool bytes) {
   using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                      const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                      const cuuint32_t *, CUtensorMapInterleave,
@@ -33,7 +33,8 @@ bool encode_tensor_map(CUtensorMap *map, const void *base, int rank, const cuuin
   }();
   if (fn == nullptr) return false;
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims,
+  return fn(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+            const_cast<void *>(base), dims,
             strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
@@ -131,11 +132,36 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
   const int group = static_cast<int>(h_q / h_kv);
   const bool mla = d == 576 && dv == 512;
   if (fp8) {
-    // fp8 caches: the all-heads decode kernel with page boxes and its
-    // balanced schedule (head dim 128, <= 8 KV heads, <= 16 query rows per KV
-    // head, page size a multiple of 16), the library's split choice
-    if (present(topk) || d != 128 || dv != 128 || num_splits != 0 || batch > kDecodeBalancedMaxBatch)
-      return PKV_ERR_UNSUPPORTED;
+    // fp8 caches: runs of >= kExtendMinSeqlenQ new tokens on the tcgen05
+    // extend kernel (e4m3 QK^T, f16 PV; no split, no workspace); decode on
+    // the all-heads kernel with page boxes and its balanced schedule (head
+    // dim 128, <= 8 KV heads, <= 16 query rows per KV head, page size a
+    // multiple of 16), the library's split choice
+    if (present(topk) || d != 128 || dv != 128) return PKV_ERR_UNSUPPORTED;
+    AttnParams lx{};
+    lx.d = 128;
+    lx.dv = 128;
+    lx.h_q = static_cast<int>(h_q);
+    lx.h_kv = static_cast<int>(h_kv);
+    lx.page_size = static_cast<int>(page);
+    lx.num_pages = num_pages;
+    lx.q_st = q.stride[0];
+    lx.q_sh = q.stride[1];
+    lx.k_sp = k.stride[0];
+    lx.k_spos = k.stride[1];
+    lx.k_sh = k.stride[2];
+    lx.v_sp = v.stride[0];
+    lx.v_spos = v.stride[1];
+    lx.v_sh = v.stride[2];
+    lx.kv_fp8 = 1;
+    if (max_seqlen_q >= kExtendMinSeqlenQ && extend_eligible(lx)) {
+      plan->kind = 1;
+      plan->num_splits = 1;
+      plan->n_row_tiles = 0;
+      plan->ws_o_bytes = plan->ws_lse_bytes = plan->ws_ctr_bytes = 0;
+      return PKV_OK;
+    }
+    if (num_splits != 0 || batch > kDecodeBalancedMaxBatch) return PKV_ERR_UNSUPPORTED;
     AttnParams lp{};
     lp.d = 128;
     lp.dv = 128;
@@ -439,8 +465,10 @@ int attn_impl(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache, pkv_tensor p
   if (plan.kind == 2) return launch_mla_topk(p, stream);
   if (plan.kind == 3) return launch_decode_allheads(p, stream);
   if (plan.kind == 4) return launch_decode_short(p, stream);
+  if (plan.kind == 1 && fp8) return launch_extend_tc(p, stream);  // any scale sign
   if (plan.kind == 1) {
-    // the extend kernel takes row maxima of raw scores: positive scale only
+    // the bf16 extend kernel takes row maxima of raw scores: positive scale
+    // only (the decode kernel serves the others)
     rc = scale > 0.f ? launch_extend_tc(p, stream) : PKV_ERR_UNSUPPORTED;
     if (rc != PKV_ERR_UNSUPPORTED) return rc;
     p.num_splits = 1;  // otherwise the unsplit decode kernel (no workspace)

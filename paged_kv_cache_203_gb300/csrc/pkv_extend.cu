@@ -57,31 +57,43 @@ constexpr int HALF = BN / 2;      // S / P / O columns per softmax thread
 constexpr uint32_t kTileBytes = BM * D * 2;  // 32 KB, any 128x128 bf16 tile
 constexpr int NKV = 3;            // K and V ring stages
 
+// Shared-memory plan; FP8 (a cache of e4m3 codes) adds the e4m3 Q tile, keeps
+// K and V as codes (16 KB stages) and two f16 V tiles widened from them.
+template <bool FP8>
 struct Smem {
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kTileBytes;       // NKV stages
-  static constexpr uint32_t kV = kK + NKV * kTileBytes;   // NKV stages
-  static constexpr uint32_t kMask = kV + NKV * kTileBytes;  // uint32 [4 tiles][4 words]
+  static constexpr uint32_t kKStage = FP8 ? BN * 128u : kTileBytes;  // one K / V stage
+  static constexpr uint32_t kQ = 0;                                   // Q, bf16 (TMA)
+  static constexpr uint32_t kQ8 = kQ + kTileBytes;                    // Q rounded to e4m3
+  static constexpr uint32_t kK = kQ8 + (FP8 ? BM * 128u : 0u);        // NKV stages
+  static constexpr uint32_t kV = kK + NKV * kKStage;                  // NKV stages
+  static constexpr uint32_t kV16 = kV + NKV * kKStage;                // [2] f16 V (FP8)
+  static constexpr uint32_t kMask = kV16 + (FP8 ? 2 * kTileBytes : 0u);  // uint32 [4][4]
   static constexpr uint32_t kXchg = kMask + 64;  // float [m, l][2 halves][128 rows]
   static constexpr uint32_t kBar = kXchg + 2 * 2 * BM * 4;
   // barriers: q_full, k_full[NKV], v_full[NKV], k_empty[NKV], v_empty[NKV],
-  //           s_full[2], s_free[2], p_full[2], o_done[2], xchg[2], mask_full[4]
-  static constexpr int kNumBars = 1 + 4 * NKV + 10 + 4;
+  //           s_full[2], s_free[2], p_full[2], o_done[2], xchg[2], mask_full[4],
+  //           q8_ready
+  static constexpr int kNumBars = 1 + 4 * NKV + 10 + 4 + 1;
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kEnd = kTmemSlot + 16;
   // The dynamic shared memory base must be 1024-byte aligned (128-byte
   // swizzle atoms); the kernel checks it and does no work otherwise.
   static constexpr size_t kDynamic = kEnd;
 };
-static_assert(Smem::kDynamic <= 232448, "shared memory plan exceeds 227 KB");
+static_assert(Smem<false>::kDynamic <= 232448 && Smem<true>::kDynamic <= 232448,
+              "shared memory plan exceeds 227 KB");
+static_assert(Smem<true>::kK % 1024 == 0 && Smem<true>::kV % 1024 == 0 &&
+                  Smem<true>::kV16 % 1024 == 0,
+              "swizzled tiles start on 1024-byte boundaries");
 
 enum BarId {
   Q_FULL = 0, K_FULL = 1, V_FULL = K_FULL + NKV, K_EMPTY = V_FULL + NKV,
   V_EMPTY = K_EMPTY + NKV, S_FULL = V_EMPTY + NKV, S_FREE = S_FULL + 2,
   P_FULL = S_FREE + 2, O_DONE = P_FULL + 2, XCHG = O_DONE + 2,
-  MASK_FULL = XCHG + 2  // [4]: the key mask of tile j is in slot j & 3
+  MASK_FULL = XCHG + 2,  // [4]: the key mask of tile j is in slot j & 3
+  Q8_READY = MASK_FULL + 4  // FP8: the e4m3 Q tile is written
 };
-static_assert(MASK_FULL + 4 == Smem::kNumBars, "barrier plan and count agree");
+static_assert(Q8_READY + 1 == Smem<false>::kNumBars, "barrier plan and count agree");
 
 // Byte offset of 16-byte chunk c of row r of a 128-row tile stored as
 // [2 halves][128 rows][128 B] with the 128-byte swizzle.
@@ -97,14 +109,16 @@ struct ExtendMaps {
 
 // ---------------------------------------------------------------- kernel
 
+template <bool FP8>
 __global__ void __launch_bounds__(NTHREADS, 1)
 extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ ExtendMaps maps) {
+  using SM = Smem<FP8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw;
   const uint32_t sbase = smem_addr(smem);
-  uint32_t *sMask = reinterpret_cast<uint32_t *>(smem + Smem::kMask);
-  uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + Smem::kTmemSlot);
-  auto bar = [&](int id) { return sbase + Smem::kBar + 8u * id; };
+  uint32_t *sMask = reinterpret_cast<uint32_t *>(smem + SM::kMask);
+  uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + SM::kTmemSlot);
+  auto bar = [&](int id) { return sbase + SM::kBar + 8u * id; };
 
   const int n_qt = gridDim.x;
   const int qt = n_qt - 1 - blockIdx.x;  // longest tiles first
@@ -153,6 +167,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       mbar_init(bar(XCHG + s), NSM_WARPS);
     }
     for (int s = 0; s < 4; ++s) mbar_init(bar(MASK_FULL + s), 1);
+    mbar_init(bar(Q8_READY), NSM_WARPS);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     fence_proxy_async();
   }
@@ -175,8 +190,8 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
     const int nbox = BN / pbox;
     if (lane == 0 && n_kv > 0) {  // (no keys: nothing may stay in flight)
       mbar_arrive_expect_tx(bar(Q_FULL), kTileBytes);
-      tma_load_3d(sbase + Smem::kQ, &maps.q, 0, h, q_begin + u0, bar(Q_FULL));
-      tma_load_3d(sbase + Smem::kQ + BM * 128, &maps.q, 64, h, q_begin + u0, bar(Q_FULL));
+      tma_load_3d(sbase + SM::kQ, &maps.q, 0, h, q_begin + u0, bar(Q_FULL));
+      tma_load_3d(sbase + SM::kQ + BM * 128, &maps.q, 64, h, q_begin + u0, bar(Q_FULL));
     }
     for (int jj = 0; jj < n_kv; ++jj) {
       const int s = jj % NKV;
@@ -205,7 +220,9 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
           atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
         }
       }
-      uint32_t bytes = box_ok ? static_cast<uint32_t>(pbox) * 256u : 0u;
+      // bytes of the tile: a box row is 256 B of bf16 (two 64-column boxes)
+      // or 128 B of codes (one box of all 128 columns)
+      uint32_t bytes = box_ok ? static_cast<uint32_t>(pbox) * (FP8 ? 128u : 256u) : 0u;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
       const uint32_t roff = static_cast<uint32_t>(lane * pbox) * 128u;
@@ -225,9 +242,9 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL + s), bytes);
       __syncwarp();
       if (box_ok) {
-        const uint32_t kdst = sbase + Smem::kK + s * kTileBytes + roff;
+        const uint32_t kdst = sbase + SM::kK + s * SM::kKStage + roff;
         tma_load_4d(kdst, &maps.k, 0, kvh, inpage, page, bar(K_FULL + s));
-        tma_load_4d(kdst + BN * 128, &maps.k, 64, kvh, inpage, page, bar(K_FULL + s));
+        if (!FP8) tma_load_4d(kdst + BN * 128, &maps.k, 64, kvh, inpage, page, bar(K_FULL + s));
       }
       // ---- V tile (stage freed when the PV of tile jj-NKV completed) ----
       if (jj >= NKV && !mbar_wait_sleep(bar(V_EMPTY + s), prev)) {
@@ -238,18 +255,20 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       if (lane == 0) mbar_arrive_expect_tx(bar(V_FULL + s), bytes);
       __syncwarp();
       if (box_ok) {
-        const uint32_t vdst = sbase + Smem::kV + s * kTileBytes + roff;
+        const uint32_t vdst = sbase + SM::kV + s * SM::kKStage + roff;
         tma_load_4d(vdst, &maps.v, 0, kvh, inpage, page, bar(V_FULL + s));
-        tma_load_4d(vdst + BN * 128, &maps.v, 64, kvh, inpage, page, bar(V_FULL + s));
+        if (!FP8) tma_load_4d(vdst + BN * 128, &maps.v, 64, kvh, inpage, page, bar(V_FULL + s));
       }
     }
   } else if (warp == kMmaWarp) {
     // ================================== MMA ==================================
     if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16(BM, BN, false);
-      constexpr uint32_t kIdescPV = idesc_bf16(BM, BN, true);
-      bool ok = n_kv == 0 || mbar_wait_sleep(bar(Q_FULL), 0);
-      const uint64_t qd0 = smem_desc(sbase + Smem::kQ, 0, 1024, 2);
+      // bf16: QK^T and PV kind::f16 on bf16; FP8: QK^T kind::f8f6f4 on e4m3
+      // (K 32 a step), PV kind::f16 on f16 (P in f16, V widened to f16)
+      constexpr uint32_t kIdescQK = FP8 ? idesc_e4m3(BM, BN) : idesc_bf16(BM, BN, false);
+      constexpr uint32_t kIdescPV = FP8 ? idesc_f16(BM, BN, true) : idesc_bf16(BM, BN, true);
+      bool ok = n_kv == 0 || mbar_wait_sleep(bar(FP8 ? Q8_READY : Q_FULL), 0);
+      const uint64_t qd0 = smem_desc(sbase + (FP8 ? SM::kQ8 : SM::kQ), 0, 1024, 2);
       for (int j = 0; ok && j <= n_kv; ++j) {
         if (j < n_kv) {  // S_j = Q K_j^T
           const int s = j & 1, sk = j % NKV;
@@ -260,11 +279,18 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
           // descriptors formed once per tile; a K step adds a constant to the
           // start-address field (16-byte units), so the single issuing
           // thread does no 64-bit descriptor arithmetic per MMA
-          const uint64_t kd0 = smem_desc(sbase + Smem::kK + sk * kTileBytes, 0, 1024, 2);
+          const uint64_t kd0 = smem_desc(sbase + SM::kK + sk * SM::kKStage, 0, 1024, 2);
+          if (FP8) {
+            // one 128-byte row holds all 128 dims: four K = 32 steps of 32 B
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t koff = ((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4;
-            umma(tS0 + s * 128, qd0 + koff, kd0 + koff, kIdescQK, ks > 0);
+            for (int ks = 0; ks < 4; ++ks)
+              umma_f8(tS0 + s * 128, qd0 + ks * 2, kd0 + ks * 2, kIdescQK, ks > 0);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint64_t koff = ((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4;
+              umma(tS0 + s * 128, qd0 + koff, kd0 + koff, kIdescQK, ks > 0);
+            }
           }
           umma_commit(bar(S_FULL + s));
           umma_commit(bar(K_EMPTY + sk));
@@ -272,11 +298,14 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
         if (j >= 1) {  // O += P_{j-1} V_{j-1}
           const int jj = j - 1;
           const int s = jj & 1, sv = jj % NKV;
+          // FP8: P_FULL also says the softmax warps widened V_jj to f16
           ok = mbar_wait_sleep(bar(P_FULL + s), (jj >> 1) & 1) &&
-               mbar_wait_sleep(bar(V_FULL + sv), (jj / NKV) & 1);
+               (FP8 || mbar_wait_sleep(bar(V_FULL + sv), (jj / NKV) & 1));
           if (!ok) break;
           tc_fence_after();
-          const uint64_t vd0 = smem_desc(sbase + Smem::kV + sv * kTileBytes, BN * 128, 1024, 2);
+          const uint64_t vd0 =
+              smem_desc(sbase + (FP8 ? SM::kV16 + (jj & 1) * kTileBytes : SM::kV + sv * kTileBytes),
+                        BN * 128, 1024, 2);
           // keys 0-63 of the tile accumulate into O_A, keys 64-127 into O_B
           // (each half of the softmax keeps its own reference max); P_j is
           // read from TMEM: keys 64h + 16k.. at column 128 s + 64 h + 8 k
@@ -302,11 +331,53 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
     const int lo_r = p.window_left >= 0 ? i_r - p.window_left : INT_MIN;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t col0 = hf * HALF;
-    const float c = p.scale_log2;  // > 0 on this path
-    float *xchg = reinterpret_cast<float *>(smem + Smem::kXchg);  // [m, l][2 halves][128]
+    // the softmax scale (log2 domain), times k_descale of the (request, KV
+    // head) for an fp8 cache; the row maxima below are of raw scores, so a
+    // negative product flips the scores' sign instead
+    float c = p.scale_log2;
+    float vdesc = 1.f;
+    if (FP8) {
+      const int64_t di = static_cast<int64_t>(b) * p.h_kv + kvh;
+      if (p.k_descale != nullptr) c *= p.k_descale[di];
+      if (p.v_descale != nullptr) vdesc = p.v_descale[di];
+    }
+    const bool flip = c < 0.f;
+    c = fabsf(c);
+    float *xchg = reinterpret_cast<float *>(smem + SM::kXchg);  // [m, l][2 halves][128]
     float m_ref = -INFINITY;  // reference max (log2 domain) of O and l
     float l = 0.f;            // this half's share of the row sum
     bool ok = true;
+
+    if (FP8 && n_kv > 0) {
+      // Q rounded to e4m3 (the cache's type) once: bf16 tile [2 halves][128
+      // rows][128 B] -> e4m3 tile [128 rows][128 B], both 128-byte swizzled;
+      // 16-byte chunk c8 of a row holds dims 16 c8 .. 16 c8 + 15
+      ok = mbar_wait_sleep(bar(Q_FULL), 0);
+      if (ok) {
+        const int t = warp * 32 + lane;  // 0..255
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int pr = t + 256 * k;
+          const int r = pr >> 3, c8 = pr & 7;
+          const uint4 a = *reinterpret_cast<const uint4 *>(smem + SM::kQ + tile_off(r, 2 * c8));
+          const uint4 bq = *reinterpret_cast<const uint4 *>(smem + SM::kQ + tile_off(r, 2 * c8 + 1));
+          const uint32_t w[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+          uint32_t o4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = w[2 * i], hi = w[2 * i + 1];  // dims 4i .. 4i + 3
+            o4[i] = round_e4m3x2(__uint_as_float(lo << 16), __uint_as_float(lo & 0xffff0000u)) |
+                    (round_e4m3x2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u))
+                     << 16);
+          }
+          *reinterpret_cast<uint4 *>(smem + SM::kQ8 + r * 128 + ((c8 ^ (r & 7)) << 4)) =
+              make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        }
+        fence_proxy_async();  // generic writes -> the tensor core's reads
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Q8_READY));
+    }
 
     for (int jj = 0; jj < n_kv; ++jj) {
       const int s = jj & 1;
@@ -315,6 +386,10 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       tc_fence_after();
       float x[HALF];
       tmem_ld64(tS0 + s * 128 + col0 + lane_off, x);
+      if (FP8 && flip) {
+#pragma unroll
+        for (int i = 0; i < HALF; ++i) x[i] = -x[i];
+      }
 
       // the tile's key mask (its slot is rewritten only for tile jj + 4,
       // after this softmax is done, so the phase cannot run ahead)
@@ -397,7 +472,8 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       {
         uint32_t pw[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pw[i] = pack_bf16(x[2 * i], x[2 * i + 1]);
+        for (int i = 0; i < 32; ++i)
+          pw[i] = FP8 ? pack_f16(x[2 * i], x[2 * i + 1]) : pack_bf16(x[2 * i], x[2 * i + 1]);
         tmem_st32u(tS0 + s * 128 + col0 + lane_off, pw);
       }
       // V rows of keys outside the sequence or in skipped pages must be zero
@@ -405,14 +481,40 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
       // `row` of the tile, this thread's half of its columns
       const uint32_t own = quad == 0 ? sMask[ms] : quad == 1 ? sMask[ms + 1]
                          : quad == 2 ? sMask[ms + 2] : sMask[ms + 3];
-      if (!all_valid && !(ok = mbar_wait_sleep(bar(V_FULL + skv), pkv))) break;  // rows to zero
-      if (!all_valid && !((own >> lane) & 1u)) {
-        uint8_t *vt = smem + Smem::kV + skv * kTileBytes;
+      if (FP8) {
+        // key row `row` of V_jj, this thread's 64 columns: codes widened to
+        // f16 into the tile the PV reads (zeros for keys outside the
+        // sequence or in skipped pages).  The f16 tile jj & 1 was last read
+        // by the PV of tile jj - 2, done before S_jj (its QK^T waited for
+        // that buffer).
+        if (!(ok = mbar_wait_sleep(bar(V_FULL + skv), pkv))) break;
+        uint8_t *vt = smem + SM::kV16 + (jj & 1) * kTileBytes;
+        const uint8_t *vc = smem + SM::kV + skv * SM::kKStage + row * 128;
+        const bool live = (own >> lane) & 1u;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          *reinterpret_cast<uint4 *>(vt + tile_off(row, hf * 8 + cc)) = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 4; ++i) {  // 16 codes -> two 16-byte f16 chunks
+          uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+          if (live) {
+            const uint4 cw = *reinterpret_cast<const uint4 *>(vc + (((hf * 4 + i) ^ (row & 7)) << 4));
+            o0 = make_uint4(e4m3x2_to_f16x2(cw.x), e4m3x2_to_f16x2(cw.x >> 16),
+                            e4m3x2_to_f16x2(cw.y), e4m3x2_to_f16x2(cw.y >> 16));
+            o1 = make_uint4(e4m3x2_to_f16x2(cw.z), e4m3x2_to_f16x2(cw.z >> 16),
+                            e4m3x2_to_f16x2(cw.w), e4m3x2_to_f16x2(cw.w >> 16));
+          }
+          *reinterpret_cast<uint4 *>(vt + tile_off(row, hf * 8 + 2 * i)) = o0;
+          *reinterpret_cast<uint4 *>(vt + tile_off(row, hf * 8 + 2 * i + 1)) = o1;
+        }
+        fence_proxy_async();  // the f16 rows visible to the tensor core
+      } else {
+        if (!all_valid && !(ok = mbar_wait_sleep(bar(V_FULL + skv), pkv))) break;  // rows to zero
+        if (!all_valid && !((own >> lane) & 1u)) {
+          uint8_t *vt = smem + SM::kV + skv * kTileBytes;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc)
+            *reinterpret_cast<uint4 *>(vt + tile_off(row, hf * 8 + cc)) = make_uint4(0, 0, 0, 0);
+        }
+        if (!all_valid) fence_proxy_async();  // zeroed V rows visible to the tensor core
       }
-      if (!all_valid) fence_proxy_async();  // zeroed V rows visible to the tensor core
       tmem_st_wait();     // P in TMEM
       tc_fence_before();  // (and the rescaled O columns)
       __syncwarp();
@@ -458,7 +560,7 @@ extend_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ E
     for (int i = 0; i < HALF; ++i) o[i] = oa[i] * f_a + ob[i] * f_b;
     m_ref = m_tot;
     if (row < n_rows) {
-      const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+      const float inv = l_tot > 0.f ? vdesc / l_tot : 0.f;  // v_descale: fp8 cache
       const int tok = q_begin + u;
       bf16 *dst = p.out + static_cast<int64_t>(tok) * p.o_st + static_cast<int64_t>(h) * p.o_sh +
                   col0;
@@ -517,29 +619,38 @@ int launch_extend_tc(const AttnParams &p, cudaStream_t stream) {
     cuuint32_t box[3] = {64, 1, BM};
     if (!encode_tensor_map(&maps.q, p.q, 3, dims, str, box)) return PKV_ERR_UNSUPPORTED;
   }
+  const bool fp8 = p.kv_fp8 != 0;
   {
+    // bf16: boxes of 64 columns (128 B) per half; fp8 codes: one box of all
+    // 128 columns (128 B); strides in bytes
+    const cuuint64_t eb = fp8 ? 1 : 2;
     cuuint64_t dims[4] = {D, static_cast<cuuint64_t>(p.h_kv), static_cast<cuuint64_t>(p.page_size),
                           static_cast<cuuint64_t>(p.num_pages)};
-    cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(pbox), 1};
-    cuuint64_t sk[3] = {static_cast<cuuint64_t>(p.k_sh) * 2, static_cast<cuuint64_t>(p.k_spos) * 2,
-                        static_cast<cuuint64_t>(p.k_sp) * 2};
-    cuuint64_t sv[3] = {static_cast<cuuint64_t>(p.v_sh) * 2, static_cast<cuuint64_t>(p.v_spos) * 2,
-                        static_cast<cuuint64_t>(p.v_sp) * 2};
-    if (!encode_tensor_map(&maps.k, p.k, 4, dims, sk, box) ||
-        !encode_tensor_map(&maps.v, p.v, 4, dims, sv, box))
+    cuuint32_t box[4] = {fp8 ? 128u : 64u, 1, static_cast<cuuint32_t>(pbox), 1};
+    cuuint64_t sk[3] = {static_cast<cuuint64_t>(p.k_sh) * eb, static_cast<cuuint64_t>(p.k_spos) * eb,
+                        static_cast<cuuint64_t>(p.k_sp) * eb};
+    cuuint64_t sv[3] = {static_cast<cuuint64_t>(p.v_sh) * eb, static_cast<cuuint64_t>(p.v_spos) * eb,
+                        static_cast<cuuint64_t>(p.v_sp) * eb};
+    if (!encode_tensor_map(&maps.k, p.k, 4, dims, sk, box, fp8) ||
+        !encode_tensor_map(&maps.v, p.v, 4, dims, sv, box, fp8))
       return PKV_ERR_UNSUPPORTED;
   }
   static std::atomic<bool> configured[64] = {};  // per device; calls may race
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(extend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Smem::kDynamic)) != cudaSuccess)
+    if (cudaFuncSetAttribute(extend_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Smem<false>::kDynamic)) != cudaSuccess ||
+        cudaFuncSetAttribute(extend_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Smem<true>::kDynamic)) != cudaSuccess)
       return PKV_ERR_CUDA;
     if (dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   dim3 grid(n_qt, p.h_q, p.batch);
-  extend_tc_kernel<<<grid, NTHREADS, Smem::kDynamic, stream>>>(p, maps);
+  if (fp8)
+    extend_tc_kernel<true><<<grid, NTHREADS, Smem<true>::kDynamic, stream>>>(p, maps);
+  else
+    extend_tc_kernel<false><<<grid, NTHREADS, Smem<false>::kDynamic, stream>>>(p, maps);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

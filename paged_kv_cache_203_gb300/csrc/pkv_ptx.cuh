@@ -279,6 +279,26 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major)
   return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
+// Instruction descriptor, kind::f16: f16 x f16 -> f32 (format fields 0).
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool b_mn_major) {
+  return (1u << 4) | (b_mn_major ? (1u << 16) : 0u) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+// Instruction descriptor, kind::f8f6f4: e4m3 x e4m3 -> f32 (format fields 0),
+// both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+// D (+)= A B, kind::f8f6f4 (8-bit operands, K = 32 per instruction), both
+// operands in shared memory.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                      uint32_t accumulate) {
   asm volatile(
@@ -438,6 +458,19 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+// Two e4m3 codes (low byte first) to f16x2, exactly (e4m3 values are f16 values).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  const uint16_t v = static_cast<uint16_t>(two_codes & 0xffffu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(v));
+  return r;
+}
+// (lo, hi) rounded to f16 (nearest), lo in the low half.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
@@ -446,8 +479,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }  // namespace ptx
 
 // Host side: cuTensorMapEncodeTiled through the runtime's driver entry
-// point (no link-time dependency on libcuda).
+// point (no link-time dependency on libcuda); bf16 elements, or bytes (fp8
+// codes) when `bytes`; 128-byte swizzle.
 bool encode_tensor_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
-                       const cuuint64_t *strides_bytes, const cuuint32_t *box);
+                       const cuuint64_t *strides_bytes, const cuuint32_t *box,
+                       bool bytes = false);
 
 }  // namespace pkv

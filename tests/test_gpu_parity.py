@@ -1221,9 +1221,10 @@ def _to_fp8(t):
     return t.float().to(torch.float8_e4m3fn)
 
 
-def _fp8_run(wl, descale=True, seed=0, entry="fp8"):
+def _fp8_run(wl, descale=True, seed=0, entry="fp8", scale=None):
     """GPU fp8 attention and the oracle's, on the workload's cache cast to
     e4m3 codes; per-(request, KV head) descales drawn in [0.5, 2)."""
+    scale = wl.scale if scale is None else scale
     B, h_kv = wl.cache_seqlens.shape[0], wl.k_cache.shape[2]
     k8, v8 = _to_fp8(wl.k_cache), _to_fp8(wl.v_cache)
     gen = torch.Generator().manual_seed(seed)
@@ -1233,18 +1234,20 @@ def _fp8_run(wl, descale=True, seed=0, entry="fp8"):
     if entry == "fp8":
         out, lse = pkv.attn_with_kvcache_fp8(
             g.q, k8.to(DEV), v8.to(DEV), g.page_table, g.cache_seqlens, g.cu_seqlens_q,
-            g.max_seqlen_q, g.scale, causal=g.causal,
+            g.max_seqlen_q, scale, causal=g.causal, window_left=g.window_left,
             k_descale=None if kd is None else kd.to(DEV),
             v_descale=None if vd is None else vd.to(DEV), return_softmax_lse=True)
     else:  # the bf16 entry point with an fp8 cache: descales of 1
         out, lse = pkv.attn_with_kvcache(
             g.q, k8.to(DEV), v8.to(DEV), g.page_table, g.cache_seqlens, g.cu_seqlens_q,
-            g.max_seqlen_q, g.scale, causal=g.causal, return_softmax_lse=True)
+            g.max_seqlen_q, scale, causal=g.causal, window_left=g.window_left,
+            return_softmax_lse=True)
     torch.cuda.synchronize()
     ref_o, ref_l, _ = oracle.attention_fp8(
         oracle.bf16_bits(wl.q), k8.view(torch.uint8).numpy(), v8.view(torch.uint8).numpy(),
-        wl.page_table.numpy(), wl.cache_seqlens.numpy(), wl.cu_seqlens_q.numpy(), wl.scale,
-        causal=wl.causal, k_descale=None if kd is None else kd.numpy(),
+        wl.page_table.numpy(), wl.cache_seqlens.numpy(), wl.cu_seqlens_q.numpy(), scale,
+        causal=wl.causal, window_left=wl.window_left,
+        k_descale=None if kd is None else kd.numpy(),
         v_descale=None if vd is None else vd.numpy())
     return out, lse, ref_o, ref_l
 
@@ -1261,6 +1264,45 @@ def test_fp8_decode(page_size, h_q, q_len):
     out, lse, ref_o, ref_l = _fp8_run(wl, seed=page_size)
     check_close(out, lse, ref_o, ref_l, f"fp8 P={page_size} h_q={h_q} q_len={q_len}")
     assert pkv.get_error_flags() == 0
+
+
+@pytest.mark.parametrize("page_size,window,causal,entry", [
+    (64, -1, True, "fp8"), (16, -1, True, "fp8"), (128, 300, True, "fp8"),
+    (64, -1, False, "fp8"), (32, -1, True, "bf16")])
+def test_fp8_extend(page_size, window, causal, entry):
+    """Varlen extend over an fp8 cache on the tcgen05 kernel: q rounded to
+    e4m3, QK^T on e4m3 tensor-core MMAs, V widened to f16 for PV, descales
+    per (request, KV head) (or 1 through the bf16 entry point); NaN in every
+    unused slot of the pool."""
+    wl = workloads.make("varlen_extend", batch=4, new_lo=64, new_hi=700, prefix_lo=0,
+                        prefix_hi=900, page_size=page_size,
+                        pool_pages=4 * (1600 // page_size + 2) + 8, window_left=window,
+                        seed=1203 + page_size)
+    wl.causal = causal
+    valid = torch.zeros(wl.k_cache.shape[0] * page_size, dtype=torch.bool)
+    for b in range(4):
+        j = torch.arange(int(wl.cache_seqlens[b]))
+        valid[wl.page_table[b, j // page_size].long() * page_size + j % page_size] = True
+    valid = valid.view(-1, page_size)
+    wl.k_cache[~valid] = float("nan")
+    wl.v_cache[~valid] = float("nan")
+    out, lse, ref_o, ref_l = _fp8_run(wl, descale=entry == "fp8", seed=page_size, entry=entry)
+    check_close(out, lse, ref_o, ref_l, f"fp8 extend P={page_size} w={window} c={causal}")
+    assert pkv.get_error_flags() == 0
+
+
+def test_fp8_extend_negative_scale_and_bad_page():
+    """The fp8 extend kernel with a negative softmax scale (its row maxima
+    are taken on sign-flipped scores) and an out-of-pool page id (those keys
+    skipped and flagged, as the oracle skips them)."""
+    wl = workloads.make("varlen_extend", batch=3, new_lo=100, new_hi=400, prefix_lo=50,
+                        prefix_hi=600, page_size=64, pool_pages=3 * 17 + 10, seed=1301)
+    wl.page_table[1, 2] = 10_000_000
+    wl.cache_seqlens[1] = max(int(wl.cache_seqlens[1]), 3 * 64 + 1)
+    wl.cache_seqlens[1] = min(int(wl.cache_seqlens[1]), wl.page_table.shape[1] * 64)
+    out, lse, ref_o, ref_l = _fp8_run(wl, seed=9, scale=-0.08)
+    check_close(out, lse, ref_o, ref_l, "fp8 extend negative scale")
+    assert pkv.get_error_flags() == pkv.EFLAG_PAGE_OOB
 
 
 def test_fp8_unit_descale_entry_and_edges():
@@ -1282,8 +1324,9 @@ def test_fp8_unit_descale_entry_and_edges():
 
 
 def test_fp8_unsupported_shapes_are_refused():
-    """Shapes outside the fp8 path return PKV_ERR_UNSUPPORTED: page size 1,
-    fixed splits."""
+    """Decode shapes outside the fp8 path return PKV_ERR_UNSUPPORTED: page
+    size 1, fixed splits (runs of >= 64 new tokens go to the extend kernel,
+    test_fp8_extend)."""
     wl = workloads.make("tiny_decode", d=128, page_size=1, h_q=8, h_kv=2, batch=2,
                         len_lo=10, len_hi=50, pool_tokens=256, seed=112)
     g = wl.to(DEV)
