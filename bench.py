@@ -491,6 +491,37 @@ def fp8_line(dev, peaks):
             "tokens_per_s": g.q.shape[0] / (a_ms / 1e3)}
 
 
+def fp8_swa_line(dev, peaks):
+    """The sliding-window decode workload over an fp8 cache (page size 1:
+    slot rows of codes): the prefill-aware table, then the attention with
+    descales 0.75 / 1.25.  Algorithmic bytes are the codes of the kept rows
+    (1 byte per element)."""
+    st = Step("swa_decode", dev, {})
+    g = st.g
+    k8 = g.k_cache.to(torch.float8_e4m3fn)
+    v8 = g.v_cache.to(torch.float8_e4m3fn)
+    del g.k_cache, g.v_cache
+    pkv.build_swa_page_table(g.req_to_token, g.req_pool_indices, g.seq_lens, g.prefill_lens,
+                             g.window, st.pt, st.kv)
+    B, h_kv = st.kv.shape[0], k8.shape[2]
+    kd = torch.full((B, h_kv), 0.75, device=dev)
+    vd = torch.full((B, h_kv), 1.25, device=dev)
+    out = torch.empty(g.q.shape[0], g.q.shape[1], 128, dtype=torch.bfloat16, device=dev)
+    ws_n = pkv.attn_workspace_size(g.q, k8, v8, st.pt, st.kv, 1)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=dev)
+
+    def attend():
+        pkv.attn_with_kvcache_fp8(g.q, k8, v8, st.pt, st.kv, g.cu_seqlens_q, 1, g.scale,
+                                  k_descale=kd, v_descale=vd, out=out, workspace=ws)
+
+    a_ms, a_how = _timed(attend)
+    code_bytes = st.kv_bytes // 2
+    return {"kernel": "decode_allheads_kernel (slot rows, balanced, fp8)", "attn_ms": a_ms,
+            "timing": a_how, "kv_GBps": code_bytes / 1e9 / (a_ms / 1e3),
+            "kv_frac_hbm": code_bytes / 1e9 / (a_ms / 1e3) / peaks["hbm_gbs"],
+            "tokens_per_s": g.q.shape[0] / (a_ms / 1e3)}
+
+
 def fp8_extend_line(dev, peaks):
     """The varlen extend workload over an fp8 cache (the bf16 cache cast to
     e4m3 codes, descales 0.75 / 1.25): e4m3 QK^T and f16 PV on the tensor
@@ -609,7 +640,7 @@ def merge_line(dev, peaks, sizes=(("decode_batch", 64), ("prefill", 32768))):
 EXTRA_LINES = {"local": local_attention_line, "cascade": cascade_line, "append": append_line,
                "fp8": fp8_line, "topk": topk_line, "merge": merge_line,
                "merge_prefill": lambda dev, peaks: merge_line(dev, peaks, (("prefill", 32768),)),
-               "fp8_extend": fp8_extend_line,
+               "fp8_extend": fp8_extend_line, "fp8_swa": fp8_swa_line,
                "append_decode": append_decode_line}
 
 
@@ -1002,7 +1033,8 @@ def main():
                           ("varlen_extend@append_then_attend", append_line),
                           (HEADLINE + "@fused_append", append_decode_line),
                           (HEADLINE + "@fp8_kv", fp8_line),
-                          ("varlen_extend@fp8_kv", fp8_extend_line)):
+                          ("varlen_extend@fp8_kv", fp8_extend_line),
+                          ("swa_decode@fp8_kv", fp8_swa_line)):
             try:
                 others[label] = fn(dev, peaks)
             except pkv.PkvError as e:

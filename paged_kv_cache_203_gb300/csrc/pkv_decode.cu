@@ -808,7 +808,7 @@ __host__ __device__ inline AhLayout ah_layout(int hpc, bool boxes, bool balanced
   // page boxes: [head][16 positions][128 B] per 64-column half (bf16) or for
   // all 128 columns (fp8 codes)
   L.stage = boxes ? static_cast<uint32_t>(hpc) * AH_BK * (fp8 ? 128u : 256u)
-                  : AH_BK * (static_cast<uint32_t>(hpc) * 256u + 16u);
+                  : AH_BK * (static_cast<uint32_t>(hpc) * (fp8 ? 128u : 256u) + 16u);
   L.k = 0;
   L.v = L.k + ns * L.stage;
   L.pos = L.v + ns * L.stage;  // int [NSTAGE][BK]
@@ -981,7 +981,6 @@ template <bool BOXES, bool FP8, bool APPEND>
 __global__ void __launch_bounds__((AH_MAXH + 2) * 32, 1)
 decode_allheads_kernel(const __grid_constant__ AttnParams p,
                        const __grid_constant__ AhMaps maps) {
-  static_assert(BOXES || !FP8, "fp8 caches use page boxes");
   static_assert(!(FP8 && APPEND), "the fused append serves bf16 caches");
   constexpr int NST = FP8 ? AH_NSTAGE_FP8 : AH_NSTAGE;  // ring stages
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -1017,7 +1016,8 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   int *sFirstShare = sQHead + 3;
   int *sClaim = sQHead + 4;
   int *share_ctr = p.ws_counter + static_cast<int64_t>(p.batch) * p.h_kv;  // balanced
-  const uint32_t row_bytes = static_cast<uint32_t>(hpc) * 256u;  // the CTA's heads of one key
+  // the CTA's heads of one key (bf16, or one byte per fp8 code)
+  const uint32_t row_bytes = static_cast<uint32_t>(hpc) * (FP8 ? 128u : 256u);
   const uint32_t pitch = row_bytes + 16u;                         // slot-row mode
 
   if (tid == 0) {
@@ -1316,7 +1316,9 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
         __syncwarp();
         if (pos >= 0)
           bulk_g2s(kdst + lane * pitch,
-                   tk_new >= 0 ? p.k_new + tk_new * p.kn_st + head0 * p.kn_sh : p.k + koff,
+                   tk_new >= 0 ? static_cast<const void *>(p.k_new + tk_new * p.kn_st + head0 * p.kn_sh)
+                   : FP8       ? static_cast<const void *>(reinterpret_cast<const uint8_t *>(p.k) + koff)
+                               : static_cast<const void *>(p.k + koff),
                    row_bytes, full);
       }
       // fused append: the CTA that takes the request's last tile stores the
@@ -1483,6 +1485,8 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
   // byte offset of 16-byte chunk c of key `key` of this head within a stage
   // (fp8: chunk c holds the 16 codes of columns 16c..16c+15)
   auto soff = [&](int key, int c) -> uint32_t {
+    if (FP8 && !BOXES)  // slot rows of codes: [key][pitch], the head's 128 B at w * 128
+      return static_cast<uint32_t>(key) * pitch + static_cast<uint32_t>(w * 128 + c * 16);
     if (FP8)
       return static_cast<uint32_t>(w * 2048 + key * 128 + (((c & 7) ^ (key & 7)) << 4));
     if (BOXES)
@@ -1509,17 +1513,29 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
     if (!BOXES) {  // the producer publishes V offsets up to two tiles past the CTA's last
       const int sx = x % NST;
       if (!mbar_wait_sleep(vmeta0 + 8 * sx, (x / NST) & 1)) return false;
-      const int c = lane & 15;
       const uint32_t vdst = sbase + L.v + sx * L.stage;
+      if (FP8) {  // 128 codes (8 chunks) per key: 16 rows x 8 chunks, 4 per lane
+        const int c = lane & 7;
+        const uint8_t *vb8 = reinterpret_cast<const uint8_t *>(p.v);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int rr = (lane >> 4) + 2 * i;
-        const int64_t vo = sVoff[sx * AH_BK + rr];
-        const int tk = APPEND ? sNew[sx * AH_BK + rr] : -1;  // fused append: the new row
-        const bf16 *src = tk >= 0   ? p.v_new + tk * p.vn_st + h * p.vn_sh + c * 8
-                          : vo >= 0 ? p.v + vo + h * 128 + c * 8
-                                    : p.v;
-        cp_async16(vdst + soff(rr, c), src, (tk >= 0 || vo >= 0) ? 16 : 0);
+        for (int i = 0; i < 4; ++i) {
+          const int rr = (lane >> 3) + 4 * i;
+          const int64_t vo = sVoff[sx * AH_BK + rr];
+          cp_async16(vdst + soff(rr, c), vo >= 0 ? vb8 + vo + h * 128 + c * 16 : vb8,
+                     vo >= 0 ? 16 : 0);
+        }
+      } else {
+        const int c = lane & 15;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = (lane >> 4) + 2 * i;
+          const int64_t vo = sVoff[sx * AH_BK + rr];
+          const int tk = APPEND ? sNew[sx * AH_BK + rr] : -1;  // fused append: the new row
+          const bf16 *src = tk >= 0   ? p.v_new + tk * p.vn_st + h * p.vn_sh + c * 8
+                            : vo >= 0 ? p.v + vo + h * 128 + c * 8
+                                      : p.v;
+          cp_async16(vdst + soff(rr, c), src, (tk >= 0 || vo >= 0) ? 16 : 0);
+        }
       }
     }
     if (!BOXES) cp_async_commit();
@@ -2211,7 +2227,8 @@ bool encode_allheads_maps(AhMaps *m, const AttnParams &p, int hpc) {
 bool decode_allheads_eligible(const AttnParams &p) {
   if (p.topk != nullptr || p.d != 128 || p.dv != 128) return false;
   if (p.h_kv > AH_MAXH || p.max_seqlen_q < 1 || p.max_seqlen_q * p.group > 16) return false;
-  if (p.kv_fp8 && p.page_size % AH_BK != 0) return false;  // fp8: page boxes only
+  // fp8: page boxes (multiples of 16) or slot rows (page size < 8)
+  if (p.kv_fp8 && p.page_size >= 8 && p.page_size % AH_BK != 0) return false;
   if (p.page_size < 8) {
     // slot rows: every slot's heads form one contiguous H_kv x 128 row
     return p.k_sh == 128 && p.k_spos == static_cast<int64_t>(p.h_kv) * 128 &&
@@ -2231,7 +2248,7 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
   if (balanced && p.batch > AH_MAXB) return PKV_ERR_UNSUPPORTED;
   const bool boxes = p.page_size >= 8;
   const bool fp8 = p.kv_fp8 != 0;
-  if (fp8 && (!boxes || !balanced)) return PKV_ERR_UNSUPPORTED;
+  if (fp8 && !balanced) return PKV_ERR_UNSUPPORTED;
   // Page boxes with fixed splits: kAhFixedHeads KV heads per CTA, so a
   // request's chunk is kAhFixedHeads / h_kv of a work item that covers every
   // head, and the items balance over the grid (longest requests first).
@@ -2248,7 +2265,8 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
                          reinterpret_cast<const void *>(decode_allheads_kernel<false, false, false>),
                          reinterpret_cast<const void *>(decode_allheads_kernel<true, true, false>),
                          reinterpret_cast<const void *>(decode_allheads_kernel<true, false, true>),
-                         reinterpret_cast<const void *>(decode_allheads_kernel<false, false, true>)};
+                         reinterpret_cast<const void *>(decode_allheads_kernel<false, false, true>),
+                         reinterpret_cast<const void *>(decode_allheads_kernel<false, true, false>)};
     for (const void *fn : fns)
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, AH_SMEM_MAX) !=
           cudaSuccess)
@@ -2263,8 +2281,10 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream) {
   const dim3 grid = balanced ? dim3(kDecodeBalancedCtas, 1, 1)
                              : dim3(p.num_splits, p.h_kv / hpc, p.batch);
   const dim3 block((hpc + (balanced ? 2 : 1)) * 32);  // + producer (+ merge warp)
-  if (fp8)
+  if (fp8 && boxes)
     decode_allheads_kernel<true, true, false><<<grid, block, L.end, stream>>>(p, maps);
+  else if (fp8)
+    decode_allheads_kernel<false, true, false><<<grid, block, L.end, stream>>>(p, maps);
   else if (boxes && p.append)
     decode_allheads_kernel<true, false, true><<<grid, block, L.end, stream>>>(p, maps);
   else if (boxes)

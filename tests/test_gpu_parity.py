@@ -1252,12 +1252,13 @@ def _fp8_run(wl, descale=True, seed=0, entry="fp8", scale=None):
     return out, lse, ref_o, ref_l
 
 
-@pytest.mark.parametrize("page_size,h_q,q_len", [(16, 32, 1), (64, 32, 2), (16, 64, 2)])
+@pytest.mark.parametrize("page_size,h_q,q_len", [(16, 32, 1), (64, 32, 2), (16, 64, 2),
+                                                 (1, 32, 1), (2, 16, 2)])
 def test_fp8_decode(page_size, h_q, q_len):
     """FP8 cache (e4m3 codes), per-(request, KV head) descales, q cast to
     e4m3 in the kernel: GQA decode shapes, 8 KV heads, head dim 128, up to 16
     query rows per KV head, ragged lengths (the balanced schedule splits the
-    long requests over CTAs)."""
+    long requests over CTAs); page boxes and slot rows (page sizes 1, 2)."""
     wl = workloads.make("tiny_decode", d=128, page_size=page_size, h_q=h_q, h_kv=8,
                         q_len=q_len, causal=q_len > 1, batch=24, len_lo=q_len,
                         len_hi=3000, pool_tokens=24 * 3072 + 256, seed=101 + page_size)
@@ -1325,9 +1326,9 @@ def test_fp8_unit_descale_entry_and_edges():
 
 def test_fp8_unsupported_shapes_are_refused():
     """Decode shapes outside the fp8 path return PKV_ERR_UNSUPPORTED: page
-    size 1, fixed splits (runs of >= 64 new tokens go to the extend kernel,
+    size 8, fixed splits (runs of >= 64 new tokens go to the extend kernel,
     test_fp8_extend)."""
-    wl = workloads.make("tiny_decode", d=128, page_size=1, h_q=8, h_kv=2, batch=2,
+    wl = workloads.make("tiny_decode", d=128, page_size=8, h_q=8, h_kv=2, batch=2,
                         len_lo=10, len_hi=50, pool_tokens=256, seed=112)
     g = wl.to(DEV)
     k8, v8 = _to_fp8(g.k_cache), _to_fp8(g.v_cache)
