@@ -522,6 +522,35 @@ def fp8_swa_line(dev, peaks):
             "tokens_per_s": g.q.shape[0] / (a_ms / 1e3)}
 
 
+def fp8_mla_line(dev, peaks):
+    """The MLA top-k decode workload over an fp8 latent cache (codes of the
+    bf16 rows, descales 0.75 / 1.25): algorithmic bytes are the listed rows'
+    codes (576 B per key per token), flops as for the bf16 cache."""
+    g = workloads.make("mla_topk_decode", value_device=dev)
+    st = Step.__new__(Step)
+    st.g = g
+    flops = Step._flops(st)
+    k8 = g.k_cache.to(torch.float8_e4m3fn)
+    del g.k_cache, g.v_cache
+    B = g.cache_seqlens.shape[0]
+    kd = torch.full((B, 1), 0.75, device=dev)
+    vd = torch.full((B, 1), 1.25, device=dev)
+    out = torch.empty(g.q.shape[0], 128, 512, dtype=torch.bfloat16, device=dev)
+
+    def attend():
+        pkv.attn_with_kvcache_fp8(g.q, k8, k8[..., :512], g.page_table, g.cache_seqlens,
+                                  g.cu_seqlens_q, g.max_seqlen_q, g.scale,
+                                  topk_indices=g.topk_indices, k_descale=kd, v_descale=vd,
+                                  out=out)
+
+    a_ms, a_how = _timed(attend)
+    code_bytes = int((g.topk_indices >= 0).sum()) * 576
+    return {"kernel": "mla_topk_kernel (fp8 cache)", "attn_ms": a_ms, "timing": a_how,
+            "kv_GBps": code_bytes / 1e9 / (a_ms / 1e3),
+            "kv_frac_hbm": code_bytes / 1e9 / (a_ms / 1e3) / peaks["hbm_gbs"],
+            "TFLOPs": flops / 1e12 / (a_ms / 1e3)}
+
+
 def fp8_extend_line(dev, peaks):
     """The varlen extend workload over an fp8 cache (the bf16 cache cast to
     e4m3 codes, descales 0.75 / 1.25): e4m3 QK^T and f16 PV on the tensor
@@ -641,6 +670,7 @@ EXTRA_LINES = {"local": local_attention_line, "cascade": cascade_line, "append":
                "fp8": fp8_line, "topk": topk_line, "merge": merge_line,
                "merge_prefill": lambda dev, peaks: merge_line(dev, peaks, (("prefill", 32768),)),
                "fp8_extend": fp8_extend_line, "fp8_swa": fp8_swa_line,
+               "fp8_mla": fp8_mla_line,
                "append_decode": append_decode_line}
 
 
@@ -1034,7 +1064,8 @@ def main():
                           (HEADLINE + "@fused_append", append_decode_line),
                           (HEADLINE + "@fp8_kv", fp8_line),
                           ("varlen_extend@fp8_kv", fp8_extend_line),
-                          ("swa_decode@fp8_kv", fp8_swa_line)):
+                          ("swa_decode@fp8_kv", fp8_swa_line),
+                          ("mla_topk_decode@fp8_kv", fp8_mla_line)):
             try:
                 others[label] = fn(dev, peaks)
             except pkv.PkvError as e:

@@ -157,24 +157,29 @@ int pkv_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
  *                    contiguous), or NULL for 1.
  * Other arguments, outputs and workspace as pkv_attn_with_kvcache
  * (pkv_attn_workspace_size takes the fp8 tensors as they are).
- * Supported, head dim 128 and no top-k lists in both cases:
- *  - extend (max_seqlen_q >= 64): page size a multiple of 8 that divides 128
- *    or is a multiple of 128, strides that nest (head inside position inside
- *    page), any num_splits (no split is made, no workspace), any sign of
- *    scale * k_descale;
- *  - decode: H_kv <= 8, at most 16 query rows per KV head
- *    (max_seqlen_q * H_q / H_kv), page size a multiple of 16, num_splits = 0,
- *    B <= 2048;
+ * topk_indices (optional, absorbed MLA only) as pkv_attn_with_kvcache.
+ * Supported:
+ *  - head dim 128, no top-k lists, extend (max_seqlen_q >= 64): page size a
+ *    multiple of 8 that divides 128 or is a multiple of 128, strides that
+ *    nest (head inside position inside page), any num_splits (no split is
+ *    made, no workspace), any sign of scale * k_descale;
+ *  - head dim 128, no top-k lists, decode: H_kv <= 8, at most 16 query rows
+ *    per KV head (max_seqlen_q * H_q / H_kv), page size < 8 or a multiple of
+ *    16, num_splits = 0, B <= 2048;
+ *  - absorbed MLA over top-k lists (576 / 512 dims, 128 heads, one latent
+ *    head, v_cache the first 512 columns of k_cache): as pkv_attn_with_kvcache,
+ *    k_descale / v_descale per request;
  * otherwise PKV_ERR_UNSUPPORTED.
  */
 int pkv_attn_with_kvcache_fp8(pkv_tensor q, pkv_tensor k_cache,
                               pkv_tensor v_cache, pkv_tensor page_table,
                               pkv_tensor cache_seqlens, pkv_tensor cu_seqlens_q,
                               int max_seqlen_q, float scale, int causal,
-                              int window_left, const float *k_descale,
-                              const float *v_descale, int num_splits,
-                              pkv_tensor out, pkv_tensor lse, void *workspace,
-                              size_t workspace_bytes, cudaStream_t stream);
+                              int window_left, pkv_tensor topk_indices,
+                              const float *k_descale, const float *v_descale,
+                              int num_splits, pkv_tensor out, pkv_tensor lse,
+                              void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
 
 /* Bytes of workspace pkv_attn_with_kvcache needs for these sizes (0 if
  * none).  Arguments mirror the attention call's; returns 0 and sets

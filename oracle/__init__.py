@@ -104,7 +104,7 @@ def _lib():
             _int, _int, _i64,
             _i32p, _i64, _int,
             _i32p, _i32p, _int, ctypes.c_double, _int, _int,
-            _f32p, _f32p, _f64p, _f64p, _int]
+            _f32p, _f32p, _i32p, _i64, _int, _f64p, _f64p, _int]
         lib.orc_attention_fp8.restype = ctypes.c_int
         lib.orc_set_kv_buffer.argtypes = [
             _u16p, _i64, _i64, _int, _int, _int, _i64p, _u16p, _i64, _i64, _i64,
@@ -218,12 +218,14 @@ def e4m3_round(x: float) -> int:
 
 def attention_fp8(q_bits, k_codes, v_codes, page_table, cache_seqlens, cu_seqlens_q,
                   scale: float, causal: bool = False, window_left: int = -1,
-                  k_descale=None, v_descale=None, num_threads: int = 0):
+                  k_descale=None, v_descale=None, num_threads: int = 0, topk=None):
     """Attention over an fp8 (e4m3) paged cache in float64: q rounded to
     e4m3, K/V codes widened and multiplied by their (request, KV head)
     descales.  q_bits: uint16 [total_q, H_q, D]; k_codes / v_codes: uint8
-    [num_pages, P, H_kv, D] (D contiguous); descales: float32 [B, H_kv] or
-    None.  Returns (out [total_q, H_q, Dv], lse [total_q, H_q], n_skipped)."""
+    [num_pages, P, H_kv, D] (D contiguous; V may be a column slice of K, as
+    for absorbed MLA); descales: float32 [B, H_kv] or None; topk: optional
+    int32 [total_q, L] position lists (as in attention).  Returns (out
+    [total_q, H_q, Dv], lse [total_q, H_q], n_skipped)."""
     q = np.asarray(q_bits)
     k = np.asarray(k_codes)
     v = np.asarray(v_codes)
@@ -238,6 +240,7 @@ def attention_fp8(q_bits, k_codes, v_codes, page_table, cache_seqlens, cu_seqlen
     cu = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
     kd = None if k_descale is None else np.ascontiguousarray(k_descale, dtype=np.float32)
     vd = None if v_descale is None else np.ascontiguousarray(v_descale, dtype=np.float32)
+    tk = None if topk is None else np.ascontiguousarray(topk, dtype=np.int32)
     out = np.zeros((total_q * h_q, d_v), dtype=np.float64)
     lse = np.zeros(total_q * h_q, dtype=np.float64)
     rc = _lib().orc_attention_fp8(
@@ -247,6 +250,8 @@ def attention_fp8(q_bits, k_codes, v_codes, page_table, cache_seqlens, cu_seqlen
         h_kv, page_size, num_pages, _ptr(pt, ctypes.c_int32), pt.shape[1], pt.shape[1],
         _ptr(cs, ctypes.c_int32), _ptr(cu, ctypes.c_int32), len(cs), float(scale),
         int(bool(causal)), int(window_left), _ptr(kd, ctypes.c_float), _ptr(vd, ctypes.c_float),
+        _ptr(tk, ctypes.c_int32), 0 if tk is None else tk.shape[1],
+        0 if tk is None else tk.shape[1],
         _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double), int(num_threads))
     if rc < 0:
         raise ValueError(f"orc_attention_fp8 rejected its arguments ({rc})")

@@ -419,13 +419,18 @@ int orc_attention_fp8(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q
                       const int32_t *cache_seqlens, const int32_t *cu_seqlens_q,
                       int batch, double scale, int causal, int window_left,
                       const float *k_descale, const float *v_descale,
+                      const int32_t *topk, int64_t topk_stride, int topk_len,
                       double *out, double *lse, int num_threads) {
   if (total_q < 0 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0 || d_qk < 1 ||
-      d_v < 1 || page_size < 1 || batch < 0 || window_left < -1)
+      d_v < 1 || page_size < 1 || batch < 0 || window_left < -1 || (topk && topk_len < 0))
     return -1;
   int64_t max_keys = 1;
-  for (int b = 0; b < batch; ++b)
-    if (cache_seqlens[b] > max_keys) max_keys = cache_seqlens[b];
+  if (topk) {
+    if (topk_len > max_keys) max_keys = topk_len;
+  } else {
+    for (int b = 0; b < batch; ++b)
+      if (cache_seqlens[b] > max_keys) max_keys = cache_seqlens[b];
+  }
   int skipped_total = 0;
 #ifdef _OPENMP
   if (num_threads > 0) omp_set_num_threads(num_threads);
@@ -454,9 +459,20 @@ int orc_attention_fp8(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q
       const uint16_t *qrow = q + (int64_t)t * q_st + (int64_t)h * q_sh;
       for (int dd = 0; dd < d_qk; ++dd)
         qv[dd] = orc_e4m3_value(orc_e4m3_round(bf16_bits_to_double(qrow[dd])));
-      /* 2. the visible keys and their slots */
+      /* 2. the visible keys and their slots: every position, or the token's
+         top-k list (nsa_backend.py: -1 pads the list, other positions
+         outside [0, kv_len) are skipped and counted, a repeated position
+         counts each time, and the causal bound applies to the listed
+         positions) */
       int64_t n = 0;
-      for (int64_t j = 0; j < kv_len; ++j) {
+      const int64_t n_cand = topk ? topk_len : kv_len;
+      for (int64_t cnd = 0; cnd < n_cand; ++cnd) {
+        int64_t j = cnd;
+        if (topk) {
+          j = topk[(int64_t)t * topk_stride + cnd];
+          if (j == -1) continue;
+          if (j < -1 || j >= kv_len) { ++skipped_total; continue; }
+        }
         if (causal && j > i) continue;
         if (window_left >= 0 && (j > i || j < i - window_left)) continue;
         if (j / page_size >= pt_cols) { ++skipped_total; continue; }

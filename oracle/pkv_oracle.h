@@ -204,7 +204,8 @@ int orc_set_kv_buffer_fp8(const uint16_t *rows, int64_t r_st, int64_t r_sh, int 
 /* Attention over an fp8 cache: q rounded to e4m3 (orc_e4m3_round) and widened;
  * K_j = value(k code) * k_descale[b * n_kv_heads + kvh], V_j likewise with
  * v_descale (NULL descales = 1); then the definition of orc_attention (same
- * layouts, masks, bottom-right alignment and empty-key result, no top-k).
+ * layouts, masks, bottom-right alignment, top-k lists and empty-key result;
+ * the skipped count is per (token, head) row here).
  * k / v: uint8 codes, (page, pos, head, d) at page*sp + pos*spos + head*sh + d. */
 int orc_attention_fp8(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q,
                       int h_q, int d_qk, const uint8_t *k_cache, int64_t k_sp,
@@ -215,6 +216,7 @@ int orc_attention_fp8(const uint16_t *q, int64_t q_st, int64_t q_sh, int total_q
                       const int32_t *cache_seqlens, const int32_t *cu_seqlens_q,
                       int batch, double scale, int causal, int window_left,
                       const float *k_descale, const float *v_descale,
+                      const int32_t *topk, int64_t topk_stride, int topk_len,
                       double *out, double *lse, int num_threads);
 
 /* Log-sum-exp state merge (dual_chunk_flashattention_backend.py,

@@ -154,7 +154,7 @@ def load_library(path: str | None = None):
     lib.pkv_set_kv_buffer.argtypes = [T, T, T, T, T, c_void_p]
     lib.pkv_set_kv_buffer_fp8.argtypes = [T, T, T, T, T, c_void_p, c_void_p, c_void_p]
     lib.pkv_attn_with_kvcache_fp8.argtypes = [T, T, T, T, T, T, c_int, c_float, c_int, c_int,
-                                              c_void_p, c_void_p, c_int, T, T, c_void_p,
+                                              T, c_void_p, c_void_p, c_int, T, T, c_void_p,
                                               c_size_t, c_void_p]
     TP = ctypes.POINTER(T)
     lib.pkv_append_attn_with_kvcache.argtypes = [T, T, T, T, T, T, c_int, c_float, c_int,
@@ -254,11 +254,13 @@ def attn_with_kvcache_fp8(q, k_cache, v_cache, page_table, cache_seqlens, cu_seq
                           max_seqlen_q: int, softmax_scale: float, causal: bool = False,
                           window_left: int = -1, k_descale=None, v_descale=None,
                           out=None, lse=None, return_softmax_lse: bool = False,
-                          workspace=None):
+                          workspace=None, topk_indices=None, num_splits: int = 0):
     """Paged attention over an fp8 (e4m3) cache (include/pkv.h,
     pkv_attn_with_kvcache_fp8): ``k_cache`` / ``v_cache`` are
     torch.float8_e4m3fn tensors, ``k_descale`` / ``v_descale`` optional fp32
-    [B, H_kv]; q (bf16) is rounded to e4m3 inside the kernel."""
+    [B, H_kv]; q (bf16) is rounded to e4m3 inside the kernel.  Absorbed MLA
+    (576 / 512 dims, one latent head, ``v_cache`` the first 512 columns of
+    ``k_cache``) takes ``topk_indices`` as pkv_attn_with_kvcache does."""
     lib = load_library()
     if out is None:
         out = torch.empty(q.shape[0], q.shape[1], v_cache.shape[-1], dtype=torch.bfloat16,
@@ -266,16 +268,17 @@ def attn_with_kvcache_fp8(q, k_cache, v_cache, page_table, cache_seqlens, cu_seq
     if return_softmax_lse and lse is None:
         lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
     ws_bytes = attn_workspace_size(q, k_cache, v_cache, page_table, cache_seqlens,
-                                   max_seqlen_q)
+                                   max_seqlen_q, topk_indices, num_splits)
     if ws_bytes > 0 and (workspace is None or workspace.numel() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if ws_bytes > 0 else None
     _check("pkv_attn_with_kvcache_fp8", lib.pkv_attn_with_kvcache_fp8(
         _desc(q), _desc(k_cache), _desc(v_cache), _desc(page_table), _desc(cache_seqlens),
         _desc(cu_seqlens_q), int(max_seqlen_q), float(softmax_scale), int(bool(causal)),
-        int(window_left), _descale_ptr(k_descale, cache_seqlens, k_cache),
-        _descale_ptr(v_descale, cache_seqlens, k_cache), 0, _desc(out), _desc(lse),
-        ws_ptr, ws_bytes, _stream(q)))
+        int(window_left), _desc(topk_indices),
+        _descale_ptr(k_descale, cache_seqlens, k_cache),
+        _descale_ptr(v_descale, cache_seqlens, k_cache), int(num_splits), _desc(out),
+        _desc(lse), ws_ptr, ws_bytes, _stream(q)))
     return (out, lse) if return_softmax_lse else out
 
 

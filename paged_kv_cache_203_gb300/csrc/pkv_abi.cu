@@ -131,7 +131,7 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
 
   const int group = static_cast<int>(h_q / h_kv);
   const bool mla = d == 576 && dv == 512;
-  if (fp8) {
+  if (fp8 && !mla) {
     // fp8 caches: runs of >= kExtendMinSeqlenQ new tokens on the tcgen05
     // extend kernel (e4m3 QK^T, f16 PV; no split, no workspace); decode on
     // the all-heads kernel with page boxes and its balanced schedule (head
@@ -512,14 +512,13 @@ int pkv_append_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_
 int pkv_attn_with_kvcache_fp8(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
                               pkv_tensor page_table, pkv_tensor cache_seqlens,
                               pkv_tensor cu_seqlens_q, int max_seqlen_q, float scale,
-                              int causal, int window_left, const float *k_descale,
-                              const float *v_descale, int num_splits, pkv_tensor out,
-                              pkv_tensor lse, void *workspace, size_t workspace_bytes,
-                              cudaStream_t stream) {
+                              int causal, int window_left, pkv_tensor topk_indices,
+                              const float *k_descale, const float *v_descale, int num_splits,
+                              pkv_tensor out, pkv_tensor lse, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
   if (k_cache.data == nullptr || k_cache.dtype != PKV_FP8_E4M3 || k_cache.ndim != 4 ||
       cache_seqlens.data == nullptr || cache_seqlens.ndim != 1)
     return PKV_ERR_INVALID_ARG;
-  const pkv_tensor none{};
   // the descales as [B][H_kv] fp32 descriptors (contiguous rows)
   pkv_tensor kd{}, vd{};
   for (int i = 0; i < 2; ++i) {
@@ -533,8 +532,8 @@ int pkv_attn_with_kvcache_fp8(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cac
     t.stride[1] = 1;
   }
   return pkv::attn_impl(q, k_cache, v_cache, page_table, cache_seqlens, cu_seqlens_q,
-                        max_seqlen_q, scale, causal, window_left, none, num_splits, kd, vd,
-                        out, lse, workspace, workspace_bytes, stream);
+                        max_seqlen_q, scale, causal, window_left, topk_indices, num_splits, kd,
+                        vd, out, lse, workspace, workspace_bytes, stream);
 }
 
 int pkv_merge_state(pkv_tensor v_a, pkv_tensor lse_a, pkv_tensor v_b,

@@ -71,6 +71,15 @@ constexpr uint32_t kPTile = H * BK * 2;             // 16384: P [128 heads][64 k
 constexpr uint32_t kFacWarp = 144;                  // 32 factors, a flag word, padding
 constexpr uint32_t kPXfer = kPTile + NSOFT * kFacWarp;  // 16960 bytes per P buffer
 constexpr uint32_t kFinBytes = H * 8;               // (1/l, lse) per head
+// fp8 cache: two MMA stages of f16 tiles plus two staging tiles of the
+// gathered codes (rows of 576 B on the score side, 512 B on the value side)
+// take the bytes of the three bf16 stages
+constexpr int NSTG_F8 = 2;
+constexpr uint32_t kStgScore = BK * DQK;            // 36864
+constexpr uint32_t kStgValue = BK * DV;             // 32768
+static_assert(NSTG_F8 * kKTile + 2 * kStgScore <= NSTG * kKTile &&
+                  NSTG_F8 * kVTile + 2 * kStgValue <= NSTG * kVTile,
+              "fp8 staging fits the bf16 stage budget");
 // TMEM columns.  Score CTA: Q [0, 288) as packed bf16 pairs, S0 at 384, S1 at
 // 448.  Value CTA: O [0, 512).
 constexpr uint32_t kTmQ = 0, kTmS = 384;
@@ -160,8 +169,10 @@ __device__ __forceinline__ RowRef resolve(const AttnParams &p, int e, int pc, in
   return r;
 }
 
+template <bool FP8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 mla_topk_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int NS = FP8 ? NSTG_F8 : NSTG;  // MMA stages
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_addr(smem);
   uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + Smem::kTmemSlot);
@@ -208,7 +219,7 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
     for (int i = 0; i < NCH; ++i) prefetch_line_l2(qrow + i * 64);
   }
   if (tid == 0) {
-    for (int s = 0; s < NSTG; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(bar(FULL + s), NPROD * 32);
       mbar_init(bar(EMPTY + s), score ? 1 + NSOFT : 1);
     }
@@ -280,52 +291,128 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
 #pragma unroll
     for (int k = 0; k < kLagP; ++k) G[k] = page(E[k]);
     float *sBias = reinterpret_cast<float *>(smem + Smem::kBias);
+    auto key_bias = [&](int pos) {
+      const bool vis = pos >= 0 && !(use_upper && pos > i_pos) && pos >= lo_r;
+      return vis ? 0.f : -INFINITY;
+    };
+    // fp8 cache: the codes of tile jj land in staging slot jj & 1 (rows of
+    // 576 / 512 B); one tile later this warp widens its own 8 rows to f16
+    // into MMA stage jj % NS (exact: an e4m3 value is an f16 value), writes
+    // the key mask, and arrives on the stage's barrier
+    const uint8_t *k8 = reinterpret_cast<const uint8_t *>(p.k);
+    const uint32_t stg_row = score ? DQK : DV;
+    const uint32_t stg0 = ring + NS * tile_bytes;
+    auto widen = [&](int jt, int pos, bool last) -> bool {
+      const int s = jt % NS;
+      if (last) cp_async_wait_group<0>();
+      else cp_async_wait_group<1>();
+      __syncwarp();  // the warp's other lanes' copies are visible
+      int ok = 1;
+      if (lane == 0 && jt >= NS) ok = mbar_wait_sleep(bar(EMPTY + s), ((jt / NS) & 1) ^ 1) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      if (score && own) sBias[s * BK + myrow] = key_bias(pos);
+      const uint32_t dst0 = ring + s * tile_bytes;
+      const uint32_t src0 = stg0 + (jt & 1) * (BK * stg_row);
+#pragma unroll
+      for (int rl = 0; rl < kRowsPerWarp; ++rl) {  // value columns: 16 codes a lane
+        const int row = pw * kRowsPerWarp + rl;
+        uint4 cw;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                     : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
+                     : "r"(src0 + row * stg_row + lane * 16));
+        const uint4 o0 = make_uint4(e4m3x2_to_f16x2(cw.x), e4m3x2_to_f16x2(cw.x >> 16),
+                                    e4m3x2_to_f16x2(cw.y), e4m3x2_to_f16x2(cw.y >> 16));
+        const uint4 o1 = make_uint4(e4m3x2_to_f16x2(cw.z), e4m3x2_to_f16x2(cw.z >> 16),
+                                    e4m3x2_to_f16x2(cw.w), e4m3x2_to_f16x2(cw.w >> 16));
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst0 + sw_off(row, 2 * lane)),
+                     "r"(o0.x), "r"(o0.y), "r"(o0.z), "r"(o0.w) : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst0 + sw_off(row, 2 * lane + 1)),
+                     "r"(o1.x), "r"(o1.y), "r"(o1.z), "r"(o1.w) : "memory");
+      }
+      if (score) {  // rope columns: 4 lanes a row
+        const int row = pw * kRowsPerWarp + (lane >> 2), c = lane & 3;
+        uint4 cw;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                     : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
+                     : "r"(src0 + row * stg_row + DV + c * 16));
+        const uint4 o0 = make_uint4(e4m3x2_to_f16x2(cw.x), e4m3x2_to_f16x2(cw.x >> 16),
+                                    e4m3x2_to_f16x2(cw.y), e4m3x2_to_f16x2(cw.y >> 16));
+        const uint4 o1 = make_uint4(e4m3x2_to_f16x2(cw.z), e4m3x2_to_f16x2(cw.z >> 16),
+                                    e4m3x2_to_f16x2(cw.w), e4m3x2_to_f16x2(cw.w >> 16));
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst0 + sw_off(row, 64 + 2 * c)),
+                     "r"(o0.x), "r"(o0.y), "r"(o0.z), "r"(o0.w) : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n"
+                     ::"r"(dst0 + sw_off(row, 64 + 2 * c + 1)),
+                     "r"(o1.x), "r"(o1.y), "r"(o1.z), "r"(o1.w) : "memory");
+      }
+      fence_proxy_async();  // generic writes -> the tensor core's reads
+      mbar_arrive(bar(FULL + s));
+      return true;
+    };
+    int prev_pos = -1;  // fp8: the key of this lane's row in the tile being widened
+    bool ok_all = true;
     for (int jj = 0; jj < n_kv; ++jj) {
-      const int s = jj % NSTG;
+      const int s = jj % NS;
       E[kLagP + kLagE] = entry(jj + kAhead + kLagP + kLagE);
       G[kLagP] = page(E[kLagP]);
       rr[kAhead] = res(E[0], G[0]);
-      int ok = 1;
-      if (lane == 0 && jj >= NSTG)
-        ok = mbar_wait_sleep(bar(EMPTY + s), ((jj / NSTG) & 1) ^ 1) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
-        break;
-      }
-      const uint32_t dst0 = ring + s * tile_bytes;
-      if (score && own) {
-        const int pos = rr[0].pos;
-        const bool vis = pos >= 0 && !(use_upper && pos > i_pos) && pos >= lo_r;
-        sBias[s * BK + myrow] = vis ? 0.f : -INFINITY;
-      }
       // the warp's 8 row offsets, broadcast once (shuffles share the pipe
       // with the copies and barrier polls); skipped keys read zeros
       int64_t ro[kRowsPerWarp];
 #pragma unroll
       for (int r = 0; r < kRowsPerWarp; ++r) ro[r] = __shfl_sync(0xffffffffu, rr[0].off, r);
-      // value chunks 0-7: half a row (512 B) per instruction, row known at
-      // compile time
+      if (FP8) {
+        const uint32_t stg = stg0 + (jj & 1) * (BK * stg_row);
 #pragma unroll
-      for (int i = 0; i < 2 * kRowsPerWarp; ++i) {
-        const int rl = i >> 1;
-        const int c = lane + 32 * (i & 1);
-        const bf16 *src = ro[rl] >= 0 ? p.k + ro[rl] + c * 8 : p.k;
-        cp_async16(dst0 + sw_off(pw * kRowsPerWarp + rl, c), src, ro[rl] >= 0 ? 16 : 0);
-      }
-      if (score) {
-        // the rope chunk (8): 4 rows per instruction
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int rl = (lane >> 3) + 4 * i;
-          const int c = (NCH - 1) * 8 + (lane & 7);
+        for (int rl = 0; rl < kRowsPerWarp; ++rl)  // 512 codes of a row per instruction
+          cp_async16(stg + (pw * kRowsPerWarp + rl) * stg_row + lane * 16,
+                     ro[rl] >= 0 ? k8 + ro[rl] + lane * 16 : k8, ro[rl] >= 0 ? 16 : 0);
+        if (score) {  // the 64 rope codes: 8 rows per instruction
+          const int rl = lane >> 2, c = lane & 3;
           const int64_t r8 = __shfl_sync(0xffffffffu, rr[0].off, rl);
-          const bf16 *src = r8 >= 0 ? p.k + r8 + c * 8 : p.k;
-          cp_async16(dst0 + sw_off(pw * kRowsPerWarp + rl, c), src, r8 >= 0 ? 16 : 0);
+          cp_async16(stg + (pw * kRowsPerWarp + rl) * stg_row + DV + c * 16,
+                     r8 >= 0 ? k8 + r8 + DV + c * 16 : k8, r8 >= 0 ? 16 : 0);
         }
+        cp_async_commit();
+        if (jj >= 1 && !widen(jj - 1, prev_pos, false)) {
+          ok_all = false;
+          break;
+        }
+        prev_pos = rr[0].pos;
+      } else {
+        int ok = 1;
+        if (lane == 0 && jj >= NS)
+          ok = mbar_wait_sleep(bar(EMPTY + s), ((jj / NS) & 1) ^ 1) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          ok_all = false;
+          break;
+        }
+        const uint32_t dst0 = ring + s * tile_bytes;
+        if (score && own) sBias[s * BK + myrow] = key_bias(rr[0].pos);
+        // value chunks 0-7: half a row (512 B) per instruction, row known at
+        // compile time
+#pragma unroll
+        for (int i = 0; i < 2 * kRowsPerWarp; ++i) {
+          const int rl = i >> 1;
+          const int c = lane + 32 * (i & 1);
+          const bf16 *src = ro[rl] >= 0 ? p.k + ro[rl] + c * 8 : p.k;
+          cp_async16(dst0 + sw_off(pw * kRowsPerWarp + rl, c), src, ro[rl] >= 0 ? 16 : 0);
+        }
+        if (score) {
+          // the rope chunk (8): 4 rows per instruction
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int rl = (lane >> 3) + 4 * i;
+            const int c = (NCH - 1) * 8 + (lane & 7);
+            const int64_t r8 = __shfl_sync(0xffffffffu, rr[0].off, rl);
+            const bf16 *src = r8 >= 0 ? p.k + r8 + c * 8 : p.k;
+            cp_async16(dst0 + sw_off(pw * kRowsPerWarp + rl, c), src, r8 >= 0 ? 16 : 0);
+          }
+        }
+        cp_async_arrive(bar(FULL + s));
+        mbar_arrive(bar(FULL + s));
       }
-      cp_async_arrive(bar(FULL + s));
-      mbar_arrive(bar(FULL + s));
 #pragma unroll
       for (int k = 0; k < kAhead; ++k) rr[k] = rr[k + 1];
 #pragma unroll
@@ -333,15 +420,18 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
 #pragma unroll
       for (int k = 0; k < kLagP; ++k) G[k] = G[k + 1];
     }
+    if (FP8 && ok_all && n_kv >= 1 && !widen(n_kv - 1, prev_pos, true)) ok_all = false;
+    if (!ok_all && lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
     cp_async_wait_all();
   } else if (warp == kMmaWarp) {
     // ================================== MMA ==================================
     if (lane == 0 && score) {
-      constexpr uint32_t kIdescQK = idesc_bf16(H, BK, false);
+      // fp8 cache: f16 operands (codes widened exactly, q rounded to e4m3)
+      constexpr uint32_t kIdescQK = FP8 ? idesc_f16(H, BK, false) : idesc_bf16(H, BK, false);
       bool ok = n_kv == 0 || mbar_wait_sleep(bar(Q_TMEM), 0);
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j % NSTG, bb = j & 1;
-        ok = mbar_wait_sleep(bar(FULL + s), (j / NSTG) & 1) &&
+        const int s = j % NS, bb = j & 1;
+        ok = mbar_wait_sleep(bar(FULL + s), (j / NS) & 1) &&
              (j < 2 || mbar_wait_sleep(bar(S_FREE + bb), ((j >> 1) - 1) & 1));
         if (!ok) break;
         fence_proxy_async();
@@ -360,12 +450,12 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
       }
       if (!ok) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
     } else if (lane == 0) {
-      constexpr uint32_t kIdescPV = idesc_bf16(H, 256, true);
+      constexpr uint32_t kIdescPV = FP8 ? idesc_f16(H, 256, true) : idesc_bf16(H, 256, true);
       bool ok = true;
       int n_corr = 0;
       for (int j = 0; j < n_kv; ++j) {
-        const int s = j % NSTG, bb = j & 1;
-        ok = mbar_wait_sleep(bar(FULL + s), (j / NSTG) & 1) &&
+        const int s = j % NS, bb = j & 1;
+        ok = mbar_wait_sleep(bar(FULL + s), (j / NS) & 1) &&
              mbar_wait_cluster_sleep(bar(P_FULL + bb), (j >> 1) & 1);
         if (!ok) break;
         // did the score CTA raise any head's reference max for this tile?
@@ -419,7 +509,8 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
   } else if (score) {
     // ============================ softmax (score CTA) ============================
     const int row = tid;  // head = TMEM lane
-    const float c = p.scale_log2;
+    // softmax scale (log2 domain), times the request's k_descale (fp8)
+    const float c = p.scale_log2 * ((FP8 && p.k_descale != nullptr) ? p.k_descale[b] : 1.f);
     float m_ref = -INFINITY;
     float l = 0.f;
     bool ok = true;
@@ -446,6 +537,12 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
             r[4 * i + 2] = w[8 * k + i].z;
             r[4 * i + 3] = w[8 * k + i].w;
           }
+          if (FP8) {  // q rounded to e4m3 (the cache's type), held as f16 pairs
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              r[i] = e4m3x2_to_f16x2(round_e4m3x2(__uint_as_float(r[i] << 16),
+                                                  __uint_as_float(r[i] & 0xffff0000u)));
+          }
           tmem_st32u(tmem + kTmQ + lane_off + (cb0 + k) * 32, r);
         }
       }
@@ -456,9 +553,9 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
     }
     const float *sBias = reinterpret_cast<const float *>(smem + Smem::kBias);
     for (int jj = 0; jj < n_kv; ++jj) {
-      const int s = jj % NSTG, bb = jj & 1;
+      const int s = jj % NS, bb = jj & 1;
       if (!(ok = mbar_wait_sleep(bar(S_FULL + bb), (jj >> 1) & 1) &&
-                 mbar_wait_sleep(bar(FULL + s), (jj / NSTG) & 1)))
+                 mbar_wait_sleep(bar(FULL + s), (jj / NS) & 1)))
         break;
       tc_fence_after();
       float x[BK];
@@ -510,10 +607,17 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
 #pragma unroll
       for (int cc = 0; cc < BK / 8; ++cc) {
         uint4 w;
-        w.x = pack_bf16(x[8 * cc], x[8 * cc + 1]);
-        w.y = pack_bf16(x[8 * cc + 2], x[8 * cc + 3]);
-        w.z = pack_bf16(x[8 * cc + 4], x[8 * cc + 5]);
-        w.w = pack_bf16(x[8 * cc + 6], x[8 * cc + 7]);
+        if (FP8) {  // the value CTA's PV runs on f16
+          w.x = pack_f16(x[8 * cc], x[8 * cc + 1]);
+          w.y = pack_f16(x[8 * cc + 2], x[8 * cc + 3]);
+          w.z = pack_f16(x[8 * cc + 4], x[8 * cc + 5]);
+          w.w = pack_f16(x[8 * cc + 6], x[8 * cc + 7]);
+        } else {
+          w.x = pack_bf16(x[8 * cc], x[8 * cc + 1]);
+          w.y = pack_bf16(x[8 * cc + 2], x[8 * cc + 3]);
+          w.z = pack_bf16(x[8 * cc + 4], x[8 * cc + 5]);
+          w.w = pack_bf16(x[8 * cc + 6], x[8 * cc + 7]);
+        }
         st_cluster_v4(dst + p_off(row, cc), w);
       }
       const uint32_t fac = dst + kPTile + warp * kFacWarp;
@@ -582,7 +686,10 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
     if (!ok && lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
     const float2 fl = ok ? reinterpret_cast<const float2 *>(smem + Smem::kFin)[row]
                          : make_float2(0.f, -INFINITY);
-    const float inv = fl.x, lse_nat = fl.y;
+    // v_descale of the request multiplies the output (and every partial:
+    // the merge is linear)
+    const float inv = fl.x * ((FP8 && p.v_descale != nullptr) ? p.v_descale[b] : 1.f);
+    const float lse_nat = fl.y;
     const int64_t rows_total = static_cast<int64_t>(p.total_q) * p.h_q;
     const int64_t grow = static_cast<int64_t>(t) * p.h_q + row;
     const bool split_mode = p.num_splits > 1;
@@ -688,13 +795,18 @@ int launch_mla_topk(const AttnParams &p, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(mla_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mla_topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Smem::kDynamic)) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Smem::kDynamic)) != cudaSuccess)
       return PKV_ERR_CUDA;
     if (dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   dim3 grid(2 * p.num_splits, 1, p.total_q);
-  mla_topk_kernel<<<grid, NTHREADS, Smem::kDynamic, stream>>>(p);
+  if (p.kv_fp8)
+    mla_topk_kernel<true><<<grid, NTHREADS, Smem::kDynamic, stream>>>(p);
+  else
+    mla_topk_kernel<false><<<grid, NTHREADS, Smem::kDynamic, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

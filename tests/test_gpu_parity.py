@@ -793,6 +793,38 @@ def test_mla_topk_decode_reduced(num_splits):
     assert pkv.get_error_flags() == 0
 
 
+@pytest.mark.parametrize("num_splits", [1, 3, 0])
+def test_mla_topk_fp8(num_splits):
+    """Absorbed MLA over an fp8 latent cache: the codes gathered and widened
+    to f16 inside the kernel, q rounded to e4m3, per-request k / v descales;
+    top-k lists with -1 padding, a duplicate and an out-of-range entry
+    (skipped and flagged); against the fp8 oracle."""
+    wl = _mla_reduced()
+    wl.topk_indices[:, -37:] = -1
+    wl.topk_indices[2, 5] = wl.topk_indices[2, 6]
+    wl.topk_indices[4, 9] = int(wl.cache_seqlens[0]) + 5  # past kv_len
+    B = wl.cache_seqlens.shape[0]
+    k8 = wl.k_cache.float().to(torch.float8_e4m3fn)
+    gen = torch.Generator().manual_seed(31 + num_splits)
+    kd = torch.rand(B, 1, generator=gen) * 1.5 + 0.5
+    vd = torch.rand(B, 1, generator=gen) * 1.5 + 0.5
+    g = wl.to(DEV)
+    k8d = k8.to(DEV)
+    out, lse = pkv.attn_with_kvcache_fp8(
+        g.q, k8d, k8d[..., :512], g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+        g.max_seqlen_q, g.scale, topk_indices=g.topk_indices, k_descale=kd.to(DEV),
+        v_descale=vd.to(DEV), num_splits=num_splits, return_softmax_lse=True)
+    torch.cuda.synchronize()
+    codes = k8.view(torch.uint8).numpy()
+    ref_o, ref_l, skipped = oracle.attention_fp8(
+        oracle.bf16_bits(wl.q), codes, codes[..., :512], wl.page_table.numpy(),
+        wl.cache_seqlens.numpy(), wl.cu_seqlens_q.numpy(), wl.scale, k_descale=kd.numpy(),
+        v_descale=vd.numpy(), topk=wl.topk_indices.numpy())
+    assert skipped > 0
+    check_close(out, lse, ref_o, ref_l, f"mla fp8 splits={num_splits}")
+    assert pkv.get_error_flags() == pkv.EFLAG_TOPK_OOB
+
+
 @pytest.mark.parametrize("num_splits", [1, 3])
 def test_mla_topk_reference_max_rises(num_splits):
     """Scores that grow along the list (rope parts of later tiles' keys scaled up) make

@@ -885,6 +885,62 @@ def test_fp8_per_request_descales_against_scipy():
                 assert abs(lse[t, h] - l) < 1e-12
 
 
+def _topk_lists(rng, cu, kv_lens, width):
+    """Per token: a random subset of its request's positions in random order,
+    one repeated position, one position past kv_len, -1 padding."""
+    total_q = int(cu[-1])
+    tk = np.full((total_q, width), -1, np.int32)
+    for b, n in enumerate(kv_lens):
+        for t in range(int(cu[b]), int(cu[b + 1])):
+            k = int(rng.integers(1, n + 1))
+            sel = list(rng.permutation(n)[:k])
+            sel = sel + [sel[0], n + 3]
+            tk[t, :len(sel)] = np.array(sel[:width], np.int32)
+    return tk
+
+
+def test_fp8_topk_full_list_equals_dense_fp8():
+    """A top-k list that names every position once (in any order, -1
+    padded) gives the dense fp8 attention."""
+    rng = np.random.default_rng(95)
+    q_lens, kv_lens = [1, 2], [7, 12]
+    c, kc, vc = _fp8_case(rng, q_lens, kv_lens, 4)
+    tk = np.full((3, 16), -1, np.int32)
+    for b, n in enumerate(kv_lens):
+        for t in range(int(c["cu"][b]), int(c["cu"][b + 1])):
+            tk[t, :n] = rng.permutation(n)
+    kd = rng.uniform(0.5, 2.0, (2, 2)).astype(np.float32)
+    vd = rng.uniform(0.5, 2.0, (2, 2)).astype(np.float32)
+    o1, l1, _ = oracle.attention_fp8(c["qb"], kc, vc, c["pt"], c["kv"], c["cu"], 0.4,
+                                     k_descale=kd, v_descale=vd, topk=tk)
+    o2, l2, _ = oracle.attention_fp8(c["qb"], kc, vc, c["pt"], c["kv"], c["cu"], 0.4,
+                                     k_descale=kd, v_descale=vd)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, atol=1e-12)
+
+
+def test_fp8_topk_equals_bf16_topk_on_the_widened_values():
+    """With unit descales, fp8 attention over top-k lists (repeats, -1,
+    positions past kv_len, causal) equals the bf16-path attention over the
+    same lists on the widened codes and q rounded to e4m3, with V the first
+    columns of the K rows as for absorbed MLA; the skipped entries agree."""
+    rng = np.random.default_rng(96)
+    q_lens, kv_lens, P = [1, 3, 2], [9, 20, 5], 4
+    c, kc, _ = _fp8_case(rng, q_lens, kv_lens, P, h_q=4, h_kv=1, d=24)
+    vc = kc[..., :16]
+    tk = _topk_lists(rng, c["cu"], kv_lens, 24)
+    q8 = torch.from_numpy(c["qf"].astype(np.float32)).to(torch.float8_e4m3fn).float()
+    kb = _codes_to_bf16_bits(kc)
+    out, lse, sk = oracle.attention_fp8(c["qb"], kc, vc, c["pt"], c["kv"], c["cu"], 0.3,
+                                        causal=True, topk=tk)
+    ref_o, ref_l, ref_sk = oracle.attention(oracle.bf16_bits(q8.to(torch.bfloat16)), kb,
+                                            kb[..., :16], c["pt"], c["kv"], c["cu"], 0.3,
+                                            causal=True, topk=tk, d_v=16)
+    np.testing.assert_allclose(out, ref_o, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_l, atol=1e-12)
+    assert sk > 0 and sk == ref_sk * 4  # (per row here, per token's head 0 there)
+
+
 # ------------------------------------------------- KV write into an fp8 pool
 
 @pytest.mark.parametrize("scale", [1.0, 0.05, 0.3, 7.0])
