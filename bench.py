@@ -50,6 +50,11 @@ L2_BYTES = 129 * 1024 * 1024
 # kernel as it is now; a kernel changed since its capture has no entry (its
 # traffic is reported as null).
 MEASURED_TRAFFIC = {
+    ("gqa_split_decode", "decode_allheads_kernel (page boxes, fixed splits)"): 1_116_558_400,
+    ("swa_decode", "decode_allheads_kernel (slot rows)"): 647_964_416,
+    ("varlen_extend", "extend_tc_kernel"): 264_708_352,
+    ("mla_topk_decode", "mla_topk_kernel"): 335_132_160,
+    ("tiny_decode", "decode_short_kernel"): 583_680,  # its 2 MB of K / V sit in L2
 }
 
 
