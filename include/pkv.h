@@ -488,6 +488,19 @@ int pkv_clear_error_flags(void);
 /* Library version, for the bindings' sanity check. */
 int pkv_version(void);
 
+/*
+ * pkv_check_bounded_wait -- exercises the expiry path of the library's
+ * bounded in-kernel waits (no construct of the pages: every pipeline wait
+ * of these kernels gives up after about 2^31 SM cycles, about a second at
+ * full clock, sets PKV_EFLAG_TIMEOUT and lets the kernel return instead of
+ * hanging).  Launches one CTA whose two waiters (the sleeping wait and its
+ * cluster-scope variant) wait on a barrier that nothing arrives on; both
+ * expire, the flag is set and the kernel ends, leaving the context usable.
+ * Asynchronous on `stream`; read the flag after synchronising.  Returns
+ * PKV_OK or PKV_ERR_CUDA (launch failure).
+ */
+int pkv_check_bounded_wait(cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,6 +40,7 @@ import torch
 from ._build import build_library, lib_path
 
 __all__ = [
+    "check_bounded_wait",
     "cascade_attn_with_kvcache",
     "attn_with_kvcache",
     "attn_workspace_size",
@@ -99,6 +100,7 @@ EXPORTED_SYMBOLS = (
     "pkv_attn_with_kvcache_fp8",
     "pkv_set_kv_buffer_fp8",
     "pkv_append_attn_with_kvcache",
+    "pkv_check_bounded_wait",
 )
 
 _FP8 = 5
@@ -165,6 +167,7 @@ def load_library(path: str | None = None):
     lib.pkv_get_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.pkv_clear_error_flags.argtypes = []
     lib.pkv_version.argtypes = []
+    lib.pkv_check_bounded_wait.argtypes = [c_void_p]
     for name in EXPORTED_SYMBOLS:
         getattr(lib, name).restype = ctypes.c_int
     _LIB = lib
@@ -540,3 +543,13 @@ def get_error_flags() -> int:
 
 def clear_error_flags() -> None:
     _check("pkv_clear_error_flags", load_library().pkv_clear_error_flags())
+
+
+def check_bounded_wait(stream=None) -> None:
+    """pkv_check_bounded_wait: one CTA waits on a barrier that nothing
+    arrives on through the library's bounded waits; they expire after about
+    a second and set EFLAG_TIMEOUT (asynchronous; synchronise, then read
+    get_error_flags)."""
+    lib = load_library()
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check("pkv_check_bounded_wait", lib.pkv_check_bounded_wait(ctypes.c_void_p(s.cuda_stream)))

@@ -295,9 +295,38 @@ int plan_attention(const pkv_tensor &q, const pkv_tensor &k,
 
 using namespace pkv;
 
+namespace pkv {
+namespace {
+// One CTA whose warps wait on a barrier that nothing arrives on: thread 0
+// through the bounded sleeping wait every pipeline wait of the library
+// uses, thread 32 through its cluster-scope variant.  Each gives up after
+// its bound, records the expiry in the error word and returns.
+__global__ void bounded_wait_check_kernel(uint32_t *err) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = ptx::smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(b, 1);
+    ptx::mbar_init_fence();
+  }
+  __syncthreads();
+  bool ok = true;
+  if (threadIdx.x == 0) ok = ptx::mbar_wait_sleep(b, 0);
+  else if (threadIdx.x == 32) ok = ptx::mbar_wait_cluster_sleep(b, 0);
+  if (!ok) atomicOr(err, PKV_EFLAG_TIMEOUT);
+}
+}  // namespace
+}  // namespace pkv
+
 extern "C" {
 
 int pkv_version(void) { return 1; }
+
+int pkv_check_bounded_wait(cudaStream_t stream) {
+  uint32_t *err = device_error_word();
+  if (err == nullptr) return PKV_ERR_CUDA;
+  pkv::bounded_wait_check_kernel<<<1, 64, 0, stream>>>(err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
 
 int pkv_get_error_flags(uint32_t *flags) {
   if (flags == nullptr) return PKV_ERR_INVALID_ARG;

@@ -11,8 +11,6 @@
 namespace pkv {
 namespace ptx {
 
-constexpr uint32_t kWaitLimit = 1u << 24;  // bounded mbarrier polls
-
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -31,23 +29,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
                : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase with the given parity; false on expiry.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
 }
 // try_wait with a suspend-time hint: the warp sleeps in hardware until the
 // phase completes (or the hint runs out) instead of re-issuing the poll.
@@ -72,40 +53,8 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
     if (clock64() - t0 > kSleepWaitCycles) return false;
   }
 }
-// Bounded wait by lane 0 of the calling warp, result broadcast to the warp:
-// the other lanes do not poll the barrier (polling threads compete with the
-// warp's loads for the shared-memory pipe).  Memory seen by lane 0 is visible
-// to the warp after the __syncwarp.  sleep_ns > 0 adds a back-off between
-// polls, for waits that are long by design.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
-                                               uint32_t sleep_ns = 0) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) {
-    ok = 0;
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
-      if (mbar_try_wait(bar, parity)) {
-        ok = 1;
-        break;
-      }
-      if (sleep_ns) __nanosleep(sleep_ns);
-    }
-  }
-  __syncwarp();
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
 // The same with acquire at cluster scope: for phases completed by another
-// CTA of the cluster (remote bulk copies, remote MMA-completion arrivals).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
+// CTA of the cluster (remote stores and arrivals).
 __device__ __forceinline__ bool mbar_wait_cluster_sleep(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
   while (true) {
@@ -120,17 +69,6 @@ __device__ __forceinline__ bool mbar_wait_cluster_sleep(uint32_t bar, uint32_t p
     if (ok) return true;
     if (clock64() - t0 > kSleepWaitCycles) return false;
   }
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-  return false;
-}
-__device__ __forceinline__ bool mbar_wait_cluster_warp(uint32_t bar, uint32_t parity) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait_cluster(bar, parity) ? 1 : 0;
-  __syncwarp();
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // -------------------------------------------------------------- clusters

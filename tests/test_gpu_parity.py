@@ -1612,3 +1612,28 @@ def test_fp8_write_then_attend():
         k_descale=np.full((B, h_kv), ks, np.float32), v_descale=np.full((B, h_kv), vs, np.float32))
     check_close(out, lse, ref_o, ref_l, "fp8 write then attend")
     assert pkv.get_error_flags() == 0
+
+
+# ------------------------------------------------ bounded in-kernel waits
+
+def test_bounded_wait_expires_and_the_context_stays_usable():
+    """The expiry path of the library's bounded waits, exercised without a
+    fault: a CTA waits on a barrier that nothing arrives on, both wait
+    flavours give up after their bound (about a second), PKV_EFLAG_TIMEOUT
+    is set, the kernel ends, and the next attention call on the same
+    context is correct and raises no flag."""
+    import time
+    pkv.clear_error_flags()
+    t0 = time.perf_counter()
+    pkv.check_bounded_wait()
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert pkv.get_error_flags() == pkv.EFLAG_TIMEOUT
+    assert 0.2 < waited < 30.0, waited
+    pkv.clear_error_flags()
+    wl = workloads.make("tiny_decode", batch=3, len_lo=5, len_hi=120)
+    g = wl.to(DEV)
+    out, lse = gpu_attn(g, num_splits=1)
+    ref_o, ref_l, _ = oracle_attn(wl)
+    check_close(out, lse, ref_o, ref_l, "after an expired wait")
+    assert pkv.get_error_flags() == 0
