@@ -54,7 +54,7 @@ MEASURED_TRAFFIC = {
     ("swa_decode", "decode_allheads_kernel (slot rows)"): 647_964_416,
     ("varlen_extend", "extend_tc_kernel"): 264_708_352,
     ("mla_topk_decode", "mla_topk_kernel"): 335_132_160,
-    ("tiny_decode", "decode_short_kernel"): 583_680,  # its 2 MB of K / V sit in L2
+    ("tiny_decode", "decode_short_cluster_kernel"): 586_496,  # its 2 MB of K / V sit in L2
 }
 
 
@@ -260,6 +260,9 @@ class Step:
         rows = g.max_seqlen_q * (g.q.shape[1] // h_kv)
         if (g.topk_indices is None and g.q.shape[-1] == 128 and rows <= 16
                 and g.num_splits <= 1 and self.pt.shape[1] * p <= 256):
+            # a 4-CTA cluster per (request, KV head) up to 76 pairs
+            if g.cache_seqlens.shape[0] * h_kv <= 76:
+                return "decode_short_cluster_kernel"
             return "decode_short_kernel"
         if g.topk_indices is None and g.q.shape[-1] == 128 and h_kv <= 8 and rows <= 16:
             if p < 8:

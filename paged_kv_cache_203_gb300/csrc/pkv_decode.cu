@@ -80,6 +80,12 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0,
       : "r"(addr));
 }
 
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t &r0, uint32_t &r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
 // D(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col)
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0,
                                          uint32_t a1, uint32_t a2, uint32_t a3,
@@ -1901,6 +1907,8 @@ decode_short_kernel(const __grid_constant__ AttnParams p) {
   const uint32_t kw = sbase + static_cast<uint32_t>(warp * SD_KEYS * SD_PITCH);
   const uint32_t vw = kw + static_cast<uint32_t>(SD_WARPS * SD_KEYS * SD_PITCH);
   const int g = lane >> 2, tq = lane & 3;
+  griddep_wait();  // launched with programmatic serialization
+  griddep_launch_dependents();
 
   // ---- lengths and this lane's page id, loaded together ----
   const int j = warp * SD_KEYS + lane;  // this lane's key
@@ -2111,6 +2119,279 @@ decode_short_kernel(const __grid_constant__ AttnParams p) {
   }
 }
 
+// ============================================================================
+// Short decode on a cluster (the same calls as decode_short_kernel, for
+// batches of few (request, KV head) pairs): the SC_CTAS CTAs of a cluster
+// share one pair.  Rank r scores keys [64r, 64r + 64), one 16-key block per
+// warp, and computes output columns [32r, 32r + 32) of P V over all the
+// pair's keys, so each CTA copies a quarter of the K rows and a quarter of
+// every V row (the copies of one SM were the step's longest part).  A warp
+// stores its block's P (bf16, as mma A fragments) and each row's block max m
+// and sum l into every CTA of the cluster; after one cluster barrier, warp w
+// of rank r forms its 8 output columns as sum_b 2^(m_b - M) (P_b V_b) with M
+// the row's max over blocks -- the split-softmax identity of the state
+// merge, applied per 16-key block -- so no CTA waits for another's max
+// before its exponentials, and only P and (m, l) cross the cluster.
+// ============================================================================
+
+constexpr int SC_CTAS = 4;
+constexpr int SC_WARPS = 4;
+constexpr int SC_KEYS = kDecodeShortMaxKeys;       // 256: the whole table row
+constexpr int SC_BLOCKS = SC_KEYS / 16;            // 16-key blocks
+constexpr int SC_KPITCH = 128 * 2 + 16;            // K row, skewed: conflict-free ldmatrix
+constexpr int SC_VCOLS = 128 / SC_CTAS;            // value columns per CTA
+constexpr int SC_VPITCH = SC_VCOLS * 2 + 16;       // 80 B: conflict-free ldmatrix
+static_assert(SC_CTAS * SC_WARPS * 16 == SC_KEYS, "one 16-key block per warp");
+static_assert(SC_WARPS * 8 == SC_VCOLS, "8 output columns per warp");
+static_assert(SC_WARPS * 32 * 2 == SC_KEYS, "each thread resolves two keys");
+struct ScSmem {
+  static constexpr uint32_t kK = 0;                               // [64 keys][KPITCH]
+  static constexpr uint32_t kV = kK + SC_WARPS * 16 * SC_KPITCH;  // [256 keys][VPITCH]
+  static constexpr uint32_t kP = kV + SC_KEYS * SC_VPITCH;        // uint4 [blocks][32 lanes]
+  static constexpr uint32_t kML = kP + SC_BLOCKS * 32 * 16;       // float4 [blocks][8]
+  static constexpr uint32_t kVoff = kML + SC_BLOCKS * 8 * 16;     // int64 [256]
+  static constexpr uint32_t kKoff = kVoff + SC_KEYS * 8;          // int64 [64]
+  static constexpr uint32_t kLive = kKoff + SC_WARPS * 16 * 8;    // uint32 [8]: key bits
+  static constexpr uint32_t kEnd = kLive + 8 * 4;
+};
+static_assert(ScSmem::kV % 16 == 0 && ScSmem::kP % 16 == 0 && ScSmem::kML % 16 == 0 &&
+                  ScSmem::kVoff % 8 == 0,
+              "aligned short-cluster areas");
+
+__global__ void __cluster_dims__(SC_CTAS, 1, 1) __launch_bounds__(SC_WARPS * 32, 1)
+decode_short_cluster_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int h = blockIdx.x / SC_CTAS;  // KV head
+  const int b = blockIdx.y;            // request
+  const uint32_t sbase = smem_addr(smem);
+  const int g = lane >> 2, tq = lane & 3;
+  griddep_wait();  // launched with programmatic serialization
+  griddep_launch_dependents();
+
+  // ---- lengths and page ids, loaded together: keys tid and tid + 128 (V
+  // columns of every key), key 64 * rank + tid (K rows of this rank) ----
+  const int64_t prow = static_cast<int64_t>(b) * p.pt_stride;
+  const int j0 = tid, j1 = tid + SC_WARPS * 32;
+  const int jk = rank * SC_WARPS * 16 + (tid & 63);
+  const int pi0 = j0 / p.page_size, pi1 = j1 / p.page_size, pik = jk / p.page_size;
+  const int pg0 = pi0 < p.pt_cols ? p.page_table[prow + pi0] : -1;
+  const int pg1 = pi1 < p.pt_cols ? p.page_table[prow + pi1] : -1;
+  const int pgk = (tid < 64 && pik < p.pt_cols) ? p.page_table[prow + pik] : -1;
+  const int q_begin = p.cu_seqlens_q[b];
+  const int q_len = p.cu_seqlens_q[b + 1] - q_begin;
+  const int kv_len = p.cache_seqlens[b];
+  if (q_len <= 0 || q_begin < 0 || q_begin + q_len > p.total_q) return;  // the whole cluster
+  cluster_arrive_relaxed();  // its wait precedes the first store into a peer
+  const int n_rows = min(q_len, p.max_seqlen_q) * p.group;  // <= 16
+  const int hi = max(kv_len, 0);
+  const int lo = p.window_left >= 0 ? max(0, kv_len - q_len - p.window_left) : 0;
+  auto key_live = [&](int j, int pidx, int pg, bool report) {
+    bool live = j >= lo && j < hi;
+    if (live && pidx >= p.pt_cols) {
+      if (report) atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
+      live = false;
+    }
+    if (live && (pg < 0 || pg >= p.num_pages)) {
+      if (report) atomicOr(p.err, PKV_EFLAG_PAGE_OOB);
+      live = false;
+    }
+    return live;
+  };
+  const bool live0 = key_live(j0, pi0, pg0, rank == 0);
+  const bool live1 = key_live(j1, pi1, pg1, rank == 0);
+  const bool livek = tid < 64 && key_live(jk, pik, pgk, false);
+  int64_t *sVoff = reinterpret_cast<int64_t *>(smem + ScSmem::kVoff);
+  int64_t *sKoff = reinterpret_cast<int64_t *>(smem + ScSmem::kKoff);
+  uint32_t *sLive = reinterpret_cast<uint32_t *>(smem + ScSmem::kLive);
+  const int64_t vcol = static_cast<int64_t>(h) * p.v_sh + rank * SC_VCOLS;
+  sVoff[j0] = live0 ? pg0 * p.v_sp + static_cast<int64_t>(j0 - pi0 * p.page_size) * p.v_spos + vcol : -1;
+  sVoff[j1] = live1 ? pg1 * p.v_sp + static_cast<int64_t>(j1 - pi1 * p.page_size) * p.v_spos + vcol : -1;
+  if (tid < 64)
+    sKoff[tid] = livek ? pgk * p.k_sp + static_cast<int64_t>(jk - pik * p.page_size) * p.k_spos +
+                             static_cast<int64_t>(h) * p.k_sh
+                       : -1;
+  {
+    const uint32_t w0 = __ballot_sync(0xffffffffu, live0), w1 = __ballot_sync(0xffffffffu, live1);
+    if (lane == 0) {
+      sLive[warp] = w0;             // keys 32 * warp + lane
+      sLive[SC_WARPS + warp] = w1;  // keys 128 + 32 * warp + lane
+    }
+  }
+  __syncthreads();
+  uint32_t blk = 0;  // bit i: 16-key block i holds a live key
+#pragma unroll
+  for (int i = 0; i < SC_KEYS / 32; ++i) {
+    const uint32_t w = sLive[i];
+    blk |= ((w & 0xffffu) != 0u ? 1u : 0u) << (2 * i);
+    blk |= ((w >> 16) != 0u ? 1u : 0u) << (2 * i + 1);
+  }
+
+  // ---- copies: this CTA's value columns of every key of a live block, and
+  // the K rows of its own keys (dead keys of a live block read zeros) ----
+  const uint32_t sK = sbase + ScSmem::kK, sV = sbase + ScSmem::kV;
+#pragma unroll
+  for (int it = 0; it < SC_KEYS * 4 / (SC_WARPS * 32); ++it) {  // 4 16-B chunks a key
+    const int idx = tid + SC_WARPS * 32 * it;
+    const int key = idx >> 2, c = idx & 3;
+    if ((blk >> (key >> 4)) & 1u) {
+      const int64_t off = sVoff[key];
+      cp_async16(sV + static_cast<uint32_t>(key * SC_VPITCH + c * 16),
+                 off >= 0 ? p.v + off + c * 8 : p.v, off >= 0 ? 16 : 0);
+    }
+  }
+#pragma unroll
+  for (int it = 0; it < SC_WARPS * 16 * 16 / (SC_WARPS * 32); ++it) {  // 16 chunks a row
+    const int idx = tid + SC_WARPS * 32 * it;
+    const int key = idx >> 4, c = idx & 15;
+    if ((blk >> (rank * SC_WARPS + (key >> 4))) & 1u) {
+      const int64_t off = sKoff[key];
+      cp_async16(sK + static_cast<uint32_t>(key * SC_KPITCH + c * 16),
+                 off >= 0 ? p.k + off + c * 8 : p.k, off >= 0 ? 16 : 0);
+    }
+  }
+  cp_async_commit();
+  uint32_t qf[8][4];
+  int rpos[2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int rr = g + 8 * hh;
+    const bool rv = rr < n_rows;
+    const int u = rv ? rr / p.group : 0;
+    const int gg = rv ? rr % p.group : 0;
+    rpos[hh] = kv_len - q_len + u;
+    const bf16 *qrow = p.q + static_cast<int64_t>(q_begin + u) * p.q_st +
+                       static_cast<int64_t>(h * p.group + gg) * p.q_sh;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int c0 = kk * 16 + 2 * tq;
+      qf[kk][hh] = rv ? *reinterpret_cast<const uint32_t *>(qrow + c0) : 0u;
+      qf[kk][2 + hh] = rv ? *reinterpret_cast<const uint32_t *>(qrow + c0 + 8) : 0u;
+    }
+  }
+  cp_async_wait_group<0>();
+  __syncthreads();  // rows copied by other warps
+
+  // ---- this warp's 16-key block: scores, mask, block softmax ----
+  const int blk_id = rank * SC_WARPS + warp;
+  const bool my_live = ((blk >> blk_id) & 1u) != 0u;
+  uint4 pf = make_uint4(0u, 0u, 0u, 0u);
+  float m_row[2] = {-INFINITY, -INFINITY}, l_row[2] = {0.f, 0.f};
+  if (my_live) {
+    float sc[2][4];
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+    const int key = (lane >> 4) * 8 + (lane & 7);
+    const int kc = (lane >> 3) & 1;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(sK + static_cast<uint32_t>((warp * 16 + key) * SC_KPITCH + (2 * kk + kc) * 16), b0, b1,
+              b2, b3);
+      mma_bf16(sc[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+      mma_bf16(sc[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+    }
+    const uint32_t kbits = (sLive[blk_id >> 1] >> ((blk_id & 1) * 16)) & 0xffffu;
+    const bool use_upper = p.causal || p.window_left >= 0;
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int kl = nb * 8 + 2 * tq + (e & 1);
+        const int kp = blk_id * 16 + kl;
+        const int hh = e >> 1;
+        bool masked = ((kbits >> kl) & 1u) == 0u;
+        if (use_upper && kp > rpos[hh]) masked = true;
+        if (p.window_left >= 0 && kp < rpos[hh] - p.window_left) masked = true;
+        sc[nb][e] = masked ? -INFINITY : sc[nb][e] * p.scale_log2;
+      }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float mx = fmaxf(fmaxf(sc[0][2 * hh], sc[0][2 * hh + 1]), fmaxf(sc[1][2 * hh], sc[1][2 * hh + 1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float mu = mx == -INFINITY ? 0.f : mx;
+      float sum = 0.f;
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb) {
+        sc[nb][2 * hh] = fast_exp2(sc[nb][2 * hh] - mu);
+        sc[nb][2 * hh + 1] = fast_exp2(sc[nb][2 * hh + 1] - mu);
+        sum += sc[nb][2 * hh] + sc[nb][2 * hh + 1];
+      }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      m_row[hh] = mx;
+      l_row[hh] = sum;
+    }
+    pf = make_uint4(pack_bf16(sc[0][0], sc[0][1]), pack_bf16(sc[0][2], sc[0][3]),
+                    pack_bf16(sc[1][0], sc[1][1]), pack_bf16(sc[1][2], sc[1][3]));
+  }
+
+  // ---- the block's P and (m, l) into every CTA of the cluster ----
+  cluster_wait();  // every CTA of the cluster runs
+  if (my_live) {
+    const uint32_t pl = sbase + ScSmem::kP + static_cast<uint32_t>((blk_id * 32 + lane) * 16);
+    const uint32_t ml = sbase + ScSmem::kML + static_cast<uint32_t>((blk_id * 8 + g) * 16);
+    const uint4 mlv = make_uint4(__float_as_uint(m_row[0]), __float_as_uint(m_row[1]),
+                                 __float_as_uint(l_row[0]), __float_as_uint(l_row[1]));
+#pragma unroll
+    for (int d = 0; d < SC_CTAS; ++d) {
+      st_cluster_v4(map_to_cta(pl, static_cast<uint32_t>(d)), pf);
+      if (tq == 0) st_cluster_v4(map_to_cta(ml, static_cast<uint32_t>(d)), mlv);
+    }
+  }
+  cluster_sync();  // every live block's P, m and l are in every CTA
+
+  // ---- this warp's 8 output columns over every live block ----
+  const float4 *sML = reinterpret_cast<const float4 *>(smem + ScSmem::kML);
+  const uint4 *sP = reinterpret_cast<const uint4 *>(smem + ScSmem::kP);
+  float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll 4
+  for (int i = 0; i < SC_BLOCKS; ++i)
+    if ((blk >> i) & 1u) {
+      const float4 mlb = sML[i * 8 + g];
+      M0 = fmaxf(M0, mlb.x);
+      M1 = fmaxf(M1, mlb.y);
+    }
+  float o[4] = {0.f, 0.f, 0.f, 0.f}, L0 = 0.f, L1 = 0.f;
+#pragma unroll 4
+  for (int i = 0; i < SC_BLOCKS; ++i) {
+    if (!((blk >> i) & 1u)) continue;
+    const float4 mlb = sML[i * 8 + g];
+    const uint4 a = sP[i * 32 + lane];
+    uint32_t b0, b1;
+    ldsm_x2_t(sV + static_cast<uint32_t>((i * 16 + (lane & 15)) * SC_VPITCH + warp * 16), b0, b1);
+    float t[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_bf16(t, a.x, a.y, a.z, a.w, b0, b1);
+    const float f0 = mlb.x == -INFINITY ? 0.f : fast_exp2(mlb.x - M0);
+    const float f1 = mlb.y == -INFINITY ? 0.f : fast_exp2(mlb.y - M1);
+    o[0] += f0 * t[0];
+    o[1] += f0 * t[1];
+    o[2] += f1 * t[2];
+    o[3] += f1 * t[3];
+    L0 += f0 * mlb.z;
+    L1 += f1 * mlb.w;
+  }
+  const int col = rank * SC_VCOLS + warp * 8 + 2 * tq;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int r = g + 8 * hh;
+    if (r >= n_rows) continue;
+    const float L = hh ? L1 : L0;
+    const float M = hh ? M1 : M0;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int tok = q_begin + r / p.group;
+    const int head = h * p.group + r % p.group;
+    *reinterpret_cast<uint32_t *>(p.out + static_cast<int64_t>(tok) * p.o_st +
+                                  static_cast<int64_t>(head) * p.o_sh + col) =
+        pack_bf16(o[2 * hh] * inv, o[2 * hh + 1] * inv);
+    if (p.lse != nullptr && rank == 0 && warp == 0 && tq == 0)
+      p.lse[static_cast<int64_t>(tok) * p.lse_st + static_cast<int64_t>(head) * p.lse_sh] =
+          L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+  }
+}
+
 // ------------------------------------------------------------------- host
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
@@ -2315,8 +2596,24 @@ int launch_decode_short(const AttnParams &p, cudaStream_t stream) {
       return PKV_ERR_CUDA;
     if (dev < 64) configured[dev].store(true, std::memory_order_release);
   }
-  decode_short_kernel<<<dim3(p.h_kv, p.batch), SD_WARPS * 32, SD_SMEM, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  if (static_cast<int64_t>(p.batch) * p.h_kv <= kDecodeShortClusterMaxPairs) {
+    if (p.h_kv * SC_CTAS > 65535) return PKV_ERR_UNSUPPORTED;
+    static std::atomic<bool> configured_c[64] = {};
+    if (dev >= 64 || !configured_c[dev].load(std::memory_order_acquire)) {
+      if (cudaFuncSetAttribute(decode_short_cluster_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(ScSmem::kEnd)) != cudaSuccess)
+        return PKV_ERR_CUDA;
+      if (dev < 64) configured_c[dev].store(true, std::memory_order_release);
+    }
+    const cudaError_t e = launch_programmatic(decode_short_cluster_kernel,
+                                              dim3(p.h_kv * SC_CTAS, p.batch), dim3(SC_WARPS * 32),
+                                              ScSmem::kEnd, stream, p);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  }
+  const cudaError_t e = launch_programmatic(decode_short_kernel, dim3(p.h_kv, p.batch),
+                                            dim3(SD_WARPS * 32), SD_SMEM, stream, p);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 int launch_decode_gqa(const AttnParams &p, cudaStream_t stream) {

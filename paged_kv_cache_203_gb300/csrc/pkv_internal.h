@@ -17,6 +17,27 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 #ifdef __CUDACC__
+// Launches `kernel` with programmatic stream serialization: it may be
+// scheduled while the previous kernel of the stream still runs, and must call
+// griddepcontrol.wait (ptx::griddep_wait) before its first global access.
+// Used for the short kernels of a decode step, where the launch latency of
+// the next kernel is a large part of the step.
+template <typename... Params, typename... Args>
+cudaError_t launch_programmatic(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t stream, Args &&...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // (lo, hi) rounded to e4m3 (nearest, ties to even; magnitudes past 448
 // saturate to 448): lo in the low byte of the result.
 __device__ __forceinline__ uint32_t round_e4m3x2(float lo, float hi) {
@@ -114,8 +135,11 @@ int launch_decode_allheads(const AttnParams &p, cudaStream_t stream);
 // Short decode (head dim 128, <= 16 query rows per KV head, bf16 cache, a
 // page table of at most kDecodeShortMaxKeys keys, no split): one CTA per
 // (request, KV head) with every row loaded up front and the warps' states
-// merged in shared memory; no workspace.
+// merged in shared memory; no workspace.  Batches of at most
+// kDecodeShortClusterMaxPairs (request, KV head) pairs run a 4-CTA cluster
+// per pair instead, the keys and value columns split over its CTAs.
 constexpr int kDecodeShortMaxKeys = 256;
+constexpr int kDecodeShortClusterMaxPairs = 2 * kNumSMs / 4;
 bool decode_short_eligible(const AttnParams &p);
 int launch_decode_short(const AttnParams &p, cudaStream_t stream);
 // tcgen05 varlen extend kernel (head dim 128, whole-page TMA boxes).

@@ -5,9 +5,13 @@
 #include <atomic>
 
 #include "pkv_internal.h"
+#include "pkv_ptx.cuh"
 
 namespace pkv {
 namespace {
+
+using ptx::griddep_launch_dependents;
+using ptx::griddep_wait;
 
 __device__ __forceinline__ int64_t load_index(const void *p, int is64, int i) {
   return is64 ? static_cast<const int64_t *>(p)[i]
@@ -91,6 +95,8 @@ __global__ void strided_page_table_kernel(
     const int32_t *__restrict__ rtt, int64_t rtt_stride, int64_t rtt_rows,
     int64_t rtt_cols, const void *rpi, int rpi_is_64, int page_size,
     int32_t *__restrict__ out, int64_t out_stride, int n_cols, uint32_t *err) {
+  griddep_wait();  // launched with programmatic serialization
+  griddep_launch_dependents();
   const int b = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= n_cols) return;
@@ -382,11 +388,11 @@ int launch_strided_page_table(const int32_t *rtt, int64_t rtt_stride,
                               int page_size, int32_t *out, int64_t out_stride,
                               int n_cols, uint32_t *err, cudaStream_t stream) {
   if (batch == 0 || n_cols == 0) return PKV_OK;
-  dim3 grid((n_cols + 255) / 256, batch);
-  strided_page_table_kernel<<<grid, 256, 0, stream>>>(
-      rtt, rtt_stride, rtt_rows, rtt_cols, rpi, rpi_is_64, page_size, out,
-      out_stride, n_cols, err);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  const dim3 grid((n_cols + 255) / 256, batch);
+  const cudaError_t e = launch_programmatic(strided_page_table_kernel, grid, dim3(256), 0, stream,
+                                            rtt, rtt_stride, rtt_rows, rtt_cols, rpi, rpi_is_64,
+                                            page_size, out, out_stride, n_cols, err);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 int launch_topk_to_slots(const int32_t *topk, int64_t topk_stride,

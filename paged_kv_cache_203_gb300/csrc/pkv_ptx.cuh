@@ -71,6 +71,21 @@ __device__ __forceinline__ bool mbar_wait_cluster_sleep(uint32_t bar, uint32_t p
   }
 }
 
+// ------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel of its stream is still running.  griddep_wait() blocks
+// until that kernel has completed and its writes are visible; it returns at
+// once when the launch carried no such dependency.  Every global access of
+// such a kernel comes after it.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+// Lets the next kernel of the stream (if launched with the attribute) be
+// scheduled now; it still waits in griddep_wait() for this grid to finish.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // -------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -81,6 +96,15 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n"
                "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// The two halves of cluster_sync(), for a barrier whose arrival and wait are
+// far apart: arrive (no ordering) at kernel entry, wait before the first
+// access to another CTA's shared memory, so no CTA is written before it runs.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
 }
 // Shared::cluster address of the same shared-memory offset in CTA `rank`.
 __device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t rank) {

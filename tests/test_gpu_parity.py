@@ -412,14 +412,15 @@ def test_bad_page_ids_are_skipped_and_flagged():
     (1, 64, 8, 1, -1),   # 8 rows per KV head
     (8, 16, 1, 1, 100),  # one KV head, 16 rows
     (2, 32, 8, 4, 7)])   # 4 new tokens x group 4 = 16 rows, window
-def test_short_decode(page_size, h_q, h_kv, q_len, window):
-    """Page tables of at most 256 keys, no split: the short-decode kernel (one
-    CTA per request and KV head, all rows loaded up front, the warps' states
-    merged in shared memory).  NaN in every slot outside the valid rows, an
-    empty request, an out-of-pool page id (skipped and flagged, as the oracle
-    skips it), lengths up to the table's last key; no workspace; against the
-    oracle and against the all-heads kernel with two splits."""
-    batch = 9
+@pytest.mark.parametrize("batch", [9, 80])
+def test_short_decode(page_size, h_q, h_kv, q_len, window, batch):
+    """Page tables of at most 256 keys, no split: the short-decode kernels --
+    a 4-CTA cluster per (request, KV head) for batches of at most 76 pairs
+    (batch 9), one CTA per pair above that (batch 80).  NaN in every slot
+    outside the valid rows, an empty request, an out-of-pool page id (skipped
+    and flagged, as the oracle skips it), lengths up to the table's last key;
+    no workspace; against the oracle and against the all-heads kernel with
+    two splits."""
     len_hi = 256 - 256 % page_size
     wl = workloads.make("tiny_decode", d=128, page_size=page_size, h_q=h_q, h_kv=h_kv,
                         q_len=q_len, causal=q_len > 1, window_left=window, len_lo=q_len,
