@@ -312,6 +312,14 @@ def _multi_step_ms(fn, n: int = 20, reps: int = 10) -> float:
     return ms
 
 
+def _graph_floor_ms() -> float:
+    """Time per replay of a CUDA graph holding one trivial op (a one-element
+    add), replayed back to back like the steps: the launch-rate floor under
+    a step of a few microseconds on this machine."""
+    x = torch.zeros(1, device="cuda")
+    return _timed(lambda: x.add_(1.0), reps=200)[0]
+
+
 def _timed(fn, reps: int = 20) -> tuple[float, dict]:
     """Device time of ``fn`` as a serving engine runs it: the calls captured
     once into a CUDA graph and replayed (a short call timed eagerly measures
@@ -988,8 +996,11 @@ def main():
                    if graph is not None else graph_note)
     ms = t0.elapsed_time(t1) / args.steps
     attn_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    short_step = {}
     if ms < 0.05:  # a few microseconds: eager launches time the host
         attn_ms = min(attn_ms, _timed(step.attend)[0])
+        short_step = {"ms_per_step_20_steps_per_graph": _multi_step_ms(step.run),
+                      "ms_per_replay_of_a_one_op_graph": _graph_floor_ms()}
     flags = pkv.get_error_flags()
     if dist is not None:
         t = torch.tensor([ms], device=dev)
@@ -1046,12 +1057,14 @@ def main():
                     # and the step also with 20 steps in one graph
                     kms = min(kms, _timed(s2.attend)[0])
                     how = dict(how, ms_per_step_20_steps_per_graph=_multi_step_ms(s2.run),
-                               attn_ms_20_per_graph=_multi_step_ms(s2.attend))
+                               attn_ms_20_per_graph=_multi_step_ms(s2.attend),
+                               ms_per_replay_of_a_one_op_graph=_graph_floor_ms())
                 if not ov:
                     configs[label] = config_summary(s2, kms, sms, peaks)
-                    if "ms_per_step_20_steps_per_graph" in how:
-                        configs[label]["ms_per_step_20_steps_per_graph"] = \
-                            how["ms_per_step_20_steps_per_graph"]
+                    for key in ("ms_per_step_20_steps_per_graph",
+                                "ms_per_replay_of_a_one_op_graph"):
+                        if key in how:
+                            configs[label][key] = how[key]
                 others[label] = {
                     "kernel": s2.attention_kernel(),
                     "ms_per_step": sms, "step_timing": how, "attn_ms": kms,
@@ -1106,6 +1119,8 @@ def main():
             "tokens_per_s": n_tokens * world / (ms / 1e3),
             "error_flags": flags,
         }
+        if short_step:  # a step of a few microseconds: device-side times too
+            line["short_step"] = short_step
         if configs:  # the five workloads, compact, ahead of the long details
             line["configs"] = configs
         if others:

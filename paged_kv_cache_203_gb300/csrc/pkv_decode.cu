@@ -2131,7 +2131,11 @@ decode_short_kernel(const __grid_constant__ AttnParams p) {
 // of rank r forms its 8 output columns as sum_b 2^(m_b - M) (P_b V_b) with M
 // the row's max over blocks -- the split-softmax identity of the state
 // merge, applied per 16-key block -- so no CTA waits for another's max
-// before its exponentials, and only P and (m, l) cross the cluster.
+// before its exponentials, and only P and (m, l) cross the cluster.  The
+// stores are asynchronous and complete bytes on an mbarrier of the
+// receiving CTA, which expects 640 B per live block: a CTA waits only for
+// what it receives (every CTA receives everything addressed to it before it
+// leaves, so none is written after it exits).
 // ============================================================================
 
 constexpr int SC_CTAS = 4;
@@ -2152,11 +2156,13 @@ struct ScSmem {
   static constexpr uint32_t kVoff = kML + SC_BLOCKS * 8 * 16;     // int64 [256]
   static constexpr uint32_t kKoff = kVoff + SC_KEYS * 8;          // int64 [64]
   static constexpr uint32_t kLive = kKoff + SC_WARPS * 16 * 8;    // uint32 [8]: key bits
-  static constexpr uint32_t kEnd = kLive + 8 * 4;
+  static constexpr uint32_t kBar = kLive + 8 * 4;                 // mbarrier: blocks received
+  static constexpr uint32_t kEnd = kBar + 8;
 };
 static_assert(ScSmem::kV % 16 == 0 && ScSmem::kP % 16 == 0 && ScSmem::kML % 16 == 0 &&
-                  ScSmem::kVoff % 8 == 0,
+                  ScSmem::kVoff % 8 == 0 && ScSmem::kBar % 8 == 0,
               "aligned short-cluster areas");
+constexpr uint32_t kScBlockBytes = 32 * 16 + 8 * 16;  // one block's P and (m, l) rows
 
 __global__ void __cluster_dims__(SC_CTAS, 1, 1) __launch_bounds__(SC_WARPS * 32, 1)
 decode_short_cluster_kernel(const __grid_constant__ AttnParams p) {
@@ -2183,7 +2189,11 @@ decode_short_cluster_kernel(const __grid_constant__ AttnParams p) {
   const int q_len = p.cu_seqlens_q[b + 1] - q_begin;
   const int kv_len = p.cache_seqlens[b];
   if (q_len <= 0 || q_begin < 0 || q_begin + q_len > p.total_q) return;  // the whole cluster
-  cluster_arrive_relaxed();  // its wait precedes the first store into a peer
+  const uint32_t xbar = sbase + ScSmem::kBar;
+  if (tid == 0) {
+    mbar_init(xbar, 1);
+    mbar_init_fence();
+  }
   const int n_rows = min(q_len, p.max_seqlen_q) * p.group;  // <= 16
   const int hi = max(kv_len, 0);
   const int lo = p.window_left >= 0 ? max(0, kv_len - q_len - p.window_left) : 0;
@@ -2227,6 +2237,11 @@ decode_short_cluster_kernel(const __grid_constant__ AttnParams p) {
     blk |= ((w & 0xffffu) != 0u ? 1u : 0u) << (2 * i);
     blk |= ((w >> 16) != 0u ? 1u : 0u) << (2 * i + 1);
   }
+  // every live block of the pair arrives here once; the barrier's
+  // initialisation and this expectation precede every peer's stores (the
+  // cluster barrier below is released here and waited on before they send)
+  if (tid == 0) mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(__popc(blk)) * kScBlockBytes);
+  cluster_arrive_release();
 
   // ---- copies: this CTA's value columns of every key of a live block, and
   // the K rows of its own keys (dead keys of a live block read zeros) ----
@@ -2329,7 +2344,7 @@ decode_short_cluster_kernel(const __grid_constant__ AttnParams p) {
   }
 
   // ---- the block's P and (m, l) into every CTA of the cluster ----
-  cluster_wait();  // every CTA of the cluster runs
+  cluster_wait();  // every CTA of the cluster runs and expects its bytes
   if (my_live) {
     const uint32_t pl = sbase + ScSmem::kP + static_cast<uint32_t>((blk_id * 32 + lane) * 16);
     const uint32_t ml = sbase + ScSmem::kML + static_cast<uint32_t>((blk_id * 8 + g) * 16);
@@ -2337,11 +2352,13 @@ decode_short_cluster_kernel(const __grid_constant__ AttnParams p) {
                                  __float_as_uint(l_row[0]), __float_as_uint(l_row[1]));
 #pragma unroll
     for (int d = 0; d < SC_CTAS; ++d) {
-      st_cluster_v4(map_to_cta(pl, static_cast<uint32_t>(d)), pf);
-      if (tq == 0) st_cluster_v4(map_to_cta(ml, static_cast<uint32_t>(d)), mlv);
+      const uint32_t rb = map_to_cta(xbar, static_cast<uint32_t>(d));
+      st_async_v4(map_to_cta(pl, static_cast<uint32_t>(d)), pf, rb);
+      if (tq == 0) st_async_v4(map_to_cta(ml, static_cast<uint32_t>(d)), mlv, rb);
     }
   }
-  cluster_sync();  // every live block's P, m and l are in every CTA
+  // every live block's P, m and l are in this CTA
+  if (!mbar_wait_sleep(xbar, 0) && tid == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
 
   // ---- this warp's 8 output columns over every live block ----
   const float4 *sML = reinterpret_cast<const float4 *>(smem + ScSmem::kML);

@@ -103,6 +103,9 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
 }
@@ -206,6 +209,16 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t remote, uint4 v) {
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(remote), "r"(v.x),
                "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
+}
+// Asynchronous 16-byte store into the shared memory of a CTA of the cluster;
+// its bytes complete transaction count on `remote_bar`, an mbarrier of the
+// same CTA (both shared::cluster addresses).  The receiver waits on its
+// barrier instead of the sender releasing a cluster barrier.
+__device__ __forceinline__ void st_async_v4(uint32_t remote, uint4 v, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];\n"
+      ::"r"(remote), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+      : "memory");
 }
 __device__ __forceinline__ void st_cluster_b32(uint32_t remote, uint32_t v) {
   asm volatile("st.shared::cluster.b32 [%0], %1;\n" ::"r"(remote), "r"(v) : "memory");
