@@ -54,7 +54,7 @@ MEASURED_TRAFFIC = {
     ("swa_decode", "decode_allheads_kernel (slot rows)"): 647_964_416,
     ("varlen_extend", "extend_tc_kernel"): 264_708_352,
     ("mla_topk_decode", "mla_topk_kernel"): 335_132_160,
-    ("tiny_decode", "decode_short_cluster_kernel"): 586_496,  # its 2 MB of K / V sit in L2
+    ("tiny_decode", "decode_short_cluster_kernel"): 591_104,  # its 2 MB of K / V sit in L2
 }
 
 
@@ -312,12 +312,16 @@ def _multi_step_ms(fn, n: int = 20, reps: int = 10) -> float:
     return ms
 
 
-def _graph_floor_ms() -> float:
-    """Time per replay of a CUDA graph holding one trivial op (a one-element
-    add), replayed back to back like the steps: the launch-rate floor under
-    a step of a few microseconds on this machine."""
+def _graph_floor_ms(n_ops: int = 1) -> float:
+    """Time per replay of a CUDA graph holding ``n_ops`` trivial ops (one-
+    element adds), replayed back to back like the steps: the launch-rate
+    floor under a step of a few microseconds made of that many kernels."""
     x = torch.zeros(1, device="cuda")
-    return _timed(lambda: x.add_(1.0), reps=200)[0]
+
+    def ops():
+        for _ in range(n_ops):
+            x.add_(1.0)
+    return _timed(ops, reps=200)[0]
 
 
 def _timed(fn, reps: int = 20) -> tuple[float, dict]:
@@ -1000,7 +1004,8 @@ def main():
     if ms < 0.05:  # a few microseconds: eager launches time the host
         attn_ms = min(attn_ms, _timed(step.attend)[0])
         short_step = {"ms_per_step_20_steps_per_graph": _multi_step_ms(step.run),
-                      "ms_per_replay_of_a_one_op_graph": _graph_floor_ms()}
+                      "ms_per_replay_of_a_one_op_graph": _graph_floor_ms(1),
+                      "ms_per_replay_of_a_two_op_graph": _graph_floor_ms(2)}
     flags = pkv.get_error_flags()
     if dist is not None:
         t = torch.tensor([ms], device=dev)
@@ -1058,11 +1063,13 @@ def main():
                     kms = min(kms, _timed(s2.attend)[0])
                     how = dict(how, ms_per_step_20_steps_per_graph=_multi_step_ms(s2.run),
                                attn_ms_20_per_graph=_multi_step_ms(s2.attend),
-                               ms_per_replay_of_a_one_op_graph=_graph_floor_ms())
+                               ms_per_replay_of_a_one_op_graph=_graph_floor_ms(1),
+                               ms_per_replay_of_a_two_op_graph=_graph_floor_ms(2))
                 if not ov:
                     configs[label] = config_summary(s2, kms, sms, peaks)
                     for key in ("ms_per_step_20_steps_per_graph",
-                                "ms_per_replay_of_a_one_op_graph"):
+                                "ms_per_replay_of_a_one_op_graph",
+                                "ms_per_replay_of_a_two_op_graph"):
                         if key in how:
                             configs[label][key] = how[key]
                 others[label] = {

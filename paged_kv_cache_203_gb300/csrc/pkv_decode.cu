@@ -2363,32 +2363,36 @@ decode_short_cluster_kernel(const __grid_constant__ AttnParams p) {
   // ---- this warp's 8 output columns over every live block ----
   const float4 *sML = reinterpret_cast<const float4 *>(smem + ScSmem::kML);
   const uint4 *sP = reinterpret_cast<const uint4 *>(smem + ScSmem::kP);
+  // every block's row maxima first (all loads in flight together), then
+  // each block's P V with its factor, the loop unrolled so that the loads
+  // of later blocks are issued ahead; a dead block (its shared memory not
+  // written in this launch) issues no MMA and has the factor 0
+  float4 mlb[SC_BLOCKS];
   float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll 4
-  for (int i = 0; i < SC_BLOCKS; ++i)
-    if ((blk >> i) & 1u) {
-      const float4 mlb = sML[i * 8 + g];
-      M0 = fmaxf(M0, mlb.x);
-      M1 = fmaxf(M1, mlb.y);
-    }
-  float o[4] = {0.f, 0.f, 0.f, 0.f}, L0 = 0.f, L1 = 0.f;
-#pragma unroll 4
+#pragma unroll
   for (int i = 0; i < SC_BLOCKS; ++i) {
-    if (!((blk >> i) & 1u)) continue;
-    const float4 mlb = sML[i * 8 + g];
+    mlb[i] = sML[i * 8 + g];
+    if (!((blk >> i) & 1u)) mlb[i] = make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
+    M0 = fmaxf(M0, mlb[i].x);
+    M1 = fmaxf(M1, mlb[i].y);
+  }
+  float o[4] = {0.f, 0.f, 0.f, 0.f}, L0 = 0.f, L1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < SC_BLOCKS; ++i) {
+    const bool lv = ((blk >> i) & 1u) != 0u;
     const uint4 a = sP[i * 32 + lane];
     uint32_t b0, b1;
     ldsm_x2_t(sV + static_cast<uint32_t>((i * 16 + (lane & 15)) * SC_VPITCH + warp * 16), b0, b1);
     float t[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_bf16(t, a.x, a.y, a.z, a.w, b0, b1);
-    const float f0 = mlb.x == -INFINITY ? 0.f : fast_exp2(mlb.x - M0);
-    const float f1 = mlb.y == -INFINITY ? 0.f : fast_exp2(mlb.y - M1);
+    if (lv) mma_bf16(t, a.x, a.y, a.z, a.w, b0, b1);
+    const float f0 = mlb[i].x == -INFINITY ? 0.f : fast_exp2(mlb[i].x - M0);
+    const float f1 = mlb[i].y == -INFINITY ? 0.f : fast_exp2(mlb[i].y - M1);
     o[0] += f0 * t[0];
     o[1] += f0 * t[1];
     o[2] += f1 * t[2];
     o[3] += f1 * t[3];
-    L0 += f0 * mlb.z;
-    L1 += f1 * mlb.w;
+    L0 += f0 * mlb[i].z;
+    L1 += f1 * mlb[i].w;
   }
   const int col = rank * SC_VCOLS + warp * 8 + 2 * tq;
 #pragma unroll
