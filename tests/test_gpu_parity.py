@@ -457,6 +457,60 @@ def test_short_decode(page_size, h_q, h_kv, q_len, window, batch):
     assert (out.float() - out2.float()).abs().max().item() <= MAX_ABS
 
 
+def test_table_then_attention_in_order_across_replays():
+    """The strided table builder and the short decode kernel are launched with
+    programmatic serialization: the attention may start before the builder
+    ends and must still read the table the builder wrote in the same step.
+    The requests' pool rows and lengths are permuted before every replay of
+    a captured step (and before every eager step), so a table read ahead of
+    its write would show as another request's keys."""
+    wl = workloads.make("tiny_decode")
+    g = wl.to(DEV)
+    batch, n_cols, P = wl.page_table.shape[0], wl.page_table.shape[1], wl.page_size
+    rpi = g.req_pool_indices.clone()
+    cs = g.cache_seqlens.clone()
+    pt = torch.empty(batch, n_cols, dtype=torch.int32, device=DEV)
+    out = torch.empty(g.q.shape[0], g.q.shape[1], wl.v_cache.shape[-1], dtype=torch.bfloat16,
+                      device=DEV)
+    lse = torch.empty(g.q.shape[0], g.q.shape[1], dtype=torch.float32, device=DEV)
+
+    def step():
+        pkv.strided_page_table(g.req_to_token, rpi, P, n_cols, out=pt)
+        pkv.attn_with_kvcache(g.q, g.k_cache, g.v_cache, pt, cs, g.cu_seqlens_q, g.max_seqlen_q,
+                              g.scale, num_splits=1, out=out, lse=lse)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(11)
+    perms = [np.roll(np.arange(batch), k) for k in range(1, batch)] + \
+            [rng.permutation(batch) for _ in range(3)]
+    for mode in ("graph", "eager"):
+        for perm in perms:
+            idx = torch.as_tensor(perm, device=DEV)
+            rpi.copy_(g.req_pool_indices[idx])
+            cs.copy_(g.cache_seqlens[idx])
+            if mode == "graph":
+                graph.replay()
+            else:
+                step()
+            torch.cuda.synchronize()
+            ref_pt = oracle.strided_page_table(wl.req_to_token.numpy(),
+                                               wl.req_pool_indices.numpy()[perm], P, n_cols)
+            assert np.array_equal(pt.cpu().numpy(), ref_pt), mode
+            ref_o, ref_l, _ = oracle_attn(wl, page_table=torch.from_numpy(ref_pt),
+                                          cache_seqlens=wl.cache_seqlens[torch.as_tensor(perm)])
+            check_close(out, lse, ref_o, ref_l, f"{mode} perm={perm.tolist()}")
+    assert pkv.get_error_flags() == 0
+
+
 # ------------------------------------- full-size workloads, every output row
 
 @pytest.mark.parametrize("num_splits", [4, 0])
