@@ -1921,6 +1921,9 @@ decode_short_kernel(const __grid_constant__ AttnParams p) {
   const int n_rows = min(q_len, p.max_seqlen_q) * p.group;  // <= 16
   const int hi = max(kv_len, 0);
   const int lo = p.window_left >= 0 ? max(0, kv_len - q_len - p.window_left) : 0;
+  // keys past the kernel's 256 lie past the table (at most 256 keys): the
+  // row is too short for them, as for the keys checked one by one below
+  if (tid == 0 && hi > max(lo, kDecodeShortMaxKeys)) atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
   bool live = j >= lo && j < hi;
   if (live && pidx >= p.pt_cols) {
     atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
@@ -2197,6 +2200,9 @@ decode_short_cluster_kernel(const __grid_constant__ AttnParams p) {
   const int n_rows = min(q_len, p.max_seqlen_q) * p.group;  // <= 16
   const int hi = max(kv_len, 0);
   const int lo = p.window_left >= 0 ? max(0, kv_len - q_len - p.window_left) : 0;
+  // keys past the kernel's 256 lie past the table (at most 256 keys): the
+  // row is too short for them, as for the keys checked one by one below
+  if (tid == 0 && rank == 0 && hi > max(lo, SC_KEYS)) atomicOr(p.err, PKV_EFLAG_ROW_TOO_SHORT);
   auto key_live = [&](int j, int pidx, int pg, bool report) {
     bool live = j >= lo && j < hi;
     if (live && pidx >= p.pt_cols) {

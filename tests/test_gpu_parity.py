@@ -457,6 +457,26 @@ def test_short_decode(page_size, h_q, h_kv, q_len, window, batch):
     assert (out.float() - out2.float()).abs().max().item() <= MAX_ABS
 
 
+@pytest.mark.parametrize("batch", [9, 80])
+def test_short_decode_lengths_past_the_table(batch):
+    """Short page tables (at most 256 keys) whose requests claim more keys
+    than the table holds (up to 300 against 256): those keys are skipped, as
+    the oracle skips them, and the row-too-short bit is set, on the cluster
+    kernel (batch 9) and the one-CTA kernel (batch 80)."""
+    wl = workloads.make("tiny_decode", batch=batch, len_lo=200, len_hi=256,
+                        pool_tokens=batch * 256 + 64, seed=23)
+    assert wl.page_table.shape[1] * wl.page_size <= 256
+    wl.cache_seqlens[1] = 300
+    wl.cache_seqlens[batch - 1] = 257
+    g = wl.to(DEV)
+    ref_o, ref_l, skipped = oracle_attn(wl)
+    assert skipped > 0
+    pkv.clear_error_flags()
+    out, lse = gpu_attn(g, num_splits=1)
+    check_close(out, lse, ref_o, ref_l, f"batch {batch}")
+    assert pkv.get_error_flags() == pkv.EFLAG_ROW_TOO_SHORT
+
+
 def test_table_then_attention_in_order_across_replays():
     """The strided table builder and the short decode kernel are launched with
     programmatic serialization: the attention may start before the builder
