@@ -98,11 +98,9 @@ __device__ __forceinline__ void cluster_sync() {
                "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 // The two halves of cluster_sync(), for a barrier whose arrival and wait are
-// far apart: arrive (no ordering) at kernel entry, wait before the first
-// access to another CTA's shared memory, so no CTA is written before it runs.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
-}
+// far apart: arrive (releasing this CTA's earlier writes, e.g. mbarrier
+// initialisations) early, wait before the first access to another CTA's
+// shared memory, so no CTA is written before it runs.
 __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
 }
@@ -114,17 +112,6 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t rank) {
   uint32_t d;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(d) : "r"(saddr), "r"(rank));
   return d;
-}
-// Bulk copy of `bytes` (multiple of 16, both ends 16-byte aligned) from this
-// CTA's shared memory into another CTA's; completes `bytes` of transaction
-// count on `remote_bar` (an mbarrier in the destination CTA).
-__device__ __forceinline__ void bulk_s2s(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,
-                                         uint32_t remote_bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
-      " [%0], [%1], %2, [%3];\n" ::"r"(remote_dst),
-      "r"(local_src), "r"(bytes), "r"(remote_bar)
-      : "memory");
 }
 // Arrive (release, cluster scope) on an mbarrier of another CTA of the
 // cluster, given its shared::cluster address.
@@ -361,18 +348,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 // 16 consecutive fp32 columns of this thread's TMEM lane (load + wait).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];\n"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : PKV_O16(0)
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
