@@ -226,17 +226,21 @@ def attn_with_kvcache(q, k_cache, v_cache, page_table, cache_seqlens,
     if return_softmax_lse and lse is None:
         lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32,
                           device=q.device)
-    ws_bytes = attn_workspace_size(q, k_cache, v_cache, page_table,
-                                   cache_seqlens, max_seqlen_q, topk_indices,
-                                   num_splits)
+    # each descriptor is built once and serves both calls (marshalling is most
+    # of the binding's host time)
+    dq, dk, dv, dpt, dcs, dtk = (_desc(q), _desc(k_cache), _desc(v_cache), _desc(page_table),
+                                 _desc(cache_seqlens), _desc(topk_indices))
+    n = ctypes.c_size_t(0)
+    _check("pkv_attn_workspace_size", lib.pkv_attn_workspace_size(
+        dq, dk, dv, dpt, dcs, int(max_seqlen_q), dtk, int(num_splits), ctypes.byref(n)))
+    ws_bytes = n.value
     if ws_bytes > 0 and (workspace is None or workspace.numel() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if ws_bytes > 0 else None
     _check("pkv_attn_with_kvcache", lib.pkv_attn_with_kvcache(
-        _desc(q), _desc(k_cache), _desc(v_cache), _desc(page_table),
-        _desc(cache_seqlens), _desc(cu_seqlens_q), int(max_seqlen_q),
+        dq, dk, dv, dpt, dcs, _desc(cu_seqlens_q), int(max_seqlen_q),
         float(softmax_scale), int(bool(causal)), int(window_left),
-        _desc(topk_indices), int(num_splits), _desc(out), _desc(lse), ws_ptr,
+        dtk, int(num_splits), _desc(out), _desc(lse), ws_ptr,
         ws_bytes, _stream(q)))
     return (out, lse) if return_softmax_lse else out
 
@@ -270,15 +274,19 @@ def attn_with_kvcache_fp8(q, k_cache, v_cache, page_table, cache_seqlens, cu_seq
                           device=q.device)
     if return_softmax_lse and lse is None:
         lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
-    ws_bytes = attn_workspace_size(q, k_cache, v_cache, page_table, cache_seqlens,
-                                   max_seqlen_q, topk_indices, num_splits)
+    dq, dk, dv, dpt, dcs, dtk = (_desc(q), _desc(k_cache), _desc(v_cache), _desc(page_table),
+                                 _desc(cache_seqlens), _desc(topk_indices))
+    n = ctypes.c_size_t(0)
+    _check("pkv_attn_workspace_size", lib.pkv_attn_workspace_size(
+        dq, dk, dv, dpt, dcs, int(max_seqlen_q), dtk, int(num_splits), ctypes.byref(n)))
+    ws_bytes = n.value
     if ws_bytes > 0 and (workspace is None or workspace.numel() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if ws_bytes > 0 else None
     _check("pkv_attn_with_kvcache_fp8", lib.pkv_attn_with_kvcache_fp8(
-        _desc(q), _desc(k_cache), _desc(v_cache), _desc(page_table), _desc(cache_seqlens),
+        dq, dk, dv, dpt, dcs,
         _desc(cu_seqlens_q), int(max_seqlen_q), float(softmax_scale), int(bool(causal)),
-        int(window_left), _desc(topk_indices),
+        int(window_left), dtk,
         _descale_ptr(k_descale, cache_seqlens, k_cache),
         _descale_ptr(v_descale, cache_seqlens, k_cache), int(num_splits), _desc(out),
         _desc(lse), ws_ptr, ws_bytes, _stream(q)))
