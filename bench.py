@@ -53,7 +53,7 @@ MEASURED_TRAFFIC = {
     ("gqa_split_decode", "decode_allheads_kernel (page boxes, fixed splits)"): 1_116_558_400,
     ("swa_decode", "decode_allheads_kernel (slot rows)"): 647_964_416,
     ("varlen_extend", "extend_tc_kernel"): 264_708_352,
-    ("mla_topk_decode", "mla_topk_kernel"): 335_132_160,
+    ("mla_topk_decode", "mla_topk_kernel"): 335_151_616,
     ("tiny_decode", "decode_short_cluster_kernel"): 591_104,  # its 2 MB of K / V sit in L2
 }
 

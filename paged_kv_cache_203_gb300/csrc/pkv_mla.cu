@@ -85,10 +85,14 @@ static_assert(NSTG_F8 * kKTile + 2 * kStgScore <= NSTG * kKTile &&
 constexpr uint32_t kTmQ = 0, kTmS = 384;
 static_assert(kTmQ + DQK / 2 <= kTmS && kTmS + 2 * BK <= 512, "TMEM plan");
 
+constexpr uint32_t kQRow = DQK * 2 + 16;  // a staged Q row (padded: 4-way banked reads)
 struct Smem {
   // score CTA
   static constexpr uint32_t kK = 0;                          // NSTG key tiles
-  static constexpr uint32_t kBias = kK + NSTG * kKTile;      // float [NSTG][BK]: 0 or -inf
+  // bf16: Q rows staged by bulk copies in the bytes of stages 1-2 (and a
+  // little past them) until the softmax warps have moved them to TMEM
+  static constexpr uint32_t kQStage = kK + kKTile;
+  static constexpr uint32_t kBias = kQStage + H * kQRow;     // float [NSTG][BK]: 0 or -inf
   // value CTA
   static constexpr uint32_t kV = 0;                          // NSTG value tiles
   static constexpr uint32_t kP = kV + NSTG * kVTile;         // P as received [2][kPXfer]
@@ -103,6 +107,8 @@ struct Smem {
   static constexpr size_t kDynamic = kEnd;  // base must be 1024-aligned (checked)
 };
 static_assert(Smem::kBias + NSTG * BK * 4 <= Smem::kCtl, "score-CTA plan overlaps the control block");
+static_assert(Smem::kBias >= Smem::kK + NSTG * kKTile && Smem::kBias >= NSTG_F8 * kKTile + 2 * BK * DQK,
+              "key masks past every score-CTA stage");
 static_assert(Smem::kDynamic <= 232448, "shared memory plan exceeds 227 KB");
 static_assert(kPXfer % 16 == 0 && kFacWarp % 16 == 0, "16-byte aligned P buffers");
 
@@ -117,7 +123,9 @@ enum BarId {
   Q_TMEM = 12,       //     score CTA: Q is in TMEM   | value CTA: O_DONE (each PV done)
   O_DONE = 12,
   CORR_REQ = 13,     // value CTA: rescale request (or stop) to the epilogue warps
+  Q_LANDED = 13,     // score CTA: the staged Q rows landed (bytes)
   CORR_DONE = 14,    // value CTA: rescale done
+  Q_STAGED = 14,     // score CTA: the staged rows are in TMEM (stages 1-2 reusable)
   FIN = 15           // value CTA: (1/l, lse) landed (4 remote arrivals)
 };
 
@@ -213,7 +221,11 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
   const int tile0 = min(n_tiles_all, split * per);
   const int n_kv = min(n_tiles_all, tile0 + per) - tile0;
 
-  if (score && warp < NSOFT && covered) {  // warm L2 with this head's Q row
+  // bf16 Q rows go through shared memory by bulk copies when their rows are
+  // 16-byte aligned (else each softmax thread loads its row from global)
+  const bool qstage = !FP8 && (reinterpret_cast<uintptr_t>(p.q) & 15) == 0 && p.q_st % 8 == 0 &&
+                      p.q_sh % 8 == 0;
+  if (score && warp < NSOFT && covered && !qstage) {  // warm L2 with this head's Q row
     const bf16 *qrow = p.q + static_cast<int64_t>(t) * p.q_st + static_cast<int64_t>(tid) * p.q_sh;
 #pragma unroll
     for (int i = 0; i < NCH; ++i) prefetch_line_l2(qrow + i * 64);
@@ -230,6 +242,8 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
         mbar_init(bar(P_FREE + i), 1);
       }
       mbar_init(bar(Q_TMEM), NSOFT);
+      mbar_init(bar(Q_LANDED), 1);
+      mbar_init(bar(Q_STAGED), NSOFT);
     } else {
       for (int i = 0; i < 2; ++i) {
         mbar_init(bar(P_FULL + i), NSOFT);
@@ -383,6 +397,9 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
         int ok = 1;
         if (lane == 0 && jj >= NS)
           ok = mbar_wait_sleep(bar(EMPTY + s), ((jj / NS) & 1) ^ 1) ? 1 : 0;
+        // stages 1-2 hold the staged Q rows until they are in TMEM
+        if (lane == 0 && ok && score && qstage && jj == 1)
+          ok = mbar_wait_sleep(bar(Q_STAGED), 0) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
           ok_all = false;
@@ -518,15 +535,35 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
     const uint32_t peer_pfull = map_to_cta(bar(P_FULL), peer);
     if (n_kv > 0) {
       // Q row `row` (576 bf16) as packed pairs into TMEM columns 0..287 of
-      // this thread's lane: the A operand of Q K^T (three 192-column loads
-      // in flight at a time; the row's lines were warmed at kernel start)
+      // this thread's lane: the A operand of Q K^T.  bf16 (aligned rows):
+      // one bulk copy per row into shared memory, read back 384 bytes at a
+      // time; else three 192-column loads from global in flight at a time
+      // (the row's lines were warmed at kernel start)
       const uint4 *qsrc = reinterpret_cast<const uint4 *>(
           p.q + static_cast<int64_t>(t) * p.q_st + static_cast<int64_t>(row) * p.q_sh);
+      const uint32_t qs = sbase + Smem::kQStage + static_cast<uint32_t>(row) * kQRow;
+      if (qstage) {
+        if (row == 0) mbar_arrive_expect_tx(bar(Q_LANDED), H * DQK * 2);
+        asm volatile("bar.sync 2, %0;\n" ::"n"(NSOFT * 32) : "memory");  // expectation first
+        bulk_g2s(qs, qsrc, DQK * 2, bar(Q_LANDED));
+        if (!mbar_wait_sleep(bar(Q_LANDED), 0)) {
+          ok = false;
+          if (lane == 0) atomicOr(p.err, PKV_EFLAG_TIMEOUT);
+        }
+      }
 #pragma unroll 1
       for (int cb0 = 0; cb0 < NCH; cb0 += 3) {
         uint4 w[24];
+        if (qstage) {
 #pragma unroll
-        for (int i = 0; i < 24; ++i) w[i] = qsrc[cb0 * 8 + i];
+          for (int i = 0; i < 24; ++i)
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                         : "=r"(w[i].x), "=r"(w[i].y), "=r"(w[i].z), "=r"(w[i].w)
+                         : "r"(qs + (cb0 * 8 + i) * 16));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 24; ++i) w[i] = qsrc[cb0 * 8 + i];
+        }
 #pragma unroll
         for (int k = 0; k < 3; ++k) {
           uint32_t r[32];
@@ -549,7 +586,10 @@ mla_topk_kernel(const __grid_constant__ AttnParams p) {
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(Q_TMEM));
+      if (lane == 0) {
+        mbar_arrive(bar(Q_TMEM));
+        if (qstage) mbar_arrive(bar(Q_STAGED));  // the staged rows were read
+      }
     }
     const float *sBias = reinterpret_cast<const float *>(smem + Smem::kBias);
     for (int jj = 0; jj < n_kv; ++jj) {
