@@ -923,6 +923,54 @@ def test_mla_topk_reference_max_rises(num_splits):
     assert pkv.get_error_flags() == 0
 
 
+@pytest.mark.parametrize("batch,topk,seed", [(100, 256, 5), (90, 200, 6), (77, 64, 7)])
+def test_mla_topk_more_tokens_than_sm_pairs(batch, topk, seed):
+    """More tokens than SM pairs (clusters in a second wave) with the
+    library's split choice; ragged last tiles, -1 padding, a duplicate, an
+    out-of-range entry (skipped, flagged) and a row of only -1; every row
+    against the oracle."""
+    wl = _mla_reduced(batch=batch, kv_len=700, topk=topk, seed=seed)
+    wl.topk_indices[:, -9:] = -1
+    wl.topk_indices[2, 5] = wl.topk_indices[2, 6]
+    wl.topk_indices[7, 1] = 700                # == kv_len
+    wl.topk_indices[batch - 1, :] = -1         # nothing to attend
+    g = wl.to(DEV)
+    pkv.clear_error_flags()
+    out, lse = gpu_attn(g, num_splits=0)
+    ref_o, ref_l, skipped = oracle_attn(wl)
+    assert skipped == 1
+    check_close(out, lse, ref_o, ref_l, f"mla batch={batch} topk={topk}")
+    assert pkv.get_error_flags() == pkv.EFLAG_TOPK_OOB
+    assert torch.all(out[batch - 1] == 0) and torch.all(torch.isneginf(lse[batch - 1]))
+
+
+def test_mla_topk_fp8_more_tokens_than_sm_pairs():
+    """More tokens than SM pairs over an fp8 latent cache (codes widened to
+    f16, q rounded to e4m3, per-request descales); against the fp8 oracle."""
+    wl = _mla_reduced(batch=80, kv_len=700, topk=192, seed=8)
+    wl.topk_indices[:, -5:] = -1
+    B = wl.cache_seqlens.shape[0]
+    k8 = wl.k_cache.float().to(torch.float8_e4m3fn)
+    gen = torch.Generator().manual_seed(41)
+    kd = torch.rand(B, 1, generator=gen) * 1.5 + 0.5
+    vd = torch.rand(B, 1, generator=gen) * 1.5 + 0.5
+    g = wl.to(DEV)
+    k8d = k8.to(DEV)
+    pkv.clear_error_flags()
+    out, lse = pkv.attn_with_kvcache_fp8(
+        g.q, k8d, k8d[..., :512], g.page_table, g.cache_seqlens, g.cu_seqlens_q,
+        g.max_seqlen_q, g.scale, topk_indices=g.topk_indices, k_descale=kd.to(DEV),
+        v_descale=vd.to(DEV), num_splits=0, return_softmax_lse=True)
+    torch.cuda.synchronize()
+    codes = k8.view(torch.uint8).numpy()
+    ref_o, ref_l, _ = oracle.attention_fp8(
+        oracle.bf16_bits(wl.q), codes, codes[..., :512], wl.page_table.numpy(),
+        wl.cache_seqlens.numpy(), wl.cu_seqlens_q.numpy(), wl.scale, k_descale=kd.numpy(),
+        v_descale=vd.numpy(), topk=wl.topk_indices.numpy())
+    check_close(out, lse, ref_o, ref_l, "mla fp8, more tokens than SM pairs")
+    assert pkv.get_error_flags() == 0
+
+
 def test_mla_topk_bad_indices_and_empty_rows():
     """Out-of-range top-k entries are skipped and flagged; a row of only -1
     gives out 0 / lse -inf."""
