@@ -17,6 +17,11 @@
  *   and returns an `int` status: PKV_OK (0) or a negative PKV_ERR_* code.  A
  *   negative status means nothing was launched.  No C++ exception crosses
  *   this boundary.
+ * - Stream order is kept.  The short kernels (the strided page table, short
+ *   decode) are launched with programmatic stream serialization: they may be
+ *   scheduled while the previous kernel on the stream is still running, but
+ *   wait for it to complete (griddepcontrol.wait) before their first access
+ *   to global memory, so they see everything it wrote.
  * - Data-dependent faults that can only be seen on the device (a page id
  *   outside the KV pool, a top-k index outside [-1, kv_len), a page-table row
  *   too short for its sequence) never trap: the offending entry is skipped
