@@ -54,7 +54,7 @@ MEASURED_TRAFFIC = {
     ("swa_decode", "decode_allheads_kernel (slot rows)"): 647_964_416,
     ("varlen_extend", "extend_tc_kernel"): 264_708_352,
     ("mla_topk_decode", "mla_topk_kernel"): 335_151_616,
-    ("tiny_decode", "decode_short_cluster_kernel"): 591_104,  # its 2 MB of K / V sit in L2
+    ("tiny_decode", "decode_short_cluster_kernel"): 599_808,  # its 2 MB of K / V sit in L2
 }
 
 
@@ -141,7 +141,6 @@ class Step:
         self.dev = device
         self.g = workloads.make(name, value_device=device, **overrides)
         g = self.g
-        self.kernels_per_step = 0
         self.ws = None
         self.h2d_bytes = 0
         self.d2h_bytes = 0
@@ -169,6 +168,11 @@ class Step:
         self.kv_bytes = kv_tokens * h_kv * (d + dv) * 2 if g.topk_indices is None else \
             kv_tokens * d * 2  # absorbed MLA: one 576-wide row per gathered key
         self.flops = self._flops()
+        # where the short decode kernels serve the attention, the library
+        # builds the strided table inside the attention launch
+        self.one_launch = (g.kind != "swa" and g.topk_indices is None
+                           and self.attention_kernel().startswith("decode_short"))
+        self.kernels_per_step = 1 if self.one_launch else 2
 
     def prepare(self):
         """Allocate the library's workspace (library arm only: the reference
@@ -217,8 +221,21 @@ class Step:
             return ql * (cs - ql) + ql * (ql + 1) / 2
         return ql * cs
 
+    def _table_and_attend(self):
+        """The table built and the attention run by one library call."""
+        g = self.g
+        pkv.strided_table_attn_with_kvcache(
+            g.req_to_token, g.req_pool_indices, self.pt, g.q, g.k_cache, g.v_cache,
+            g.cache_seqlens, g.cu_seqlens_q, g.max_seqlen_q, g.scale, causal=g.causal,
+            window_left=g.window_left, num_splits=g.num_splits, out=self.out, lse=self.lse,
+            workspace=self.ws)
+
     def attend(self):
-        """The step's attention call alone (the table built by an earlier run)."""
+        """The step's attention launch alone (the table built by an earlier
+        run); with the table built inside the attention launch, that launch."""
+        if self.one_launch:
+            self._table_and_attend()
+            return
         g = self.g
         pt, cs = (self.pt, self.kv) if g.kind == "swa" else (self.pt, g.cache_seqlens)
         pkv.attn_with_kvcache(g.q, g.k_cache, g.v_cache, pt, cs, g.cu_seqlens_q,
@@ -229,6 +246,13 @@ class Step:
 
     def run(self, ev=None):
         g = self.g
+        if self.one_launch:
+            if ev is not None:
+                ev[0].record()
+            self._table_and_attend()
+            if ev is not None:
+                ev[1].record()
+            return
         if (g.kind == "swa"):
             pkv.build_swa_page_table(g.req_to_token, g.req_pool_indices, g.seq_lens,
                                      g.prefill_lens, g.window, self.pt, self.kv)
@@ -246,8 +270,6 @@ class Step:
                               workspace=self.ws)
         if ev is not None:
             ev[1].record()
-
-    KERNELS_PER_STEP = 2  # table builder + attention
 
     def attention_kernel(self):
         """Name of the kernel the library picks for this step's attention."""
@@ -1208,7 +1230,7 @@ def main():
                     "copies": "one packed copy each way per step, on their own streams, two buffer sets, overlapped with the steps",
                     "step_launch": e2e_launch,
                     "read_back_matches_a_plain_step": e2e_same},
-            "gpu_launches": Step.KERNELS_PER_STEP * args.steps,
+            "gpu_launches": step.kernels_per_step * args.steps,
             "clocks": clk,
             "tokens_per_s": n_tokens * world / (ms / 1e3),
             "error_flags": flags,

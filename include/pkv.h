@@ -309,6 +309,40 @@ int pkv_strided_page_table(pkv_tensor req_to_token,
                            pkv_tensor out, cudaStream_t stream);
 
 /*
+ * pkv_strided_table_attn_with_kvcache -- build the page table, then attend.
+ *
+ * flashattention_backend.py forms the page-level table in
+ * `init_forward_metadata` ("Convert the page table to a strided format")
+ * and passes it to `flash_attn_with_kvcache` (`forward_decode`).  This call
+ * has the result of
+ *   pkv_strided_page_table(req_to_token, req_pool_indices, P, page_table)
+ *   pkv_attn_with_kvcache(q, k_cache, v_cache, page_table, ...)
+ * on one stream, P = k_cache.shape[1]: page_table (int32 [B, n_cols], rows
+ * contiguous) is written, the attention reads the pages it names, and the
+ * error bits are those of the two calls.  When the short decode kernels
+ * serve the attention (head dim 128, at most 16 query rows per KV head, no
+ * split, n_cols * P <= 256 keys, a bf16 cache, no top-k lists) both happen
+ * in one launch: each CTA forms the page ids it needs from the token pool
+ * and one CTA per request stores the request's table row; otherwise the
+ * builder runs first, then the attention.
+ *
+ * req_to_token, req_pool_indices  (descriptors passed by host pointer, read
+ *          during the call) as pkv_strided_page_table, B entries; NULL is
+ *          PKV_ERR_INVALID_ARG.
+ * All other arguments as pkv_attn_with_kvcache (page_table is written, not
+ * read); the workspace size is pkv_attn_workspace_size of the same
+ * attention arguments.
+ */
+int pkv_strided_table_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
+                                        pkv_tensor page_table, pkv_tensor cache_seqlens,
+                                        pkv_tensor cu_seqlens_q, int max_seqlen_q, float scale,
+                                        int causal, int window_left, pkv_tensor topk_indices,
+                                        int num_splits, pkv_tensor out, pkv_tensor lse,
+                                        const pkv_tensor *req_to_token,
+                                        const pkv_tensor *req_pool_indices, void *workspace,
+                                        size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * pkv_topk_to_slots -- top-k logical positions to physical KV slots.
  *
  * Defined by nsa_backend.py `TopkTransformMethod.PAGED` (the page-table

@@ -50,6 +50,7 @@ __all__ = [
     "merge_state",
     "build_swa_page_table",
     "strided_page_table",
+    "strided_table_attn_with_kvcache",
     "topk_to_slots",
     "make_local_attention_virtual_batches",
     "local_virtual_batch_capacity",
@@ -101,6 +102,7 @@ EXPORTED_SYMBOLS = (
     "pkv_set_kv_buffer_fp8",
     "pkv_append_attn_with_kvcache",
     "pkv_check_bounded_wait",
+    "pkv_strided_table_attn_with_kvcache",
 )
 
 _FP8 = 5
@@ -162,6 +164,9 @@ def load_library(path: str | None = None):
     lib.pkv_append_attn_with_kvcache.argtypes = [T, T, T, T, T, T, c_int, c_float, c_int,
                                                  c_int, TP, TP, TP, c_int, T, T, c_void_p,
                                                  c_size_t, c_void_p]
+    lib.pkv_strided_table_attn_with_kvcache.argtypes = [T, T, T, T, T, T, c_int, c_float,
+                                                        c_int, c_int, T, c_int, T, T, TP, TP,
+                                                        c_void_p, c_size_t, c_void_p]
     lib.pkv_make_local_attention_virtual_batches.argtypes = [
         c_int, c_int, T, T, T, T, T, T, T, T, c_void_p]
     lib.pkv_get_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -377,6 +382,41 @@ def strided_page_table(req_to_token, req_pool_indices, page_size: int,
         _desc(req_to_token), _desc(req_pool_indices), int(page_size),
         _desc(out), _stream(req_to_token)))
     return out
+
+
+def strided_table_attn_with_kvcache(req_to_token, req_pool_indices, page_table, q, k_cache,
+                                    v_cache, cache_seqlens, cu_seqlens_q, max_seqlen_q: int,
+                                    softmax_scale: float, causal: bool = False,
+                                    window_left: int = -1, topk_indices=None,
+                                    num_splits: int = 0, out=None, lse=None,
+                                    return_softmax_lse: bool = False, workspace=None):
+    """The strided page table written into ``page_table`` ([B, n_cols] int32)
+    and the attention over it, in one launch where the short decode kernels
+    serve the call (see include/pkv.h, pkv_strided_table_attn_with_kvcache).
+
+    Returns ``out`` or ``(out, lse)`` when ``return_softmax_lse``."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty(q.shape[0], q.shape[1], v_cache.shape[-1],
+                          dtype=torch.bfloat16, device=q.device)
+    if return_softmax_lse and lse is None:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32,
+                          device=q.device)
+    dq, dk, dv, dpt, dcs, dtk = (_desc(q), _desc(k_cache), _desc(v_cache), _desc(page_table),
+                                 _desc(cache_seqlens), _desc(topk_indices))
+    n = ctypes.c_size_t(0)
+    _check("pkv_attn_workspace_size", lib.pkv_attn_workspace_size(
+        dq, dk, dv, dpt, dcs, int(max_seqlen_q), dtk, int(num_splits), ctypes.byref(n)))
+    ws_bytes = n.value
+    if ws_bytes > 0 and (workspace is None or workspace.numel() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if ws_bytes > 0 else None
+    _check("pkv_strided_table_attn_with_kvcache", lib.pkv_strided_table_attn_with_kvcache(
+        dq, dk, dv, dpt, dcs, _desc(cu_seqlens_q), int(max_seqlen_q), float(softmax_scale),
+        int(bool(causal)), int(window_left), dtk, int(num_splits), _desc(out), _desc(lse),
+        ctypes.byref(_desc(req_to_token)), ctypes.byref(_desc(req_pool_indices)), ws_ptr,
+        ws_bytes, _stream(q)))
+    return (out, lse) if return_softmax_lse else out
 
 
 def topk_to_slots(topk, cu_seqlens_q, page_table, cache_seqlens,

@@ -365,12 +365,18 @@ namespace {
 struct AppendArgs {
   pkv_tensor k_new, v_new, loc;
 };
+// The token pool of a page table built by the same call
+// (pkv_strided_table_attn_with_kvcache).
+struct TableArgs {
+  pkv_tensor req_to_token, req_pool_indices;
+};
 
 int attn_impl(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache, pkv_tensor page_table,
               pkv_tensor cache_seqlens, pkv_tensor cu_seqlens_q, int max_seqlen_q,
               float scale, int causal, int window_left, pkv_tensor topk_indices,
               int num_splits, pkv_tensor k_descale, pkv_tensor v_descale, pkv_tensor out,
-              pkv_tensor lse, void *workspace, size_t workspace_bytes, cudaStream_t stream, const AppendArgs *app = nullptr) {
+              pkv_tensor lse, void *workspace, size_t workspace_bytes, cudaStream_t stream,
+              const AppendArgs *app = nullptr, const TableArgs *tab = nullptr) {
   AttnPlan plan;
   int rc = plan_attention(q, k_cache, v_cache, page_table, cache_seqlens,
                           max_seqlen_q, topk_indices, num_splits, &plan);
@@ -387,6 +393,13 @@ int attn_impl(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache, pkv_tensor p
                        lse.shape[1] != q.shape[1]))
     return PKV_ERR_INVALID_ARG;
   if (window_left < -1 || !isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (tab != nullptr) {  // the token pool of a table built by this call
+    const pkv_tensor &rtt = tab->req_to_token, &rpi = tab->req_pool_indices;
+    if (!has(rtt, PKV_I32, 2) || rtt.stride[1] != 1) return PKV_ERR_INVALID_ARG;
+    if (rpi.data == nullptr || rpi.ndim != 1 || (rpi.dtype != PKV_I32 && rpi.dtype != PKV_I64) ||
+        rpi.stride[0] != 1 || rpi.shape[0] != batch)
+      return PKV_ERR_INVALID_ARG;
+  }
   const bool fp8 = k_cache.dtype == PKV_FP8_E4M3;
   for (const pkv_tensor *ds : {&k_descale, &v_descale}) {
     if (!present(*ds)) continue;
@@ -481,6 +494,27 @@ int attn_impl(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache, pkv_tensor p
     p.vn_sh = app->v_new.stride[1];
     p.new_loc = app->loc.data;
     p.new_loc_is64 = app->loc.dtype == PKV_I64 ? 1 : 0;
+  }
+  if (tab != nullptr) {
+    // the page table is built from the token pool first: by the short
+    // kernels inside the attention launch, else by the strided builder
+    const pkv_tensor &rtt = tab->req_to_token, &rpi = tab->req_pool_indices;
+    if (plan.kind == 4 && p.total_q > 0) {
+      p.rtt = static_cast<const int32_t *>(rtt.data);
+      p.rtt_stride = rtt.stride[0];
+      p.rtt_rows = rtt.shape[0];
+      p.rtt_cols = rtt.shape[1];
+      p.rpi = rpi.data;
+      p.rpi_is64 = rpi.dtype == PKV_I64 ? 1 : 0;
+      p.pt_out = static_cast<int32_t *>(page_table.data);
+    } else {
+      if (batch > 65535) return PKV_ERR_UNSUPPORTED;
+      rc = launch_strided_page_table(
+          static_cast<const int32_t *>(rtt.data), rtt.stride[0], rtt.shape[0], rtt.shape[1],
+          rpi.data, rpi.dtype == PKV_I64, static_cast<int>(batch), p.page_size,
+          static_cast<int32_t *>(page_table.data), page_table.stride[0], p.pt_cols, err, stream);
+      if (rc != PKV_OK) return rc;
+    }
   }
   if (plan.split()) {
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -637,6 +671,22 @@ int pkv_build_swa_page_table(pkv_tensor req_to_token,
       static_cast<int32_t *>(dst_page_table.data), dst_page_table.stride[0],
       static_cast<int>(dst_page_table.shape[1]),
       static_cast<int32_t *>(dst_kv_lens.data), err, stream);
+}
+
+int pkv_strided_table_attn_with_kvcache(pkv_tensor q, pkv_tensor k_cache, pkv_tensor v_cache,
+                                        pkv_tensor page_table, pkv_tensor cache_seqlens,
+                                        pkv_tensor cu_seqlens_q, int max_seqlen_q, float scale,
+                                        int causal, int window_left, pkv_tensor topk_indices,
+                                        int num_splits, pkv_tensor out, pkv_tensor lse,
+                                        const pkv_tensor *req_to_token,
+                                        const pkv_tensor *req_pool_indices, void *workspace,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+  if (req_to_token == nullptr || req_pool_indices == nullptr) return PKV_ERR_INVALID_ARG;
+  const pkv_tensor none{};
+  const pkv::TableArgs tab{*req_to_token, *req_pool_indices};
+  return pkv::attn_impl(q, k_cache, v_cache, page_table, cache_seqlens, cu_seqlens_q,
+                        max_seqlen_q, scale, causal, window_left, topk_indices, num_splits,
+                        none, none, out, lse, workspace, workspace_bytes, stream, nullptr, &tab);
 }
 
 int pkv_strided_page_table(pkv_tensor req_to_token,

@@ -1887,6 +1887,37 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
 // is a few microseconds of latency.
 // ============================================================================
 
+// Page ids of the short kernels.  With a table built in the launch
+// (p.rtt set) a column's page id is formed from the token pool exactly as
+// the strided table builder forms it, and one CTA per request stores the
+// request's table row, so the launch has the result of the builder followed
+// by the attention.
+// Token-pool row of request b (-1: none; every column is then -1).
+__device__ __forceinline__ int64_t short_pool_row(const AttnParams &p, int b) {
+  if (p.rtt == nullptr) return -1;
+  const int64_t r = p.rpi_is64 ? static_cast<const int64_t *>(p.rpi)[b]
+                               : static_cast<const int32_t *>(p.rpi)[b];
+  return r >= 0 && r < p.rtt_rows ? r : -1;
+}
+// Page id of column c of request b's table row (-1 past the row).
+__device__ __forceinline__ int short_page_id(const AttnParams &p, int b, int64_t rrow, int c) {
+  if (c >= p.pt_cols) return -1;
+  if (p.rtt == nullptr) return p.page_table[static_cast<int64_t>(b) * p.pt_stride + c];
+  const int64_t col = static_cast<int64_t>(c) * p.page_size;
+  // slots are non-negative: C division is the page's floor division
+  return rrow >= 0 && col < p.rtt_cols ? p.rtt[rrow * p.rtt_stride + col] / p.page_size : -1;
+}
+// Store request b's table row (threads t = 0 .. nthreads - 1 of one CTA);
+// a column whose source lies outside the token pool is -1 and flagged.
+__device__ __forceinline__ void short_store_table_row(const AttnParams &p, int b, int64_t rrow,
+                                                      int t, int nthreads) {
+  for (int c = t; c < p.pt_cols; c += nthreads) {
+    if (rrow < 0 || static_cast<int64_t>(c) * p.page_size >= p.rtt_cols)
+      atomicOr(p.err, PKV_EFLAG_SRC_OOB);
+    p.pt_out[static_cast<int64_t>(b) * p.pt_stride + c] = short_page_id(p, b, rrow, c);
+  }
+}
+
 constexpr int SD_WARPS = 8;
 constexpr int SD_KEYS = 32;                  // keys per warp
 constexpr int SD_PITCH = 128 * 2 + 16;       // bytes per K / V row (skewed: conflict-free ldmatrix)
@@ -1913,10 +1944,12 @@ decode_short_kernel(const __grid_constant__ AttnParams p) {
   // ---- lengths and this lane's page id, loaded together ----
   const int j = warp * SD_KEYS + lane;  // this lane's key
   const int pidx = j / p.page_size;
-  const int pg_raw = pidx < p.pt_cols ? p.page_table[static_cast<int64_t>(b) * p.pt_stride + pidx] : -1;
+  const int64_t rrow = short_pool_row(p, b);
+  const int pg_raw = short_page_id(p, b, rrow, pidx);
   const int q_begin = p.cu_seqlens_q[b];
   const int q_len = p.cu_seqlens_q[b + 1] - q_begin;
   const int kv_len = p.cache_seqlens[b];
+  if (p.rtt != nullptr && h == 0) short_store_table_row(p, b, rrow, tid, SD_WARPS * 32);
   if (q_len <= 0 || q_begin < 0 || q_begin + q_len > p.total_q) return;  // uniform
   const int n_rows = min(q_len, p.max_seqlen_q) * p.group;  // <= 16
   const int hi = max(kv_len, 0);
@@ -2181,16 +2214,17 @@ decode_short_cluster_kernel(const __grid_constant__ AttnParams p) {
 
   // ---- lengths and page ids, loaded together: keys tid and tid + 128 (V
   // columns of every key), key 64 * rank + tid (K rows of this rank) ----
-  const int64_t prow = static_cast<int64_t>(b) * p.pt_stride;
   const int j0 = tid, j1 = tid + SC_WARPS * 32;
   const int jk = rank * SC_WARPS * 16 + (tid & 63);
   const int pi0 = j0 / p.page_size, pi1 = j1 / p.page_size, pik = jk / p.page_size;
-  const int pg0 = pi0 < p.pt_cols ? p.page_table[prow + pi0] : -1;
-  const int pg1 = pi1 < p.pt_cols ? p.page_table[prow + pi1] : -1;
-  const int pgk = (tid < 64 && pik < p.pt_cols) ? p.page_table[prow + pik] : -1;
+  const int64_t rrow = short_pool_row(p, b);
+  const int pg0 = short_page_id(p, b, rrow, pi0);
+  const int pg1 = short_page_id(p, b, rrow, pi1);
+  const int pgk = tid < 64 ? short_page_id(p, b, rrow, pik) : -1;
   const int q_begin = p.cu_seqlens_q[b];
   const int q_len = p.cu_seqlens_q[b + 1] - q_begin;
   const int kv_len = p.cache_seqlens[b];
+  if (p.rtt != nullptr && h == 0 && rank == 0) short_store_table_row(p, b, rrow, tid, SC_WARPS * 32);
   if (q_len <= 0 || q_begin < 0 || q_begin + q_len > p.total_q) return;  // the whole cluster
   const uint32_t xbar = sbase + ScSmem::kBar;
   if (tid == 0) {

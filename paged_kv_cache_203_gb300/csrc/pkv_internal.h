@@ -95,6 +95,16 @@ struct AttnParams {
   int64_t vn_st, vn_sh;
   const void *new_loc;
   int new_loc_is64;
+  // page table built in the same launch (short decode kernels): page ids are
+  // formed from the token pool as the strided table builder forms them,
+  // req_to_token[req_pool_indices[b]][c * page_size] / page_size, and the
+  // request's row of the table is stored into pt_out (the page_table
+  // memory, pt_stride / pt_cols as above)
+  const int32_t *rtt;                 // req_to_token [rtt_rows][rtt_cols]
+  int64_t rtt_stride, rtt_rows, rtt_cols;
+  const void *rpi;                    // req_pool_indices [batch]
+  int rpi_is64;
+  int32_t *pt_out;
 };
 
 // Error word of the current device (static __device__ in pkv_abi.cu).

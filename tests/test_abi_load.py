@@ -81,6 +81,27 @@ def test_binding_rejects_bad_arguments_on_host(lib):
     assert e.value.code == -1
     with pytest.raises(ValueError):
         pkv.set_kv_buffer(k, None, loc, rows, k_scale=torch.ones(1))
+    # the table-building attention call: its descriptors arrive in order (an
+    # lse of the wrong shape, a missing or malformed token pool and a pool
+    # index list of the wrong length are refused)
+    rtt = torch.zeros(3, 64, dtype=torch.int32)
+    rpi = torch.zeros(2, dtype=torch.int64)
+    cu = torch.zeros(3, dtype=torch.int32)
+    out = torch.zeros(2, 4, 128, dtype=torch.bfloat16)
+    fused = pkv.load_library().pkv_strided_table_attn_with_kvcache
+
+    def call(lse, r=rtt, ri=rpi, byref=True):
+        d = pkv._desc
+        return fused(d(q), d(k), d(k), d(pt), d(cs), d(cu), 1, 0.1, 0, -1, d(None), 0, d(out),
+                     d(lse), ctypes.byref(d(r)) if byref else None,
+                     ctypes.byref(d(ri)) if byref else None, None, 0, None)
+
+    assert call(torch.zeros(3, 4)) == -1
+    assert call(torch.zeros(2, 4), byref=False) == -1
+    assert call(torch.zeros(2, 4), r=rtt.t()) == -1
+    assert call(torch.zeros(2, 4), ri=rpi[:1]) == -1
+    if not torch.cuda.is_available():  # (host tensors must not reach a device)
+        assert call(torch.zeros(2, 4)) == -3  # well formed: stops at the missing device
     # workspace planning: no split -> no workspace; 4 splits -> partials
     assert pkv.attn_workspace_size(q, k, k, pt, cs, 1, num_splits=1) == 0
     ws = pkv.attn_workspace_size(q, k, k, pt, cs, 1, num_splits=4)

@@ -477,10 +477,13 @@ def test_short_decode_lengths_past_the_table(batch):
     assert pkv.get_error_flags() == pkv.EFLAG_ROW_TOO_SHORT
 
 
-def test_table_then_attention_in_order_across_replays():
+@pytest.mark.parametrize("one_launch", [False, True])
+def test_table_then_attention_in_order_across_replays(one_launch):
     """The strided table builder and the short decode kernel are launched with
     programmatic serialization: the attention may start before the builder
-    ends and must still read the table the builder wrote in the same step.
+    ends and must still read the table the builder wrote in the same step
+    (with `one_launch`, the table is built inside the attention launch,
+    which may start before the previous step's launch ends).
     The requests' pool rows and lengths are permuted before every replay of
     a captured step (and before every eager step), so a table read ahead of
     its write would show as another request's keys."""
@@ -495,6 +498,11 @@ def test_table_then_attention_in_order_across_replays():
     lse = torch.empty(g.q.shape[0], g.q.shape[1], dtype=torch.float32, device=DEV)
 
     def step():
+        if one_launch:
+            pkv.strided_table_attn_with_kvcache(g.req_to_token, rpi, pt, g.q, g.k_cache,
+                                                g.v_cache, cs, g.cu_seqlens_q, g.max_seqlen_q,
+                                                g.scale, num_splits=1, out=out, lse=lse)
+            return
         pkv.strided_page_table(g.req_to_token, rpi, P, n_cols, out=pt)
         pkv.attn_with_kvcache(g.q, g.k_cache, g.v_cache, pt, cs, g.cu_seqlens_q, g.max_seqlen_q,
                               g.scale, num_splits=1, out=out, lse=lse)
@@ -529,6 +537,111 @@ def test_table_then_attention_in_order_across_replays():
                                           cache_seqlens=wl.cache_seqlens[torch.as_tensor(perm)])
             check_close(out, lse, ref_o, ref_l, f"{mode} perm={perm.tolist()}")
     assert pkv.get_error_flags() == 0
+
+
+def _two_call_step(g, rtt, rpi, pt, cu, q, n_cols, num_splits):
+    """The builder followed by the attention: (table, out, lse, error bits)."""
+    pkv.clear_error_flags()
+    table = pkv.strided_page_table(rtt, rpi, g.page_size, n_cols, out=pt.clone())
+    out, lse = pkv.attn_with_kvcache(q, g.k_cache, g.v_cache, table, g.cache_seqlens, cu,
+                                     g.max_seqlen_q, g.scale, causal=g.causal,
+                                     window_left=g.window_left, num_splits=num_splits,
+                                     return_softmax_lse=True)
+    torch.cuda.synchronize()
+    return table, out, lse, pkv.get_error_flags()
+
+
+def _one_call_step(g, rtt, rpi, pt, cu, q, num_splits):
+    pkv.clear_error_flags()
+    table = pt.clone()
+    out, lse = pkv.strided_table_attn_with_kvcache(
+        rtt, rpi, table, q, g.k_cache, g.v_cache, g.cache_seqlens, cu, g.max_seqlen_q, g.scale,
+        causal=g.causal, window_left=g.window_left, num_splits=num_splits,
+        return_softmax_lse=True)
+    torch.cuda.synchronize()
+    return table, out, lse, pkv.get_error_flags()
+
+
+@pytest.mark.parametrize("batch,page_size,idx64,narrow", [
+    (4, 1, True, False),    # the tiny decode shape: cluster kernel
+    (9, 3, False, True),    # cluster kernel, odd page size, narrow token pool
+    (80, 1, True, True),    # one CTA per (request, KV head)
+    (80, 16, False, False)])
+def test_strided_table_attention_one_launch(batch, page_size, idx64, narrow):
+    """pkv_strided_table_attn_with_kvcache served by the short kernels (the
+    table built inside the attention launch): the table it writes is
+    bit-exact against the oracle's strided table, the attention matches the
+    oracle over that table, and table, out, lse and error bits are identical
+    to the builder followed by pkv_attn_with_kvcache.  In the same launch: a
+    request whose pool row lies outside req_to_token (its row all -1,
+    SRC_OOB, its keys skipped with PAGE_OOB), a request with no new tokens
+    (its table row still written, no output rows), and with `narrow` a token
+    pool narrower than the table's last column (that column -1, SRC_OOB)."""
+    len_hi = 256 - 256 % page_size
+    wl = workloads.make("tiny_decode", page_size=page_size, batch=batch, len_lo=1,
+                        len_hi=len_hi, pool_tokens=batch * (len_hi + page_size) + 64,
+                        seed=31 + page_size)
+    P, n_cols = page_size, wl.page_table.shape[1]
+    assert n_cols * P <= 256
+    rtt = wl.req_to_token
+    if narrow:
+        rtt = rtt[:, :(n_cols - 1) * P]  # a view: rows keep their stride
+    rpi = wl.req_pool_indices.clone().to(torch.int64 if idx64 else torch.int32)
+    rpi[1] = rtt.shape[0] + 3
+    # request 2 has no new tokens: its query row is dropped
+    cu = wl.cu_seqlens_q.clone()
+    cu[3:] -= 1
+    q = torch.cat([wl.q[:2], wl.q[3:]])
+    # expected table: the oracle's strided table where the source lies in
+    # the token pool, -1 (the documented value) where it does not
+    full = np.full((batch, n_cols), -1, dtype=np.int32)
+    rows = rpi.numpy().astype(np.int64)
+    ok = (rows >= 0) & (rows < rtt.shape[0])
+    n_in = -(-rtt.shape[1] // P)  # columns c with c * P inside the pool's width
+    assert n_in == (n_cols - 1 if narrow else n_cols)
+    full[ok, :n_in] = oracle.strided_page_table(
+        np.ascontiguousarray(rtt.numpy()), rows[ok], P, n_in)
+    ref_o, ref_l, skipped = oracle.attention(
+        oracle.bf16_bits(q), oracle.bf16_bits(wl.k_cache), oracle.bf16_bits(wl.v_cache),
+        full, wl.cache_seqlens.numpy(), cu.numpy(), wl.scale, causal=wl.causal,
+        window_left=wl.window_left, d_v=wl.v_cache.shape[-1])
+    assert skipped > 0
+    g = wl.to(DEV)
+    args = (g, rtt.to(DEV), rpi.to(DEV), torch.full((batch, n_cols), -5, dtype=torch.int32,
+                                                    device=DEV), cu.to(DEV), q.to(DEV))
+    with pytest.raises(pkv.PkvError) as e:  # every descriptor arrives in its place
+        pkv.strided_table_attn_with_kvcache(
+            args[1], args[2], args[3], args[5], g.k_cache, g.v_cache, g.cache_seqlens, args[4],
+            g.max_seqlen_q, g.scale, num_splits=1, lse=torch.empty(1, 1, device=DEV))
+    assert e.value.code == -1
+    t1, o1, l1, f1 = _one_call_step(*args, num_splits=1)
+    assert np.array_equal(t1.cpu().numpy(), full)
+    check_close(o1, l1, ref_o, ref_l, f"one launch batch={batch} P={P}")
+    want = pkv.EFLAG_SRC_OOB | pkv.EFLAG_PAGE_OOB
+    assert (f1 & want) == want and (f1 & ~(want | pkv.EFLAG_ROW_TOO_SHORT)) == 0
+    t2, o2, l2, f2 = _two_call_step(*args, n_cols=n_cols, num_splits=1)
+    assert torch.equal(t1, t2) and torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert f1 == f2
+
+
+def test_strided_table_attention_two_launches():
+    """Calls the short kernels do not serve (a split asked for; a table of
+    more than 256 keys) run the builder, then the attention: the same table,
+    and the attention of the two separate calls."""
+    for kw, splits in ((dict(batch=6), 2), (dict(batch=6, len_lo=300, len_hi=900), 1)):
+        wl = workloads.make("tiny_decode", pool_tokens=8192, seed=41, **kw)
+        n_cols = wl.page_table.shape[1]
+        g = wl.to(DEV)
+        args = (g, g.req_to_token, g.req_pool_indices,
+                torch.full((wl.page_table.shape[0], n_cols), -5, dtype=torch.int32, device=DEV),
+                g.cu_seqlens_q, g.q)
+        t1, o1, l1, f1 = _one_call_step(*args, num_splits=splits)
+        assert np.array_equal(t1.cpu().numpy(), wl.page_table.numpy())
+        ref_o, ref_l, _ = oracle_attn(wl)
+        check_close(o1, l1, ref_o, ref_l, f"two launches {kw} splits={splits}")
+        t2, o2, l2, f2 = _two_call_step(*args, n_cols=n_cols, num_splits=splits)
+        assert torch.equal(t1, t2) and f1 == f2 == 0
+        assert (o1.float() - o2.float()).abs().max().item() <= MAX_ABS
 
 
 # ------------------------------------- full-size workloads, every output row
