@@ -323,7 +323,7 @@ int pkv_strided_page_table(pkv_tensor req_to_token,
  * serve the attention (head dim 128, at most 16 query rows per KV head, no
  * split, n_cols * P <= 256 keys, a bf16 cache, no top-k lists) both happen
  * in one launch: each CTA forms the page ids it needs from the token pool
- * and one CTA per request stores the request's table row; otherwise the
+ * and the CTAs of KV head 0 store the request's table row; otherwise the
  * builder runs first, then the attention.
  *
  * req_to_token, req_pool_indices  (descriptors passed by host pointer, read

@@ -1889,9 +1889,9 @@ decode_allheads_kernel(const __grid_constant__ AttnParams p,
 
 // Page ids of the short kernels.  With a table built in the launch
 // (p.rtt set) a column's page id is formed from the token pool exactly as
-// the strided table builder forms it, and one CTA per request stores the
-// request's table row, so the launch has the result of the builder followed
-// by the attention.
+// the strided table builder forms it, and the CTAs of the request's KV head
+// 0 store the request's table row (one column per thread), so the launch
+// has the result of the builder followed by the attention.
 // Token-pool row of request b (-1: none; every column is then -1).
 __device__ __forceinline__ int64_t short_pool_row(const AttnParams &p, int b) {
   if (p.rtt == nullptr) return -1;
@@ -1907,15 +1907,15 @@ __device__ __forceinline__ int short_page_id(const AttnParams &p, int b, int64_t
   // slots are non-negative: C division is the page's floor division
   return rrow >= 0 && col < p.rtt_cols ? p.rtt[rrow * p.rtt_stride + col] / p.page_size : -1;
 }
-// Store request b's table row (threads t = 0 .. nthreads - 1 of one CTA);
-// a column whose source lies outside the token pool is -1 and flagged.
-__device__ __forceinline__ void short_store_table_row(const AttnParams &p, int b, int64_t rrow,
-                                                      int t, int nthreads) {
-  for (int c = t; c < p.pt_cols; c += nthreads) {
-    if (rrow < 0 || static_cast<int64_t>(c) * p.page_size >= p.rtt_cols)
-      atomicOr(p.err, PKV_EFLAG_SRC_OOB);
-    p.pt_out[static_cast<int64_t>(b) * p.pt_stride + c] = short_page_id(p, b, rrow, c);
-  }
+// Store column c of request b's table row (one thread per column, its load
+// issued beside the page-id loads); a column whose source lies outside the
+// token pool is -1 and flagged.
+__device__ __forceinline__ void short_store_table_col(const AttnParams &p, int b, int64_t rrow,
+                                                      int c) {
+  if (c >= p.pt_cols) return;
+  if (rrow < 0 || static_cast<int64_t>(c) * p.page_size >= p.rtt_cols)
+    atomicOr(p.err, PKV_EFLAG_SRC_OOB);
+  p.pt_out[static_cast<int64_t>(b) * p.pt_stride + c] = short_page_id(p, b, rrow, c);
 }
 
 constexpr int SD_WARPS = 8;
@@ -1949,7 +1949,8 @@ decode_short_kernel(const __grid_constant__ AttnParams p) {
   const int q_begin = p.cu_seqlens_q[b];
   const int q_len = p.cu_seqlens_q[b + 1] - q_begin;
   const int kv_len = p.cache_seqlens[b];
-  if (p.rtt != nullptr && h == 0) short_store_table_row(p, b, rrow, tid, SD_WARPS * 32);
+  // the table row (at most 256 columns): column tid
+  if (p.rtt != nullptr && h == 0) short_store_table_col(p, b, rrow, tid);
   if (q_len <= 0 || q_begin < 0 || q_begin + q_len > p.total_q) return;  // uniform
   const int n_rows = min(q_len, p.max_seqlen_q) * p.group;  // <= 16
   const int hi = max(kv_len, 0);
@@ -2224,7 +2225,8 @@ decode_short_cluster_kernel(const __grid_constant__ AttnParams p) {
   const int q_begin = p.cu_seqlens_q[b];
   const int q_len = p.cu_seqlens_q[b + 1] - q_begin;
   const int kv_len = p.cache_seqlens[b];
-  if (p.rtt != nullptr && h == 0 && rank == 0) short_store_table_row(p, b, rrow, tid, SC_WARPS * 32);
+  // the table row (at most 256 columns): column 64 rank + tid of KV head 0
+  if (p.rtt != nullptr && h == 0 && tid < 64) short_store_table_col(p, b, rrow, rank * 64 + tid);
   if (q_len <= 0 || q_begin < 0 || q_begin + q_len > p.total_q) return;  // the whole cluster
   const uint32_t xbar = sbase + ScSmem::kBar;
   if (tid == 0) {
