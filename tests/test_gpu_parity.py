@@ -562,12 +562,13 @@ def _one_call_step(g, rtt, rpi, pt, cu, q, num_splits):
     return table, out, lse, pkv.get_error_flags()
 
 
-@pytest.mark.parametrize("batch,page_size,idx64,narrow", [
-    (4, 1, True, False),    # the tiny decode shape: cluster kernel
-    (9, 3, False, True),    # cluster kernel, odd page size, narrow token pool
-    (80, 1, True, True),    # one CTA per (request, KV head)
-    (80, 16, False, False)])
-def test_strided_table_attention_one_launch(batch, page_size, idx64, narrow):
+@pytest.mark.parametrize("batch,page_size,idx64,narrow,q_len,window", [
+    (4, 1, True, False, 1, -1),    # the tiny decode shape: cluster kernel
+    (9, 3, False, True, 1, -1),    # cluster kernel, odd page size, narrow token pool
+    (9, 2, True, False, 2, 40),    # two new tokens (causal) per request, a window
+    (80, 1, True, True, 1, -1),    # one CTA per (request, KV head)
+    (80, 16, False, False, 2, 7)])
+def test_strided_table_attention_one_launch(batch, page_size, idx64, narrow, q_len, window):
     """pkv_strided_table_attn_with_kvcache served by the short kernels (the
     table built inside the attention launch): the table it writes is
     bit-exact against the oracle's strided table, the attention matches the
@@ -578,9 +579,11 @@ def test_strided_table_attention_one_launch(batch, page_size, idx64, narrow):
     (its table row still written, no output rows), and with `narrow` a token
     pool narrower than the table's last column (that column -1, SRC_OOB)."""
     len_hi = 256 - 256 % page_size
-    wl = workloads.make("tiny_decode", page_size=page_size, batch=batch, len_lo=1,
+    wl = workloads.make("tiny_decode", page_size=page_size, batch=batch, len_lo=q_len,
                         len_hi=len_hi, pool_tokens=batch * (len_hi + page_size) + 64,
-                        seed=31 + page_size)
+                        q_len=q_len, causal=q_len > 1, window_left=window,
+                        h_q=16 if q_len > 1 else 8, h_kv=4 if q_len > 1 else 2,
+                        seed=31 + page_size + q_len)
     P, n_cols = page_size, wl.page_table.shape[1]
     assert n_cols * P <= 256
     rtt = wl.req_to_token
@@ -588,10 +591,10 @@ def test_strided_table_attention_one_launch(batch, page_size, idx64, narrow):
         rtt = rtt[:, :(n_cols - 1) * P]  # a view: rows keep their stride
     rpi = wl.req_pool_indices.clone().to(torch.int64 if idx64 else torch.int32)
     rpi[1] = rtt.shape[0] + 3
-    # request 2 has no new tokens: its query row is dropped
+    # request 2 has no new tokens: its query rows are dropped
     cu = wl.cu_seqlens_q.clone()
-    cu[3:] -= 1
-    q = torch.cat([wl.q[:2], wl.q[3:]])
+    cu[3:] -= q_len
+    q = torch.cat([wl.q[:2 * q_len], wl.q[3 * q_len:]])
     # expected table: the oracle's strided table where the source lies in
     # the token pool, -1 (the documented value) where it does not
     full = np.full((batch, n_cols), -1, dtype=np.int32)
